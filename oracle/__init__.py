@@ -1,0 +1,189 @@
+"""Parity oracle -- TEST INFRASTRUCTURE ONLY.
+
+A plain fp64 CPU restatement of the Gated DeltaNet forward (``gdn_fwd``) and of
+the span summary (``gdn_summary``), following the cuDNN "Linear Attention"
+operations page (sections "Layout" and "Semantics worth knowing").  The
+arithmetic lives in ``gdn_oracle.c`` (token-by-token recurrence, fp64); this
+module only compiles it with gcc, converts inputs to fp64 and marshals
+arguments.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA library never does, and this
+package imports nothing from the library: the two share no code.
+
+Parity pins: every entry point is pinned in ``tests/test_oracle_pins.py``
+(brute-force dense products, closed forms, linearity, span composition,
+hand-derived golden values in ``tests/golden/``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "gdn_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB = os.path.join(_BUILD, "libgdn_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+# planted mistakes understood by gdn_oracle.c (0 = the correct oracle)
+MUTATIONS = {
+    1: "decay dropped",
+    2: "erase sign flipped",
+    3: "erase term dropped",
+    4: "exclusive output (reads the previous state)",
+    5: "L2 norm without the square root",
+    6: "interleaved grouped-head mapping",
+    7: "transition stored untransposed",
+    8: "checkpoints taken one token late",
+}
+
+
+def build(force: bool = False) -> str:
+    """Compile gdn_oracle.c into oracle/_build/libgdn_oracle.so (plain gcc, -O2)."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    tmp = _LIB + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm", "-lpthread"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            d = ctypes.POINTER(ctypes.c_double)
+            i64 = ctypes.POINTER(ctypes.c_int64)
+            lib.gdn_oracle_run.restype = ctypes.c_int
+            lib.gdn_oracle_run.argtypes = [
+                d, d, d, d, d, i64,
+                ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_double, ctypes.c_int, d,
+                d, d,
+                d, ctypes.c_int64, i64,
+                d, ctypes.c_void_p,
+                ctypes.c_int, ctypes.c_int,
+            ]
+            _lib = lib
+    return _lib
+
+
+def _f64(x):
+    """Exact conversion of a torch tensor (bf16/fp32) or array to contiguous fp64."""
+    if x is None:
+        return None
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().float().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+
+
+def _i64(x):
+    if hasattr(x, "detach"):
+        x = x.detach().cpu().numpy()
+    return np.ascontiguousarray(np.asarray(x, dtype=np.int64))
+
+
+def _ptr(a, ctype=ctypes.c_double):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ctypes.POINTER(ctype))
+
+
+def checkpoint_offsets(cu_seqlens, n: int):
+    """First checkpoint row of each sequence and the total row count.
+
+    A sequence of length L owns ceil(L / n) rows: the states entering token
+    offsets 0, n, 2n, ... < L (cuDNN page, "States and checkpoints").
+    """
+    cu = _i64(cu_seqlens)
+    lens = np.diff(cu)
+    rows = (lens + n - 1) // n
+    off = np.concatenate([[0], np.cumsum(rows)]).astype(np.int64)
+    return off[:-1].copy(), int(off[-1])
+
+
+def _default_threads():
+    return max(1, os.cpu_count() or 1)
+
+
+def gdn_fwd(q, k, v, g, beta, cu_seqlens, *, scale=None, use_qk_l2norm=True,
+            initial_state=None, output_final_state=True, checkpoint_every_n=0,
+            want_o=True, unit_mask=None, nthreads=None, mutation=0):
+    """fp64 forward: returns dict(o [T,HO,V], final_state [N,HO,K,V], checkpoints [R,HO,K,V]).
+
+    q, k: [T, HK, K]; v: [T, HV, V]; g, beta: [T, HO] (g in natural-log space);
+    cu_seqlens: [N + 1]; initial_state: [N, HO, K, V] or None (zero start).
+    scale defaults to 1/sqrt(K) and multiplies the (normalised) query.
+    unit_mask: optional bool [N, HO]; unmarked units are left at zero.
+    """
+    return _run(q, k, v, g, beta, cu_seqlens, scale=scale, use_qk_l2norm=use_qk_l2norm,
+                s0=initial_state, want_final=output_final_state,
+                checkpoint_every_n=checkpoint_every_n, want_o=want_o,
+                want_transition=False, unit_mask=unit_mask, nthreads=nthreads,
+                mutation=mutation)
+
+
+def gdn_summary(k, v, g, beta, cu_seqlens, *, use_qk_l2norm=True, start_state=None,
+                unit_mask=None, nthreads=None, mutation=0):
+    """fp64 span summary: returns dict(end_state [N,HO,K,V], transition [N,HO,K,K]).
+
+    end_state is the state after each span's last token from ``start_state``
+    (zero when None); transition = P^T with P the product of the span's decayed
+    erase steps exp(g_t)(I - beta_t k_t k_t^T), later steps on the left, so that
+    end_state = einsum('ab,av->bv', transition, S_init) + S_H.
+    """
+    T = k.shape[0]
+    HK, K = k.shape[1], k.shape[2]
+    q = np.zeros((T, HK, K), dtype=np.float64)
+    r = _run(q, k, v, g, beta, cu_seqlens, scale=1.0, use_qk_l2norm=use_qk_l2norm,
+             s0=start_state, want_final=True, checkpoint_every_n=0, want_o=False,
+             want_transition=True, unit_mask=unit_mask, nthreads=nthreads,
+             mutation=mutation)
+    return {"end_state": r["final_state"], "transition": r["transition"]}
+
+
+def _run(q, k, v, g, beta, cu_seqlens, *, scale, use_qk_l2norm, s0, want_final,
+         checkpoint_every_n, want_o, want_transition, unit_mask, nthreads, mutation):
+    q, k, v, g, beta = (_f64(x) for x in (q, k, v, g, beta))
+    cu = _i64(cu_seqlens)
+    T, HK, K = k.shape
+    HV, V = v.shape[1], v.shape[2]
+    N = cu.shape[0] - 1
+    HO = HV
+    assert q.shape == (T, HK, K) and v.shape[0] == T
+    assert g.shape == (T, HO) and beta.shape == (T, HO)
+    if scale is None:
+        scale = 1.0 / np.sqrt(K)
+    s0 = _f64(s0)
+    if s0 is not None:
+        assert s0.shape == (N, HO, K, V)
+    o = np.zeros((T, HO, V)) if want_o else None
+    fin = np.zeros((N, HO, K, V)) if want_final else None
+    ck = ck_off = None
+    if checkpoint_every_n:
+        ck_off, R = checkpoint_offsets(cu, checkpoint_every_n)
+        ck = np.zeros((R, HO, K, V))
+    tr = np.zeros((N, HO, K, K)) if want_transition else None
+    mask = None
+    if unit_mask is not None:
+        mask = np.ascontiguousarray(np.asarray(unit_mask, dtype=np.uint8).reshape(N * HO))
+    rc = _load().gdn_oracle_run(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu, ctypes.c_int64),
+        T, N, HK, HV, K, V, float(scale), int(bool(use_qk_l2norm)), _ptr(s0),
+        _ptr(o), _ptr(fin), _ptr(ck), int(checkpoint_every_n or 0),
+        _ptr(ck_off, ctypes.c_int64), _ptr(tr),
+        mask.ctypes.data if mask is not None else None,
+        int(nthreads or _default_threads()), int(mutation))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments (cu_seqlens or shapes)")
+    return {"o": o, "final_state": fin, "checkpoints": ck, "transition": tr}

@@ -1,0 +1,349 @@
+"""Pins for the fp64 oracle: checks against facts fixed by the pages and by mathematics.
+
+Every check below is an independent statement of what the Gated DeltaNet forward
+(cuDNN Linear Attention page: the GDN recurrence, "States and checkpoints",
+"Summaries") must produce, evaluated without the oracle's own loop:
+  * a hand-derived worked example (tests/golden/gdn_hand_3tok.json);
+  * brute-force dense products of the explicit K x K factors on tiny inputs;
+  * closed forms: exact retrieval with orthonormal keys, pure decay (beta = 0),
+    a single token from a zero start;
+  * invariants: joint linearity in (v, S0), scale linearity, L2-norm invariance
+    under positive row rescaling, grouped heads == duplicated heads;
+  * summaries: span composition and the transition product order;
+  * checkpoints: entry j equals the final state of the prefix of length j*n;
+  * state round trip: [0, m) then [m, L) equals the unsplit run;
+  * empty sequences.
+test_planted_mistakes_are_caught plants each of the oracle's known mutations
+and requires at least one check to fail, so a plausible slip anywhere (a dropped
+term, a flipped sign, a wrong index or orientation) cannot pass unnoticed.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+RNG = np.random.default_rng(12345)
+
+
+def _rand_case(lengths, HK, HV, K, V, seed, s0=False, gscale=1.0):
+    rng = np.random.default_rng(seed)
+    T = int(sum(lengths))
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    q = rng.standard_normal((T, HK, K))
+    k = rng.standard_normal((T, HK, K))
+    v = rng.standard_normal((T, HV, V))
+    g = -np.log1p(np.exp(rng.standard_normal((T, HV)))) * gscale
+    beta = 1.0 / (1.0 + np.exp(-rng.standard_normal((T, HV))))
+    S0 = 0.3 * rng.standard_normal((len(lengths), HV, K, V)) if s0 else None
+    return q, k, v, g, beta, cu, S0
+
+
+def _rel(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    den = max(np.abs(b).max(), 1e-300)
+    return float(np.abs(a - b).max() / den)
+
+
+# --------------------------------------------------------------------------------------
+# checks: each returns the worst relative error it saw for the given oracle mutation
+# --------------------------------------------------------------------------------------
+
+def check_golden(mutation=0):
+    d = json.load(open(os.path.join(GOLDEN, "gdn_hand_3tok.json")))
+    q = np.array(d["q"], dtype=np.float64)[:, None, :]
+    k = np.array(d["k"], dtype=np.float64)[:, None, :]
+    v = np.array(d["v"], dtype=np.float64)[:, None, :]
+    g = np.log(np.array(d["decay"]))[:, None]
+    beta = np.array(d["beta"], dtype=np.float64)[:, None]
+    cu = np.array(d["cu_seqlens"])
+    r = oracle.gdn_fwd(q, k, v, g, beta, cu, scale=d["scale"], use_qk_l2norm=False,
+                       checkpoint_every_n=d["checkpoint_every_n"], mutation=mutation)
+    s = oracle.gdn_summary(k, v, g, beta, cu, use_qk_l2norm=False, mutation=mutation)
+    errs = [
+        np.abs(r["o"][:, 0, :] - np.array(d["o"])).max(),
+        np.abs(r["final_state"][0, 0] - np.array(d["final_state"])).max(),
+        np.abs(r["checkpoints"][:, 0] - np.array(d["checkpoints"])).max(),
+        np.abs(s["transition"][0, 0] - np.array(d["transition"])).max(),
+        np.abs(s["end_state"][0, 0] - np.array(d["final_state"])).max(),
+    ]
+    return float(max(errs))
+
+
+def _dense_reference(q, k, v, g, beta, cu, S0, scale, l2norm, HK, HV):
+    """Explicit K x K factors multiplied densely: S_t = M_t S_{t-1} + beta k v^T."""
+    T, _, K = k.shape
+    V = v.shape[2]
+    N = len(cu) - 1
+    o = np.zeros((T, HV, V))
+    fin = np.zeros((N, HV, K, V))
+    trans = np.zeros((N, HV, K, K))
+    for i in range(N):
+        for h in range(HV):
+            hk = h // (HV // HK)
+            S = np.zeros((K, V)) if S0 is None else S0[i, h].copy()
+            P = np.eye(K)
+            for t in range(cu[i], cu[i + 1]):
+                kt, qt = k[t, hk].copy(), q[t, hk].copy()
+                if l2norm:
+                    kt = kt / math.sqrt(kt @ kt + 1e-6)
+                    qt = qt / math.sqrt(qt @ qt + 1e-6)
+                M = math.exp(g[t, h]) * (np.eye(K) - beta[t, h] * np.outer(kt, kt))
+                S = M @ S + beta[t, h] * np.outer(kt, v[t, h])
+                P = M @ P
+                o[t, h] = scale * S.T @ qt
+            fin[i, h] = S
+            trans[i, h] = P.T
+    return o, fin, trans
+
+
+def check_brute_force(mutation=0):
+    worst = 0.0
+    for l2 in (False, True):
+        for (lengths, HK, HV, K, V, s0) in (([5, 3], 1, 1, 3, 4, True), ([4, 0, 6], 2, 4, 4, 3, False)):
+            q, k, v, g, beta, cu, S0 = _rand_case(lengths, HK, HV, K, V, seed=7 + K, s0=s0)
+            o, fin, tr = _dense_reference(q, k, v, g, beta, cu, S0, 0.7, l2, HK, HV)
+            r = oracle.gdn_fwd(q, k, v, g, beta, cu, scale=0.7, use_qk_l2norm=l2,
+                               initial_state=S0, mutation=mutation)
+            s = oracle.gdn_summary(k, v, g, beta, cu, use_qk_l2norm=l2, mutation=mutation)
+            _, fin0, _ = _dense_reference(q, k, v, g, beta, cu, None, 0.7, l2, HK, HV)
+            worst = max(worst, _rel(r["o"], o), _rel(r["final_state"], fin),
+                        _rel(s["transition"], tr), _rel(s["end_state"], fin0))
+    return worst
+
+
+def check_retrieval(mutation=0):
+    """g = 0, beta = 1, orthonormal keys: o_t = scale * (newest value written under q's key)."""
+    K = V = 8
+    rng = np.random.default_rng(3)
+    order = [0, 3, 5, 3, 7, 0, 1]           # key indices written, with rewrites
+    T = len(order)
+    basis = np.eye(K)
+    k = basis[order][:, None, :]
+    q = k.copy()                             # query the key just written
+    v = rng.standard_normal((T, 1, V))
+    g = np.zeros((T, 1))
+    beta = np.ones((T, 1))
+    cu = np.array([0, T])
+    r = oracle.gdn_fwd(q, k, v, g, beta, cu, scale=1.5, use_qk_l2norm=False, mutation=mutation)
+    err = _rel(r["o"][:, 0], 1.5 * v[:, 0])
+    # the final state holds, in row j, the newest value written under key j
+    expect = np.zeros((K, V))
+    for t, j in enumerate(order):
+        expect[j] = v[t, 0]
+    err = max(err, _rel(r["final_state"][0, 0], expect))
+    # querying an older key after later writes still returns its newest value
+    q2 = basis[[0] * T][:, None, :]
+    r2 = oracle.gdn_fwd(q2, k, v, g, beta, cu, scale=1.0, use_qk_l2norm=False, mutation=mutation)
+    newest0 = [v[max(s for s in range(t + 1) if order[s] == 0), 0] for t in range(T)]
+    err = max(err, _rel(r2["o"][:, 0], np.array(newest0)))
+    return err
+
+
+def check_pure_decay(mutation=0):
+    """beta = 0: S_t = exp(sum g) S0 and o_t = scale exp(b_t) S0^T q_hat_t."""
+    q, k, v, g, beta, cu, S0 = _rand_case([9, 4], 1, 2, 5, 3, seed=11, s0=True, gscale=0.3)
+    beta[:] = 0.0
+    r = oracle.gdn_fwd(q, k, v, g, beta, cu, scale=0.9, use_qk_l2norm=True, initial_state=S0,
+                       mutation=mutation)
+    worst = 0.0
+    for i in range(2):
+        for h in range(2):
+            b = 0.0
+            for t in range(cu[i], cu[i + 1]):
+                b += g[t, h]
+                qh = q[t, 0] / math.sqrt(q[t, 0] @ q[t, 0] + 1e-6)
+                worst = max(worst, _rel(r["o"][t, h], 0.9 * math.exp(b) * S0[i, h].T @ qh))
+            worst = max(worst, _rel(r["final_state"][i, h], math.exp(b) * S0[i, h]))
+    return worst
+
+
+def check_single_token(mutation=0):
+    """One token from zero: S1 = beta k_hat v^T, o = scale beta (k_hat . q_hat) v."""
+    rng = np.random.default_rng(5)
+    K, V = 6, 4
+    q = rng.standard_normal((1, 1, K))
+    k = rng.standard_normal((1, 1, K))
+    v = rng.standard_normal((1, 1, V))
+    g = np.array([[-0.4]])
+    beta = np.array([[0.6]])
+    r = oracle.gdn_fwd(q, k, v, g, beta, np.array([0, 1]), scale=0.5, use_qk_l2norm=True,
+                       mutation=mutation)
+    kh = k[0, 0] / math.sqrt(k[0, 0] @ k[0, 0] + 1e-6)
+    qh = q[0, 0] / math.sqrt(q[0, 0] @ q[0, 0] + 1e-6)
+    return max(_rel(r["final_state"][0, 0], 0.6 * np.outer(kh, v[0, 0])),
+               _rel(r["o"][0, 0], 0.5 * 0.6 * (kh @ qh) * v[0, 0]))
+
+
+def check_linearity(mutation=0):
+    """o and the final state are jointly linear in (v, S0); o is linear in scale."""
+    q, k, v, g, beta, cu, S0 = _rand_case([7, 5], 1, 1, 4, 3, seed=21, s0=True)
+    _, _, v2, _, _, _, S02 = _rand_case([7, 5], 1, 1, 4, 3, seed=22, s0=True)
+    f = lambda vv, ss, sc=1.0, qq=q, kk=k: oracle.gdn_fwd(
+        qq, kk, vv, g, beta, cu, scale=sc, initial_state=ss, use_qk_l2norm=True, mutation=mutation)
+    a, b = 0.7, -1.3
+    r = f(a * v + b * v2, a * S0 + b * S02)
+    r1, r2 = f(v, S0), f(v2, S02)
+    err = max(_rel(r["o"], a * r1["o"] + b * r2["o"]),
+              _rel(r["final_state"], a * r1["final_state"] + b * r2["final_state"]))
+    err = max(err, _rel(f(v, S0, sc=2.5)["o"], 2.5 * r1["o"]))
+    return err
+
+
+def check_norm_invariance(mutation=0):
+    """With the L2 norm on, positive per-row rescaling of q and k leaves o unchanged
+    up to the 1e-6 inside the square root (rows here have |x|^2 >= 0.5)."""
+    q, k, v, g, beta, cu, S0 = _rand_case([7, 5], 1, 1, 4, 3, seed=21, s0=True)
+    rs = np.random.default_rng(23).uniform(1.0, 5.0, size=(q.shape[0], 1, 1))
+    f = lambda qq, kk: oracle.gdn_fwd(qq, kk, v, g, beta, cu, initial_state=S0,
+                                      use_qk_l2norm=True, mutation=mutation)["o"]
+    return _rel(f(q * rs, k * rs[::-1]), f(q, k))
+
+
+def check_gva(mutation=0):
+    """HK = 2, HV = 6 equals HK = HV = 6 with q/k heads duplicated in contiguous groups."""
+    q, k, v, g, beta, cu, S0 = _rand_case([6, 3], 2, 6, 4, 3, seed=31, s0=True)
+    idx = [h // 3 for h in range(6)]
+    r = oracle.gdn_fwd(q, k, v, g, beta, cu, initial_state=S0, mutation=mutation)
+    rd = oracle.gdn_fwd(q[:, idx], k[:, idx], v, g, beta, cu, initial_state=S0, mutation=mutation)
+    return max(_rel(r["o"], rd["o"]), _rel(r["final_state"], rd["final_state"]))
+
+
+def check_span_composition(mutation=0):
+    """Summaries of consecutive spans compose to the unsplit end state and transition."""
+    lengths = [5, 7, 4]
+    q, k, v, g, beta, _, _ = _rand_case([sum(lengths)], 1, 2, 4, 3, seed=41, gscale=0.2)
+    S_init = 0.5 * np.random.default_rng(42).standard_normal((1, 2, 4, 3))
+    whole_cu = np.array([0, sum(lengths)])
+    span_cu = np.concatenate([[0], np.cumsum(lengths)])
+    full = oracle.gdn_fwd(q, k, v, g, beta, whole_cu, initial_state=S_init, mutation=mutation)
+    s = oracle.gdn_summary(k, v, g, beta, span_cu, mutation=mutation)
+    sw = oracle.gdn_summary(k, v, g, beta, whole_cu, mutation=mutation)
+    S = S_init[0].copy()
+    tr_prod = np.stack([np.eye(4)] * 2)
+    for j in range(len(lengths)):
+        S = np.einsum("hab,hav->hbv", s["transition"][j], S) + s["end_state"][j]
+        tr_prod = np.einsum("hab,hbc->hac", tr_prod, s["transition"][j])
+    err = max(_rel(S, full["final_state"][0]), _rel(tr_prod, sw["transition"][0]))
+    # summary from a non-zero start equals transition applied to the start plus S_H
+    st = oracle.gdn_summary(k, v, g, beta, whole_cu, start_state=S_init, mutation=mutation)
+    err = max(err, _rel(st["end_state"][0],
+                        np.einsum("hab,hav->hbv", sw["transition"][0], S_init[0]) + sw["end_state"][0]))
+    return err
+
+
+def check_checkpoints(mutation=0):
+    """Checkpoint entry j of a sequence equals the final state of its first j*n tokens."""
+    n = 3
+    lengths = [7, 3, 0, 5]
+    q, k, v, g, beta, cu, S0 = _rand_case(lengths, 1, 1, 3, 2, seed=51, s0=True, gscale=0.2)
+    r = oracle.gdn_fwd(q, k, v, g, beta, cu, initial_state=S0, checkpoint_every_n=n,
+                       mutation=mutation)
+    off, R = oracle.checkpoint_offsets(cu, n)
+    assert R == 3 + 1 + 0 + 2
+    worst = 0.0
+    for i, L in enumerate(lengths):
+        for j in range(-(-L // n)):
+            m = j * n
+            if m == 0:
+                expect = S0[i]
+            else:
+                sl = slice(cu[i], cu[i] + m)
+                pr = oracle.gdn_fwd(q[sl], k[sl], v[sl], g[sl], beta[sl], np.array([0, m]),
+                                    initial_state=S0[i:i + 1], mutation=0)
+                expect = pr["final_state"][0]
+            worst = max(worst, _rel(r["checkpoints"][off[i] + j], expect))
+    return worst
+
+
+def check_round_trip(mutation=0):
+    """Running [0, m) then [m, L) with final -> initial equals the unsplit run."""
+    L, m = 13, 6
+    q, k, v, g, beta, _, S0 = _rand_case([L], 1, 2, 4, 3, seed=61, s0=True, gscale=0.2)
+    full = oracle.gdn_fwd(q, k, v, g, beta, np.array([0, L]), initial_state=S0, mutation=mutation)
+    a = oracle.gdn_fwd(q[:m], k[:m], v[:m], g[:m], beta[:m], np.array([0, m]),
+                       initial_state=S0, mutation=mutation)
+    b = oracle.gdn_fwd(q[m:], k[m:], v[m:], g[m:], beta[m:], np.array([0, L - m]),
+                       initial_state=a["final_state"], mutation=mutation)
+    return max(_rel(b["final_state"], full["final_state"]), _rel(b["o"], full["o"][m:]),
+               _rel(a["o"], full["o"][:m]))
+
+
+def check_empty(mutation=0):
+    """Empty sequences: final = initial, no checkpoint rows, transition = identity."""
+    lengths = [0, 4, 0]
+    q, k, v, g, beta, cu, S0 = _rand_case(lengths, 1, 1, 3, 2, seed=71, s0=True)
+    r = oracle.gdn_fwd(q, k, v, g, beta, cu, initial_state=S0, checkpoint_every_n=2,
+                       mutation=mutation)
+    s = oracle.gdn_summary(k, v, g, beta, cu, mutation=mutation)
+    off, R = oracle.checkpoint_offsets(cu, 2)
+    assert R == 2 and list(off) == [0, 0, 2]
+    return max(_rel(r["final_state"][0], S0[0]), _rel(r["final_state"][2], S0[2]),
+               _rel(s["transition"][0, 0], np.eye(3)), _rel(s["transition"][2, 0], np.eye(3)),
+               float(np.abs(s["end_state"][[0, 2]]).max()))
+
+
+CHECKS = {
+    "golden": (check_golden, 1e-12),
+    "brute_force": (check_brute_force, 1e-12),
+    "retrieval": (check_retrieval, 1e-12),
+    "pure_decay": (check_pure_decay, 1e-12),
+    "single_token": (check_single_token, 1e-12),
+    "linearity": (check_linearity, 1e-10),
+    "norm_invariance": (check_norm_invariance, 2e-5),
+    "gva": (check_gva, 1e-13),
+    "span_composition": (check_span_composition, 1e-12),
+    "checkpoints": (check_checkpoints, 1e-13),
+    "round_trip": (check_round_trip, 1e-12),
+    "empty": (check_empty, 1e-15),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CHECKS))
+def test_oracle_pin(name):
+    fn, tol = CHECKS[name]
+    err = fn(0)
+    assert err <= tol, f"{name}: relative error {err:.3e} > {tol:.1e}"
+
+
+@pytest.mark.parametrize("mutation", sorted(oracle.MUTATIONS))
+def test_planted_mistakes_are_caught(mutation):
+    failed = []
+    for name, (fn, tol) in CHECKS.items():
+        try:
+            err = fn(mutation)
+        except (AssertionError, ValueError):
+            err = float("inf")
+        if not err <= tol:
+            failed.append(name)
+    assert failed, f"planted mistake '{oracle.MUTATIONS[mutation]}' passed every pin"
+
+
+def test_retrieval_with_l2norm_close():
+    """With the L2 norm on, unit keys are rescaled by 1/sqrt(1 + 1e-6): retrieval holds to ~1e-6."""
+    K = V = 4
+    k = np.eye(K)[[0, 1, 2, 1]][:, None, :]
+    v = np.random.default_rng(9).standard_normal((4, 1, V))
+    r = oracle.gdn_fwd(k, k, v, np.zeros((4, 1)), np.ones((4, 1)), np.array([0, 4]), scale=1.0)
+    assert _rel(r["o"][:, 0], v[:, 0]) < 2e-6
+
+
+def test_unit_mask_computes_only_marked_units():
+    q, k, v, g, beta, cu, S0 = _rand_case([4, 5], 1, 2, 3, 2, seed=81, s0=True)
+    full = oracle.gdn_fwd(q, k, v, g, beta, cu, initial_state=S0)
+    mask = np.array([[False, True], [True, False]])
+    part = oracle.gdn_fwd(q, k, v, g, beta, cu, initial_state=S0, unit_mask=mask)
+    assert np.array_equal(part["final_state"][0, 1], full["final_state"][0, 1])
+    assert np.array_equal(part["final_state"][1, 0], full["final_state"][1, 0])
+    assert not part["final_state"][0, 0].any()
+
+
+def test_rejects_bad_cu_seqlens():
+    q, k, v, g, beta, cu, _ = _rand_case([3, 2], 1, 1, 2, 2, seed=91)
+    with pytest.raises(ValueError):
+        oracle.gdn_fwd(q, k, v, g, beta, np.array([0, 4, 3]))
