@@ -1,0 +1,404 @@
+"""Benchmark: chunked GDN forward tokens/s and fraction of the GB300 roofline.
+
+Workload (one step = one gdn_fwd over the whole batch, prologue + fused chunk
+kernel): the dense batch of 8 sequences x 8192 tokens (T = 65536), 32 heads,
+K = V = 128, bf16 q/k/v, fp32 g/beta, fp32 initial state, final state and fp32
+checkpoints every 1024 tokens, q/k L2-normalised in kernel.  Inputs are seeded
+synthetic tensors with the cuDNN page's distributions; q/k/v alone are 1.6 GB per
+step, far larger than the 129 MB L2, so no flush is needed between steps.
+
+Multi-GPU (torchrun): every rank runs its own copy of the batch (independent
+sequences, no data-path collective: weak scaling); value = tokens of all ranks /
+the slowest rank's time.
+
+--impl reference times the fp64 CPU oracle (the parity oracle, untuned) on a
+bounded sample of the same workload on the host cores (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GDN fwd tokens/s and % of GB300 roofline (T=65536,H=32,K=V=128 bf16)"
+WORKLOAD = "dense batch: N=8 x 8192 tokens (T=65536), H=32, K=V=128, bf16 q/k/v, fp32 start state, " \
+           "final state and fp32 checkpoints every 1024 tokens, q/k L2 norm in kernel"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def algorithmic_bytes(T, N, HK, HV, K, V, ckpt_rows, s0=True, final=True, ckpt_bytes=4):
+    """Bytes the forward must move at least once: inputs read, outputs written."""
+    HO = HV
+    b = T * (2 * HK * K + HV * V) * 2      # q, k, v
+    b += T * HO * V * 2                    # o
+    b += 2 * T * HO * 4                    # g, beta
+    b += N * HO * K * V * 4 if s0 else 0   # initial state
+    b += N * HO * K * V * 4 if final else 0
+    b += ckpt_rows * HO * K * V * ckpt_bytes
+    b += (N + 1) * 4                       # cu_seqlens
+    return b
+
+
+def algorithmic_flops(lengths, HO, K, V):
+    """Chunked-form tensor work per 64-token chunk and head: KK^T, QK^T, T*(beta V),
+    T*(beta gamma K), the intra-chunk output (5 x 2 C^2 d) plus W S, Q S and the
+    state update (3 x 2 C d^2), with d = K = V."""
+    chunks = sum((int(L) + 63) // 64 for L in lengths)
+    C = 64
+    per = 2 * C * C * K * 2 + 2 * C * C * V * 3 + 2 * C * K * V * 3
+    return chunks * HO * per
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d.get("bf16_tflops", FALLBACK_BF16_TFLOPS)), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "gated_delta_rule_29_gb300", "csrc")
+    for name in sorted(os.listdir(d)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(d, name), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the fused kernel from the committed ncu summary, if it
+    was taken from the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "gdn_chunk_kernel_dense_batch.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return d.get("traffic_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n_, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n_)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_sample(w, units, nthreads):
+    """Runs the CPU oracle on the given (sequence, head) units; returns (seconds, token-heads).
+
+    Only the sampled sequences are sliced out and converted to fp64 before the clock starts;
+    the timed call is the oracle's recurrence on exactly those units."""
+    import oracle
+    seqs = sorted({i for i, _ in units})
+    cu = w.cu_seqlens.numpy().astype(np.int64)
+    idx = np.concatenate([np.arange(cu[i], cu[i + 1]) for i in seqs])
+    lens = [int(cu[i + 1] - cu[i]) for i in seqs]
+    sub_cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    f64 = lambda x: np.ascontiguousarray(x.float().numpy(), dtype=np.float64)
+    q, k, v, g, b = (f64(x[idx]) for x in (w.q, w.k, w.v, w.g, w.beta))
+    s0 = None if w.initial_state is None else f64(w.initial_state[seqs])
+    mask = np.zeros((len(seqs), w.HV), dtype=bool)
+    for i, h in units:
+        mask[seqs.index(i), h] = True
+    t0 = time.perf_counter()
+    oracle.gdn_fwd(q, k, v, g, b, sub_cu, initial_state=s0, checkpoint_every_n=w.checkpoint_every_n,
+                   unit_mask=mask, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return dt, int(sum(lens[seqs.index(i)] for i, _ in units))
+
+
+def cpu_units(w, count):
+    """A fixed spread of (sequence, head) units for the CPU sample: heads spread over the
+    first two sequences."""
+    return [(j % 2, (7 * j + 3) % w.HV) for j in range(count)]
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    from gated_delta_rule_29_gb300 import workloads as W
+    w = W.config(3)
+    cores = os.cpu_count() or 1
+    units = cpu_units(w, args.ref_units)
+    for _ in range(args.warmup):
+        oracle_sample(w, units[:1], cores)
+    times, th = [], 0
+    for _ in range(args.steps):
+        dt, n = oracle_sample(w, units, cores)
+        times.append(dt)
+        th += n
+    total = sum(times)
+    tokens_per_s = th / w.HV / total  # token-heads -> tokens of all HO heads
+    line = {
+        "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": WORKLOAD, "sample": f"{len(units)} (sequence, head) units x 8192 tokens per step"},
+        "cpu_baseline": {"value": tokens_per_s, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{len(units)} of 256 (sequence, head) units of the workload per step, "
+                                   f"fp64 token-by-token C recurrence, {cores} threads"},
+        "e2e": {"value": tokens_per_s, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, world, rank, local):
+    import gated_delta_rule_29_gb300 as la
+    from gated_delta_rule_29_gb300 import binding as B
+    from gated_delta_rule_29_gb300 import workloads as W
+
+    assert torch.cuda.is_available(), "bench needs a CUDA device (there is no CPU fallback)"
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lib = B.load()
+    if args.seq_len == 8192:
+        w = W.config(3)
+    else:  # a smaller dense batch of the same shape family (profiling captures)
+        w = W.draw(f"dense batch N=8 x {args.seq_len}", [args.seq_len] * 8, 32, 32, 128, 128, seed=1003,
+                   initial_state=True, checkpoint_every_n=1024, checkpoint_dtype=torch.float32)
+    T, N, HK, HV, K, V = w.T, w.N, w.HK, w.HV, w.K, w.V
+    HO = HV
+    n_ck = w.checkpoint_every_n
+    R = la.checkpoint_rows(w.cu_seqlens, n_ck)
+
+    # device-resident inputs and outputs
+    q, k, v = w.q.to(dev), w.k.to(dev), w.v.to(dev)
+    g, beta = w.g.to(dev), w.beta.to(dev)
+    cu = w.cu_seqlens.to(dev)
+    s0 = w.initial_state.to(dev)
+    o = torch.empty(T, HO, V, dtype=torch.bfloat16, device=dev)
+    fin = torch.empty(N, HO, K, V, dtype=torch.float32, device=dev)
+    ck = torch.empty(R, HO, K, V, dtype=torch.float32, device=dev)
+    ws = torch.empty(la.workspace_bytes(N), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step(qq=q, kk=k, vv=v, gg=g, bb=beta, cc=cu, ss=s0, oo=o, ff=fin, kc=ck):
+        la.gdn_fwd(qq, kk, vv, gg, bb, cc, initial_state=ss, checkpoint_every_n=n_ck,
+                   checkpoint_dtype=torch.float32, checkpoint_rows_hint=R, o=oo, final_state=ff,
+                   checkpoints=kc, workspace=ws, status=status)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert la.read_status(status) == 0, "device status after warm-up"
+
+    stream = torch.cuda.current_stream()
+    k_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a_, b_ in k_ev:  # torch creates the underlying cudaEvent_t on first record
+        a_.record(stream)
+        b_.record(stream)
+    torch.cuda.synchronize()
+    assert all(a_.cuda_event and b_.cuda_event for a_, b_ in k_ev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(args.steps):
+            lib.la_set_kernel_timing_events(k_ev[i][0].cuda_event, k_ev[i][1].cuda_event)
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    ms_local = e0.elapsed_time(e1) / args.steps
+    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in k_ev)
+    ms = max_over_ranks(ms_local, world)
+    assert la.read_status(status) == 0, "device status after the timed region"
+
+    tokens = T * world
+    value = tokens / (ms * 1e-3)
+    hbm_peak, tc_peak, peak_src = load_peaks()
+    alg_bytes = algorithmic_bytes(T, N, HK, HV, K, V, R)
+    alg_flops = algorithmic_flops(w.lengths(), HO, K, V)
+    achieved = alg_bytes / (kern_ms * 1e-3) / 1e9
+    tflops = alg_flops / (kern_ms * 1e-3) / 1e12
+
+    # end to end through the public API with host buffers: pinned H2D of the step's inputs,
+    # the forward, D2H of its outputs, all inside the timed region
+    host_in = [x.pin_memory() for x in (w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, w.initial_state)]
+    host_out = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (o, fin, ck)]
+    dev_in = [torch.empty_like(x, device=dev) for x in host_in]
+    h2d = sum(x.numel() * x.element_size() for x in host_in)
+    d2h = sum(x.numel() * x.element_size() for x in host_out)
+
+    def e2e_step():
+        for dst, src in zip(dev_in, host_in):
+            dst.copy_(src, non_blocking=True)
+        step(*dev_in)
+        for dst, src in zip(host_out, (o, fin, ck)):
+            dst.copy_(src, non_blocking=True)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e_steps = max(3, min(args.steps, 10))
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        x0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        x1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        e2e_ms = max_over_ranks(x0.elapsed_time(x1) / e2e_steps, world)
+        e2e = {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+        assert la.read_status(status) == 0
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cores = os.cpu_count() or 1
+        units = cpu_units(w, args.cpu_units)
+        dt, th = oracle_sample(w, units, cores)
+        cpu = {"value": th / HO / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{len(units)} of 256 (sequence, head) units x 8192 tokens of the same workload "
+                         f"({dt:.1f} s), fp64 token-by-token C recurrence on {cores} threads"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD if args.seq_len == 8192 else w.name, "global_batch": N * world,
+                       "seq_len": args.seq_len,
+                       "parallelism": f"independent batches per GPU x{world}" if world > 1 else "single GPU",
+                       "l2": "inputs larger than L2 (1.6 GB of q/k/v per step); no flush"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": profiled_traffic(),
+                         "peak_source": peak_src, "kernel": "gdn_chunk_kernel<128, fwd>",
+                         "kernel_ms": kern_ms, "algorithmic_bytes": alg_bytes,
+                         "tensor_tflops": tflops, "tensor_frac": tflops / tc_peak},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": 2 * args.steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-units", type=int, default=16, help="(sequence, head) units in the CPU-baseline sample")
+    ap.add_argument("--ref-units", type=int, default=2, help="units per step of the reference arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--seq-len", type=int, default=8192,
+                    help="tokens per sequence of the dense batch (8192 is the benchmark workload)")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    world, rank, local = dist_setup()
+    try:
+        if args.impl == "reference":
+            return run_reference(args, world, rank)
+        return run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

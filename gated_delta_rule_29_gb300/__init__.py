@@ -1,0 +1,11 @@
+"""gated_delta_rule_29_gb300 -- GB300-native (sm_103a) chunked Gated DeltaNet forward.
+
+The computation lives in liblinattn.so (C ABI: include/liblinattn.h), built
+in-tree from csrc/ by ``_build.build()``.  This package is its thin Python
+binding: ``gdn_fwd`` and ``gdn_summary`` marshal torch tensors into the C
+structs and launch on the current CUDA stream.  There is no CPU fallback.
+"""
+from .api import checkpoint_rows, gdn_fwd, gdn_summary, read_status, workspace_bytes  # noqa: F401
+from . import binding  # noqa: F401
+
+__all__ = ["gdn_fwd", "gdn_summary", "read_status", "checkpoint_rows", "workspace_bytes", "binding"]

@@ -1,0 +1,162 @@
+"""Torch-facing wrappers of the liblinattn C ABI (same names: gdn_fwd, gdn_summary).
+
+PyTorch only supplies device memory and the current stream; every step of the
+computation runs in the library's CUDA kernels.  Shapes follow the cuDNN Linear
+Attention page: packed THD operands [T, heads, dim], cu_seqlens [N + 1].
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+from typing import Optional, Tuple
+
+import torch
+
+from . import binding as B
+
+
+def _stream_ptr(stream: Optional[torch.cuda.Stream]) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _check_thd(name, x, dtype, heads_dim=True):
+    if not isinstance(x, torch.Tensor) or not x.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if x.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {x.dtype} (dtypes are strict)")
+    if x.dim() != (3 if heads_dim else 2):
+        raise ValueError(f"{name} must be rank {3 if heads_dim else 2}, got shape {tuple(x.shape)}")
+    if heads_dim and x.shape[-1] > 1 and x.stride(-1) != 1:
+        raise ValueError(f"{name} must have a contiguous innermost axis")
+
+
+def _cu_bits(cu: torch.Tensor) -> int:
+    if cu.dtype == torch.int32:
+        return 32
+    if cu.dtype == torch.int64:
+        return 64
+    raise TypeError("cu_seqlens must be int32 or int64")
+
+
+def checkpoint_rows(cu_seqlens: torch.Tensor, n: int) -> int:
+    """Rows of the checkpoint series, sum_i ceil(L_i / n) (reads cu_seqlens on the host)."""
+    cu = cu_seqlens.detach().to("cpu", torch.int64).contiguous()
+    out = ctypes.c_int64(0)
+    B.check(B.load().la_checkpoint_rows(cu.data_ptr(), 64, cu.numel() - 1, int(n), ctypes.byref(out)),
+            "la_checkpoint_rows")
+    return int(out.value)
+
+
+def workspace_bytes(N: int, summary: bool = False) -> int:
+    return int(B.load().la_gdn_workspace_bytes(int(N), int(bool(summary))))
+
+
+def gdn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
+            cu_seqlens: torch.Tensor, *, scale: Optional[float] = None, use_qk_l2norm: bool = True,
+            initial_state: Optional[torch.Tensor] = None, output_final_state: bool = True,
+            checkpoint_every_n: int = 0, checkpoint_dtype: torch.dtype = torch.bfloat16,
+            checkpoint_rows_hint: Optional[int] = None, o: Optional[torch.Tensor] = None,
+            final_state: Optional[torch.Tensor] = None, checkpoints: Optional[torch.Tensor] = None,
+            workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+            stream: Optional[torch.cuda.Stream] = None
+            ) -> Tuple[torch.Tensor, Optional[torch.Tensor], Optional[torch.Tensor]]:
+    """Chunked GDN forward.  Returns (o [T, HO, V] bf16, final_state [N, HO, K, V] fp32 or None,
+    checkpoints [R, HO, K, V] or None).  Asynchronous on the current stream."""
+    _check_thd("q", q, torch.bfloat16)
+    _check_thd("k", k, torch.bfloat16)
+    _check_thd("v", v, torch.bfloat16)
+    _check_thd("g", g, torch.float32, heads_dim=False)
+    _check_thd("beta", beta, torch.float32, heads_dim=False)
+    T, HK, K = k.shape
+    HV, V = v.shape[1], v.shape[2]
+    N = cu_seqlens.numel() - 1
+    HO = HV
+    dev = q.device
+    if o is None:
+        o = torch.empty(T, HO, V, dtype=torch.bfloat16, device=dev)
+    if output_final_state and final_state is None:
+        final_state = torch.empty(N, HO, K, V, dtype=torch.float32, device=dev)
+    if not output_final_state:
+        final_state = None
+    if checkpoint_every_n and checkpoints is None:
+        R = checkpoint_rows_hint if checkpoint_rows_hint is not None else checkpoint_rows(cu_seqlens, checkpoint_every_n)
+        checkpoints = torch.empty(R, HO, K, V, dtype=checkpoint_dtype, device=dev)
+    if workspace is None:
+        workspace = torch.empty(workspace_bytes(N), dtype=torch.uint8, device=dev)
+    if initial_state is not None:
+        initial_state = initial_state.contiguous()
+    p = B.GdnFwdParams()
+    p.q, p.q_stride_t, p.q_stride_h = q.data_ptr(), q.stride(0), q.stride(1)
+    p.k, p.k_stride_t, p.k_stride_h = k.data_ptr(), k.stride(0), k.stride(1)
+    p.v, p.v_stride_t, p.v_stride_h = v.data_ptr(), v.stride(0), v.stride(1)
+    p.g, p.g_stride_t, p.g_stride_h = g.data_ptr(), g.stride(0), g.stride(1)
+    p.beta, p.beta_stride_t, p.beta_stride_h = beta.data_ptr(), beta.stride(0), beta.stride(1)
+    p.cu_seqlens, p.cu_seqlens_bits = cu_seqlens.data_ptr(), _cu_bits(cu_seqlens)
+    p.T, p.N, p.HK, p.HV, p.K, p.V = T, N, HK, HV, K, V
+    p.scale = float(scale) if scale is not None else 1.0 / math.sqrt(K)
+    p.use_qk_l2norm = int(bool(use_qk_l2norm))
+    if initial_state is not None:
+        p.initial_state = initial_state.data_ptr()
+        p.initial_state_dtype = B.LA_DTYPE_BF16 if initial_state.dtype == torch.bfloat16 else B.LA_DTYPE_F32
+    p.o, p.o_stride_t, p.o_stride_h = o.data_ptr(), o.stride(0), o.stride(1)
+    p.final_state = final_state.data_ptr() if final_state is not None else None
+    if checkpoints is not None:
+        p.checkpoints = checkpoints.data_ptr()
+        p.checkpoint_dtype = B.LA_DTYPE_BF16 if checkpoints.dtype == torch.bfloat16 else B.LA_DTYPE_F32
+        p.checkpoint_every_n = int(checkpoint_every_n)
+    p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel()
+    p.status = status.data_ptr() if status is not None else None
+    B.check(B.load().gdn_fwd(ctypes.byref(p), _stream_ptr(stream)), "gdn_fwd")
+    return o, final_state, checkpoints
+
+
+def gdn_summary(k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
+                cu_seqlens: torch.Tensor, *, use_qk_l2norm: bool = True,
+                start_state: Optional[torch.Tensor] = None, end_state: Optional[torch.Tensor] = None,
+                transition: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                status: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None
+                ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Span summary.  Returns (end_state [N, HO, K, V] fp32, transition [N, HO, K, K] fp32) with
+    end_state = einsum('ab,av->bv', transition, S_init) + S_H across spans."""
+    _check_thd("k", k, torch.bfloat16)
+    _check_thd("v", v, torch.bfloat16)
+    _check_thd("g", g, torch.float32, heads_dim=False)
+    _check_thd("beta", beta, torch.float32, heads_dim=False)
+    T, HK, K = k.shape
+    HV, V = v.shape[1], v.shape[2]
+    N = cu_seqlens.numel() - 1
+    HO = HV
+    dev = k.device
+    if end_state is None:
+        end_state = torch.empty(N, HO, K, V, dtype=torch.float32, device=dev)
+    if transition is None:
+        transition = torch.empty(N, HO, K, K, dtype=torch.float32, device=dev)
+    if workspace is None:
+        workspace = torch.empty(workspace_bytes(N, True), dtype=torch.uint8, device=dev)
+    if start_state is not None:
+        start_state = start_state.contiguous()
+    p = B.GdnSummaryParams()
+    p.k, p.k_stride_t, p.k_stride_h = k.data_ptr(), k.stride(0), k.stride(1)
+    p.v, p.v_stride_t, p.v_stride_h = v.data_ptr(), v.stride(0), v.stride(1)
+    p.g, p.g_stride_t, p.g_stride_h = g.data_ptr(), g.stride(0), g.stride(1)
+    p.beta, p.beta_stride_t, p.beta_stride_h = beta.data_ptr(), beta.stride(0), beta.stride(1)
+    p.cu_seqlens, p.cu_seqlens_bits = cu_seqlens.data_ptr(), _cu_bits(cu_seqlens)
+    p.T, p.N, p.HK, p.HV, p.K, p.V = T, N, HK, HV, K, V
+    p.use_qk_l2norm = int(bool(use_qk_l2norm))
+    if start_state is not None:
+        p.start_state = start_state.data_ptr()
+        p.start_state_dtype = B.LA_DTYPE_BF16 if start_state.dtype == torch.bfloat16 else B.LA_DTYPE_F32
+    p.end_state = end_state.data_ptr()
+    p.transition = transition.data_ptr()
+    p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel()
+    p.status = status.data_ptr() if status is not None else None
+    B.check(B.load().gdn_summary(ctypes.byref(p), _stream_ptr(stream)), "gdn_summary")
+    return end_state, transition
+
+
+def read_status(status: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> int:
+    """Synchronises the stream and returns the device status word (an la_status code)."""
+    out = ctypes.c_int32(0)
+    B.check(B.load().la_read_status(status.data_ptr(), _stream_ptr(stream), ctypes.byref(out)), "la_read_status")
+    return int(out.value)

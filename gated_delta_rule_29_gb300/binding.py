@@ -1,0 +1,131 @@
+"""ctypes binding of liblinattn (include/liblinattn.h), argument marshalling only.
+
+Every step of the computation runs in the library's CUDA kernels.  There is no
+fallback: if the shared library cannot be built or loaded, importing the
+functions below raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+from . import _build
+
+LA_OK = 0
+LA_ERR_INVALID_ARG = 1
+LA_ERR_UNSUPPORTED = 2
+LA_ERR_CUDA = 3
+LA_ERR_BAD_SEQLENS = 4
+LA_ERR_TIMEOUT = 5
+LA_ERR_WORKSPACE = 6
+
+LA_DTYPE_BF16 = 0
+LA_DTYPE_F32 = 1
+
+EXPORTED_SYMBOLS = (
+    "gdn_fwd",
+    "gdn_summary",
+    "la_gdn_workspace_bytes",
+    "la_checkpoint_rows",
+    "la_read_status",
+    "la_status_string",
+    "la_version",
+    "la_set_kernel_timing_events",
+)
+
+_i64 = ctypes.c_int64
+_i32 = ctypes.c_int32
+_vp = ctypes.c_void_p
+
+
+class GdnFwdParams(ctypes.Structure):
+    """Mirror of la_gdn_fwd_params (same field order and types)."""
+    _fields_ = [
+        ("q", _vp), ("q_stride_t", _i64), ("q_stride_h", _i64),
+        ("k", _vp), ("k_stride_t", _i64), ("k_stride_h", _i64),
+        ("v", _vp), ("v_stride_t", _i64), ("v_stride_h", _i64),
+        ("g", _vp), ("g_stride_t", _i64), ("g_stride_h", _i64),
+        ("beta", _vp), ("beta_stride_t", _i64), ("beta_stride_h", _i64),
+        ("cu_seqlens", _vp), ("cu_seqlens_bits", _i32),
+        ("T", _i64),
+        ("N", _i32), ("HK", _i32), ("HV", _i32), ("K", _i32), ("V", _i32),
+        ("scale", ctypes.c_float), ("use_qk_l2norm", _i32),
+        ("initial_state", _vp), ("initial_state_dtype", _i32),
+        ("o", _vp), ("o_stride_t", _i64), ("o_stride_h", _i64),
+        ("final_state", _vp),
+        ("checkpoints", _vp), ("checkpoint_dtype", _i32), ("checkpoint_every_n", _i64),
+        ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
+        ("status", _vp),
+    ]
+
+
+class GdnSummaryParams(ctypes.Structure):
+    """Mirror of la_gdn_summary_params (same field order and types)."""
+    _fields_ = [
+        ("k", _vp), ("k_stride_t", _i64), ("k_stride_h", _i64),
+        ("v", _vp), ("v_stride_t", _i64), ("v_stride_h", _i64),
+        ("g", _vp), ("g_stride_t", _i64), ("g_stride_h", _i64),
+        ("beta", _vp), ("beta_stride_t", _i64), ("beta_stride_h", _i64),
+        ("cu_seqlens", _vp), ("cu_seqlens_bits", _i32),
+        ("T", _i64),
+        ("N", _i32), ("HK", _i32), ("HV", _i32), ("K", _i32), ("V", _i32),
+        ("use_qk_l2norm", _i32),
+        ("start_state", _vp), ("start_state_dtype", _i32),
+        ("end_state", _vp),
+        ("transition", _vp),
+        ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
+        ("status", _vp),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load liblinattn.so (building it in-tree first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if build_if_missing and not _build.up_to_date():
+            _build.build()
+        if not os.path.exists(path):
+            raise RuntimeError(f"liblinattn.so not found at {path}; run __graft_entry__.build()")
+        lib = ctypes.CDLL(path)
+        lib.gdn_fwd.restype = ctypes.c_int
+        lib.gdn_fwd.argtypes = [ctypes.POINTER(GdnFwdParams), _vp]
+        lib.gdn_summary.restype = ctypes.c_int
+        lib.gdn_summary.argtypes = [ctypes.POINTER(GdnSummaryParams), _vp]
+        lib.la_gdn_workspace_bytes.restype = ctypes.c_size_t
+        lib.la_gdn_workspace_bytes.argtypes = [_i32, _i32]
+        lib.la_checkpoint_rows.restype = ctypes.c_int
+        lib.la_checkpoint_rows.argtypes = [_vp, _i32, _i32, _i64, ctypes.POINTER(_i64)]
+        lib.la_read_status.restype = ctypes.c_int
+        lib.la_read_status.argtypes = [_vp, _vp, ctypes.POINTER(_i32)]
+        lib.la_status_string.restype = ctypes.c_char_p
+        lib.la_status_string.argtypes = [ctypes.c_int]
+        lib.la_version.restype = _i32
+        lib.la_version.argtypes = []
+        lib.la_set_kernel_timing_events.restype = ctypes.c_int
+        lib.la_set_kernel_timing_events.argtypes = [_vp, _vp]
+        _lib = lib
+        return lib
+
+
+class LinAttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        msg = load().la_status_string(code).decode()
+        super().__init__(f"{where}: {msg} (la_status {code})")
+        self.code = code
+
+
+def check(code: int, where: str) -> None:
+    if code != LA_OK:
+        raise LinAttnError(code, where)

@@ -1,0 +1,99 @@
+// gdn_kernel.h -- internal interface between the C ABI (la_api.cu) and the kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+namespace la {
+
+constexpr int kChunk = 64;          // tokens per chunk; the chunk grid restarts at each sequence
+constexpr int kThreads = 256;       // threads of the fused chunk kernel
+constexpr int kPrologueThreads = 1024;
+
+enum Mode : int { kModeFwd = 0, kModeSummary = 1 };
+enum TileKind : int { kTileValue = 0, kTileTransition = 1 };
+
+// Workspace layout (bytes from the 256-aligned workspace base).
+//   [0, 256)                 header: status, ticket
+//   [256, 256 + 4N)          order[N]: sequences sorted longest-first (ties by index)
+//   next 256-aligned, 8N     ckpt_off[N]: first checkpoint row of each sequence
+//   next 256-aligned, 8P     sort keys (P = next power of two >= N), used only when N is
+//                            too large for the prologue's shared-memory sort
+struct WorkspaceLayout {
+    size_t order, ckpt_off, keys, total;
+};
+__host__ __device__ inline size_t ws_align(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+__host__ __device__ inline uint32_t next_pow2(uint32_t n) {
+    uint32_t p = 1;
+    while (p < n) p <<= 1;
+    return p;
+}
+constexpr uint32_t kSmemSortMax = 8192;  // keys sorted in shared memory up to this many
+__host__ __device__ inline WorkspaceLayout ws_layout(int32_t N) {
+    WorkspaceLayout L;
+    const size_t n = N > 0 ? static_cast<size_t>(N) : 1;
+    L.order = 256;
+    L.ckpt_off = ws_align(L.order + 4 * n);
+    L.keys = ws_align(L.ckpt_off + 8 * n);
+    const size_t p = n > kSmemSortMax ? next_pow2(static_cast<uint32_t>(n)) : 0;
+    L.total = ws_align(L.keys + 8 * p);
+    return L;
+}
+
+struct WsHeader {
+    int32_t status;     // LA_OK or a device-side error code
+    int32_t reserved;
+    uint64_t ticket;    // next unit to hand out (8-byte aligned for the 64-bit atomic)
+};
+
+struct PrologueArgs {
+    const void* cu;
+    int32_t cu64;
+    int64_t T;
+    int32_t N;
+    int64_t ckpt_n;       // 0: no checkpoint offsets
+    WsHeader* hdr;
+    int32_t* order;
+    int64_t* ckpt_off;
+    uint64_t* keys;       // global sort scratch (N > kSmemSortMax)
+    int32_t* user_status; // nullable
+};
+
+struct ChunkArgs {
+    // per-token scalars [T, HO]
+    const float* g;
+    int64_t g_st, g_sh;
+    const float* beta;
+    int64_t b_st, b_sh;
+    const void* cu;
+    int32_t cu64;
+    int64_t T;
+    int32_t N, HK, HV, K, V, group;  // group = HV / HK
+    float scale;
+    int32_t l2norm;
+    const void* s0;                  // [N, HO, K, V] or null
+    int32_t s0_bf16;
+    uint16_t* o;                     // [T, HO, V] bf16 bits (fwd)
+    int64_t o_st, o_sh;
+    float* final_state;              // fwd: final state; summary: end state
+    void* ckpt;                      // [R, HO, K, V]
+    int32_t ckpt_bf16;
+    int64_t ckpt_n;
+    float* transition;               // summary: [N, HO, K, K]
+    int32_t tiles_per_head;          // fwd 1; summary 2 (value tile, transition tile)
+    int64_t num_units;               // N * HO * tiles_per_head
+    WsHeader* hdr;
+    const int32_t* order;
+    const int64_t* ckpt_off;
+    int32_t* user_status;
+    uint64_t wait_budget_ns;
+};
+
+// Launchers (return cudaError_t of the launch).
+cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t s);
+cudaError_t launch_chunk_kernel(const ChunkArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
+                                const CUtensorMap& vmap, int mode, cudaStream_t s);
+int chunk_kernel_grid(int device, int64_t num_units);
+
+}  // namespace la

@@ -1,0 +1,330 @@
+// la_api.cu -- the extern "C" boundary of liblinattn (declared in include/liblinattn.h).
+//
+// Host work only: argument validation (metadata, never values), TMA descriptor
+// encoding from the caller's strides, workspace selection, and two launches on
+// the caller's stream: the device prologue and the fused chunk kernel.  No host
+// synchronisation happens on this path.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/liblinattn.h"
+#include "gdn_kernel.h"
+
+namespace {
+
+using la::ChunkArgs;
+using la::PrologueArgs;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+constexpr uint64_t kWaitBudgetNs = 1000000000ull;  // 1 s per bounded wait
+
+// Events recorded around the next chunk-kernel launch of this host thread.
+thread_local cudaEvent_t t_timing_start = nullptr;
+thread_local cudaEvent_t t_timing_stop = nullptr;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// [T, H, D] bf16 view with 64 x 1 x 64 boxes (64 features of one head, 64 tokens), 128-byte swizzle.
+la_status make_map(CUtensorMap* m, const void* base, int64_t T, int64_t H, int64_t D, int64_t st, int64_t sh) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return LA_ERR_CUDA;
+    if (H == 1) sh = D;  // the stride of a size-1 axis is never used
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(sh) * 2, static_cast<cuuint64_t>(st) * 2};
+    cuuint32_t box[3] = {64, 1, 64};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? LA_OK : LA_ERR_INVALID_ARG;
+}
+
+// A bf16 [T, H, D] operand read through TMA: 16-byte base, strides multiples of 8 elements.
+la_status check_tma_operand(const void* p, int64_t st, int64_t sh, int64_t H) {
+    if (!p) return LA_ERR_INVALID_ARG;
+    if (!aligned(p, 16)) return LA_ERR_INVALID_ARG;
+    if (st <= 0 || st % 8 != 0) return LA_ERR_INVALID_ARG;
+    if (H > 1 && (sh <= 0 || sh % 8 != 0)) return LA_ERR_INVALID_ARG;
+    return LA_OK;
+}
+
+struct DeviceWorkspace {
+    void* ptr = nullptr;
+    size_t bytes = 0;
+};
+std::mutex g_ws_mutex;
+DeviceWorkspace g_ws[128];
+
+// Internal per-device workspace, grown on demand (growth synchronises the device once).
+la_status internal_workspace(size_t need, void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return LA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_ws_mutex);
+    DeviceWorkspace& w = g_ws[dev];
+    if (w.bytes < need) {
+        if (w.ptr) {
+            if (cudaDeviceSynchronize() != cudaSuccess) return LA_ERR_CUDA;
+            cudaFree(w.ptr);
+            w.ptr = nullptr;
+            w.bytes = 0;
+        }
+        size_t grow = need < (1u << 20) ? (1u << 20) : need;
+        if (cudaMalloc(&w.ptr, grow) != cudaSuccess) return LA_ERR_CUDA;
+        w.bytes = grow;
+    }
+    *out = w.ptr;
+    return LA_OK;
+}
+
+la_status resolve_workspace(void* user, size_t user_bytes, int32_t N, void** out) {
+    const size_t need = la::ws_layout(N).total;
+    if (user) {
+        if (user_bytes < need || !aligned(user, 256)) return LA_ERR_WORKSPACE;
+        *out = user;
+        return LA_OK;
+    }
+    return internal_workspace(need, out);
+}
+
+struct Common {
+    int64_t T;
+    int32_t N, HK, HV, K, V;
+    const void* cu;
+    int32_t cu_bits;
+    const float* g;
+    const float* beta;
+};
+
+la_status check_common(const Common& c) {
+    if (c.T < 0 || c.N < 0 || c.HK <= 0 || c.HV <= 0) return LA_ERR_INVALID_ARG;
+    if (c.cu_bits != 32 && c.cu_bits != 64) return LA_ERR_INVALID_ARG;
+    if (!c.cu || !aligned(c.cu, c.cu_bits / 8)) return LA_ERR_INVALID_ARG;
+    if ((c.K != 64 && c.K != 128) || (c.V != 64 && c.V != 128)) return LA_ERR_UNSUPPORTED;
+    if (c.HV % c.HK != 0) return LA_ERR_UNSUPPORTED;
+    if (c.T >= (int64_t(1) << 31) - 64) return LA_ERR_UNSUPPORTED;  // TMA coordinates are int32
+    if (c.T > 0 && (!c.g || !c.beta || !aligned(c.g, 4) || !aligned(c.beta, 4))) return LA_ERR_INVALID_ARG;
+    return LA_OK;
+}
+
+la_status run(const Common& c, ChunkArgs& ka, const void* q, int64_t q_st, int64_t q_sh, const void* k, int64_t k_st,
+              int64_t k_sh, const void* v, int64_t v_st, int64_t v_sh, int64_t ckpt_n, void* workspace,
+              size_t workspace_bytes, int32_t* user_status, int mode, cudaStream_t stream) {
+    void* ws = nullptr;
+    la_status st = resolve_workspace(workspace, workspace_bytes, c.N, &ws);
+    if (st != LA_OK) return st;
+    const la::WorkspaceLayout L = la::ws_layout(c.N);
+    uint8_t* wsb = static_cast<uint8_t*>(ws);
+
+    PrologueArgs pa;
+    pa.cu = c.cu;
+    pa.cu64 = c.cu_bits == 64;
+    pa.T = c.T;
+    pa.N = c.N;
+    pa.ckpt_n = ckpt_n;
+    pa.hdr = reinterpret_cast<la::WsHeader*>(wsb);
+    pa.order = reinterpret_cast<int32_t*>(wsb + L.order);
+    pa.ckpt_off = reinterpret_cast<int64_t*>(wsb + L.ckpt_off);
+    pa.keys = reinterpret_cast<uint64_t*>(wsb + L.keys);
+    pa.user_status = user_status;
+    if (la::launch_prologue(pa, stream) != cudaSuccess) return LA_ERR_CUDA;
+
+    const int32_t HO = c.HV;
+    ka.g = c.g;
+    ka.beta = c.beta;
+    ka.cu = c.cu;
+    ka.cu64 = c.cu_bits == 64;
+    ka.T = c.T;
+    ka.N = c.N;
+    ka.HK = c.HK;
+    ka.HV = c.HV;
+    ka.K = c.K;
+    ka.V = c.V;
+    ka.group = c.HV / c.HK;
+    ka.num_units = static_cast<int64_t>(c.N) * HO * ka.tiles_per_head;
+    ka.hdr = pa.hdr;
+    ka.order = pa.order;
+    ka.ckpt_off = pa.ckpt_off;
+    ka.user_status = user_status;
+    ka.wait_budget_ns = kWaitBudgetNs;
+    if (ka.num_units == 0) return LA_OK;
+
+    CUtensorMap qm, km, vm;
+    std::memset(&qm, 0, sizeof(qm));
+    std::memset(&km, 0, sizeof(km));
+    std::memset(&vm, 0, sizeof(vm));
+    const int64_t Tm = c.T > 0 ? c.T : 1;  // descriptors need a non-empty extent
+    if (c.T > 0) {
+        if ((st = make_map(&km, k, Tm, c.HK, c.K, k_st, k_sh)) != LA_OK) return st;
+        if ((st = make_map(&vm, v, Tm, c.HV, c.V, v_st, v_sh)) != LA_OK) return st;
+        if (q) {
+            if ((st = make_map(&qm, q, Tm, c.HK, c.K, q_st, q_sh)) != LA_OK) return st;
+        } else {
+            qm = km;
+        }
+    }
+    cudaEvent_t ev0 = t_timing_start, ev1 = t_timing_stop;
+    t_timing_start = t_timing_stop = nullptr;
+    if (ev0 && cudaEventRecord(ev0, stream) != cudaSuccess) return LA_ERR_CUDA;
+    if (la::launch_chunk_kernel(ka, qm, km, vm, mode, stream) != cudaSuccess) return LA_ERR_CUDA;
+    if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess) return LA_ERR_CUDA;
+    return LA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+la_status gdn_fwd(const la_gdn_fwd_params* p, void* stream) {
+    if (!p) return LA_ERR_INVALID_ARG;
+    Common c{p->T, p->N, p->HK, p->HV, p->K, p->V, p->cu_seqlens, p->cu_seqlens_bits, p->g, p->beta};
+    la_status st = check_common(c);
+    if (st != LA_OK) return st;
+    if (p->T > 0) {
+        if ((st = check_tma_operand(p->q, p->q_stride_t, p->q_stride_h, p->HK)) != LA_OK) return st;
+        if ((st = check_tma_operand(p->k, p->k_stride_t, p->k_stride_h, p->HK)) != LA_OK) return st;
+        if ((st = check_tma_operand(p->v, p->v_stride_t, p->v_stride_h, p->HV)) != LA_OK) return st;
+        if (!p->o || !aligned(p->o, 2) || p->o_stride_t <= 0 || (p->HV > 1 && p->o_stride_h <= 0))
+            return LA_ERR_INVALID_ARG;
+    }
+    if (p->initial_state) {
+        if (p->initial_state_dtype != LA_DTYPE_F32 && p->initial_state_dtype != LA_DTYPE_BF16) return LA_ERR_UNSUPPORTED;
+        if (!aligned(p->initial_state, p->initial_state_dtype == LA_DTYPE_F32 ? 4 : 2)) return LA_ERR_INVALID_ARG;
+    }
+    if (p->final_state && !aligned(p->final_state, 4)) return LA_ERR_INVALID_ARG;
+    if (p->checkpoints) {
+        if (p->checkpoint_every_n <= 0 || p->checkpoint_every_n % la::kChunk != 0) return LA_ERR_INVALID_ARG;
+        if (p->checkpoint_dtype != LA_DTYPE_F32 && p->checkpoint_dtype != LA_DTYPE_BF16) return LA_ERR_UNSUPPORTED;
+        if (!aligned(p->checkpoints, p->checkpoint_dtype == LA_DTYPE_F32 ? 4 : 2)) return LA_ERR_INVALID_ARG;
+    }
+    ChunkArgs ka;
+    std::memset(&ka, 0, sizeof(ka));
+    ka.g_st = p->g_stride_t;
+    ka.g_sh = p->g_stride_h;
+    ka.b_st = p->beta_stride_t;
+    ka.b_sh = p->beta_stride_h;
+    ka.scale = p->scale > 0.f ? p->scale : 1.0f / std::sqrt(static_cast<float>(p->K));
+    ka.l2norm = p->use_qk_l2norm != 0;
+    ka.s0 = p->initial_state;
+    ka.s0_bf16 = p->initial_state_dtype == LA_DTYPE_BF16;
+    ka.o = static_cast<uint16_t*>(p->o);
+    ka.o_st = p->o_stride_t;
+    ka.o_sh = p->o_stride_h;
+    ka.final_state = p->final_state;
+    ka.ckpt = p->checkpoints;
+    ka.ckpt_bf16 = p->checkpoint_dtype == LA_DTYPE_BF16;
+    ka.ckpt_n = p->checkpoints ? p->checkpoint_every_n : 0;
+    ka.transition = nullptr;
+    ka.tiles_per_head = 1;
+    return run(c, ka, p->q, p->q_stride_t, p->q_stride_h, p->k, p->k_stride_t, p->k_stride_h, p->v, p->v_stride_t,
+               p->v_stride_h, ka.ckpt_n, p->workspace, p->workspace_bytes, p->status, la::kModeFwd,
+               static_cast<cudaStream_t>(stream));
+}
+
+la_status gdn_summary(const la_gdn_summary_params* p, void* stream) {
+    if (!p) return LA_ERR_INVALID_ARG;
+    Common c{p->T, p->N, p->HK, p->HV, p->K, p->V, p->cu_seqlens, p->cu_seqlens_bits, p->g, p->beta};
+    la_status st = check_common(c);
+    if (st != LA_OK) return st;
+    if (p->T > 0) {
+        if ((st = check_tma_operand(p->k, p->k_stride_t, p->k_stride_h, p->HK)) != LA_OK) return st;
+        if ((st = check_tma_operand(p->v, p->v_stride_t, p->v_stride_h, p->HV)) != LA_OK) return st;
+    }
+    if (!p->end_state || !p->transition) return LA_ERR_INVALID_ARG;
+    if (!aligned(p->end_state, 4) || !aligned(p->transition, 16)) return LA_ERR_INVALID_ARG;
+    if (p->start_state) {
+        if (p->start_state_dtype != LA_DTYPE_F32 && p->start_state_dtype != LA_DTYPE_BF16) return LA_ERR_UNSUPPORTED;
+        if (!aligned(p->start_state, p->start_state_dtype == LA_DTYPE_F32 ? 4 : 2)) return LA_ERR_INVALID_ARG;
+    }
+    ChunkArgs ka;
+    std::memset(&ka, 0, sizeof(ka));
+    ka.g_st = p->g_stride_t;
+    ka.g_sh = p->g_stride_h;
+    ka.b_st = p->beta_stride_t;
+    ka.b_sh = p->beta_stride_h;
+    ka.scale = 1.f;
+    ka.l2norm = p->use_qk_l2norm != 0;
+    ka.s0 = p->start_state;
+    ka.s0_bf16 = p->start_state_dtype == LA_DTYPE_BF16;
+    ka.final_state = p->end_state;
+    ka.transition = p->transition;
+    ka.tiles_per_head = 2;
+    return run(c, ka, nullptr, 0, 0, p->k, p->k_stride_t, p->k_stride_h, p->v, p->v_stride_t, p->v_stride_h, 0,
+               p->workspace, p->workspace_bytes, p->status, la::kModeSummary, static_cast<cudaStream_t>(stream));
+}
+
+size_t la_gdn_workspace_bytes(int32_t N, int32_t summary) {
+    (void)summary;
+    return la::ws_layout(N).total;
+}
+
+la_status la_checkpoint_rows(const void* cu_seqlens_host, int32_t idx_bits, int32_t N, int64_t n, int64_t* rows_out) {
+    if (!cu_seqlens_host || !rows_out || n <= 0 || N < 0 || (idx_bits != 32 && idx_bits != 64))
+        return LA_ERR_INVALID_ARG;
+    int64_t rows = 0;
+    for (int32_t i = 0; i < N; ++i) {
+        int64_t a, b;
+        if (idx_bits == 64) {
+            a = static_cast<const int64_t*>(cu_seqlens_host)[i];
+            b = static_cast<const int64_t*>(cu_seqlens_host)[i + 1];
+        } else {
+            a = static_cast<const int32_t*>(cu_seqlens_host)[i];
+            b = static_cast<const int32_t*>(cu_seqlens_host)[i + 1];
+        }
+        if (b < a) return LA_ERR_INVALID_ARG;
+        rows += (b - a + n - 1) / n;
+    }
+    *rows_out = rows;
+    return LA_OK;
+}
+
+la_status la_read_status(const int32_t* device_status, void* stream, int32_t* out) {
+    if (!device_status || !out) return LA_ERR_INVALID_ARG;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return LA_ERR_CUDA;
+    if (cudaMemcpy(out, device_status, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess) return LA_ERR_CUDA;
+    return LA_OK;
+}
+
+la_status la_set_kernel_timing_events(void* start_event, void* stop_event) {
+    t_timing_start = static_cast<cudaEvent_t>(start_event);
+    t_timing_stop = static_cast<cudaEvent_t>(stop_event);
+    return LA_OK;
+}
+
+const char* la_status_string(la_status s) {
+    switch (s) {
+        case LA_OK: return "ok";
+        case LA_ERR_INVALID_ARG: return "invalid argument (pointer, shape, stride or alignment)";
+        case LA_ERR_UNSUPPORTED: return "unsupported configuration (head dims, head grouping or dtype)";
+        case LA_ERR_CUDA: return "a CUDA call failed";
+        case LA_ERR_BAD_SEQLENS: return "cu_seqlens must start at 0, be nondecreasing and end at T";
+        case LA_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
+        case LA_ERR_WORKSPACE: return "workspace too small or not 256-byte aligned";
+    }
+    return "unknown status";
+}
+
+int32_t la_version(void) { return 100; }
+
+}  // extern "C"

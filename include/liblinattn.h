@@ -1,0 +1,182 @@
+/*
+ * liblinattn.h -- C ABI of the GB300 (sm_103a) chunked Gated DeltaNet forward.
+ *
+ * The operation is defined on the cuDNN "Linear Attention" operations page
+ * (docs.nvidia.com/cudnn/operations/LinearAttention): for every sequence of a
+ * packed THD batch and every output head, a recurrent matrix state
+ * S[K][V] evolves token by token as
+ *
+ *     S_t = exp(g_t) (I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = scale * S_t^T q_t
+ *
+ * (the page's Householder-product family with one update per token), with the
+ * options of its worked example and of its "Semantics worth knowing" section:
+ * in-kernel L2 normalisation of q and k, an initial state, the final state,
+ * state checkpoints every n tokens, and the span summary.
+ *
+ * Conventions shared by every entry point
+ *   - Layout is packed THD ("Layout" section): tokens of all N sequences are
+ *     concatenated on axis 0; cu_seqlens[N+1] (int32 or int64, device memory)
+ *     gives the boundaries and must start at 0, be nondecreasing and end at T.
+ *   - Operands are rank-3 [T, heads, dim] views given by a device pointer and
+ *     two strides in ELEMENTS (token stride, head stride); the innermost (dim)
+ *     axis must be contiguous.  Base addresses must be 16-byte aligned and
+ *     the token/head strides of bf16 operands multiples of 8 elements (the
+ *     kernels read q/k/v through TMA descriptors built from these strides,
+ *     "Layout" section: column slices of a fused projection are accepted).
+ *   - Dtypes are fixed, as on the page's support matrix (callers convert):
+ *     q, k, v and o are bf16; g and beta are fp32 [T, HO]; states are fp32 (an
+ *     initial state may also be bf16).  K and V must be 64 or 128.
+ *   - Heads: HK q/k heads, HV value heads, HO = HV output heads; HV must be a
+ *     multiple of HK and output head h reads q/k head h / (HV / HK).
+ *   - Every pointer is device memory unless stated.  The caller owns every
+ *     buffer; the library never frees caller memory.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL is the legacy default stream) and never synchronise the host.
+ *   - Errors: argument problems found on the host are returned synchronously
+ *     and nothing is launched.  Problems only the device can see (bad
+ *     cu_seqlens values, a bounded wait that ran out) are written to the
+ *     device status word; the outputs are then unspecified.
+ *   - Batch invariance (batch_invariant, same section): a sequence's results
+ *     are bitwise identical whatever else is in the batch.
+ */
+#ifndef LIBLINATTN_H
+#define LIBLINATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum la_status {
+    LA_OK = 0,
+    LA_ERR_INVALID_ARG = 1,  /* null pointer, bad shape/stride/alignment, N < 0, ... */
+    LA_ERR_UNSUPPORTED = 2,  /* K or V not in {64,128}, HV % HK != 0, HK > HV, dtype */
+    LA_ERR_CUDA = 3,         /* a CUDA runtime or driver call failed (launch, encode) */
+    LA_ERR_BAD_SEQLENS = 4,  /* device-side: cu_seqlens not 0-based, decreasing or != T at N */
+    LA_ERR_TIMEOUT = 5,      /* device-side: a bounded wait in a kernel gave up */
+    LA_ERR_WORKSPACE = 6     /* workspace smaller than la_gdn_workspace_bytes() */
+} la_status;
+
+typedef enum la_dtype { LA_DTYPE_BF16 = 0, LA_DTYPE_F32 = 1 } la_dtype;
+
+/* Parameters of gdn_fwd.  Strides are in elements. */
+typedef struct la_gdn_fwd_params {
+    /* ---- inputs ---- */
+    const void* q;    int64_t q_stride_t, q_stride_h;       /* [T, HK, K] bf16 */
+    const void* k;    int64_t k_stride_t, k_stride_h;       /* [T, HK, K] bf16 */
+    const void* v;    int64_t v_stride_t, v_stride_h;       /* [T, HV, V] bf16 */
+    const float* g;   int64_t g_stride_t, g_stride_h;       /* [T, HO] fp32, natural-log decay */
+    const float* beta; int64_t beta_stride_t, beta_stride_h; /* [T, HO] fp32 */
+    const void* cu_seqlens;                                 /* [N + 1] */
+    int32_t cu_seqlens_bits;                                /* 32 or 64 */
+    int64_t T;
+    int32_t N, HK, HV, K, V;
+    float scale;              /* multiplies the (normalised) query; <= 0 selects 1/sqrt(K) */
+    int32_t use_qk_l2norm;    /* q, k <- x / sqrt(sum x^2 + 1e-6) before the recurrence */
+    const void* initial_state;  /* [N, HO, K, V] contiguous, or NULL for a zero start */
+    int32_t initial_state_dtype; /* la_dtype */
+    /* ---- outputs ---- */
+    void* o;          int64_t o_stride_t, o_stride_h;       /* [T, HO, V] bf16 */
+    float* final_state;       /* [N, HO, K, V] fp32 contiguous, or NULL (output_final_state=False) */
+    void* checkpoints;        /* [R, HO, K, V] contiguous, or NULL; R = la_checkpoint_rows() */
+    int32_t checkpoint_dtype; /* la_dtype of the checkpoint rows */
+    int64_t checkpoint_every_n; /* > 0 and a multiple of 64 when checkpoints != NULL */
+    /* ---- scratch and status ---- */
+    void* workspace;          /* >= la_gdn_workspace_bytes(N, 0) bytes, 256-byte aligned, or NULL */
+    size_t workspace_bytes;
+    int32_t* status;          /* optional device int32; receives LA_OK or a device-side error */
+} la_gdn_fwd_params;
+
+/*
+ * gdn_fwd -- the chunked GDN forward over a packed THD batch.
+ *
+ * Page: "Example" (gated_delta_net(q, k, v, g, beta, cu_seqlens,
+ * output_final_state, use_qk_l2norm_in_kernel)) and "States and checkpoints".
+ *   o[t, h, :]       = scale * S_t^T q_hat_t for every token (inclusive of t).
+ *   final_state      = the state after each sequence's last token (an empty
+ *                      sequence returns its initial state, or zeros).
+ *   checkpoints      = the state entering token offsets 0, n, 2n, ... < L of
+ *                      each sequence (entry 0 is the initial state), packed in
+ *                      sequence order: sequence i owns ceil(L_i / n) rows
+ *                      starting at sum_{j<i} ceil(L_j / n).
+ * Workspace: if `workspace` is NULL an internal per-device buffer is used;
+ * overlapping calls on different streams must then each pass their own.
+ * Returns LA_OK once the work is enqueued.
+ */
+la_status gdn_fwd(const la_gdn_fwd_params* p, void* stream);
+
+/* Parameters of gdn_summary.  Strides are in elements. */
+typedef struct la_gdn_summary_params {
+    const void* k;    int64_t k_stride_t, k_stride_h;       /* [T, HK, K] bf16 */
+    const void* v;    int64_t v_stride_t, v_stride_h;       /* [T, HV, V] bf16 */
+    const float* g;   int64_t g_stride_t, g_stride_h;       /* [T, HO] fp32 */
+    const float* beta; int64_t beta_stride_t, beta_stride_h; /* [T, HO] fp32 */
+    const void* cu_seqlens;                                 /* [N + 1]: the spans */
+    int32_t cu_seqlens_bits;
+    int64_t T;
+    int32_t N, HK, HV, K, V;
+    int32_t use_qk_l2norm;
+    const void* start_state;  /* [N, HO, K, V] contiguous, or NULL for a zero start */
+    int32_t start_state_dtype;
+    float* end_state;         /* [N, HO, K, V] fp32: S_H, the end state from start_state */
+    float* transition;        /* [N, HO, K, K] fp32 */
+    void* workspace;          /* >= la_gdn_workspace_bytes(N, 1) bytes, or NULL */
+    size_t workspace_bytes;
+    int32_t* status;
+} la_gdn_summary_params;
+
+/*
+ * gdn_summary -- per-span end state and state-transition operator.
+ *
+ * Page: "Summaries" (for the delta-rule variants the transition is a
+ * [N, HO, K, K] fp32 matrix: the span's decayed erase factors multiplied
+ * together, composed across spans as S_final = S_init * transition + S_H).
+ * With P = prod_{t = L-1 .. 0} exp(g_t)(I - beta_t k_hat_t k_hat_t^T), later
+ * steps on the left, the library stores transition = P^T, i.e.
+ *     S_final[b][v] = sum_a transition[a][b] * S_init[a][v] + S_H[b][v]
+ * which is the page's S_init * transition with states read V-major, and the
+ * orientation a backward applies (dS_0 = P^T dS_L).  An empty span returns the
+ * identity and its start state.
+ */
+la_status gdn_summary(const la_gdn_summary_params* p, void* stream);
+
+/* Bytes of device workspace gdn_fwd (summary = 0) or gdn_summary (summary = 1) needs. */
+size_t la_gdn_workspace_bytes(int32_t N, int32_t summary);
+
+/*
+ * Host helper: total checkpoint rows R = sum_i ceil(L_i / n) for a HOST copy of
+ * cu_seqlens (idx_bits 32 or 64).  Returns LA_ERR_INVALID_ARG for n <= 0 or a
+ * decreasing cu_seqlens.
+ */
+la_status la_checkpoint_rows(const void* cu_seqlens_host, int32_t idx_bits, int32_t N, int64_t n,
+                             int64_t* rows_out);
+
+/*
+ * Reads a device status word written by gdn_fwd / gdn_summary.  Synchronises
+ * `stream` first, so it belongs in tests and error paths, not in a hot loop.
+ */
+la_status la_read_status(const int32_t* device_status, void* stream, int32_t* out);
+
+/*
+ * Profiling hook: record `start_event` and `stop_event` (cudaEvent_t handles) on
+ * the launch stream immediately before and after the fused chunk kernel of the
+ * next gdn_fwd / gdn_summary call made by this host thread, so a caller can time
+ * that kernel alone with CUDA events.  The hook is consumed by that one call;
+ * pass NULL, NULL to clear it.  Not part of the computation; no citation.
+ */
+la_status la_set_kernel_timing_events(void* start_event, void* stop_event);
+
+/* Static description of a status code. */
+const char* la_status_string(la_status s);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int32_t la_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBLINATTN_H */

@@ -1,0 +1,183 @@
+"""The C ABI on the host: exports, struct layout, and argument errors (no GPU needed).
+
+Every case here returns from the library before any CUDA call, so it runs on a
+machine without a GPU.  Device pointers are fake, suitably aligned integers:
+validation rejects the call before anything could dereference them.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+from gated_delta_rule_29_gb300 import binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "liblinattn.h")
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:la_status|size_t|const char\*|int32_t)\s+(\w+)\s*\(", text, re.M)))
+
+
+def test_library_exports_every_declared_function():
+    lib = B.load()
+    declared = _declared_functions()
+    assert set(declared) == set(B.EXPORTED_SYMBOLS), declared
+    for name in declared:
+        assert hasattr(lib, name), f"{name} not exported"
+
+
+def _c_layout(struct_name, fields):
+    src = ["#include <stdio.h>", "#include <stddef.h>", f'#include "{HEADER}"', "int main(void) {",
+           f'  printf("%zu\\n", sizeof({struct_name}));']
+    for f in fields:
+        src.append(f'  printf("%zu\\n", offsetof({struct_name}, {f}));')
+    src.append("  return 0; }")
+    d = os.path.join(ROOT, "tests", "_build")
+    os.makedirs(d, exist_ok=True)
+    c = os.path.join(d, f"layout_{struct_name}.c")
+    exe = os.path.join(d, f"layout_{struct_name}")
+    open(c, "w").write("\n".join(src))
+    subprocess.run(["gcc", "-std=c11", "-o", exe, c], check=True)
+    out = subprocess.run([exe], check=True, capture_output=True, text=True).stdout.split()
+    return int(out[0]), [int(x) for x in out[1:]]
+
+
+@pytest.mark.parametrize("cls,cname", [(B.GdnFwdParams, "la_gdn_fwd_params"),
+                                       (B.GdnSummaryParams, "la_gdn_summary_params")])
+def test_ctypes_mirror_matches_c_layout(cls, cname):
+    names = [f[0] for f in cls._fields_]
+    size, offs = _c_layout(cname, names)
+    assert ctypes.sizeof(cls) == size
+    for name, off in zip(names, offs):
+        assert getattr(cls, name).offset == off, name
+
+
+FAKE = 0x10000  # 64 KiB: aligned for every check; never dereferenced
+
+
+def _fwd(**over):
+    p = B.GdnFwdParams()
+    T, N, HK, HV, K, V = 256, 2, 2, 2, 64, 64
+    p.q, p.q_stride_t, p.q_stride_h = FAKE, HK * K, K
+    p.k, p.k_stride_t, p.k_stride_h = FAKE, HK * K, K
+    p.v, p.v_stride_t, p.v_stride_h = FAKE, HV * V, V
+    p.g, p.g_stride_t, p.g_stride_h = FAKE, HV, 1
+    p.beta, p.beta_stride_t, p.beta_stride_h = FAKE, HV, 1
+    p.cu_seqlens, p.cu_seqlens_bits = FAKE, 32
+    p.T, p.N, p.HK, p.HV, p.K, p.V = T, N, HK, HV, K, V
+    p.scale, p.use_qk_l2norm = 0.0, 1
+    p.o, p.o_stride_t, p.o_stride_h = FAKE, HV * V, V
+    for k, v in over.items():
+        setattr(p, k, v)
+    return p
+
+
+def _summary(**over):
+    p = B.GdnSummaryParams()
+    T, N, HK, HV, K, V = 256, 2, 2, 2, 64, 64
+    p.k, p.k_stride_t, p.k_stride_h = FAKE, HK * K, K
+    p.v, p.v_stride_t, p.v_stride_h = FAKE, HV * V, V
+    p.g, p.g_stride_t, p.g_stride_h = FAKE, HV, 1
+    p.beta, p.beta_stride_t, p.beta_stride_h = FAKE, HV, 1
+    p.cu_seqlens, p.cu_seqlens_bits = FAKE, 32
+    p.T, p.N, p.HK, p.HV, p.K, p.V = T, N, HK, HV, K, V
+    p.end_state, p.transition = FAKE, FAKE
+    for k, v in over.items():
+        setattr(p, k, v)
+    return p
+
+
+FWD_ERRORS = [
+    ("K not 64/128", dict(K=96), B.LA_ERR_UNSUPPORTED),
+    ("V not 64/128", dict(V=32), B.LA_ERR_UNSUPPORTED),
+    ("HV not a multiple of HK", dict(HK=3, HV=4), B.LA_ERR_UNSUPPORTED),
+    ("more q/k heads than value heads", dict(HK=4, HV=2), B.LA_ERR_UNSUPPORTED),
+    ("negative T", dict(T=-1), B.LA_ERR_INVALID_ARG),
+    ("negative N", dict(N=-1), B.LA_ERR_INVALID_ARG),
+    ("zero heads", dict(HK=0), B.LA_ERR_INVALID_ARG),
+    ("cu_seqlens bits", dict(cu_seqlens_bits=16), B.LA_ERR_INVALID_ARG),
+    ("null cu_seqlens", dict(cu_seqlens=None), B.LA_ERR_INVALID_ARG),
+    ("misaligned int64 cu_seqlens", dict(cu_seqlens=FAKE + 4, cu_seqlens_bits=64), B.LA_ERR_INVALID_ARG),
+    ("null q", dict(q=None), B.LA_ERR_INVALID_ARG),
+    ("null k", dict(k=None), B.LA_ERR_INVALID_ARG),
+    ("null v", dict(v=None), B.LA_ERR_INVALID_ARG),
+    ("null o", dict(o=None), B.LA_ERR_INVALID_ARG),
+    ("null g", dict(g=None), B.LA_ERR_INVALID_ARG),
+    ("null beta", dict(beta=None), B.LA_ERR_INVALID_ARG),
+    ("q base not 16-byte aligned", dict(q=FAKE + 8), B.LA_ERR_INVALID_ARG),
+    ("k token stride not a multiple of 8", dict(k_stride_t=132), B.LA_ERR_INVALID_ARG),
+    ("v head stride not a multiple of 8", dict(v_stride_h=65), B.LA_ERR_INVALID_ARG),
+    ("misaligned g", dict(g=FAKE + 2), B.LA_ERR_INVALID_ARG),
+    ("checkpoints without n", dict(checkpoints=FAKE, checkpoint_every_n=0), B.LA_ERR_INVALID_ARG),
+    ("checkpoint n not a multiple of 64", dict(checkpoints=FAKE, checkpoint_every_n=100), B.LA_ERR_INVALID_ARG),
+    ("checkpoint dtype", dict(checkpoints=FAKE, checkpoint_every_n=64, checkpoint_dtype=7), B.LA_ERR_UNSUPPORTED),
+    ("initial state dtype", dict(initial_state=FAKE, initial_state_dtype=3), B.LA_ERR_UNSUPPORTED),
+    ("misaligned fp32 initial state", dict(initial_state=FAKE + 2, initial_state_dtype=1), B.LA_ERR_INVALID_ARG),
+    ("misaligned final state", dict(final_state=FAKE + 1), B.LA_ERR_INVALID_ARG),
+    ("T beyond int32 TMA coordinates", dict(T=1 << 31), B.LA_ERR_UNSUPPORTED),
+]
+
+
+@pytest.mark.parametrize("name,over,code", FWD_ERRORS, ids=[e[0] for e in FWD_ERRORS])
+def test_gdn_fwd_rejects(name, over, code):
+    lib = B.load()
+    p = _fwd(**over)
+    assert lib.gdn_fwd(ctypes.byref(p), None) == code
+
+
+SUM_ERRORS = [
+    ("K not 64/128", dict(K=80), B.LA_ERR_UNSUPPORTED),
+    ("null end state", dict(end_state=None), B.LA_ERR_INVALID_ARG),
+    ("null transition", dict(transition=None), B.LA_ERR_INVALID_ARG),
+    ("transition not 16-byte aligned", dict(transition=FAKE + 4), B.LA_ERR_INVALID_ARG),
+    ("null k", dict(k=None), B.LA_ERR_INVALID_ARG),
+    ("start state dtype", dict(start_state=FAKE, start_state_dtype=9), B.LA_ERR_UNSUPPORTED),
+    ("HV not a multiple of HK", dict(HK=2, HV=3), B.LA_ERR_UNSUPPORTED),
+]
+
+
+@pytest.mark.parametrize("name,over,code", SUM_ERRORS, ids=[e[0] for e in SUM_ERRORS])
+def test_gdn_summary_rejects(name, over, code):
+    lib = B.load()
+    p = _summary(**over)
+    assert lib.gdn_summary(ctypes.byref(p), None) == code
+
+
+def test_null_params():
+    lib = B.load()
+    assert lib.gdn_fwd(None, None) == B.LA_ERR_INVALID_ARG
+    assert lib.gdn_summary(None, None) == B.LA_ERR_INVALID_ARG
+
+
+def test_checkpoint_rows_host_helper():
+    lib = B.load()
+    for bits, ctype in ((32, ctypes.c_int32), (64, ctypes.c_int64)):
+        cu = (ctype * 5)(0, 100, 100, 1124, 1125)
+        out = ctypes.c_int64(-1)
+        assert lib.la_checkpoint_rows(ctypes.addressof(cu), bits, 4, 64, ctypes.byref(out)) == B.LA_OK
+        assert out.value == 2 + 0 + 16 + 1
+        bad = (ctype * 3)(0, 5, 3)
+        assert lib.la_checkpoint_rows(ctypes.addressof(bad), bits, 2, 64, ctypes.byref(out)) == B.LA_ERR_INVALID_ARG
+    assert lib.la_checkpoint_rows(ctypes.addressof(cu), 64, 4, 0, ctypes.byref(out)) == B.LA_ERR_INVALID_ARG
+
+
+def test_status_strings_and_version():
+    lib = B.load()
+    for code in range(7):
+        assert lib.la_status_string(code)
+    assert lib.la_status_string(99) == b"unknown status"
+    assert lib.la_version() >= 100
+    assert lib.la_read_status(None, None, ctypes.byref(ctypes.c_int32())) == B.LA_ERR_INVALID_ARG
+
+
+def test_workspace_bytes_grows_with_batch():
+    lib = B.load()
+    small = lib.la_gdn_workspace_bytes(4, 0)
+    big = lib.la_gdn_workspace_bytes(100000, 0)
+    assert small >= 256 and small % 256 == 0
+    assert big > small and big % 256 == 0
+    assert big >= 256 + 4 * 100000 + 8 * 100000 + 8 * 131072

@@ -1,0 +1,298 @@
+"""CUDA path vs the fp64 oracle, element by element, through the C ABI.
+
+Tolerances (max|x - ref| / max|ref| over each output tensor):
+  o (bf16)                         1e-2
+  fp32 states, checkpoints, transitions   2e-3
+  bf16 checkpoints / bf16-start states     1e-2   (bf16 storage alone is 2^-9 relative)
+Full-size workloads are compared on sampled (sequence, head) units, in the same
+launch configuration as the benchmark (one call over the whole batch).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import gated_delta_rule_29_gb300 as la
+from gated_delta_rule_29_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+O_TOL = 1e-2
+S_TOL = 2e-3
+BF16_STATE_TOL = 1e-2
+
+
+def dev():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return torch.device("cuda:0")
+
+
+def rel(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    den = np.abs(ref).max()
+    assert den > 0, "reference is all zero: the comparison would be vacuous"
+    return float(np.abs(got - ref).max() / den)
+
+
+def to_dev(w, d):
+    return dict(q=w.q.to(d), k=w.k.to(d), v=w.v.to(d), g=w.g.to(d), beta=w.beta.to(d),
+                cu=w.cu_seqlens.to(d),
+                s0=None if w.initial_state is None else w.initial_state.to(d))
+
+
+def gpu_fwd(w, d=None, **kw):
+    d = d or dev()
+    t = to_dev(w, d)
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    args = dict(use_qk_l2norm=w.use_qk_l2norm, initial_state=t["s0"],
+                output_final_state=w.output_final_state, checkpoint_every_n=w.checkpoint_every_n,
+                checkpoint_dtype=w.checkpoint_dtype, status=status)
+    args.update(kw)
+    o, fin, ck = la.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu"], **args)
+    assert la.read_status(status) == 0
+    f = lambda x: None if x is None else x.float().cpu().numpy()
+    return f(o), f(fin), f(ck)
+
+
+def oracle_fwd(w, units=None):
+    mask = None
+    if units is not None:
+        mask = np.zeros((w.N, w.HV), dtype=bool)
+        for i, h in units:
+            mask[i, h] = True
+    return oracle.gdn_fwd(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, use_qk_l2norm=w.use_qk_l2norm,
+                          initial_state=w.initial_state, checkpoint_every_n=w.checkpoint_every_n,
+                          unit_mask=mask)
+
+
+def compare_units(w, got, ref, units, ck_tol=S_TOL):
+    o, fin, ck = got
+    cu = w.cu_seqlens.numpy().astype(np.int64)
+    go = np.concatenate([o[cu[i]:cu[i + 1], h] for i, h in units])
+    ro = np.concatenate([ref["o"][cu[i]:cu[i + 1], h] for i, h in units])
+    errs = {"o": rel(go, ro)}
+    if fin is not None:
+        errs["final"] = rel(np.stack([fin[i, h] for i, h in units]),
+                            np.stack([ref["final_state"][i, h] for i, h in units]))
+    if ck is not None:
+        off, _ = oracle.checkpoint_offsets(cu, w.checkpoint_every_n)
+        rows = [(off[i] + j, h) for i, h in units for j in range(-(-(cu[i + 1] - cu[i]) // w.checkpoint_every_n))]
+        errs["ckpt"] = rel(np.stack([ck[r_, h] for r_, h in rows]), np.stack([ref["checkpoints"][r_, h] for r_, h in rows]))
+    print(f"[parity] {w.name}: " + ", ".join(f"{k_} {v_:.2e}" for k_, v_ in errs.items()))
+    assert errs["o"] <= O_TOL, errs
+    assert errs.get("final", 0) <= S_TOL, errs
+    assert errs.get("ckpt", 0) <= ck_tol, errs
+    return errs
+
+
+def all_units(w):
+    return [(i, h) for i in range(w.N) for h in range(w.HV) if w.lengths()[i] > 0]
+
+
+# ------------------------------------------------------------------ the five workloads
+@pytest.mark.parametrize("slow", [False, True])
+def test_tiny_workload(slow):
+    w = W.config(1, slow_decay=slow)
+    got = gpu_fwd(w)
+    compare_units(w, got, oracle_fwd(w), all_units(w))
+
+
+@pytest.mark.parametrize("slow", [False, True])
+def test_varlen_workload(slow):
+    w = W.config(2, slow_decay=slow)
+    got = gpu_fwd(w)
+    compare_units(w, got, oracle_fwd(w), all_units(w))
+
+
+_C3 = {}
+
+
+def c3(slow):
+    if slow not in _C3:
+        _C3[slow] = W.config(3, slow_decay=slow)
+    return _C3[slow]
+
+
+@pytest.mark.parametrize("slow", [False, True])
+def test_dense_batch_full_size_sampled(slow):
+    """T = 65536, H = 32, K = V = 128, fp32 start state, final state and fp32 checkpoints every
+    1024 tokens: the benchmark's launch; the oracle recomputes sampled units."""
+    w = c3(slow)
+    got = gpu_fwd(w)
+    units = [(0, 0), (3, 17), (7, 31), (5, 8)]
+    compare_units(w, got, oracle_fwd(w, units), units)
+    assert np.isfinite(got[0]).all() and np.isfinite(got[1]).all()
+
+
+def test_skewed_gva_sampled_and_batch_invariant():
+    w = W.config(4)
+    got = gpu_fwd(w)
+    lens = w.lengths()
+    order = np.argsort(lens)
+    picks = [int(order[0]), int(order[len(order) // 2]), int(order[-1])]
+    units = [(i, h) for i in picks for h in (0, 1, 31)]
+    compare_units(w, got, oracle_fwd(w, units), units)
+    # bitwise batch invariance: each picked sequence alone and inside shuffled batches
+    cu = w.cu_seqlens.numpy().astype(np.int64)
+    rng = np.random.default_rng(7)
+    for trial in range(4):
+        if trial == 0:
+            seqs = [picks[0]]
+        elif trial == 1:
+            seqs = [picks[2]]
+        else:
+            seqs = list(rng.permutation(w.N)[: 20 + 10 * trial])
+            for p_ in picks:
+                if p_ not in seqs:
+                    seqs.insert(int(rng.integers(0, len(seqs) + 1)), p_)
+        idx = np.concatenate([np.arange(cu[i], cu[i + 1]) for i in seqs])
+        sub = W.Workload(name="sub", cu_seqlens=W._cu([lens[i] for i in seqs]), q=w.q[idx], k=w.k[idx],
+                         v=w.v[idx], g=w.g[idx].contiguous(), beta=w.beta[idx].contiguous())
+        o2, f2, _ = gpu_fwd(sub)
+        cu2 = sub.cu_seqlens.numpy().astype(np.int64)
+        for j, i in enumerate(seqs):
+            if i not in picks:
+                continue
+            assert np.array_equal(o2[cu2[j]:cu2[j + 1]], got[0][cu[i]:cu[i + 1]]), (trial, i)
+            assert np.array_equal(f2[j], got[1][i]), (trial, i)
+
+
+@pytest.mark.parametrize("slow", [False, True])
+def test_summary_span_composition(slow):
+    """One 131072-token sequence cut into 8 spans: composing the span summaries
+    (S <- transition^T S + S_H) reproduces the unsplit forward's final state."""
+    w = W.config(5, slow_decay=slow)
+    d = dev()
+    t = to_dev(w, d)
+    spans = w.spans.to(d)
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    end, tr = la.gdn_summary(t["k"], t["v"], t["g"], t["beta"], spans, use_qk_l2norm=True, status=status)
+    assert la.read_status(status) == 0
+    _, fin, _ = la.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu"], use_qk_l2norm=True)
+    end = end.double().cpu().numpy()
+    tr = tr.double().cpu().numpy()
+    S = np.zeros_like(end[0])
+    for j in range(end.shape[0]):
+        S = np.einsum("hab,hav->hbv", tr[j], S) + end[j]
+    fin = fin.double().cpu().numpy()[0]
+    errs = {"composed_vs_unsplit": rel(S, fin)}
+    assert errs["composed_vs_unsplit"] <= S_TOL
+    # the oracle on two sampled heads: span end states, transitions and the composed state
+    heads = [0, 11]
+    mask = np.zeros((8, w.HV), dtype=bool)
+    mask[:, heads] = True
+    ref = oracle.gdn_summary(w.k, w.v, w.g, w.beta, w.spans, unit_mask=mask)
+    errs["end_state"] = rel(end[:, heads], ref["end_state"][:, heads])
+    if slow:
+        errs["transition"] = rel(tr[:, heads], ref["transition"][:, heads])
+    refS = np.zeros_like(ref["end_state"][0])
+    for j in range(8):
+        refS = np.einsum("hab,hav->hbv", ref["transition"][j], refS) + ref["end_state"][j]
+    errs["composed_vs_oracle"] = rel(S[heads], refS[heads])
+    print(f"[parity] summary slow={slow}: " + ", ".join(f"{k_} {v_:.2e}" for k_, v_ in errs.items()))
+    assert max(errs.values()) <= S_TOL, errs
+
+
+# ------------------------------------------------------------------ edge cases
+def small(lengths, HK=2, HV=2, K=64, V=64, seed=5, **kw):
+    return W.draw("edge", lengths, HK, HV, K, V, seed=seed, **kw)
+
+
+@pytest.mark.parametrize("K,V", [(64, 128), (128, 64), (128, 128), (64, 64)])
+def test_head_dims(K, V):
+    w = small([1, 63, 64, 65, 200], K=K, V=V, seed=K + V, initial_state=True, checkpoint_every_n=64,
+              checkpoint_dtype=torch.float32, slow_decay=True)
+    compare_units(w, gpu_fwd(w), oracle_fwd(w), all_units(w))
+
+
+def test_empty_and_ragged_sequences():
+    w = small([0, 1, 64, 0, 129, 0], initial_state=True, checkpoint_every_n=64,
+              checkpoint_dtype=torch.float32, slow_decay=True)
+    got = gpu_fwd(w)
+    compare_units(w, got, oracle_fwd(w), all_units(w))
+    s0 = w.initial_state.numpy()
+    for i in (0, 3, 5):
+        assert np.array_equal(got[1][i], s0[i])  # empty sequence: final = initial state
+
+
+def test_bf16_checkpoints_and_bf16_initial_state():
+    w = small([300, 128, 70], initial_state=True, checkpoint_every_n=128, slow_decay=True)
+    w.initial_state = w.initial_state.to(torch.bfloat16).float()  # the oracle sees the rounded start
+    d = dev()
+    got = gpu_fwd(w, initial_state=w.initial_state.to(d).to(torch.bfloat16), checkpoint_dtype=torch.bfloat16)
+    compare_units(w, got, oracle_fwd(w), all_units(w), ck_tol=BF16_STATE_TOL)
+
+
+def test_grouped_heads_hk1():
+    w = small([130, 77], HK=1, HV=4, seed=9, slow_decay=True)
+    compare_units(w, gpu_fwd(w), oracle_fwd(w), all_units(w))
+
+
+def test_no_l2norm():
+    w = small([150, 90], seed=11)
+    w.q = (w.q.float() * 0.05).to(torch.bfloat16)
+    w.k = (w.k.float() * 0.05).to(torch.bfloat16)
+    w.use_qk_l2norm = False
+    compare_units(w, gpu_fwd(w), oracle_fwd(w), all_units(w))
+
+
+def test_strided_fused_projection_views():
+    """q, k, v as column slices of one fused [T, 2*HK*K + HV*V] projection (no copies)."""
+    w = small([100, 156], HK=2, HV=4, K=64, V=64, seed=13, slow_decay=True)
+    d = dev()
+    T = w.T
+    fused = torch.cat([w.q.reshape(T, -1), w.k.reshape(T, -1), w.v.reshape(T, -1)], dim=1).to(d)
+    a, b = w.HK * w.K, 2 * w.HK * w.K
+    q = fused[:, :a].view(T, w.HK, w.K)
+    k = fused[:, a:b].view(T, w.HK, w.K)
+    v = fused[:, b:].view(T, w.HV, w.V)
+    assert not q.is_contiguous()
+    o, fin, _ = la.gdn_fwd(q, k, v, w.g.to(d), w.beta.to(d), w.cu_seqlens.to(d))
+    compare_units(w, (o.float().cpu().numpy(), fin.cpu().numpy(), None), oracle_fwd(w), all_units(w))
+
+
+def test_int64_cu_seqlens_and_explicit_scale():
+    w = small([77, 200], seed=17, slow_decay=True)
+    d = dev()
+    t = to_dev(w, d)
+    o, fin, _ = la.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu"].long(), scale=0.3)
+    ref = oracle.gdn_fwd(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, scale=0.3)
+    assert rel(o.float().cpu().numpy(), ref["o"]) <= O_TOL
+    assert rel(fin.cpu().numpy(), ref["final_state"]) <= S_TOL
+
+
+def test_bad_cu_seqlens_sets_status():
+    w = small([100, 156], seed=19)
+    d = dev()
+    t = to_dev(w, d)
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    for bad in ([0, 300, 256], [1, 100, 256], [0, 100, 255]):
+        cu = torch.tensor(bad, dtype=torch.int32, device=d)
+        la.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], cu, status=status)
+        assert la.read_status(status) == la.binding.LA_ERR_BAD_SEQLENS
+    la.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu"], status=status)
+    assert la.read_status(status) == 0
+
+
+def test_many_sequences_global_sort_path():
+    """More than 8192 sequences: the prologue sorts in global memory."""
+    rng = np.random.default_rng(23)
+    lengths = [int(x) for x in rng.integers(0, 4, size=9000)] + [150]
+    w = small(lengths, HK=1, HV=1, K=64, V=64, seed=23)
+    got = gpu_fwd(w)
+    ref = oracle_fwd(w)
+    compare_units(w, got, ref, all_units(w))
+
+
+def test_summary_start_state_and_empty_spans():
+    w = small([0, 150, 0, 64], HK=1, HV=2, K=64, V=64, seed=29, initial_state=True, slow_decay=True)
+    d = dev()
+    t = to_dev(w, d)
+    end, tr = la.gdn_summary(t["k"], t["v"], t["g"], t["beta"], t["cu"], start_state=t["s0"])
+    ref = oracle.gdn_summary(w.k, w.v, w.g, w.beta, w.cu_seqlens, start_state=w.initial_state)
+    assert rel(end.cpu().numpy(), ref["end_state"]) <= S_TOL
+    assert rel(tr.cpu().numpy(), ref["transition"]) <= S_TOL
+    eye = np.eye(64)
+    for i in (0, 2):
+        assert np.array_equal(tr[i].cpu().numpy(), np.stack([eye, eye]).astype(np.float32))
