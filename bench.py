@@ -94,7 +94,7 @@ def profiled_traffic():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+    """nvidia-smi clocks and throttle reasons sampled every 50 ms during the timed region."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -108,7 +108,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
         except (OSError, FileNotFoundError):
@@ -200,9 +200,10 @@ def oracle_sample(w, units, nthreads):
 
 
 def cpu_units(w, count):
-    """A fixed spread of (sequence, head) units for the CPU sample: heads spread over the
-    first two sequences."""
-    return [(j % 2, (7 * j + 3) % w.HV) for j in range(count)]
+    """The first `count` (sequence, head) units of a fixed interleaved order over the batch
+    (all of them when count >= N * HO)."""
+    units = [(i, h) for h in range(w.HV) for i in range(w.N)]
+    return units[:min(count, len(units))]
 
 
 def run_reference(args, world, rank):
@@ -348,8 +349,8 @@ def run_ours(args, world, rank, local):
         units = cpu_units(w, args.cpu_units)
         dt, th = oracle_sample(w, units, cores)
         cpu = {"value": th / HO / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-               "sample": f"{len(units)} of 256 (sequence, head) units x 8192 tokens of the same workload "
-                         f"({dt:.1f} s), fp64 token-by-token C recurrence on {cores} threads"}
+               "sample": f"{len(units)} of {N * HO} (sequence, head) units x {w.lengths()[0]} tokens of the same "
+                         f"workload ({dt:.1f} s), fp64 token-by-token C recurrence on {cores} threads"}
 
     if rank == 0:
         line = {
@@ -377,10 +378,11 @@ def run_ours(args, world, rank, local):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-units", type=int, default=16, help="(sequence, head) units in the CPU-baseline sample")
+    ap.add_argument("--cpu-units", type=int, default=256,
+                    help="(sequence, head) units in the CPU-baseline sample (256 = the whole batch)")
     ap.add_argument("--ref-units", type=int, default=2, help="units per step of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
