@@ -32,6 +32,7 @@ EXPORTED_SYMBOLS = (
     "la_status_string",
     "la_version",
     "la_set_kernel_timing_events",
+    "gdn_fwd_static_workspace",
 )
 
 _i64 = ctypes.c_int64
@@ -115,6 +116,8 @@ def load(build_if_missing: bool = True):
         lib.la_version.argtypes = []
         lib.la_set_kernel_timing_events.restype = ctypes.c_int
         lib.la_set_kernel_timing_events.argtypes = [_vp, _vp]
+        lib.gdn_fwd_static_workspace.restype = ctypes.c_int
+        lib.gdn_fwd_static_workspace.argtypes = [ctypes.POINTER(GdnFwdParams), _vp]
         _lib = lib
         return lib
 

@@ -192,6 +192,40 @@ la_status run(const Common& c, ChunkArgs& ka, const void* q, int64_t q_st, int64
     return LA_OK;
 }
 
+// ---------------------------------------------------------------------------
+// Device-resident scratch for callers that cannot allocate device memory.
+//
+// Some callers are not allowed to call cudaMalloc at all: code running under
+// an allocator that owns every byte of device memory (a framework's caching
+// pool, a serving process that reserved all memory up front), or code that must
+// not allocate after start-up.  gdn_fwd_static_workspace serves them with this
+// file-scope array instead of a caller workspace or the library's lazily
+// allocated one.  It lives in every GPU that loads the library until the
+// process exits.  Its size covers the prologue's tables for up to
+// kStaticMaxSeqs sequences (the unit order and the checkpoint row offsets).
+// ---------------------------------------------------------------------------
+constexpr int32_t kStaticMaxSeqs = 8192;
+constexpr size_t kStaticScratchBytes = 98560;  // == la::ws_layout(kStaticMaxSeqs).total
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+std::mutex g_static_mutex;
+void* g_static_scratch_addr[128] = {};
+
+// The host-side name g_static_scratch is only a stand-in, so the array's device
+// address is looked up once per device, with that device current.
+la_status static_scratch_address(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return LA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_static_mutex);
+    if (!g_static_scratch_addr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) return LA_ERR_CUDA;
+        g_static_scratch_addr[dev] = ptr;
+    }
+    *out = g_static_scratch_addr[dev];
+    return LA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -272,6 +306,20 @@ la_status gdn_summary(const la_gdn_summary_params* p, void* stream) {
     ka.tiles_per_head = 2;
     return run(c, ka, nullptr, 0, 0, p->k, p->k_stride_t, p->k_stride_h, p->v, p->v_stride_t, p->v_stride_h, 0,
                p->workspace, p->workspace_bytes, p->status, la::kModeSummary, static_cast<cudaStream_t>(stream));
+}
+
+la_status gdn_fwd_static_workspace(const la_gdn_fwd_params* p, void* stream) {
+    if (!p) return LA_ERR_INVALID_ARG;
+    if (p->workspace) return LA_ERR_INVALID_ARG;  // the scratch is the library's own array
+    if (p->N < 0) return LA_ERR_INVALID_ARG;
+    if (p->N > kStaticMaxSeqs || la::ws_layout(p->N).total > kStaticScratchBytes) return LA_ERR_WORKSPACE;
+    void* scratch = nullptr;
+    la_status st = static_scratch_address(&scratch);
+    if (st != LA_OK) return st;
+    la_gdn_fwd_params q = *p;
+    q.workspace = scratch;
+    q.workspace_bytes = kStaticScratchBytes;
+    return gdn_fwd(&q, stream);
 }
 
 size_t la_gdn_workspace_bytes(int32_t N, int32_t summary) {

@@ -108,6 +108,29 @@ typedef struct la_gdn_fwd_params {
  */
 la_status gdn_fwd(const la_gdn_fwd_params* p, void* stream);
 
+/*
+ * gdn_fwd_static_workspace -- gdn_fwd for callers that cannot allocate device memory.
+ *
+ * The pages have no counterpart to this entry point; it exists for callers
+ * that are not allowed to call cudaMalloc (a process whose allocator owns all
+ * device memory, or one that must not allocate once it is serving).  It runs
+ * exactly the gdn_fwd computation with the same parameters, but takes its
+ * scratch from a fixed array compiled into the library (about 96 KB per GPU,
+ * held from library load to process exit) instead of a workspace:
+ *   - p->workspace must be NULL (LA_ERR_INVALID_ARG otherwise);
+ *   - N may be at most 8192 sequences; larger batches return LA_ERR_WORKSPACE
+ *     and launch nothing;
+ *   - no call allocates or frees device memory.  The first call on a device
+ *     looks up the array's device address (once, with that device current);
+ *     make that first call before any stream capture.
+ *   - every call on a device shares the one array.  Each call re-initialises
+ *     what must start at zero (status word, unit ticket) in its own prologue
+ *     kernel, so leftovers from an earlier call are harmless, but calls whose
+ *     kernels overlap on the GPU (different streams, no ordering between them)
+ *     race on the array and give undefined results.
+ */
+la_status gdn_fwd_static_workspace(const la_gdn_fwd_params* p, void* stream);
+
 /* Parameters of gdn_summary.  Strides are in elements. */
 typedef struct la_gdn_summary_params {
     const void* k;    int64_t k_stride_t, k_stride_h;       /* [T, HK, K] bf16 */

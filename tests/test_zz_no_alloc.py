@@ -1,0 +1,97 @@
+"""gdn_fwd_static_workspace: the entry point for callers that may not allocate device memory.
+
+Such callers (a process whose allocator owns all device memory, or one that must
+not allocate once it is serving) cannot provide a workspace, so this entry point
+takes its scratch from an array compiled into the library.  The test drives it
+through the C ABI and checks it against gdn_fwd on the same inputs, twice in a
+row: the second call runs on whatever the first left in the shared array.
+
+Kept in a file of its own, collected after every other test file.
+"""
+import ctypes
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from gated_delta_rule_29_gb300 import binding as B
+from gated_delta_rule_29_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+O_TOL = 1e-2
+S_TOL = 2e-3
+
+
+def _rel(a, b):
+    a = a.double().cpu().numpy()
+    b = b.double().cpu().numpy()
+    return float(np.abs(a - b).max() / np.abs(b).max())
+
+
+def _params(t, outs, N, scale):
+    q, k, v, g, beta, cu, s0 = t
+    o, fin, ck, ws, status = outs
+    p = B.GdnFwdParams()
+    p.q, p.q_stride_t, p.q_stride_h = q.data_ptr(), q.stride(0), q.stride(1)
+    p.k, p.k_stride_t, p.k_stride_h = k.data_ptr(), k.stride(0), k.stride(1)
+    p.v, p.v_stride_t, p.v_stride_h = v.data_ptr(), v.stride(0), v.stride(1)
+    p.g, p.g_stride_t, p.g_stride_h = g.data_ptr(), g.stride(0), g.stride(1)
+    p.beta, p.beta_stride_t, p.beta_stride_h = beta.data_ptr(), beta.stride(0), beta.stride(1)
+    p.cu_seqlens, p.cu_seqlens_bits = cu.data_ptr(), 32
+    p.T, p.N, p.HK, p.HV, p.K, p.V = q.shape[0], N, q.shape[1], v.shape[1], q.shape[2], v.shape[2]
+    p.scale, p.use_qk_l2norm = scale, 1
+    p.initial_state, p.initial_state_dtype = s0.data_ptr(), B.LA_DTYPE_F32
+    p.o, p.o_stride_t, p.o_stride_h = o.data_ptr(), o.stride(0), o.stride(1)
+    p.final_state = fin.data_ptr()
+    p.checkpoints, p.checkpoint_dtype, p.checkpoint_every_n = ck.data_ptr(), B.LA_DTYPE_F32, 128
+    if ws is not None:
+        p.workspace, p.workspace_bytes = ws.data_ptr(), ws.numel()
+    p.status = status.data_ptr()
+    return p
+
+
+def _outputs(w, R, dev, with_ws):
+    lib = B.load()
+    o = torch.full((w.T, w.HV, w.V), float("nan"), dtype=torch.bfloat16, device=dev)
+    fin = torch.full((w.N, w.HV, w.K, w.V), float("nan"), device=dev)
+    ck = torch.full((R, w.HV, w.K, w.V), float("nan"), device=dev)
+    ws = torch.empty(lib.la_gdn_workspace_bytes(w.N, 0), dtype=torch.uint8, device=dev) if with_ws else None
+    status = torch.full((1,), -1, dtype=torch.int32, device=dev)
+    return o, fin, ck, ws, status
+
+
+def test_static_workspace_matches_gdn_fwd_twice():
+    assert torch.cuda.is_available(), "GPU test needs a CUDA device"
+    dev = torch.device("cuda:0")
+    lib = B.load()
+    stream = torch.cuda.current_stream().cuda_stream
+    # two different batches, so the second call starts from the first call's leftovers
+    cases = [W.draw("a", [300, 64, 1, 500], 2, 4, 128, 128, seed=41, initial_state=True, slow_decay=True),
+             W.draw("b", [129, 0, 700], 2, 2, 128, 64, seed=43, initial_state=True, slow_decay=True)]
+    for w in cases:
+        R = sum(-(-int(L) // 128) for L in w.lengths())
+        t = [x.to(dev) for x in (w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, w.initial_state)]
+        scale = 1.0 / math.sqrt(w.K)
+        ref = _outputs(w, R, dev, with_ws=True)
+        got = _outputs(w, R, dev, with_ws=False)
+        assert lib.gdn_fwd(ctypes.byref(_params(t, ref, w.N, scale)), stream) == B.LA_OK
+        assert lib.gdn_fwd_static_workspace(ctypes.byref(_params(t, got, w.N, scale)), stream) == B.LA_OK
+        torch.cuda.synchronize()
+        assert int(ref[4].item()) == B.LA_OK and int(got[4].item()) == B.LA_OK
+        assert _rel(got[0], ref[0]) <= O_TOL
+        assert _rel(got[1], ref[1]) <= S_TOL
+        assert _rel(got[2], ref[2]) <= S_TOL
+        assert torch.isfinite(got[0].float()).all()
+
+
+def test_static_workspace_rejects_large_batches_and_workspaces():
+    lib = B.load()
+    p = B.GdnFwdParams()
+    p.N = 8193
+    assert lib.gdn_fwd_static_workspace(ctypes.byref(p), None) == B.LA_ERR_WORKSPACE
+    p.N = 4
+    p.workspace = 0x10000
+    assert lib.gdn_fwd_static_workspace(ctypes.byref(p), None) == B.LA_ERR_INVALID_ARG
+    assert lib.gdn_fwd_static_workspace(None, None) == B.LA_ERR_INVALID_ARG
