@@ -6,7 +6,7 @@
 // rk/rq the per-row inverse L2 norms and S0 the state entering the chunk:
 //
 //   A  = strict_tril( beta_i rk_i rk_j (k_i . k_j) 2^{b_i - b_j} )        (64 x 64)
-//   T  = (I + A)^{-1}                                   forward substitution, fp32
+//   T  = (I + A)^{-1}                                      block substitution, fp32/tf32
 //   X  = beta (.) V - (beta gamma rk) (.) (K S0)                          (64 x V)
 //   D  = T X                                                   (the delta rows)
 //   O  = (scale rq gamma) (.) (Q S0) + P D,
@@ -15,20 +15,21 @@
 //
 // which equals the token-by-token recurrence exactly (up to rounding order).
 //
-// Mapping.  One CTA (256 threads) per SM walks a ticket-ordered list of units
-// (sequence, head, tile).  Every product runs on the 5th-generation tensor cores
-// (tcgen05.mma kind::f16, bf16 operands, fp32 accumulators in TMEM, M = 128) in
-// transposed form so that M is the value dimension (padded to 128) or the
-// stacked [K; Q] token rows.  q/k/v tiles arrive by TMA (128-byte swizzle,
-// double buffered).  The state S stays in fp32 registers: thread (r, hf) holds
-// column v = r of S for half hf of the k rows.  X and the decayed delta rows
-// are split into bf16 hi + lo parts so the state update keeps ~16 bits.
+// Mapping.  Persistent CTAs of 128 threads (two per SM) take units (sequence, head,
+// tile) from a ticket.  Thread r owns TMEM lane r.  The state S lives in TMEM as
+// fp32 S^T (lane = value column, column = k) and is updated in place by the
+// tensor core.  Every product is a tcgen05.mma (kind::f16, bf16 operands, fp32
+// accumulation, M = 128) in transposed form: M is the value dimension (padded to
+// 128) or the stacked [K; Q] token rows.  q/k/v tiles arrive by TMA (128-byte
+// swizzle).  X and the decayed delta rows are split into bf16 hi + lo parts so
+// the state keeps ~16 bits per update; summaries also split the state operand of
+// K S (the transition's small entries need it).  The 64 x 64 unit-lower-
+// triangular inverse runs on the CUDA cores: 16 x 16 diagonal blocks by
+// substitution, the off-diagonal blocks by tf32 warp MMAs.
 //
 // Tiles: a forward unit has one value tile.  A summary unit has a value tile
 // (the span end state from the given start) and a transition tile: the same
-// recurrence on P with v = 0 and P0 = I, stored transposed.  Summaries also
-// split the state operand of K S into bf16 hi + lo: the transition's small
-// off-diagonal entries need it to stay within the fp32-state tolerance.
+// recurrence on P with v = 0 and P0 = I, stored transposed.
 #include <cuda_bf16.h>
 
 #include "../../include/liblinattn.h"
@@ -37,31 +38,28 @@
 
 namespace la {
 
+constexpr int kCta = 128;  // threads per CTA
+
 // ------------------------------------------------------------------ shared memory map
-constexpr uint32_t SM_KQ0 = 0;         // [region 0..1][128 rows: K 0-63, Q 64-127][128 B]
-constexpr uint32_t SM_KQ1 = 32768;
-constexpr uint32_t SM_V0 = 65536;      // [region 0..1][64 rows][128 B]
-constexpr uint32_t SM_V1 = 81920;
-constexpr uint32_t SM_WB = 98304;      // S^T bf16 [2][128][128 B] | X^T hi,lo | Ddec^T hi,lo
-constexpr uint32_t SM_DT = 131072;     // A fp32 [64][64] during the solve | D^T bf16 [128][128 B]
-constexpr uint32_t SM_TF = 147456;     // T fp32 [64][64]
-constexpr uint32_t SM_PB = 163840;     // P bf16 [64][128 B]
-constexpr uint32_t SM_TB = 172032;     // T bf16 [64][128 B]
-constexpr uint32_t SM_SCAL = 180224;   // Scalars
-constexpr uint32_t SM_SLO = 188416;    // summary only: S^T bf16 residual (lo part), same layout as WB
+constexpr uint32_t SM_KQ = 0;        // [region 0..1][128 rows: K 0-63, Q 64-127][128 B]
+constexpr uint32_t SM_V = 32768;     // V tile [region 0..1][64 rows][128 B] | later T bf16 [64][128 B]
+constexpr uint32_t SM_WB = 49152;    // S^T bf16 [2][128][128 B] | X^T hi,lo | Ddec^T hi,lo
+constexpr uint32_t SM_M = 81920;     // A (lower) + T (upper, transposed) fp32 [64][64] | D^T bf16
+constexpr uint32_t SM_PB = 98304;    // P bf16 [64][128 B]
+constexpr uint32_t SM_SC = 106496;   // Scalars (7 KB)
+constexpr uint32_t SM_SLO = 114688;  // summary only: S^T bf16 residual (lo part), same layout as WB
 __host__ __device__ constexpr uint32_t smem_alloc(int mode) {
-    return (mode == kModeSummary ? SM_SLO + 32768 : SM_SCAL + 8192) + 1024;
+    return (mode == kModeSummary ? SM_SLO + 32768 : SM_SC + 7168) + 1024;
 }
 
-// TMEM columns (fp32 accumulators, 128 lanes)
-constexpr uint32_t COL_G = 0;     // [K;Q] K^T            (64 columns)
-constexpr uint32_t COL_D = 0;     // D^T                   (64)
-constexpr uint32_t COL_SU = 0;    // K^T Ddec, transposed  (128)
-constexpr uint32_t COL_KS = 128;  // (K S)^T               (64)
-constexpr uint32_t COL_QS = 192;  // (Q' S)^T, then += D^T P^T = O^T
+// TMEM columns (fp32, 128 lanes)
+constexpr uint32_t COL_S = 0;     // S^T (K columns)
+constexpr uint32_t COL_R1 = 128;  // G -> (K S)^T -> D^T      (64 columns)
+constexpr uint32_t COL_R2 = 192;  // (Q' S)^T, then += D^T P^T = O^T
 constexpr uint32_t TMEM_COLS = 256;
 
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kFastRange = 100.f;  // factorised decays when |b_i - b_31| <= this (log2 units)
 
 struct Scalars {
     float b[64];    // chunk-local inclusive cumsum of g * log2(e)
@@ -72,16 +70,23 @@ struct Scalars {
     float sx[64];   // beta_j 2^{b_j} rk_j
     float sq[64];   // scale rq_i 2^{b_i}
     float sd[64];   // 2^{b_C - b_j} rk_j
-    float red[256]; // norm partial sums
-    float Y[768];   // solve scratch
-    uint64_t tma_bar[2];
-    uint64_t mma_bar;
+    float u[64];    // rk_j 2^{b_31 - b_j}           (factorised decay, column factor)
+    float cA[64];   // beta_i rk_i 2^{b_i - b_31}    (row factor of A)
+    float cP[64];   // scale rq_i 2^{b_i - b_31}     (row factor of P)
+    float Y[4][256];  // per-warp 16 x 16 solve scratch
+    uint64_t bar_kq, bar_v, bar_mma;
     uint32_t tmem_base;
     int32_t unit_lo, unit_hi;
 };
-static_assert(sizeof(Scalars) <= 8192, "scalar area");
+static_assert(sizeof(Scalars) <= 7168, "scalar area");
 
-__device__ __forceinline__ int aidx(int i, int j) { return i * 64 + (j ^ (i & 31)); }
+// Packed A/T buffer: A[i][j] (i > j) at (i, j); T[i][j] (i > j) at (j, i); T[i][i] = 1.
+// 16-byte chunks are XOR-swizzled by row to spread rows over the banks.
+__device__ __forceinline__ int midx(int r, int c) { return r * 64 + ((((c >> 2) ^ (r & 15)) << 2) | (c & 3)); }
+__device__ __forceinline__ float a_at(const float* M, int i, int j) { return i > j ? M[midx(i, j)] : 0.f; }
+__device__ __forceinline__ float t_at(const float* M, int i, int j) {
+    return i == j ? 1.f : (i > j ? M[midx(j, i)] : 0.f);
+}
 
 __device__ __forceinline__ uint32_t pack_bf16(float x0, float x1) {
     __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
@@ -111,80 +116,98 @@ __device__ __forceinline__ void store8_split(uint8_t* hi, uint8_t* lo, const flo
     if (lo) *reinterpret_cast<uint4*>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
-// T = (I + A)^{-1} for strictly lower-triangular A (fp32, 64 x 64): 16 x 16 diagonal
-// blocks by substitution, off-diagonal blocks by block forward substitution
-//   T[bi][bj] = -T[bi][bi] * sum_{m=bj}^{bi-1} A[bi][m] T[m][bj].
-// Writes T as bf16 (K-major, 128-byte swizzle) into tb.  All 256 threads.
-__device__ void solve_unit_lower(const float* A, float* TF, float* Y, uint8_t* tb, int tid) {
-    if (tid < 64) {
-        const int o = 16 * (tid >> 4), c = tid & 15;
+// T = (I + A)^{-1} for the strictly lower-triangular A held in the packed buffer M;
+// T is written into M's upper half (transposed).  128 threads.
+//   diagonal 16 x 16 blocks: substitution, one warp per block, lane = column;
+//   T[bi][bj] = -T[bi][bi] * sum_{m = bj}^{bi - 1} A[bi][m] T[m][bj], block distance
+//   d = bi - bj = 1, 2, 3 in turn, one warp per block, on tf32 warp MMAs.
+__device__ void solve_unit_lower(float* M, float (*Ys)[256], int tid) {
+    const int warp = tid >> 5, lane = tid & 31;
+    if (lane < 16) {
+        const int o = 16 * warp, c = lane;
         float t[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             float acc = (i == c) ? 1.f : 0.f;
 #pragma unroll
-            for (int j = 0; j < i; ++j) acc = fmaf(-A[aidx(o + i, o + j)], t[j], acc);
+            for (int j = 0; j < i; ++j) acc = fmaf(-M[midx(o + i, o + j)], t[j], acc);
             t[i] = acc;
         }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) TF[aidx(o + i, o + c)] = t[i];
+        for (int i = 1; i < 16; ++i)
+            if (i > c) M[midx(o + c, o + i)] = t[i];
     }
     __syncthreads();
+    const int g = lane >> 2, q = lane & 3;
+    float* Y = Ys[warp];
     for (int d = 1; d < 4; ++d) {
-        const int ne = (4 - d) * 256;
-        for (int e = tid; e < ne; e += kThreads) {
-            const int p = e >> 8, i = (e >> 4) & 15, j = e & 15;
-            const int rowA = 16 * (p + d) + i, colT = 16 * p + j;
-            float acc = 0.f;
-            for (int m = 16 * p; m < 16 * (p + d); ++m) acc = fmaf(A[aidx(rowA, m)], TF[aidx(m, colT)], acc);
-            Y[e] = acc;
-        }
-        __syncthreads();
-        for (int e = tid; e < ne; e += kThreads) {
-            const int p = e >> 8, i = (e >> 4) & 15, j = e & 15;
-            const int bi = 16 * (p + d);
-            float acc = 0.f;
-            for (int m = 0; m <= i; ++m) acc = fmaf(TF[aidx(bi + i, bi + m)], Y[(p << 8) + (m << 4) + j], acc);
-            TF[aidx(bi + i, 16 * p + j)] = -acc;
-        }
-        __syncthreads();
-    }
-    {
-        const int i = tid >> 2;
+        if (warp <= 3 - d) {
+            const int r0 = 16 * (warp + d), c0 = 16 * warp;
+            float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            for (int m0 = c0; m0 < r0; m0 += 8) {
+                const uint32_t a[4] = {to_tf32(a_at(M, r0 + g, m0 + q)), to_tf32(a_at(M, r0 + g + 8, m0 + q)),
+                                       to_tf32(a_at(M, r0 + g, m0 + q + 4)), to_tf32(a_at(M, r0 + g + 8, m0 + q + 4))};
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-            const int jc = (tid & 3) * 2 + cc;
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int j = jc * 8 + e;
-                x[e] = (j <= i) ? TF[aidx(i, j)] : 0.f;
+                for (int nt = 0; nt < 2; ++nt) {
+                    const uint32_t b[2] = {to_tf32(t_at(M, m0 + q, c0 + 8 * nt + g)),
+                                           to_tf32(t_at(M, m0 + q + 4, c0 + 8 * nt + g))};
+                    mma_tf32_16x8x8(y[nt], a, b);
+                }
             }
-            store8_split(tb + sw128_off(i, jc), nullptr, x);
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                Y[g * 16 + 8 * nt + 2 * q] = y[nt][0];
+                Y[g * 16 + 8 * nt + 2 * q + 1] = y[nt][1];
+                Y[(g + 8) * 16 + 8 * nt + 2 * q] = y[nt][2];
+                Y[(g + 8) * 16 + 8 * nt + 2 * q + 1] = y[nt][3];
+            }
+            __syncwarp();
+            float o[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+            for (int k0 = 0; k0 < 16; k0 += 8) {
+                const uint32_t a[4] = {to_tf32(t_at(M, r0 + g, r0 + k0 + q)), to_tf32(t_at(M, r0 + g + 8, r0 + k0 + q)),
+                                       to_tf32(t_at(M, r0 + g, r0 + k0 + q + 4)),
+                                       to_tf32(t_at(M, r0 + g + 8, r0 + k0 + q + 4))};
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const uint32_t b[2] = {to_tf32(Y[(k0 + q) * 16 + 8 * nt + g]),
+                                           to_tf32(Y[(k0 + q + 4) * 16 + 8 * nt + g])};
+                    mma_tf32_16x8x8(o[nt], a, b);
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int cc = c0 + 8 * nt + 2 * q;
+                M[midx(cc, r0 + g)] = -o[nt][0];
+                M[midx(cc + 1, r0 + g)] = -o[nt][1];
+                M[midx(cc, r0 + g + 8)] = -o[nt][2];
+                M[midx(cc + 1, r0 + g + 8)] = -o[nt][3];
+            }
+            __syncwarp();
         }
+        __syncthreads();
     }
 }
 
 template <int KD, int MODE>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kCta, 2)
     gdn_chunk_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap, const ChunkArgs a) {
-    constexpr int KH = KD / 2;  // state rows held per thread
     constexpr bool kFwd = MODE == kModeFwd;
+    constexpr int KP = KD / 16;  // 16-column pieces of the state
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Scalars& sc = *reinterpret_cast<Scalars*>(sm + SM_SCAL);
-    float* Asm = reinterpret_cast<float*>(sm + SM_DT);
-    float* TF = reinterpret_cast<float*>(sm + SM_TF);
+    Scalars& sc = *reinterpret_cast<Scalars*>(sm + SM_SC);
+    uint8_t* KQ = sm + SM_KQ;
+    uint8_t* VT = sm + SM_V;
     uint8_t* WB = sm + SM_WB;
-    uint8_t* DT = sm + SM_DT;
+    float* M = reinterpret_cast<float*>(sm + SM_M);
+    uint8_t* DT = sm + SM_M;
     uint8_t* PB = sm + SM_PB;
-    uint8_t* TB = sm + SM_TB;
     uint8_t* SLO = kFwd ? nullptr : sm + SM_SLO;
 
     const int tid = threadIdx.x;
-    const int r = tid & 127;   // TMEM lane / value column / stacked token row
-    const int hf = tid >> 7;   // column half
+    const int r = tid;  // TMEM lane, value column, stacked token row
     const int HO = a.HV;
 
     if (*reinterpret_cast<volatile int32_t*>(&a.hdr->status) != LA_OK) return;
@@ -194,9 +217,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     if (tid == 0) {
-        mbar_init(&sc.tma_bar[0], 1);
-        mbar_init(&sc.tma_bar[1], 1);
-        mbar_init(&sc.mma_bar, 1);
+        mbar_init(&sc.bar_kq, 1);
+        mbar_init(&sc.bar_v, 1);
+        mbar_init(&sc.bar_mma, 1);
         fence_mbar_init();
     }
     tc_fence_before();
@@ -205,12 +228,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = sc.tmem_base;
     const uint32_t trow = tmem + (static_cast<uint32_t>(r & ~31) << 16);
 
-    uint32_t tma_phase = 0, mma_phase = 0;  // parity of the next wait per barrier
-    uint32_t tma_pending = 0;               // stages with an issued, unconsumed load
-    bool mma_pending = false;
+    uint32_t ph_kq = 0, ph_v = 0, ph_mma = 0;  // parity of the next wait on each barrier
+    bool pend_kq = false, pend_v = false, pend_mma = false;
     bool failed = false;
     const uint64_t budget = a.wait_budget_ns;
     const int64_t per_seq = static_cast<int64_t>(HO) * a.tiles_per_head;
+    const uint32_t kq_bytes = (kFwd ? 2u : 1u) * KD * 128u;
+    const uint32_t v_bytes = static_cast<uint32_t>(a.V) * 128u;
 
     for (;;) {
         if (tid == 0) {
@@ -231,49 +255,71 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int64_t ts = cu_get(a.cu, a.cu64, seq);
         const int64_t L = cu_get(a.cu, a.cu64, seq + 1) - ts;
         const int nchunks = static_cast<int>((L + kChunk - 1) / kChunk);
-        const int64_t unit_state = (static_cast<int64_t>(seq) * HO + h);
-        const uint32_t tile_bytes = (kFwd ? 2u : 1u) * KD * 128u + (value_tile ? static_cast<uint32_t>(a.V) * 128u : 0u);
+        const int64_t unit_state = static_cast<int64_t>(seq) * HO + h;
 
-        // ---- initial state: thread (r, hf) holds S[k][r], k = hf*KH + i
-        float st[KH];
+        // ---- initial state -> TMEM (fp32 S^T) and WB (bf16 S^T, the A operand of K S)
+        {
+            const int64_t base = unit_state * KD * a.V + r;
+#pragma unroll 1
+            for (int p = 0; p < KP; ++p) {
+                float x[16];
 #pragma unroll
-        for (int i = 0; i < KH; ++i) st[i] = 0.f;
-        if (value_tile) {
-            if (a.s0 && r < a.V) {
-                const int64_t base = unit_state * KD * a.V + r;
+                for (int e = 0; e < 16; ++e) {
+                    const int k = 16 * p + e;
+                    float val = 0.f;
+                    if (value_tile) {
+                        if (a.s0 && r < a.V) {
+                            const int64_t idx = base + static_cast<int64_t>(k) * a.V;
+                            val = a.s0_bf16 ? bf16_bits_to_f(static_cast<const uint16_t*>(a.s0)[idx])
+                                            : static_cast<const float*>(a.s0)[idx];
+                        }
+                    } else {
+                        val = (k == r) ? 1.f : 0.f;
+                    }
+                    x[e] = val;
+                }
+                tmem_st16(trow + COL_S + 16 * p, x);
 #pragma unroll
-                for (int i = 0; i < KH; ++i) {
-                    const int64_t idx = base + static_cast<int64_t>(hf * KH + i) * a.V;
-                    st[i] = a.s0_bf16 ? bf16_bits_to_f(static_cast<const uint16_t*>(a.s0)[idx])
-                                      : static_cast<const float*>(a.s0)[idx];
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int kc = 2 * p + hh;  // 16-byte chunk index along k
+                    const uint32_t off = (kc >> 3) * 16384 + sw128_off(r, kc & 7);
+                    store8_split(WB + off, kFwd ? nullptr : SLO + off, &x[8 * hh]);
+                }
+                if (nchunks == 0) {  // empty sequence: the start state is the end state
+                    if (value_tile) {
+                        if (a.final_state && r < a.V)
+#pragma unroll
+                            for (int e = 0; e < 16; ++e)
+                                a.final_state[base + static_cast<int64_t>(16 * p + e) * a.V] = x[e];
+                    } else if (r < KD) {
+                        float* tp = a.transition + (unit_state * KD + r) * KD + 16 * p;
+#pragma unroll
+                        for (int e = 0; e < 16; e += 4)
+                            *reinterpret_cast<float4*>(tp + e) = make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
+                    }
                 }
             }
-        } else {
-#pragma unroll
-            for (int i = 0; i < KH; ++i) st[i] = (hf * KH + i == r) ? 1.f : 0.f;
-        }
-        // S^T bf16 -> WB (A operand of the K S / Q S products)
-#pragma unroll
-        for (int c8 = 0; c8 < KH / 8; ++c8) {
-            const int kc = (hf * KH) / 8 + c8;  // 16-byte chunk index along k
-            const uint32_t off = (kc >> 3) * 16384 + sw128_off(r, kc & 7);
-            store8_split(WB + off, kFwd ? nullptr : SLO + off, &st[c8 * 8]);
+            tmem_wait_st();
         }
 
         // ---- first chunk's tiles and per-token scalars
-        if (tid == 0 && nchunks > 0) {
-            uint8_t* KQ = sm + SM_KQ0;
-            mbar_arrive_expect_tx(&sc.tma_bar[0], tile_bytes);
+        if (nchunks > 0) {
+            if (tid == 0) {
+                mbar_arrive_expect_tx(&sc.bar_kq, kq_bytes);
 #pragma unroll
-            for (int rg = 0; rg < KD / 64; ++rg) {
-                tma_load_3d(KQ + rg * 16384, &kmap, &sc.tma_bar[0], rg * 64, hk, static_cast<int>(ts));
-                if (kFwd) tma_load_3d(KQ + rg * 16384 + 8192, &qmap, &sc.tma_bar[0], rg * 64, hk, static_cast<int>(ts));
+                for (int rg = 0; rg < KD / 64; ++rg) {
+                    tma_load_3d(KQ + rg * 16384, &kmap, &sc.bar_kq, rg * 64, hk, static_cast<int>(ts));
+                    if (kFwd) tma_load_3d(KQ + rg * 16384 + 8192, &qmap, &sc.bar_kq, rg * 64, hk, static_cast<int>(ts));
+                }
+                if (value_tile) {
+                    mbar_arrive_expect_tx(&sc.bar_v, v_bytes);
+                    for (int rg = 0; rg < a.V / 64; ++rg)
+                        tma_load_3d(VT + rg * 8192, &vmap, &sc.bar_v, rg * 64, h, static_cast<int>(ts));
+                }
             }
-            if (value_tile)
-                for (int rg = 0; rg < (a.V + 63) / 64; ++rg)
-                    tma_load_3d(sm + SM_V0 + rg * 8192, &vmap, &sc.tma_bar[0], rg * 64, h, static_cast<int>(ts));
+            pend_kq = true;
+            pend_v = value_tile;
         }
-        if (nchunks > 0) tma_pending |= 1u;
         float g_nx = 0.f, b_nx = 0.f;
         if (tid < 64 && tid < L) {
             g_nx = a.g[(ts + tid) * a.g_st + h * a.g_sh];
@@ -284,50 +330,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t t0 = ts + static_cast<int64_t>(c) * kChunk;
             const int64_t left = L - static_cast<int64_t>(c) * kChunk;
             const int n = left < kChunk ? static_cast<int>(left) : kChunk;
-            const int s = c & 1;
-            uint8_t* KQ = sm + (s ? SM_KQ1 : SM_KQ0);
-            uint8_t* VT = sm + (s ? SM_V1 : SM_V0);
+            const bool last = c + 1 == nchunks;
             const float g_cur = g_nx, b_cur = b_nx;
-
-            // prefetch chunk c+1 (tiles by TMA, scalars into registers)
-            if (c + 1 < nchunks) {
-                const int64_t t1 = t0 + kChunk;
-                if (tid == 0) {
-                    uint8_t* KQn = sm + (s ? SM_KQ0 : SM_KQ1);
-                    uint8_t* VTn = sm + (s ? SM_V0 : SM_V1);
-                    uint64_t* bar = &sc.tma_bar[s ^ 1];
-                    fence_proxy_async_smem();
-                    mbar_arrive_expect_tx(bar, tile_bytes);
-#pragma unroll
-                    for (int rg = 0; rg < KD / 64; ++rg) {
-                        tma_load_3d(KQn + rg * 16384, &kmap, bar, rg * 64, hk, static_cast<int>(t1));
-                        if (kFwd) tma_load_3d(KQn + rg * 16384 + 8192, &qmap, bar, rg * 64, hk, static_cast<int>(t1));
-                    }
-                    if (value_tile)
-                        for (int rg = 0; rg < (a.V + 63) / 64; ++rg)
-                            tma_load_3d(VTn + rg * 8192, &vmap, bar, rg * 64, h, static_cast<int>(t1));
-                }
-                tma_pending |= 1u << (s ^ 1);
+            if (!last) {
                 g_nx = b_nx = 0.f;
-                if (tid < 64 && static_cast<int64_t>(c + 1) * kChunk + tid < L) {
-                    g_nx = a.g[(t1 + tid) * a.g_st + h * a.g_sh];
-                    b_nx = a.beta[(t1 + tid) * a.b_st + h * a.b_sh];
+                if (tid < 64 && tid < left - kChunk) {
+                    g_nx = a.g[(t0 + kChunk + tid) * a.g_st + h * a.g_sh];
+                    b_nx = a.beta[(t0 + kChunk + tid) * a.b_st + h * a.b_sh];
                 }
             }
 
-            bool ok = mbar_wait(&sc.tma_bar[s], (tma_phase >> s) & 1u, budget);
+            // ---- S1: K/Q tile; G = [K; Q] K^T on the tensor core while norms and the gate scan run
+            bool ok = mbar_wait(&sc.bar_kq, ph_kq, budget);
             if (ok) {
-                tma_phase ^= 1u << s;
-                tma_pending &= ~(1u << s);
+                ph_kq ^= 1u;
+                pend_kq = false;
             }
-
-            // ---- row norms (partial over a feature half) and the gate scan
+            if (tid == 0 && ok) {
+                tc_fence_after();
+                const uint32_t idesc = idesc_bf16_f32(128, 64, false, false);
+                const uint32_t kq = smem_u32(KQ);
+#pragma unroll
+                for (int kk = 0; kk < KD / 16; ++kk) {
+                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    umma_bf16(tmem + COL_R1, sdesc_sw128(kq + off, 16, 1024), sdesc_sw128(kq + off, 16, 1024), idesc,
+                              kk > 0);
+                }
+                umma_commit(&sc.bar_mma);
+            }
+            pend_mma = ok;
             {
                 float ss = 0.f;
                 if (r < 64 || kFwd) {
 #pragma unroll
-                    for (int c8 = 0; c8 < KH / 8; ++c8) {
-                        const int kc = (hf * KH) / 8 + c8;
+                    for (int kc = 0; kc < KD / 8; ++kc) {
                         const uint4 w = *reinterpret_cast<const uint4*>(KQ + (kc >> 3) * 16384 + sw128_off(r, kc & 7));
                         const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -337,7 +373,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                sc.red[tid] = ss;
+                const int row = r & 63;
+                const float inv = (row < n) ? (a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.f) : 0.f;
+                if (r < 64) sc.rk[row] = inv;
+                else sc.rq[row] = inv;
                 if (tid < 64) {
                     float x = (tid < n) ? g_cur * kLog2e : 0.f;
 #pragma unroll
@@ -349,95 +388,80 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (__syncthreads_or(!ok)) { failed = true; break; }
+            bool in_range = true;
             if (tid < 64) {
                 const int i = tid;
-                const bool valid = i < n;
-                float rk = 0.f, rq = 0.f;
-                if (valid) {
-                    rk = a.l2norm ? 1.0f / sqrtf(sc.red[i] + sc.red[128 + i] + 1e-6f) : 1.f;
-                    rq = a.l2norm ? 1.0f / sqrtf(sc.red[64 + i] + sc.red[192 + i] + 1e-6f) : 1.f;
-                }
                 const float bi = sc.bw[i] + (i >= 32 ? sc.bw[31] : 0.f);
+                const float b31 = sc.bw[31];
                 const float bC = sc.bw[31] + sc.bw[63];
-                const float bet = valid ? b_cur : 0.f;
+                const float rk = sc.rk[i], rq = sc.rq[i];
+                const float bet = i < n ? b_cur : 0.f;
                 const float gam = exp2f(bi);
+                const float e = exp2f(bi - b31);
                 sc.b[i] = bi;
-                sc.rk[i] = rk;
-                sc.rq[i] = rq;
                 sc.bet[i] = bet;
                 sc.sx[i] = bet * gam * rk;
                 sc.sq[i] = a.scale * rq * gam;
                 sc.sd[i] = exp2f(bC - bi) * rk;
+                sc.u[i] = rk * exp2f(b31 - bi);
+                sc.cA[i] = bet * rk * e;
+                sc.cP[i] = a.scale * rq * e;
+                in_range = fabsf(bi - b31) <= kFastRange;
             }
-            __syncthreads();
+            const bool fast = __syncthreads_and(in_range) != 0;
 
-            // ---- G = [K; Q] K^T  (M = 128 stacked rows, N = 64 key rows, contraction over K)
-            if (tid == 0) {
-                tc_fence_after();
-                const uint32_t idesc = idesc_bf16_f32(128, 64, false, false);
-                const uint32_t kq = smem_u32(KQ);
-#pragma unroll
-                for (int kk = 0; kk < KD / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    umma_bf16(tmem + COL_G, sdesc_sw128(kq + off, 16, 1024), sdesc_sw128(kq + off, 16, 1024), idesc,
-                              kk > 0);
-                }
-                umma_commit(&sc.mma_bar);
-            }
-            mma_pending = true;
-
-            // checkpoint: the state entering this chunk, at token offsets that are multiples of n
-            if (kFwd && a.ckpt && (static_cast<int64_t>(c) * kChunk) % a.ckpt_n == 0 && r < a.V) {
-                const int64_t row = a.ckpt_off[seq] + static_cast<int64_t>(c) * kChunk / a.ckpt_n;
-                const int64_t base = ((row * HO + h) * KD) * a.V + r;
-#pragma unroll
-                for (int i = 0; i < KH; ++i) {
-                    const int64_t idx = base + static_cast<int64_t>(hf * KH + i) * a.V;
-                    if (a.ckpt_bf16) static_cast<uint16_t*>(a.ckpt)[idx] = f_to_bf16_bits(st[i]);
-                    else static_cast<float*>(a.ckpt)[idx] = st[i];
-                }
-            }
-
-            ok = mbar_wait(&sc.mma_bar, mma_phase, budget);
+            // ---- S2: A (fp32, for the solve) and P (bf16) from G; Q' = (scale rq gamma) Q in place
+            ok = mbar_wait(&sc.bar_mma, ph_mma, budget);
             if (ok) {
-                mma_phase ^= 1u;
-                mma_pending = false;
+                ph_mma ^= 1u;
+                pend_mma = false;
             }
             tc_fence_after();
-            {
-                float gv[32];
-                tmem_ld16(trow + COL_G + 32 * hf, *reinterpret_cast<float(*)[16]>(&gv[0]));
-                tmem_ld16(trow + COL_G + 32 * hf + 16, *reinterpret_cast<float(*)[16]>(&gv[16]));
-                tmem_wait_ld();
-                if (r < 64) {
-                    // A row i = r (strictly lower), fp32 for the solve
-                    const int i = r;
-                    const float ci = sc.bet[i] * sc.rk[i], bi = sc.b[i];
+            if (r < 64 || kFwd) {
+                const int i = r & 63;
+                const bool is_a = r < 64;
+                const float ci = fast ? (is_a ? sc.cA[i] : sc.cP[i]) : (is_a ? sc.bet[i] * sc.rk[i] : a.scale * sc.rq[i]);
+                const float bi = sc.b[i];
+#pragma unroll 1
+                for (int p = 0; p < 4; ++p) {
+                    float gv[16];
+                    tmem_ld16(trow + COL_R1 + 16 * p, gv);
+                    tmem_wait_ld();
+                    if (fast) {
 #pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) {
-                        const int j = 32 * hf + jj;
-                        Asm[aidx(i, j)] = (j < i) ? ci * sc.rk[j] * gv[jj] * exp2f(bi - sc.b[j]) : 0.f;
-                    }
-                } else if (kFwd) {
-                    // P row i = r - 64 (lower incl. diagonal), bf16 K-major
-                    const int i = r - 64;
-                    const float ci = a.scale * sc.rq[i], bi = sc.b[i];
+                        for (int e = 0; e < 16; ++e) gv[e] *= ci * sc.u[16 * p + e];
+                    } else {
 #pragma unroll
-                    for (int cc = 0; cc < 4; ++cc) {
-                        float x[8];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int j = 32 * hf + 8 * cc + e;
-                            x[e] = (j <= i) ? ci * sc.rk[j] * gv[8 * cc + e] * exp2f(bi - sc.b[j]) : 0.f;
+                        for (int e = 0; e < 16; ++e) {
+                            const int j = 16 * p + e;
+                            const float dec = (j <= i) ? exp2f(bi - sc.b[j]) : 0.f;
+                            gv[e] *= ci * sc.rk[j] * dec;
                         }
-                        store8_split(PB + sw128_off(i, 4 * hf + cc), nullptr, x);
+                    }
+                    if (is_a) {
+#pragma unroll
+                        for (int j4 = 0; j4 < 4; ++j4) {
+                            const int j = 16 * p + 4 * j4;
+                            float4 w;
+                            w.x = (j + 0 < i) ? gv[4 * j4 + 0] : 0.f;
+                            w.y = (j + 1 < i) ? gv[4 * j4 + 1] : 0.f;
+                            w.z = (j + 2 < i) ? gv[4 * j4 + 2] : 0.f;
+                            w.w = (j + 3 < i) ? gv[4 * j4 + 3] : 0.f;
+                            *reinterpret_cast<float4*>(&M[midx(i, j)]) = w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e)
+                            if (16 * p + e > i) gv[e] = 0.f;
+                        store8_split(PB + sw128_off(i, 2 * p), nullptr, &gv[0]);
+                        store8_split(PB + sw128_off(i, 2 * p + 1), nullptr, &gv[8]);
                     }
                 }
             }
             if (kFwd) {
-                // Q' = (scale rq gamma) (.) Q in place: the B rows 64-127 of the next product
                 constexpr int kQChunks = 64 * (KD / 8);
-                for (int e = tid; e < kQChunks; e += kThreads) {
+#pragma unroll 2
+                for (int e = tid; e < kQChunks; e += kCta) {
                     const int row = e / (KD / 8), cc = e % (KD / 8);
                     uint4* p = reinterpret_cast<uint4*>(KQ + (cc >> 3) * 16384 + (64 + row) * 128 + (cc & 7) * 16);
                     const float f = sc.sq[row];
@@ -453,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             if (__syncthreads_or(!ok)) { failed = true; break; }
 
-            // ---- (K S)^T and (Q' S)^T = S^T [K; Q']^T  (M = 128 value rows)
+            // ---- S3: (K S)^T and (Q' S)^T = S^T [K; Q']^T; the solve runs meanwhile
             if (tid == 0) {
                 tc_fence_after();
                 const uint32_t idesc = idesc_bf16_f32(128, kFwd ? 128 : 64, false, false);
@@ -461,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < KD / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    umma_bf16(tmem + COL_KS, sdesc_sw128(wb + off, 16, 1024), sdesc_sw128(kq + off, 16, 1024), idesc,
+                    umma_bf16(tmem + COL_R1, sdesc_sw128(wb + off, 16, 1024), sdesc_sw128(kq + off, 16, 1024), idesc,
                               kk > 0);
                 }
                 if (!kFwd) {
@@ -469,90 +493,149 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < KD / 16; ++kk) {
                         const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        umma_bf16(tmem + COL_KS, sdesc_sw128(slo + off, 16, 1024), sdesc_sw128(kq + off, 16, 1024),
+                        umma_bf16(tmem + COL_R1, sdesc_sw128(slo + off, 16, 1024), sdesc_sw128(kq + off, 16, 1024),
                                   idesc, 1u);
                     }
                 }
-                umma_commit(&sc.mma_bar);
+                umma_commit(&sc.bar_mma);
             }
-            mma_pending = true;
+            pend_mma = true;
+            solve_unit_lower(M, sc.Y, tid);
 
-            // T = (I + A)^{-1} on the CUDA cores while the tensor cores run
-            solve_unit_lower(Asm, TF, sc.Y, TB, tid);
-
-            ok = mbar_wait(&sc.mma_bar, mma_phase, budget);
+            // ---- S4: X^T = beta V^T - sx (K S)^T (hi + lo); then T -> bf16 into the V tile's space
+            ok = mbar_wait(&sc.bar_mma, ph_mma, budget);
             if (ok) {
-                mma_phase ^= 1u;
-                mma_pending = false;
+                ph_mma ^= 1u;
+                pend_mma = false;
+            }
+            if (value_tile) {
+                const bool okv = mbar_wait(&sc.bar_v, ph_v, budget);
+                if (okv) {
+                    ph_v ^= 1u;
+                    pend_v = false;
+                }
+                ok = ok && okv;
             }
             tc_fence_after();
             {
-                // X^T[v][j] = beta_j V[j][v] - sx_j (K S)^T[v][j], split into bf16 hi + lo
-                float ks[32];
-                tmem_ld16(trow + COL_KS + 32 * hf, *reinterpret_cast<float(*)[16]>(&ks[0]));
-                tmem_ld16(trow + COL_KS + 32 * hf + 16, *reinterpret_cast<float(*)[16]>(&ks[16]));
-                tmem_wait_ld();
                 const int v = r;
                 const bool has_v = value_tile && v < a.V;
                 const uint8_t* vcol = VT + (v >> 6) * 8192 + (v & 7) * 2;
                 const uint32_t vchunk = (v & 63) >> 3;
+#pragma unroll 1
+                for (int p = 0; p < 4; ++p) {
+                    float ks[16];
+                    tmem_ld16(trow + COL_R1 + 16 * p, ks);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int cc = 2 * p + hh;
+                        float x[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int j = 8 * cc + e;
+                            const float vv = has_v
+                                ? bf16_bits_to_f(*reinterpret_cast<const uint16_t*>(vcol + sw128_off(j, vchunk)))
+                                : 0.f;
+                            x[e] = sc.bet[j] * vv - sc.sx[j] * ks[8 * hh + e];
+                        }
+                        store8_split(WB + sw128_off(v, cc), WB + 16384 + sw128_off(v, cc), x);
+                    }
+                }
+            }
+            __syncthreads();  // every V read is done before T overwrites the tile
+            {
+                const int i = tid >> 1;
+#pragma unroll 1
+                for (int cc4 = 0; cc4 < 4; ++cc4) {
+                    const int cc = (tid & 1) * 4 + cc4;
                     float x[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int j = 32 * hf + 8 * cc + e;
-                        const float vv =
-                            has_v ? bf16_bits_to_f(*reinterpret_cast<const uint16_t*>(vcol + sw128_off(j, vchunk))) : 0.f;
-                        x[e] = sc.bet[j] * vv - sc.sx[j] * ks[8 * cc + e];
-                    }
-                    store8_split(WB + sw128_off(v, 4 * hf + cc), WB + 16384 + sw128_off(v, 4 * hf + cc), x);
+                    for (int e = 0; e < 8; ++e) x[e] = t_at(M, i, 8 * cc + e);
+                    store8_split(VT + sw128_off(i, cc), nullptr, x);
                 }
             }
             fence_proxy_async_smem();
             tc_fence_before();
             if (__syncthreads_or(!ok)) { failed = true; break; }
 
-            // ---- D^T = X^T T^T  (hi and lo parts accumulate; contraction over 64 tokens)
+            // ---- S5: D^T = X^T T^T (hi + lo); meanwhile S <- 2^{b_C} S in TMEM (checkpoint first)
             if (tid == 0) {
                 tc_fence_after();
                 const uint32_t idesc = idesc_bf16_f32(128, 64, false, false);
-                const uint32_t wb = smem_u32(WB), tb = smem_u32(TB);
+                const uint32_t wb = smem_u32(WB), tb = smem_u32(VT);
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16(tmem + COL_D, sdesc_sw128(wb + part * 16384 + kk * 32, 16, 1024),
+                        umma_bf16(tmem + COL_R1, sdesc_sw128(wb + part * 16384 + kk * 32, 16, 1024),
                                   sdesc_sw128(tb + kk * 32, 16, 1024), idesc, (part | kk) != 0);
-                umma_commit(&sc.mma_bar);
+                umma_commit(&sc.bar_mma);
             }
-            mma_pending = true;
-            ok = mbar_wait(&sc.mma_bar, mma_phase, budget);
+            pend_mma = true;
+            {
+                const float gC = exp2f(sc.b[63]);
+                const bool ckpt = kFwd && a.ckpt && (static_cast<int64_t>(c) * kChunk) % a.ckpt_n == 0 && r < a.V;
+                int64_t cbase = 0;
+                if (ckpt) {
+                    const int64_t row = a.ckpt_off[seq] + static_cast<int64_t>(c) * kChunk / a.ckpt_n;
+                    cbase = ((row * HO + h) * KD) * a.V + r;
+                }
+#pragma unroll 1
+                for (int p = 0; p < KP; ++p) {
+                    float x[16];
+                    tmem_ld16(trow + COL_S + 16 * p, x);
+                    tmem_wait_ld();
+                    if (ckpt) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int64_t idx = cbase + static_cast<int64_t>(16 * p + e) * a.V;
+                            if (a.ckpt_bf16) static_cast<uint16_t*>(a.ckpt)[idx] = f_to_bf16_bits(x[e]);
+                            else static_cast<float*>(a.ckpt)[idx] = x[e];
+                        }
+                    }
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) x[e] *= gC;
+                    tmem_st16(trow + COL_S + 16 * p, x);
+                }
+                tmem_wait_st();
+            }
+            ok = mbar_wait(&sc.bar_mma, ph_mma, budget);
             if (ok) {
-                mma_phase ^= 1u;
-                mma_pending = false;
+                ph_mma ^= 1u;
+                pend_mma = false;
             }
             tc_fence_after();
+            if (tid == 0 && ok && value_tile && !last) {
+                // the V tile's space (now T) is free: fetch the next chunk's V
+                mbar_arrive_expect_tx(&sc.bar_v, v_bytes);
+                for (int rg = 0; rg < a.V / 64; ++rg)
+                    tma_load_3d(VT + rg * 8192, &vmap, &sc.bar_v, rg * 64, h, static_cast<int>(t0 + kChunk));
+            }
+            if (value_tile && !last) pend_v = true;
             {
-                float dd[32];
-                tmem_ld16(trow + COL_D + 32 * hf, *reinterpret_cast<float(*)[16]>(&dd[0]));
-                tmem_ld16(trow + COL_D + 32 * hf + 16, *reinterpret_cast<float(*)[16]>(&dd[16]));
-                tmem_wait_ld();
                 const int v = r;
+#pragma unroll 1
+                for (int p = 0; p < 4; ++p) {
+                    float dd[16];
+                    tmem_ld16(trow + COL_R1 + 16 * p, dd);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    float x[8];
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int cc = 2 * p + hh;
+                        float x[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) x[e] = sc.sd[32 * hf + 8 * cc + e] * dd[8 * cc + e];
-                    if (kFwd) store8_split(DT + sw128_off(v, 4 * hf + cc), nullptr, &dd[8 * cc]);
-                    store8_split(WB + sw128_off(v, 4 * hf + cc), WB + 16384 + sw128_off(v, 4 * hf + cc), x);
+                        for (int e = 0; e < 8; ++e) x[e] = sc.sd[8 * cc + e] * dd[8 * hh + e];
+                        if (kFwd) store8_split(DT + sw128_off(v, cc), nullptr, &dd[8 * hh]);
+                        store8_split(WB + sw128_off(v, cc), WB + 16384 + sw128_off(v, cc), x);
+                    }
                 }
             }
             fence_proxy_async_smem();
             tc_fence_before();
             if (__syncthreads_or(!ok)) { failed = true; break; }
 
-            // ---- O^T += D^T P^T (fwd) and SU = Ddec^T K (state update, K read MN-major)
+            // ---- S6: O^T += D^T P^T (fwd); S^T += Ddec^T K (K read MN-major)
             if (tid == 0) {
                 tc_fence_after();
                 const uint32_t wb = smem_u32(WB), kq = smem_u32(KQ);
@@ -561,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t dt = smem_u32(DT), pb = smem_u32(PB);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16(tmem + COL_QS, sdesc_sw128(dt + kk * 32, 16, 1024), sdesc_sw128(pb + kk * 32, 16, 1024),
+                        umma_bf16(tmem + COL_R2, sdesc_sw128(dt + kk * 32, 16, 1024), sdesc_sw128(pb + kk * 32, 16, 1024),
                                   idesc_o, 1u);
                 }
                 const uint32_t idesc_s = idesc_bf16_f32(128, KD, false, true);
@@ -569,44 +652,71 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16(tmem + COL_SU, sdesc_sw128(wb + part * 16384 + kk * 32, 16, 1024),
-                                  sdesc_sw128(kq + kk * 2048, 16384, 1024), idesc_s, (part | kk) != 0);
-                umma_commit(&sc.mma_bar);
+                        umma_bf16(tmem + COL_S, sdesc_sw128(wb + part * 16384 + kk * 32, 16, 1024),
+                                  sdesc_sw128(kq + kk * 2048, 16384, 1024), idesc_s, 1u);
+                umma_commit(&sc.bar_mma);
             }
-            mma_pending = true;
-            ok = mbar_wait(&sc.mma_bar, mma_phase, budget);
+            pend_mma = true;
+            ok = mbar_wait(&sc.bar_mma, ph_mma, budget);
             if (ok) {
-                mma_phase ^= 1u;
-                mma_pending = false;
+                ph_mma ^= 1u;
+                pend_mma = false;
             }
             tc_fence_after();
-            if (kFwd) {
-                float ov[32];
-                tmem_ld16(trow + COL_QS + 32 * hf, *reinterpret_cast<float(*)[16]>(&ov[0]));
-                tmem_ld16(trow + COL_QS + 32 * hf + 16, *reinterpret_cast<float(*)[16]>(&ov[16]));
-                tmem_wait_ld();
-                if (r < a.V) {
-                    uint16_t* op = a.o + (t0 + 32 * hf) * a.o_st + static_cast<int64_t>(h) * a.o_sh + r;
+            if (tid == 0 && ok && !last) {
+                // the K/Q tile is free: fetch the next chunk's
+                const int t1 = static_cast<int>(t0 + kChunk);
+                mbar_arrive_expect_tx(&sc.bar_kq, kq_bytes);
 #pragma unroll
-                    for (int ii = 0; ii < 32; ++ii)
-                        if (32 * hf + ii < n) op[static_cast<int64_t>(ii) * a.o_st] = f_to_bf16_bits(ov[ii]);
+                for (int rg = 0; rg < KD / 64; ++rg) {
+                    tma_load_3d(KQ + rg * 16384, &kmap, &sc.bar_kq, rg * 64, hk, t1);
+                    if (kFwd) tma_load_3d(KQ + rg * 16384 + 8192, &qmap, &sc.bar_kq, rg * 64, hk, t1);
+                }
+            }
+            if (!last) pend_kq = true;
+            if (kFwd) {
+                uint16_t* op = a.o + t0 * a.o_st + static_cast<int64_t>(h) * a.o_sh + r;
+#pragma unroll 1
+                for (int p = 0; p < 4; ++p) {
+                    float ov[16];
+                    tmem_ld16(trow + COL_R2 + 16 * p, ov);
+                    tmem_wait_ld();
+                    if (r < a.V) {
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const int i = 16 * p + e;
+                            if (i < n) op[static_cast<int64_t>(i) * a.o_st] = f_to_bf16_bits(ov[e]);
+                        }
+                    }
                 }
             }
             {
-                const float gC = exp2f(sc.b[63]);
-#pragma unroll
-                for (int c16 = 0; c16 < KH / 16; ++c16) {
-                    float su[16];
-                    tmem_ld16(trow + COL_SU + hf * KH + 16 * c16, su);
+                const int64_t fbase = unit_state * KD * a.V + r;
+#pragma unroll 1
+                for (int p = 0; p < KP; ++p) {
+                    float x[16];
+                    tmem_ld16(trow + COL_S + 16 * p, x);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) st[16 * c16 + e] = fmaf(gC, st[16 * c16 + e], su[e]);
-                }
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int kc = 2 * p + hh;
+                        const uint32_t off = (kc >> 3) * 16384 + sw128_off(r, kc & 7);
+                        store8_split(WB + off, kFwd ? nullptr : SLO + off, &x[8 * hh]);
+                    }
+                    if (last) {
+                        if (value_tile) {
+                            if (a.final_state && r < a.V)
 #pragma unroll
-                for (int c8 = 0; c8 < KH / 8; ++c8) {
-                    const int kc = (hf * KH) / 8 + c8;
-                    const uint32_t off = (kc >> 3) * 16384 + sw128_off(r, kc & 7);
-                    store8_split(WB + off, kFwd ? nullptr : SLO + off, &st[c8 * 8]);
+                                for (int e = 0; e < 16; ++e)
+                                    a.final_state[fbase + static_cast<int64_t>(16 * p + e) * a.V] = x[e];
+                        } else if (r < KD) {
+                            // transition[j][k] = P[k][j]: lane r = j holds column j of P
+                            float* tp = a.transition + (unit_state * KD + r) * KD + 16 * p;
+#pragma unroll
+                            for (int e = 0; e < 16; e += 4)
+                                *reinterpret_cast<float4*>(tp + e) = make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
+                        }
+                    }
                 }
             }
             fence_proxy_async_smem();
@@ -614,28 +724,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (__syncthreads_or(!ok)) { failed = true; break; }
         }
         if (failed) break;
-
-        // ---- end of unit: final state / span end state / transition
-        if (value_tile) {
-            if (a.final_state && r < a.V) {
-                float* fp = a.final_state + unit_state * KD * a.V + r;
-#pragma unroll
-                for (int i = 0; i < KH; ++i) fp[static_cast<int64_t>(hf * KH + i) * a.V] = st[i];
-            }
-        } else if (r < KD) {
-            // transition[j][k] = P[k][j]: thread row r = j holds column j of P
-            float* tp = a.transition + (unit_state * KD + r) * KD + hf * KH;
-#pragma unroll
-            for (int i = 0; i < KH; i += 4)
-                *reinterpret_cast<float4*>(tp + i) = make_float4(st[i], st[i + 1], st[i + 2], st[i + 3]);
-        }
     }
 
     if (failed) {
         // Let in-flight copies and products finish (bounded) before TMEM and shared memory go away.
-        for (int s = 0; s < 2; ++s)
-            if (tma_pending & (1u << s)) mbar_wait(&sc.tma_bar[s], (tma_phase >> s) & 1u, budget);
-        if (mma_pending) mbar_wait(&sc.mma_bar, mma_phase, budget);
+        if (pend_kq) mbar_wait(&sc.bar_kq, ph_kq, budget);
+        if (pend_v) mbar_wait(&sc.bar_v, ph_v, budget);
+        if (pend_mma) mbar_wait(&sc.bar_mma, ph_mma, budget);
         if (tid == 0) {
             atomicCAS(&a.hdr->status, LA_OK, LA_ERR_TIMEOUT);
             if (a.user_status) atomicCAS(a.user_status, LA_OK, LA_ERR_TIMEOUT);
@@ -649,19 +744,44 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------ host side
 template <int KD, int MODE>
 static cudaError_t launch_one(const ChunkArgs& a, const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm,
-                              int grid, cudaStream_t s) {
+                              int device, cudaStream_t s) {
     auto* fn = gdn_chunk_kernel<KD, MODE>;
     constexpr uint32_t smem = smem_alloc(MODE);
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    fn<<<grid, kThreads, smem, s>>>(qm, km, vm, a);
+    // Ask for the largest shared-memory carveout so two CTAs fit per SM.
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0, sms = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kCta, smem);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    if (e != cudaSuccess) return e;
+    {
+        // Residency from the hardware limits (registers are allocated per warp in units of
+        // 256, shared memory per SM minus the per-block reserve); the larger of the two
+        // answers is used.  A CTA that cannot be resident yet simply starts later and finds
+        // the ticket exhausted, so overestimating costs nothing.
+        cudaFuncAttributes fa;
+        int smem_sm = 0, reserve = 0, regs_sm = 0;
+        if (cudaFuncGetAttributes(&fa, fn) == cudaSuccess &&
+            cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device) == cudaSuccess &&
+            cudaDeviceGetAttribute(&reserve, cudaDevAttrReservedSharedMemoryPerBlock, device) == cudaSuccess &&
+            cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, device) == cudaSuccess) {
+            const int regs_cta = ((fa.numRegs * 32 + 255) / 256) * 256 * (kCta / 32);
+            const int by_regs = regs_cta > 0 ? regs_sm / regs_cta : 1;
+            const int by_smem = smem_sm / (static_cast<int>(smem) + reserve);
+            int hw = by_regs < by_smem ? by_regs : by_smem;
+            if (hw > 2) hw = 2;
+            if (hw > per_sm) per_sm = hw;
+        }
+    }
+    if (per_sm < 1) per_sm = 1;
+    const int64_t slots = static_cast<int64_t>(per_sm) * sms;
+    const int grid = static_cast<int>(a.num_units < slots ? a.num_units : slots);
+    if (grid <= 0) return cudaSuccess;
+    fn<<<grid, kCta, smem, s>>>(qm, km, vm, a);
     return cudaGetLastError();
-}
-
-int chunk_kernel_grid(int device, int64_t num_units) {
-    int sms = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess || sms <= 0) sms = 1;
-    return static_cast<int>(num_units < sms ? num_units : sms);
 }
 
 cudaError_t launch_chunk_kernel(const ChunkArgs& a, const CUtensorMap& qm, const CUtensorMap& km,
@@ -669,12 +789,10 @@ cudaError_t launch_chunk_kernel(const ChunkArgs& a, const CUtensorMap& qm, const
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const int grid = chunk_kernel_grid(dev, a.num_units);
-    if (grid <= 0) return cudaSuccess;
-    if (a.K == 128) return mode == kModeFwd ? launch_one<128, kModeFwd>(a, qm, km, vm, grid, s)
-                                            : launch_one<128, kModeSummary>(a, qm, km, vm, grid, s);
-    return mode == kModeFwd ? launch_one<64, kModeFwd>(a, qm, km, vm, grid, s)
-                            : launch_one<64, kModeSummary>(a, qm, km, vm, grid, s);
+    if (a.K == 128) return mode == kModeFwd ? launch_one<128, kModeFwd>(a, qm, km, vm, dev, s)
+                                            : launch_one<128, kModeSummary>(a, qm, km, vm, dev, s);
+    return mode == kModeFwd ? launch_one<64, kModeFwd>(a, qm, km, vm, dev, s)
+                            : launch_one<64, kModeSummary>(a, qm, km, vm, dev, s);
 }
 
 }  // namespace la
