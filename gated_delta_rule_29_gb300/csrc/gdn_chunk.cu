@@ -42,9 +42,9 @@ constexpr int kCta = 128;  // threads per CTA
 
 // ------------------------------------------------------------------ shared memory map
 constexpr uint32_t SM_KQ = 0;        // [region 0..1][128 rows: K 0-63, Q 64-127][128 B]
-constexpr uint32_t SM_V = 32768;     // V tile [region 0..1][64 rows][128 B] | later T bf16 [64][128 B]
+constexpr uint32_t SM_V = 32768;     // V tile [region 0..1][64 rows][128 B] | later T fp32 [64][64]
 constexpr uint32_t SM_WB = 49152;    // S^T bf16 [2][128][128 B] | X^T hi,lo | Ddec^T hi,lo
-constexpr uint32_t SM_M = 81920;     // A (lower) + T (upper, transposed) fp32 [64][64] | D^T bf16
+constexpr uint32_t SM_M = 81920;     // A fp32 [64][64] | T bf16 [64][128 B] | D^T bf16 [128][128 B]
 constexpr uint32_t SM_PB = 98304;    // P bf16 [64][128 B]
 constexpr uint32_t SM_SC = 106496;   // Scalars (7 KB)
 constexpr uint32_t SM_SLO = 114688;  // summary only: S^T bf16 residual (lo part), same layout as WB
@@ -80,13 +80,8 @@ struct Scalars {
 };
 static_assert(sizeof(Scalars) <= 7168, "scalar area");
 
-// Packed A/T buffer: A[i][j] (i > j) at (i, j); T[i][j] (i > j) at (j, i); T[i][i] = 1.
-// 16-byte chunks are XOR-swizzled by row to spread rows over the banks.
+// fp32 64 x 64 tiles (A, T): 16-byte chunks XOR-swizzled by row to spread rows over the banks.
 __device__ __forceinline__ int midx(int r, int c) { return r * 64 + ((((c >> 2) ^ (r & 15)) << 2) | (c & 3)); }
-__device__ __forceinline__ float a_at(const float* M, int i, int j) { return i > j ? M[midx(i, j)] : 0.f; }
-__device__ __forceinline__ float t_at(const float* M, int i, int j) {
-    return i == j ? 1.f : (i > j ? M[midx(j, i)] : 0.f);
-}
 
 __device__ __forceinline__ uint32_t pack_bf16(float x0, float x1) {
     __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
@@ -116,26 +111,34 @@ __device__ __forceinline__ void store8_split(uint8_t* hi, uint8_t* lo, const flo
     if (lo) *reinterpret_cast<uint4*>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
-// T = (I + A)^{-1} for the strictly lower-triangular A held in the packed buffer M;
-// T is written into M's upper half (transposed).  128 threads.
-//   diagonal 16 x 16 blocks: substitution, one warp per block, lane = column;
-//   T[bi][bj] = -T[bi][bi] * sum_{m = bj}^{bi - 1} A[bi][m] T[m][bj], block distance
+// T = (I + A)^{-1} for the strictly lower-triangular A held (fp32) in the packed buffer M.
+// T is written explicitly, zeros above the diagonal and ones on it, into Tf (fp32
+// [64][64], same swizzle).  128 threads.
+//   diagonal 16 x 16 blocks: right-looking substitution, one warp per block, lane =
+//   column (each step updates all later rows at once, so the FMAs are independent);
+//   T[bi][bj] = -T[bi][bi] * sum_{m = bj}^{bi - 1} A[bi][m] T[m][bj] for block distance
 //   d = bi - bj = 1, 2, 3 in turn, one warp per block, on tf32 warp MMAs.
-__device__ void solve_unit_lower(float* M, float (*Ys)[256], int tid) {
+__device__ void solve_unit_lower(const float* M, float* Tf, float (*Ys)[256], int tid) {
     const int warp = tid >> 5, lane = tid & 31;
+    // zero the six blocks above the block diagonal
+    for (int e = tid; e < 6 * 256; e += kCta) {
+        const int blk = e >> 8, i = (e >> 4) & 15, j = e & 15;
+        const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+        const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+        Tf[midx(16 * bi + i, 16 * bj + j)] = 0.f;
+    }
     if (lane < 16) {
         const int o = 16 * warp, c = lane;
-        float t[16];
+        float acc[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            float acc = (i == c) ? 1.f : 0.f;
+        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
 #pragma unroll
-            for (int j = 0; j < i; ++j) acc = fmaf(-M[midx(o + i, o + j)], t[j], acc);
-            t[i] = acc;
+        for (int j = 0; j < 16; ++j) {
+            const float tj = ((j == c) ? 1.f : 0.f) - acc[j];
+            Tf[midx(o + j, o + c)] = tj;
+#pragma unroll
+            for (int i = j + 1; i < 16; ++i) acc[i] = fmaf(M[midx(o + i, o + j)], tj, acc[i]);
         }
-#pragma unroll
-        for (int i = 1; i < 16; ++i)
-            if (i > c) M[midx(o + c, o + i)] = t[i];
     }
     __syncthreads();
     const int g = lane >> 2, q = lane & 3;
@@ -145,12 +148,12 @@ __device__ void solve_unit_lower(float* M, float (*Ys)[256], int tid) {
             const int r0 = 16 * (warp + d), c0 = 16 * warp;
             float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
             for (int m0 = c0; m0 < r0; m0 += 8) {
-                const uint32_t a[4] = {to_tf32(a_at(M, r0 + g, m0 + q)), to_tf32(a_at(M, r0 + g + 8, m0 + q)),
-                                       to_tf32(a_at(M, r0 + g, m0 + q + 4)), to_tf32(a_at(M, r0 + g + 8, m0 + q + 4))};
+                const uint32_t a[4] = {to_tf32(M[midx(r0 + g, m0 + q)]), to_tf32(M[midx(r0 + g + 8, m0 + q)]),
+                                       to_tf32(M[midx(r0 + g, m0 + q + 4)]), to_tf32(M[midx(r0 + g + 8, m0 + q + 4)])};
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
-                    const uint32_t b[2] = {to_tf32(t_at(M, m0 + q, c0 + 8 * nt + g)),
-                                           to_tf32(t_at(M, m0 + q + 4, c0 + 8 * nt + g))};
+                    const uint32_t b[2] = {to_tf32(Tf[midx(m0 + q, c0 + 8 * nt + g)]),
+                                           to_tf32(Tf[midx(m0 + q + 4, c0 + 8 * nt + g)])};
                     mma_tf32_16x8x8(y[nt], a, b);
                 }
             }
@@ -165,9 +168,9 @@ __device__ void solve_unit_lower(float* M, float (*Ys)[256], int tid) {
             float o[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
             for (int k0 = 0; k0 < 16; k0 += 8) {
-                const uint32_t a[4] = {to_tf32(t_at(M, r0 + g, r0 + k0 + q)), to_tf32(t_at(M, r0 + g + 8, r0 + k0 + q)),
-                                       to_tf32(t_at(M, r0 + g, r0 + k0 + q + 4)),
-                                       to_tf32(t_at(M, r0 + g + 8, r0 + k0 + q + 4))};
+                const uint32_t a[4] = {to_tf32(Tf[midx(r0 + g, r0 + k0 + q)]), to_tf32(Tf[midx(r0 + g + 8, r0 + k0 + q)]),
+                                       to_tf32(Tf[midx(r0 + g, r0 + k0 + q + 4)]),
+                                       to_tf32(Tf[midx(r0 + g + 8, r0 + k0 + q + 4)])};
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
                     const uint32_t b[2] = {to_tf32(Y[(k0 + q) * 16 + 8 * nt + g]),
@@ -178,10 +181,10 @@ __device__ void solve_unit_lower(float* M, float (*Ys)[256], int tid) {
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 const int cc = c0 + 8 * nt + 2 * q;
-                M[midx(cc, r0 + g)] = -o[nt][0];
-                M[midx(cc + 1, r0 + g)] = -o[nt][1];
-                M[midx(cc, r0 + g + 8)] = -o[nt][2];
-                M[midx(cc + 1, r0 + g + 8)] = -o[nt][3];
+                Tf[midx(r0 + g, cc)] = -o[nt][0];
+                Tf[midx(r0 + g, cc + 1)] = -o[nt][1];
+                Tf[midx(r0 + g + 8, cc)] = -o[nt][2];
+                Tf[midx(r0 + g + 8, cc + 1)] = -o[nt][3];
             }
             __syncwarp();
         }
@@ -201,8 +204,10 @@ __global__ void __launch_bounds__(kCta, 2)
     uint8_t* KQ = sm + SM_KQ;
     uint8_t* VT = sm + SM_V;
     uint8_t* WB = sm + SM_WB;
-    float* M = reinterpret_cast<float*>(sm + SM_M);
+    float* M = reinterpret_cast<float*>(sm + SM_M);   // A (fp32) -> T bf16 (TB) -> D^T bf16 (DT)
+    uint8_t* TB = sm + SM_M;
     uint8_t* DT = sm + SM_M;
+    float* Tf = reinterpret_cast<float*>(sm + SM_V);  // T fp32, in the V tile's space after X
     uint8_t* PB = sm + SM_PB;
     uint8_t* SLO = kFwd ? nullptr : sm + SM_SLO;
 
@@ -477,7 +482,7 @@ __global__ void __launch_bounds__(kCta, 2)
             tc_fence_before();
             if (__syncthreads_or(!ok)) { failed = true; break; }
 
-            // ---- S3: (K S)^T and (Q' S)^T = S^T [K; Q']^T; the solve runs meanwhile
+            // ---- S3: (K S)^T and (Q' S)^T = S^T [K; Q']^T
             if (tid == 0) {
                 tc_fence_after();
                 const uint32_t idesc = idesc_bf16_f32(128, kFwd ? 128 : 64, false, false);
@@ -500,9 +505,8 @@ __global__ void __launch_bounds__(kCta, 2)
                 umma_commit(&sc.bar_mma);
             }
             pend_mma = true;
-            solve_unit_lower(M, sc.Y, tid);
 
-            // ---- S4: X^T = beta V^T - sx (K S)^T (hi + lo); then T -> bf16 into the V tile's space
+            // ---- S4: X^T = beta V^T - sx (K S)^T (hi + lo); then T = (I + A)^{-1} in the V tile's space
             ok = mbar_wait(&sc.bar_mma, ph_mma, budget);
             if (ok) {
                 ph_mma ^= 1u;
@@ -543,27 +547,36 @@ __global__ void __launch_bounds__(kCta, 2)
                     }
                 }
             }
-            __syncthreads();  // every V read is done before T overwrites the tile
+            __syncthreads();  // every V read is done before T takes the tile's space
+            solve_unit_lower(M, Tf, sc.Y, tid);
             {
+                // T (fp32) -> bf16, K-major, into the A buffer's space (A is no longer needed)
                 const int i = tid >> 1;
-#pragma unroll 1
+#pragma unroll
                 for (int cc4 = 0; cc4 < 4; ++cc4) {
                     const int cc = (tid & 1) * 4 + cc4;
-                    float x[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) x[e] = t_at(M, i, 8 * cc + e);
-                    store8_split(VT + sw128_off(i, cc), nullptr, x);
+                    const float4 lo4 = *reinterpret_cast<const float4*>(&Tf[midx(i, 8 * cc)]);
+                    const float4 hi4 = *reinterpret_cast<const float4*>(&Tf[midx(i, 8 * cc + 4)]);
+                    const float x[8] = {lo4.x, lo4.y, lo4.z, lo4.w, hi4.x, hi4.y, hi4.z, hi4.w};
+                    store8_split(TB + sw128_off(i, cc), nullptr, x);
                 }
             }
             fence_proxy_async_smem();
             tc_fence_before();
             if (__syncthreads_or(!ok)) { failed = true; break; }
+            if (tid == 0 && value_tile && !last) {
+                // the V tile's space (T, fp32) is free: fetch the next chunk's V
+                mbar_arrive_expect_tx(&sc.bar_v, v_bytes);
+                for (int rg = 0; rg < a.V / 64; ++rg)
+                    tma_load_3d(VT + rg * 8192, &vmap, &sc.bar_v, rg * 64, h, static_cast<int>(t0 + kChunk));
+            }
+            if (value_tile && !last) pend_v = true;
 
             // ---- S5: D^T = X^T T^T (hi + lo); meanwhile S <- 2^{b_C} S in TMEM (checkpoint first)
             if (tid == 0) {
                 tc_fence_after();
                 const uint32_t idesc = idesc_bf16_f32(128, 64, false, false);
-                const uint32_t wb = smem_u32(WB), tb = smem_u32(VT);
+                const uint32_t wb = smem_u32(WB), tb = smem_u32(TB);
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
@@ -606,13 +619,6 @@ __global__ void __launch_bounds__(kCta, 2)
                 pend_mma = false;
             }
             tc_fence_after();
-            if (tid == 0 && ok && value_tile && !last) {
-                // the V tile's space (now T) is free: fetch the next chunk's V
-                mbar_arrive_expect_tx(&sc.bar_v, v_bytes);
-                for (int rg = 0; rg < a.V / 64; ++rg)
-                    tma_load_3d(VT + rg * 8192, &vmap, &sc.bar_v, rg * 64, h, static_cast<int>(t0 + kChunk));
-            }
-            if (value_tile && !last) pend_v = true;
             {
                 const int v = r;
 #pragma unroll 1
