@@ -74,7 +74,8 @@ struct Scalars {
     float cA[64];   // beta_i rk_i 2^{b_i - b_31}    (row factor of A)
     float cP[64];   // scale rq_i 2^{b_i - b_31}     (row factor of P)
     float Y[4][256];  // per-warp 16 x 16 solve scratch
-    uint64_t bar_kq, bar_v, bar_mma;
+    float gsum[2];    // per-warp sums of the next chunk's g * log2(e)
+    uint64_t bar_kq, bar_v, bar_mma, bar_o;
     uint32_t tmem_base;
     int32_t unit_lo, unit_hi;
 };
@@ -225,6 +226,7 @@ __global__ void __launch_bounds__(kCta, 2)
         mbar_init(&sc.bar_kq, 1);
         mbar_init(&sc.bar_v, 1);
         mbar_init(&sc.bar_mma, 1);
+        mbar_init(&sc.bar_o, 1);
         fence_mbar_init();
     }
     tc_fence_before();
@@ -233,8 +235,8 @@ __global__ void __launch_bounds__(kCta, 2)
     const uint32_t tmem = sc.tmem_base;
     const uint32_t trow = tmem + (static_cast<uint32_t>(r & ~31) << 16);
 
-    uint32_t ph_kq = 0, ph_v = 0, ph_mma = 0;  // parity of the next wait on each barrier
-    bool pend_kq = false, pend_v = false, pend_mma = false;
+    uint32_t ph_kq = 0, ph_v = 0, ph_mma = 0, ph_o = 0;  // parity of the next wait on each barrier
+    bool pend_kq = false, pend_v = false, pend_mma = false, pend_o = false;
     bool failed = false;
     const uint64_t budget = a.wait_budget_ns;
     const int64_t per_seq = static_cast<int64_t>(HO) * a.tiles_per_head;
@@ -262,9 +264,28 @@ __global__ void __launch_bounds__(kCta, 2)
         const int nchunks = static_cast<int>((L + kChunk - 1) / kChunk);
         const int64_t unit_state = static_cast<int64_t>(seq) * HO + h;
 
-        // ---- initial state -> TMEM (fp32 S^T) and WB (bf16 S^T, the A operand of K S)
+        // ---- chunk 0's gate total: the state kept in TMEM is pre-multiplied by the decay of the
+        // chunk it is about to enter, so the state-update product can accumulate onto it
+        float g_nx = 0.f, b_nx = 0.f;
+        if (tid < 64 && tid < L) {
+            g_nx = a.g[(ts + tid) * a.g_st + h * a.g_sh];
+            b_nx = a.beta[(ts + tid) * a.b_st + h * a.b_sh];
+        }
+        if (tid < 64) {
+            float x = g_nx * kLog2e;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+            if ((tid & 31) == 0) sc.gsum[tid >> 5] = x;
+        }
+        __syncthreads();
+        const float gam0 = nchunks > 0 ? exp2f(sc.gsum[0] + sc.gsum[1]) : 1.f;
+
+        // ---- initial state -> TMEM (fp32 2^{b_C} S^T), WB (bf16 S^T, the A operand of K S),
+        // checkpoint entry 0, and the end state of an empty sequence
         {
             const int64_t base = unit_state * KD * a.V + r;
+            const bool ckpt0 = kFwd && a.ckpt && nchunks > 0 && r < a.V;
+            const int64_t cbase = ckpt0 ? ((a.ckpt_off[seq] * HO + h) * KD) * a.V + r : 0;
 #pragma unroll 1
             for (int p = 0; p < KP; ++p) {
                 float x[16];
@@ -283,12 +304,19 @@ __global__ void __launch_bounds__(kCta, 2)
                     }
                     x[e] = val;
                 }
-                tmem_st16(trow + COL_S + 16 * p, x);
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     const int kc = 2 * p + hh;  // 16-byte chunk index along k
                     const uint32_t off = (kc >> 3) * 16384 + sw128_off(r, kc & 7);
                     store8_split(WB + off, kFwd ? nullptr : SLO + off, &x[8 * hh]);
+                }
+                if (ckpt0) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int64_t idx = cbase + static_cast<int64_t>(16 * p + e) * a.V;
+                        if (a.ckpt_bf16) static_cast<uint16_t*>(a.ckpt)[idx] = f_to_bf16_bits(x[e]);
+                        else static_cast<float*>(a.ckpt)[idx] = x[e];
+                    }
                 }
                 if (nchunks == 0) {  // empty sequence: the start state is the end state
                     if (value_tile) {
@@ -303,6 +331,9 @@ __global__ void __launch_bounds__(kCta, 2)
                             *reinterpret_cast<float4*>(tp + e) = make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
                     }
                 }
+#pragma unroll
+                for (int e = 0; e < 16; ++e) x[e] *= gam0;
+                tmem_st16(trow + COL_S + 16 * p, x);
             }
             tmem_wait_st();
         }
@@ -325,12 +356,6 @@ __global__ void __launch_bounds__(kCta, 2)
             pend_kq = true;
             pend_v = value_tile;
         }
-        float g_nx = 0.f, b_nx = 0.f;
-        if (tid < 64 && tid < L) {
-            g_nx = a.g[(ts + tid) * a.g_st + h * a.g_sh];
-            b_nx = a.beta[(ts + tid) * a.b_st + h * a.b_sh];
-        }
-
         for (int c = 0; c < nchunks; ++c) {
             const int64_t t0 = ts + static_cast<int64_t>(c) * kChunk;
             const int64_t left = L - static_cast<int64_t>(c) * kChunk;
@@ -427,11 +452,13 @@ __global__ void __launch_bounds__(kCta, 2)
                 const bool is_a = r < 64;
                 const float ci = fast ? (is_a ? sc.cA[i] : sc.cP[i]) : (is_a ? sc.bet[i] * sc.rk[i] : a.scale * sc.rq[i]);
                 const float bi = sc.b[i];
-#pragma unroll 1
+                float g64[64];
+#pragma unroll
+                for (int p = 0; p < 4; ++p) tmem_ld16(trow + COL_R1 + 16 * p, *reinterpret_cast<float(*)[16]>(&g64[16 * p]));
+                tmem_wait_ld();
+#pragma unroll
                 for (int p = 0; p < 4; ++p) {
-                    float gv[16];
-                    tmem_ld16(trow + COL_R1 + 16 * p, gv);
-                    tmem_wait_ld();
+                    float* gv = &g64[16 * p];
                     if (fast) {
 #pragma unroll
                         for (int e = 0; e < 16; ++e) gv[e] *= ci * sc.u[16 * p + e];
@@ -526,11 +553,13 @@ __global__ void __launch_bounds__(kCta, 2)
                 const bool has_v = value_tile && v < a.V;
                 const uint8_t* vcol = VT + (v >> 6) * 8192 + (v & 7) * 2;
                 const uint32_t vchunk = (v & 63) >> 3;
-#pragma unroll 1
+                float k64[64];
+#pragma unroll
+                for (int p = 0; p < 4; ++p) tmem_ld16(trow + COL_R1 + 16 * p, *reinterpret_cast<float(*)[16]>(&k64[16 * p]));
+                tmem_wait_ld();
+#pragma unroll
                 for (int p = 0; p < 4; ++p) {
-                    float ks[16];
-                    tmem_ld16(trow + COL_R1 + 16 * p, ks);
-                    tmem_wait_ld();
+                    const float* ks = &k64[16 * p];
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         const int cc = 2 * p + hh;
@@ -572,7 +601,7 @@ __global__ void __launch_bounds__(kCta, 2)
             }
             if (value_tile && !last) pend_v = true;
 
-            // ---- S5: D^T = X^T T^T (hi + lo); meanwhile S <- 2^{b_C} S in TMEM (checkpoint first)
+            // ---- S5: D^T = X^T T^T (hi + lo)
             if (tid == 0) {
                 tc_fence_after();
                 const uint32_t idesc = idesc_bf16_f32(128, 64, false, false);
@@ -586,32 +615,12 @@ __global__ void __launch_bounds__(kCta, 2)
                 umma_commit(&sc.bar_mma);
             }
             pend_mma = true;
-            {
-                const float gC = exp2f(sc.b[63]);
-                const bool ckpt = kFwd && a.ckpt && (static_cast<int64_t>(c) * kChunk) % a.ckpt_n == 0 && r < a.V;
-                int64_t cbase = 0;
-                if (ckpt) {
-                    const int64_t row = a.ckpt_off[seq] + static_cast<int64_t>(c) * kChunk / a.ckpt_n;
-                    cbase = ((row * HO + h) * KD) * a.V + r;
-                }
-#pragma unroll 1
-                for (int p = 0; p < KP; ++p) {
-                    float x[16];
-                    tmem_ld16(trow + COL_S + 16 * p, x);
-                    tmem_wait_ld();
-                    if (ckpt) {
+            if (tid < 64) {
+                // total gate of the next chunk (its values were prefetched at the chunk start)
+                float x = last ? 0.f : g_nx * kLog2e;
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int64_t idx = cbase + static_cast<int64_t>(16 * p + e) * a.V;
-                            if (a.ckpt_bf16) static_cast<uint16_t*>(a.ckpt)[idx] = f_to_bf16_bits(x[e]);
-                            else static_cast<float*>(a.ckpt)[idx] = x[e];
-                        }
-                    }
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) x[e] *= gC;
-                    tmem_st16(trow + COL_S + 16 * p, x);
-                }
-                tmem_wait_st();
+                for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+                if ((tid & 31) == 0) sc.gsum[tid >> 5] = x;
             }
             ok = mbar_wait(&sc.bar_mma, ph_mma, budget);
             if (ok) {
@@ -621,11 +630,13 @@ __global__ void __launch_bounds__(kCta, 2)
             tc_fence_after();
             {
                 const int v = r;
-#pragma unroll 1
+                float d64[64];
+#pragma unroll
+                for (int p = 0; p < 4; ++p) tmem_ld16(trow + COL_R1 + 16 * p, *reinterpret_cast<float(*)[16]>(&d64[16 * p]));
+                tmem_wait_ld();
+#pragma unroll
                 for (int p = 0; p < 4; ++p) {
-                    float dd[16];
-                    tmem_ld16(trow + COL_R1 + 16 * p, dd);
-                    tmem_wait_ld();
+                    float* dd = &d64[16 * p];
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         const int cc = 2 * p + hh;
@@ -652,6 +663,7 @@ __global__ void __launch_bounds__(kCta, 2)
                     for (int kk = 0; kk < 4; ++kk)
                         umma_bf16(tmem + COL_R2, sdesc_sw128(dt + kk * 32, 16, 1024), sdesc_sw128(pb + kk * 32, 16, 1024),
                                   idesc_o, 1u);
+                    umma_commit(&sc.bar_o);
                 }
                 const uint32_t idesc_s = idesc_bf16_f32(128, KD, false, true);
 #pragma unroll
@@ -663,10 +675,34 @@ __global__ void __launch_bounds__(kCta, 2)
                 umma_commit(&sc.bar_mma);
             }
             pend_mma = true;
-            ok = mbar_wait(&sc.bar_mma, ph_mma, budget);
-            if (ok) {
-                ph_mma ^= 1u;
-                pend_mma = false;
+            pend_o = kFwd;
+            if (kFwd) {
+                // O is complete before the state update: store it while the update runs
+                const bool oko = mbar_wait(&sc.bar_o, ph_o, budget);
+                if (oko) {
+                    ph_o ^= 1u;
+                    pend_o = false;
+                }
+                ok = ok && oko;
+                tc_fence_after();
+                float o64[64];
+#pragma unroll
+                for (int p = 0; p < 4; ++p) tmem_ld16(trow + COL_R2 + 16 * p, *reinterpret_cast<float(*)[16]>(&o64[16 * p]));
+                tmem_wait_ld();
+                if (r < a.V) {
+                    uint16_t* op = a.o + t0 * a.o_st + static_cast<int64_t>(h) * a.o_sh + r;
+#pragma unroll
+                    for (int i = 0; i < 64; ++i)
+                        if (i < n) op[static_cast<int64_t>(i) * a.o_st] = f_to_bf16_bits(o64[i]);
+                }
+            }
+            {
+                const bool okm = mbar_wait(&sc.bar_mma, ph_mma, budget);
+                if (okm) {
+                    ph_mma ^= 1u;
+                    pend_mma = false;
+                }
+                ok = ok && okm;
             }
             tc_fence_after();
             if (tid == 0 && ok && !last) {
@@ -680,50 +716,64 @@ __global__ void __launch_bounds__(kCta, 2)
                 }
             }
             if (!last) pend_kq = true;
-            if (kFwd) {
-                uint16_t* op = a.o + t0 * a.o_st + static_cast<int64_t>(h) * a.o_sh + r;
-#pragma unroll 1
-                for (int p = 0; p < 4; ++p) {
-                    float ov[16];
-                    tmem_ld16(trow + COL_R2 + 16 * p, ov);
-                    tmem_wait_ld();
-                    if (r < a.V) {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int i = 16 * p + e;
-                            if (i < n) op[static_cast<int64_t>(i) * a.o_st] = f_to_bf16_bits(ov[e]);
-                        }
-                    }
-                }
-            }
             {
+                // new state: bf16 copy for the next K S product, end state or checkpoint entry,
+                // then pre-multiplied by the next chunk's decay for its state update
+                const float gnext = last ? 1.f : exp2f(sc.gsum[0] + sc.gsum[1]);
                 const int64_t fbase = unit_state * KD * a.V + r;
+                const bool ckpt = kFwd && a.ckpt && !last && (static_cast<int64_t>(c + 1) * kChunk) % a.ckpt_n == 0 &&
+                                  r < a.V;
+                const int64_t cbase =
+                    ckpt ? (((a.ckpt_off[seq] + static_cast<int64_t>(c + 1) * kChunk / a.ckpt_n) * HO + h) * KD) * a.V + r
+                         : 0;
 #pragma unroll 1
-                for (int p = 0; p < KP; ++p) {
-                    float x[16];
-                    tmem_ld16(trow + COL_S + 16 * p, x);
+                for (int p0 = 0; p0 < KP; p0 += 4) {
+                    float s64[64];
+#pragma unroll
+                    for (int pp = 0; pp < 4; ++pp)
+                        if (p0 + pp < KP)
+                            tmem_ld16(trow + COL_S + 16 * (p0 + pp), *reinterpret_cast<float(*)[16]>(&s64[16 * pp]));
                     tmem_wait_ld();
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int kc = 2 * p + hh;
-                        const uint32_t off = (kc >> 3) * 16384 + sw128_off(r, kc & 7);
-                        store8_split(WB + off, kFwd ? nullptr : SLO + off, &x[8 * hh]);
-                    }
-                    if (last) {
-                        if (value_tile) {
-                            if (a.final_state && r < a.V)
+                    for (int pp = 0; pp < 4; ++pp) {
+                        const int p = p0 + pp;
+                        if (p >= KP) break;
+                        float* x = &s64[16 * pp];
 #pragma unroll
-                                for (int e = 0; e < 16; ++e)
-                                    a.final_state[fbase + static_cast<int64_t>(16 * p + e) * a.V] = x[e];
-                        } else if (r < KD) {
-                            // transition[j][k] = P[k][j]: lane r = j holds column j of P
-                            float* tp = a.transition + (unit_state * KD + r) * KD + 16 * p;
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int kc = 2 * p + hh;
+                            const uint32_t off = (kc >> 3) * 16384 + sw128_off(r, kc & 7);
+                            store8_split(WB + off, kFwd ? nullptr : SLO + off, &x[8 * hh]);
+                        }
+                        if (last) {
+                            if (value_tile) {
+                                if (a.final_state && r < a.V)
 #pragma unroll
-                            for (int e = 0; e < 16; e += 4)
-                                *reinterpret_cast<float4*>(tp + e) = make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
+                                    for (int e = 0; e < 16; ++e)
+                                        a.final_state[fbase + static_cast<int64_t>(16 * p + e) * a.V] = x[e];
+                            } else if (r < KD) {
+                                // transition[j][k] = P[k][j]: lane r = j holds column j of P
+                                float* tp = a.transition + (unit_state * KD + r) * KD + 16 * p;
+#pragma unroll
+                                for (int e = 0; e < 16; e += 4)
+                                    *reinterpret_cast<float4*>(tp + e) = make_float4(x[e], x[e + 1], x[e + 2], x[e + 3]);
+                            }
+                        } else {
+                            if (ckpt) {
+#pragma unroll
+                                for (int e = 0; e < 16; ++e) {
+                                    const int64_t idx = cbase + static_cast<int64_t>(16 * p + e) * a.V;
+                                    if (a.ckpt_bf16) static_cast<uint16_t*>(a.ckpt)[idx] = f_to_bf16_bits(x[e]);
+                                    else static_cast<float*>(a.ckpt)[idx] = x[e];
+                                }
+                            }
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) x[e] *= gnext;
+                            tmem_st16(trow + COL_S + 16 * p, *reinterpret_cast<float(*)[16]>(x));
                         }
                     }
                 }
+                if (!last) tmem_wait_st();
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -737,6 +787,7 @@ __global__ void __launch_bounds__(kCta, 2)
         if (pend_kq) mbar_wait(&sc.bar_kq, ph_kq, budget);
         if (pend_v) mbar_wait(&sc.bar_v, ph_v, budget);
         if (pend_mma) mbar_wait(&sc.bar_mma, ph_mma, budget);
+        if (pend_o) mbar_wait(&sc.bar_o, ph_o, budget);
         if (tid == 0) {
             atomicCAS(&a.hdr->status, LA_OK, LA_ERR_TIMEOUT);
             if (a.user_status) atomicCAS(a.user_status, LA_OK, LA_ERR_TIMEOUT);
