@@ -160,3 +160,107 @@ def read_status(status: torch.Tensor, stream: Optional[torch.cuda.Stream] = None
     out = ctypes.c_int32(0)
     B.check(B.load().la_read_status(status.data_ptr(), _stream_ptr(stream), ctypes.byref(out)), "la_read_status")
     return int(out.value)
+
+
+def _groups_by_tokens(lengths, parts):
+    """Consecutive sequence groups with roughly equal token counts (at least one sequence each)."""
+    total = int(sum(lengths))
+    parts = max(1, min(parts, len(lengths)))
+    bounds, acc, target = [0], 0, total / parts
+    for i, L in enumerate(lengths):
+        acc += int(L)
+        if len(bounds) < parts and acc >= target * len(bounds) and i + 1 < len(lengths):
+            bounds.append(i + 1)
+    bounds.append(len(lengths))
+    return [(bounds[j], bounds[j + 1]) for j in range(len(bounds) - 1) if bounds[j + 1] > bounds[j]]
+
+
+def gdn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
+                 cu_seqlens: torch.Tensor, *, scale: Optional[float] = None, use_qk_l2norm: bool = True,
+                 initial_state: Optional[torch.Tensor] = None, output_final_state: bool = True,
+                 checkpoint_every_n: int = 0, checkpoint_dtype: torch.dtype = torch.bfloat16,
+                 out: Optional[Tuple[torch.Tensor, Optional[torch.Tensor], Optional[torch.Tensor]]] = None,
+                 device: Optional[torch.device] = None, groups: int = 4, staging: Optional[dict] = None):
+    """gdn_fwd on HOST tensors: copies in, computes, copies out, pipelined by sequence groups.
+
+    q, k, v, g, beta, cu_seqlens (and initial_state) are contiguous CPU tensors (pin them for
+    asynchronous copies).  The batch is cut into `groups` consecutive sequence groups of similar
+    token counts; each group's host-to-device copy, forward and device-to-host copy run on their
+    own streams, so copies overlap computation and the group kernels share the GPU.  Outputs are
+    CPU tensors (pinned when `out` is not given).  Returns (o, final_state, checkpoints) once every
+    copy is enqueued; the current stream is made to wait for them, so synchronise it (or an event
+    recorded on it) before reading the outputs on the host.  Because every sequence's results are
+    independent of the batch, the grouped run gives the same bits as one gdn_fwd call.  `staging`
+    may carry device buffers and streams from an earlier call of the same shapes to avoid
+    reallocation.
+    """
+    dev = device or torch.device("cuda", torch.cuda.current_device())
+    T, HK, K = k.shape
+    HV, V = v.shape[1], v.shape[2]
+    HO = HV
+    N = cu_seqlens.numel() - 1
+    cu = cu_seqlens.to(torch.int64)
+    lengths = (cu[1:] - cu[:-1]).tolist()
+    n = int(checkpoint_every_n or 0)
+    rows = [(int(L) + n - 1) // n for L in lengths] if n else [0] * N
+    if out is None:
+        o_h = torch.empty(T, HO, V, dtype=torch.bfloat16).pin_memory()
+        fin_h = torch.empty(N, HO, K, V, dtype=torch.float32).pin_memory() if output_final_state else None
+        ck_h = torch.empty(sum(rows), HO, K, V, dtype=checkpoint_dtype).pin_memory() if n else None
+    else:
+        o_h, fin_h, ck_h = out
+    st = staging if staging is not None else {}
+
+    def dbuf(name, like, dtype=None):
+        t = st.get(name)
+        if t is None or t.shape != like.shape:
+            t = torch.empty(like.shape, dtype=dtype or like.dtype, device=dev)
+            st[name] = t
+        return t
+
+    qd, kd, vd = dbuf("q", q), dbuf("k", k), dbuf("v", v)
+    gd, bd = dbuf("g", g), dbuf("beta", beta)
+    s0d = dbuf("s0", initial_state) if initial_state is not None else None
+    od = dbuf("o", o_h)
+    find = dbuf("fin", fin_h) if fin_h is not None else None
+    ckd = dbuf("ck", ck_h) if ck_h is not None else None
+    cur = torch.cuda.current_stream(dev)
+    h2d = st.setdefault("h2d_stream", torch.cuda.Stream(dev))
+    d2h = st.setdefault("d2h_stream", torch.cuda.Stream(dev))
+    h2d.wait_stream(cur)
+    d2h.wait_stream(cur)
+    row_off = [0]
+    for r_ in rows:
+        row_off.append(row_off[-1] + r_)
+    for gi, (a, b) in enumerate(_groups_by_tokens(lengths, groups)):
+        t_a, t_b = int(cu[a]), int(cu[b])
+        cu_g = (cu[a:b + 1] - t_a).to(torch.int32)
+        cs = st.setdefault(f"compute_stream{gi}", torch.cuda.Stream(dev))
+        with torch.cuda.stream(h2d):
+            for dst, src in ((qd, q), (kd, k), (vd, v), (gd, g), (bd, beta)):
+                dst[t_a:t_b].copy_(src[t_a:t_b], non_blocking=True)
+            if s0d is not None:
+                s0d[a:b].copy_(initial_state[a:b], non_blocking=True)
+            cu_d = cu_g.to(dev, non_blocking=True)
+            ev_in = torch.cuda.Event()
+            ev_in.record(h2d)
+        cs.wait_event(ev_in)
+        with torch.cuda.stream(cs):
+            gdn_fwd(qd[t_a:t_b], kd[t_a:t_b], vd[t_a:t_b], gd[t_a:t_b], bd[t_a:t_b], cu_d, scale=scale,
+                    use_qk_l2norm=use_qk_l2norm, initial_state=s0d[a:b] if s0d is not None else None,
+                    output_final_state=find is not None, checkpoint_every_n=n,
+                    checkpoint_dtype=checkpoint_dtype, checkpoint_rows_hint=row_off[b] - row_off[a],
+                    o=od[t_a:t_b], final_state=find[a:b] if find is not None else None,
+                    checkpoints=ckd[row_off[a]:row_off[b]] if ckd is not None else None, stream=cs)
+            cu_d.record_stream(cs)
+            ev_c = torch.cuda.Event()
+            ev_c.record(cs)
+        d2h.wait_event(ev_c)
+        with torch.cuda.stream(d2h):
+            o_h[t_a:t_b].copy_(od[t_a:t_b], non_blocking=True)
+            if fin_h is not None:
+                fin_h[a:b].copy_(find[a:b], non_blocking=True)
+            if ck_h is not None and row_off[b] > row_off[a]:
+                ck_h[row_off[a]:row_off[b]].copy_(ckd[row_off[a]:row_off[b]], non_blocking=True)
+    cur.wait_stream(d2h)
+    return o_h, fin_h, ck_h

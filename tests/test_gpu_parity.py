@@ -296,3 +296,19 @@ def test_summary_start_state_and_empty_spans():
     eye = np.eye(64)
     for i in (0, 2):
         assert np.array_equal(tr[i].cpu().numpy(), np.stack([eye, eye]).astype(np.float32))
+
+
+@pytest.mark.parametrize("groups", [1, 3])
+def test_host_pipeline_matches_device_call(groups):
+    """gdn_fwd_host (host buffers, pipelined by sequence groups) gives the same bits as gdn_fwd."""
+    w = small([300, 1, 0, 200, 129, 64], HK=2, HV=4, K=128, V=128, seed=37, initial_state=True,
+              checkpoint_every_n=64, checkpoint_dtype=torch.float32, slow_decay=True)
+    o_d, f_d, c_d = gpu_fwd(w)
+    pin = lambda x: x.contiguous().pin_memory()
+    o_h, f_h, c_h = la.gdn_fwd_host(pin(w.q), pin(w.k), pin(w.v), pin(w.g), pin(w.beta), w.cu_seqlens,
+                                    initial_state=pin(w.initial_state), checkpoint_every_n=64,
+                                    checkpoint_dtype=torch.float32, groups=groups)
+    torch.cuda.synchronize()
+    assert np.array_equal(o_h.float().numpy(), o_d)
+    assert np.array_equal(f_h.numpy(), f_d)
+    assert np.array_equal(c_h.numpy(), c_d)
