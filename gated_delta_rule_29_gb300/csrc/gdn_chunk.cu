@@ -54,7 +54,7 @@ __host__ __device__ constexpr uint32_t smem_alloc(int mode) {
 
 // TMEM columns (fp32, 128 lanes)
 constexpr uint32_t COL_S = 0;     // S^T (K columns)
-constexpr uint32_t COL_R1 = 128;  // G -> (K S)^T -> D^T      (64 columns)
+constexpr uint32_t COL_R1 = 128;  // G (128 columns with R2) -> (K S)^T -> D^T
 constexpr uint32_t COL_R2 = 192;  // (Q' S)^T, then += D^T P^T = O^T
 constexpr uint32_t TMEM_COLS = 256;
 
@@ -234,6 +234,14 @@ __global__ void __launch_bounds__(kCta, 2)
     tc_fence_after();
     const uint32_t tmem = sc.tmem_base;
     const uint32_t trow = tmem + (static_cast<uint32_t>(r & ~31) << 16);
+    // shared-memory matrix descriptors of the operand buffers; an operand at byte offset off
+    // from a buffer uses base + (off >> 4) (the start-address field counts 16-byte units)
+    const uint64_t d_kq = sdesc_sw128(smem_u32(KQ), 16, 1024);
+    const uint64_t d_kq_mn = sdesc_sw128(smem_u32(KQ), 16384, 1024);  // K read MN-major
+    const uint64_t d_wb = sdesc_sw128(smem_u32(WB), 16, 1024);
+    const uint64_t d_m = sdesc_sw128(smem_u32(sm + SM_M), 16, 1024);   // T bf16, then D^T bf16
+    const uint64_t d_pb = sdesc_sw128(smem_u32(PB), 16, 1024);
+    const uint64_t d_slo = kFwd ? 0 : sdesc_sw128(smem_u32(SLO), 16, 1024);
 
     uint32_t ph_kq = 0, ph_v = 0, ph_mma = 0, ph_o = 0;  // parity of the next wait on each barrier
     bool pend_kq = false, pend_v = false, pend_mma = false, pend_o = false;
@@ -370,7 +378,8 @@ __global__ void __launch_bounds__(kCta, 2)
                 }
             }
 
-            // ---- S1: K/Q tile; G = [K; Q] K^T on the tensor core while norms and the gate scan run
+            // ---- S1: K/Q tile; G = [K; Q] [K; Q]^T on the tensor core while the gate scan runs.
+            // Its diagonal holds the squared row norms of K (lanes 0-63) and Q (lanes 64-127).
             bool ok = mbar_wait(&sc.bar_kq, ph_kq, budget);
             if (ok) {
                 ph_kq ^= 1u;
@@ -378,44 +387,61 @@ __global__ void __launch_bounds__(kCta, 2)
             }
             if (tid == 0 && ok) {
                 tc_fence_after();
-                const uint32_t idesc = idesc_bf16_f32(128, 64, false, false);
-                const uint32_t kq = smem_u32(KQ);
+                const uint32_t idesc = idesc_bf16_f32(128, kFwd ? 128 : 64, false, false);
 #pragma unroll
                 for (int kk = 0; kk < KD / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    umma_bf16(tmem + COL_R1, sdesc_sw128(kq + off, 16, 1024), sdesc_sw128(kq + off, 16, 1024), idesc,
-                              kk > 0);
+                    const uint64_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                    umma_bf16(tmem + COL_R1, d_kq + off, d_kq + off, idesc, kk > 0);
                 }
                 umma_commit(&sc.bar_mma);
             }
             pend_mma = ok;
+            if (tid < 64) {
+                float x = (tid < n) ? g_cur * kLog2e : 0.f;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const float y = __shfl_up_sync(0xffffffffu, x, off);
+                    if ((tid & 31) >= off) x += y;
+                }
+                sc.bw[tid] = x;
+            }
             {
-                float ss = 0.f;
-                if (r < 64 || kFwd) {
+                const bool okg = mbar_wait(&sc.bar_mma, ph_mma, budget);
+                if (okg) {
+                    ph_mma ^= 1u;
+                    pend_mma = false;
+                }
+                ok = ok && okg;
+            }
+            tc_fence_after();
+            const int lane = r & 31;
+            float g64[64];
+            if (r < 64 || kFwd) {
 #pragma unroll
-                    for (int kc = 0; kc < KD / 8; ++kc) {
-                        const uint4 w = *reinterpret_cast<const uint4*>(KQ + (kc >> 3) * 16384 + sw128_off(r, kc & 7));
-                        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+                for (int p = 0; p < 4; ++p) tmem_ld16(trow + COL_R1 + 16 * p, *reinterpret_cast<float(*)[16]>(&g64[16 * p]));
+                float nrm = 0.f;
+                if (r < 64) {
+                    tmem_wait_ld();
+                    if (r < 32) {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float x0 = bf16_lo(ww[e]), x1 = bf16_hi(ww[e]);
-                            ss = fmaf(x0, x0, fmaf(x1, x1, ss));
-                        }
+                        for (int e = 0; e < 32; ++e) nrm = (e == lane) ? g64[e] : nrm;
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) nrm = (e == lane) ? g64[32 + e] : nrm;
                     }
+                } else {
+                    float d32[32];
+                    const uint32_t cbase = COL_R1 + (r & ~31);
+                    tmem_ld16(trow + cbase, *reinterpret_cast<float(*)[16]>(&d32[0]));
+                    tmem_ld16(trow + cbase + 16, *reinterpret_cast<float(*)[16]>(&d32[16]));
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) nrm = (e == lane) ? d32[e] : nrm;
                 }
                 const int row = r & 63;
-                const float inv = (row < n) ? (a.l2norm ? 1.0f / sqrtf(ss + 1e-6f) : 1.f) : 0.f;
+                const float inv = (row < n) ? (a.l2norm ? 1.0f / sqrtf(nrm + 1e-6f) : 1.f) : 0.f;
                 if (r < 64) sc.rk[row] = inv;
                 else sc.rq[row] = inv;
-                if (tid < 64) {
-                    float x = (tid < n) ? g_cur * kLog2e : 0.f;
-#pragma unroll
-                    for (int off = 1; off < 32; off <<= 1) {
-                        const float y = __shfl_up_sync(0xffffffffu, x, off);
-                        if ((tid & 31) >= off) x += y;
-                    }
-                    sc.bw[tid] = x;
-                }
             }
             if (__syncthreads_or(!ok)) { failed = true; break; }
             bool in_range = true;
@@ -424,7 +450,7 @@ __global__ void __launch_bounds__(kCta, 2)
                 const float bi = sc.bw[i] + (i >= 32 ? sc.bw[31] : 0.f);
                 const float b31 = sc.bw[31];
                 const float bC = sc.bw[31] + sc.bw[63];
-                const float rk = sc.rk[i], rq = sc.rq[i];
+                const float rk = sc.rk[i], rq = kFwd ? sc.rq[i] : 0.f;
                 const float bet = i < n ? b_cur : 0.f;
                 const float gam = exp2f(bi);
                 const float e = exp2f(bi - b31);
@@ -441,21 +467,11 @@ __global__ void __launch_bounds__(kCta, 2)
             const bool fast = __syncthreads_and(in_range) != 0;
 
             // ---- S2: A (fp32, for the solve) and P (bf16) from G; Q' = (scale rq gamma) Q in place
-            ok = mbar_wait(&sc.bar_mma, ph_mma, budget);
-            if (ok) {
-                ph_mma ^= 1u;
-                pend_mma = false;
-            }
-            tc_fence_after();
             if (r < 64 || kFwd) {
                 const int i = r & 63;
                 const bool is_a = r < 64;
                 const float ci = fast ? (is_a ? sc.cA[i] : sc.cP[i]) : (is_a ? sc.bet[i] * sc.rk[i] : a.scale * sc.rq[i]);
                 const float bi = sc.b[i];
-                float g64[64];
-#pragma unroll
-                for (int p = 0; p < 4; ++p) tmem_ld16(trow + COL_R1 + 16 * p, *reinterpret_cast<float(*)[16]>(&g64[16 * p]));
-                tmem_wait_ld();
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
                     float* gv = &g64[16 * p];
@@ -513,20 +529,16 @@ __global__ void __launch_bounds__(kCta, 2)
             if (tid == 0) {
                 tc_fence_after();
                 const uint32_t idesc = idesc_bf16_f32(128, kFwd ? 128 : 64, false, false);
-                const uint32_t wb = smem_u32(WB), kq = smem_u32(KQ);
 #pragma unroll
                 for (int kk = 0; kk < KD / 16; ++kk) {
-                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    umma_bf16(tmem + COL_R1, sdesc_sw128(wb + off, 16, 1024), sdesc_sw128(kq + off, 16, 1024), idesc,
-                              kk > 0);
+                    const uint64_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                    umma_bf16(tmem + COL_R1, d_wb + off, d_kq + off, idesc, kk > 0);
                 }
                 if (!kFwd) {
-                    const uint32_t slo = smem_u32(SLO);
 #pragma unroll
                     for (int kk = 0; kk < KD / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                        umma_bf16(tmem + COL_R1, sdesc_sw128(slo + off, 16, 1024), sdesc_sw128(kq + off, 16, 1024),
-                                  idesc, 1u);
+                        const uint64_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                        umma_bf16(tmem + COL_R1, d_slo + off, d_kq + off, idesc, 1u);
                     }
                 }
                 umma_commit(&sc.bar_mma);
@@ -605,13 +617,12 @@ __global__ void __launch_bounds__(kCta, 2)
             if (tid == 0) {
                 tc_fence_after();
                 const uint32_t idesc = idesc_bf16_f32(128, 64, false, false);
-                const uint32_t wb = smem_u32(WB), tb = smem_u32(TB);
 #pragma unroll
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16(tmem + COL_R1, sdesc_sw128(wb + part * 16384 + kk * 32, 16, 1024),
-                                  sdesc_sw128(tb + kk * 32, 16, 1024), idesc, (part | kk) != 0);
+                        umma_bf16(tmem + COL_R1, d_wb + ((part * 16384 + kk * 32) >> 4), d_m + ((kk * 32) >> 4), idesc,
+                                  (part | kk) != 0);
                 umma_commit(&sc.bar_mma);
             }
             pend_mma = true;
@@ -655,14 +666,11 @@ __global__ void __launch_bounds__(kCta, 2)
             // ---- S6: O^T += D^T P^T (fwd); S^T += Ddec^T K (K read MN-major)
             if (tid == 0) {
                 tc_fence_after();
-                const uint32_t wb = smem_u32(WB), kq = smem_u32(KQ);
                 if (kFwd) {
                     const uint32_t idesc_o = idesc_bf16_f32(128, 64, false, false);
-                    const uint32_t dt = smem_u32(DT), pb = smem_u32(PB);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16(tmem + COL_R2, sdesc_sw128(dt + kk * 32, 16, 1024), sdesc_sw128(pb + kk * 32, 16, 1024),
-                                  idesc_o, 1u);
+                        umma_bf16(tmem + COL_R2, d_m + ((kk * 32) >> 4), d_pb + ((kk * 32) >> 4), idesc_o, 1u);
                     umma_commit(&sc.bar_o);
                 }
                 const uint32_t idesc_s = idesc_bf16_f32(128, KD, false, true);
@@ -670,8 +678,8 @@ __global__ void __launch_bounds__(kCta, 2)
                 for (int part = 0; part < 2; ++part)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        umma_bf16(tmem + COL_S, sdesc_sw128(wb + part * 16384 + kk * 32, 16, 1024),
-                                  sdesc_sw128(kq + kk * 2048, 16384, 1024), idesc_s, 1u);
+                        umma_bf16(tmem + COL_S, d_wb + ((part * 16384 + kk * 32) >> 4), d_kq_mn + ((kk * 2048) >> 4),
+                                  idesc_s, 1u);
                 umma_commit(&sc.bar_mma);
             }
             pend_mma = true;
