@@ -353,6 +353,7 @@ def run_ours(args, world, rank, local):
                "sample": f"{len(units)} of {N * HO} (sequence, head) units x {w.lengths()[0]} tokens of the same "
                          f"workload ({dt:.1f} s), fp64 token-by-token C recurrence on {cores} threads"}
 
+    qkv_bytes = sum(t.numel() * t.element_size() for t in (w.q, w.k, w.v))
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -361,7 +362,7 @@ def run_ours(args, world, rank, local):
             "config": {"workload": WORKLOAD if args.seq_len == 8192 else w.name, "global_batch": N * world,
                        "seq_len": args.seq_len,
                        "parallelism": f"independent batches per GPU x{world}" if world > 1 else "single GPU",
-                       "l2": "inputs larger than L2 (1.6 GB of q/k/v per step); no flush"},
+                       "l2": f"inputs larger than L2 ({qkv_bytes / 1e9:.2f} GB of q/k/v per step); no flush"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak, "traffic": profiled_traffic(),
                          "peak_source": peak_src, "kernel": "gdn_chunk_kernel<128, fwd>",

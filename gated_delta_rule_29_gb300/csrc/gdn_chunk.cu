@@ -348,20 +348,22 @@ __global__ void __launch_bounds__(kCta, 2)
 
         // ---- first chunk's tiles and per-token scalars
         if (nchunks > 0) {
-            if (tid == 0) {
+            if (tid == 0 && !a.test_skip_tile_load) {
                 mbar_arrive_expect_tx(&sc.bar_kq, kq_bytes);
 #pragma unroll
                 for (int rg = 0; rg < KD / 64; ++rg) {
                     tma_load_3d(KQ + rg * 16384, &kmap, &sc.bar_kq, rg * 64, hk, static_cast<int>(ts));
                     if (kFwd) tma_load_3d(KQ + rg * 16384 + 8192, &qmap, &sc.bar_kq, rg * 64, hk, static_cast<int>(ts));
                 }
+            }
+            if (tid == 0) {
                 if (value_tile) {
                     mbar_arrive_expect_tx(&sc.bar_v, v_bytes);
                     for (int rg = 0; rg < a.V / 64; ++rg)
                         tma_load_3d(VT + rg * 8192, &vmap, &sc.bar_v, rg * 64, h, static_cast<int>(ts));
                 }
             }
-            pend_kq = true;
+            pend_kq = !a.test_skip_tile_load;
             pend_v = value_tile;
         }
         for (int c = 0; c < nchunks; ++c) {

@@ -88,6 +88,7 @@ struct ChunkArgs {
     const int64_t* ckpt_off;
     int32_t* user_status;
     uint64_t wait_budget_ns;
+    int32_t test_skip_tile_load;     // failure-path test: never load K/Q tiles, so the first wait runs out
 };
 
 // Launchers (return cudaError_t of the launch).

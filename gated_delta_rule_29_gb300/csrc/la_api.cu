@@ -9,6 +9,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -168,6 +169,14 @@ la_status run(const Common& c, ChunkArgs& ka, const void* q, int64_t q_st, int64
     ka.ckpt_off = pa.ckpt_off;
     ka.user_status = user_status;
     ka.wait_budget_ns = kWaitBudgetNs;
+    // Test hooks for the failure path (read on every call): LA_TEST_SKIP_TILE_LOAD=1 makes the
+    // chunk kernel skip its K/Q tile loads so its first bounded wait runs out and it reports
+    // LA_ERR_TIMEOUT; LA_TEST_WAIT_BUDGET_NS shortens the bounded waits.
+    if (const char* e = std::getenv("LA_TEST_SKIP_TILE_LOAD")) ka.test_skip_tile_load = std::atoi(e) != 0;
+    if (const char* e = std::getenv("LA_TEST_WAIT_BUDGET_NS")) {
+        const long long b = std::atoll(e);
+        if (b > 0) ka.wait_budget_ns = static_cast<uint64_t>(b);
+    }
     if (ka.num_units == 0) return LA_OK;
 
     CUtensorMap qm, km, vm;

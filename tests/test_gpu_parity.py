@@ -275,6 +275,30 @@ def test_bad_cu_seqlens_sets_status():
     assert la.read_status(status) == 0
 
 
+def test_bounded_wait_timeout_reports_and_context_survives(monkeypatch):
+    """The failure path of the bounded waits, made on the host: a test switch stops the
+    K/Q tile loads, so every CTA's first wait runs out after a 20 ms budget.  The kernel
+    must report LA_ERR_TIMEOUT and return; the next normal call on the same context must
+    succeed and match the oracle."""
+    w = small([100, 156, 64], seed=37)
+    d = dev()
+    t = to_dev(w, d)
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    monkeypatch.setenv("LA_TEST_SKIP_TILE_LOAD", "1")
+    monkeypatch.setenv("LA_TEST_WAIT_BUDGET_NS", "20000000")
+    la.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu"], status=status)
+    assert la.read_status(status) == la.binding.LA_ERR_TIMEOUT
+    monkeypatch.delenv("LA_TEST_SKIP_TILE_LOAD")
+    monkeypatch.delenv("LA_TEST_WAIT_BUDGET_NS")
+    torch.cuda.synchronize()
+    status.zero_()
+    o, fin, _ = la.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu"], status=status)
+    assert la.read_status(status) == 0
+    ref = oracle.gdn_fwd(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens)
+    assert rel(o.float().cpu().numpy(), ref["o"]) <= O_TOL
+    assert rel(fin.cpu().numpy(), ref["final_state"]) <= S_TOL
+
+
 def test_many_sequences_global_sort_path():
     """More than 8192 sequences: the prologue sorts in global memory."""
     rng = np.random.default_rng(23)
