@@ -5,7 +5,10 @@ the span summary (``gdn_summary``), following the cuDNN "Linear Attention"
 operations page (sections "Layout" and "Semantics worth knowing").  The
 arithmetic lives in ``gdn_oracle.c`` (token-by-token recurrence, fp64); this
 module only compiles it with gcc, converts inputs to fp64 and marshals
-arguments.
+arguments.  The optional in-kernel input transforms of cudnn-frontend PR #616
+(the softplus gate -exp(a_log) softplus(g + dt_bias), the bounded gate
+lower_bound * sigmoid(g), and beta = sigmoid(beta)) are applied here in fp64
+before the recurrence.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  The CUDA library never does, and this
@@ -41,6 +44,11 @@ MUTATIONS = {
     6: "interleaved grouped-head mapping",
     7: "transition stored untransposed",
     8: "checkpoints taken one token late",
+    # planted in the gate / beta transforms below (applied before the C recurrence)
+    9: "softplus gate without dt_bias",
+    10: "softplus gate rate a_log instead of exp(a_log)",
+    11: "beta sigmoid of the negated logit",
+    12: "bounded gate without the sigmoid",
 }
 
 
@@ -116,16 +124,65 @@ def _default_threads():
     return max(1, os.cpu_count() or 1)
 
 
+def softplus(x):
+    """log(1 + e^x) in fp64, evaluated as max(x, 0) + log1p(e^-|x|) so it never overflows."""
+    x = np.asarray(x, dtype=np.float64)
+    return np.maximum(x, 0.0) + np.log1p(np.exp(-np.abs(x)))
+
+
+def sigmoid(x):
+    """1 / (1 + e^-x) in fp64, evaluated without overflow for either sign of x."""
+    x = np.asarray(x, dtype=np.float64)
+    e = np.exp(-np.abs(x))
+    return np.where(x >= 0, 1.0 / (1.0 + e), e / (1.0 + e))
+
+
+def gate_transform(g, *, gate="log", a_log=None, dt_bias=None, gate_lower_bound=None, mutation=0):
+    """Per-token log decay from the raw gate input (cudnn-frontend PR #616, in-kernel gate fusion).
+
+    gate="log":           g is already the natural-log decay.
+    gate="softplus":      g[t,h] = -exp(a_log[h]) * softplus(g_raw[t,h] + dt_bias[h])   (a_log, dt_bias: [HO]).
+    gate="sigmoid_bound": g[t,h] = gate_lower_bound * sigmoid(g_raw[t,h]): a log decay bounded
+                          below by the (negative) lower bound.
+    """
+    g = _f64(g)
+    if gate == "log":
+        return g
+    if gate == "softplus":
+        a = _f64(a_log).reshape(1, -1)
+        dt = _f64(dt_bias).reshape(1, -1)
+        rate = a if mutation == 10 else np.exp(a)
+        return -rate * softplus(g if mutation == 9 else g + dt)
+    if gate == "sigmoid_bound":
+        lb = float(gate_lower_bound)
+        return lb * (g if mutation == 12 else sigmoid(g))
+    raise ValueError(f"unknown gate mode {gate!r}")
+
+
+def beta_transform(beta, *, beta_sigmoid=False, mutation=0):
+    """beta, or sigmoid(beta) when the logits are given (PR #616, in-kernel beta sigmoid)."""
+    beta = _f64(beta)
+    if not beta_sigmoid:
+        return beta
+    return sigmoid(-beta if mutation == 11 else beta)
+
+
 def gdn_fwd(q, k, v, g, beta, cu_seqlens, *, scale=None, use_qk_l2norm=True,
             initial_state=None, output_final_state=True, checkpoint_every_n=0,
-            want_o=True, unit_mask=None, nthreads=None, mutation=0):
+            want_o=True, unit_mask=None, nthreads=None, mutation=0,
+            gate="log", a_log=None, dt_bias=None, gate_lower_bound=None, beta_sigmoid=False):
     """fp64 forward: returns dict(o [T,HO,V], final_state [N,HO,K,V], checkpoints [R,HO,K,V]).
 
-    q, k: [T, HK, K]; v: [T, HV, V]; g, beta: [T, HO] (g in natural-log space);
-    cu_seqlens: [N + 1]; initial_state: [N, HO, K, V] or None (zero start).
+    q, k: [T, HK, K]; v: [T, HV, V]; g, beta: [T, HO] (g in natural-log space unless a gate
+    transform is named; beta the logits when beta_sigmoid); cu_seqlens: [N + 1];
+    initial_state: [N, HO, K, V] or None (zero start).
     scale defaults to 1/sqrt(K) and multiplies the (normalised) query.
     unit_mask: optional bool [N, HO]; unmarked units are left at zero.
     """
+    g = gate_transform(g, gate=gate, a_log=a_log, dt_bias=dt_bias, gate_lower_bound=gate_lower_bound,
+                       mutation=mutation)
+    beta = beta_transform(beta, beta_sigmoid=beta_sigmoid, mutation=mutation)
+    mutation = mutation if mutation < 9 else 0
     return _run(q, k, v, g, beta, cu_seqlens, scale=scale, use_qk_l2norm=use_qk_l2norm,
                 s0=initial_state, want_final=output_final_state,
                 checkpoint_every_n=checkpoint_every_n, want_o=want_o,
@@ -134,7 +191,8 @@ def gdn_fwd(q, k, v, g, beta, cu_seqlens, *, scale=None, use_qk_l2norm=True,
 
 
 def gdn_summary(k, v, g, beta, cu_seqlens, *, use_qk_l2norm=True, start_state=None,
-                unit_mask=None, nthreads=None, mutation=0):
+                unit_mask=None, nthreads=None, mutation=0,
+                gate="log", a_log=None, dt_bias=None, gate_lower_bound=None, beta_sigmoid=False):
     """fp64 span summary: returns dict(end_state [N,HO,K,V], transition [N,HO,K,K]).
 
     end_state is the state after each span's last token from ``start_state``
@@ -142,6 +200,10 @@ def gdn_summary(k, v, g, beta, cu_seqlens, *, use_qk_l2norm=True, start_state=No
     erase steps exp(g_t)(I - beta_t k_t k_t^T), later steps on the left, so that
     end_state = einsum('ab,av->bv', transition, S_init) + S_H.
     """
+    g = gate_transform(g, gate=gate, a_log=a_log, dt_bias=dt_bias, gate_lower_bound=gate_lower_bound,
+                       mutation=mutation)
+    beta = beta_transform(beta, beta_sigmoid=beta_sigmoid, mutation=mutation)
+    mutation = mutation if mutation < 9 else 0
     T = k.shape[0]
     HK, K = k.shape[1], k.shape[2]
     q = np.zeros((T, HK, K), dtype=np.float64)

@@ -12,7 +12,9 @@ Every check below is an independent statement of what the Gated DeltaNet forward
   * summaries: span composition and the transition product order;
   * checkpoints: entry j equals the final state of the prefix of length j*n;
   * state round trip: [0, m) then [m, L) equals the unsplit run;
-  * empty sequences.
+  * empty sequences;
+  * the optional input transforms (softplus gate, bounded sigmoid gate, beta
+    sigmoid) at arguments where they take exact values (ln 2, 1, 1/2, 3/4).
 test_planted_mistakes_are_caught plants each of the oracle's known mutations
 and requires at least one check to fail, so a plausible slip anywhere (a dropped
 term, a flipped sign, a wrong index or orientation) cannot pass unnoticed.
@@ -288,6 +290,71 @@ def check_empty(mutation=0):
                float(np.abs(s["end_state"][[0, 2]]).max()))
 
 
+def check_gate_softplus(mutation=0):
+    """Softplus gate -exp(a_log) softplus(g + dt_bias), with beta = 0 so only the decay acts.
+
+    Head 0: a_log = 0, dt_bias = 0, g = 0 gives log decay -ln 2 per token (softplus(0) = ln 2).
+    Head 1: a_log = ln 3, dt_bias = ln(e - 1), g = 0 gives -3 per token (softplus = ln e = 1).
+    Head 2: a_log = -3, g = 50 checks the large-argument branch: softplus(50) = 50 + log1p(e^-50).
+    The state after L tokens is exp(sum of log decays) S0, and the transition that factor times I.
+    """
+    L, K, V = 5, 3, 2
+    rng = np.random.default_rng(91)
+    q = rng.standard_normal((L, 1, K))
+    k = rng.standard_normal((L, 1, K))
+    v = rng.standard_normal((L, 3, V))
+    S0 = rng.standard_normal((1, 3, K, V))
+    g_raw = np.zeros((L, 3))
+    g_raw[:, 2] = 50.0
+    a_log = np.array([0.0, math.log(3.0), -3.0])
+    dt_bias = np.array([0.0, math.log(math.e - 1.0), 0.0])
+    beta = np.zeros((L, 3))
+    cu = np.array([0, L])
+    kw = dict(gate="softplus", a_log=a_log, dt_bias=dt_bias, mutation=mutation)
+    r = oracle.gdn_fwd(q, k, v, g_raw, beta, cu, initial_state=S0, **kw)
+    s = oracle.gdn_summary(k, v, g_raw, beta, cu, **kw)
+    per_token = np.array([-math.log(2.0), -3.0, -math.exp(-3.0) * (50.0 + math.log1p(math.exp(-50.0)))])
+    factor = np.exp(L * per_token)
+    errs = [_rel(r["final_state"][0, h], factor[h] * S0[0, h]) for h in range(3)]
+    errs += [_rel(s["transition"][0, h], factor[h] * np.eye(K)) for h in range(3)]
+    return max(errs)
+
+
+def check_gate_sigmoid_bound(mutation=0):
+    """Bounded gate lower_bound * sigmoid(g) with lower_bound = -2 ln 2 and beta = 0:
+    g = 0 gives sigmoid 1/2, a decay of exactly 1/2 per token; g = ln 3 gives sigmoid 3/4,
+    a decay of 2^-1.5."""
+    L, K, V = 4, 2, 3
+    rng = np.random.default_rng(92)
+    q = rng.standard_normal((L, 1, K))
+    k = rng.standard_normal((L, 1, K))
+    v = rng.standard_normal((L, 2, V))
+    S0 = rng.standard_normal((1, 2, K, V))
+    g_raw = np.zeros((L, 2))
+    g_raw[:, 1] = math.log(3.0)
+    beta = np.zeros((L, 2))
+    r = oracle.gdn_fwd(q, k, v, g_raw, beta, np.array([0, L]), initial_state=S0, gate="sigmoid_bound",
+                       gate_lower_bound=-2.0 * math.log(2.0), mutation=mutation)
+    return max(_rel(r["final_state"][0, 0], 0.5 ** L * S0[0, 0]),
+               _rel(r["final_state"][0, 1], 2.0 ** (-1.5 * L) * S0[0, 1]))
+
+
+def check_beta_sigmoid(mutation=0):
+    """beta given as logits: beta_raw = ln 3 is beta = 3/4.  One token from a zero start with
+    k = q = e_0, no norm, scale 1: S_1 = beta e_0 v^T and o_0 = beta v."""
+    K, V = 3, 2
+    k = np.zeros((1, 1, K))
+    k[0, 0, 0] = 1.0
+    v = np.array([[[1.0, -2.0]]])
+    g = np.array([[-0.3]])
+    beta_raw = np.array([[math.log(3.0)]])
+    r = oracle.gdn_fwd(k, k, v, g, beta_raw, np.array([0, 1]), scale=1.0, use_qk_l2norm=False,
+                       beta_sigmoid=True, mutation=mutation)
+    expect_S = np.zeros((K, V))
+    expect_S[0] = 0.75 * v[0, 0]
+    return max(_rel(r["o"][0, 0], 0.75 * v[0, 0]), _rel(r["final_state"][0, 0], expect_S))
+
+
 CHECKS = {
     "golden": (check_golden, 1e-12),
     "brute_force": (check_brute_force, 1e-12),
@@ -301,6 +368,9 @@ CHECKS = {
     "checkpoints": (check_checkpoints, 1e-13),
     "round_trip": (check_round_trip, 1e-12),
     "empty": (check_empty, 1e-15),
+    "gate_softplus": (check_gate_softplus, 1e-12),
+    "gate_sigmoid_bound": (check_gate_sigmoid_bound, 1e-12),
+    "beta_sigmoid": (check_beta_sigmoid, 1e-14),
 }
 
 
