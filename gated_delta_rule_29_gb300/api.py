@@ -31,6 +31,35 @@ def _check_thd(name, x, dtype, heads_dim=True):
         raise ValueError(f"{name} must have a contiguous innermost axis")
 
 
+def _set_transforms(p, HO, dev, a_log, dt_bias, gate_lower_bound, beta_sigmoid, beta):
+    """Fills the optional input-transform fields (cudnn-frontend PR #616 in-kernel fusions):
+    a_log + dt_bias select the softplus gate, gate_lower_bound the bounded sigmoid gate."""
+    if (a_log is None) != (dt_bias is None):
+        raise ValueError("the softplus gate needs both a_log and dt_bias")
+    if a_log is not None and gate_lower_bound is not None:
+        raise ValueError("choose one gate transform: (a_log, dt_bias) or gate_lower_bound")
+    keep = []
+    if a_log is not None:
+        for name, x in (("a_log", a_log), ("dt_bias", dt_bias)):
+            if not isinstance(x, torch.Tensor) or x.device != dev or x.dtype != torch.float32 or x.numel() != HO:
+                raise ValueError(f"{name} must be a float32 tensor of {HO} elements on {dev}")
+        a_log, dt_bias = a_log.contiguous(), dt_bias.contiguous()
+        keep += [a_log, dt_bias]
+        p.gate_mode, p.a_log, p.dt_bias = B.LA_GATE_SOFTPLUS, a_log.data_ptr(), dt_bias.data_ptr()
+    elif gate_lower_bound is not None:
+        p.gate_mode, p.gate_lower_bound = B.LA_GATE_SIGMOID_BOUND, float(gate_lower_bound)
+    p.beta_sigmoid = int(bool(beta_sigmoid))
+    p.beta_bf16 = int(beta.dtype == torch.bfloat16)
+    return keep
+
+
+def _check_beta(beta, beta_sigmoid):
+    if beta_sigmoid and isinstance(beta, torch.Tensor) and beta.dtype == torch.bfloat16:
+        _check_thd("beta", beta, torch.bfloat16, heads_dim=False)
+    else:
+        _check_thd("beta", beta, torch.float32, heads_dim=False)
+
+
 def _cu_bits(cu: torch.Tensor) -> int:
     if cu.dtype == torch.int32:
         return 32
@@ -59,15 +88,21 @@ def gdn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
             checkpoint_rows_hint: Optional[int] = None, o: Optional[torch.Tensor] = None,
             final_state: Optional[torch.Tensor] = None, checkpoints: Optional[torch.Tensor] = None,
             workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
-            stream: Optional[torch.cuda.Stream] = None
+            stream: Optional[torch.cuda.Stream] = None, a_log: Optional[torch.Tensor] = None,
+            dt_bias: Optional[torch.Tensor] = None, gate_lower_bound: Optional[float] = None,
+            beta_sigmoid: bool = False
             ) -> Tuple[torch.Tensor, Optional[torch.Tensor], Optional[torch.Tensor]]:
     """Chunked GDN forward.  Returns (o [T, HO, V] bf16, final_state [N, HO, K, V] fp32 or None,
-    checkpoints [R, HO, K, V] or None).  Asynchronous on the current stream."""
+    checkpoints [R, HO, K, V] or None).  Asynchronous on the current stream.
+
+    g is the natural-log decay, unless a_log and dt_bias ([HO] fp32) are given (the kernel then
+    uses -exp(a_log) softplus(g + dt_bias)) or gate_lower_bound (< 0; the kernel uses
+    gate_lower_bound * sigmoid(g)).  With beta_sigmoid, beta holds logits (fp32 or bf16)."""
     _check_thd("q", q, torch.bfloat16)
     _check_thd("k", k, torch.bfloat16)
     _check_thd("v", v, torch.bfloat16)
     _check_thd("g", g, torch.float32, heads_dim=False)
-    _check_thd("beta", beta, torch.float32, heads_dim=False)
+    _check_beta(beta, beta_sigmoid)
     T, HK, K = k.shape
     HV, V = v.shape[1], v.shape[2]
     N = cu_seqlens.numel() - 1
@@ -107,6 +142,7 @@ def gdn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
         p.checkpoint_every_n = int(checkpoint_every_n)
     p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel()
     p.status = status.data_ptr() if status is not None else None
+    keep = _set_transforms(p, HO, dev, a_log, dt_bias, gate_lower_bound, beta_sigmoid, beta)  # noqa: F841
     B.check(B.load().gdn_fwd(ctypes.byref(p), _stream_ptr(stream)), "gdn_fwd")
     return o, final_state, checkpoints
 
@@ -115,14 +151,17 @@ def gdn_summary(k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.T
                 cu_seqlens: torch.Tensor, *, use_qk_l2norm: bool = True,
                 start_state: Optional[torch.Tensor] = None, end_state: Optional[torch.Tensor] = None,
                 transition: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
-                status: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None
+                status: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
+                a_log: Optional[torch.Tensor] = None, dt_bias: Optional[torch.Tensor] = None,
+                gate_lower_bound: Optional[float] = None, beta_sigmoid: bool = False
                 ) -> Tuple[torch.Tensor, torch.Tensor]:
     """Span summary.  Returns (end_state [N, HO, K, V] fp32, transition [N, HO, K, K] fp32) with
-    end_state = einsum('ab,av->bv', transition, S_init) + S_H across spans."""
+    end_state = einsum('ab,av->bv', transition, S_init) + S_H across spans.  The gate and beta
+    transforms are as in gdn_fwd."""
     _check_thd("k", k, torch.bfloat16)
     _check_thd("v", v, torch.bfloat16)
     _check_thd("g", g, torch.float32, heads_dim=False)
-    _check_thd("beta", beta, torch.float32, heads_dim=False)
+    _check_beta(beta, beta_sigmoid)
     T, HK, K = k.shape
     HV, V = v.shape[1], v.shape[2]
     N = cu_seqlens.numel() - 1
@@ -151,6 +190,7 @@ def gdn_summary(k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.T
     p.transition = transition.data_ptr()
     p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel()
     p.status = status.data_ptr() if status is not None else None
+    keep = _set_transforms(p, HO, dev, a_log, dt_bias, gate_lower_bound, beta_sigmoid, beta)  # noqa: F841
     B.check(B.load().gdn_summary(ctypes.byref(p), _stream_ptr(stream)), "gdn_summary")
     return end_state, transition
 

@@ -22,6 +22,9 @@ LA_ERR_WORKSPACE = 6
 
 LA_DTYPE_BF16 = 0
 LA_DTYPE_F32 = 1
+LA_GATE_LOG = 0
+LA_GATE_SOFTPLUS = 1
+LA_GATE_SIGMOID_BOUND = 2
 
 EXPORTED_SYMBOLS = (
     "gdn_fwd",
@@ -58,6 +61,8 @@ class GdnFwdParams(ctypes.Structure):
         ("checkpoints", _vp), ("checkpoint_dtype", _i32), ("checkpoint_every_n", _i64),
         ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
         ("status", _vp),
+        ("gate_mode", _i32), ("a_log", _vp), ("dt_bias", _vp), ("gate_lower_bound", ctypes.c_float),
+        ("beta_sigmoid", _i32), ("beta_bf16", _i32),
     ]
 
 
@@ -77,6 +82,8 @@ class GdnSummaryParams(ctypes.Structure):
         ("transition", _vp),
         ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
         ("status", _vp),
+        ("gate_mode", _i32), ("a_log", _vp), ("dt_bias", _vp), ("gate_lower_bound", ctypes.c_float),
+        ("beta_sigmoid", _i32), ("beta_bf16", _i32),
     ]
 
 

@@ -96,6 +96,26 @@ __device__ __forceinline__ uint16_t f_to_bf16_bits(float x) {
     return *reinterpret_cast<uint16_t*>(&h);
 }
 
+// Per-token gate and beta as the recurrence uses them: the natural-log decay and beta in
+// [0, 1], after the optional input transforms (cudnn-frontend PR #616, in-kernel fusions):
+// softplus gate -exp(a_log) softplus(g + dt_bias) (gA = -exp(a_log[h]), gdt = dt_bias[h]),
+// bounded gate lower_bound * sigmoid(g), beta = sigmoid(beta) from bf16 or fp32 logits.
+__device__ __forceinline__ float gate_at(const ChunkArgs& a, int64_t t, int h, float gA, float gdt) {
+    const float x = a.g[t * a.g_st + h * a.g_sh];
+    if (a.gate_mode == LA_GATE_SOFTPLUS) {
+        const float z = x + gdt;
+        return gA * (z > 20.f ? z : log1pf(expf(z)));
+    }
+    if (a.gate_mode == LA_GATE_SIGMOID_BOUND) return a.gate_lb / (1.f + expf(-x));
+    return x;
+}
+__device__ __forceinline__ float beta_at(const ChunkArgs& a, int64_t t, int h) {
+    const int64_t i = t * a.b_st + h * a.b_sh;
+    const float x = a.beta_bf16 ? __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(a.beta)[i]) << 16)
+                                : a.beta[i];
+    return a.beta_sigmoid ? 1.f / (1.f + expf(-x)) : x;
+}
+
 __device__ __forceinline__ int64_t cu_get(const void* cu, int cu64, int64_t i) {
     return cu64 ? static_cast<const int64_t*>(cu)[i] : static_cast<int64_t>(static_cast<const int32_t*>(cu)[i]);
 }
@@ -275,9 +295,14 @@ __global__ void __launch_bounds__(kCta, 2)
         // ---- chunk 0's gate total: the state kept in TMEM is pre-multiplied by the decay of the
         // chunk it is about to enter, so the state-update product can accumulate onto it
         float g_nx = 0.f, b_nx = 0.f;
+        float gA = 0.f, gdt = 0.f;
+        if (a.gate_mode == LA_GATE_SOFTPLUS && tid < 64) {
+            gA = -expf(a.a_log[h]);
+            gdt = a.dt_bias[h];
+        }
         if (tid < 64 && tid < L) {
-            g_nx = a.g[(ts + tid) * a.g_st + h * a.g_sh];
-            b_nx = a.beta[(ts + tid) * a.b_st + h * a.b_sh];
+            g_nx = gate_at(a, ts + tid, h, gA, gdt);
+            b_nx = beta_at(a, ts + tid, h);
         }
         if (tid < 64) {
             float x = g_nx * kLog2e;
@@ -375,8 +400,8 @@ __global__ void __launch_bounds__(kCta, 2)
             if (!last) {
                 g_nx = b_nx = 0.f;
                 if (tid < 64 && tid < left - kChunk) {
-                    g_nx = a.g[(t0 + kChunk + tid) * a.g_st + h * a.g_sh];
-                    b_nx = a.beta[(t0 + kChunk + tid) * a.b_st + h * a.b_sh];
+                    g_nx = gate_at(a, t0 + kChunk + tid, h, gA, gdt);
+                    b_nx = beta_at(a, t0 + kChunk + tid, h);
                 }
             }
 

@@ -89,6 +89,13 @@ struct ChunkArgs {
     int32_t* user_status;
     uint64_t wait_budget_ns;
     int32_t test_skip_tile_load;     // failure-path test: never load K/Q tiles, so the first wait runs out
+    // optional input transforms (la_gate_mode, beta logits)
+    int32_t gate_mode;
+    const float* a_log;              // [HO]
+    const float* dt_bias;            // [HO]
+    float gate_lb;
+    int32_t beta_sigmoid;
+    int32_t beta_bf16;
 };
 
 // Launchers (return cudaError_t of the launch).

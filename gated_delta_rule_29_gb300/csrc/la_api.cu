@@ -116,7 +116,28 @@ struct Common {
     int32_t cu_bits;
     const float* g;
     const float* beta;
+    int32_t beta_bytes;  // 4 (fp32) or 2 (bf16)
 };
+
+// The optional input transforms (cudnn-frontend PR #616: in-kernel softplus / bounded gate,
+// beta sigmoid); validated here, applied by the chunk kernel as it loads g and beta.
+la_status set_transforms(ChunkArgs& ka, int32_t gate_mode, const float* a_log, const float* dt_bias, float lb,
+                         int32_t beta_sigmoid, int32_t beta_bf16) {
+    if (gate_mode == LA_GATE_SOFTPLUS) {
+        if (!a_log || !dt_bias || !aligned(a_log, 4) || !aligned(dt_bias, 4)) return LA_ERR_INVALID_ARG;
+    } else if (gate_mode == LA_GATE_SIGMOID_BOUND) {
+        if (!(lb < 0.f) || !std::isfinite(lb)) return LA_ERR_INVALID_ARG;
+    } else if (gate_mode != LA_GATE_LOG) {
+        return LA_ERR_INVALID_ARG;
+    }
+    ka.gate_mode = gate_mode;
+    ka.a_log = gate_mode == LA_GATE_SOFTPLUS ? a_log : nullptr;
+    ka.dt_bias = gate_mode == LA_GATE_SOFTPLUS ? dt_bias : nullptr;
+    ka.gate_lb = lb;
+    ka.beta_sigmoid = beta_sigmoid != 0;
+    ka.beta_bf16 = beta_bf16 != 0;
+    return LA_OK;
+}
 
 la_status check_common(const Common& c) {
     if (c.T < 0 || c.N < 0 || c.HK <= 0 || c.HV <= 0) return LA_ERR_INVALID_ARG;
@@ -125,7 +146,7 @@ la_status check_common(const Common& c) {
     if ((c.K != 64 && c.K != 128) || (c.V != 64 && c.V != 128)) return LA_ERR_UNSUPPORTED;
     if (c.HV % c.HK != 0) return LA_ERR_UNSUPPORTED;
     if (c.T >= (int64_t(1) << 31) - 64) return LA_ERR_UNSUPPORTED;  // TMA coordinates are int32
-    if (c.T > 0 && (!c.g || !c.beta || !aligned(c.g, 4) || !aligned(c.beta, 4))) return LA_ERR_INVALID_ARG;
+    if (c.T > 0 && (!c.g || !c.beta || !aligned(c.g, 4) || !aligned(c.beta, c.beta_bytes))) return LA_ERR_INVALID_ARG;
     return LA_OK;
 }
 
@@ -241,7 +262,8 @@ extern "C" {
 
 la_status gdn_fwd(const la_gdn_fwd_params* p, void* stream) {
     if (!p) return LA_ERR_INVALID_ARG;
-    Common c{p->T, p->N, p->HK, p->HV, p->K, p->V, p->cu_seqlens, p->cu_seqlens_bits, p->g, p->beta};
+    Common c{p->T, p->N, p->HK, p->HV, p->K, p->V, p->cu_seqlens, p->cu_seqlens_bits, p->g, p->beta,
+             p->beta_bf16 ? 2 : 4};
     la_status st = check_common(c);
     if (st != LA_OK) return st;
     if (p->T > 0) {
@@ -280,6 +302,9 @@ la_status gdn_fwd(const la_gdn_fwd_params* p, void* stream) {
     ka.ckpt_n = p->checkpoints ? p->checkpoint_every_n : 0;
     ka.transition = nullptr;
     ka.tiles_per_head = 1;
+    if ((st = set_transforms(ka, p->gate_mode, p->a_log, p->dt_bias, p->gate_lower_bound, p->beta_sigmoid,
+                             p->beta_bf16)) != LA_OK)
+        return st;
     return run(c, ka, p->q, p->q_stride_t, p->q_stride_h, p->k, p->k_stride_t, p->k_stride_h, p->v, p->v_stride_t,
                p->v_stride_h, ka.ckpt_n, p->workspace, p->workspace_bytes, p->status, la::kModeFwd,
                static_cast<cudaStream_t>(stream));
@@ -287,7 +312,8 @@ la_status gdn_fwd(const la_gdn_fwd_params* p, void* stream) {
 
 la_status gdn_summary(const la_gdn_summary_params* p, void* stream) {
     if (!p) return LA_ERR_INVALID_ARG;
-    Common c{p->T, p->N, p->HK, p->HV, p->K, p->V, p->cu_seqlens, p->cu_seqlens_bits, p->g, p->beta};
+    Common c{p->T, p->N, p->HK, p->HV, p->K, p->V, p->cu_seqlens, p->cu_seqlens_bits, p->g, p->beta,
+             p->beta_bf16 ? 2 : 4};
     la_status st = check_common(c);
     if (st != LA_OK) return st;
     if (p->T > 0) {
@@ -313,6 +339,9 @@ la_status gdn_summary(const la_gdn_summary_params* p, void* stream) {
     ka.final_state = p->end_state;
     ka.transition = p->transition;
     ka.tiles_per_head = 2;
+    if ((st = set_transforms(ka, p->gate_mode, p->a_log, p->dt_bias, p->gate_lower_bound, p->beta_sigmoid,
+                             p->beta_bf16)) != LA_OK)
+        return st;
     return run(c, ka, nullptr, 0, 0, p->k, p->k_stride_t, p->k_stride_h, p->v, p->v_stride_t, p->v_stride_h, 0,
                p->workspace, p->workspace_bytes, p->status, la::kModeSummary, static_cast<cudaStream_t>(stream));
 }

@@ -62,6 +62,17 @@ typedef enum la_status {
 
 typedef enum la_dtype { LA_DTYPE_BF16 = 0, LA_DTYPE_F32 = 1 } la_dtype;
 
+/*
+ * How the kernel reads g (cudnn-frontend PR #616: in-kernel gate fusion, used
+ * by the FLA GatedDeltaNet layer).  a_log and dt_bias are per output head.
+ *   LA_GATE_LOG           g is the natural-log decay itself (default).
+ *   LA_GATE_SOFTPLUS      log decay = -exp(a_log[h]) * softplus(g[t,h] + dt_bias[h]),
+ *                         softplus(x) = log(1 + e^x) (taken as x above 20).
+ *   LA_GATE_SIGMOID_BOUND log decay = gate_lower_bound * sigmoid(g[t,h]), bounded
+ *                         below by gate_lower_bound (< 0; PR #616 uses -5 by default).
+ */
+typedef enum la_gate_mode { LA_GATE_LOG = 0, LA_GATE_SOFTPLUS = 1, LA_GATE_SIGMOID_BOUND = 2 } la_gate_mode;
+
 /* Parameters of gdn_fwd.  Strides are in elements. */
 typedef struct la_gdn_fwd_params {
     /* ---- inputs ---- */
@@ -88,6 +99,13 @@ typedef struct la_gdn_fwd_params {
     void* workspace;          /* >= la_gdn_workspace_bytes(N, 0) bytes, 256-byte aligned, or NULL */
     size_t workspace_bytes;
     int32_t* status;          /* optional device int32; receives LA_OK or a device-side error */
+    /* ---- optional input transforms (all zero = off; PR #616 in-kernel fusions) ---- */
+    int32_t gate_mode;        /* la_gate_mode */
+    const float* a_log;       /* [HO] fp32 (LA_GATE_SOFTPLUS) */
+    const float* dt_bias;     /* [HO] fp32 (LA_GATE_SOFTPLUS) */
+    float gate_lower_bound;   /* < 0 (LA_GATE_SIGMOID_BOUND) */
+    int32_t beta_sigmoid;     /* beta holds logits: beta <- 1 / (1 + exp(-beta)) */
+    int32_t beta_bf16;        /* beta is bf16 (same strides) instead of fp32 */
 } la_gdn_fwd_params;
 
 /*
@@ -149,6 +167,13 @@ typedef struct la_gdn_summary_params {
     void* workspace;          /* >= la_gdn_workspace_bytes(N, 1) bytes, or NULL */
     size_t workspace_bytes;
     int32_t* status;
+    /* optional input transforms, as in la_gdn_fwd_params */
+    int32_t gate_mode;
+    const float* a_log;
+    const float* dt_bias;
+    float gate_lower_bound;
+    int32_t beta_sigmoid;
+    int32_t beta_bf16;
 } la_gdn_summary_params;
 
 /*

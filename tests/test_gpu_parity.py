@@ -336,3 +336,70 @@ def test_host_pipeline_matches_device_call(groups):
     assert np.array_equal(o_h.float().numpy(), o_d)
     assert np.array_equal(f_h.numpy(), f_d)
     assert np.array_equal(c_h.numpy(), c_d)
+
+
+# ------------------------------------------------------------------ in-kernel input transforms
+def _raw_gate_inputs(w, seed, beta_dtype=torch.float32):
+    """Raw gate and beta logits of a workload's shape (the layer's projections, N(0,1))."""
+    gen = torch.Generator().manual_seed(seed)
+    T = int(w.cu_seqlens[-1])
+    g_raw = torch.randn(T, w.HV, generator=gen)
+    beta_raw = torch.randn(T, w.HV, generator=gen).to(beta_dtype)
+    return g_raw, beta_raw
+
+
+@pytest.mark.parametrize("rate,beta_dtype", [(1.0, torch.float32), (0.01, torch.bfloat16)])
+def test_softplus_gate_and_beta_sigmoid(rate, beta_dtype):
+    """g = -exp(a_log) softplus(g_raw + dt_bias) and beta = sigmoid(beta_raw) computed in the
+    kernel, against the oracle applying the same transforms in fp64.  rate scales exp(a_log):
+    1.0 gives the layer's usual fast decay, 0.01 a slow one that keeps the start state alive."""
+    w = small([1, 63, 64, 65, 200], HK=2, HV=4, K=128, V=128, seed=41, initial_state=True,
+              checkpoint_every_n=64, checkpoint_dtype=torch.float32)
+    g_raw, beta_raw = _raw_gate_inputs(w, 43, beta_dtype)
+    a_log = torch.log(rate * torch.tensor([1.0, 2.0, 4.0, 8.0]))
+    dt_bias = torch.tensor([-4.0, -2.0, 0.0, 1.0])
+    d = dev()
+    t = to_dev(w, d)
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    o, fin, ck = la.gdn_fwd(t["q"], t["k"], t["v"], g_raw.to(d), beta_raw.to(d), t["cu"],
+                            initial_state=t["s0"], checkpoint_every_n=64, checkpoint_dtype=torch.float32,
+                            a_log=a_log.to(d), dt_bias=dt_bias.to(d), beta_sigmoid=True, status=status)
+    assert la.read_status(status) == 0
+    ref = oracle.gdn_fwd(w.q, w.k, w.v, g_raw, beta_raw.float(), w.cu_seqlens, initial_state=w.initial_state,
+                         checkpoint_every_n=64, gate="softplus", a_log=a_log, dt_bias=dt_bias, beta_sigmoid=True)
+    got = (o.float().cpu().numpy(), fin.cpu().numpy(), ck.cpu().numpy())
+    compare_units(w, got, ref, all_units(w))
+
+
+def test_bounded_gate_summary_and_forward():
+    """g = lower_bound * sigmoid(g_raw) with lower_bound = -0.05 (slow decay, so the start state
+    and the transitions stay large) and fp32 beta logits: summary and forward against the oracle."""
+    w = small([0, 150, 64, 300], HK=1, HV=2, K=64, V=128, seed=47, initial_state=True)
+    g_raw, beta_raw = _raw_gate_inputs(w, 53)
+    d = dev()
+    t = to_dev(w, d)
+    kw = dict(gate_lower_bound=-0.05, beta_sigmoid=True)
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    end, tr = la.gdn_summary(t["k"], t["v"], g_raw.to(d), beta_raw.to(d), t["cu"], start_state=t["s0"],
+                             status=status, **kw)
+    assert la.read_status(status) == 0
+    o, fin, _ = la.gdn_fwd(t["q"], t["k"], t["v"], g_raw.to(d), beta_raw.to(d), t["cu"], initial_state=t["s0"],
+                           status=status, **kw)
+    assert la.read_status(status) == 0
+    okw = dict(gate="sigmoid_bound", gate_lower_bound=-0.05, beta_sigmoid=True)
+    ref_s = oracle.gdn_summary(w.k, w.v, g_raw, beta_raw, w.cu_seqlens, start_state=w.initial_state, **okw)
+    ref_f = oracle.gdn_fwd(w.q, w.k, w.v, g_raw, beta_raw, w.cu_seqlens, initial_state=w.initial_state, **okw)
+    errs = {"end": rel(end.cpu().numpy(), ref_s["end_state"]), "transition": rel(tr.cpu().numpy(), ref_s["transition"]),
+            "o": rel(o.float().cpu().numpy(), ref_f["o"]), "final": rel(fin.cpu().numpy(), ref_f["final_state"])}
+    print("[parity] bounded gate: " + ", ".join(f"{k_} {v_:.2e}" for k_, v_ in errs.items()))
+    assert errs["o"] <= O_TOL and max(errs["end"], errs["transition"], errs["final"]) <= S_TOL, errs
+
+
+def test_transform_arguments_rejected():
+    w = small([64], seed=59)
+    d = dev()
+    t = to_dev(w, d)
+    with pytest.raises(la.binding.LinAttnError):
+        la.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu"], gate_lower_bound=0.5)
+    with pytest.raises(ValueError):
+        la.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu"], a_log=torch.zeros(2, device=d))
