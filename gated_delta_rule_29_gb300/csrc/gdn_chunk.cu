@@ -216,7 +216,8 @@ __device__ void solve_unit_lower(const float* M, float* Tf, float (*Ys)[256], in
 template <int KD, int MODE>
 __global__ void __launch_bounds__(kCta, 2)
     gdn_chunk_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-                     const __grid_constant__ CUtensorMap vmap, const ChunkArgs a) {
+                     const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
+                     const ChunkArgs a) {
     constexpr bool kFwd = MODE == kModeFwd;
     constexpr int KP = KD / 16;  // 16-column pieces of the state
     extern __shared__ uint8_t smem_raw[];
@@ -231,6 +232,7 @@ __global__ void __launch_bounds__(kCta, 2)
     float* Tf = reinterpret_cast<float*>(sm + SM_V);  // T fp32, in the V tile's space after X
     uint8_t* PB = sm + SM_PB;
     uint8_t* SLO = kFwd ? nullptr : sm + SM_SLO;
+    uint8_t* OST = sm + SM_M;  // O staging for the bulk store, once the O product has read D^T
 
     const int tid = threadIdx.x;
     const int r = tid;  // TMEM lane, value column, stacked token row
@@ -396,6 +398,7 @@ __global__ void __launch_bounds__(kCta, 2)
             const int64_t left = L - static_cast<int64_t>(c) * kChunk;
             const int n = left < kChunk ? static_cast<int>(left) : kChunk;
             const bool last = c + 1 == nchunks;
+            const bool o_tma_chunk = kFwd && a.o_tma && n == kChunk;
             const float g_cur = g_nx, b_cur = b_nx;
             if (!last) {
                 g_nx = b_nx = 0.f;
@@ -724,7 +727,24 @@ __global__ void __launch_bounds__(kCta, 2)
 #pragma unroll
                 for (int p = 0; p < 4; ++p) tmem_ld16(trow + COL_R2 + 16 * p, *reinterpret_cast<float(*)[16]>(&o64[16 * p]));
                 tmem_wait_ld();
-                if (r < a.V) {
+                if (o_tma_chunk) {
+                    // a full chunk: O (bf16) into the free M buffer in the TMA box layout
+                    // ([v / 64][64 tokens][128 B], 128-byte swizzle), then one bulk store per 64 columns
+                    if (r < a.V) {
+                        uint8_t* col = OST + (r >> 6) * 8192 + (r & 7) * 2;
+                        const uint32_t vchunk = (r & 63) >> 3;
+#pragma unroll
+                        for (int i = 0; i < 64; ++i)
+                            *reinterpret_cast<uint16_t*>(col + sw128_off(i, vchunk)) = f_to_bf16_bits(o64[i]);
+                    }
+                    fence_proxy_async_smem();
+                    __syncthreads();
+                    if (tid == 0) {
+                        for (int rg = 0; rg < a.V / 64; ++rg)
+                            tma_store_3d(&omap, OST + rg * 8192, rg * 64, h, static_cast<int>(t0));
+                        bulk_commit_group();
+                    }
+                } else if (r < a.V) {
                     uint16_t* op = a.o + t0 * a.o_st + static_cast<int64_t>(h) * a.o_sh + r;
 #pragma unroll
                     for (int i = 0; i < 64; ++i)
@@ -810,12 +830,15 @@ __global__ void __launch_bounds__(kCta, 2)
                 }
                 if (!last) tmem_wait_st();
             }
+            // the O staging buffer is the next chunk's A: the bulk store must have read it
+            if (kFwd && tid == 0) bulk_wait_read_all();
             fence_proxy_async_smem();
             tc_fence_before();
             if (__syncthreads_or(!ok)) { failed = true; break; }
         }
         if (failed) break;
     }
+    if (kFwd && tid == 0) bulk_wait_all();
 
     if (failed) {
         // Let in-flight copies and products finish (bounded) before TMEM and shared memory go away.
@@ -836,7 +859,7 @@ __global__ void __launch_bounds__(kCta, 2)
 // ------------------------------------------------------------------ host side
 template <int KD, int MODE>
 static cudaError_t launch_one(const ChunkArgs& a, const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm,
-                              int device, cudaStream_t s) {
+                              const CUtensorMap& om, int device, cudaStream_t s) {
     auto* fn = gdn_chunk_kernel<KD, MODE>;
     constexpr uint32_t smem = smem_alloc(MODE);
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -872,19 +895,19 @@ static cudaError_t launch_one(const ChunkArgs& a, const CUtensorMap& qm, const C
     const int64_t slots = static_cast<int64_t>(per_sm) * sms;
     const int grid = static_cast<int>(a.num_units < slots ? a.num_units : slots);
     if (grid <= 0) return cudaSuccess;
-    fn<<<grid, kCta, smem, s>>>(qm, km, vm, a);
+    fn<<<grid, kCta, smem, s>>>(qm, km, vm, om, a);
     return cudaGetLastError();
 }
 
 cudaError_t launch_chunk_kernel(const ChunkArgs& a, const CUtensorMap& qm, const CUtensorMap& km,
-                                const CUtensorMap& vm, int mode, cudaStream_t s) {
+                                const CUtensorMap& vm, const CUtensorMap& om, int mode, cudaStream_t s) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (a.K == 128) return mode == kModeFwd ? launch_one<128, kModeFwd>(a, qm, km, vm, dev, s)
-                                            : launch_one<128, kModeSummary>(a, qm, km, vm, dev, s);
-    return mode == kModeFwd ? launch_one<64, kModeFwd>(a, qm, km, vm, dev, s)
-                            : launch_one<64, kModeSummary>(a, qm, km, vm, dev, s);
+    if (a.K == 128) return mode == kModeFwd ? launch_one<128, kModeFwd>(a, qm, km, vm, om, dev, s)
+                                            : launch_one<128, kModeSummary>(a, qm, km, vm, om, dev, s);
+    return mode == kModeFwd ? launch_one<64, kModeFwd>(a, qm, km, vm, om, dev, s)
+                            : launch_one<64, kModeSummary>(a, qm, km, vm, om, dev, s);
 }
 
 }  // namespace la

@@ -76,6 +76,7 @@ struct ChunkArgs {
     int32_t s0_bf16;
     uint16_t* o;                     // [T, HO, V] bf16 bits (fwd)
     int64_t o_st, o_sh;
+    int32_t o_tma;                   // o is 16-byte aligned with strides in 16-byte units: full chunks go out by TMA
     float* final_state;              // fwd: final state; summary: end state
     void* ckpt;                      // [R, HO, K, V]
     int32_t ckpt_bf16;
@@ -101,7 +102,7 @@ struct ChunkArgs {
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t s);
 cudaError_t launch_chunk_kernel(const ChunkArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
-                                const CUtensorMap& vmap, int mode, cudaStream_t s);
+                                const CUtensorMap& vmap, const CUtensorMap& omap, int mode, cudaStream_t s);
 int chunk_kernel_grid(int device, int64_t num_units);
 
 }  // namespace la

@@ -200,10 +200,11 @@ la_status run(const Common& c, ChunkArgs& ka, const void* q, int64_t q_st, int64
     }
     if (ka.num_units == 0) return LA_OK;
 
-    CUtensorMap qm, km, vm;
+    CUtensorMap qm, km, vm, om;
     std::memset(&qm, 0, sizeof(qm));
     std::memset(&km, 0, sizeof(km));
     std::memset(&vm, 0, sizeof(vm));
+    std::memset(&om, 0, sizeof(om));
     const int64_t Tm = c.T > 0 ? c.T : 1;  // descriptors need a non-empty extent
     if (c.T > 0) {
         if ((st = make_map(&km, k, Tm, c.HK, c.K, k_st, k_sh)) != LA_OK) return st;
@@ -213,11 +214,17 @@ la_status run(const Common& c, ChunkArgs& ka, const void* q, int64_t q_st, int64
         } else {
             qm = km;
         }
+        // o goes out by TMA stores when its layout allows (16-byte base and strides); otherwise
+        // the kernel stores it element by element
+        ka.o_tma = 0;
+        if (ka.o && aligned(ka.o, 16) && ka.o_st % 8 == 0 && (c.HV == 1 || ka.o_sh % 8 == 0) &&
+            make_map(&om, ka.o, Tm, c.HV, c.V, ka.o_st, ka.o_sh) == LA_OK)
+            ka.o_tma = 1;
     }
     cudaEvent_t ev0 = t_timing_start, ev1 = t_timing_stop;
     t_timing_start = t_timing_stop = nullptr;
     if (ev0 && cudaEventRecord(ev0, stream) != cudaSuccess) return LA_ERR_CUDA;
-    if (la::launch_chunk_kernel(ka, qm, km, vm, mode, stream) != cudaSuccess) return LA_ERR_CUDA;
+    if (la::launch_chunk_kernel(ka, qm, km, vm, om, mode, stream) != cudaSuccess) return LA_ERR_CUDA;
     if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess) return LA_ERR_CUDA;
     return LA_OK;
 }
