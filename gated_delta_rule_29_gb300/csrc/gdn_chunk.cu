@@ -132,85 +132,103 @@ __device__ __forceinline__ void store8_split(uint8_t* hi, uint8_t* lo, const flo
     if (lo) *reinterpret_cast<uint4*>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
+// One off-diagonal block of T = (I + A)^{-1}, on tf32 warp MMAs (one warp, 16 x 16 result):
+//   T[bj + D][bj] = -T[bj + D][bj + D] * sum_{m = bj}^{bj + D - 1} A[bj + D][m] T[m][bj]
+// (16-row block indices).  It reads only T blocks of column bj computed earlier by the same
+// warp and the diagonal block T[bj + D][bj + D], so consecutive stages of one warp need no
+// block-wide barrier.  The k loops have compile-time lengths so every operand load can be
+// issued ahead of the products.
+template <int D>
+__device__ __forceinline__ void solve_stage(const float* M, float* Tf, float* Y, int bj, int g, int q) {
+    const int r0 = 16 * (bj + D), c0 = 16 * bj;
+    float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    uint32_t af[2 * D][4], bf[2 * D][2][2];
+#pragma unroll
+    for (int s = 0; s < 2 * D; ++s) {
+        const int m0 = c0 + 8 * s;
+        af[s][0] = to_tf32(M[midx(r0 + g, m0 + q)]);
+        af[s][1] = to_tf32(M[midx(r0 + g + 8, m0 + q)]);
+        af[s][2] = to_tf32(M[midx(r0 + g, m0 + q + 4)]);
+        af[s][3] = to_tf32(M[midx(r0 + g + 8, m0 + q + 4)]);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            bf[s][nt][0] = to_tf32(Tf[midx(m0 + q, c0 + 8 * nt + g)]);
+            bf[s][nt][1] = to_tf32(Tf[midx(m0 + q + 4, c0 + 8 * nt + g)]);
+        }
+    }
+#pragma unroll
+    for (int s = 0; s < 2 * D; ++s)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) mma_tf32_16x8x8(y[nt], af[s], bf[s][nt]);
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        Y[g * 16 + 8 * nt + 2 * q] = y[nt][0];
+        Y[g * 16 + 8 * nt + 2 * q + 1] = y[nt][1];
+        Y[(g + 8) * 16 + 8 * nt + 2 * q] = y[nt][2];
+        Y[(g + 8) * 16 + 8 * nt + 2 * q + 1] = y[nt][3];
+    }
+    __syncwarp();
+    float o[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+    for (int k0 = 0; k0 < 16; k0 += 8) {
+        const uint32_t a[4] = {to_tf32(Tf[midx(r0 + g, r0 + k0 + q)]), to_tf32(Tf[midx(r0 + g + 8, r0 + k0 + q)]),
+                               to_tf32(Tf[midx(r0 + g, r0 + k0 + q + 4)]),
+                               to_tf32(Tf[midx(r0 + g + 8, r0 + k0 + q + 4)])};
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const uint32_t b[2] = {to_tf32(Y[(k0 + q) * 16 + 8 * nt + g]), to_tf32(Y[(k0 + q + 4) * 16 + 8 * nt + g])};
+            mma_tf32_16x8x8(o[nt], a, b);
+        }
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const int cc = c0 + 8 * nt + 2 * q;
+        Tf[midx(r0 + g, cc)] = -o[nt][0];
+        Tf[midx(r0 + g, cc + 1)] = -o[nt][1];
+        Tf[midx(r0 + g + 8, cc)] = -o[nt][2];
+        Tf[midx(r0 + g + 8, cc + 1)] = -o[nt][3];
+    }
+    __syncwarp();
+}
+
 // T = (I + A)^{-1} for the strictly lower-triangular A held (fp32) in the packed buffer M.
-// T is written explicitly, zeros above the diagonal and ones on it, into Tf (fp32
-// [64][64], same swizzle).  128 threads.
+// T's blocks on and below the diagonal are written (fp32 [64][64], same swizzle) into Tf;
+// the blocks above it are never written (the caller writes zeros there).  128 threads.
 //   diagonal 16 x 16 blocks: right-looking substitution, one warp per block, lane =
-//   column (each step updates all later rows at once, so the FMAs are independent);
-//   T[bi][bj] = -T[bi][bi] * sum_{m = bj}^{bi - 1} A[bi][m] T[m][bj] for block distance
-//   d = bi - bj = 1, 2, 3 in turn, one warp per block, on tf32 warp MMAs.
+//   column (each step updates all later rows at once, so the FMAs are independent; the
+//   next column of A is loaded while the current one is applied);
+//   then warp w computes column block w below the diagonal, T[w + 1][w], T[w + 2][w], ...
+//   in order (solve_stage), with no block-wide barrier between the stages.
 __device__ void solve_unit_lower(const float* M, float* Tf, float (*Ys)[256], int tid) {
     const int warp = tid >> 5, lane = tid & 31;
-    // zero the six blocks above the block diagonal
-    for (int e = tid; e < 6 * 256; e += kCta) {
-        const int blk = e >> 8, i = (e >> 4) & 15, j = e & 15;
-        const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-        const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-        Tf[midx(16 * bi + i, 16 * bj + j)] = 0.f;
-    }
     if (lane < 16) {
         const int o = 16 * warp, c = lane;
-        float acc[16];
+        float acc[16], col[16], nxt[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) acc[i] = 0.f;
 #pragma unroll
+        for (int i = 1; i < 16; ++i) col[i] = M[midx(o + i, o)];
+#pragma unroll
         for (int j = 0; j < 16; ++j) {
+            if (j + 1 < 16) {
+#pragma unroll
+                for (int i = j + 2; i < 16; ++i) nxt[i] = M[midx(o + i, o + j + 1)];
+            }
             const float tj = ((j == c) ? 1.f : 0.f) - acc[j];
             Tf[midx(o + j, o + c)] = tj;
 #pragma unroll
-            for (int i = j + 1; i < 16; ++i) acc[i] = fmaf(M[midx(o + i, o + j)], tj, acc[i]);
+            for (int i = j + 1; i < 16; ++i) acc[i] = fmaf(col[i], tj, acc[i]);
+#pragma unroll
+            for (int i = j + 2; i < 16; ++i) col[i] = nxt[i];
         }
     }
     __syncthreads();
     const int g = lane >> 2, q = lane & 3;
     float* Y = Ys[warp];
-    for (int d = 1; d < 4; ++d) {
-        if (warp <= 3 - d) {
-            const int r0 = 16 * (warp + d), c0 = 16 * warp;
-            float y[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            for (int m0 = c0; m0 < r0; m0 += 8) {
-                const uint32_t a[4] = {to_tf32(M[midx(r0 + g, m0 + q)]), to_tf32(M[midx(r0 + g + 8, m0 + q)]),
-                                       to_tf32(M[midx(r0 + g, m0 + q + 4)]), to_tf32(M[midx(r0 + g + 8, m0 + q + 4)])};
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const uint32_t b[2] = {to_tf32(Tf[midx(m0 + q, c0 + 8 * nt + g)]),
-                                           to_tf32(Tf[midx(m0 + q + 4, c0 + 8 * nt + g)])};
-                    mma_tf32_16x8x8(y[nt], a, b);
-                }
-            }
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                Y[g * 16 + 8 * nt + 2 * q] = y[nt][0];
-                Y[g * 16 + 8 * nt + 2 * q + 1] = y[nt][1];
-                Y[(g + 8) * 16 + 8 * nt + 2 * q] = y[nt][2];
-                Y[(g + 8) * 16 + 8 * nt + 2 * q + 1] = y[nt][3];
-            }
-            __syncwarp();
-            float o[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-#pragma unroll
-            for (int k0 = 0; k0 < 16; k0 += 8) {
-                const uint32_t a[4] = {to_tf32(Tf[midx(r0 + g, r0 + k0 + q)]), to_tf32(Tf[midx(r0 + g + 8, r0 + k0 + q)]),
-                                       to_tf32(Tf[midx(r0 + g, r0 + k0 + q + 4)]),
-                                       to_tf32(Tf[midx(r0 + g + 8, r0 + k0 + q + 4)])};
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const uint32_t b[2] = {to_tf32(Y[(k0 + q) * 16 + 8 * nt + g]),
-                                           to_tf32(Y[(k0 + q + 4) * 16 + 8 * nt + g])};
-                    mma_tf32_16x8x8(o[nt], a, b);
-                }
-            }
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int cc = c0 + 8 * nt + 2 * q;
-                Tf[midx(r0 + g, cc)] = -o[nt][0];
-                Tf[midx(r0 + g, cc + 1)] = -o[nt][1];
-                Tf[midx(r0 + g + 8, cc)] = -o[nt][2];
-                Tf[midx(r0 + g + 8, cc + 1)] = -o[nt][3];
-            }
-            __syncwarp();
-        }
-        __syncthreads();
-    }
+    if (warp <= 2) solve_stage<1>(M, Tf, Y, warp, g, q);
+    if (warp <= 1) solve_stage<2>(M, Tf, Y, warp, g, q);
+    if (warp == 0) solve_stage<3>(M, Tf, Y, warp, g, q);
+    __syncthreads();
 }
 
 template <int KD, int MODE>
@@ -626,6 +644,11 @@ __global__ void __launch_bounds__(kCta, 2)
 #pragma unroll
                 for (int cc4 = 0; cc4 < 4; ++cc4) {
                     const int cc = (tid & 1) * 4 + cc4;
+                    if ((cc >> 1) > (i >> 4)) {
+                        // a block above the diagonal: zeros
+                        *reinterpret_cast<uint4*>(TB + sw128_off(i, cc)) = make_uint4(0u, 0u, 0u, 0u);
+                        continue;
+                    }
                     const float4 lo4 = *reinterpret_cast<const float4*>(&Tf[midx(i, 8 * cc)]);
                     const float4 hi4 = *reinterpret_cast<const float4*>(&Tf[midx(i, 8 * cc + 4)]);
                     const float x[8] = {lo4.x, lo4.y, lo4.z, lo4.w, hi4.x, hi4.y, hi4.z, hi4.w};
