@@ -61,7 +61,7 @@ constexpr uint32_t TMEM_COLS = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kFastRange = 100.f;  // factorised decays when |b_i - b_31| <= this (log2 units)
 
-struct Scalars {
+struct __align__(16) Scalars {
     float b[64];    // chunk-local inclusive cumsum of g * log2(e)
     float bw[64];   // per-warp partial scans
     float rk[64];   // inverse key norms (0 on rows past the sequence end)
@@ -87,6 +87,13 @@ __device__ __forceinline__ int midx(int r, int c) { return r * 64 + ((((c >> 2) 
 __device__ __forceinline__ uint32_t pack_bf16(float x0, float x1) {
     __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
     return *reinterpret_cast<uint32_t*>(&h);
+}
+// Eight consecutive floats of a 16-byte-aligned shared array, as two vector loads.
+__device__ __forceinline__ void ld8(float* dst, const float* src) {
+    const float4 a = *reinterpret_cast<const float4*>(src);
+    const float4 b = *reinterpret_cast<const float4*>(src + 4);
+    dst[0] = a.x; dst[1] = a.y; dst[2] = a.z; dst[3] = a.w;
+    dst[4] = b.x; dst[5] = b.y; dst[6] = b.z; dst[7] = b.w;
 }
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -524,8 +531,11 @@ __global__ void __launch_bounds__(kCta, 2)
                 for (int p = 0; p < 4; ++p) {
                     float* gv = &g64[16 * p];
                     if (fast) {
+                        float uv[16];
+                        ld8(uv, &sc.u[16 * p]);
+                        ld8(uv + 8, &sc.u[16 * p + 8]);
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) gv[e] *= ci * sc.u[16 * p + e];
+                        for (int e = 0; e < 16; ++e) gv[e] *= ci * uv[e];
                     } else {
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
@@ -623,14 +633,16 @@ __global__ void __launch_bounds__(kCta, 2)
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         const int cc = 2 * p + hh;
-                        float x[8];
+                        float x[8], bt[8], sxv[8];
+                        ld8(bt, &sc.bet[8 * cc]);
+                        ld8(sxv, &sc.sx[8 * cc]);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
                             const int j = 8 * cc + e;
                             const float vv = has_v
                                 ? bf16_bits_to_f(*reinterpret_cast<const uint16_t*>(vcol + sw128_off(j, vchunk)))
                                 : 0.f;
-                            x[e] = sc.bet[j] * vv - sc.sx[j] * ks[8 * hh + e];
+                            x[e] = bt[e] * vv - sxv[e] * ks[8 * hh + e];
                         }
                         store8_split(WB + sw128_off(v, cc), WB + 16384 + sw128_off(v, cc), x);
                     }
@@ -704,9 +716,10 @@ __global__ void __launch_bounds__(kCta, 2)
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
                         const int cc = 2 * p + hh;
-                        float x[8];
+                        float x[8], sdv[8];
+                        ld8(sdv, &sc.sd[8 * cc]);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) x[e] = sc.sd[8 * cc + e] * dd[8 * hh + e];
+                        for (int e = 0; e < 8; ++e) x[e] = sdv[e] * dd[8 * hh + e];
                         if (kFwd) store8_split(DT + sw128_off(v, cc), nullptr, &dd[8 * hh]);
                         store8_split(WB + sw128_off(v, cc), WB + 16384 + sw128_off(v, cc), x);
                     }
