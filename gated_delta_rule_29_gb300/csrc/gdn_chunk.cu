@@ -139,6 +139,43 @@ __device__ __forceinline__ void store8_split(uint8_t* hi, uint8_t* lo, const flo
     if (lo) *reinterpret_cast<uint4*>(lo) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
+// y (16 x 16, as two m16n8 accumulator fragments) = sum over KS steps of 8 of
+// la(row, m) * lb(m, col), on tf32 warp MMAs; every operand is loaded before the products.
+template <int KS, class LA, class LB>
+__device__ __forceinline__ void mma16x16(float (&y)[2][4], LA la, LB lb, int g, int q) {
+    uint32_t af[KS][4], bf[KS][2][2];
+#pragma unroll
+    for (int s = 0; s < KS; ++s) {
+        const int m0 = 8 * s;
+        af[s][0] = to_tf32(la(g, m0 + q));
+        af[s][1] = to_tf32(la(g + 8, m0 + q));
+        af[s][2] = to_tf32(la(g, m0 + q + 4));
+        af[s][3] = to_tf32(la(g + 8, m0 + q + 4));
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            bf[s][nt][0] = to_tf32(lb(m0 + q, 8 * nt + g));
+            bf[s][nt][1] = to_tf32(lb(m0 + q + 4, 8 * nt + g));
+        }
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) y[nt][0] = y[nt][1] = y[nt][2] = y[nt][3] = 0.f;
+#pragma unroll
+    for (int s = 0; s < KS; ++s)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) mma_tf32_16x8x8(y[nt], af[s], bf[s][nt]);
+}
+
+// A 16 x 16 accumulator (two m16n8 fragments) into a row-major 16 x 16 scratch tile.
+__device__ __forceinline__ void store_frag16(float* Y, const float (&y)[2][4], int g, int q) {
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        Y[g * 16 + 8 * nt + 2 * q] = y[nt][0];
+        Y[g * 16 + 8 * nt + 2 * q + 1] = y[nt][1];
+        Y[(g + 8) * 16 + 8 * nt + 2 * q] = y[nt][2];
+        Y[(g + 8) * 16 + 8 * nt + 2 * q + 1] = y[nt][3];
+    }
+}
+
 // One off-diagonal block of T = (I + A)^{-1}, on tf32 warp MMAs (one warp, 16 x 16 result):
 //   T[bj + D][bj] = -T[bj + D][bj + D] * sum_{m = bj}^{bj + D - 1} A[bj + D][m] T[m][bj]
 // (16-row block indices).  It reads only T blocks of column bj computed earlier by the same
@@ -204,8 +241,8 @@ __device__ __forceinline__ void solve_stage(const float* M, float* Tf, float* Y,
 //   diagonal 16 x 16 blocks: right-looking substitution, one warp per block, lane =
 //   column (each step updates all later rows at once, so the FMAs are independent; the
 //   next column of A is loaded while the current one is applied);
-//   then warp w computes column block w below the diagonal, T[w + 1][w], T[w + 2][w], ...
-//   in order (solve_stage), with no block-wide barrier between the stages.
+//   then by doubling: the two 32 x 32 diagonal blocks (T[1][0], T[3][2]: solve_stage), and
+//   the 32 x 32 block below them, T_BA = -T_BB A_BA T_AA, as two products over all four warps.
 __device__ void solve_unit_lower(const float* M, float* Tf, float (*Ys)[256], int tid) {
     const int warp = tid >> 5, lane = tid & 31;
     if (lane < 16) {
@@ -231,10 +268,40 @@ __device__ void solve_unit_lower(const float* M, float* Tf, float (*Ys)[256], in
     }
     __syncthreads();
     const int g = lane >> 2, q = lane & 3;
-    float* Y = Ys[warp];
-    if (warp <= 2) solve_stage<1>(M, Tf, Y, warp, g, q);
-    if (warp <= 1) solve_stage<2>(M, Tf, Y, warp, g, q);
-    if (warp == 0) solve_stage<3>(M, Tf, Y, warp, g, q);
+    // 32 x 32 diagonal blocks: T[1][0] (warp 0) and T[3][2] (warp 1)
+    if (warp <= 1) solve_stage<1>(M, Tf, Ys[warp], 2 * warp, g, q);
+    __syncthreads();
+    // the 32 x 32 block below them, T_BA = -T_BB A_BA T_AA (A = rows 0-31, B = rows 32-63), as
+    // 2 x 2 blocks of 16: warp (i, j) forms Y[i][j] = sum_m A[32 + 16 i ..][m] T[m][16 j ..]
+    // over m = 16 j .. 31 (T_AA is block lower triangular) ...
+    const int bi = warp >> 1, bj = warp & 1;
+    {
+        float y[2][4];
+        const int r0 = 32 + 16 * bi, c0 = 16 * bj;
+        auto la = [&](int r, int m) { return M[midx(r0 + r, c0 + m)]; };
+        auto lb = [&](int m, int c) { return Tf[midx(c0 + m, c0 + c)]; };
+        if (bj == 0) mma16x16<4>(y, la, lb, g, q);
+        else mma16x16<2>(y, la, lb, g, q);
+        store_frag16(Ys[warp], y, g, q);
+    }
+    __syncthreads();
+    // ... then T[32 + 16 i ..][16 j ..] = -sum_{k <= i} T[32 + 16 i ..][32 + 16 k ..] Y[k][j]
+    {
+        float z[2][4];
+        const int r0 = 32 + 16 * bi;
+        auto la = [&](int r, int m) { return Tf[midx(r0 + r, 32 + m)]; };
+        auto lb = [&](int m, int c) { return Ys[(m >> 4) * 2 + bj][(m & 15) * 16 + c]; };
+        if (bi == 0) mma16x16<2>(z, la, lb, g, q);
+        else mma16x16<4>(z, la, lb, g, q);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const int cc = 16 * bj + 8 * nt + 2 * q;
+            Tf[midx(r0 + g, cc)] = -z[nt][0];
+            Tf[midx(r0 + g, cc + 1)] = -z[nt][1];
+            Tf[midx(r0 + g + 8, cc)] = -z[nt][2];
+            Tf[midx(r0 + g + 8, cc + 1)] = -z[nt][3];
+        }
+    }
     __syncthreads();
 }
 
