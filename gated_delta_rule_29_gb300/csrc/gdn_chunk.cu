@@ -238,32 +238,70 @@ __device__ __forceinline__ void solve_stage(const float* M, float* Tf, float* Y,
 // T = (I + A)^{-1} for the strictly lower-triangular A held (fp32) in the packed buffer M.
 // T's blocks on and below the diagonal are written (fp32 [64][64], same swizzle) into Tf;
 // the blocks above it are never written (the caller writes zeros there).  128 threads.
-//   diagonal 16 x 16 blocks: right-looking substitution, one warp per block, lane =
-//   column (each step updates all later rows at once, so the FMAs are independent; the
-//   next column of A is loaded while the current one is applied);
+//   diagonal 16 x 16 blocks, one warp per block: 8 x 8 diagonal blocks by right-looking
+//   substitution (lane = column; each step updates all later rows at once, and the next
+//   column of A is loaded while the current one is applied), then the 8 x 8 block below;
 //   then by doubling: the two 32 x 32 diagonal blocks (T[1][0], T[3][2]: solve_stage), and
 //   the 32 x 32 block below them, T_BA = -T_BB A_BA T_AA, as two products over all four warps.
 __device__ void solve_unit_lower(const float* M, float* Tf, float (*Ys)[256], int tid) {
     const int warp = tid >> 5, lane = tid & 31;
-    if (lane < 16) {
-        const int o = 16 * warp, c = lane;
-        float acc[16], col[16], nxt[16];
+    {
+        // diagonal 16 x 16 block o of warp w, itself by doubling: its two 8 x 8 diagonal blocks by
+        // substitution (lanes 0-7 and 8-15, lane = column), then the lower-left 8 x 8 block
+        // T10 = -T11 A10 T00 on all 32 lanes; lanes 16-31 meanwhile clear the upper-right block
+        const int o = 16 * warp;
+        if (lane < 16) {
+            const int b = o + 8 * (lane >> 3), c = lane & 7;
+            float acc[8], col[8], nxt[8];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+            for (int i = 0; i < 8; ++i) acc[i] = 0.f;
 #pragma unroll
-        for (int i = 1; i < 16; ++i) col[i] = M[midx(o + i, o)];
+            for (int i = 1; i < 8; ++i) col[i] = M[midx(b + i, b)];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            if (j + 1 < 16) {
+            for (int j = 0; j < 8; ++j) {
 #pragma unroll
-                for (int i = j + 2; i < 16; ++i) nxt[i] = M[midx(o + i, o + j + 1)];
+                for (int i = j + 2; i < 8; ++i) nxt[i] = M[midx(b + i, b + j + 1)];
+                const float tj = ((j == c) ? 1.f : 0.f) - acc[j];
+                Tf[midx(b + j, b + c)] = tj;
+#pragma unroll
+                for (int i = j + 1; i < 8; ++i) acc[i] = fmaf(col[i], tj, acc[i]);
+#pragma unroll
+                for (int i = j + 2; i < 8; ++i) col[i] = nxt[i];
             }
-            const float tj = ((j == c) ? 1.f : 0.f) - acc[j];
-            Tf[midx(o + j, o + c)] = tj;
+        } else {
 #pragma unroll
-            for (int i = j + 1; i < 16; ++i) acc[i] = fmaf(col[i], tj, acc[i]);
+            for (int e = 0; e < 4; ++e) {
+                const int idx = (lane - 16) * 4 + e;  // 0 .. 63
+                Tf[midx(o + (idx >> 3), o + 8 + (idx & 7))] = 0.f;
+            }
+        }
+        __syncwarp();
+        float* Y = Ys[warp];
+        const int i = lane >> 2, c = 2 * (lane & 3);
+        {
+            float a8[8], y0 = 0.f, y1 = 0.f;
 #pragma unroll
-            for (int i = j + 2; i < 16; ++i) col[i] = nxt[i];
+            for (int m = 0; m < 8; ++m) a8[m] = M[midx(o + 8 + i, o + m)];
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                y0 = fmaf(a8[m], Tf[midx(o + m, o + c)], y0);
+                y1 = fmaf(a8[m], Tf[midx(o + m, o + c + 1)], y1);
+            }
+            Y[i * 8 + c] = y0;
+            Y[i * 8 + c + 1] = y1;
+        }
+        __syncwarp();
+        {
+            float t8[8], z0 = 0.f, z1 = 0.f;
+#pragma unroll
+            for (int m = 0; m < 8; ++m) t8[m] = Tf[midx(o + 8 + i, o + 8 + m)];
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                z0 = fmaf(t8[m], Y[m * 8 + c], z0);
+                z1 = fmaf(t8[m], Y[m * 8 + c + 1], z1);
+            }
+            Tf[midx(o + 8 + i, o + c)] = -z0;
+            Tf[midx(o + 8 + i, o + c + 1)] = -z1;
         }
     }
     __syncthreads();
