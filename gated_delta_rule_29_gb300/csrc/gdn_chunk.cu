@@ -55,7 +55,7 @@ __host__ __device__ constexpr uint32_t smem_alloc(int mode) {
 // TMEM columns (fp32, 128 lanes)
 constexpr uint32_t COL_S = 0;     // S^T (K columns)
 constexpr uint32_t COL_R1 = 128;  // G (128 columns with R2) -> (K S)^T -> D^T
-constexpr uint32_t COL_R2 = 192;  // (Q' S)^T, then += D^T P^T = O^T
+constexpr uint32_t COL_R2 = 192;  // (Q S)^T, scaled per query row in place, then += D^T P^T = O^T
 constexpr uint32_t TMEM_COLS = 256;
 
 constexpr float kLog2e = 1.4426950408889634f;
@@ -603,7 +603,29 @@ __global__ void __launch_bounds__(kCta, 2)
                 if (r < 64) sc.rk[row] = inv;
                 else sc.rq[row] = inv;
             }
+            tc_fence_before();
             if (__syncthreads_or(!ok)) { failed = true; break; }
+            // ---- S3: (K S)^T and (Q S)^T = S^T [K; Q]^T, issued as soon as every thread holds its row of
+            // G (the product reuses G's columns); it runs while the scalars and A / P are formed
+            if (tid == 0) {
+                tc_fence_after();
+                const uint32_t idesc = idesc_bf16_f32(128, kFwd ? 128 : 64, false, false);
+#pragma unroll
+                for (int kk = 0; kk < KD / 16; ++kk) {
+                    const uint64_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                    umma_bf16(tmem + COL_R1, d_wb + off, d_kq + off, idesc, kk > 0);
+                }
+                if (!kFwd) {
+#pragma unroll
+                    for (int kk = 0; kk < KD / 16; ++kk) {
+                        const uint64_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                        umma_bf16(tmem + COL_R1, d_slo + off, d_kq + off, idesc, 1u);
+                    }
+                }
+                umma_commit(&sc.bar_mma);
+            }
+            pend_mma = true;
+
             bool in_range = true;
             if (tid < 64) {
                 const int i = tid;
@@ -626,7 +648,7 @@ __global__ void __launch_bounds__(kCta, 2)
             }
             const bool fast = __syncthreads_and(in_range) != 0;
 
-            // ---- S2: A (fp32, for the solve) and P (bf16) from G; Q' = (scale rq gamma) Q in place
+            // ---- S2: A (fp32, for the solve) and P (bf16) from G
             if (r < 64 || kFwd) {
                 const int i = r & 63;
                 const bool is_a = r < 64;
@@ -669,44 +691,9 @@ __global__ void __launch_bounds__(kCta, 2)
                     }
                 }
             }
-            if (kFwd) {
-                constexpr int kQChunks = 64 * (KD / 8);
-#pragma unroll 2
-                for (int e = tid; e < kQChunks; e += kCta) {
-                    const int row = e / (KD / 8), cc = e % (KD / 8);
-                    uint4* p = reinterpret_cast<uint4*>(KQ + (cc >> 3) * 16384 + (64 + row) * 128 + (cc & 7) * 16);
-                    const float f = sc.sq[row];
-                    uint4 w = *p;
-                    w.x = pack_bf16(bf16_lo(w.x) * f, bf16_hi(w.x) * f);
-                    w.y = pack_bf16(bf16_lo(w.y) * f, bf16_hi(w.y) * f);
-                    w.z = pack_bf16(bf16_lo(w.z) * f, bf16_hi(w.z) * f);
-                    w.w = pack_bf16(bf16_lo(w.w) * f, bf16_hi(w.w) * f);
-                    *p = w;
-                }
-            }
             fence_proxy_async_smem();
             tc_fence_before();
             if (__syncthreads_or(!ok)) { failed = true; break; }
-
-            // ---- S3: (K S)^T and (Q' S)^T = S^T [K; Q']^T
-            if (tid == 0) {
-                tc_fence_after();
-                const uint32_t idesc = idesc_bf16_f32(128, kFwd ? 128 : 64, false, false);
-#pragma unroll
-                for (int kk = 0; kk < KD / 16; ++kk) {
-                    const uint64_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                    umma_bf16(tmem + COL_R1, d_wb + off, d_kq + off, idesc, kk > 0);
-                }
-                if (!kFwd) {
-#pragma unroll
-                    for (int kk = 0; kk < KD / 16; ++kk) {
-                        const uint64_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                        umma_bf16(tmem + COL_R1, d_slo + off, d_kq + off, idesc, 1u);
-                    }
-                }
-                umma_commit(&sc.bar_mma);
-            }
-            pend_mma = true;
 
             // ---- S4: X^T = beta V^T - sx (K S)^T (hi + lo); then T = (I + A)^{-1} in the V tile's space
             ok = mbar_wait(&sc.bar_mma, ph_mma, budget);
@@ -752,6 +739,22 @@ __global__ void __launch_bounds__(kCta, 2)
                         store8_split(WB + sw128_off(v, cc), WB + 16384 + sw128_off(v, cc), x);
                     }
                 }
+            }
+            if (kFwd) {
+                // (Q S)^T -> (scale rq gamma) (Q S)^T in place: column i is query row i
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    float qs[16], f[16];
+                    tmem_ld16(trow + COL_R2 + 16 * p, qs);
+                    ld8(f, &sc.sq[16 * p]);
+                    ld8(f + 8, &sc.sq[16 * p + 8]);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) qs[e] *= f[e];
+                    tmem_st16(trow + COL_R2 + 16 * p, qs);
+                }
+                tmem_wait_st();
+                tc_fence_before();
             }
             __syncthreads();  // every V read is done before T takes the tile's space
             solve_unit_lower(M, Tf, sc.Y, tid);
