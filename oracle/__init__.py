@@ -49,6 +49,7 @@ MUTATIONS = {
     10: "softplus gate rate a_log instead of exp(a_log)",
     11: "beta sigmoid of the negated logit",
     12: "bounded gate without the sigmoid",
+    13: "state pool written back to slot i instead of state_indices[i]",
 }
 
 
@@ -170,7 +171,8 @@ def beta_transform(beta, *, beta_sigmoid=False, mutation=0):
 def gdn_fwd(q, k, v, g, beta, cu_seqlens, *, scale=None, use_qk_l2norm=True,
             initial_state=None, output_final_state=True, checkpoint_every_n=0,
             want_o=True, unit_mask=None, nthreads=None, mutation=0,
-            gate="log", a_log=None, dt_bias=None, gate_lower_bound=None, beta_sigmoid=False):
+            gate="log", a_log=None, dt_bias=None, gate_lower_bound=None, beta_sigmoid=False,
+            state_indices=None):
     """fp64 forward: returns dict(o [T,HO,V], final_state [N,HO,K,V], checkpoints [R,HO,K,V]).
 
     q, k: [T, HK, K]; v: [T, HV, V]; g, beta: [T, HO] (g in natural-log space unless a gate
@@ -178,16 +180,36 @@ def gdn_fwd(q, k, v, g, beta, cu_seqlens, *, scale=None, use_qk_l2norm=True,
     initial_state: [N, HO, K, V] or None (zero start).
     scale defaults to 1/sqrt(K) and multiplies the (normalised) query.
     unit_mask: optional bool [N, HO]; unmarked units are left at zero.
+
+    state_indices ([N] ints; cuDNN page, "States and checkpoints"): initial_state is then a
+    pool [N_pool, HO, K, V]; sequence i starts from pool[state_indices[i]] and its end state
+    is written back to that slot.  The result then also holds "state_pool", the pool after
+    the write-back (untouched slots unchanged).  Exclusive with checkpoints.
     """
     g = gate_transform(g, gate=gate, a_log=a_log, dt_bias=dt_bias, gate_lower_bound=gate_lower_bound,
                        mutation=mutation)
     beta = beta_transform(beta, beta_sigmoid=beta_sigmoid, mutation=mutation)
-    mutation = mutation if mutation < 9 else 0
-    return _run(q, k, v, g, beta, cu_seqlens, scale=scale, use_qk_l2norm=use_qk_l2norm,
-                s0=initial_state, want_final=output_final_state,
-                checkpoint_every_n=checkpoint_every_n, want_o=want_o,
-                want_transition=False, unit_mask=unit_mask, nthreads=nthreads,
-                mutation=mutation)
+    pool = idx = None
+    if state_indices is not None:
+        if checkpoint_every_n:
+            raise ValueError("state_indices and checkpoints are exclusive")
+        pool = _f64(initial_state)
+        idx = _i64(state_indices)
+        if idx.shape != (_i64(cu_seqlens).shape[0] - 1,) or (idx < 0).any() or (idx >= pool.shape[0]).any():
+            raise ValueError("state_indices must hold one slot in [0, N_pool) per sequence")
+        initial_state = pool[idx]
+        output_final_state = True
+    r = _run(q, k, v, g, beta, cu_seqlens, scale=scale, use_qk_l2norm=use_qk_l2norm,
+             s0=initial_state, want_final=output_final_state,
+             checkpoint_every_n=checkpoint_every_n, want_o=want_o,
+             want_transition=False, unit_mask=unit_mask, nthreads=nthreads,
+             mutation=mutation if mutation < 9 else 0)
+    if pool is not None:
+        out = pool.copy()
+        dst = np.arange(idx.shape[0]) if mutation == 13 else idx
+        out[dst] = r["final_state"]
+        r["state_pool"] = out
+    return r
 
 
 def gdn_summary(k, v, g, beta, cu_seqlens, *, use_qk_l2norm=True, start_state=None,

@@ -14,7 +14,9 @@ Every check below is an independent statement of what the Gated DeltaNet forward
   * state round trip: [0, m) then [m, L) equals the unsplit run;
   * empty sequences;
   * the optional input transforms (softplus gate, bounded sigmoid gate, beta
-    sigmoid) at arguments where they take exact values (ln 2, 1, 1/2, 3/4).
+    sigmoid) at arguments where they take exact values (ln 2, 1, 1/2, 3/4);
+  * the state pool (state_indices): one-token updates against the explicit
+    factor form, written back to the named slots, other slots untouched.
 test_planted_mistakes_are_caught plants each of the oracle's known mutations
 and requires at least one check to fail, so a plausible slip anywhere (a dropped
 term, a flipped sign, a wrong index or orientation) cannot pass unnoticed.
@@ -355,6 +357,34 @@ def check_beta_sigmoid(mutation=0):
     return max(_rel(r["o"][0, 0], 0.75 * v[0, 0]), _rel(r["final_state"][0, 0], expect_S))
 
 
+def check_state_pool(mutation=0):
+    """Decode from a state pool: N sequences of one token each start from pool[state_indices[i]]
+    and write back there.  Each update is checked against the explicit one-token form
+    S' = e^g (I - beta k k^T) S + beta k v^T, o = scale S'^T q (no norm), and the slots that
+    no sequence names must come back unchanged."""
+    rng = np.random.default_rng(97)
+    N, P, HV, K, V = 3, 5, 2, 4, 3
+    idx = np.array([3, 0, 4])
+    q = rng.standard_normal((N, 1, K))
+    k = rng.standard_normal((N, 1, K))
+    v = rng.standard_normal((N, HV, V))
+    g = -0.1 * rng.random((N, HV))
+    beta = rng.random((N, HV))
+    pool = rng.standard_normal((P, HV, K, V))
+    r = oracle.gdn_fwd(q, k, v, g, beta, np.arange(N + 1), scale=0.7, use_qk_l2norm=False,
+                       initial_state=pool, state_indices=idx, mutation=mutation)
+    errs = []
+    for i in range(N):
+        for h in range(HV):
+            kk = k[i, 0]
+            S1 = math.exp(g[i, h]) * (np.eye(K) - beta[i, h] * np.outer(kk, kk)) @ pool[idx[i], h] \
+                + beta[i, h] * np.outer(kk, v[i, h])
+            errs.append(_rel(r["state_pool"][idx[i], h], S1))
+            errs.append(_rel(r["o"][i, h], 0.7 * S1.T @ q[i, 0]))
+    errs.append(float(np.abs(r["state_pool"][[1, 2]] - pool[[1, 2]]).max()))
+    return max(errs)
+
+
 CHECKS = {
     "golden": (check_golden, 1e-12),
     "brute_force": (check_brute_force, 1e-12),
@@ -371,6 +401,7 @@ CHECKS = {
     "gate_softplus": (check_gate_softplus, 1e-12),
     "gate_sigmoid_bound": (check_gate_sigmoid_bound, 1e-12),
     "beta_sigmoid": (check_beta_sigmoid, 1e-14),
+    "state_pool": (check_state_pool, 1e-13),
 }
 
 
