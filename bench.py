@@ -377,6 +377,123 @@ def run_ours(args, world, rank, local):
     return 0
 
 
+DECODE_METRIC = "GDN decode tokens/s and % of GB300 HBM roofline (N=1024 sequences, H=32, K=V=128, fp32 state pool)"
+
+
+def run_decode(args, world, rank, local):
+    """One decode step = gdn_decode over N = 1024 sequences (one new token each), 32 heads,
+    K = V = 128, against an fp32 state pool of 2048 slots (4.3 GB) with a random slot per
+    sequence: the state is read and written once (4.3 GB of the 4.3 GB moved per step)."""
+    import gated_delta_rule_29_gb300 as la
+    from gated_delta_rule_29_gb300 import binding as B
+    from gated_delta_rule_29_gb300 import workloads as W
+
+    assert torch.cuda.is_available(), "bench needs a CUDA device (there is no CPU fallback)"
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lib = B.load()
+    N, H, K, V, P = 1024, 32, 128, 128, 2048
+    w = W.draw("decode step", [1] * N, H, H, K, V, seed=1006)
+    gen = torch.Generator().manual_seed(1007)
+    idx = torch.randperm(P, generator=gen)[:N].to(torch.int32)
+    pool = torch.empty(P, H, K, V, dtype=torch.float32, device=dev)
+    for s_ in range(0, P, 256):  # 0.1 N(0,1) states, drawn in slices on the device
+        pool[s_:s_ + 256].normal_(0.0, 0.1, generator=torch.Generator(device=dev).manual_seed(1008 + s_))
+    q, k, v, g, b, ix = (x.to(dev) for x in (w.q, w.k, w.v, w.g, w.beta, idx))
+    o = torch.empty(N, H, V, dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        la.gdn_decode(q, k, v, g, b, pool, state_indices=ix, o=o, status=status)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert la.read_status(status) == 0
+    stream = torch.cuda.current_stream()
+    k_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a_, b_ in k_ev:
+        a_.record(stream)
+        b_.record(stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(args.steps):
+            lib.la_set_kernel_timing_events(k_ev[i][0].cuda_event, k_ev[i][1].cuda_event)
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    kern_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in k_ev)
+    assert la.read_status(status) == 0
+    state_bytes = 2 * N * H * K * V * 4
+    io_bytes = N * H * (2 * K * 2 + 2 * V * 2 + 2 * 4) + N * 4
+    alg_bytes = state_bytes + io_bytes
+    hbm_peak, _, peak_src = load_peaks()
+    achieved = alg_bytes / (kern_ms * 1e-3) / 1e9
+
+    # end to end: the step's token inputs from pinned host memory, o back to pinned host memory;
+    # the pool is the serving state and stays on the device
+    host_in = [x.pin_memory() for x in (w.q, w.k, w.v, w.g, w.beta, idx)]
+    host_o = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in host_in)
+    d2h = host_o.numel() * host_o.element_size()
+
+    def e2e_step():
+        qq, kk, vv, gg, bb, ii = (x.to(dev, non_blocking=True) for x in host_in)
+        la.gdn_decode(qq, kk, vv, gg, bb, pool, state_indices=ii, o=o, status=status)
+        host_o.copy_(o, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    x0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    x1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(x0.elapsed_time(x1) / args.steps, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle  # CPU baseline only
+        cores = os.cpu_count() or 1
+        m = 256  # sequences in the sample
+        pool_s = pool[idx[:m].long().to(dev)].double().cpu().numpy()
+        t0 = time.perf_counter()
+        oracle.gdn_fwd(w.q[:m], w.k[:m], w.v[:m], w.g[:m], w.beta[:m], torch.arange(m + 1), initial_state=pool_s,
+                       state_indices=torch.arange(m), nthreads=cores)
+        dt = time.perf_counter() - t0
+        cpu = {"value": m / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{m} of {N} sequences x {H} heads, one decode step ({dt:.2f} s), fp64 C recurrence "
+                         f"on {cores} threads"}
+    if rank == 0:
+        line = {
+            "metric": DECODE_METRIC, "value": N * world / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"decode step: N={N} sequences x 1 token, H={H}, K=V={K}, fp32 state pool of "
+                                   f"{P} slots (random slot per sequence)", "global_batch": N * world,
+                       "parallelism": "single GPU" if world == 1 else f"independent pools per GPU x{world}",
+                       "l2": f"state moved per step {state_bytes / 1e9:.2f} GB > L2; no flush"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": None, "peak_source": peak_src,
+                         "kernel": "gdn_decode_kernel<128, 128>", "kernel_ms": kern_ms, "algorithmic_bytes": alg_bytes},
+            "cpu_baseline": cpu,
+            "e2e": {"value": N * world / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -389,6 +506,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--e2e-groups", type=int, default=4, help="sequence groups pipelined by gdn_fwd_host")
+    ap.add_argument("--workload", choices=["dense", "decode"], default="dense",
+                    help="dense: the chunked forward over the dense batch (the headline); "
+                         "decode: one decode step against a state pool")
     ap.add_argument("--seq-len", type=int, default=8192,
                     help="tokens per sequence of the dense batch (8192 is the benchmark workload)")
     args = ap.parse_args()
@@ -398,6 +518,8 @@ def main():
     try:
         if args.impl == "reference":
             return run_reference(args, world, rank)
+        if args.workload == "decode":
+            return run_decode(args, world, rank, local)
         return run_ours(args, world, rank, local)
     finally:
         if world > 1:

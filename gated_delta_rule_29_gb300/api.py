@@ -90,14 +90,18 @@ def gdn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
             workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
             stream: Optional[torch.cuda.Stream] = None, a_log: Optional[torch.Tensor] = None,
             dt_bias: Optional[torch.Tensor] = None, gate_lower_bound: Optional[float] = None,
-            beta_sigmoid: bool = False
+            beta_sigmoid: bool = False, state_indices: Optional[torch.Tensor] = None
             ) -> Tuple[torch.Tensor, Optional[torch.Tensor], Optional[torch.Tensor]]:
     """Chunked GDN forward.  Returns (o [T, HO, V] bf16, final_state [N, HO, K, V] fp32 or None,
     checkpoints [R, HO, K, V] or None).  Asynchronous on the current stream.
 
     g is the natural-log decay, unless a_log and dt_bias ([HO] fp32) are given (the kernel then
     uses -exp(a_log) softplus(g + dt_bias)) or gate_lower_bound (< 0; the kernel uses
-    gate_lower_bound * sigmoid(g)).  With beta_sigmoid, beta holds logits (fp32 or bf16)."""
+    gate_lower_bound * sigmoid(g)).  With beta_sigmoid, beta holds logits (fp32 or bf16).
+
+    state_indices ([N] int32): initial_state is then a contiguous state pool [P, HO, K, V]
+    (fp32 or bf16); sequence i starts from pool[state_indices[i]] and its end state is
+    written back into that slot in place.  No final_state or checkpoints are returned."""
     _check_thd("q", q, torch.bfloat16)
     _check_thd("k", k, torch.bfloat16)
     _check_thd("v", v, torch.bfloat16)
@@ -110,6 +114,14 @@ def gdn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
     dev = q.device
     if o is None:
         o = torch.empty(T, HO, V, dtype=torch.bfloat16, device=dev)
+    if state_indices is not None:
+        if initial_state is None or not initial_state.is_contiguous() or initial_state.dim() != 4:
+            raise ValueError("state_indices needs initial_state as a contiguous pool [P, HO, K, V]")
+        if state_indices.dtype != torch.int32 or state_indices.numel() != N or state_indices.device != dev:
+            raise ValueError(f"state_indices must be int32 [{N}] on {dev}")
+        if checkpoint_every_n:
+            raise ValueError("state_indices and checkpoints are exclusive")
+        output_final_state = False
     if output_final_state and final_state is None:
         final_state = torch.empty(N, HO, K, V, dtype=torch.float32, device=dev)
     if not output_final_state:
@@ -143,6 +155,8 @@ def gdn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
     p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel()
     p.status = status.data_ptr() if status is not None else None
     keep = _set_transforms(p, HO, dev, a_log, dt_bias, gate_lower_bound, beta_sigmoid, beta)  # noqa: F841
+    if state_indices is not None:
+        p.state_indices, p.state_pool_size = state_indices.data_ptr(), initial_state.shape[0]
     B.check(B.load().gdn_fwd(ctypes.byref(p), _stream_ptr(stream)), "gdn_fwd")
     return o, final_state, checkpoints
 
@@ -193,6 +207,50 @@ def gdn_summary(k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.T
     keep = _set_transforms(p, HO, dev, a_log, dt_bias, gate_lower_bound, beta_sigmoid, beta)  # noqa: F841
     B.check(B.load().gdn_summary(ctypes.byref(p), _stream_ptr(stream)), "gdn_summary")
     return end_state, transition
+
+
+def gdn_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
+               state_pool: torch.Tensor, *, state_indices: Optional[torch.Tensor] = None,
+               scale: Optional[float] = None, use_qk_l2norm: bool = True, o: Optional[torch.Tensor] = None,
+               status: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
+               a_log: Optional[torch.Tensor] = None, dt_bias: Optional[torch.Tensor] = None,
+               gate_lower_bound: Optional[float] = None, beta_sigmoid: bool = False) -> torch.Tensor:
+    """One new token for each of N sequences: q, k [N, HK, K], v [N, HV, V], g, beta [N, HO].
+    Sequence i steps the state pool[state_indices[i]] (pool[i] when state_indices is None) in
+    place and returns o [N, HO, V] bf16.  Gate and beta transforms as in gdn_fwd."""
+    _check_thd("q", q, torch.bfloat16)
+    _check_thd("k", k, torch.bfloat16)
+    _check_thd("v", v, torch.bfloat16)
+    _check_thd("g", g, torch.float32, heads_dim=False)
+    _check_beta(beta, beta_sigmoid)
+    N, HK, K = k.shape
+    HV, V = v.shape[1], v.shape[2]
+    dev = q.device
+    if state_pool.dim() != 4 or not state_pool.is_contiguous() or state_pool.shape[1:] != (HV, K, V):
+        raise ValueError(f"state_pool must be a contiguous [P, {HV}, {K}, {V}] tensor")
+    if state_pool.dtype not in (torch.float32, torch.bfloat16):
+        raise TypeError("state_pool must be float32 or bfloat16")
+    if state_indices is not None and (state_indices.dtype != torch.int32 or state_indices.numel() != N):
+        raise ValueError(f"state_indices must be int32 [{N}]")
+    if o is None:
+        o = torch.empty(N, HV, V, dtype=torch.bfloat16, device=dev)
+    p = B.GdnDecodeParams()
+    p.q, p.q_stride_n, p.q_stride_h = q.data_ptr(), q.stride(0), q.stride(1)
+    p.k, p.k_stride_n, p.k_stride_h = k.data_ptr(), k.stride(0), k.stride(1)
+    p.v, p.v_stride_n, p.v_stride_h = v.data_ptr(), v.stride(0), v.stride(1)
+    p.g, p.g_stride_n, p.g_stride_h = g.data_ptr(), g.stride(0), g.stride(1)
+    p.beta, p.beta_stride_n, p.beta_stride_h = beta.data_ptr(), beta.stride(0), beta.stride(1)
+    p.N, p.HK, p.HV, p.K, p.V = N, HK, HV, K, V
+    p.scale = float(scale) if scale is not None else 1.0 / math.sqrt(K)
+    p.use_qk_l2norm = int(bool(use_qk_l2norm))
+    p.state_pool, p.state_pool_size = state_pool.data_ptr(), state_pool.shape[0]
+    p.state_dtype = B.LA_DTYPE_BF16 if state_pool.dtype == torch.bfloat16 else B.LA_DTYPE_F32
+    p.state_indices = state_indices.data_ptr() if state_indices is not None else None
+    p.o, p.o_stride_n, p.o_stride_h = o.data_ptr(), o.stride(0), o.stride(1)
+    p.status = status.data_ptr() if status is not None else None
+    keep = _set_transforms(p, HV, dev, a_log, dt_bias, gate_lower_bound, beta_sigmoid, beta)  # noqa: F841
+    B.check(B.load().gdn_decode(ctypes.byref(p), _stream_ptr(stream)), "gdn_decode")
+    return o
 
 
 def read_status(status: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> int:

@@ -19,6 +19,7 @@ LA_ERR_CUDA = 3
 LA_ERR_BAD_SEQLENS = 4
 LA_ERR_TIMEOUT = 5
 LA_ERR_WORKSPACE = 6
+LA_ERR_BAD_STATE_INDEX = 7
 
 LA_DTYPE_BF16 = 0
 LA_DTYPE_F32 = 1
@@ -36,6 +37,7 @@ EXPORTED_SYMBOLS = (
     "la_version",
     "la_set_kernel_timing_events",
     "gdn_fwd_static_workspace",
+    "gdn_decode",
 )
 
 _i64 = ctypes.c_int64
@@ -63,6 +65,7 @@ class GdnFwdParams(ctypes.Structure):
         ("status", _vp),
         ("gate_mode", _i32), ("a_log", _vp), ("dt_bias", _vp), ("gate_lower_bound", ctypes.c_float),
         ("beta_sigmoid", _i32), ("beta_bf16", _i32),
+        ("state_indices", _vp), ("state_pool_size", _i64),
     ]
 
 
@@ -109,6 +112,8 @@ def load(build_if_missing: bool = True):
         lib = ctypes.CDLL(path)
         lib.gdn_fwd.restype = ctypes.c_int
         lib.gdn_fwd.argtypes = [ctypes.POINTER(GdnFwdParams), _vp]
+        lib.gdn_decode.restype = ctypes.c_int
+        lib.gdn_decode.argtypes = [ctypes.POINTER(GdnDecodeParams), _vp]
         lib.gdn_summary.restype = ctypes.c_int
         lib.gdn_summary.argtypes = [ctypes.POINTER(GdnSummaryParams), _vp]
         lib.la_gdn_workspace_bytes.restype = ctypes.c_size_t
@@ -127,6 +132,25 @@ def load(build_if_missing: bool = True):
         lib.gdn_fwd_static_workspace.argtypes = [ctypes.POINTER(GdnFwdParams), _vp]
         _lib = lib
         return lib
+
+
+class GdnDecodeParams(ctypes.Structure):
+    """Mirror of la_gdn_decode_params (same field order and types)."""
+    _fields_ = [
+        ("q", _vp), ("q_stride_n", _i64), ("q_stride_h", _i64),
+        ("k", _vp), ("k_stride_n", _i64), ("k_stride_h", _i64),
+        ("v", _vp), ("v_stride_n", _i64), ("v_stride_h", _i64),
+        ("g", _vp), ("g_stride_n", _i64), ("g_stride_h", _i64),
+        ("beta", _vp), ("beta_stride_n", _i64), ("beta_stride_h", _i64),
+        ("N", _i32), ("HK", _i32), ("HV", _i32), ("K", _i32), ("V", _i32),
+        ("scale", ctypes.c_float), ("use_qk_l2norm", _i32),
+        ("state_pool", _vp), ("state_dtype", _i32), ("state_pool_size", _i64),
+        ("state_indices", _vp),
+        ("o", _vp), ("o_stride_n", _i64), ("o_stride_h", _i64),
+        ("status", _vp),
+        ("gate_mode", _i32), ("a_log", _vp), ("dt_bias", _vp), ("gate_lower_bound", ctypes.c_float),
+        ("beta_sigmoid", _i32), ("beta_bf16", _i32),
+    ]
 
 
 class LinAttnError(RuntimeError):

@@ -123,6 +123,12 @@ __device__ __forceinline__ float beta_at(const ChunkArgs& a, int64_t t, int h) {
     return a.beta_sigmoid ? 1.f / (1.f + expf(-x)) : x;
 }
 
+// One element of the end state: fp32, or bf16 when it goes back into a bf16 state pool.
+__device__ __forceinline__ void store_state(const ChunkArgs& a, int64_t i, float x) {
+    if (a.final_bf16) reinterpret_cast<uint16_t*>(a.final_state)[i] = f_to_bf16_bits(x);
+    else a.final_state[i] = x;
+}
+
 __device__ __forceinline__ int64_t cu_get(const void* cu, int cu64, int64_t i) {
     return cu64 ? static_cast<const int64_t*>(cu)[i] : static_cast<int64_t>(static_cast<const int32_t*>(cu)[i]);
 }
@@ -423,6 +429,21 @@ __global__ void __launch_bounds__(kCta, 2)
         const int64_t L = cu_get(a.cu, a.cu64, seq + 1) - ts;
         const int nchunks = static_cast<int>((L + kChunk - 1) / kChunk);
         const int64_t unit_state = static_cast<int64_t>(seq) * HO + h;
+        // the start state's slot, and where the end state goes (the same pool slot when a state
+        // pool is used: written back in place)
+        int64_t s0_unit = unit_state;
+        if (a.state_idx) {
+            const int32_t slot = a.state_idx[seq];
+            if (slot < 0 || slot >= a.pool_size) {
+                if (tid == 0) {
+                    atomicCAS(&a.hdr->status, LA_OK, LA_ERR_BAD_STATE_INDEX);
+                    if (a.user_status) atomicCAS(a.user_status, LA_OK, LA_ERR_BAD_STATE_INDEX);
+                }
+                continue;
+            }
+            s0_unit = static_cast<int64_t>(slot) * HO + h;
+        }
+        const int64_t fin_unit = a.state_idx ? s0_unit : unit_state;
 
         // ---- chunk 0's gate total: the state kept in TMEM is pre-multiplied by the decay of the
         // chunk it is about to enter, so the state-update product can accumulate onto it
@@ -448,7 +469,8 @@ __global__ void __launch_bounds__(kCta, 2)
         // ---- initial state -> TMEM (fp32 2^{b_C} S^T), WB (bf16 S^T, the A operand of K S),
         // checkpoint entry 0, and the end state of an empty sequence
         {
-            const int64_t base = unit_state * KD * a.V + r;
+            const int64_t base = s0_unit * KD * a.V + r;
+            const int64_t fbase0 = fin_unit * KD * a.V + r;
             const bool ckpt0 = kFwd && a.ckpt && nchunks > 0 && r < a.V;
             const int64_t cbase = ckpt0 ? ((a.ckpt_off[seq] * HO + h) * KD) * a.V + r : 0;
 #pragma unroll 1
@@ -488,7 +510,7 @@ __global__ void __launch_bounds__(kCta, 2)
                         if (a.final_state && r < a.V)
 #pragma unroll
                             for (int e = 0; e < 16; ++e)
-                                a.final_state[base + static_cast<int64_t>(16 * p + e) * a.V] = x[e];
+                                store_state(a, fbase0 + static_cast<int64_t>(16 * p + e) * a.V, x[e]);
                     } else if (r < KD) {
                         float* tp = a.transition + (unit_state * KD + r) * KD + 16 * p;
 #pragma unroll
@@ -919,7 +941,7 @@ __global__ void __launch_bounds__(kCta, 2)
                 // new state: bf16 copy for the next K S product, end state or checkpoint entry,
                 // then pre-multiplied by the next chunk's decay for its state update
                 const float gnext = last ? 1.f : exp2f(sc.gsum[0] + sc.gsum[1]);
-                const int64_t fbase = unit_state * KD * a.V + r;
+                const int64_t fbase = fin_unit * KD * a.V + r;
                 const bool ckpt = kFwd && a.ckpt && !last && (static_cast<int64_t>(c + 1) * kChunk) % a.ckpt_n == 0 &&
                                   r < a.V;
                 const int64_t cbase =
@@ -949,7 +971,7 @@ __global__ void __launch_bounds__(kCta, 2)
                                 if (a.final_state && r < a.V)
 #pragma unroll
                                     for (int e = 0; e < 16; ++e)
-                                        a.final_state[fbase + static_cast<int64_t>(16 * p + e) * a.V] = x[e];
+                                        store_state(a, fbase + static_cast<int64_t>(16 * p + e) * a.V, x[e]);
                             } else if (r < KD) {
                                 // transition[j][k] = P[k][j]: lane r = j holds column j of P
                                 float* tp = a.transition + (unit_state * KD + r) * KD + 16 * p;

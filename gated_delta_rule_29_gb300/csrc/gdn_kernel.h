@@ -97,9 +97,39 @@ struct ChunkArgs {
     float gate_lb;
     int32_t beta_sigmoid;
     int32_t beta_bf16;
+    // state pool: sequence i reads and writes back slot state_idx[i] of s0 (then final_state
+    // aliases s0 and final_bf16 follows the pool's dtype)
+    const int32_t* state_idx;
+    int64_t pool_size;
+    int32_t final_bf16;
+};
+
+// One recurrence step per sequence against a state pool (gdn_decode).
+struct DecodeArgs {
+    const uint16_t* q; int64_t q_sn, q_sh;
+    const uint16_t* k; int64_t k_sn, k_sh;
+    const uint16_t* v; int64_t v_sn, v_sh;
+    const float* g; int64_t g_sn, g_sh;
+    const void* beta; int64_t b_sn, b_sh;
+    int32_t N, HK, HV, K, V, group;
+    float scale;
+    int32_t l2norm;
+    void* pool;                      // [pool_size, HV, K, V], updated in place
+    int32_t pool_bf16;
+    int64_t pool_size;
+    const int32_t* idx;              // [N] or null (sequence i uses slot i)
+    uint16_t* o; int64_t o_sn, o_sh;
+    int32_t* status;                 // nullable
+    int32_t gate_mode;
+    const float* a_log;
+    const float* dt_bias;
+    float gate_lb;
+    int32_t beta_sigmoid;
+    int32_t beta_bf16;
 };
 
 // Launchers (return cudaError_t of the launch).
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t s);
 cudaError_t launch_chunk_kernel(const ChunkArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
                                 const CUtensorMap& vmap, const CUtensorMap& omap, int mode, cudaStream_t s);

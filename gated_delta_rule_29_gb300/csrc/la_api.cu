@@ -312,9 +312,65 @@ la_status gdn_fwd(const la_gdn_fwd_params* p, void* stream) {
     if ((st = set_transforms(ka, p->gate_mode, p->a_log, p->dt_bias, p->gate_lower_bound, p->beta_sigmoid,
                              p->beta_bf16)) != LA_OK)
         return st;
+    if (p->state_indices) {
+        // state pool: the end states go back into initial_state in place
+        if (!p->initial_state || p->final_state || p->checkpoints || p->state_pool_size <= 0 ||
+            !aligned(p->state_indices, 4))
+            return LA_ERR_INVALID_ARG;
+        ka.state_idx = p->state_indices;
+        ka.pool_size = p->state_pool_size;
+        ka.final_state = static_cast<float*>(const_cast<void*>(p->initial_state));
+        ka.final_bf16 = p->initial_state_dtype == LA_DTYPE_BF16;
+    }
     return run(c, ka, p->q, p->q_stride_t, p->q_stride_h, p->k, p->k_stride_t, p->k_stride_h, p->v, p->v_stride_t,
                p->v_stride_h, ka.ckpt_n, p->workspace, p->workspace_bytes, p->status, la::kModeFwd,
                static_cast<cudaStream_t>(stream));
+}
+
+la_status gdn_decode(const la_gdn_decode_params* p, void* stream) {
+    if (!p) return LA_ERR_INVALID_ARG;
+    if (p->N < 0 || p->HK <= 0 || p->HV <= 0) return LA_ERR_INVALID_ARG;
+    if ((p->K != 64 && p->K != 128) || (p->V != 64 && p->V != 128)) return LA_ERR_UNSUPPORTED;
+    if (p->HV % p->HK != 0) return LA_ERR_UNSUPPORTED;
+    if (p->state_dtype != LA_DTYPE_F32 && p->state_dtype != LA_DTYPE_BF16) return LA_ERR_UNSUPPORTED;
+    if (!p->state_pool || !aligned(p->state_pool, 16) || p->state_pool_size <= 0) return LA_ERR_INVALID_ARG;
+    if (!p->state_indices && p->state_pool_size < p->N) return LA_ERR_INVALID_ARG;
+    if (p->state_indices && !aligned(p->state_indices, 4)) return LA_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(p->N) * p->HV >= (int64_t(1) << 31)) return LA_ERR_UNSUPPORTED;
+    if (p->N > 0) {
+        if (!p->q || !p->k || !p->v || !p->o || !p->g || !p->beta) return LA_ERR_INVALID_ARG;
+        if (!aligned(p->q, 2) || !aligned(p->k, 2) || !aligned(p->v, 2) || !aligned(p->o, 2) || !aligned(p->g, 4) ||
+            !aligned(p->beta, p->beta_bf16 ? 2 : 4))
+            return LA_ERR_INVALID_ARG;
+    }
+    ChunkArgs tr;  // transform fields validated the same way as for gdn_fwd
+    std::memset(&tr, 0, sizeof(tr));
+    la_status st = set_transforms(tr, p->gate_mode, p->a_log, p->dt_bias, p->gate_lower_bound, p->beta_sigmoid,
+                                  p->beta_bf16);
+    if (st != LA_OK) return st;
+    la::DecodeArgs d;
+    std::memset(&d, 0, sizeof(d));
+    d.q = static_cast<const uint16_t*>(p->q); d.q_sn = p->q_stride_n; d.q_sh = p->q_stride_h;
+    d.k = static_cast<const uint16_t*>(p->k); d.k_sn = p->k_stride_n; d.k_sh = p->k_stride_h;
+    d.v = static_cast<const uint16_t*>(p->v); d.v_sn = p->v_stride_n; d.v_sh = p->v_stride_h;
+    d.g = p->g; d.g_sn = p->g_stride_n; d.g_sh = p->g_stride_h;
+    d.beta = p->beta; d.b_sn = p->beta_stride_n; d.b_sh = p->beta_stride_h;
+    d.N = p->N; d.HK = p->HK; d.HV = p->HV; d.K = p->K; d.V = p->V; d.group = p->HV / p->HK;
+    d.scale = p->scale > 0.f ? p->scale : 1.0f / std::sqrt(static_cast<float>(p->K));
+    d.l2norm = p->use_qk_l2norm != 0;
+    d.pool = p->state_pool; d.pool_bf16 = p->state_dtype == LA_DTYPE_BF16; d.pool_size = p->state_pool_size;
+    d.idx = p->state_indices;
+    d.o = static_cast<uint16_t*>(p->o); d.o_sn = p->o_stride_n; d.o_sh = p->o_stride_h;
+    d.status = p->status;
+    d.gate_mode = tr.gate_mode; d.a_log = tr.a_log; d.dt_bias = tr.dt_bias; d.gate_lb = tr.gate_lb;
+    d.beta_sigmoid = tr.beta_sigmoid; d.beta_bf16 = tr.beta_bf16;
+    cudaEvent_t ev0 = t_timing_start, ev1 = t_timing_stop;
+    t_timing_start = t_timing_stop = nullptr;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (ev0 && cudaEventRecord(ev0, s) != cudaSuccess) return LA_ERR_CUDA;
+    if (la::launch_decode(d, s) != cudaSuccess) return LA_ERR_CUDA;
+    if (ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return LA_ERR_CUDA;
+    return LA_OK;
 }
 
 la_status gdn_summary(const la_gdn_summary_params* p, void* stream) {
@@ -414,6 +470,7 @@ const char* la_status_string(la_status s) {
         case LA_ERR_BAD_SEQLENS: return "cu_seqlens must start at 0, be nondecreasing and end at T";
         case LA_ERR_TIMEOUT: return "a bounded wait inside a kernel ran out";
         case LA_ERR_WORKSPACE: return "workspace too small or not 256-byte aligned";
+        case LA_ERR_BAD_STATE_INDEX: return "a state_indices entry lies outside the state pool";
     }
     return "unknown status";
 }

@@ -57,7 +57,8 @@ typedef enum la_status {
     LA_ERR_CUDA = 3,         /* a CUDA runtime or driver call failed (launch, encode) */
     LA_ERR_BAD_SEQLENS = 4,  /* device-side: cu_seqlens not 0-based, decreasing or != T at N */
     LA_ERR_TIMEOUT = 5,      /* device-side: a bounded wait in a kernel gave up */
-    LA_ERR_WORKSPACE = 6     /* workspace smaller than la_gdn_workspace_bytes() */
+    LA_ERR_WORKSPACE = 6,    /* workspace smaller than la_gdn_workspace_bytes() */
+    LA_ERR_BAD_STATE_INDEX = 7 /* device-side: a state_indices entry outside [0, state_pool_size) */
 } la_status;
 
 typedef enum la_dtype { LA_DTYPE_BF16 = 0, LA_DTYPE_F32 = 1 } la_dtype;
@@ -106,6 +107,16 @@ typedef struct la_gdn_fwd_params {
     float gate_lower_bound;   /* < 0 (LA_GATE_SIGMOID_BOUND) */
     int32_t beta_sigmoid;     /* beta holds logits: beta <- 1 / (1 + exp(-beta)) */
     int32_t beta_bf16;        /* beta is bf16 (same strides) instead of fp32 */
+    /* ---- optional state pool (page: "States and checkpoints", state_indices) ----
+     * When state_indices ([N] int32, device) is set, initial_state is a pool
+     * [state_pool_size, HO, K, V] (contiguous, fp32 or bf16): sequence i starts
+     * from slot state_indices[i] and its end state is written back to that slot
+     * in place, in the pool's dtype.  final_state and checkpoints must be NULL.
+     * Two sequences of one call must not name the same slot (their write-backs
+     * would race).  An index outside the pool sets LA_ERR_BAD_STATE_INDEX in the
+     * status word and that sequence is skipped. */
+    const int32_t* state_indices;
+    int64_t state_pool_size;
 } la_gdn_fwd_params;
 
 /*
@@ -191,6 +202,44 @@ typedef struct la_gdn_summary_params {
  */
 la_status gdn_summary(const la_gdn_summary_params* p, void* stream);
 
+/* Parameters of gdn_decode: one new token for each of N sequences.  Strides are in elements. */
+typedef struct la_gdn_decode_params {
+    const void* q;    int64_t q_stride_n, q_stride_h;       /* [N, HK, K] bf16 */
+    const void* k;    int64_t k_stride_n, k_stride_h;       /* [N, HK, K] bf16 */
+    const void* v;    int64_t v_stride_n, v_stride_h;       /* [N, HV, V] bf16 */
+    const float* g;   int64_t g_stride_n, g_stride_h;       /* [N, HO] fp32 (raw gate if gate_mode != 0) */
+    const float* beta; int64_t beta_stride_n, beta_stride_h; /* [N, HO] fp32 (or bf16 logits, see beta_bf16) */
+    int32_t N, HK, HV, K, V;
+    float scale;              /* <= 0 selects 1/sqrt(K) */
+    int32_t use_qk_l2norm;
+    void* state_pool;         /* [state_pool_size, HO, K, V] contiguous, updated in place */
+    int32_t state_dtype;      /* la_dtype of the pool */
+    int64_t state_pool_size;
+    const int32_t* state_indices; /* [N] int32, or NULL: sequence i uses slot i (state_pool_size >= N) */
+    void* o;          int64_t o_stride_n, o_stride_h;       /* [N, HO, V] bf16 */
+    int32_t* status;          /* optional; LA_ERR_BAD_STATE_INDEX for an index outside the pool */
+    int32_t gate_mode;        /* as in la_gdn_fwd_params */
+    const float* a_log;
+    const float* dt_bias;
+    float gate_lower_bound;
+    int32_t beta_sigmoid;
+    int32_t beta_bf16;
+} la_gdn_decode_params;
+
+/*
+ * gdn_decode -- one recurrence step per sequence against a state pool.
+ *
+ * Page: "States and checkpoints" (state_indices turns initial_state into a pool
+ * addressed per sequence and written back in place), for the serving case where
+ * every sequence brings exactly one token: for each sequence i and head h, with
+ * S = pool[state_indices[i], h],
+ *     S <- exp(g) (I - beta k_hat k_hat^T) S + beta k_hat v^T,   o = scale S^T q_hat
+ * and S is stored back into the same slot.  Equal to gdn_fwd over
+ * cu_seqlens = [0, 1, ..., N] with the same pool.  No workspace; never syncs.
+ * Two sequences must not name the same slot.
+ */
+la_status gdn_decode(const la_gdn_decode_params* p, void* stream);
+
 /* Bytes of device workspace gdn_fwd (summary = 0) or gdn_summary (summary = 1) needs. */
 size_t la_gdn_workspace_bytes(int32_t N, int32_t summary);
 
@@ -211,7 +260,8 @@ la_status la_read_status(const int32_t* device_status, void* stream, int32_t* ou
 /*
  * Profiling hook: record `start_event` and `stop_event` (cudaEvent_t handles) on
  * the launch stream immediately before and after the fused chunk kernel of the
- * next gdn_fwd / gdn_summary call made by this host thread, so a caller can time
+ * next gdn_fwd / gdn_summary call (or the decode kernel of the next gdn_decode
+ * call) made by this host thread, so a caller can time
  * that kernel alone with CUDA events.  The hook is consumed by that one call;
  * pass NULL, NULL to clear it.  Not part of the computation; no citation.
  */

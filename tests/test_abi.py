@@ -47,7 +47,8 @@ def _c_layout(struct_name, fields):
 
 
 @pytest.mark.parametrize("cls,cname", [(B.GdnFwdParams, "la_gdn_fwd_params"),
-                                       (B.GdnSummaryParams, "la_gdn_summary_params")])
+                                       (B.GdnSummaryParams, "la_gdn_summary_params"),
+                                       (B.GdnDecodeParams, "la_gdn_decode_params")])
 def test_ctypes_mirror_matches_c_layout(cls, cname):
     names = [f[0] for f in cls._fields_]
     size, offs = _c_layout(cname, names)
@@ -119,6 +120,17 @@ FWD_ERRORS = [
     ("misaligned fp32 initial state", dict(initial_state=FAKE + 2, initial_state_dtype=1), B.LA_ERR_INVALID_ARG),
     ("misaligned final state", dict(final_state=FAKE + 1), B.LA_ERR_INVALID_ARG),
     ("T beyond int32 TMA coordinates", dict(T=1 << 31), B.LA_ERR_UNSUPPORTED),
+    ("unknown gate mode", dict(gate_mode=5), B.LA_ERR_INVALID_ARG),
+    ("softplus gate without a_log", dict(gate_mode=1, dt_bias=FAKE), B.LA_ERR_INVALID_ARG),
+    ("bounded gate with a positive bound", dict(gate_mode=2, gate_lower_bound=1.0), B.LA_ERR_INVALID_ARG),
+    ("state pool without a pool", dict(state_indices=FAKE, state_pool_size=4), B.LA_ERR_INVALID_ARG),
+    ("state pool and final state", dict(state_indices=FAKE, state_pool_size=4, initial_state=FAKE,
+                                        initial_state_dtype=1, final_state=FAKE), B.LA_ERR_INVALID_ARG),
+    ("state pool and checkpoints", dict(state_indices=FAKE, state_pool_size=4, initial_state=FAKE,
+                                        initial_state_dtype=1, checkpoints=FAKE, checkpoint_every_n=64),
+     B.LA_ERR_INVALID_ARG),
+    ("empty state pool", dict(state_indices=FAKE, state_pool_size=0, initial_state=FAKE, initial_state_dtype=1),
+     B.LA_ERR_INVALID_ARG),
 ]
 
 
@@ -147,10 +159,49 @@ def test_gdn_summary_rejects(name, over, code):
     assert lib.gdn_summary(ctypes.byref(p), None) == code
 
 
+def _decode(**over):
+    p = B.GdnDecodeParams()
+    N, HK, HV, K, V = 4, 2, 4, 128, 128
+    p.q, p.q_stride_n, p.q_stride_h = FAKE, HK * K, K
+    p.k, p.k_stride_n, p.k_stride_h = FAKE, HK * K, K
+    p.v, p.v_stride_n, p.v_stride_h = FAKE, HV * V, V
+    p.g, p.g_stride_n, p.g_stride_h = FAKE, HV, 1
+    p.beta, p.beta_stride_n, p.beta_stride_h = FAKE, HV, 1
+    p.N, p.HK, p.HV, p.K, p.V = N, HK, HV, K, V
+    p.state_pool, p.state_dtype, p.state_pool_size = FAKE, B.LA_DTYPE_F32, 8
+    p.o, p.o_stride_n, p.o_stride_h = FAKE, HV * V, V
+    for k, v in over.items():
+        setattr(p, k, v)
+    return p
+
+
+DECODE_ERRORS = [
+    ("K not 64/128", dict(K=96), B.LA_ERR_UNSUPPORTED),
+    ("HV not a multiple of HK", dict(HK=3), B.LA_ERR_UNSUPPORTED),
+    ("pool dtype", dict(state_dtype=4), B.LA_ERR_UNSUPPORTED),
+    ("null pool", dict(state_pool=None), B.LA_ERR_INVALID_ARG),
+    ("pool not 16-byte aligned", dict(state_pool=FAKE + 8), B.LA_ERR_INVALID_ARG),
+    ("pool smaller than N without indices", dict(state_pool_size=3), B.LA_ERR_INVALID_ARG),
+    ("misaligned indices", dict(state_indices=FAKE + 2), B.LA_ERR_INVALID_ARG),
+    ("null q", dict(q=None), B.LA_ERR_INVALID_ARG),
+    ("null o", dict(o=None), B.LA_ERR_INVALID_ARG),
+    ("negative N", dict(N=-1), B.LA_ERR_INVALID_ARG),
+    ("unknown gate mode", dict(gate_mode=9), B.LA_ERR_INVALID_ARG),
+]
+
+
+@pytest.mark.parametrize("name,over,code", DECODE_ERRORS, ids=[e[0] for e in DECODE_ERRORS])
+def test_gdn_decode_rejects(name, over, code):
+    lib = B.load()
+    p = _decode(**over)
+    assert lib.gdn_decode(ctypes.byref(p), None) == code
+
+
 def test_null_params():
     lib = B.load()
     assert lib.gdn_fwd(None, None) == B.LA_ERR_INVALID_ARG
     assert lib.gdn_summary(None, None) == B.LA_ERR_INVALID_ARG
+    assert lib.gdn_decode(None, None) == B.LA_ERR_INVALID_ARG
 
 
 def test_checkpoint_rows_host_helper():
@@ -167,8 +218,8 @@ def test_checkpoint_rows_host_helper():
 
 def test_status_strings_and_version():
     lib = B.load()
-    for code in range(7):
-        assert lib.la_status_string(code)
+    for code in range(8):
+        assert lib.la_status_string(code) != b"unknown status"
     assert lib.la_status_string(99) == b"unknown status"
     assert lib.la_version() >= 100
     assert lib.la_read_status(None, None, ctypes.byref(ctypes.c_int32())) == B.LA_ERR_INVALID_ARG
