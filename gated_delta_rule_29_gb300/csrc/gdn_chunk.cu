@@ -78,6 +78,7 @@ struct __align__(16) Scalars {
     uint64_t bar_kq, bar_v, bar_mma, bar_o;
     uint32_t tmem_base;
     int32_t unit_lo, unit_hi;
+    int32_t status0;
 };
 static_assert(sizeof(Scalars) <= 7168, "scalar area");
 
@@ -374,7 +375,10 @@ __global__ void __launch_bounds__(kCta, 2)
     const int r = tid;  // TMEM lane, value column, stacked token row
     const int HO = a.HV;
 
-    if (*reinterpret_cast<volatile int32_t*>(&a.hdr->status) != LA_OK) return;
+    // one read of the status word for the whole CTA (another CTA may set it meanwhile)
+    if (tid == 0) sc.status0 = *reinterpret_cast<volatile int32_t*>(&a.hdr->status);
+    __syncthreads();
+    if (sc.status0 != LA_OK) return;
 
     if (tid < 32) {
         tmem_alloc(&sc.tmem_base, TMEM_COLS);
