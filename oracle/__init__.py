@@ -1,7 +1,8 @@
 """Parity oracle -- TEST INFRASTRUCTURE ONLY.
 
-A plain fp64 CPU restatement of the Gated DeltaNet forward (``gdn_fwd``) and of
-the span summary (``gdn_summary``), following the cuDNN "Linear Attention"
+A plain fp64 CPU restatement of the Gated DeltaNet forward (``gdn_fwd``), of
+the span summary (``gdn_summary``) and of the forward's backward (``gdn_bwd``,
+reverse-mode differentiation of the token recurrence), following the cuDNN "Linear Attention"
 operations page (sections "Layout" and "Semantics worth knowing").  The
 arithmetic lives in ``gdn_oracle.c`` (token-by-token recurrence, fp64); this
 module only compiles it with gcc, converts inputs to fp64 and marshals
@@ -16,7 +17,8 @@ package imports nothing from the library: the two share no code.
 
 Parity pins: every entry point is pinned in ``tests/test_oracle_pins.py``
 (brute-force dense products, closed forms, linearity, span composition,
-hand-derived golden values in ``tests/golden/``).
+hand-derived golden values in ``tests/golden/``; the backward against central
+finite differences of the forward).
 """
 from __future__ import annotations
 
@@ -50,6 +52,9 @@ MUTATIONS = {
     11: "beta sigmoid of the negated logit",
     12: "bounded gate without the sigmoid",
     13: "state pool written back to slot i instead of state_indices[i]",
+    # planted in the backward
+    14: "backward: decay gradient misses the erase path (uses dS instead of dS')",
+    15: "backward: key gradient misses the S' dx term",
 }
 
 
@@ -82,6 +87,15 @@ def _load():
                 d, ctypes.c_int64, i64,
                 d, ctypes.c_void_p,
                 ctypes.c_int, ctypes.c_int,
+            ]
+            lib.gdn_oracle_bwd.restype = ctypes.c_int
+            lib.gdn_oracle_bwd.argtypes = [
+                d, d, d, d, d, i64,
+                ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_double, ctypes.c_int, d,
+                d, d,
+                d, d, d, d, d, d,
+                ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
             ]
             _lib = lib
     return _lib
@@ -210,6 +224,48 @@ def gdn_fwd(q, k, v, g, beta, cu_seqlens, *, scale=None, use_qk_l2norm=True,
         out[dst] = r["final_state"]
         r["state_pool"] = out
     return r
+
+
+def gdn_bwd(q, k, v, g, beta, cu_seqlens, do, *, scale=None, use_qk_l2norm=True, initial_state=None,
+            d_final_state=None, unit_mask=None, nthreads=None, mutation=0):
+    """fp64 backward of gdn_fwd (natural-log gate, beta as given) by reverse-mode differentiation
+    of the token recurrence: the gradients of L = sum(do * o) + sum(d_final_state * S_final).
+
+    Returns dict(dq [T,HK,K], dk [T,HK,K], dv [T,HV,V], dg [T,HO], dbeta [T,HO],
+    d_initial_state [N,HO,K,V]).  Grouped heads: dq, dk sum the contributions of every value
+    head of the group.
+    """
+    q, k, v, g, beta, do = (_f64(x) for x in (q, k, v, g, beta, do))
+    cu = _i64(cu_seqlens)
+    T, HK, K = k.shape
+    HV, V = v.shape[1], v.shape[2]
+    N = cu.shape[0] - 1
+    HO = HV
+    if scale is None:
+        scale = 1.0 / np.sqrt(K)
+    s0 = _f64(initial_state)
+    dfin = _f64(d_final_state)
+    dqh = np.zeros((T, HO, K))
+    dkh = np.zeros((T, HO, K))
+    dv = np.zeros((T, HV, V))
+    dg = np.zeros((T, HO))
+    db = np.zeros((T, HO))
+    ds0 = np.zeros((N, HO, K, V))
+    mask = None
+    if unit_mask is not None:
+        mask = np.ascontiguousarray(np.asarray(unit_mask, dtype=np.uint8).reshape(N * HO))
+    rc = _load().gdn_oracle_bwd(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(cu, ctypes.c_int64),
+        T, N, HK, HV, K, V, float(scale), int(bool(use_qk_l2norm)), _ptr(s0),
+        _ptr(do), _ptr(dfin),
+        _ptr(dqh), _ptr(dkh), _ptr(dv), _ptr(dg), _ptr(db), _ptr(ds0),
+        mask.ctypes.data if mask is not None else None, int(nthreads or _default_threads()), int(mutation))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments (cu_seqlens or shapes)")
+    grp = HV // HK
+    dq = dqh.reshape(T, HK, grp, K).sum(axis=2)
+    dk = dkh.reshape(T, HK, grp, K).sum(axis=2)
+    return {"dq": dq, "dk": dk, "dv": dv, "dg": dg, "dbeta": db, "d_initial_state": ds0}
 
 
 def gdn_summary(k, v, g, beta, cu_seqlens, *, use_qk_l2norm=True, start_state=None,

@@ -16,7 +16,9 @@ Every check below is an independent statement of what the Gated DeltaNet forward
   * the optional input transforms (softplus gate, bounded sigmoid gate, beta
     sigmoid) at arguments where they take exact values (ln 2, 1, 1/2, 3/4);
   * the state pool (state_indices): one-token updates against the explicit
-    factor form, written back to the named slots, other slots untouched.
+    factor form, written back to the named slots, other slots untouched;
+  * the backward: every gradient against central finite differences of the
+    pinned forward (with and without the L2 norm, grouped heads, start state).
 test_planted_mistakes_are_caught plants each of the oracle's known mutations
 and requires at least one check to fail, so a plausible slip anywhere (a dropped
 term, a flipped sign, a wrong index or orientation) cannot pass unnoticed.
@@ -385,6 +387,50 @@ def check_state_pool(mutation=0):
     return max(errs)
 
 
+def _fd_case(l2norm, seed):
+    rng = np.random.default_rng(seed)
+    lengths = [4, 5]
+    T, HK, HV, K, V = sum(lengths), 1, 2, 3, 2
+    cu = np.array([0, 4, 9])
+    q = rng.standard_normal((T, HK, K))
+    k = rng.standard_normal((T, HK, K))
+    v = rng.standard_normal((T, HV, V))
+    g = -0.3 * rng.random((T, HV))
+    beta = rng.random((T, HV))
+    S0 = 0.5 * rng.standard_normal((2, HV, K, V))
+    do = rng.standard_normal((T, HV, V))
+    dfin = rng.standard_normal((2, HV, K, V))
+    return dict(q=q, k=k, v=v, g=g, beta=beta, S0=S0), cu, do, dfin, l2norm
+
+
+def check_backward_finite_differences(mutation=0):
+    """Every gradient of L = sum(do * o) + sum(dS_T * S_final) against central differences of
+    the (pinned) forward, with and without the L2 norm, grouped heads and a start state."""
+    worst = 0.0
+    names = {"q": "dq", "k": "dk", "v": "dv", "g": "dg", "beta": "dbeta", "S0": "d_initial_state"}
+    for l2norm, seed in ((True, 101), (False, 102)):
+        x, cu, do, dfin, l2 = _fd_case(l2norm, seed)
+
+        def loss(xx):
+            r = oracle.gdn_fwd(xx["q"], xx["k"], xx["v"], xx["g"], xx["beta"], cu, scale=0.8, use_qk_l2norm=l2,
+                               initial_state=xx["S0"], nthreads=1)
+            return float((r["o"] * do).sum() + (r["final_state"] * dfin).sum())
+
+        grads = oracle.gdn_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], cu, do, scale=0.8, use_qk_l2norm=l2,
+                               initial_state=x["S0"], d_final_state=dfin, nthreads=1, mutation=mutation)
+        eps = 1e-6
+        for name, gname in names.items():
+            fd = np.zeros_like(x[name])
+            for idx in np.ndindex(x[name].shape):
+                xp = {kk: vv.copy() for kk, vv in x.items()}
+                xm = {kk: vv.copy() for kk, vv in x.items()}
+                xp[name][idx] += eps
+                xm[name][idx] -= eps
+                fd[idx] = (loss(xp) - loss(xm)) / (2 * eps)
+            worst = max(worst, _rel(grads[gname], fd))
+    return worst
+
+
 CHECKS = {
     "golden": (check_golden, 1e-12),
     "brute_force": (check_brute_force, 1e-12),
@@ -402,6 +448,7 @@ CHECKS = {
     "gate_sigmoid_bound": (check_gate_sigmoid_bound, 1e-12),
     "beta_sigmoid": (check_beta_sigmoid, 1e-14),
     "state_pool": (check_state_pool, 1e-13),
+    "backward_finite_differences": (check_backward_finite_differences, 1e-6),
 }
 
 
