@@ -209,6 +209,70 @@ def gdn_summary(k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.T
     return end_state, transition
 
 
+def gdn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
+            cu_seqlens: torch.Tensor, d_o: torch.Tensor, *, scale: Optional[float] = None,
+            use_qk_l2norm: bool = True, initial_state: Optional[torch.Tensor] = None,
+            d_final_state: Optional[torch.Tensor] = None, checkpoints: Optional[torch.Tensor] = None,
+            workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+            stream: Optional[torch.cuda.Stream] = None):
+    """Backward of gdn_fwd: returns (dq, dk, dv, dg, dbeta, d_initial_state or None) for the loss
+    sum(d_o * o) + sum(d_final_state * final_state).  `checkpoints`, if given, are the forward's
+    fp32 checkpoints every 64 tokens; otherwise the forward is re-run for them."""
+    _check_thd("q", q, torch.bfloat16)
+    _check_thd("k", k, torch.bfloat16)
+    _check_thd("v", v, torch.bfloat16)
+    _check_thd("g", g, torch.float32, heads_dim=False)
+    _check_thd("beta", beta, torch.float32, heads_dim=False)
+    _check_thd("d_o", d_o, torch.bfloat16)
+    T, HK, K = k.shape
+    HV, V = v.shape[1], v.shape[2]
+    N = cu_seqlens.numel() - 1
+    dev = q.device
+    dq = torch.empty(T, HK, K, dtype=torch.bfloat16, device=dev)
+    dk = torch.empty(T, HK, K, dtype=torch.bfloat16, device=dev)
+    dv = torch.empty(T, HV, V, dtype=torch.bfloat16, device=dev)
+    dg = torch.empty(T, HV, dtype=torch.float32, device=dev)
+    db = torch.empty(T, HV, dtype=torch.float32, device=dev)
+    ds0 = torch.empty(N, HV, K, V, dtype=torch.float32, device=dev) if initial_state is not None else None
+    lib = B.load()
+    if workspace is None:
+        need = lib.la_gdn_bwd_workspace_bytes(T, N, HK, HV, K, V, int(checkpoints is not None))
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    if initial_state is not None:
+        initial_state = initial_state.contiguous()
+    if d_final_state is not None:
+        d_final_state = d_final_state.contiguous().float()
+    if checkpoints is not None:
+        if checkpoints.dtype != torch.float32 or not checkpoints.is_contiguous():
+            raise ValueError("checkpoints must be the forward's contiguous fp32 rows every 64 tokens")
+    p = B.GdnBwdParams()
+    p.q, p.q_stride_t, p.q_stride_h = q.data_ptr(), q.stride(0), q.stride(1)
+    p.k, p.k_stride_t, p.k_stride_h = k.data_ptr(), k.stride(0), k.stride(1)
+    p.v, p.v_stride_t, p.v_stride_h = v.data_ptr(), v.stride(0), v.stride(1)
+    p.g, p.g_stride_t, p.g_stride_h = g.data_ptr(), g.stride(0), g.stride(1)
+    p.beta, p.beta_stride_t, p.beta_stride_h = beta.data_ptr(), beta.stride(0), beta.stride(1)
+    p.cu_seqlens, p.cu_seqlens_bits = cu_seqlens.data_ptr(), _cu_bits(cu_seqlens)
+    p.T, p.N, p.HK, p.HV, p.K, p.V = T, N, HK, HV, K, V
+    p.scale = float(scale) if scale is not None else 1.0 / math.sqrt(K)
+    p.use_qk_l2norm = int(bool(use_qk_l2norm))
+    if initial_state is not None:
+        p.initial_state = initial_state.data_ptr()
+        p.initial_state_dtype = B.LA_DTYPE_BF16 if initial_state.dtype == torch.bfloat16 else B.LA_DTYPE_F32
+    p.checkpoints = checkpoints.data_ptr() if checkpoints is not None else None
+    p.d_o, p.d_o_stride_t, p.d_o_stride_h = d_o.data_ptr(), d_o.stride(0), d_o.stride(1)
+    p.d_final_state = d_final_state.data_ptr() if d_final_state is not None else None
+    p.dq, p.dq_stride_t, p.dq_stride_h = dq.data_ptr(), dq.stride(0), dq.stride(1)
+    p.dk, p.dk_stride_t, p.dk_stride_h = dk.data_ptr(), dk.stride(0), dk.stride(1)
+    p.dv, p.dv_stride_t, p.dv_stride_h = dv.data_ptr(), dv.stride(0), dv.stride(1)
+    p.dg, p.dg_stride_t, p.dg_stride_h = dg.data_ptr(), dg.stride(0), dg.stride(1)
+    p.dbeta, p.dbeta_stride_t, p.dbeta_stride_h = db.data_ptr(), db.stride(0), db.stride(1)
+    p.d_initial_state = ds0.data_ptr() if ds0 is not None else None
+    p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel()
+    p.status = status.data_ptr() if status is not None else None
+    B.check(lib.gdn_bwd(ctypes.byref(p), _stream_ptr(stream)), "gdn_bwd")
+    return dq, dk, dv, dg, db, ds0
+
+
 def gdn_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
                state_pool: torch.Tensor, *, state_indices: Optional[torch.Tensor] = None,
                scale: Optional[float] = None, use_qk_l2norm: bool = True, o: Optional[torch.Tensor] = None,

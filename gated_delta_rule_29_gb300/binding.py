@@ -38,6 +38,8 @@ EXPORTED_SYMBOLS = (
     "la_set_kernel_timing_events",
     "gdn_fwd_static_workspace",
     "gdn_decode",
+    "gdn_bwd",
+    "la_gdn_bwd_workspace_bytes",
 )
 
 _i64 = ctypes.c_int64
@@ -112,6 +114,10 @@ def load(build_if_missing: bool = True):
         lib = ctypes.CDLL(path)
         lib.gdn_fwd.restype = ctypes.c_int
         lib.gdn_fwd.argtypes = [ctypes.POINTER(GdnFwdParams), _vp]
+        lib.gdn_bwd.restype = ctypes.c_int
+        lib.gdn_bwd.argtypes = [ctypes.POINTER(GdnBwdParams), _vp]
+        lib.la_gdn_bwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.la_gdn_bwd_workspace_bytes.argtypes = [_i64, _i32, _i32, _i32, _i32, _i32, _i32]
         lib.gdn_decode.restype = ctypes.c_int
         lib.gdn_decode.argtypes = [ctypes.POINTER(GdnDecodeParams), _vp]
         lib.gdn_summary.restype = ctypes.c_int
@@ -150,6 +156,33 @@ class GdnDecodeParams(ctypes.Structure):
         ("status", _vp),
         ("gate_mode", _i32), ("a_log", _vp), ("dt_bias", _vp), ("gate_lower_bound", ctypes.c_float),
         ("beta_sigmoid", _i32), ("beta_bf16", _i32),
+    ]
+
+
+class GdnBwdParams(ctypes.Structure):
+    """Mirror of la_gdn_bwd_params (same field order and types)."""
+    _fields_ = [
+        ("q", _vp), ("q_stride_t", _i64), ("q_stride_h", _i64),
+        ("k", _vp), ("k_stride_t", _i64), ("k_stride_h", _i64),
+        ("v", _vp), ("v_stride_t", _i64), ("v_stride_h", _i64),
+        ("g", _vp), ("g_stride_t", _i64), ("g_stride_h", _i64),
+        ("beta", _vp), ("beta_stride_t", _i64), ("beta_stride_h", _i64),
+        ("cu_seqlens", _vp), ("cu_seqlens_bits", _i32),
+        ("T", _i64),
+        ("N", _i32), ("HK", _i32), ("HV", _i32), ("K", _i32), ("V", _i32),
+        ("scale", ctypes.c_float), ("use_qk_l2norm", _i32),
+        ("initial_state", _vp), ("initial_state_dtype", _i32),
+        ("checkpoints", _vp),
+        ("d_o", _vp), ("d_o_stride_t", _i64), ("d_o_stride_h", _i64),
+        ("d_final_state", _vp),
+        ("dq", _vp), ("dq_stride_t", _i64), ("dq_stride_h", _i64),
+        ("dk", _vp), ("dk_stride_t", _i64), ("dk_stride_h", _i64),
+        ("dv", _vp), ("dv_stride_t", _i64), ("dv_stride_h", _i64),
+        ("dg", _vp), ("dg_stride_t", _i64), ("dg_stride_h", _i64),
+        ("dbeta", _vp), ("dbeta_stride_t", _i64), ("dbeta_stride_h", _i64),
+        ("d_initial_state", _vp),
+        ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
+        ("status", _vp),
     ]
 
 

@@ -128,8 +128,38 @@ struct DecodeArgs {
     int32_t beta_bf16;
 };
 
+// The backward (gdn_bwd): one CTA per (sequence, head), reverse over chunks.
+struct BwdArgs {
+    const uint16_t* q; int64_t q_st, q_sh;
+    const uint16_t* k; int64_t k_st, k_sh;
+    const uint16_t* v; int64_t v_st, v_sh;
+    const float* g; int64_t g_st, g_sh;
+    const float* beta; int64_t b_st, b_sh;
+    const void* cu;
+    int32_t cu64;
+    int64_t T;
+    int32_t N, HK, HV, K, V, group;
+    float scale;
+    int32_t l2norm;
+    const uint16_t* dout; int64_t do_st, do_sh;
+    const float* dfinal;             // [N, HO, K, V] or null
+    const float* ckpt;               // states entering every chunk, [rows, HO, K, V] fp32
+    const int64_t* ckpt_off;         // [N] first chunk row of each sequence
+    const WsHeader* hdr;             // the prologue's status word: nothing runs unless LA_OK
+    float* dS_work;                  // [N * HO, K, V]
+    uint16_t* dq; int64_t dq_st, dq_sh;
+    uint16_t* dk; int64_t dk_st, dk_sh;
+    uint16_t* dv; int64_t dv_st, dv_sh;
+    float* dg; int64_t dg_st, dg_sh;
+    float* dbeta; int64_t db_st, db_sh;
+    float* ds0;                      // [N, HO, K, V] or null
+    float* dqh;                      // [T, HO, K] fp32 per value head (grouped heads)
+    float* dkh;
+};
+
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t s);
 cudaError_t launch_chunk_kernel(const ChunkArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
                                 const CUtensorMap& vmap, const CUtensorMap& omap, int mode, cudaStream_t s);

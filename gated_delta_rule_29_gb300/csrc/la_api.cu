@@ -373,6 +373,141 @@ la_status gdn_decode(const la_gdn_decode_params* p, void* stream) {
     return LA_OK;
 }
 
+}  // extern "C"
+
+namespace {
+struct BwdLayout {
+    size_t pro, ck, o, ds, gh, total;
+};
+size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
+BwdLayout bwd_layout(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, int32_t V, bool ck_given) {
+    BwdLayout L{};
+    size_t off = up256(la::ws_layout(N).total);
+    const size_t rows = static_cast<size_t>((T + la::kChunk - 1) / la::kChunk + N);  // >= sum ceil(L_i / 64)
+    L.pro = 0;
+    L.ck = off;
+    if (!ck_given) off += up256(rows * HV * K * V * sizeof(float));
+    L.o = off;
+    if (!ck_given) off += up256(static_cast<size_t>(T) * HV * V * 2);
+    L.ds = off;
+    off += up256(static_cast<size_t>(N) * HV * K * V * sizeof(float));
+    L.gh = off;
+    if (HV != HK) off += up256(2 * static_cast<size_t>(T) * HV * K * sizeof(float));
+    L.total = off;
+    return L;
+}
+}  // namespace
+
+extern "C" {
+
+size_t la_gdn_bwd_workspace_bytes(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, int32_t V,
+                                  int32_t checkpoints_given) {
+    if (T < 0 || N < 0 || HK <= 0 || HV <= 0) return 0;
+    return bwd_layout(T, N, HK, HV, K, V, checkpoints_given != 0).total;
+}
+
+la_status gdn_bwd(const la_gdn_bwd_params* p, void* stream) {
+    if (!p) return LA_ERR_INVALID_ARG;
+    Common c{p->T, p->N, p->HK, p->HV, p->K, p->V, p->cu_seqlens, p->cu_seqlens_bits, p->g, p->beta, 4};
+    la_status st = check_common(c);
+    if (st != LA_OK) return st;
+    if (p->T > 0) {
+        if ((st = check_tma_operand(p->q, p->q_stride_t, p->q_stride_h, p->HK)) != LA_OK) return st;
+        if ((st = check_tma_operand(p->k, p->k_stride_t, p->k_stride_h, p->HK)) != LA_OK) return st;
+        if ((st = check_tma_operand(p->v, p->v_stride_t, p->v_stride_h, p->HV)) != LA_OK) return st;
+        if (!p->d_o || !p->dq || !p->dk || !p->dv || !p->dg || !p->dbeta) return LA_ERR_INVALID_ARG;
+        if (!aligned(p->d_o, 2) || !aligned(p->dq, 2) || !aligned(p->dk, 2) || !aligned(p->dv, 2) ||
+            !aligned(p->dg, 4) || !aligned(p->dbeta, 4))
+            return LA_ERR_INVALID_ARG;
+    }
+    if (p->initial_state) {
+        if (p->initial_state_dtype != LA_DTYPE_F32 && p->initial_state_dtype != LA_DTYPE_BF16) return LA_ERR_UNSUPPORTED;
+        if (!aligned(p->initial_state, p->initial_state_dtype == LA_DTYPE_F32 ? 4 : 2)) return LA_ERR_INVALID_ARG;
+    }
+    if (p->checkpoints && !aligned(p->checkpoints, 4)) return LA_ERR_INVALID_ARG;
+    if ((p->d_final_state && !aligned(p->d_final_state, 4)) || (p->d_initial_state && !aligned(p->d_initial_state, 4)))
+        return LA_ERR_INVALID_ARG;
+    const bool ck_given = p->checkpoints != nullptr;
+    const BwdLayout BL = bwd_layout(p->T, p->N, p->HK, p->HV, p->K, p->V, ck_given);
+    void* ws = p->workspace;
+    if (ws) {
+        if (p->workspace_bytes < BL.total || !aligned(ws, 256)) return LA_ERR_WORKSPACE;
+    } else if ((st = internal_workspace(BL.total, &ws)) != LA_OK) {
+        return st;
+    }
+    uint8_t* wb = static_cast<uint8_t*>(ws);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const float* ck = p->checkpoints;
+    const la::WorkspaceLayout PL = la::ws_layout(p->N);
+    if (!ck_given) {
+        // states entering every chunk: the forward with fp32 checkpoints every 64 tokens
+        la_gdn_fwd_params f;
+        std::memset(&f, 0, sizeof(f));
+        f.q = p->q; f.q_stride_t = p->q_stride_t; f.q_stride_h = p->q_stride_h;
+        f.k = p->k; f.k_stride_t = p->k_stride_t; f.k_stride_h = p->k_stride_h;
+        f.v = p->v; f.v_stride_t = p->v_stride_t; f.v_stride_h = p->v_stride_h;
+        f.g = p->g; f.g_stride_t = p->g_stride_t; f.g_stride_h = p->g_stride_h;
+        f.beta = p->beta; f.beta_stride_t = p->beta_stride_t; f.beta_stride_h = p->beta_stride_h;
+        f.cu_seqlens = p->cu_seqlens; f.cu_seqlens_bits = p->cu_seqlens_bits;
+        f.T = p->T; f.N = p->N; f.HK = p->HK; f.HV = p->HV; f.K = p->K; f.V = p->V;
+        f.scale = p->scale; f.use_qk_l2norm = p->use_qk_l2norm;
+        f.initial_state = p->initial_state; f.initial_state_dtype = p->initial_state_dtype;
+        f.o = wb + BL.o; f.o_stride_t = static_cast<int64_t>(p->HV) * p->V; f.o_stride_h = p->V;
+        f.checkpoints = wb + BL.ck; f.checkpoint_dtype = LA_DTYPE_F32; f.checkpoint_every_n = la::kChunk;
+        f.workspace = wb + BL.pro; f.workspace_bytes = PL.total;
+        f.status = p->status;
+        if ((st = gdn_fwd(&f, stream)) != LA_OK) return st;
+        ck = reinterpret_cast<const float*>(wb + BL.ck);
+    } else {
+        // only the prologue: validation and the chunk-row offsets of the caller's checkpoints
+        PrologueArgs pa;
+        pa.cu = p->cu_seqlens;
+        pa.cu64 = p->cu_seqlens_bits == 64;
+        pa.T = p->T;
+        pa.N = p->N;
+        pa.ckpt_n = la::kChunk;
+        pa.hdr = reinterpret_cast<la::WsHeader*>(wb + BL.pro);
+        pa.order = reinterpret_cast<int32_t*>(wb + BL.pro + PL.order);
+        pa.ckpt_off = reinterpret_cast<int64_t*>(wb + BL.pro + PL.ckpt_off);
+        pa.keys = reinterpret_cast<uint64_t*>(wb + BL.pro + PL.keys);
+        pa.user_status = p->status;
+        if (la::launch_prologue(pa, s) != cudaSuccess) return LA_ERR_CUDA;
+    }
+    la::BwdArgs b;
+    std::memset(&b, 0, sizeof(b));
+    b.q = static_cast<const uint16_t*>(p->q); b.q_st = p->q_stride_t; b.q_sh = p->q_stride_h;
+    b.k = static_cast<const uint16_t*>(p->k); b.k_st = p->k_stride_t; b.k_sh = p->k_stride_h;
+    b.v = static_cast<const uint16_t*>(p->v); b.v_st = p->v_stride_t; b.v_sh = p->v_stride_h;
+    b.g = p->g; b.g_st = p->g_stride_t; b.g_sh = p->g_stride_h;
+    b.beta = p->beta; b.b_st = p->beta_stride_t; b.b_sh = p->beta_stride_h;
+    b.cu = p->cu_seqlens; b.cu64 = p->cu_seqlens_bits == 64;
+    b.T = p->T; b.N = p->N; b.HK = p->HK; b.HV = p->HV; b.K = p->K; b.V = p->V; b.group = p->HV / p->HK;
+    b.scale = p->scale > 0.f ? p->scale : 1.0f / std::sqrt(static_cast<float>(p->K));
+    b.l2norm = p->use_qk_l2norm != 0;
+    b.dout = static_cast<const uint16_t*>(p->d_o); b.do_st = p->d_o_stride_t; b.do_sh = p->d_o_stride_h;
+    b.dfinal = p->d_final_state;
+    b.ckpt = ck;
+    b.ckpt_off = reinterpret_cast<const int64_t*>(wb + BL.pro + PL.ckpt_off);
+    b.hdr = reinterpret_cast<const la::WsHeader*>(wb + BL.pro);
+    b.dS_work = reinterpret_cast<float*>(wb + BL.ds);
+    b.dq = static_cast<uint16_t*>(p->dq); b.dq_st = p->dq_stride_t; b.dq_sh = p->dq_stride_h;
+    b.dk = static_cast<uint16_t*>(p->dk); b.dk_st = p->dk_stride_t; b.dk_sh = p->dk_stride_h;
+    b.dv = static_cast<uint16_t*>(p->dv); b.dv_st = p->dv_stride_t; b.dv_sh = p->dv_stride_h;
+    b.dg = p->dg; b.dg_st = p->dg_stride_t; b.dg_sh = p->dg_stride_h;
+    b.dbeta = p->dbeta; b.db_st = p->dbeta_stride_t; b.db_sh = p->dbeta_stride_h;
+    b.ds0 = p->d_initial_state;
+    if (p->HV != p->HK) {
+        b.dqh = reinterpret_cast<float*>(wb + BL.gh);
+        b.dkh = b.dqh + static_cast<size_t>(p->T) * p->HV * p->K;
+    }
+    cudaEvent_t ev0 = t_timing_start, ev1 = t_timing_stop;
+    t_timing_start = t_timing_stop = nullptr;
+    if (ev0 && cudaEventRecord(ev0, s) != cudaSuccess) return LA_ERR_CUDA;
+    if (la::launch_bwd(b, s) != cudaSuccess) return LA_ERR_CUDA;
+    if (ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return LA_ERR_CUDA;
+    return LA_OK;
+}
+
 la_status gdn_summary(const la_gdn_summary_params* p, void* stream) {
     if (!p) return LA_ERR_INVALID_ARG;
     Common c{p->T, p->N, p->HK, p->HV, p->K, p->V, p->cu_seqlens, p->cu_seqlens_bits, p->g, p->beta,

@@ -240,6 +240,57 @@ typedef struct la_gdn_decode_params {
  */
 la_status gdn_decode(const la_gdn_decode_params* p, void* stream);
 
+/* Parameters of gdn_bwd.  Strides are in elements. */
+typedef struct la_gdn_bwd_params {
+    /* ---- the forward's inputs (natural-log gate, beta as given: no input transforms) ---- */
+    const void* q;    int64_t q_stride_t, q_stride_h;       /* [T, HK, K] bf16 */
+    const void* k;    int64_t k_stride_t, k_stride_h;       /* [T, HK, K] bf16 */
+    const void* v;    int64_t v_stride_t, v_stride_h;       /* [T, HV, V] bf16 */
+    const float* g;   int64_t g_stride_t, g_stride_h;       /* [T, HO] fp32 */
+    const float* beta; int64_t beta_stride_t, beta_stride_h; /* [T, HO] fp32 */
+    const void* cu_seqlens;
+    int32_t cu_seqlens_bits;
+    int64_t T;
+    int32_t N, HK, HV, K, V;
+    float scale;
+    int32_t use_qk_l2norm;
+    const void* initial_state;   /* [N, HO, K, V] or NULL */
+    int32_t initial_state_dtype;
+    /* states entering every chunk, as gdn_fwd writes them with checkpoint_every_n = 64 and
+       fp32 checkpoints ([sum ceil(L_i / 64), HO, K, V]); NULL: regenerated by a forward pass */
+    const float* checkpoints;
+    /* ---- incoming gradients ---- */
+    const void* d_o;  int64_t d_o_stride_t, d_o_stride_h;   /* [T, HO, V] bf16 */
+    const float* d_final_state;  /* [N, HO, K, V] fp32 or NULL (zero) */
+    /* ---- gradients (every one in its input's dtype; dg, dbeta fp32) ---- */
+    void* dq;         int64_t dq_stride_t, dq_stride_h;     /* [T, HK, K] bf16 */
+    void* dk;         int64_t dk_stride_t, dk_stride_h;     /* [T, HK, K] bf16 */
+    void* dv;         int64_t dv_stride_t, dv_stride_h;     /* [T, HV, V] bf16 */
+    float* dg;        int64_t dg_stride_t, dg_stride_h;     /* [T, HO] fp32 */
+    float* dbeta;     int64_t dbeta_stride_t, dbeta_stride_h; /* [T, HO] fp32 */
+    float* d_initial_state;      /* [N, HO, K, V] fp32 or NULL */
+    void* workspace;             /* >= la_gdn_bwd_workspace_bytes(...), 256-byte aligned, or NULL */
+    size_t workspace_bytes;
+    int32_t* status;
+} la_gdn_bwd_params;
+
+/*
+ * gdn_bwd -- the backward of gdn_fwd.
+ *
+ * Page: every variant has "a full backward", which reuses the forward's checkpoints at the
+ * chunk cadence.  Gradients of L = sum(d_o * o) + sum(d_final_state * final_state) with
+ * respect to q, k, v, g, beta and the initial state; grouped heads: dq and dk of a q/k head
+ * sum the contributions of its value heads.  When `checkpoints` is NULL the library first
+ * re-runs the forward with fp32 checkpoints every 64 tokens into the workspace.  Each
+ * (sequence, head) runs in a fixed order, so results do not depend on the batch around a
+ * sequence.  The gate and beta transforms of gdn_fwd are forward-only.
+ */
+la_status gdn_bwd(const la_gdn_bwd_params* p, void* stream);
+
+/* Bytes of device workspace gdn_bwd needs (checkpoints_given = 0 when they are regenerated). */
+size_t la_gdn_bwd_workspace_bytes(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, int32_t V,
+                                  int32_t checkpoints_given);
+
 /* Bytes of device workspace gdn_fwd (summary = 0) or gdn_summary (summary = 1) needs. */
 size_t la_gdn_workspace_bytes(int32_t N, int32_t summary);
 

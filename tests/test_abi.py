@@ -48,7 +48,8 @@ def _c_layout(struct_name, fields):
 
 @pytest.mark.parametrize("cls,cname", [(B.GdnFwdParams, "la_gdn_fwd_params"),
                                        (B.GdnSummaryParams, "la_gdn_summary_params"),
-                                       (B.GdnDecodeParams, "la_gdn_decode_params")])
+                                       (B.GdnDecodeParams, "la_gdn_decode_params"),
+                                       (B.GdnBwdParams, "la_gdn_bwd_params")])
 def test_ctypes_mirror_matches_c_layout(cls, cname):
     names = [f[0] for f in cls._fields_]
     size, offs = _c_layout(cname, names)
@@ -202,6 +203,7 @@ def test_null_params():
     assert lib.gdn_fwd(None, None) == B.LA_ERR_INVALID_ARG
     assert lib.gdn_summary(None, None) == B.LA_ERR_INVALID_ARG
     assert lib.gdn_decode(None, None) == B.LA_ERR_INVALID_ARG
+    assert lib.gdn_bwd(None, None) == B.LA_ERR_INVALID_ARG
 
 
 def test_checkpoint_rows_host_helper():

@@ -1,0 +1,155 @@
+"""The backward (gdn_bwd) vs the fp64 oracle's reverse-mode gradients, through the C ABI.
+
+Tolerances (max|x - ref| / max|ref| per tensor): bf16 gradients (dq, dk, dv) 1e-2, as for o;
+fp32 gradients (dg, dbeta, d_initial_state) 2e-3, as for the fp32 states.  The loss is
+sum(d_o * o) + sum(d_final_state * final_state) with seeded N(0,1) cotangents."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import gated_delta_rule_29_gb300 as la
+from gated_delta_rule_29_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+BF16_TOL = 1e-2
+F32_TOL = 2e-3
+
+
+def dev():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return torch.device("cuda:0")
+
+
+def rel(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    den = np.abs(ref).max()
+    assert den > 0, "reference is all zero: the comparison would be vacuous"
+    return float(np.abs(got - ref).max() / den)
+
+
+def cotangents(w, seed, with_final=True):
+    gen = torch.Generator().manual_seed(seed)
+    T = int(w.cu_seqlens[-1])
+    do = torch.randn(T, w.HV, w.V, generator=gen).to(torch.bfloat16)
+    dfin = torch.randn(w.N, w.HV, w.K, w.V, generator=gen) if with_final else None
+    return do, dfin
+
+
+def run_bwd(w, do, dfin, l2=True, checkpoints=None, scale=None):
+    d = dev()
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    out = la.gdn_bwd(w.q.to(d), w.k.to(d), w.v.to(d), w.g.to(d), w.beta.to(d), w.cu_seqlens.to(d), do.to(d),
+                     use_qk_l2norm=l2, scale=scale,
+                     initial_state=None if w.initial_state is None else w.initial_state.to(d),
+                     d_final_state=None if dfin is None else dfin.to(d), checkpoints=checkpoints, status=status)
+    assert la.read_status(status) == 0
+    return [None if x is None else x.float().cpu().numpy() for x in out]
+
+
+def compare(w, got, ref, units=None, label=""):
+    names = ["dq", "dk", "dv", "dg", "dbeta", "d_initial_state"]
+    errs = {}
+    for name, x in zip(names, got):
+        if x is None or (name == "d_initial_state" and w.initial_state is None):
+            continue
+        r = ref[name]
+        if units is not None and name in ("dv", "dg", "dbeta"):
+            cu = w.cu_seqlens.numpy().astype(np.int64)
+            x = np.concatenate([x[cu[i]:cu[i + 1], h] for i, h in units])
+            r = np.concatenate([r[cu[i]:cu[i + 1], h] for i, h in units])
+        errs[name] = rel(x, r)
+    print(f"[parity] bwd {w.name}{label}: " + ", ".join(f"{k_} {v_:.2e}" for k_, v_ in errs.items()))
+    for name, e in errs.items():
+        assert e <= (BF16_TOL if name in ("dq", "dk", "dv") else F32_TOL), errs
+    return errs
+
+
+@pytest.mark.parametrize("K,V", [(64, 64), (128, 128), (64, 128), (128, 64)])
+def test_bwd_ragged_grouped_heads(K, V):
+    w = W.draw("bwd ragged", [1, 63, 64, 65, 200], 2, 4, K, V, seed=401 + K + V, initial_state=True,
+               slow_decay=True)
+    do, dfin = cotangents(w, 402)
+    got = run_bwd(w, do, dfin)
+    ref = oracle.gdn_bwd(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, do, initial_state=w.initial_state,
+                         d_final_state=dfin)
+    compare(w, got, ref)
+
+
+def test_bwd_page_distributions_no_final_no_start():
+    """The pages' gate and beta distributions (fast decay), no start state, no final-state
+    cotangent."""
+    w = W.draw("bwd page", [300, 129, 1000], 4, 4, 128, 128, seed=411)
+    do, _ = cotangents(w, 412, with_final=False)
+    got = run_bwd(w, do, None)
+    ref = oracle.gdn_bwd(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, do)
+    compare(w, got, ref)
+
+
+def test_bwd_without_l2norm():
+    """Keys and queries scaled to unit-order norms by hand, the kernel's norm off."""
+    w = W.draw("bwd no-norm", [150, 70], 1, 2, 64, 64, seed=421, initial_state=True, slow_decay=True)
+    w.q = (w.q.float() / 8.0).to(torch.bfloat16)
+    w.k = (w.k.float() / 8.0).to(torch.bfloat16)
+    do, dfin = cotangents(w, 422)
+    got = run_bwd(w, do, dfin, l2=False, scale=0.5)
+    ref = oracle.gdn_bwd(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, do, scale=0.5, use_qk_l2norm=False,
+                         initial_state=w.initial_state, d_final_state=dfin)
+    compare(w, got, ref)
+
+
+def test_bwd_reuses_forward_checkpoints_bitwise():
+    """Checkpoints every 64 tokens from gdn_fwd give bitwise the gradients of the regenerated path."""
+    w = W.draw("bwd ckpt", [130, 64, 257], 2, 2, 128, 128, seed=431, initial_state=True, slow_decay=True)
+    do, dfin = cotangents(w, 432)
+    d = dev()
+    _, _, ck = la.gdn_fwd(w.q.to(d), w.k.to(d), w.v.to(d), w.g.to(d), w.beta.to(d), w.cu_seqlens.to(d),
+                          initial_state=w.initial_state.to(d), checkpoint_every_n=64, checkpoint_dtype=torch.float32)
+    a = run_bwd(w, do, dfin)
+    b = run_bwd(w, do, dfin, checkpoints=ck)
+    for x, y in zip(a, b):
+        assert np.array_equal(x, y)
+
+
+def test_bwd_batch_invariant():
+    """A sequence's gradients are bitwise the same alone and inside a batch."""
+    w = W.draw("bwd batch", [90, 200, 33, 128], 2, 2, 64, 64, seed=441, initial_state=True, slow_decay=True)
+    do, dfin = cotangents(w, 442)
+    full = run_bwd(w, do, dfin)
+    cu = w.cu_seqlens.numpy().astype(np.int64)
+    i = 1
+    sl = slice(cu[i], cu[i + 1])
+    sub = W.Workload(name="one", cu_seqlens=torch.tensor([0, cu[i + 1] - cu[i]]), q=w.q[sl], k=w.k[sl], v=w.v[sl],
+                     g=w.g[sl].contiguous(), beta=w.beta[sl].contiguous(), initial_state=w.initial_state[i:i + 1])
+    alone = run_bwd(sub, do[sl], dfin[i:i + 1])
+    for name, x, y in zip(["dq", "dk", "dv", "dg", "dbeta"], full[:5], alone[:5]):
+        assert np.array_equal(x[sl], y), name
+    assert np.array_equal(full[5][i], alone[5][0])
+
+
+def test_bwd_dense_batch_sampled():
+    """The dense batch (T = 65536, H = 32, K = V = 128, start state): the oracle recomputes two
+    sampled (sequence, head) units."""
+    w = W.config(3)
+    do, dfin = cotangents(w, 451)
+    got = run_bwd(w, do, dfin)
+    units = [(0, 0), (6, 21)]
+    mask = np.zeros((w.N, w.HV), dtype=bool)
+    for i, h in units:
+        mask[i, h] = True
+    ref = oracle.gdn_bwd(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, do, initial_state=w.initial_state,
+                         d_final_state=dfin, unit_mask=mask)
+    cu = w.cu_seqlens.numpy().astype(np.int64)
+    # per-unit rows of every gradient (dq / dk rows of a unit's q/k head: H = HK here)
+    errs = {}
+    for name, x in zip(["dq", "dk", "dv", "dg", "dbeta"], got[:5]):
+        xs = np.concatenate([x[cu[i]:cu[i + 1], h] for i, h in units])
+        rs = np.concatenate([ref[name][cu[i]:cu[i + 1], h] for i, h in units])
+        errs[name] = rel(xs, rs)
+    errs["d_initial_state"] = rel(np.stack([got[5][i, h] for i, h in units]),
+                                  np.stack([ref["d_initial_state"][i, h] for i, h in units]))
+    print("[parity] bwd dense batch sampled: " + ", ".join(f"{k_} {v_:.2e}" for k_, v_ in errs.items()))
+    for name, e in errs.items():
+        assert e <= (BF16_TOL if name in ("dq", "dk", "dv") else F32_TOL), errs
