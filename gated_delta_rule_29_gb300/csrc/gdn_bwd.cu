@@ -37,8 +37,6 @@ namespace {
 constexpr int kBT = 256;   // threads
 constexpr int kC = 64;     // chunk
 constexpr int kVT = 16;    // value columns per tile
-constexpr int kPC = kC + 1;     // padded row strides (fp32 words)
-constexpr int kPT = kVT + 1;
 
 __device__ __forceinline__ float bfv(const uint16_t* p, int64_t i) {
     return __uint_as_float(static_cast<uint32_t>(p[i]) << 16);
@@ -48,39 +46,84 @@ __device__ __forceinline__ uint16_t f2b(float x) {
     return *reinterpret_cast<uint16_t*>(&h);
 }
 
+// Shared-memory layout of the key-length rows (K, Q, S^T, dS^T): the four KD/4-column slices
+// that four neighbouring threads read are staggered by 4 words, and the row stride is 4 mod 8
+// words, so that 16-byte reads of neighbouring rows or of the four slices hit distinct banks.
+template <int KD>
+__device__ __forceinline__ int colp(int d) { return d + (d / (KD / 4)) * 4; }
+
 template <int KD>
 struct BwdSmem {
-    static constexpr int PK = KD + 1;
+    static constexpr int PK = KD + 12;  // row stride of K / Q / S^T / dS^T (4 mod 8 words)
+    static constexpr int PC = kC + 4;   // row stride of the 64 x 64 matrices and of the tiles
     float Kh[kC * PK];      // normalised keys (rows past the end are zero)
     float Qh[kC * PK];      // normalised queries
-    float Tm[kC * kPC];     // T = (I + A)^{-1}
-    float Pm[kC * kPC];     // P (incl. lower)
-    float Gk[kC * kPC];     // (k_i . k_j) Gamma_ij, lower incl.
-    float dA[kC * kPC];     // accumulated over tiles
-    float dP[kC * kPC];
-    float SJ[KD * kPT];     // tile of the entering state
-    float dSJ[KD * kPT];    // tile of dS_next (then dS)
-    float VJ[kC * kPT], OJ[kC * kPT], X[kC * kPT], D[kC * kPT], dD[kC * kPT], dY[kC * kPT];
+    float Tm[kC * PC];      // T = (I + A)^{-1}
+    float Pm[kC * PC];      // P (lower incl.)
+    float Gk[kC * PC];      // (k_i . k_j) Gamma_ij, lower incl.
+    float dA[kC * PC];      // accumulated over tiles, then M
+    float dP[kC * PC];      // accumulated over tiles, then H
+    // value tiles, stored transposed: row = value column cc, contiguous along the token / key index
+    float SJ[kVT * PK];     // S[:, tile]^T
+    float dSJ[kVT * PK];    // dS_next[:, tile]^T
+    float X[kVT * PC], Y[kVT * PC], D[kVT * PC], dD[kVT * PC], dY[kVT * PC];
+    float VJ[kVT * PC], OJ[kVT * PC], QS[kVT * PC], KdS[kVT * PC];
     float beta[kC], b[kC], gam[kC], GC[kC], rk[kC], rq[kC];
     float dbeta[kC], db[kC], wv[kC];
     float red[kBT / 32];
 };
 
-// out[r][c] (+)= alpha * sum_m L(r, m) R(m, c) for an RxC output spread over the CTA.
-template <int R, int CC, int MM, class FL, class FR, class FO>
-__device__ __forceinline__ void cta_mm(FL L, FR Rm, FO out) {
-    constexpr int PER = R * CC / kBT;
-    static_assert(R * CC % kBT == 0, "tile");
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
+    return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, acc))));
+}
+
+// out[c][r] = sum_m Lt[c][m] * R[r][m] for a kVT x kC output (c = value column, r = token),
+// both operands contiguous along m in groups of 4 (column map CM); each thread computes
+// rows r, r + 16, r + 32, r + 48 of one column.
+template <int MM, class CM, class FO>
+__device__ __forceinline__ void tile_nt(const float* Lt, int ldl, const float* R, int ldr, CM cm, FO out) {
     const int tid = threadIdx.x;
+    const int c = tid >> 4, r = tid & 15;
+    float4 acc[4];
 #pragma unroll
-    for (int e = 0; e < PER; ++e) {
-        const int idx = tid + e * kBT;
-        const int r = idx / CC, c = idx % CC;
-        float acc = 0.f;
-#pragma unroll 8
-        for (int m = 0; m < MM; ++m) acc = fmaf(L(r, m), Rm(m, c), acc);
-        out(r, c, acc);
+    for (int e = 0; e < 4; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int m = 0; m < MM; m += 4) {
+        const int mp = cm(m);
+        const float4 l = ld4(Lt + c * ldl + mp);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float4 rv = ld4(R + (r + 16 * e) * ldr + mp);
+            acc[e].x = fmaf(l.x, rv.x, acc[e].x);
+            acc[e].y = fmaf(l.y, rv.y, acc[e].y);
+            acc[e].z = fmaf(l.z, rv.z, acc[e].z);
+            acc[e].w = fmaf(l.w, rv.w, acc[e].w);
+        }
     }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) out(c, r + 16 * e, (acc[e].x + acc[e].y) + (acc[e].z + acc[e].w));
+}
+
+// out[c][r] = sum_m Lt[c][m] * R[m][r] for a kVT x kC output, R contiguous along r.
+template <int MM, class FL, class FO>
+__device__ __forceinline__ void tile_nn(FL Lt, const float* R, int ldr, FO out) {
+    const int tid = threadIdx.x;
+    const int c = tid >> 4, r0 = (tid & 15) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int m = 0; m < MM; ++m) {
+        const float l = Lt(c, m);
+        const float4 rv = ld4(R + m * ldr + r0);
+        acc.x = fmaf(l, rv.x, acc.x);
+        acc.y = fmaf(l, rv.y, acc.y);
+        acc.z = fmaf(l, rv.z, acc.z);
+        acc.w = fmaf(l, rv.w, acc.w);
+    }
+    out(c, r0 + 0, acc.x);
+    out(c, r0 + 1, acc.y);
+    out(c, r0 + 2, acc.z);
+    out(c, r0 + 3, acc.w);
 }
 
 template <int KD, int VD>
@@ -88,6 +131,7 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
     extern __shared__ __align__(16) uint8_t smem_raw[];
     BwdSmem<KD>& s = *reinterpret_cast<BwdSmem<KD>*>(smem_raw);
     constexpr int PK = BwdSmem<KD>::PK;
+    constexpr int PC = BwdSmem<KD>::PC;
     const int tid = threadIdx.x;
     if (tid == 0) s.red[0] = __int_as_float(*reinterpret_cast<const volatile int32_t*>(&a.hdr->status));
     __syncthreads();
@@ -108,7 +152,7 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
     for (int64_t e = tid; e < KV; e += kBT) dSg[e] = a.dfinal ? a.dfinal[unit * KV + e] : 0.f;
     __syncthreads();
 
-    // thread ownership for the per-row accumulators of dK and dQ: row i, 32-column slice
+    // thread ownership for the per-row accumulators of dK and dQ: row i, KD/4-column slice
     constexpr int KSL = KD / 4;
     const int own_r = tid >> 2, own_c0 = (tid & 3) * KSL;
 
@@ -118,15 +162,24 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
         const float* Sc = a.ckpt + ((a.ckpt_off[seq] + c) * HO + h) * KV;  // state entering this chunk
 
         // ---- chunk-level quantities: normalised rows, decays, A, T, P
-        for (int e = tid; e < kC * KD; e += kBT) {
-            const int i = e / KD, d = e % KD;
-            float kv = 0.f, qv = 0.f;
+        for (int e = tid; e < kC * KD / 8; e += kBT) {
+            // 8 bf16 (16 bytes) per load: k and q rows are 16-byte aligned (TMA operand rules)
+            const int i = e / (KD / 8), d = (e % (KD / 8)) * 8;
+            uint4 kw = make_uint4(0u, 0u, 0u, 0u), qw = kw;
             if (i < n) {
-                kv = bfv(a.k, (t0 + i) * a.k_st + hk * a.k_sh + d);
-                qv = bfv(a.q, (t0 + i) * a.q_st + hk * a.q_sh + d);
+                kw = *reinterpret_cast<const uint4*>(a.k + (t0 + i) * a.k_st + hk * a.k_sh + d);
+                qw = *reinterpret_cast<const uint4*>(a.q + (t0 + i) * a.q_st + hk * a.q_sh + d);
             }
-            s.Kh[i * PK + d] = kv;
-            s.Qh[i * PK + d] = qv;
+            float* kd = &s.Kh[i * PK + colp<KD>(d)];
+            float* qd = &s.Qh[i * PK + colp<KD>(d)];
+            const uint32_t kk[4] = {kw.x, kw.y, kw.z, kw.w}, qq[4] = {qw.x, qw.y, qw.z, qw.w};
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                kd[2 * x] = __uint_as_float(kk[x] << 16);
+                kd[2 * x + 1] = __uint_as_float(kk[x] & 0xFFFF0000u);
+                qd[2 * x] = __uint_as_float(qq[x] << 16);
+                qd[2 * x + 1] = __uint_as_float(qq[x] & 0xFFFF0000u);
+            }
         }
         if (tid < kC) {
             const int i = tid;
@@ -134,27 +187,43 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
             s.b[i] = i < n ? a.g[(t0 + i) * a.g_st + h * a.g_sh] : 0.f;
         }
         __syncthreads();
-        if (tid < kC) {
-            // row norms (one thread per row; K is at most 128) and the chunk-local cumsum of g
-            const int i = tid;
+        {
+            // row norms: four threads per row (rows = tid / 4), quarter rows each
+            const int i = tid >> 2, q4 = tid & 3;
             float sk = 0.f, sq = 0.f;
-            for (int d = 0; d < KD; ++d) {
-                sk = fmaf(s.Kh[i * PK + d], s.Kh[i * PK + d], sk);
-                sq = fmaf(s.Qh[i * PK + d], s.Qh[i * PK + d], sq);
+#pragma unroll 4
+            for (int d = q4 * KSL; d < (q4 + 1) * KSL; d += 4) {
+                const float4 kv = ld4(&s.Kh[i * PK + colp<KD>(d)]), qv = ld4(&s.Qh[i * PK + colp<KD>(d)]);
+                sk = dot4(kv, kv, sk);
+                sq = dot4(qv, qv, sq);
             }
-            s.rk[i] = (i < n && a.l2norm) ? 1.0f / sqrtf(sk + 1e-6f) : (i < n ? 1.f : 0.f);
-            s.rq[i] = (i < n && a.l2norm) ? 1.0f / sqrtf(sq + 1e-6f) : (i < n ? 1.f : 0.f);
+            sk += __shfl_xor_sync(0xffffffffu, sk, 1);
+            sk += __shfl_xor_sync(0xffffffffu, sk, 2);
+            sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+            sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+            if (q4 == 0) {
+                s.rk[i] = (i < n && a.l2norm) ? 1.0f / sqrtf(sk + 1e-6f) : (i < n ? 1.f : 0.f);
+                s.rq[i] = (i < n && a.l2norm) ? 1.0f / sqrtf(sq + 1e-6f) : (i < n ? 1.f : 0.f);
+            }
         }
-        if (tid == 64) {
-            float acc = 0.f;
-            for (int i = 0; i < kC; ++i) {
-                acc += s.b[i];
-                s.b[i] = acc;  // rows past the end carry g = 0, so b stays at b_last
+        if (tid < 32) {
+            // chunk-local inclusive cumsum of g (rows past the end carry g = 0)
+            float x0 = s.b[tid], x1 = s.b[tid + 32];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y0 = __shfl_up_sync(0xffffffffu, x0, off), y1 = __shfl_up_sync(0xffffffffu, x1, off);
+                if (tid >= off) {
+                    x0 += y0;
+                    x1 += y1;
+                }
             }
+            x1 += __shfl_sync(0xffffffffu, x0, 31);
+            s.b[tid] = x0;
+            s.b[tid + 32] = x1;
         }
         __syncthreads();
         for (int e = tid; e < kC * KD; e += kBT) {
-            const int i = e / KD, d = e % KD;
+            const int i = e / KD, d = colp<KD>(e % KD);
             s.Kh[i * PK + d] *= s.rk[i];
             s.Qh[i * PK + d] *= s.rq[i];
         }
@@ -166,42 +235,110 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
             s.db[tid] = 0.f;
         }
         __syncthreads();
-        // Gk = (k_i . k_j) Gamma_ij and P (lower incl.), zero dA / dP
-        for (int e = tid; e < kC * kC; e += kBT) {
-            const int i = e / kC, j = e % kC;
-            float kk = 0.f, qk = 0.f;
-            if (j <= i) {
-                for (int d = 0; d < KD; ++d) {
-                    kk = fmaf(s.Kh[i * PK + d], s.Kh[j * PK + d], kk);
-                    qk = fmaf(s.Qh[i * PK + d], s.Kh[j * PK + d], qk);
+        {
+            // Gk = (k_i . k_j) Gamma_ij and P = (q_i . k_j) Gamma_ij (lower incl.): 4 x 4 blocks
+            // rows i = 4 bi + x, columns j = bj + 16 y (neighbouring threads read neighbouring rows)
+            const int bi = tid >> 4, bj = tid & 15;
+            const int i0 = 4 * bi;
+            float kk[4][4], qk[4][4];
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+#pragma unroll
+                for (int y = 0; y < 4; ++y) kk[x][y] = qk[x][y] = 0.f;
+            if (bj <= i0 + 3) {
+#pragma unroll 2
+                for (int d = 0; d < KD; d += 4) {
+                    const int dp = colp<KD>(d);
+                    float4 ki[4], qi[4], kj[4];
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        ki[x] = ld4(&s.Kh[(i0 + x) * PK + dp]);
+                        qi[x] = ld4(&s.Qh[(i0 + x) * PK + dp]);
+                        kj[x] = ld4(&s.Kh[(bj + 16 * x) * PK + dp]);
+                    }
+#pragma unroll
+                    for (int x = 0; x < 4; ++x)
+#pragma unroll
+                        for (int y = 0; y < 4; ++y) {
+                            kk[x][y] = dot4(ki[x], kj[y], kk[x][y]);
+                            qk[x][y] = dot4(qi[x], kj[y], qk[x][y]);
+                        }
                 }
-                const float G = expf(s.b[i] - s.b[j]);
-                kk *= G;
-                qk *= G;
             }
-            s.Gk[i * kPC + j] = kk;
-            s.Pm[i * kPC + j] = qk;
-            s.dA[i * kPC + j] = 0.f;
-            s.dP[i * kPC + j] = 0.f;
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+#pragma unroll
+                for (int y = 0; y < 4; ++y) {
+                    const int i = i0 + x, j = bj + 16 * y;
+                    const float G = j <= i ? expf(s.b[i] - s.b[j]) : 0.f;
+                    s.Gk[i * PC + j] = kk[x][y] * G;
+                    s.Pm[i * PC + j] = qk[x][y] * G;
+                    s.dA[i * PC + j] = 0.f;
+                    s.dP[i * PC + j] = 0.f;
+                }
         }
         __syncthreads();
-        // T = (I + A)^{-1}: column j by forward substitution, one thread per column
-        if (tid < kC) {
-            const int j = tid;
-            for (int i = 0; i < kC; ++i) {
-                float t = (i == j) ? 1.f : 0.f;
-                if (i > j) {
-                    float acc = 0.f;
-                    for (int m = j; m < i; ++m) acc = fmaf(s.beta[i] * s.Gk[i * kPC + m], s.Tm[m * kPC + j], acc);
-                    t = -acc;
-                } else if (i < j) {
-                    t = 0.f;
+        {
+            // T = (I + A)^{-1}, A = strict_tril(beta_i Gk_ij), in 16 x 16 blocks: the diagonal
+            // blocks by substitution (warp w, lane = column), then the blocks below by
+            // T[bi][bj] = -T[bi][bi] sum_{m = bj}^{bi - 1} A[bi][m] T[m][bj], one level of block
+            // distance at a time (scratch: the dD tile, not yet in use)
+            const int w = tid >> 5, lane = tid & 31;
+            if (w < 4 && lane < 16) {
+                const int o = 16 * w, cc = lane;
+                float acc[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float tj = ((j == cc) ? 1.f : 0.f) - acc[j];
+                    s.Tm[(o + j) * PC + o + cc] = tj;
+#pragma unroll
+                    for (int i = j + 1; i < 16; ++i)
+                        acc[i] = fmaf(s.beta[o + i] * s.Gk[(o + i) * PC + o + j], tj, acc[i]);
                 }
-                s.Tm[i * kPC + j] = t;
+            }
+            // the blocks above the diagonal are zero
+            for (int e = tid; e < 6 * 256; e += kBT) {
+                const int blk = e >> 8, i = (e >> 4) & 15, j = e & 15;
+                const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
+                const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
+                s.Tm[(16 * bi + i) * PC + 16 * bj + j] = 0.f;
+            }
+            __syncthreads();
+            float* Ysc = s.dD + w * 256;
+#pragma unroll 1
+            for (int d = 1; d < 4; ++d) {
+                if (w < 4 - d) {
+                    const int bj = w, bi = w + d;
+                    const int r = lane >> 1, c0 = (lane & 1) * 8;
+                    float y[8];
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) y[x] = 0.f;
+                    for (int m = 16 * bj; m < 16 * bi; ++m) {
+                        const float am = s.beta[16 * bi + r] * s.Gk[(16 * bi + r) * PC + m];
+#pragma unroll
+                        for (int x = 0; x < 8; ++x) y[x] = fmaf(am, s.Tm[m * PC + 16 * bj + c0 + x], y[x]);
+                    }
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) Ysc[r * 16 + c0 + x] = y[x];
+                    __syncwarp();
+                    float t[8];
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) t[x] = 0.f;
+#pragma unroll
+                    for (int k = 0; k < 16; ++k) {
+                        const float tk = s.Tm[(16 * bi + r) * PC + 16 * bi + k];
+#pragma unroll
+                        for (int x = 0; x < 8; ++x) t[x] = fmaf(tk, Ysc[k * 16 + c0 + x], t[x]);
+                    }
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) s.Tm[(16 * bi + r) * PC + 16 * bj + c0 + x] = -t[x];
+                    __syncwarp();
+                }
+                __syncthreads();
             }
         }
-        __syncthreads();
-
         float dKacc[KSL], dQacc[KSL];
 #pragma unroll
         for (int e = 0; e < KSL; ++e) dKacc[e] = dQacc[e] = 0.f;
@@ -210,8 +347,8 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
         for (int j0 = 0; j0 < VD; j0 += kVT) {
             for (int e = tid; e < KD * kVT; e += kBT) {
                 const int r = e / kVT, cc = e % kVT;
-                s.SJ[r * kPT + cc] = Sc[r * VD + j0 + cc];
-                s.dSJ[r * kPT + cc] = dSg[r * VD + j0 + cc];
+                s.SJ[cc * PK + colp<KD>(r)] = Sc[r * VD + j0 + cc];
+                s.dSJ[cc * PK + colp<KD>(r)] = dSg[r * VD + j0 + cc];
             }
             for (int e = tid; e < kC * kVT; e += kBT) {
                 const int i = e / kVT, cc = e % kVT;
@@ -220,168 +357,215 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
                     vv = bfv(a.v, (t0 + i) * a.v_st + h * a.v_sh + j0 + cc);
                     ov = bfv(a.dout, (t0 + i) * a.do_st + h * a.do_sh + j0 + cc);
                 }
-                s.VJ[i * kPT + cc] = vv;
-                s.OJ[i * kPT + cc] = ov;
+                s.VJ[cc * PC + i] = vv;
+                s.OJ[cc * PC + i] = ov;
             }
             __syncthreads();
-            // x = K S_J
-            cta_mm<kC, kVT, KD>([&](int r, int m) { return s.Kh[r * PK + m]; },
-                                [&](int m, int cc) { return s.SJ[m * kPT + cc]; },
-                                [&](int r, int cc, float acc) { s.X[r * kPT + cc] = acc; });
+            // x = K S_J, Q S_J, K dS_J (transposed tiles)
+            auto ck = [](int m) { return colp<KD>(m); };
+            auto cc_id = [](int m) { return m; };
+            tile_nt<KD>(s.SJ, PK, s.Kh, PK, ck, [&](int cc, int r, float v) {
+                s.X[cc * PC + r] = v;
+                s.Y[cc * PC + r] = s.beta[r] * (s.VJ[cc * PC + r] - s.gam[r] * v);
+            });
+            tile_nt<KD>(s.SJ, PK, s.Qh, PK, ck, [&](int cc, int r, float v) { s.QS[cc * PC + r] = v; });
+            tile_nt<KD>(s.dSJ, PK, s.Kh, PK, ck, [&](int cc, int r, float v) { s.KdS[cc * PC + r] = v; });
             __syncthreads();
-            // D = T Y with Y = beta V - beta gamma x; dD = scale P^T dO + Gamma_C (K dS_J)
-            cta_mm<kC, kVT, kC>([&](int r, int m) { return s.Tm[r * kPC + m]; },
-                                [&](int m, int cc) {
-                                    return s.beta[m] * (s.VJ[m * kPT + cc] - s.gam[m] * s.X[m * kPT + cc]);
-                                },
-                                [&](int r, int cc, float acc) { s.D[r * kPT + cc] = acc; });
-            cta_mm<kC, kVT, KD>([&](int r, int m) { return s.Kh[r * PK + m]; },
-                                [&](int m, int cc) { return s.dSJ[m * kPT + cc]; },
-                                [&](int r, int cc, float acc) { s.dD[r * kPT + cc] = s.GC[r] * acc; });
+            // D = T Y;  dD = scale P^T dO + Gamma_C (K dS_J)
+            tile_nt<kC>(s.Y, PC, s.Tm, PC, cc_id, [&](int cc, int r, float v) { s.D[cc * PC + r] = v; });
+            tile_nn<kC>([&](int cc, int m) { return s.OJ[cc * PC + m]; }, s.Pm, PC,
+                        [&](int cc, int r, float v) { s.dD[cc * PC + r] = a.scale * v + s.GC[r] * s.KdS[cc * PC + r]; });
             __syncthreads();
-            cta_mm<kC, kVT, kC>([&](int r, int m) { return s.Pm[m * kPC + r]; },
-                                [&](int m, int cc) { return s.OJ[m * kPT + cc]; },
-                                [&](int r, int cc, float acc) { s.dD[r * kPT + cc] += a.scale * acc; });
+            // dY = T^T dD
+            tile_nn<kC>([&](int cc, int m) { return s.dD[cc * PC + m]; }, s.Tm, PC,
+                        [&](int cc, int r, float v) { s.dY[cc * PC + r] = v; });
             __syncthreads();
-            // dY = T^T dD; dV = beta dY (final)
-            cta_mm<kC, kVT, kC>([&](int r, int m) { return s.Tm[m * kPC + r]; },
-                                [&](int m, int cc) { return s.dD[m * kPT + cc]; },
-                                [&](int r, int cc, float acc) {
-                                    s.dY[r * kPT + cc] = acc;
-                                    if (r < n) a.dv[(t0 + r) * a.dv_st + h * a.dv_sh + j0 + cc] = f2b(s.beta[r] * acc);
-                                });
-            __syncthreads();
-            // per-row sums: dbeta (Y's beta), db (Y's gamma and O's gamma)
+            // dV = beta dY (final): four consecutive columns of one row per thread
+            {
+                const int r = tid >> 2, c4 = (tid & 3) * 4;
+                if (r < n) {
+                    uint16_t* dst = a.dv + (t0 + r) * a.dv_st + h * a.dv_sh + j0 + c4;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) dst[e] = f2b(s.beta[r] * s.dY[(c4 + e) * PC + r]);
+                }
+            }
+            // per-row sums: dbeta (Y's beta), db (Y's gamma, O's gamma); the Gamma_Cj terms of
+            // S_next, w_j = Gamma_Cj sum_v (K dS_J)_jv D_jv, move from b_j to b_last
             if (tid < kC) {
                 const int i = tid;
-                float sb = 0.f, sg = 0.f, so = 0.f;
+                float sb = 0.f, sg = 0.f, so = 0.f, w = 0.f;
+#pragma unroll
                 for (int cc = 0; cc < kVT; ++cc) {
-                    const float dy = s.dY[i * kPT + cc], xv = s.X[i * kPT + cc];
-                    sb = fmaf(dy, s.VJ[i * kPT + cc] - s.gam[i] * xv, sb);
+                    const float dy = s.dY[cc * PC + i], xv = s.X[cc * PC + i];
+                    sb = fmaf(dy, s.VJ[cc * PC + i] - s.gam[i] * xv, sb);
                     sg = fmaf(dy, xv, sg);
-                    float qs = 0.f;
-                    for (int d = 0; d < KD; ++d) qs = fmaf(s.Qh[i * PK + d], s.SJ[d * kPT + cc], qs);
-                    so = fmaf(s.OJ[i * kPT + cc], qs, so);
+                    so = fmaf(s.OJ[cc * PC + i], s.QS[cc * PC + i], so);
+                    w = fmaf(s.KdS[cc * PC + i], s.D[cc * PC + i], w);
                 }
                 s.dbeta[i] += sb;
-                s.db[i] += s.gam[i] * (a.scale * so - s.beta[i] * sg);
-            } else if (tid < 2 * kC) {
-                // the Gamma_Cj terms of S_next: w_j = Gamma_Cj sum_v (K dS_J)_jv D_jv moves from b_j
-                // to b_last
-                const int j = tid - kC;
-                float w = 0.f;
-                for (int cc = 0; cc < kVT; ++cc) {
-                    float kd = 0.f;
-                    for (int d = 0; d < KD; ++d) kd = fmaf(s.Kh[j * PK + d], s.dSJ[d * kPT + cc], kd);
-                    w = fmaf(kd, s.D[j * kPT + cc], w);
-                }
-                s.wv[j] = w * s.GC[j];
+                s.db[i] += s.gam[i] * (a.scale * so - s.beta[i] * sg) - w * s.GC[i];
+                s.wv[i] = w * s.GC[i];
             }
             {
                 // gamma_last <dS_J, S_J>: the decay of the entering state into S_next
                 float p = 0.f;
                 for (int e = tid; e < KD * kVT; e += kBT) {
-                    const int r = e / kVT, cc = e % kVT;
-                    p = fmaf(s.dSJ[r * kPT + cc], s.SJ[r * kPT + cc], p);
+                    const int r = colp<KD>(e % KD), cc = e / KD;
+                    p = fmaf(s.dSJ[cc * PK + r], s.SJ[cc * PK + r], p);
                 }
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
                 if ((tid & 31) == 0) s.red[tid >> 5] = p;
             }
-            __syncthreads();
-            if (tid < kC) s.db[tid] -= s.wv[tid];
+            // dA += -dY D^T, dP += scale dO D^T (lower parts), 4 x 4 blocks
+            {
+                const int bi = tid >> 4, bj = tid & 15;
+                const int i0 = 4 * bi, jj0 = 4 * bj;
+                if (bj <= bi) {
+                    float ad[4][4], pd[4][4];
+#pragma unroll
+                    for (int x = 0; x < 4; ++x)
+#pragma unroll
+                        for (int y = 0; y < 4; ++y) ad[x][y] = pd[x][y] = 0.f;
+#pragma unroll 4
+                    for (int cc = 0; cc < kVT; ++cc) {
+                        const float4 yv = ld4(&s.dY[cc * PC + i0]), ov = ld4(&s.OJ[cc * PC + i0]);
+                        const float4 dv = ld4(&s.D[cc * PC + jj0]);
+                        const float yy[4] = {yv.x, yv.y, yv.z, yv.w}, oo[4] = {ov.x, ov.y, ov.z, ov.w};
+                        const float dd[4] = {dv.x, dv.y, dv.z, dv.w};
+#pragma unroll
+                        for (int x = 0; x < 4; ++x)
+#pragma unroll
+                            for (int y = 0; y < 4; ++y) {
+                                ad[x][y] = fmaf(yy[x], dd[y], ad[x][y]);
+                                pd[x][y] = fmaf(oo[x], dd[y], pd[x][y]);
+                            }
+                    }
+#pragma unroll
+                    for (int x = 0; x < 4; ++x)
+#pragma unroll
+                        for (int y = 0; y < 4; ++y) {
+                            const int i = i0 + x, j = jj0 + y;
+                            if (j < i) s.dA[i * PC + j] -= ad[x][y];
+                            if (j <= i) s.dP[i * PC + j] += a.scale * pd[x][y];
+                        }
+                }
+            }
+            {
+                // dK += dx S_J^T + Gamma_C D dS_J^T (dx = -beta gamma dY); dQ += scale gamma dO S_J^T
+                const int i = own_r;
+                const float bx = -s.beta[i] * s.gam[i], gc = s.GC[i], sg = a.scale * s.gam[i];
+#pragma unroll 2
+                for (int cc = 0; cc < kVT; ++cc) {
+                    const float fy = bx * s.dY[cc * PC + i], fd = gc * s.D[cc * PC + i], fo = sg * s.OJ[cc * PC + i];
+#pragma unroll
+                    for (int e = 0; e < KSL; e += 4) {
+                        const float4 sj = ld4(&s.SJ[cc * PK + colp<KD>(own_c0 + e)]);
+                        const float4 dsj = ld4(&s.dSJ[cc * PK + colp<KD>(own_c0 + e)]);
+                        dKacc[e + 0] = fmaf(fy, sj.x, fmaf(fd, dsj.x, dKacc[e + 0]));
+                        dKacc[e + 1] = fmaf(fy, sj.y, fmaf(fd, dsj.y, dKacc[e + 1]));
+                        dKacc[e + 2] = fmaf(fy, sj.z, fmaf(fd, dsj.z, dKacc[e + 2]));
+                        dKacc[e + 3] = fmaf(fy, sj.w, fmaf(fd, dsj.w, dKacc[e + 3]));
+                        dQacc[e + 0] = fmaf(fo, sj.x, dQacc[e + 0]);
+                        dQacc[e + 1] = fmaf(fo, sj.y, dQacc[e + 1]);
+                        dQacc[e + 2] = fmaf(fo, sj.z, dQacc[e + 2]);
+                        dQacc[e + 3] = fmaf(fo, sj.w, dQacc[e + 3]);
+                    }
+                }
+            }
             __syncthreads();
             if (tid == 0) {
                 float p = 0.f, w = 0.f;
-                for (int i = 0; i < kBT / 32; ++i) p += s.red[i];
+                for (int x = 0; x < kBT / 32; ++x) p += s.red[x];
                 for (int j = 0; j < kC; ++j) w += s.wv[j];
                 s.db[n - 1] += s.gam[n - 1] * p + w;
             }
-            // dA += -dY D^T, dP += scale dO D^T (lower parts)
-            for (int e = tid; e < kC * kC; e += kBT) {
-                const int i = e / kC, j = e % kC;
-                if (j > i) continue;
-                float ad = 0.f, pd = 0.f;
-#pragma unroll
-                for (int cc = 0; cc < kVT; ++cc) {
-                    ad = fmaf(s.dY[i * kPT + cc], s.D[j * kPT + cc], ad);
-                    pd = fmaf(s.OJ[i * kPT + cc], s.D[j * kPT + cc], pd);
-                }
-                if (j < i) s.dA[i * kPC + j] -= ad;
-                s.dP[i * kPC + j] += a.scale * pd;
-            }
-            // dK += dx S_J^T + Gamma_C D dS_J^T (dx = -beta gamma dY); dQ += scale gamma dO S_J^T
             {
-                const int i = own_r;
-                const float bx = -s.beta[i] * s.gam[i], gc = s.GC[i], sg = a.scale * s.gam[i];
+                // dS_J <- gamma_last dS_J + K^T dx + scale Q^T (gamma dO): column cc of dS, keys
+                // d .. d+3 per thread (KD x kVT outputs over 256 threads)
+                constexpr int PER = KD * kVT / (4 * kBT);  // float4 groups per thread
 #pragma unroll
-                for (int e = 0; e < KSL; ++e) {
-                    const int d = own_c0 + e;
-                    float ak = 0.f, aq = 0.f;
-#pragma unroll
-                    for (int cc = 0; cc < kVT; ++cc) {
-                        const float sj = s.SJ[d * kPT + cc];
-                        ak = fmaf(bx * s.dY[i * kPT + cc], sj, ak);
-                        ak = fmaf(gc * s.D[i * kPT + cc], s.dSJ[d * kPT + cc], ak);
-                        aq = fmaf(s.OJ[i * kPT + cc], sj, aq);
+                for (int e = 0; e < PER; ++e) {
+                    const int idx = tid + e * kBT;
+                    const int cc = idx % kVT, d = (idx / kVT) * 4;  // 16 threads: one row segment
+                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+                    for (int m = 0; m < kC; ++m) {
+                        const float fx = -s.beta[m] * s.gam[m] * s.dY[cc * PC + m];
+                        const float fo = a.scale * s.gam[m] * s.OJ[cc * PC + m];
+                        const float4 kv = ld4(&s.Kh[m * PK + colp<KD>(d)]), qv = ld4(&s.Qh[m * PK + colp<KD>(d)]);
+                        acc.x = fmaf(fx, kv.x, fmaf(fo, qv.x, acc.x));
+                        acc.y = fmaf(fx, kv.y, fmaf(fo, qv.y, acc.y));
+                        acc.z = fmaf(fx, kv.z, fmaf(fo, qv.z, acc.z));
+                        acc.w = fmaf(fx, kv.w, fmaf(fo, qv.w, acc.w));
                     }
-                    dKacc[e] += ak;
-                    dQacc[e] += sg * aq;
+                    const float gl = s.gam[n - 1];
+                    float* dst = dSg + static_cast<int64_t>(d) * VD + j0 + cc;
+                    const float4 old = ld4(&s.dSJ[cc * PK + colp<KD>(d)]);
+                    dst[0] = fmaf(gl, old.x, acc.x);
+                    dst[VD] = fmaf(gl, old.y, acc.y);
+                    dst[2 * VD] = fmaf(gl, old.z, acc.z);
+                    dst[3 * VD] = fmaf(gl, old.w, acc.w);
                 }
             }
-            __syncthreads();
-            // dS_J <- gamma_last dS_J + K^T dx + scale Q^T (gamma dO); back to the global buffer
-            cta_mm<KD, kVT, kC>([&](int r, int m) { return s.Kh[m * PK + r]; },
-                                [&](int m, int cc) { return -s.beta[m] * s.gam[m] * s.dY[m * kPT + cc]; },
-                                [&](int r, int cc, float acc) {
-                                    float qo = 0.f;
-                                    for (int m = 0; m < kC; ++m)
-                                        qo = fmaf(s.Qh[m * PK + r], s.gam[m] * s.OJ[m * kPT + cc], qo);
-                                    dSg[r * VD + j0 + cc] = s.gam[n - 1] * s.dSJ[r * kPT + cc] + acc + a.scale * qo;
-                                });
             __syncthreads();
         }
 
         // ---- tile-independent terms: A and P backward, dbeta, db, dg, the norms
-        if (tid < kC) {
-            const int i = tid;
+        {
+            // four threads per row i (j in quarter ranges), combined by shuffles
+            const int i = tid >> 2, q4 = tid & 3;
             float sb = 0.f, rowsum = 0.f, colsum = 0.f;
-            for (int j = 0; j < kC; ++j) {
+            for (int j = q4 * 16; j < q4 * 16 + 16; ++j) {
                 if (j < i) {
-                    sb = fmaf(s.dA[i * kPC + j], s.Gk[i * kPC + j], sb);
-                    rowsum += s.dA[i * kPC + j] * s.beta[i] * s.Gk[i * kPC + j];
+                    const float x = s.dA[i * PC + j] * s.Gk[i * PC + j];
+                    sb += x;
+                    rowsum = fmaf(x, s.beta[i], rowsum);
                 }
-                if (j <= i) rowsum += s.dP[i * kPC + j] * s.Pm[i * kPC + j];
-                if (j > i) colsum += s.dA[j * kPC + i] * s.beta[j] * s.Gk[j * kPC + i];
-                if (j >= i) colsum += s.dP[j * kPC + i] * s.Pm[j * kPC + i];
+                if (j <= i) rowsum = fmaf(s.dP[i * PC + j], s.Pm[i * PC + j], rowsum);
+                if (j > i) colsum = fmaf(s.dA[j * PC + i] * s.beta[j], s.Gk[j * PC + i], colsum);
+                if (j >= i) colsum = fmaf(s.dP[j * PC + i], s.Pm[j * PC + i], colsum);
             }
-            s.dbeta[i] += sb;
-            s.db[i] += rowsum - colsum;  // log Gamma_ij = b_i - b_j
+#pragma unroll
+            for (int off = 1; off < 4; off <<= 1) {
+                sb += __shfl_xor_sync(0xffffffffu, sb, off);
+                rowsum += __shfl_xor_sync(0xffffffffu, rowsum, off);
+                colsum += __shfl_xor_sync(0xffffffffu, colsum, off);
+            }
+            if (q4 == 0) {
+                s.dbeta[i] += sb;
+                s.db[i] += rowsum - colsum;  // log Gamma_ij = b_i - b_j
+            }
         }
         __syncthreads();
         // M = dA (.) beta_i Gamma (strict), H = dP (.) Gamma (incl.), in place
         for (int e = tid; e < kC * kC; e += kBT) {
             const int i = e / kC, j = e % kC;
             const float G = j <= i ? expf(s.b[i] - s.b[j]) : 0.f;
-            s.dA[i * kPC + j] = j < i ? s.dA[i * kPC + j] * s.beta[i] * G : 0.f;
-            s.dP[i * kPC + j] = j <= i ? s.dP[i * kPC + j] * G : 0.f;
+            s.dA[i * PC + j] = j < i ? s.dA[i * PC + j] * s.beta[i] * G : 0.f;
+            s.dP[i * PC + j] = j <= i ? s.dP[i * PC + j] * G : 0.f;
         }
         __syncthreads();
         {
-            // dK += M K + M^T K + H^T Q, dQ += H K
+            // dK += (M + M^T) K + H^T Q, dQ += H K
             const int i = own_r;
+#pragma unroll 2
+            for (int j = 0; j < kC; ++j) {
+                const float mk = s.dA[i * PC + j] + s.dA[j * PC + i];
+                const float hq = s.dP[j * PC + i], hk = s.dP[i * PC + j];
 #pragma unroll
-            for (int e = 0; e < KSL; ++e) {
-                const int d = own_c0 + e;
-                float ak = 0.f, aq = 0.f;
-                for (int j = 0; j < kC; ++j) {
-                    const float kj = s.Kh[j * PK + d];
-                    ak = fmaf(s.dA[i * kPC + j] + s.dA[j * kPC + i], kj, ak);
-                    ak = fmaf(s.dP[j * kPC + i], s.Qh[j * PK + d], ak);
-                    aq = fmaf(s.dP[i * kPC + j], kj, aq);
+                for (int e = 0; e < KSL; e += 4) {
+                    const float4 kj = ld4(&s.Kh[j * PK + colp<KD>(own_c0 + e)]);
+                    const float4 qj = ld4(&s.Qh[j * PK + colp<KD>(own_c0 + e)]);
+                    dKacc[e + 0] = fmaf(mk, kj.x, fmaf(hq, qj.x, dKacc[e + 0]));
+                    dKacc[e + 1] = fmaf(mk, kj.y, fmaf(hq, qj.y, dKacc[e + 1]));
+                    dKacc[e + 2] = fmaf(mk, kj.z, fmaf(hq, qj.z, dKacc[e + 2]));
+                    dKacc[e + 3] = fmaf(mk, kj.w, fmaf(hq, qj.w, dKacc[e + 3]));
+                    dQacc[e + 0] = fmaf(hk, kj.x, dQacc[e + 0]);
+                    dQacc[e + 1] = fmaf(hk, kj.y, dQacc[e + 1]);
+                    dQacc[e + 2] = fmaf(hk, kj.z, dQacc[e + 2]);
+                    dQacc[e + 3] = fmaf(hk, kj.w, dQacc[e + 3]);
                 }
-                dKacc[e] += ak;
-                dQacc[e] += aq;
             }
         }
         __syncthreads();
@@ -401,8 +585,8 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
             float pk = 0.f, pq = 0.f;
 #pragma unroll
             for (int e = 0; e < KSL; ++e) {
-                pk = fmaf(s.Kh[i * PK + own_c0 + e], dKacc[e], pk);
-                pq = fmaf(s.Qh[i * PK + own_c0 + e], dQacc[e], pq);
+                pk = fmaf(s.Kh[i * PK + colp<KD>(own_c0 + e)], dKacc[e], pk);
+                pq = fmaf(s.Qh[i * PK + colp<KD>(own_c0 + e)], dQacc[e], pq);
             }
             pk += __shfl_xor_sync(0xffffffffu, pk, 1);
             pk += __shfl_xor_sync(0xffffffffu, pk, 2);
@@ -413,19 +597,38 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
                 const float rkk = s.rk[i], rqq = s.rq[i];
 #pragma unroll
                 for (int e = 0; e < KSL; ++e) {
-                    const int d = own_c0 + e;
-                    float gk = dKacc[e], gq = dQacc[e];
                     if (a.l2norm) {
-                        gk = rkk * (gk - pk * s.Kh[i * PK + d]);
-                        gq = rqq * (gq - pq * s.Qh[i * PK + d]);
+                        dKacc[e] = rkk * (dKacc[e] - pk * s.Kh[i * PK + colp<KD>(own_c0 + e)]);
+                        dQacc[e] = rqq * (dQacc[e] - pq * s.Qh[i * PK + colp<KD>(own_c0 + e)]);
                     }
-                    const int64_t t = t0 + i;
-                    if (a.group == 1) {
-                        a.dk[t * a.dk_st + hk * a.dk_sh + d] = f2b(gk);
-                        a.dq[t * a.dq_st + hk * a.dq_sh + d] = f2b(gq);
-                    } else {
-                        a.dkh[(t * HO + h) * KD + d] = gk;
-                        a.dqh[(t * HO + h) * KD + d] = gq;
+                }
+                const int64_t t = t0 + i;
+                if (a.group == 1 && a.vec_out) {
+                    // 8 bf16 per 16-byte store (dq, dk rows 16-byte aligned)
+                    uint4* kd = reinterpret_cast<uint4*>(a.dk + t * a.dk_st + hk * a.dk_sh + own_c0);
+                    uint4* qd = reinterpret_cast<uint4*>(a.dq + t * a.dq_st + hk * a.dq_sh + own_c0);
+#pragma unroll
+                    for (int e = 0; e < KSL; e += 8) {
+                        uint32_t kw[4], qw[4];
+#pragma unroll
+                        for (int x = 0; x < 4; ++x) {
+                            kw[x] = static_cast<uint32_t>(f2b(dKacc[e + 2 * x])) | (static_cast<uint32_t>(f2b(dKacc[e + 2 * x + 1])) << 16);
+                            qw[x] = static_cast<uint32_t>(f2b(dQacc[e + 2 * x])) | (static_cast<uint32_t>(f2b(dQacc[e + 2 * x + 1])) << 16);
+                        }
+                        kd[e / 8] = make_uint4(kw[0], kw[1], kw[2], kw[3]);
+                        qd[e / 8] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < KSL; ++e) {
+                        const int d = own_c0 + e;
+                        if (a.group == 1) {
+                            a.dk[t * a.dk_st + hk * a.dk_sh + d] = f2b(dKacc[e]);
+                            a.dq[t * a.dq_st + hk * a.dq_sh + d] = f2b(dQacc[e]);
+                        } else {
+                            a.dkh[(t * HO + h) * KD + d] = dKacc[e];
+                            a.dqh[(t * HO + h) * KD + d] = dQacc[e];
+                        }
                     }
                 }
             }

@@ -155,6 +155,7 @@ struct BwdArgs {
     float* ds0;                      // [N, HO, K, V] or null
     float* dqh;                      // [T, HO, K] fp32 per value head (grouped heads)
     float* dkh;
+    int32_t vec_out;                 // dq, dk rows 16-byte aligned: 16-byte stores
 };
 
 // Launchers (return cudaError_t of the launch).

@@ -496,6 +496,8 @@ la_status gdn_bwd(const la_gdn_bwd_params* p, void* stream) {
     b.dg = p->dg; b.dg_st = p->dg_stride_t; b.dg_sh = p->dg_stride_h;
     b.dbeta = p->dbeta; b.db_st = p->dbeta_stride_t; b.db_sh = p->dbeta_stride_h;
     b.ds0 = p->d_initial_state;
+    b.vec_out = aligned(p->dq, 16) && aligned(p->dk, 16) && p->dq_stride_t % 8 == 0 && p->dk_stride_t % 8 == 0 &&
+                (p->HK == 1 || (p->dq_stride_h % 8 == 0 && p->dk_stride_h % 8 == 0));
     if (p->HV != p->HK) {
         b.dqh = reinterpret_cast<float*>(wb + BL.gh);
         b.dkh = b.dqh + static_cast<size_t>(p->T) * p->HV * p->K;
