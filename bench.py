@@ -494,6 +494,147 @@ def run_decode(args, world, rank, local):
     return 0
 
 
+BWD_METRIC = "GDN bwd tokens/s (T=65536,H=32,K=V=128; gradients of q,k,v,g,beta,initial state)"
+FP32_LANES_PER_SM = 128  # FP32 FMA lanes per SM (4 partitions x 32)
+
+
+def bwd_algorithmic_flops(lengths, HO, K, V, C=64):
+    """Arithmetic of the chunked backward per (chunk, head), counted from its products: G and P
+    (lower halves), the triangular inverse, K S / Q S / K dS, T Y, P^T dO, T^T dD, dA and dP
+    (lower halves), the dK / dQ tile terms, the dS update and the A / P backward."""
+    per = (2 * (C * (C + 1) // 2) * K * 2 + C ** 3 // 3 * 2 + 3 * C * K * V * 2 + 3 * C * C * V * 2
+           + 2 * (C * (C + 1) // 2) * V * 2 + 3 * C * K * V * 2 + 2 * K * C * V * 2 + 3 * C * C * K * 2)
+    chunks = sum((L + C - 1) // C for L in lengths)
+    return int(per * chunks * HO)
+
+
+def run_bwd_bench(args, world, rank, local):
+    """One step = gdn_bwd over the dense batch, reusing the forward's fp32 checkpoints every 64
+    tokens (the training flow: the forward dumps them, the backward reads them)."""
+    import gated_delta_rule_29_gb300 as la
+    from gated_delta_rule_29_gb300 import binding as B
+    from gated_delta_rule_29_gb300 import workloads as W
+
+    assert torch.cuda.is_available(), "bench needs a CUDA device (there is no CPU fallback)"
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lib = B.load()
+    w = W.config(3)
+    T, N, HK, HV, K, V = w.T, w.N, w.HK, w.HV, w.K, w.V
+    gen = torch.Generator().manual_seed(1009)
+    do_h = torch.randn(T, HV, V, generator=gen).to(torch.bfloat16)
+    dfin_h = torch.randn(N, HV, K, V, generator=gen)
+    q, k, v, g, b, cu, s0, do, dfin = (x.to(dev) for x in (w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens,
+                                                            w.initial_state, do_h, dfin_h))
+    _, _, ck = la.gdn_fwd(q, k, v, g, b, cu, initial_state=s0, checkpoint_every_n=64, checkpoint_dtype=torch.float32)
+    ws = torch.empty(lib.la_gdn_bwd_workspace_bytes(T, N, HK, HV, K, V, 1), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        return la.gdn_bwd(q, k, v, g, b, cu, do, initial_state=s0, d_final_state=dfin, checkpoints=ck,
+                          workspace=ws, status=status)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert la.read_status(status) == 0
+    stream = torch.cuda.current_stream()
+    k_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a_, b_ in k_ev:
+        a_.record(stream)
+        b_.record(stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(args.steps):
+            lib.la_set_kernel_timing_events(k_ev[i][0].cuda_event, k_ev[i][1].cuda_event)
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    kern_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in k_ev)
+    assert la.read_status(status) == 0
+    flops = bwd_algorithmic_flops(w.lengths(), HV, K, V)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        pass
+    sm_mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    alu_peak = sms * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12  # TFLOP/s, fp32 FMA
+    achieved = flops / (kern_ms * 1e-3) / 1e12
+
+    # end to end: the step's inputs, cotangents and checkpoints copied from pinned host memory,
+    # the gradients copied back, all inside the timed region
+    host_in = [x.pin_memory() for x in (w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, w.initial_state, do_h, dfin_h)]
+    host_ck = ck.cpu().pin_memory()
+    outs = step()
+    host_out = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in outs]
+    h2d = sum(x.numel() * x.element_size() for x in host_in) + host_ck.numel() * 4
+    d2h = sum(x.numel() * x.element_size() for x in host_out)
+
+    def e2e_step():
+        xs = [x.to(dev, non_blocking=True) for x in host_in]
+        ckd = host_ck.to(dev, non_blocking=True)
+        r = la.gdn_bwd(xs[0], xs[1], xs[2], xs[3], xs[4], xs[5], xs[7], initial_state=xs[6], d_final_state=xs[8],
+                       checkpoints=ckd, workspace=ws, status=status)
+        for hbuf, dbuf in zip(host_out, r):
+            hbuf.copy_(dbuf, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, min(args.steps, 5))
+    x0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    x1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(x0.elapsed_time(x1) / e2e_steps, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle  # CPU baseline only
+        cores = os.cpu_count() or 1
+        units = [(0, 0), (3, 5)]
+        mask = np.zeros((N, HV), dtype=bool)
+        for i_, h_ in units:
+            mask[i_, h_] = True
+        t0 = time.perf_counter()
+        oracle.gdn_bwd(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, do_h, initial_state=w.initial_state,
+                       d_final_state=dfin_h, unit_mask=mask, nthreads=cores)
+        dt = time.perf_counter() - t0
+        cpu = {"value": len(units) * 8192 / HV / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{len(units)} of {N * HV} (sequence, head) units x 8192 tokens ({dt:.1f} s), fp64 reverse "
+                         f"mode of the token recurrence, up to {cores} threads (one per unit)"}
+    if rank == 0:
+        line = {
+            "metric": BWD_METRIC, "value": T * world / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD + "; bwd with the forward's fp32 checkpoints every 64 tokens",
+                       "global_batch": N * world, "seq_len": 8192,
+                       "parallelism": "single GPU" if world == 1 else f"independent batches per GPU x{world}",
+                       "l2": "inputs larger than L2 (1.6 GB of q/k/v + 2.1 GB of checkpoints per step); no flush"},
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
+                         "frac": achieved / alu_peak, "traffic": None,
+                         "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} fp32 FMA lanes x 2 FLOP x {sm_mhz:.0f} MHz",
+                         "kernel": "gdn_bwd_kernel<128, 128>", "kernel_ms": kern_ms, "algorithmic_flops": flops},
+            "cpu_baseline": cpu,
+            "e2e": {"value": T * world / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "gpu_launches": args.steps * 2,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -506,9 +647,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--e2e-groups", type=int, default=4, help="sequence groups pipelined by gdn_fwd_host")
-    ap.add_argument("--workload", choices=["dense", "decode"], default="dense",
+    ap.add_argument("--workload", choices=["dense", "decode", "bwd"], default="dense",
                     help="dense: the chunked forward over the dense batch (the headline); "
-                         "decode: one decode step against a state pool")
+                         "decode: one decode step against a state pool; bwd: the backward of the dense batch")
     ap.add_argument("--seq-len", type=int, default=8192,
                     help="tokens per sequence of the dense batch (8192 is the benchmark workload)")
     args = ap.parse_args()
@@ -520,6 +661,8 @@ def main():
             return run_reference(args, world, rank)
         if args.workload == "decode":
             return run_decode(args, world, rank, local)
+        if args.workload == "bwd":
+            return run_bwd_bench(args, world, rank, local)
         return run_ours(args, world, rank, local)
     finally:
         if world > 1:
