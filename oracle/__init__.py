@@ -52,6 +52,8 @@ MUTATIONS = {
     11: "beta sigmoid of the negated logit",
     12: "bounded gate without the sigmoid",
     13: "state pool written back to slot i instead of state_indices[i]",
+    16: "GDP: decay applied before every update instead of once per token",
+    17: "GDP: output read after the first update of the token instead of the last",
     # planted in the backward
     14: "backward: decay gradient misses the erase path (uses dS instead of dS')",
     15: "backward: key gradient misses the S' dx term",
@@ -223,6 +225,40 @@ def gdn_fwd(q, k, v, g, beta, cu_seqlens, *, scale=None, use_qk_l2norm=True,
         dst = np.arange(idx.shape[0]) if mutation == 13 else idx
         out[dst] = r["final_state"]
         r["state_pool"] = out
+    return r
+
+
+def gdp_fwd(q, k, v, g, beta, cu_seqlens, num_householder, *, scale=None, use_qk_l2norm=True,
+            initial_state=None, checkpoint_every_n=0, unit_mask=None, nthreads=None, mutation=0):
+    """Gated DeltaProduct forward (cuDNN Linear Attention page: GDP runs on two timelines).
+
+    q: [T, HK, K] and g: [T, HO] have one row per token; k: [T*n, HK, K], v: [T*n, HV, V] and
+    beta: [T*n, HO] have n rows per token, update-major (token t's updates are rows t*n .. t*n+n-1).
+    Per token t: S <- exp(g_t) S, then for j = 0 .. n-1 the delta step
+    S <- S + beta_{t,j} k_{t,j} (v_{t,j} - S^T k_{t,j})^T, then o_t = scale S^T q_t.
+    num_householder == 1 is exactly gdn_fwd.  Written as that recurrence on the update timeline:
+    the gate enters at each token's first update (exp(0) = 1 at the others) and the query at its
+    last (the outputs at the other updates are not part of the result).
+    Checkpoints every n tokens: the states entering tokens 0, n, 2n, ... of each sequence.
+    """
+    n = int(num_householder)
+    q, k, v, g, beta = (_f64(x) for x in (q, k, v, g, beta))
+    cu = _i64(cu_seqlens)
+    T, HK, K = q.shape
+    HO = g.shape[1]
+    assert k.shape[0] == T * n and v.shape[0] == T * n and beta.shape[0] == T * n
+    ge = np.zeros((T * n, HO))
+    ge[0::n] = g
+    if mutation == 16:
+        ge[:] = np.repeat(g, n, axis=0)
+    qe = np.zeros((T * n, HK, K))
+    qe[(n - 1 if mutation != 17 else 0)::n] = q
+    if scale is None:
+        scale = 1.0 / np.sqrt(K)
+    r = _run(qe, k, v, ge, beta, cu * n, scale=scale, use_qk_l2norm=use_qk_l2norm, s0=initial_state,
+             want_final=True, checkpoint_every_n=checkpoint_every_n * n, want_o=True, want_transition=False,
+             unit_mask=unit_mask, nthreads=nthreads, mutation=0)
+    r["o"] = r["o"][(n - 1 if mutation != 17 else 0)::n]
     return r
 
 

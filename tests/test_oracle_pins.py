@@ -18,7 +18,9 @@ Every check below is an independent statement of what the Gated DeltaNet forward
   * the state pool (state_indices): one-token updates against the explicit
     factor form, written back to the named slots, other slots untouched;
   * the backward: every gradient against central finite differences of the
-    pinned forward (with and without the L2 norm, grouped heads, start state).
+    pinned forward (with and without the L2 norm, grouped heads, start state);
+  * GDP (several updates per token) against its definition as dense products of
+    the token's Householder-like factors, and n = 1 against GDN.
 test_planted_mistakes_are_caught plants each of the oracle's known mutations
 and requires at least one check to fail, so a plausible slip anywhere (a dropped
 term, a flipped sign, a wrong index or orientation) cannot pass unnoticed.
@@ -431,6 +433,46 @@ def check_backward_finite_differences(mutation=0):
     return worst
 
 
+def check_gdp_dense_products(mutation=0):
+    """GDP against its definition written as dense products: per token, S_t = exp(g_t) H_t S_{t-1}
+    + sum_j (prod_{i > j} (I - beta_i k_i k_i^T)) beta_j k_j v_j^T with H_t the product of the
+    token's n Householder-like factors (later updates on the left); o_t = scale S_t^T q_t.
+    Also num_householder = 1 against gdn_fwd."""
+    rng = np.random.default_rng(111)
+    n, lengths, HK, HV, K, V = 3, [4, 2], 1, 2, 3, 2
+    T = sum(lengths)
+    cu = np.array([0, 4, 6])
+    q = rng.standard_normal((T, HK, K))
+    k = rng.standard_normal((T * n, HK, K))
+    v = rng.standard_normal((T * n, HV, V))
+    g = -0.4 * rng.random((T, HV))
+    beta = rng.random((T * n, HV))
+    S0 = rng.standard_normal((2, HV, K, V))
+    r = oracle.gdp_fwd(q, k, v, g, beta, cu, n, scale=0.9, use_qk_l2norm=True, initial_state=S0, mutation=mutation)
+    worst = 0.0
+    for i in range(2):
+        for h in range(HV):
+            S = S0[i, h].copy()
+            for t in range(cu[i], cu[i + 1]):
+                H = np.eye(K)
+                add = np.zeros((K, V))
+                for j in range(n):
+                    kk = k[t * n + j, 0] / np.sqrt((k[t * n + j, 0] ** 2).sum() + 1e-6)
+                    F = np.eye(K) - beta[t * n + j, h] * np.outer(kk, kk)
+                    H = F @ H
+                    add = F @ add + beta[t * n + j, h] * np.outer(kk, v[t * n + j, h])
+                S = math.exp(g[t, h]) * H @ S + add
+                qq = q[t, 0] / np.sqrt((q[t, 0] ** 2).sum() + 1e-6)
+                worst = max(worst, _rel(r["o"][t, h], 0.9 * S.T @ qq))
+            worst = max(worst, _rel(r["final_state"][i, h], S))
+    # n = 1 is GDN
+    k1, v1, b1 = k[::n], v[::n], beta[::n]
+    r1 = oracle.gdp_fwd(q, k1, v1, g, b1, cu, 1, initial_state=S0, mutation=mutation)
+    f1 = oracle.gdn_fwd(q, k1, v1, g, b1, cu, initial_state=S0)
+    worst = max(worst, _rel(r1["o"], f1["o"]), _rel(r1["final_state"], f1["final_state"]))
+    return worst
+
+
 CHECKS = {
     "golden": (check_golden, 1e-12),
     "brute_force": (check_brute_force, 1e-12),
@@ -449,6 +491,7 @@ CHECKS = {
     "beta_sigmoid": (check_beta_sigmoid, 1e-14),
     "state_pool": (check_state_pool, 1e-13),
     "backward_finite_differences": (check_backward_finite_differences, 1e-6),
+    "gdp_dense_products": (check_gdp_dense_products, 1e-12),
 }
 
 
