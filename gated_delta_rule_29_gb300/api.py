@@ -90,7 +90,8 @@ def gdn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
             workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
             stream: Optional[torch.cuda.Stream] = None, a_log: Optional[torch.Tensor] = None,
             dt_bias: Optional[torch.Tensor] = None, gate_lower_bound: Optional[float] = None,
-            beta_sigmoid: bool = False, state_indices: Optional[torch.Tensor] = None
+            beta_sigmoid: bool = False, state_indices: Optional[torch.Tensor] = None,
+            num_householder: int = 1
             ) -> Tuple[torch.Tensor, Optional[torch.Tensor], Optional[torch.Tensor]]:
     """Chunked GDN forward.  Returns (o [T, HO, V] bf16, final_state [N, HO, K, V] fp32 or None,
     checkpoints [R, HO, K, V] or None).  Asynchronous on the current stream.
@@ -101,13 +102,28 @@ def gdn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
 
     state_indices ([N] int32): initial_state is then a contiguous state pool [P, HO, K, V]
     (fp32 or bf16); sequence i starts from pool[state_indices[i]] and its end state is
-    written back into that slot in place.  No final_state or checkpoints are returned."""
+    written back into that slot in place.  No final_state or checkpoints are returned.
+
+    num_householder n > 1 (Gated DeltaProduct): k, v and beta carry n rows per token, as the
+    update timeline [T * n, ...] or token-major [T, n, ...] (contiguous per token); q, g and o
+    keep one row per token."""
+    n = int(num_householder)
+    if n > 1:
+        T_ = q.shape[0]
+        if k.dim() == 4:
+            k = k.reshape(T_ * n, k.shape[2], k.shape[3])
+        if v.dim() == 4:
+            v = v.reshape(T_ * n, v.shape[2], v.shape[3])
+        if beta.dim() == 3:
+            beta = beta.reshape(T_ * n, beta.shape[2])
+        if k.shape[0] != T_ * n or v.shape[0] != T_ * n or beta.shape[0] != T_ * n:
+            raise ValueError(f"num_householder={n}: k, v and beta need {T_ * n} update rows")
     _check_thd("q", q, torch.bfloat16)
     _check_thd("k", k, torch.bfloat16)
     _check_thd("v", v, torch.bfloat16)
     _check_thd("g", g, torch.float32, heads_dim=False)
     _check_beta(beta, beta_sigmoid)
-    T, HK, K = k.shape
+    T, HK, K = q.shape
     HV, V = v.shape[1], v.shape[2]
     N = cu_seqlens.numel() - 1
     HO = HV
@@ -130,10 +146,12 @@ def gdn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
         R = checkpoint_rows_hint if checkpoint_rows_hint is not None else checkpoint_rows(cu_seqlens, checkpoint_every_n)
         checkpoints = torch.empty(R, HO, K, V, dtype=checkpoint_dtype, device=dev)
     if workspace is None:
-        workspace = torch.empty(workspace_bytes(N), dtype=torch.uint8, device=dev)
-    if initial_state is not None:
+        need = workspace_bytes(N) if n <= 1 else B.load().la_gdp_workspace_bytes(T, N, HK, HV, K, V, n)
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    if initial_state is not None and state_indices is None:
         initial_state = initial_state.contiguous()
     p = B.GdnFwdParams()
+    p.num_householder = n
     p.q, p.q_stride_t, p.q_stride_h = q.data_ptr(), q.stride(0), q.stride(1)
     p.k, p.k_stride_t, p.k_stride_h = k.data_ptr(), k.stride(0), k.stride(1)
     p.v, p.v_stride_t, p.v_stride_h = v.data_ptr(), v.stride(0), v.stride(1)

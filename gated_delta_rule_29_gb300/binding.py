@@ -40,6 +40,7 @@ EXPORTED_SYMBOLS = (
     "gdn_decode",
     "gdn_bwd",
     "la_gdn_bwd_workspace_bytes",
+    "la_gdp_workspace_bytes",
 )
 
 _i64 = ctypes.c_int64
@@ -68,6 +69,7 @@ class GdnFwdParams(ctypes.Structure):
         ("gate_mode", _i32), ("a_log", _vp), ("dt_bias", _vp), ("gate_lower_bound", ctypes.c_float),
         ("beta_sigmoid", _i32), ("beta_bf16", _i32),
         ("state_indices", _vp), ("state_pool_size", _i64),
+        ("num_householder", _i32),
     ]
 
 
@@ -116,6 +118,8 @@ def load(build_if_missing: bool = True):
         lib.gdn_fwd.argtypes = [ctypes.POINTER(GdnFwdParams), _vp]
         lib.gdn_bwd.restype = ctypes.c_int
         lib.gdn_bwd.argtypes = [ctypes.POINTER(GdnBwdParams), _vp]
+        lib.la_gdp_workspace_bytes.restype = ctypes.c_size_t
+        lib.la_gdp_workspace_bytes.argtypes = [_i64, _i32, _i32, _i32, _i32, _i32, _i32]
         lib.la_gdn_bwd_workspace_bytes.restype = ctypes.c_size_t
         lib.la_gdn_bwd_workspace_bytes.argtypes = [_i64, _i32, _i32, _i32, _i32, _i32, _i32]
         lib.gdn_decode.restype = ctypes.c_int

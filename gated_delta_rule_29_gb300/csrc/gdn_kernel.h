@@ -158,7 +158,28 @@ struct BwdArgs {
     int32_t vec_out;                 // dq, dk rows 16-byte aligned: 16-byte stores
 };
 
+// Gated DeltaProduct: the update timeline for the chunk kernel, and the per-token outputs.
+struct GdpArgs {
+    int64_t T;                       // tokens
+    int32_t N, HK, HO, K, V, n;      // n updates per token
+    const uint16_t* q; int64_t q_st, q_sh;
+    const float* g; int64_t g_st, g_sh;
+    const void* cu;
+    int32_t cu64;
+    int32_t gate_mode;
+    const float* a_log;
+    const float* dt_bias;
+    float gate_lb;
+    uint16_t* qe;                    // [T * n, HK, K] contiguous
+    float* ge;                       // [T * n, HO] contiguous
+    int64_t* cue;                    // [N + 1]
+    const uint16_t* oe;              // [T * n, HO, V] contiguous
+    uint16_t* o; int64_t o_st, o_sh;
+};
+
 // Launchers (return cudaError_t of the launch).
+cudaError_t launch_gdp_expand(const GdpArgs& a, cudaStream_t s);
+cudaError_t launch_gdp_gather(const GdpArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t s);

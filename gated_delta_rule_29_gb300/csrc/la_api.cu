@@ -265,10 +265,16 @@ la_status static_scratch_address(void** out) {
 
 }  // namespace
 
+namespace {
+la_status gdp_fwd(const la_gdn_fwd_params* p, void* stream);  // Gated DeltaProduct, below
+}  // namespace
+
 extern "C" {
 
 la_status gdn_fwd(const la_gdn_fwd_params* p, void* stream) {
     if (!p) return LA_ERR_INVALID_ARG;
+    if (p->num_householder > 1) return gdp_fwd(p, stream);
+    if (p->num_householder < 0) return LA_ERR_INVALID_ARG;
     Common c{p->T, p->N, p->HK, p->HV, p->K, p->V, p->cu_seqlens, p->cu_seqlens_bits, p->g, p->beta,
              p->beta_bf16 ? 2 : 4};
     la_status st = check_common(c);
@@ -376,6 +382,93 @@ la_status gdn_decode(const la_gdn_decode_params* p, void* stream) {
 }  // extern "C"
 
 namespace {
+struct GdpLayout {
+    size_t pro, qe, ge, cue, oe, total;
+};
+GdpLayout gdp_layout(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, int32_t V, int32_t n) {
+    GdpLayout L{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off += (bytes + 255) & ~size_t(255);
+        return at;
+    };
+    L.pro = take(la::ws_layout(N).total);
+    L.qe = take(static_cast<size_t>(T) * n * HK * K * 2);
+    L.ge = take(static_cast<size_t>(T) * n * HV * sizeof(float));
+    L.cue = take(static_cast<size_t>(N + 1) * sizeof(int64_t));
+    L.oe = take(static_cast<size_t>(T) * n * HV * V * 2);
+    L.total = off;
+    return L;
+}
+}  // namespace
+
+extern "C" size_t la_gdp_workspace_bytes(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, int32_t V,
+                                         int32_t n) {
+    if (T < 0 || N < 0 || HK <= 0 || HV <= 0 || n < 1) return 0;
+    if (n == 1) return la::ws_layout(N).total;
+    return gdp_layout(T, N, HK, HV, K, V, n).total;
+}
+
+namespace {
+// GDP: build the update timeline (query, gate, boundaries), run the GDN path on it, gather the
+// per-token outputs.
+la_status gdp_fwd(const la_gdn_fwd_params* p, void* stream) {
+    const int32_t n = p->num_householder;
+    if (p->N < 0 || p->HK <= 0 || p->HV <= 0 || p->T < 0) return LA_ERR_INVALID_ARG;
+    if ((p->K != 64 && p->K != 128) || (p->V != 64 && p->V != 128)) return LA_ERR_UNSUPPORTED;
+    if (p->HV % p->HK != 0) return LA_ERR_UNSUPPORTED;
+    if (p->T * n >= (int64_t(1) << 31) - 64) return LA_ERR_UNSUPPORTED;
+    if (p->cu_seqlens_bits != 32 && p->cu_seqlens_bits != 64) return LA_ERR_INVALID_ARG;
+    if (!p->cu_seqlens) return LA_ERR_INVALID_ARG;
+    if (p->T > 0) {
+        if (!p->q || !aligned(p->q, 16) || p->q_stride_t % 8 != 0 || (p->HK > 1 && p->q_stride_h % 8 != 0))
+            return LA_ERR_INVALID_ARG;
+        if (!p->g || !aligned(p->g, 4) || !p->o || !aligned(p->o, 2)) return LA_ERR_INVALID_ARG;
+    }
+    const GdpLayout GL = gdp_layout(p->T, p->N, p->HK, p->HV, p->K, p->V, n);
+    void* ws = p->workspace;
+    la_status st;
+    if (ws) {
+        if (p->workspace_bytes < GL.total || !aligned(ws, 256)) return LA_ERR_WORKSPACE;
+    } else if ((st = internal_workspace(GL.total, &ws)) != LA_OK) {
+        return st;
+    }
+    uint8_t* wb = static_cast<uint8_t*>(ws);
+    ChunkArgs tr;  // the gate transform is applied while the gate rows are built
+    std::memset(&tr, 0, sizeof(tr));
+    if ((st = set_transforms(tr, p->gate_mode, p->a_log, p->dt_bias, p->gate_lower_bound, p->beta_sigmoid,
+                             p->beta_bf16)) != LA_OK)
+        return st;
+    la::GdpArgs g;
+    std::memset(&g, 0, sizeof(g));
+    g.T = p->T; g.N = p->N; g.HK = p->HK; g.HO = p->HV; g.K = p->K; g.V = p->V; g.n = n;
+    g.q = static_cast<const uint16_t*>(p->q); g.q_st = p->q_stride_t; g.q_sh = p->q_stride_h;
+    g.g = p->g; g.g_st = p->g_stride_t; g.g_sh = p->g_stride_h;
+    g.cu = p->cu_seqlens; g.cu64 = p->cu_seqlens_bits == 64;
+    g.gate_mode = tr.gate_mode; g.a_log = tr.a_log; g.dt_bias = tr.dt_bias; g.gate_lb = tr.gate_lb;
+    g.qe = reinterpret_cast<uint16_t*>(wb + GL.qe);
+    g.ge = reinterpret_cast<float*>(wb + GL.ge);
+    g.cue = reinterpret_cast<int64_t*>(wb + GL.cue);
+    g.oe = reinterpret_cast<const uint16_t*>(wb + GL.oe);
+    g.o = static_cast<uint16_t*>(p->o); g.o_st = p->o_stride_t; g.o_sh = p->o_stride_h;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (la::launch_gdp_expand(g, s) != cudaSuccess) return LA_ERR_CUDA;
+    la_gdn_fwd_params f = *p;
+    f.num_householder = 1;
+    f.q = g.qe; f.q_stride_t = static_cast<int64_t>(p->HK) * p->K; f.q_stride_h = p->K;
+    f.g = g.ge; f.g_stride_t = p->HV; f.g_stride_h = 1;
+    f.gate_mode = LA_GATE_LOG; f.a_log = nullptr; f.dt_bias = nullptr;
+    f.cu_seqlens = g.cue; f.cu_seqlens_bits = 64;
+    f.T = p->T * n;
+    f.o = wb + GL.oe; f.o_stride_t = static_cast<int64_t>(p->HV) * p->V; f.o_stride_h = p->V;
+    f.checkpoint_every_n = p->checkpoints ? p->checkpoint_every_n * n : 0;
+    f.workspace = wb + GL.pro; f.workspace_bytes = la::ws_layout(p->N).total;
+    if ((st = gdn_fwd(&f, stream)) != LA_OK) return st;
+    if (la::launch_gdp_gather(g, s) != cudaSuccess) return LA_ERR_CUDA;
+    return LA_OK;
+}
+
 struct BwdLayout {
     size_t pro, ck, o, ds, gh, total;
 };

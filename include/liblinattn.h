@@ -117,6 +117,14 @@ typedef struct la_gdn_fwd_params {
      * status word and that sequence is skipped. */
     const int32_t* state_indices;
     int64_t state_pool_size;
+    /* ---- Gated DeltaProduct (page: GDP runs on two timelines) ----
+     * num_householder n > 1: k, v and beta hold n rows per token, update-major (the n updates
+     * of token t are rows t*n .. t*n+n-1; a contiguous token-major [T, n, H, D] view is the same
+     * memory), and their row strides above are per update row; q, g and o keep one row per
+     * token and T counts tokens.  Per token the state decays once (exp(g_t)), takes the n delta
+     * updates in order, and o_t reads the state after the last.  checkpoint_every_n counts
+     * tokens (n * checkpoint_every_n must be a multiple of 64).  0 or 1: GDN. */
+    int32_t num_householder;
 } la_gdn_fwd_params;
 
 /*
@@ -290,6 +298,10 @@ la_status gdn_bwd(const la_gdn_bwd_params* p, void* stream);
 /* Bytes of device workspace gdn_bwd needs (checkpoints_given = 0 when they are regenerated). */
 size_t la_gdn_bwd_workspace_bytes(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, int32_t V,
                                   int32_t checkpoints_given);
+
+/* Bytes of device workspace gdn_fwd needs with num_householder = n > 1 (the update timeline's
+   query, gate and output rows plus the chunk kernel's scratch); n <= 1: la_gdn_workspace_bytes. */
+size_t la_gdp_workspace_bytes(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, int32_t V, int32_t n);
 
 /* Bytes of device workspace gdn_fwd (summary = 0) or gdn_summary (summary = 1) needs. */
 size_t la_gdn_workspace_bytes(int32_t N, int32_t summary);

@@ -1,0 +1,92 @@
+"""Gated DeltaProduct (num_householder n > 1) through gdn_fwd vs the fp64 oracle's gdp_fwd.
+Tolerances as in test_gpu_parity: o 1e-2, fp32 states and checkpoints 2e-3."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import gated_delta_rule_29_gb300 as la
+
+pytestmark = pytest.mark.gpu
+
+O_TOL = 1e-2
+S_TOL = 2e-3
+
+
+def dev():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return torch.device("cuda:0")
+
+
+def rel(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    den = np.abs(ref).max()
+    assert den > 0, "reference is all zero: the comparison would be vacuous"
+    return float(np.abs(got - ref).max() / den)
+
+
+def gdp_case(lengths, n, HK, HV, K, V, seed, slow=True):
+    """The pages' distributions on both timelines: q, g per token; k, v, beta per update."""
+    gen = torch.Generator().manual_seed(seed)
+    T = sum(lengths)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32)
+    q = torch.randn(T, HK, K, generator=gen).to(torch.bfloat16)
+    k = torch.randn(T * n, HK, K, generator=gen).to(torch.bfloat16)
+    v = torch.randn(T * n, HV, V, generator=gen).to(torch.bfloat16)
+    g = -torch.nn.functional.softplus(torch.randn(T, HV, generator=gen))
+    beta = torch.sigmoid(torch.randn(T * n, HV, generator=gen))
+    if slow:
+        g, beta = g * 1e-3, beta * 0.2
+    s0 = 0.1 * torch.randn(len(lengths), HV, K, V, generator=gen)
+    return dict(q=q, k=k, v=v, g=g.contiguous(), beta=beta.contiguous(), cu=cu, s0=s0)
+
+
+def test_gdp_two_updates_checkpoints_grouped_heads():
+    n = 2
+    c = gdp_case([1, 31, 32, 33, 100], n, 2, 4, 128, 128, seed=501)
+    d = dev()
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    o, fin, ck = la.gdn_fwd(c["q"].to(d), c["k"].to(d), c["v"].to(d), c["g"].to(d), c["beta"].to(d), c["cu"].to(d),
+                            initial_state=c["s0"].to(d), checkpoint_every_n=32, checkpoint_dtype=torch.float32,
+                            num_householder=n, status=status)
+    assert la.read_status(status) == 0
+    ref = oracle.gdp_fwd(c["q"], c["k"], c["v"], c["g"], c["beta"], c["cu"], n, initial_state=c["s0"],
+                         checkpoint_every_n=32)
+    errs = {"o": rel(o.float().cpu(), ref["o"]), "final": rel(fin.cpu(), ref["final_state"]),
+            "ckpt": rel(ck.cpu(), ref["checkpoints"])}
+    print("[parity] gdp n=2: " + ", ".join(f"{k_} {v_:.2e}" for k_, v_ in errs.items()))
+    assert errs["o"] <= O_TOL and errs["final"] <= S_TOL and errs["ckpt"] <= S_TOL, errs
+
+
+def test_gdp_three_updates_token_major_transforms():
+    """n = 3 (chunks end inside tokens), token-major [T, n, H, D] inputs, the softplus gate and
+    beta logits in the kernel."""
+    n = 3
+    c = gdp_case([50, 7, 130], n, 1, 2, 64, 64, seed=511, slow=False)
+    gen = torch.Generator().manual_seed(512)
+    T = c["q"].shape[0]
+    g_raw = torch.randn(T, 2, generator=gen)
+    b_raw = torch.randn(T * n, 2, generator=gen)
+    a_log, dt_bias = torch.log(torch.tensor([0.05, 0.2])), torch.tensor([-1.0, 0.5])
+    d = dev()
+    k4 = c["k"].view(T, n, 1, 64).to(d)
+    v4 = c["v"].view(T, n, 2, 64).to(d)
+    b4 = b_raw.view(T, n, 2).to(d)
+    o, fin, _ = la.gdn_fwd(c["q"].to(d), k4, v4, g_raw.to(d), b4, c["cu"].to(d), initial_state=c["s0"].to(d),
+                           num_householder=n, a_log=a_log.to(d), dt_bias=dt_bias.to(d), beta_sigmoid=True)
+    g_log = oracle.gate_transform(g_raw, gate="softplus", a_log=a_log, dt_bias=dt_bias)
+    b = oracle.beta_transform(b_raw, beta_sigmoid=True)
+    ref = oracle.gdp_fwd(c["q"], c["k"], c["v"], g_log, b, c["cu"], n, initial_state=c["s0"])
+    errs = {"o": rel(o.float().cpu(), ref["o"]), "final": rel(fin.cpu(), ref["final_state"])}
+    print("[parity] gdp n=3: " + ", ".join(f"{k_} {v_:.2e}" for k_, v_ in errs.items()))
+    assert errs["o"] <= O_TOL and errs["final"] <= S_TOL, errs
+
+
+def test_gdp_one_update_is_gdn_bitwise():
+    c = gdp_case([100, 64], 1, 2, 2, 64, 64, seed=521)
+    d = dev()
+    args = [x.to(d) for x in (c["q"], c["k"], c["v"], c["g"], c["beta"], c["cu"])]
+    o1, f1, _ = la.gdn_fwd(*args, initial_state=c["s0"].to(d))
+    o2, f2, _ = la.gdn_fwd(*args, initial_state=c["s0"].to(d), num_householder=1)
+    assert torch.equal(o1, o2) and torch.equal(f1, f2)
