@@ -635,6 +635,91 @@ def run_bwd_bench(args, world, rank, local):
     return 0
 
 
+GDP_METRIC = "GDP fwd tokens/s and % of GB300 HBM roofline (T=65536 tokens x 2 updates, H=32, K=V=128)"
+
+
+def run_gdp_bench(args, world, rank, local):
+    """Gated DeltaProduct with 2 updates per token on the dense batch's shape: 8 x 8192 tokens,
+    32 heads, K = V = 128, q and g per token, k, v and beta per update, start and final state."""
+    import gated_delta_rule_29_gb300 as la
+    from gated_delta_rule_29_gb300 import binding as B
+
+    assert torch.cuda.is_available(), "bench needs a CUDA device (there is no CPU fallback)"
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lib = B.load()
+    n, N, L, H, K, V = 2, 8, 8192, 32, 128, 128
+    T = N * L
+    gen = torch.Generator().manual_seed(1010)
+    q_h = torch.randn(T, H, K, generator=gen).to(torch.bfloat16)
+    k_h = torch.randn(T * n, H, K, generator=gen).to(torch.bfloat16)
+    v_h = torch.randn(T * n, H, V, generator=gen).to(torch.bfloat16)
+    g_h = -torch.nn.functional.softplus(torch.randn(T, H, generator=gen))
+    b_h = torch.sigmoid(torch.randn(T * n, H, generator=gen))
+    s0_h = 0.1 * torch.randn(N, H, K, V, generator=gen)
+    cu_h = torch.arange(0, T + 1, L, dtype=torch.int32)
+    q, k, v, g, b, cu, s0 = (x.to(dev) for x in (q_h, k_h, v_h, g_h, b_h, cu_h, s0_h))
+    o = torch.empty(T, H, V, dtype=torch.bfloat16, device=dev)
+    fin = torch.empty(N, H, K, V, dtype=torch.float32, device=dev)
+    ws = torch.empty(lib.la_gdp_workspace_bytes(T, N, H, H, K, V, n), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        la.gdn_fwd(q, k, v, g, b, cu, initial_state=s0, o=o, final_state=fin, workspace=ws, status=status,
+                   num_householder=n)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert la.read_status(status) == 0
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    # algorithmic bytes: q, o, g per token; k, v, beta per update; start and final state
+    alg = T * H * K * 2 + T * H * V * 2 + T * H * 4 + T * n * H * (K * 2 + V * 2 + 4) + 2 * N * H * K * V * 4
+    hbm_peak, _, peak_src = load_peaks()
+    achieved = alg / (ms * 1e-3) / 1e9
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle  # CPU baseline only
+        cores = os.cpu_count() or 1
+        mask = np.zeros((N, H), dtype=bool)
+        mask[0, :cores] = True
+        t0 = time.perf_counter()
+        oracle.gdp_fwd(q_h, k_h, v_h, g_h, b_h, cu_h, n, initial_state=s0_h, unit_mask=mask, nthreads=cores)
+        dt = time.perf_counter() - t0
+        cpu = {"value": int(mask.sum()) * L / H / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{int(mask.sum())} of {N * H} (sequence, head) units x {L} tokens ({dt:.1f} s)"}
+    if rank == 0:
+        line = {
+            "metric": GDP_METRIC, "value": T * world / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"GDP n={n}: N={N} x {L} tokens, H={H}, K=V={K}, fp32 start and final state",
+                       "global_batch": N * world, "seq_len": L, "parallelism": "single GPU",
+                       "l2": "inputs larger than L2; no flush"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": None, "peak_source": peak_src,
+                         "kernel": "update-timeline build + gdn_chunk_kernel<128, fwd> + gather (whole step)",
+                         "algorithmic_bytes": alg},
+            "cpu_baseline": cpu,
+            "e2e": None,
+            "gpu_launches": 4 * args.steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -647,9 +732,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--e2e-groups", type=int, default=4, help="sequence groups pipelined by gdn_fwd_host")
-    ap.add_argument("--workload", choices=["dense", "decode", "bwd"], default="dense",
+    ap.add_argument("--workload", choices=["dense", "decode", "bwd", "gdp"], default="dense",
                     help="dense: the chunked forward over the dense batch (the headline); "
-                         "decode: one decode step against a state pool; bwd: the backward of the dense batch")
+                         "decode: one decode step against a state pool; bwd: the backward of the dense batch; "
+                         "gdp: Gated DeltaProduct with 2 updates per token")
     ap.add_argument("--seq-len", type=int, default=8192,
                     help="tokens per sequence of the dense batch (8192 is the benchmark workload)")
     args = ap.parse_args()
@@ -663,6 +749,8 @@ def main():
             return run_decode(args, world, rank, local)
         if args.workload == "bwd":
             return run_bwd_bench(args, world, rank, local)
+        if args.workload == "gdp":
+            return run_gdp_bench(args, world, rank, local)
         return run_ours(args, world, rank, local)
     finally:
         if world > 1:
