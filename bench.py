@@ -720,6 +720,99 @@ def run_gdp_bench(args, world, rank, local):
     return 0
 
 
+SUM_METRIC = "GDN summary tokens/s and % of GB300 roofline (one 131072-token sequence, 8 spans, H=16, K=V=128)"
+
+
+def run_summary_bench(args, world, rank, local):
+    """gdn_summary over the context-parallel workload: one 131072-token sequence cut into 8 spans
+    of 16384, 16 heads, K = V = 128: per span and head the end state from a zero start and the
+    fp32 K x K transition."""
+    import gated_delta_rule_29_gb300 as la
+    from gated_delta_rule_29_gb300 import binding as B
+    from gated_delta_rule_29_gb300 import workloads as W
+
+    assert torch.cuda.is_available(), "bench needs a CUDA device (there is no CPU fallback)"
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lib = B.load()
+    w = W.config(5)
+    T, HK, HV, K, V = w.T, w.HK, w.HV, w.K, w.V
+    k, v, g, b, spans = (x.to(dev) for x in (w.k, w.v, w.g, w.beta, w.spans))
+    S = spans.numel() - 1
+    end = torch.empty(S, HV, K, V, dtype=torch.float32, device=dev)
+    tr = torch.empty(S, HV, K, K, dtype=torch.float32, device=dev)
+    ws = torch.empty(la.workspace_bytes(S, True), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        la.gdn_summary(k, v, g, b, spans, end_state=end, transition=tr, workspace=ws, status=status)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert la.read_status(status) == 0
+    stream = torch.cuda.current_stream()
+    k_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a_, b_ in k_ev:
+        a_.record(stream)
+        b_.record(stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(args.steps):
+            lib.la_set_kernel_timing_events(k_ev[i][0].cuda_event, k_ev[i][1].cuda_event)
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    kern_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in k_ev)
+    # algorithmic bytes: k, v (bf16), g, beta (fp32) in; end states and transitions (fp32) out
+    alg = T * (HK * K + HV * V) * 2 + 2 * T * HV * 4 + S * HV * (K * V + K * K) * 4 + (S + 1) * 4
+    # algorithmic tensor work per 64-token chunk and head: the value tile and the transition tile
+    # each take K K^T, the K S product, T X, and the state update (K = V = 128)
+    C = 64
+    per_chunk = 2 * (2 * C * C * K + 2 * C * K * V + 2 * C * C * V + 2 * C * K * V)
+    flops = per_chunk * (T // C) * HV
+    hbm_peak, tc_peak, peak_src = load_peaks()
+    achieved = alg / (kern_ms * 1e-3) / 1e9
+    tflops = flops / (kern_ms * 1e-3) / 1e12
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle  # CPU baseline only
+        cores = os.cpu_count() or 1
+        mask = np.zeros((S, HV), dtype=bool)
+        mask[0, :min(HV, cores)] = True
+        t0 = time.perf_counter()
+        oracle.gdn_summary(w.k, w.v, w.g, w.beta, w.spans, unit_mask=mask, nthreads=cores)
+        dt = time.perf_counter() - t0
+        cpu = {"value": int(mask.sum()) * (T // S) / HV / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{int(mask.sum())} of {S * HV} (span, head) units x {T // S} tokens ({dt:.1f} s), fp64 "
+                         f"state and K x K transition recurrence"}
+    if rank == 0:
+        line = {
+            "metric": SUM_METRIC, "value": T * world / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "summary: one sequence of 131072 tokens, 8 spans of 16384, H=16, K=V=128, zero start",
+                       "global_batch": 1, "seq_len": T, "parallelism": "single GPU",
+                       "l2": "inputs larger than L2 (1.07 GB of k/v per step); no flush"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                         "frac": achieved / hbm_peak, "traffic": None, "peak_source": peak_src,
+                         "kernel": "gdn_chunk_kernel<128, summary>", "kernel_ms": kern_ms, "algorithmic_bytes": alg,
+                         "tensor_tflops": tflops, "tensor_frac": tflops / tc_peak, "algorithmic_flops": flops},
+            "cpu_baseline": cpu,
+            "e2e": None,
+            "gpu_launches": 2 * args.steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -731,11 +824,11 @@ def main():
     ap.add_argument("--ref-units", type=int, default=2, help="units per step of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
-    ap.add_argument("--e2e-groups", type=int, default=4, help="sequence groups pipelined by gdn_fwd_host")
-    ap.add_argument("--workload", choices=["dense", "decode", "bwd", "gdp"], default="dense",
+    ap.add_argument("--e2e-groups", type=int, default=8, help="sequence groups pipelined by gdn_fwd_host")
+    ap.add_argument("--workload", choices=["dense", "decode", "bwd", "gdp", "summary"], default="dense",
                     help="dense: the chunked forward over the dense batch (the headline); "
                          "decode: one decode step against a state pool; bwd: the backward of the dense batch; "
-                         "gdp: Gated DeltaProduct with 2 updates per token")
+                         "gdp: Gated DeltaProduct with 2 updates per token; summary: gdn_summary over 8 spans")
     ap.add_argument("--seq-len", type=int, default=8192,
                     help="tokens per sequence of the dense batch (8192 is the benchmark workload)")
     args = ap.parse_args()
@@ -751,6 +844,8 @@ def main():
             return run_bwd_bench(args, world, rank, local)
         if args.workload == "gdp":
             return run_gdp_bench(args, world, rank, local)
+        if args.workload == "summary":
+            return run_summary_bench(args, world, rank, local)
         return run_ours(args, world, rank, local)
     finally:
         if world > 1:
