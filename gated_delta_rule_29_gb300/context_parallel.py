@@ -9,6 +9,9 @@ composes the state entering its span,
 
 then runs gdn_fwd on its span from that state (cuDNN Linear Attention page,
 "Summaries": the summaries compose across spans to give context parallelism).
+The backward mirrors it: each rank's state gradient from its own outputs, one
+all-gather, and the reverse composition dS_enter = transition dS_exit give every
+rank the cotangent of its span's end state for gdn_bwd.
 The composition is a handful of small fp32 products per rank and runs on
 whatever device the tensors live on; the exchange is the only collective.
 """
@@ -39,6 +42,51 @@ def compose(transitions: List[torch.Tensor], end_states: List[torch.Tensor],
     return out
 
 
+def compose_grads(transitions: List[torch.Tensor], local_grads: List[torch.Tensor],
+                  d_final: Optional[torch.Tensor] = None) -> List[torch.Tensor]:
+    """Backward of compose: the state gradient entering and leaving each span.
+
+    The gradients are linear in the final-state cotangent, and through a span the state gradient
+    moves as dS_enter = einsum('ab,bv->av', transition, dS_exit) (the transpose of the forward
+    composition).  local_grads[r] is the entering-state gradient of span r from its own outputs
+    alone (gdn_bwd with a zero final-state cotangent); d_final the cotangent of the state after
+    the last span.  Returns len(spans) + 1 tensors: the gradient leaving each span (dS_exit_r,
+    the final-state cotangent to use for span r), then the gradient entering span 0.
+    """
+    S = len(transitions)
+    d_exit = [None] * S
+    d = d_final if d_final is not None else torch.zeros_like(local_grads[-1])
+    for r in range(S - 1, -1, -1):
+        d_exit[r] = d
+        d = local_grads[r] + torch.einsum("...ab,...bv->...av", transitions[r], d)
+    return d_exit + [d]
+
+
+def exit_state_grad(transition: torch.Tensor, local_grad: torch.Tensor,
+                    d_final: Optional[torch.Tensor] = None, group=None) -> torch.Tensor:
+    """Final-state cotangent for this rank's span in the context-parallel backward.
+
+    Ranks hold consecutive spans in rank order.  Each rank first runs gdn_bwd on its span with a
+    zero final-state cotangent (local_grad = its d_initial_state), then one all-gather of
+    (transition, local_grad) lets every rank compose the gradient arriving at its span's end;
+    running gdn_bwd again with that cotangent (or adding the contribution of the second run, the
+    gradients being linear in it) completes the rank's gradients.  `d_final` is the cotangent
+    of the state after the last span (only the last rank's value is used; zero when None).
+    """
+    import torch.distributed as dist
+
+    world = dist.get_world_size(group)
+    rank = dist.get_rank(group)
+    trs = [torch.empty_like(transition) for _ in range(world)]
+    lgs = [torch.empty_like(local_grad) for _ in range(world)]
+    dist.all_gather(trs, transition.contiguous(), group=group)
+    dist.all_gather(lgs, local_grad.contiguous(), group=group)
+    dfin = d_final.contiguous().clone() if d_final is not None else torch.zeros_like(local_grad)
+    last = dist.get_global_rank(group, world - 1) if group is not None else world - 1
+    dist.broadcast(dfin, src=last, group=group)
+    return compose_grads(trs, lgs, dfin)[rank]
+
+
 def entering_state(transition: torch.Tensor, end_state: torch.Tensor,
                    initial_state: Optional[torch.Tensor] = None, group=None) -> torch.Tensor:
     """State entering this rank's span, given this rank's span summary.
@@ -55,8 +103,7 @@ def entering_state(transition: torch.Tensor, end_state: torch.Tensor,
     shs = [torch.empty_like(end_state) for _ in range(world)]
     dist.all_gather(trs, transition.contiguous(), group=group)
     dist.all_gather(shs, end_state.contiguous(), group=group)
-    s0 = initial_state
-    if s0 is not None:
-        s0 = s0.contiguous().clone()
-        dist.broadcast(s0, src=dist.get_global_rank(group, 0) if group is not None else 0, group=group)
+    # every rank takes part in the broadcast (a rank without a start state sends zeros)
+    s0 = initial_state.contiguous().clone() if initial_state is not None else torch.zeros_like(end_state)
+    dist.broadcast(s0, src=dist.get_global_rank(group, 0) if group is not None else 0, group=group)
     return compose(trs[:rank], shs[:rank], s0, like=end_state)[rank]

@@ -95,3 +95,59 @@ def test_compose_single_process():
     states = cp.compose(trs, shs, torch.from_numpy(s0[0]))
     full = oracle.gdn_fwd(q, k, v, g, beta, np.array([0, L]), initial_state=s0, nthreads=1)
     np.testing.assert_allclose(states[-1].numpy(), full["final_state"][0], rtol=1e-10, atol=1e-12)
+
+
+def _bwd_worker(rank, world, port, results):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        q, k, v, g, beta, s0 = _case()
+        L = q.shape[0]
+        do = np.random.default_rng(98).standard_normal(v.shape)
+        dfin = np.random.default_rng(97).standard_normal(s0.shape)
+        a, b = rank * L // world, (rank + 1) * L // world
+        sl = slice(a, b)
+        cu = np.array([0, b - a])
+        # forward composition (summaries + all-gather) gives the entering state
+        summ = oracle.gdn_summary(k[sl], v[sl], g[sl], beta[sl], cu, nthreads=1)
+        tr = torch.from_numpy(summ["transition"][0])
+        s_in = cp.entering_state(tr, torch.from_numpy(summ["end_state"][0]),
+                                 initial_state=torch.from_numpy(s0[0]) if rank == 0 else None)
+        # local backward (zero final cotangent), then the composed exit cotangent
+        loc = oracle.gdn_bwd(q[sl], k[sl], v[sl], g[sl], beta[sl], cu, do[sl], initial_state=s_in.numpy()[None],
+                             nthreads=1)
+        d_exit = cp.exit_state_grad(tr, torch.from_numpy(loc["d_initial_state"][0]),
+                                    d_final=torch.from_numpy(dfin[0]) if rank == world - 1 else None)
+        full = oracle.gdn_bwd(q[sl], k[sl], v[sl], g[sl], beta[sl], cu, do[sl], initial_state=s_in.numpy()[None],
+                              d_final_state=d_exit.numpy()[None], nthreads=1)
+        results[rank] = {k_: full[k_] for k_ in ("dq", "dk", "dv", "dg", "dbeta", "d_initial_state")}
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.timeout(300)
+def test_two_rank_backward_composition_matches_unsplit():
+    """Context-parallel backward on two gloo ranks: local backwards, one all-gather, the reverse
+    composition of the state gradient, and the span backwards from it reproduce the unsplit
+    backward of the whole sequence."""
+    world = 2
+    mgr = mp.Manager()
+    results = mgr.dict()
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    procs = [ctx.Process(target=_bwd_worker, args=(r, world, port, results)) for r in range(world)]
+    for p_ in procs:
+        p_.start()
+    for p_ in procs:
+        p_.join(240)
+        assert p_.exitcode == 0
+    q, k, v, g, beta, s0 = _case()
+    L = q.shape[0]
+    do = np.random.default_rng(98).standard_normal(v.shape)
+    dfin = np.random.default_rng(97).standard_normal(s0.shape)
+    ref = oracle.gdn_bwd(q, k, v, g, beta, np.array([0, L]), do, initial_state=s0, d_final_state=dfin, nthreads=1)
+    for name in ("dq", "dk", "dv", "dg", "dbeta"):
+        got = np.concatenate([results[r][name] for r in range(world)])
+        np.testing.assert_allclose(got, ref[name], rtol=1e-8, atol=1e-10)
+    np.testing.assert_allclose(results[0]["d_initial_state"], ref["d_initial_state"], rtol=1e-8, atol=1e-10)
