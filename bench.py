@@ -72,12 +72,15 @@ def load_peaks():
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
+# the sources that decide the forward chunk kernel's code and launch (its DRAM traffic)
+TRAFFIC_SOURCES = ("gdn_chunk.cu", "gdn_prologue.cu", "ptx.cuh", "la_api.cu")
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     d = os.path.join(ROOT, "gated_delta_rule_29_gb300", "csrc")
-    for name in sorted(os.listdir(d)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(d, name), "rb").read())
+    for name in TRAFFIC_SOURCES:
+        h.update(open(os.path.join(d, name), "rb").read())
     return h.hexdigest()[:16]
 
 
