@@ -38,9 +38,6 @@ constexpr int kBT = 256;   // threads
 constexpr int kC = 64;     // chunk
 constexpr int kVT = 16;    // value columns per tile
 
-__device__ __forceinline__ float bfv(const uint16_t* p, int64_t i) {
-    return __uint_as_float(static_cast<uint32_t>(p[i]) << 16);
-}
 __device__ __forceinline__ uint16_t f2b(float x) {
     __nv_bfloat16 h = __float2bfloat16_rn(x);
     return *reinterpret_cast<uint16_t*>(&h);
@@ -60,20 +57,31 @@ struct BwdSmem {
     float Qh[kC * PK];      // normalised queries
     float Tm[kC * PC];      // T = (I + A)^{-1}
     float Pm[kC * PC];      // P (lower incl.)
-    float Gk[kC * PC];      // (k_i . k_j) Gamma_ij, lower incl.
-    float dA[kC * PC];      // accumulated over tiles, then M
+    // strictly lower part: dA accumulated over the tiles, then M; strictly upper part: the
+    // transpose of Gk_ij = (k_i . k_j) Gamma_ij (j < i) stored at [j][i]; diagonal zero
+    float dA[kC * PC];
     float dP[kC * PC];      // accumulated over tiles, then H
-    // value tiles, stored transposed: row = value column cc, contiguous along the token / key index
-    float SJ[kVT * PK];     // S[:, tile]^T
-    float dSJ[kVT * PK];    // dS_next[:, tile]^T
+    // value tiles, stored transposed: row = value column cc, contiguous along the token / key index;
+    // S and dS are double buffered so that the next tile streams in while this one is computed
+    float SJ[2][kVT * PK];  // S[:, tile]^T
+    float dSJ[2][kVT * PK]; // dS_next[:, tile]^T
     float X[kVT * PC], Y[kVT * PC], D[kVT * PC], dD[kVT * PC], dY[kVT * PC];
     float VJ[kVT * PC], OJ[kVT * PC], QS[kVT * PC], KdS[kVT * PC];
+    uint16_t Vb[kC * kVT], Ob[kC * kVT];  // the next tile's raw V and dO rows (bf16, token-major)
     float beta[kC], b[kC], gam[kC], GC[kC], rk[kC], rq[kC];
     float dbeta[kC], db[kC], wv[kC];
     float red[kBT / 32];
 };
+static_assert(sizeof(BwdSmem<128>) <= 227 * 1024, "backward shared memory exceeds the per-CTA limit");
 
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
     return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, acc))));
 }
@@ -156,10 +164,47 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
     constexpr int KSL = KD / 4;
     const int own_r = tid >> 2, own_c0 = (tid & 3) * KSL;
 
+    // Asynchronous fetch of one value tile (chunk cc, columns j0..j0+15) into buffer pb: the
+    // S and dS columns (4-byte copies, transposed into the tile layout) and the raw V and dO
+    // rows (4-byte copies of bf16 pairs when the operands allow it, else plain loads).
+    auto fetch_tile = [&](int cc, int j0, int pb) {
+        const int64_t ft0 = ts + static_cast<int64_t>(cc) * kC;
+        const int fn = static_cast<int>(L - static_cast<int64_t>(cc) * kC < kC ? L - static_cast<int64_t>(cc) * kC : kC);
+        const float* Sf = a.ckpt + ((a.ckpt_off[seq] + cc) * HO + h) * KV;
+        for (int e = tid; e < KD * kVT; e += kBT) {
+            const int r = e / kVT, col = e % kVT;
+            cp_async4(&s.SJ[pb][col * PK + colp<KD>(r)], Sf + r * VD + j0 + col);
+            cp_async4(&s.dSJ[pb][col * PK + colp<KD>(r)], dSg + r * VD + j0 + col);
+        }
+        for (int e = tid; e < kC * kVT / 2; e += kBT) {
+            const int i = e / (kVT / 2), c2 = 2 * (e % (kVT / 2));
+            uint16_t* vd = &s.Vb[i * kVT + c2];
+            uint16_t* od = &s.Ob[i * kVT + c2];
+            if (i >= fn) {
+                *reinterpret_cast<uint32_t*>(vd) = 0u;
+                *reinterpret_cast<uint32_t*>(od) = 0u;
+            } else {
+                const uint16_t* vs = a.v + (ft0 + i) * a.v_st + h * a.v_sh + j0 + c2;
+                const uint16_t* os = a.dout + (ft0 + i) * a.do_st + h * a.do_sh + j0 + c2;
+                if (a.vo_async) {
+                    cp_async4(vd, vs);
+                    cp_async4(od, os);
+                } else {
+                    vd[0] = vs[0];
+                    vd[1] = vs[1];
+                    od[0] = os[0];
+                    od[1] = os[1];
+                }
+            }
+        }
+        cp_async_commit();
+    };
+    int pb = 0;  // buffer of the current tile
+    if (nch > 0) fetch_tile(nch - 1, 0, 0);
+
     for (int c = nch - 1; c >= 0; --c) {
         const int64_t t0 = ts + static_cast<int64_t>(c) * kC;
         const int n = static_cast<int>(L - static_cast<int64_t>(c) * kC < kC ? L - static_cast<int64_t>(c) * kC : kC);
-        const float* Sc = a.ckpt + ((a.ckpt_off[seq] + c) * HO + h) * KV;  // state entering this chunk
 
         // ---- chunk-level quantities: normalised rows, decays, A, T, P
         for (int e = tid; e < kC * KD / 8; e += kBT) {
@@ -271,9 +316,9 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
                 for (int y = 0; y < 4; ++y) {
                     const int i = i0 + x, j = bj + 16 * y;
                     const float G = j <= i ? expf(s.b[i] - s.b[j]) : 0.f;
-                    s.Gk[i * PC + j] = kk[x][y] * G;
+                    if (j <= i) s.dA[i * PC + j] = 0.f;              // dA accumulator, diagonal
+                    if (j < i) s.dA[j * PC + i] = kk[x][y] * G;      // Gk_ij, transposed
                     s.Pm[i * PC + j] = qk[x][y] * G;
-                    s.dA[i * PC + j] = 0.f;
                     s.dP[i * PC + j] = 0.f;
                 }
         }
@@ -295,7 +340,7 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
                     s.Tm[(o + j) * PC + o + cc] = tj;
 #pragma unroll
                     for (int i = j + 1; i < 16; ++i)
-                        acc[i] = fmaf(s.beta[o + i] * s.Gk[(o + i) * PC + o + j], tj, acc[i]);
+                        acc[i] = fmaf(s.beta[o + i] * s.dA[(o + j) * PC + o + i], tj, acc[i]);
                 }
             }
             // the blocks above the diagonal are zero
@@ -316,7 +361,7 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
 #pragma unroll
                     for (int x = 0; x < 8; ++x) y[x] = 0.f;
                     for (int m = 16 * bj; m < 16 * bi; ++m) {
-                        const float am = s.beta[16 * bi + r] * s.Gk[(16 * bi + r) * PC + m];
+                        const float am = s.beta[16 * bi + r] * s.dA[m * PC + 16 * bi + r];
 #pragma unroll
                         for (int x = 0; x < 8; ++x) y[x] = fmaf(am, s.Tm[m * PC + 16 * bj + c0 + x], y[x]);
                     }
@@ -345,32 +390,35 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
 
         // ---- the value tiles: independent columns of S and dS
         for (int j0 = 0; j0 < VD; j0 += kVT) {
-            for (int e = tid; e < KD * kVT; e += kBT) {
-                const int r = e / kVT, cc = e % kVT;
-                s.SJ[cc * PK + colp<KD>(r)] = Sc[r * VD + j0 + cc];
-                s.dSJ[cc * PK + colp<KD>(r)] = dSg[r * VD + j0 + cc];
-            }
-            for (int e = tid; e < kC * kVT; e += kBT) {
-                const int i = e / kVT, cc = e % kVT;
-                float vv = 0.f, ov = 0.f;
-                if (i < n) {
-                    vv = bfv(a.v, (t0 + i) * a.v_st + h * a.v_sh + j0 + cc);
-                    ov = bfv(a.dout, (t0 + i) * a.do_st + h * a.do_sh + j0 + cc);
+            cp_async_wait_all();
+            __syncthreads();  // this tile's S, dS, V, dO have landed
+            float* SJ = s.SJ[pb];
+            float* dSJ = s.dSJ[pb];
+            {
+                // V and dO of this tile into the fp32 tiles, each element by the thread that reads
+                // it first below (column tid / 16, rows tid % 16 + 16 e)
+                const int cc = tid >> 4, r = tid & 15;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int i = r + 16 * e;
+                    s.VJ[cc * PC + i] = __uint_as_float(static_cast<uint32_t>(s.Vb[i * kVT + cc]) << 16);
+                    s.OJ[cc * PC + i] = __uint_as_float(static_cast<uint32_t>(s.Ob[i * kVT + cc]) << 16);
                 }
-                s.VJ[cc * PC + i] = vv;
-                s.OJ[cc * PC + i] = ov;
             }
-            __syncthreads();
             // x = K S_J, Q S_J, K dS_J (transposed tiles)
             auto ck = [](int m) { return colp<KD>(m); };
             auto cc_id = [](int m) { return m; };
-            tile_nt<KD>(s.SJ, PK, s.Kh, PK, ck, [&](int cc, int r, float v) {
+            tile_nt<KD>(SJ, PK, s.Kh, PK, ck, [&](int cc, int r, float v) {
                 s.X[cc * PC + r] = v;
                 s.Y[cc * PC + r] = s.beta[r] * (s.VJ[cc * PC + r] - s.gam[r] * v);
             });
-            tile_nt<KD>(s.SJ, PK, s.Qh, PK, ck, [&](int cc, int r, float v) { s.QS[cc * PC + r] = v; });
-            tile_nt<KD>(s.dSJ, PK, s.Kh, PK, ck, [&](int cc, int r, float v) { s.KdS[cc * PC + r] = v; });
+            tile_nt<KD>(SJ, PK, s.Qh, PK, ck, [&](int cc, int r, float v) { s.QS[cc * PC + r] = v; });
+            tile_nt<KD>(dSJ, PK, s.Kh, PK, ck, [&](int cc, int r, float v) { s.KdS[cc * PC + r] = v; });
             __syncthreads();
+            // the next tile (this chunk's next columns, else the previous chunk's first) streams
+            // into the other buffer; the staged V / dO rows have been read above
+            if (j0 + kVT < VD) fetch_tile(c, j0 + kVT, pb ^ 1);
+            else if (c > 0) fetch_tile(c - 1, 0, pb ^ 1);
             // D = T Y;  dD = scale P^T dO + Gamma_C (K dS_J)
             tile_nt<kC>(s.Y, PC, s.Tm, PC, cc_id, [&](int cc, int r, float v) { s.D[cc * PC + r] = v; });
             tile_nn<kC>([&](int cc, int m) { return s.OJ[cc * PC + m]; }, s.Pm, PC,
@@ -411,7 +459,7 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
                 float p = 0.f;
                 for (int e = tid; e < KD * kVT; e += kBT) {
                     const int r = colp<KD>(e % KD), cc = e / KD;
-                    p = fmaf(s.dSJ[cc * PK + r], s.SJ[cc * PK + r], p);
+                    p = fmaf(dSJ[cc * PK + r], SJ[cc * PK + r], p);
                 }
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
@@ -460,8 +508,8 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
                     const float fy = bx * s.dY[cc * PC + i], fd = gc * s.D[cc * PC + i], fo = sg * s.OJ[cc * PC + i];
 #pragma unroll
                     for (int e = 0; e < KSL; e += 4) {
-                        const float4 sj = ld4(&s.SJ[cc * PK + colp<KD>(own_c0 + e)]);
-                        const float4 dsj = ld4(&s.dSJ[cc * PK + colp<KD>(own_c0 + e)]);
+                        const float4 sj = ld4(&SJ[cc * PK + colp<KD>(own_c0 + e)]);
+                        const float4 dsj = ld4(&dSJ[cc * PK + colp<KD>(own_c0 + e)]);
                         dKacc[e + 0] = fmaf(fy, sj.x, fmaf(fd, dsj.x, dKacc[e + 0]));
                         dKacc[e + 1] = fmaf(fy, sj.y, fmaf(fd, dsj.y, dKacc[e + 1]));
                         dKacc[e + 2] = fmaf(fy, sj.z, fmaf(fd, dsj.z, dKacc[e + 2]));
@@ -501,7 +549,7 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
                     }
                     const float gl = s.gam[n - 1];
                     float* dst = dSg + static_cast<int64_t>(d) * VD + j0 + cc;
-                    const float4 old = ld4(&s.dSJ[cc * PK + colp<KD>(d)]);
+                    const float4 old = ld4(&dSJ[cc * PK + colp<KD>(d)]);
                     dst[0] = fmaf(gl, old.x, acc.x);
                     dst[VD] = fmaf(gl, old.y, acc.y);
                     dst[2 * VD] = fmaf(gl, old.z, acc.z);
@@ -509,6 +557,7 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
                 }
             }
             __syncthreads();
+            pb ^= 1;
         }
 
         // ---- tile-independent terms: A and P backward, dbeta, db, dg, the norms
@@ -518,12 +567,12 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
             float sb = 0.f, rowsum = 0.f, colsum = 0.f;
             for (int j = q4 * 16; j < q4 * 16 + 16; ++j) {
                 if (j < i) {
-                    const float x = s.dA[i * PC + j] * s.Gk[i * PC + j];
+                    const float x = s.dA[i * PC + j] * s.dA[j * PC + i];  // dA_ij Gk_ij
                     sb += x;
                     rowsum = fmaf(x, s.beta[i], rowsum);
                 }
                 if (j <= i) rowsum = fmaf(s.dP[i * PC + j], s.Pm[i * PC + j], rowsum);
-                if (j > i) colsum = fmaf(s.dA[j * PC + i] * s.beta[j], s.Gk[j * PC + i], colsum);
+                if (j > i) colsum = fmaf(s.dA[j * PC + i] * s.beta[j], s.dA[i * PC + j], colsum);  // Gk_ji at [i][j]
                 if (j >= i) colsum = fmaf(s.dP[j * PC + i], s.Pm[j * PC + i], colsum);
             }
 #pragma unroll
@@ -538,11 +587,12 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
             }
         }
         __syncthreads();
-        // M = dA (.) beta_i Gamma (strict), H = dP (.) Gamma (incl.), in place
+        // M = dA (.) beta_i Gamma (strictly lower part; the upper part keeps Gk), H = dP (.) Gamma
+        // (incl.), in place
         for (int e = tid; e < kC * kC; e += kBT) {
             const int i = e / kC, j = e % kC;
             const float G = j <= i ? expf(s.b[i] - s.b[j]) : 0.f;
-            s.dA[i * PC + j] = j < i ? s.dA[i * PC + j] * s.beta[i] * G : 0.f;
+            if (j < i) s.dA[i * PC + j] *= s.beta[i] * G;
             s.dP[i * PC + j] = j <= i ? s.dP[i * PC + j] * G : 0.f;
         }
         __syncthreads();
@@ -551,7 +601,8 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
             const int i = own_r;
 #pragma unroll 2
             for (int j = 0; j < kC; ++j) {
-                const float mk = s.dA[i * PC + j] + s.dA[j * PC + i];
+                // M_ij + M_ji with M strictly lower (its diagonal is zero)
+                const float mk = j <= i ? s.dA[i * PC + j] : s.dA[j * PC + i];
                 const float hq = s.dP[j * PC + i], hk = s.dP[i * PC + j];
 #pragma unroll
                 for (int e = 0; e < KSL; e += 4) {
@@ -635,6 +686,7 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
         }
         __syncthreads();
     }
+    cp_async_wait_all();  // nothing is in flight here (the last tile fetches nothing)
     if (a.ds0) {
         for (int64_t e = tid; e < KV; e += kBT) a.ds0[unit * KV + e] = dSg[e];
     }

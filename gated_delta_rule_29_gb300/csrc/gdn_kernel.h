@@ -156,6 +156,7 @@ struct BwdArgs {
     float* dqh;                      // [T, HO, K] fp32 per value head (grouped heads)
     float* dkh;
     int32_t vec_out;                 // dq, dk rows 16-byte aligned: 16-byte stores
+    int32_t vo_async;                // v, dO pairs 4-byte aligned: asynchronous 4-byte copies
 };
 
 // Gated DeltaProduct: the update timeline for the chunk kernel, and the per-token outputs.

@@ -591,6 +591,8 @@ la_status gdn_bwd(const la_gdn_bwd_params* p, void* stream) {
     b.ds0 = p->d_initial_state;
     b.vec_out = aligned(p->dq, 16) && aligned(p->dk, 16) && p->dq_stride_t % 8 == 0 && p->dk_stride_t % 8 == 0 &&
                 (p->HK == 1 || (p->dq_stride_h % 8 == 0 && p->dk_stride_h % 8 == 0));
+    b.vo_async = aligned(p->v, 4) && aligned(p->d_o, 4) && p->v_stride_t % 2 == 0 && p->d_o_stride_t % 2 == 0 &&
+                 (p->HV == 1 || (p->v_stride_h % 2 == 0 && p->d_o_stride_h % 2 == 0));
     if (p->HV != p->HK) {
         b.dqh = reinterpret_cast<float*>(wb + BL.gh);
         b.dkh = b.dqh + static_cast<size_t>(p->T) * p->HV * p->K;
