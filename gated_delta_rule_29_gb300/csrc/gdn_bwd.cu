@@ -16,20 +16,28 @@
 //   dQ = scale diag(gamma) dO S^T + H K,  H = dP (.) Gamma,
 //   dbeta_i = sum_v dY (V - gamma x) + sum_j dA_ij (k_i . k_j) Gamma_ij,
 //   db collects every gamma / Gamma dependence and dg_j = sum_{i >= j} db_i,
-// then the L2-norm backward for q and k and the sum over grouped value heads.
+// then the L2-norm backward for q and k and the sum over grouped value heads.  K and Q above
+// are the normalised rows; the kernel keeps the raw rows (exact bf16 values) and applies the
+// inverse norms as row or column scales of the other operand.
 //
-// Mapping.  One CTA of 256 threads per (sequence, head) walks the chunks in reverse and
-// carries dS in a global per-unit buffer.  The value columns are independent chains (each
+// Mapping.  One CTA of 256 threads (8 warps) per (sequence, head) walks the chunks in reverse
+// and carries dS in a global per-unit buffer.  The value columns are independent chains (each
 // column of S evolves on its own), so a chunk is processed in 16-column tiles of S, dS, V and
-// dO; the tile-independent parts (normalised K and Q, A, T, P, the decays) are formed once
-// per chunk in shared memory and the cross-column sums (dA, dP, dK, dQ, dbeta, db) are
-// accumulated over the tiles in shared memory and registers.  The chunk entering states come
-// from the forward kernel run with fp32 checkpoints every 64 tokens.  All arithmetic is fp32
-// on the CUDA cores.
+// dO; the tile-independent parts (K, Q, A, T, P, the decays) are formed once per chunk in
+// shared memory and the cross-column sums (dA, dP, dK, dQ, dbeta, db) accumulate over the
+// tiles.  The next tile's S, dS, V and dO stream in with cp.async while a tile is computed.
+// Every product runs on warp-level tensor-core MMAs (m16n8k8, tf32 operands, fp32
+// accumulation) with each inexact fp32 operand split into a tf32 head and a tf32 remainder:
+// three products per MMA (head x head, head x rest, rest x head), two when one operand is an
+// exact bf16 input (k, q, dO), which keeps fp32-level accuracy.  The dK and dQ rows stay in
+// the warps' accumulator fragments for the whole chunk: warps 0-3 own dK rows 16 w .. 16 w +
+// 15, warps 4-7 the same dQ rows.  The chunk entering states come from the forward kernel run
+// with fp32 checkpoints every 64 tokens.
 #include <cuda_bf16.h>
 
 #include "../../include/liblinattn.h"
 #include "gdn_kernel.h"
+#include "ptx.cuh"
 
 namespace la {
 namespace {
@@ -42,23 +50,24 @@ __device__ __forceinline__ uint16_t f2b(float x) {
     __nv_bfloat16 h = __float2bfloat16_rn(x);
     return *reinterpret_cast<uint16_t*>(&h);
 }
+__device__ __forceinline__ float b2f(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
 
 // Shared-memory layout of the key-length rows (K, Q, S^T, dS^T): the four KD/4-column slices
-// that four neighbouring threads read are staggered by 4 words, and the row stride is 4 mod 8
-// words, so that 16-byte reads of neighbouring rows or of the four slices hit distinct banks.
+// are staggered by 4 words, and the row stride is 12 mod 32 words, so that the MMA operand
+// fragments of row-major reads (8 rows x 4 columns per warp) hit 32 distinct banks.
 template <int KD>
 __device__ __forceinline__ int colp(int d) { return d + (d / (KD / 4)) * 4; }
 
 template <int KD>
 struct BwdSmem {
-    static constexpr int PK = KD + 12;  // row stride of K / Q / S^T / dS^T (4 mod 8 words)
+    static constexpr int PK = KD + 12;  // row stride of K / Q / S^T / dS^T
     static constexpr int PC = kC + 4;   // row stride of the 64 x 64 matrices and of the tiles
-    float Kh[kC * PK];      // normalised keys (rows past the end are zero)
-    float Qh[kC * PK];      // normalised queries
+    float Kr[kC * PK];      // raw keys (rows past the end are zero); k_hat = rk k
+    float Qr[kC * PK];      // raw queries; q_hat = rq q
     float Tm[kC * PC];      // T = (I + A)^{-1}
     float Pm[kC * PC];      // P (lower incl.)
     // strictly lower part: dA accumulated over the tiles, then M; strictly upper part: the
-    // transpose of Gk_ij = (k_i . k_j) Gamma_ij (j < i) stored at [j][i]; diagonal zero
+    // transpose of Gk_ij = (k_hat_i . k_hat_j) Gamma_ij (j < i) stored at [j][i]; diagonal zero
     float dA[kC * PC];
     float dP[kC * PC];      // accumulated over tiles, then H
     // value tiles, stored transposed: row = value column cc, contiguous along the token / key index;
@@ -69,12 +78,16 @@ struct BwdSmem {
     float VJ[kVT * PC], OJ[kVT * PC], QS[kVT * PC], KdS[kVT * PC];
     uint16_t Vb[kC * kVT], Ob[kC * kVT];  // the next tile's raw V and dO rows (bf16, token-major)
     float beta[kC], b[kC], gam[kC], GC[kC], rk[kC], rq[kC];
+    float cx[kC], co[kC];   // -rk beta gamma (K^T dx) and scale rq gamma (Q^T dO) row factors
     float dbeta[kC], db[kC], wv[kC];
     float red[kBT / 32];
 };
 static_assert(sizeof(BwdSmem<128>) <= 227 * 1024, "backward shared memory exceeds the per-CTA limit");
 
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
+    return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, acc))));
+}
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
                  "l"(src)
@@ -82,56 +95,49 @@ __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ float dot4(float4 a, float4 b, float acc) {
-    return fmaf(a.x, b.x, fmaf(a.y, b.y, fmaf(a.z, b.z, fmaf(a.w, b.w, acc))));
-}
 
-// out[c][r] = sum_m Lt[c][m] * R[r][m] for a kVT x kC output (c = value column, r = token),
-// both operands contiguous along m in groups of 4 (column map CM); each thread computes
-// rows r, r + 16, r + 32, r + 48 of one column.
-template <int MM, class CM, class FO>
-__device__ __forceinline__ void tile_nt(const float* Lt, int ldl, const float* R, int ldr, CM cm, FO out) {
-    const int tid = threadIdx.x;
-    const int c = tid >> 4, r = tid & 15;
-    float4 acc[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc[e] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int m = 0; m < MM; m += 4) {
-        const int mp = cm(m);
-        const float4 l = ld4(Lt + c * ldl + mp);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float4 rv = ld4(R + (r + 16 * e) * ldr + mp);
-            acc[e].x = fmaf(l.x, rv.x, acc[e].x);
-            acc[e].y = fmaf(l.y, rv.y, acc[e].y);
-            acc[e].z = fmaf(l.z, rv.z, acc[e].z);
-            acc[e].w = fmaf(l.w, rv.w, acc[e].w);
-        }
-    }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) out(c, r + 16 * e, (acc[e].x + acc[e].y) + (acc[e].z + acc[e].w));
+// x = head + rest, both tf32 (the head rounded to nearest, the rest the rounded remainder).
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hd, uint32_t& rs) {
+    hd = to_tf32(x);
+    rs = to_tf32(x - __uint_as_float(hd));
 }
+// A fragment (16 x 8, rows m0.., columns k0..) of an element function, split in two.
+template <class F>
+__device__ __forceinline__ void frag_a_split(F f, int m0, int k0, int g, int t, uint32_t (&hd)[4], uint32_t (&rs)[4]) {
+    split_tf32(f(m0 + g, k0 + t), hd[0], rs[0]);
+    split_tf32(f(m0 + g + 8, k0 + t), hd[1], rs[1]);
+    split_tf32(f(m0 + g, k0 + t + 4), hd[2], rs[2]);
+    split_tf32(f(m0 + g + 8, k0 + t + 4), hd[3], rs[3]);
+}
+// B fragment (8 x 8, rows k0.., columns n0..) of an element function, split in two.
+template <class F>
+__device__ __forceinline__ void frag_b_split(F f, int k0, int n0, int g, int t, uint32_t (&hd)[2], uint32_t (&rs)[2]) {
+    split_tf32(f(k0 + t, n0 + g), hd[0], rs[0]);
+    split_tf32(f(k0 + t + 4, n0 + g), hd[1], rs[1]);
+}
+// c += A B with both operands split (three products), or with one exact operand (two).
+__device__ __forceinline__ void mma3(float (&c)[4], const uint32_t (&ah)[4], const uint32_t (&ar)[4],
+                                     const uint32_t (&bh)[2], const uint32_t (&br)[2]) {
+    mma_tf32_16x8x8(c, ar, bh);
+    mma_tf32_16x8x8(c, ah, br);
+    mma_tf32_16x8x8(c, ah, bh);
+}
+__device__ __forceinline__ void mma2a(float (&c)[4], const uint32_t (&a)[4], const uint32_t (&bh)[2],
+                                      const uint32_t (&br)[2]) {
+    mma_tf32_16x8x8(c, a, br);
+    mma_tf32_16x8x8(c, a, bh);
+}
+__device__ __forceinline__ void mma2b(float (&c)[4], const uint32_t (&ah)[4], const uint32_t (&ar)[4],
+                                      const uint32_t (&b)[2]) {
+    mma_tf32_16x8x8(c, ar, b);
+    mma_tf32_16x8x8(c, ah, b);
+}
+__device__ __forceinline__ uint32_t fbits(float x) { return __float_as_uint(x); }
 
-// out[c][r] = sum_m Lt[c][m] * R[m][r] for a kVT x kC output, R contiguous along r.
-template <int MM, class FL, class FO>
-__device__ __forceinline__ void tile_nn(FL Lt, const float* R, int ldr, FO out) {
-    const int tid = threadIdx.x;
-    const int c = tid >> 4, r0 = (tid & 15) * 4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-    for (int m = 0; m < MM; ++m) {
-        const float l = Lt(c, m);
-        const float4 rv = ld4(R + m * ldr + r0);
-        acc.x = fmaf(l, rv.x, acc.x);
-        acc.y = fmaf(l, rv.y, acc.y);
-        acc.z = fmaf(l, rv.z, acc.z);
-        acc.w = fmaf(l, rv.w, acc.w);
-    }
-    out(c, r0 + 0, acc.x);
-    out(c, r0 + 1, acc.y);
-    out(c, r0 + 2, acc.z);
-    out(c, r0 + 3, acc.w);
+// The 20 lower (16-row, 8-column) output tiles of a 64 x 64 lower-triangular product, in order.
+__device__ __forceinline__ void lower_tile(int p, int& mt, int& nt) {
+    mt = p < 2 ? 0 : (p < 6 ? 1 : (p < 12 ? 2 : 3));
+    nt = p - (mt == 0 ? 0 : (mt == 1 ? 2 : (mt == 2 ? 6 : 12)));
 }
 
 template <int KD, int VD>
@@ -140,7 +146,10 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
     BwdSmem<KD>& s = *reinterpret_cast<BwdSmem<KD>*>(smem_raw);
     constexpr int PK = BwdSmem<KD>::PK;
     constexpr int PC = BwdSmem<KD>::PC;
+    constexpr int NT = KD / 8;    // 8-column key tiles of the dK / dQ rows
+    constexpr int MTW = KD / 64;  // 16-row key tiles of dS per warp in the dS update
     const int tid = threadIdx.x;
+    const int w = tid >> 5, lane = tid & 31, g = lane >> 2, t = lane & 3;
     if (tid == 0) s.red[0] = __int_as_float(*reinterpret_cast<const volatile int32_t*>(&a.hdr->status));
     __syncthreads();
     if (__float_as_int(s.red[0]) != LA_OK) return;  // bad cu_seqlens: the forward ran nothing
@@ -160,9 +169,7 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
     for (int64_t e = tid; e < KV; e += kBT) dSg[e] = a.dfinal ? a.dfinal[unit * KV + e] : 0.f;
     __syncthreads();
 
-    // thread ownership for the per-row accumulators of dK and dQ: row i, KD/4-column slice
     constexpr int KSL = KD / 4;
-    const int own_r = tid >> 2, own_c0 = (tid & 3) * KSL;
 
     // Asynchronous fetch of one value tile (chunk cc, columns j0..j0+15) into buffer pb: the
     // S and dS columns (4-byte copies, transposed into the tile layout) and the raw V and dO
@@ -202,11 +209,14 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
     int pb = 0;  // buffer of the current tile
     if (nch > 0) fetch_tile(nch - 1, 0, 0);
 
+    const bool kwarp = w < 4;  // owns dK_hat rows (else dQ_hat rows) 16 (w % 4) .. + 15
+    const int om0 = 16 * (w & 3);
+
     for (int c = nch - 1; c >= 0; --c) {
         const int64_t t0 = ts + static_cast<int64_t>(c) * kC;
         const int n = static_cast<int>(L - static_cast<int64_t>(c) * kC < kC ? L - static_cast<int64_t>(c) * kC : kC);
 
-        // ---- chunk-level quantities: normalised rows, decays, A, T, P
+        // ---- chunk-level quantities: raw rows, norms, decays, Gk, P, T
         for (int e = tid; e < kC * KD / 8; e += kBT) {
             // 8 bf16 (16 bytes) per load: k and q rows are 16-byte aligned (TMA operand rules)
             const int i = e / (KD / 8), d = (e % (KD / 8)) * 8;
@@ -215,8 +225,8 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
                 kw = *reinterpret_cast<const uint4*>(a.k + (t0 + i) * a.k_st + hk * a.k_sh + d);
                 qw = *reinterpret_cast<const uint4*>(a.q + (t0 + i) * a.q_st + hk * a.q_sh + d);
             }
-            float* kd = &s.Kh[i * PK + colp<KD>(d)];
-            float* qd = &s.Qh[i * PK + colp<KD>(d)];
+            float* kd = &s.Kr[i * PK + colp<KD>(d)];
+            float* qd = &s.Qr[i * PK + colp<KD>(d)];
             const uint32_t kk[4] = {kw.x, kw.y, kw.z, kw.w}, qq[4] = {qw.x, qw.y, qw.z, qw.w};
 #pragma unroll
             for (int x = 0; x < 4; ++x) {
@@ -238,7 +248,7 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
             float sk = 0.f, sq = 0.f;
 #pragma unroll 4
             for (int d = q4 * KSL; d < (q4 + 1) * KSL; d += 4) {
-                const float4 kv = ld4(&s.Kh[i * PK + colp<KD>(d)]), qv = ld4(&s.Qh[i * PK + colp<KD>(d)]);
+                const float4 kv = ld4(&s.Kr[i * PK + colp<KD>(d)]), qv = ld4(&s.Qr[i * PK + colp<KD>(d)]);
                 sk = dot4(kv, kv, sk);
                 sq = dot4(qv, qv, sq);
             }
@@ -267,60 +277,46 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
             s.b[tid + 32] = x1;
         }
         __syncthreads();
-        for (int e = tid; e < kC * KD; e += kBT) {
-            const int i = e / KD, d = colp<KD>(e % KD);
-            s.Kh[i * PK + d] *= s.rk[i];
-            s.Qh[i * PK + d] *= s.rq[i];
-        }
         if (tid < kC) {
+            const int i = tid;
             const float bl = s.b[n - 1];
-            s.gam[tid] = expf(s.b[tid]);
-            s.GC[tid] = tid < n ? expf(bl - s.b[tid]) : 0.f;
-            s.dbeta[tid] = 0.f;
-            s.db[tid] = 0.f;
+            const float gm = expf(s.b[i]);
+            s.gam[i] = gm;
+            s.GC[i] = i < n ? expf(bl - s.b[i]) : 0.f;
+            s.cx[i] = -s.rk[i] * s.beta[i] * gm;
+            s.co[i] = a.scale * s.rq[i] * gm;
+            s.dbeta[i] = 0.f;
+            s.db[i] = 0.f;
         }
-        __syncthreads();
-        {
-            // Gk = (k_i . k_j) Gamma_ij and P = (q_i . k_j) Gamma_ij (lower incl.): 4 x 4 blocks
-            // rows i = 4 bi + x, columns j = bj + 16 y (neighbouring threads read neighbouring rows)
-            const int bi = tid >> 4, bj = tid & 15;
-            const int i0 = 4 * bi;
-            float kk[4][4], qk[4][4];
-#pragma unroll
-            for (int x = 0; x < 4; ++x)
-#pragma unroll
-                for (int y = 0; y < 4; ++y) kk[x][y] = qk[x][y] = 0.f;
-            if (bj <= i0 + 3) {
-#pragma unroll 2
-                for (int d = 0; d < KD; d += 4) {
-                    const int dp = colp<KD>(d);
-                    float4 ki[4], qi[4], kj[4];
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) {
-                        ki[x] = ld4(&s.Kh[(i0 + x) * PK + dp]);
-                        qi[x] = ld4(&s.Qh[(i0 + x) * PK + dp]);
-                        kj[x] = ld4(&s.Kh[(bj + 16 * x) * PK + dp]);
-                    }
-#pragma unroll
-                    for (int x = 0; x < 4; ++x)
-#pragma unroll
-                        for (int y = 0; y < 4; ++y) {
-                            kk[x][y] = dot4(ki[x], kj[y], kk[x][y]);
-                            qk[x][y] = dot4(qi[x], kj[y], qk[x][y]);
-                        }
-                }
+        // Gk = rk_i rk_j (k_i . k_j) Gamma_ij and P = rq_i rk_j (q_i . k_j) Gamma_ij on the
+        // lower 16 x 8 tiles (the raw rows are exact in tf32: one product per MMA)
+        for (int job = w; job < 40; job += 8) {
+            int mt, nt;
+            lower_tile(job >> 1, mt, nt);
+            const bool isP = job & 1;
+            const float* Ar = isP ? s.Qr : s.Kr;
+            const int m0 = 16 * mt, n0 = 8 * nt;
+            float cf[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+            for (int k0 = 0; k0 < KD; k0 += 8) {
+                const int kp = colp<KD>(k0) + t;
+                const uint32_t af[4] = {fbits(Ar[(m0 + g) * PK + kp]), fbits(Ar[(m0 + g + 8) * PK + kp]),
+                                        fbits(Ar[(m0 + g) * PK + kp + 4]), fbits(Ar[(m0 + g + 8) * PK + kp + 4])};
+                const uint32_t bf[2] = {fbits(s.Kr[(n0 + g) * PK + kp]), fbits(s.Kr[(n0 + g) * PK + kp + 4])};
+                mma_tf32_16x8x8(cf, af, bf);
             }
 #pragma unroll
-            for (int x = 0; x < 4; ++x)
-#pragma unroll
-                for (int y = 0; y < 4; ++y) {
-                    const int i = i0 + x, j = bj + 16 * y;
-                    const float G = j <= i ? expf(s.b[i] - s.b[j]) : 0.f;
-                    if (j <= i) s.dA[i * PC + j] = 0.f;              // dA accumulator, diagonal
-                    if (j < i) s.dA[j * PC + i] = kk[x][y] * G;      // Gk_ij, transposed
-                    s.Pm[i * PC + j] = qk[x][y] * G;
+            for (int e = 0; e < 4; ++e) {
+                const int i = m0 + g + 8 * (e >> 1), j = n0 + 2 * t + (e & 1);
+                const float G = j <= i ? expf(s.b[i] - s.b[j]) : 0.f;
+                if (isP) {
+                    s.Pm[i * PC + j] = s.rq[i] * s.rk[j] * cf[e] * G;
                     s.dP[i * PC + j] = 0.f;
+                } else {
+                    if (j <= i) s.dA[i * PC + j] = 0.f;                             // dA accumulator, diagonal
+                    if (j < i) s.dA[j * PC + i] = s.rk[i] * s.rk[j] * cf[e] * G;   // Gk_ij, transposed
                 }
+            }
         }
         __syncthreads();
         {
@@ -328,7 +324,6 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
             // blocks by substitution (warp w, lane = column), then the blocks below by
             // T[bi][bj] = -T[bi][bi] sum_{m = bj}^{bi - 1} A[bi][m] T[m][bj], one level of block
             // distance at a time (scratch: the dD tile, not yet in use)
-            const int w = tid >> 5, lane = tid & 31;
             if (w < 4 && lane < 16) {
                 const int o = 16 * w, cc = lane;
                 float acc[16];
@@ -368,92 +363,123 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
 #pragma unroll
                     for (int x = 0; x < 8; ++x) Ysc[r * 16 + c0 + x] = y[x];
                     __syncwarp();
-                    float t[8];
+                    float tt[8];
 #pragma unroll
-                    for (int x = 0; x < 8; ++x) t[x] = 0.f;
+                    for (int x = 0; x < 8; ++x) tt[x] = 0.f;
 #pragma unroll
                     for (int k = 0; k < 16; ++k) {
                         const float tk = s.Tm[(16 * bi + r) * PC + 16 * bi + k];
 #pragma unroll
-                        for (int x = 0; x < 8; ++x) t[x] = fmaf(tk, Ysc[k * 16 + c0 + x], t[x]);
+                        for (int x = 0; x < 8; ++x) tt[x] = fmaf(tk, Ysc[k * 16 + c0 + x], tt[x]);
                     }
 #pragma unroll
-                    for (int x = 0; x < 8; ++x) s.Tm[(16 * bi + r) * PC + 16 * bj + c0 + x] = -t[x];
+                    for (int x = 0; x < 8; ++x) s.Tm[(16 * bi + r) * PC + 16 * bj + c0 + x] = -tt[x];
                     __syncwarp();
                 }
                 __syncthreads();
             }
         }
-        float dKacc[KSL], dQacc[KSL];
+
+        // dK_hat (warps 0-3) or the unscaled dQ_hat sum (warps 4-7) of rows om0 .. om0 + 15:
+        // accumulator fragments, column tile nd holds key columns 8 nd + 2 t, + 1
+        float acc[NT][4];
 #pragma unroll
-        for (int e = 0; e < KSL; ++e) dKacc[e] = dQacc[e] = 0.f;
+        for (int nd = 0; nd < NT; ++nd) acc[nd][0] = acc[nd][1] = acc[nd][2] = acc[nd][3] = 0.f;
 
         // ---- the value tiles: independent columns of S and dS
         for (int j0 = 0; j0 < VD; j0 += kVT) {
             cp_async_wait_all();
-            __syncthreads();  // this tile's S, dS, V, dO have landed
-            float* SJ = s.SJ[pb];
-            float* dSJ = s.dSJ[pb];
+            __syncthreads();  // this tile's S, dS, V, dO have landed; the previous tile is done
+            if (tid == 0 && j0 > 0) {
+                // the previous tile's Gamma_C terms of S_next and the decay of S into S_next
+                float p = 0.f, wsum = 0.f;
+                for (int x = 0; x < kBT / 32; ++x) p += s.red[x];
+                for (int j = 0; j < kC; ++j) wsum += s.wv[j];
+                s.db[n - 1] += s.gam[n - 1] * p + wsum;
+            }
+            const float* SJ = s.SJ[pb];
+            const float* dSJ = s.dSJ[pb];
+            const int mt = w & 3, m0 = 16 * mt, n0 = 8 * (w >> 2);  // this warp's 16 x 8 tile
             {
-                // V and dO of this tile into the fp32 tiles, each element by the thread that reads
-                // it first below (column tid / 16, rows tid % 16 + 16 e)
-                const int cc = tid >> 4, r = tid & 15;
+                // x = K S_J, Q S_J, K dS_J (rows scaled by rk / rq afterwards); V, dO into the tiles
+                float cx4[4] = {0.f, 0.f, 0.f, 0.f}, cq4[4] = {0.f, 0.f, 0.f, 0.f}, cd4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+                for (int k0 = 0; k0 < KD; k0 += 8) {
+                    const int kp = colp<KD>(k0) + t;
+                    const uint32_t ak[4] = {fbits(s.Kr[(m0 + g) * PK + kp]), fbits(s.Kr[(m0 + g + 8) * PK + kp]),
+                                            fbits(s.Kr[(m0 + g) * PK + kp + 4]), fbits(s.Kr[(m0 + g + 8) * PK + kp + 4])};
+                    const uint32_t aq[4] = {fbits(s.Qr[(m0 + g) * PK + kp]), fbits(s.Qr[(m0 + g + 8) * PK + kp]),
+                                            fbits(s.Qr[(m0 + g) * PK + kp + 4]), fbits(s.Qr[(m0 + g + 8) * PK + kp + 4])};
+                    uint32_t sh[2], sr[2], dh[2], dr[2];
+                    split_tf32(SJ[(n0 + g) * PK + kp], sh[0], sr[0]);
+                    split_tf32(SJ[(n0 + g) * PK + kp + 4], sh[1], sr[1]);
+                    split_tf32(dSJ[(n0 + g) * PK + kp], dh[0], dr[0]);
+                    split_tf32(dSJ[(n0 + g) * PK + kp + 4], dh[1], dr[1]);
+                    mma2a(cx4, ak, sh, sr);
+                    mma2a(cq4, aq, sh, sr);
+                    mma2a(cd4, ak, dh, dr);
+                }
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int i = r + 16 * e;
-                    s.VJ[cc * PC + i] = __uint_as_float(static_cast<uint32_t>(s.Vb[i * kVT + cc]) << 16);
-                    s.OJ[cc * PC + i] = __uint_as_float(static_cast<uint32_t>(s.Ob[i * kVT + cc]) << 16);
+                    const int i = m0 + g + 8 * (e >> 1), cc = n0 + 2 * t + (e & 1);
+                    const float x = s.rk[i] * cx4[e];
+                    const float vv = b2f(s.Vb[i * kVT + cc]);
+                    s.X[cc * PC + i] = x;
+                    s.VJ[cc * PC + i] = vv;
+                    s.Y[cc * PC + i] = s.beta[i] * (vv - s.gam[i] * x);
+                    s.QS[cc * PC + i] = s.rq[i] * cq4[e];
+                    s.KdS[cc * PC + i] = s.rk[i] * cd4[e];
+                    s.OJ[cc * PC + i] = b2f(s.Ob[i * kVT + cc]);
                 }
             }
-            // x = K S_J, Q S_J, K dS_J (transposed tiles)
-            auto ck = [](int m) { return colp<KD>(m); };
-            auto cc_id = [](int m) { return m; };
-            tile_nt<KD>(SJ, PK, s.Kh, PK, ck, [&](int cc, int r, float v) {
-                s.X[cc * PC + r] = v;
-                s.Y[cc * PC + r] = s.beta[r] * (s.VJ[cc * PC + r] - s.gam[r] * v);
-            });
-            tile_nt<KD>(SJ, PK, s.Qh, PK, ck, [&](int cc, int r, float v) { s.QS[cc * PC + r] = v; });
-            tile_nt<KD>(dSJ, PK, s.Kh, PK, ck, [&](int cc, int r, float v) { s.KdS[cc * PC + r] = v; });
             __syncthreads();
             // the next tile (this chunk's next columns, else the previous chunk's first) streams
             // into the other buffer; the staged V / dO rows have been read above
             if (j0 + kVT < VD) fetch_tile(c, j0 + kVT, pb ^ 1);
             else if (c > 0) fetch_tile(c - 1, 0, pb ^ 1);
-            // D = T Y;  dD = scale P^T dO + Gamma_C (K dS_J)
-            tile_nt<kC>(s.Y, PC, s.Tm, PC, cc_id, [&](int cc, int r, float v) { s.D[cc * PC + r] = v; });
-            tile_nn<kC>([&](int cc, int m) { return s.OJ[cc * PC + m]; }, s.Pm, PC,
-                        [&](int cc, int r, float v) { s.dD[cc * PC + r] = a.scale * v + s.GC[r] * s.KdS[cc * PC + r]; });
-            __syncthreads();
-            // dY = T^T dD
-            tile_nn<kC>([&](int cc, int m) { return s.dD[cc * PC + m]; }, s.Tm, PC,
-                        [&](int cc, int r, float v) { s.dY[cc * PC + r] = v; });
-            __syncthreads();
-            // dV = beta dY (final): four consecutive columns of one row per thread
             {
-                const int r = tid >> 2, c4 = (tid & 3) * 4;
-                if (r < n) {
-                    uint16_t* dst = a.dv + (t0 + r) * a.dv_st + h * a.dv_sh + j0 + c4;
+                // D = T Y (T lower: column tiles up to the diagonal);  dD = scale P^T dO + Gamma_C (K dS_J)
+                float cD[4] = {0.f, 0.f, 0.f, 0.f}, cE[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int kt = 0; kt <= 2 * mt + 1; ++kt) {
+                    const int k0 = 8 * kt;
+                    uint32_t ah[4], ar[4], bh[2], br[2];
+                    frag_a_split([&](int i, int m) { return s.Tm[i * PC + m]; }, m0, k0, g, t, ah, ar);
+                    frag_b_split([&](int m, int cc) { return s.Y[cc * PC + m]; }, k0, n0, g, t, bh, br);
+                    mma3(cD, ah, ar, bh, br);
+                }
+                for (int kt = 2 * mt; kt < 8; ++kt) {
+                    const int k0 = 8 * kt;
+                    uint32_t ah[4], ar[4];
+                    frag_a_split([&](int i, int m) { return s.Pm[m * PC + i]; }, m0, k0, g, t, ah, ar);
+                    const uint32_t b[2] = {fbits(s.OJ[(n0 + g) * PC + k0 + t]), fbits(s.OJ[(n0 + g) * PC + k0 + t + 4])};
+                    mma2b(cE, ah, ar, b);
+                }
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) dst[e] = f2b(s.beta[r] * s.dY[(c4 + e) * PC + r]);
+                for (int e = 0; e < 4; ++e) {
+                    const int i = m0 + g + 8 * (e >> 1), cc = n0 + 2 * t + (e & 1);
+                    s.D[cc * PC + i] = cD[e];
+                    s.dD[cc * PC + i] = a.scale * cE[e] + s.GC[i] * s.KdS[cc * PC + i];
                 }
             }
-            // per-row sums: dbeta (Y's beta), db (Y's gamma, O's gamma); the Gamma_Cj terms of
-            // S_next, w_j = Gamma_Cj sum_v (K dS_J)_jv D_jv, move from b_j to b_last
-            if (tid < kC) {
-                const int i = tid;
-                float sb = 0.f, sg = 0.f, so = 0.f, w = 0.f;
-#pragma unroll
-                for (int cc = 0; cc < kVT; ++cc) {
-                    const float dy = s.dY[cc * PC + i], xv = s.X[cc * PC + i];
-                    sb = fmaf(dy, s.VJ[cc * PC + i] - s.gam[i] * xv, sb);
-                    sg = fmaf(dy, xv, sg);
-                    so = fmaf(s.OJ[cc * PC + i], s.QS[cc * PC + i], so);
-                    w = fmaf(s.KdS[cc * PC + i], s.D[cc * PC + i], w);
+            __syncthreads();
+            {
+                // dY = T^T dD (T^T upper: column tiles from the diagonal); dV = beta dY (final)
+                float cY[4] = {0.f, 0.f, 0.f, 0.f};
+                for (int kt = 2 * mt; kt < 8; ++kt) {
+                    const int k0 = 8 * kt;
+                    uint32_t ah[4], ar[4], bh[2], br[2];
+                    frag_a_split([&](int i, int m) { return s.Tm[m * PC + i]; }, m0, k0, g, t, ah, ar);
+                    frag_b_split([&](int m, int cc) { return s.dD[cc * PC + m]; }, k0, n0, g, t, bh, br);
+                    mma3(cY, ah, ar, bh, br);
                 }
-                s.dbeta[i] += sb;
-                s.db[i] += s.gam[i] * (a.scale * so - s.beta[i] * sg) - w * s.GC[i];
-                s.wv[i] = w * s.GC[i];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int i = m0 + g + 8 * (e >> 1), cc = n0 + 2 * t + (e & 1);
+                    s.dY[cc * PC + i] = cY[e];
+                    if (i < n) a.dv[(t0 + i) * a.dv_st + h * a.dv_sh + j0 + cc] = f2b(s.beta[i] * cY[e]);
+                }
             }
+            __syncthreads();
             {
                 // gamma_last <dS_J, S_J>: the decay of the entering state into S_next
                 float p = 0.f;
@@ -463,102 +489,155 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
                 }
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
-                if ((tid & 31) == 0) s.red[tid >> 5] = p;
+                if (lane == 0) s.red[w] = p;
             }
-            // dA += -dY D^T, dP += scale dO D^T (lower parts), 4 x 4 blocks
-            {
-                const int bi = tid >> 4, bj = tid & 15;
-                const int i0 = 4 * bi, jj0 = 4 * bj;
-                if (bj <= bi) {
-                    float ad[4][4], pd[4][4];
+            if (kwarp) {
+                // dK_hat += dx S_J^T + Gamma_C D dS_J^T,  dx = -beta gamma dY
 #pragma unroll
-                    for (int x = 0; x < 4; ++x)
+                for (int kt = 0; kt < 2; ++kt) {
+                    const int k0 = 8 * kt;
+                    uint32_t xh[4], xr[4], dh[4], dr[4];
+                    frag_a_split([&](int i, int cc) { return -s.beta[i] * s.gam[i] * s.dY[cc * PC + i]; }, om0, k0, g, t,
+                                 xh, xr);
+                    frag_a_split([&](int i, int cc) { return s.GC[i] * s.D[cc * PC + i]; }, om0, k0, g, t, dh, dr);
 #pragma unroll
-                        for (int y = 0; y < 4; ++y) ad[x][y] = pd[x][y] = 0.f;
-#pragma unroll 4
+                    for (int nd = 0; nd < NT; ++nd) {
+                        const int dp = colp<KD>(8 * nd) + g;
+                        uint32_t sh[2], sr[2], th[2], tr[2];
+                        split_tf32(SJ[(k0 + t) * PK + dp], sh[0], sr[0]);
+                        split_tf32(SJ[(k0 + t + 4) * PK + dp], sh[1], sr[1]);
+                        split_tf32(dSJ[(k0 + t) * PK + dp], th[0], tr[0]);
+                        split_tf32(dSJ[(k0 + t + 4) * PK + dp], th[1], tr[1]);
+                        mma3(acc[nd], xh, xr, sh, sr);
+                        mma3(acc[nd], dh, dr, th, tr);
+                    }
+                }
+                // dA -= dY D^T (strict), dP += scale dO D^T (incl.) on the lower 16 x 8 tiles
+                for (int pr = w; pr < 20; pr += 4) {
+                    int pmt, pnt;
+                    lower_tile(pr, pmt, pnt);
+                    const int p0 = 16 * pmt, q0 = 8 * pnt;
+                    float ca[4] = {0.f, 0.f, 0.f, 0.f}, cp[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int kt = 0; kt < 2; ++kt) {
+                        const int k0 = 8 * kt;
+                        uint32_t yh[4], yr[4], bh[2], br[2];
+                        frag_a_split([&](int i, int cc) { return s.dY[cc * PC + i]; }, p0, k0, g, t, yh, yr);
+                        frag_b_split([&](int cc, int j) { return s.D[cc * PC + j]; }, k0, q0, g, t, bh, br);
+                        const uint32_t ao[4] = {fbits(s.OJ[(k0 + t) * PC + p0 + g]), fbits(s.OJ[(k0 + t) * PC + p0 + g + 8]),
+                                                fbits(s.OJ[(k0 + t + 4) * PC + p0 + g]),
+                                                fbits(s.OJ[(k0 + t + 4) * PC + p0 + g + 8])};
+                        mma3(ca, yh, yr, bh, br);
+                        mma2a(cp, ao, bh, br);
+                    }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i = p0 + g + 8 * (e >> 1), j = q0 + 2 * t + (e & 1);
+                        if (j < i) s.dA[i * PC + j] -= ca[e];
+                        if (j <= i) s.dP[i * PC + j] += a.scale * cp[e];
+                    }
+                }
+            } else {
+                if (tid < 128 + kC) {
+                    // per-row sums: dbeta (Y's beta), db (Y's gamma, O's gamma); the Gamma_Cj terms
+                    // of S_next, w_j = Gamma_Cj sum_v (K dS_J)_jv D_jv, move from b_j to b_last
+                    const int i = tid - 128;
+                    float sb = 0.f, sg = 0.f, so = 0.f, wj = 0.f;
+#pragma unroll
                     for (int cc = 0; cc < kVT; ++cc) {
-                        const float4 yv = ld4(&s.dY[cc * PC + i0]), ov = ld4(&s.OJ[cc * PC + i0]);
-                        const float4 dv = ld4(&s.D[cc * PC + jj0]);
-                        const float yy[4] = {yv.x, yv.y, yv.z, yv.w}, oo[4] = {ov.x, ov.y, ov.z, ov.w};
-                        const float dd[4] = {dv.x, dv.y, dv.z, dv.w};
-#pragma unroll
-                        for (int x = 0; x < 4; ++x)
-#pragma unroll
-                            for (int y = 0; y < 4; ++y) {
-                                ad[x][y] = fmaf(yy[x], dd[y], ad[x][y]);
-                                pd[x][y] = fmaf(oo[x], dd[y], pd[x][y]);
-                            }
+                        const float dy = s.dY[cc * PC + i], xv = s.X[cc * PC + i];
+                        sb = fmaf(dy, s.VJ[cc * PC + i] - s.gam[i] * xv, sb);
+                        sg = fmaf(dy, xv, sg);
+                        so = fmaf(s.OJ[cc * PC + i], s.QS[cc * PC + i], so);
+                        wj = fmaf(s.KdS[cc * PC + i], s.D[cc * PC + i], wj);
                     }
+                    s.dbeta[i] += sb;
+                    s.db[i] += s.gam[i] * (a.scale * so - s.beta[i] * sg) - wj * s.GC[i];
+                    s.wv[i] = wj * s.GC[i];
+                }
+                // dQ_hat sum += dO S_J^T (the row factor scale gamma_i is applied after the tiles)
 #pragma unroll
-                    for (int x = 0; x < 4; ++x)
+                for (int kt = 0; kt < 2; ++kt) {
+                    const int k0 = 8 * kt;
+                    const uint32_t ao[4] = {fbits(s.OJ[(k0 + t) * PC + om0 + g]), fbits(s.OJ[(k0 + t) * PC + om0 + g + 8]),
+                                            fbits(s.OJ[(k0 + t + 4) * PC + om0 + g]),
+                                            fbits(s.OJ[(k0 + t + 4) * PC + om0 + g + 8])};
 #pragma unroll
-                        for (int y = 0; y < 4; ++y) {
-                            const int i = i0 + x, j = jj0 + y;
-                            if (j < i) s.dA[i * PC + j] -= ad[x][y];
-                            if (j <= i) s.dP[i * PC + j] += a.scale * pd[x][y];
+                    for (int nd = 0; nd < NT; ++nd) {
+                        const int dp = colp<KD>(8 * nd) + g;
+                        uint32_t sh[2], sr[2];
+                        split_tf32(SJ[(k0 + t) * PK + dp], sh[0], sr[0]);
+                        split_tf32(SJ[(k0 + t + 4) * PK + dp], sh[1], sr[1]);
+                        mma2a(acc[nd], ao, sh, sr);
+                    }
+                }
+                // dS_J <- gamma_last dS_J + K^T (cx (.) dY) + Q^T (co (.) dO): key rows
+                // kb .. kb + 16 MTW - 1 of this warp, both 8-column halves of the tile
+                const int kb = 16 * MTW * (w - 4);
+                const float gl = s.gam[n - 1];
+                float cs[MTW][2][4];
+#pragma unroll
+                for (int mi = 0; mi < MTW; ++mi)
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int d = kb + 16 * mi + g + 8 * (e >> 1), cc = 8 * h2 + 2 * t + (e & 1);
+                            cs[mi][h2][e] = gl * dSJ[cc * PK + colp<KD>(d)];
                         }
-                }
-            }
-            {
-                // dK += dx S_J^T + Gamma_C D dS_J^T (dx = -beta gamma dY); dQ += scale gamma dO S_J^T
-                const int i = own_r;
-                const float bx = -s.beta[i] * s.gam[i], gc = s.GC[i], sg = a.scale * s.gam[i];
 #pragma unroll 2
-                for (int cc = 0; cc < kVT; ++cc) {
-                    const float fy = bx * s.dY[cc * PC + i], fd = gc * s.D[cc * PC + i], fo = sg * s.OJ[cc * PC + i];
+                for (int kt = 0; kt < 8; ++kt) {
+                    const int k0 = 8 * kt;
+                    uint32_t xh[2][2], xr[2][2], oh[2][2], orr[2][2];
 #pragma unroll
-                    for (int e = 0; e < KSL; e += 4) {
-                        const float4 sj = ld4(&SJ[cc * PK + colp<KD>(own_c0 + e)]);
-                        const float4 dsj = ld4(&dSJ[cc * PK + colp<KD>(own_c0 + e)]);
-                        dKacc[e + 0] = fmaf(fy, sj.x, fmaf(fd, dsj.x, dKacc[e + 0]));
-                        dKacc[e + 1] = fmaf(fy, sj.y, fmaf(fd, dsj.y, dKacc[e + 1]));
-                        dKacc[e + 2] = fmaf(fy, sj.z, fmaf(fd, dsj.z, dKacc[e + 2]));
-                        dKacc[e + 3] = fmaf(fy, sj.w, fmaf(fd, dsj.w, dKacc[e + 3]));
-                        dQacc[e + 0] = fmaf(fo, sj.x, dQacc[e + 0]);
-                        dQacc[e + 1] = fmaf(fo, sj.y, dQacc[e + 1]);
-                        dQacc[e + 2] = fmaf(fo, sj.z, dQacc[e + 2]);
-                        dQacc[e + 3] = fmaf(fo, sj.w, dQacc[e + 3]);
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        frag_b_split([&](int m, int cc) { return s.cx[m] * s.dY[cc * PC + m]; }, k0, 8 * h2, g, t, xh[h2],
+                                     xr[h2]);
+                        frag_b_split([&](int m, int cc) { return s.co[m] * s.OJ[cc * PC + m]; }, k0, 8 * h2, g, t, oh[h2],
+                                     orr[h2]);
+                    }
+#pragma unroll
+                    for (int mi = 0; mi < MTW; ++mi) {
+                        const int dp = colp<KD>(kb + 16 * mi) + g;
+                        const uint32_t ak[4] = {fbits(s.Kr[(k0 + t) * PK + dp]), fbits(s.Kr[(k0 + t) * PK + dp + 8]),
+                                                fbits(s.Kr[(k0 + t + 4) * PK + dp]), fbits(s.Kr[(k0 + t + 4) * PK + dp + 8])};
+                        const uint32_t aq[4] = {fbits(s.Qr[(k0 + t) * PK + dp]), fbits(s.Qr[(k0 + t) * PK + dp + 8]),
+                                                fbits(s.Qr[(k0 + t + 4) * PK + dp]), fbits(s.Qr[(k0 + t + 4) * PK + dp + 8])};
+#pragma unroll
+                        for (int h2 = 0; h2 < 2; ++h2) {
+                            mma2a(cs[mi][h2], ak, xh[h2], xr[h2]);
+                            mma2a(cs[mi][h2], aq, oh[h2], orr[h2]);
+                        }
                     }
                 }
-            }
-            __syncthreads();
-            if (tid == 0) {
-                float p = 0.f, w = 0.f;
-                for (int x = 0; x < kBT / 32; ++x) p += s.red[x];
-                for (int j = 0; j < kC; ++j) w += s.wv[j];
-                s.db[n - 1] += s.gam[n - 1] * p + w;
-            }
-            {
-                // dS_J <- gamma_last dS_J + K^T dx + scale Q^T (gamma dO): column cc of dS, keys
-                // d .. d+3 per thread (KD x kVT outputs over 256 threads)
-                constexpr int PER = KD * kVT / (4 * kBT);  // float4 groups per thread
 #pragma unroll
-                for (int e = 0; e < PER; ++e) {
-                    const int idx = tid + e * kBT;
-                    const int cc = idx % kVT, d = (idx / kVT) * 4;  // 16 threads: one row segment
-                    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-                    for (int m = 0; m < kC; ++m) {
-                        const float fx = -s.beta[m] * s.gam[m] * s.dY[cc * PC + m];
-                        const float fo = a.scale * s.gam[m] * s.OJ[cc * PC + m];
-                        const float4 kv = ld4(&s.Kh[m * PK + colp<KD>(d)]), qv = ld4(&s.Qh[m * PK + colp<KD>(d)]);
-                        acc.x = fmaf(fx, kv.x, fmaf(fo, qv.x, acc.x));
-                        acc.y = fmaf(fx, kv.y, fmaf(fo, qv.y, acc.y));
-                        acc.z = fmaf(fx, kv.z, fmaf(fo, qv.z, acc.z));
-                        acc.w = fmaf(fx, kv.w, fmaf(fo, qv.w, acc.w));
-                    }
-                    const float gl = s.gam[n - 1];
-                    float* dst = dSg + static_cast<int64_t>(d) * VD + j0 + cc;
-                    const float4 old = ld4(&dSJ[cc * PK + colp<KD>(d)]);
-                    dst[0] = fmaf(gl, old.x, acc.x);
-                    dst[VD] = fmaf(gl, old.y, acc.y);
-                    dst[2 * VD] = fmaf(gl, old.z, acc.z);
-                    dst[3 * VD] = fmaf(gl, old.w, acc.w);
-                }
+                for (int mi = 0; mi < MTW; ++mi)
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2)
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int d = kb + 16 * mi + g + 8 * hh;
+                            *reinterpret_cast<float2*>(dSg + static_cast<int64_t>(d) * VD + j0 + 8 * h2 + 2 * t) =
+                                make_float2(cs[mi][h2][2 * hh], cs[mi][h2][2 * hh + 1]);
+                        }
             }
-            __syncthreads();
             pb ^= 1;
         }
+        __syncthreads();
+        if (tid == 0) {
+            float p = 0.f, wsum = 0.f;
+            for (int x = 0; x < kBT / 32; ++x) p += s.red[x];
+            for (int j = 0; j < kC; ++j) wsum += s.wv[j];
+            s.db[n - 1] += s.gam[n - 1] * p + wsum;
+        }
+        if (!kwarp) {
+            // the dQ_hat row factor scale gamma_i
+#pragma unroll
+            for (int nd = 0; nd < NT; ++nd)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[nd][e] *= a.scale * s.gam[om0 + g + 8 * (e >> 1)];
+        }
+        __syncthreads();
 
         // ---- tile-independent terms: A and P backward, dbeta, db, dg, the norms
         {
@@ -587,6 +666,16 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
             }
         }
         __syncthreads();
+        if (tid < kC) {
+            // dg_j = sum_{i >= j} db_i within the chunk
+            const int j = tid;
+            float sacc = 0.f;
+            for (int i = j; i < n; ++i) sacc += s.db[i];
+            if (j < n) {
+                a.dg[(t0 + j) * a.dg_st + h * a.dg_sh] = sacc;
+                a.dbeta[(t0 + j) * a.db_st + h * a.db_sh] = s.dbeta[j];
+            }
+        }
         // M = dA (.) beta_i Gamma (strictly lower part; the upper part keeps Gk), H = dP (.) Gamma
         // (incl.), in place
         for (int e = tid; e < kC * kC; e += kBT) {
@@ -596,90 +685,100 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
             s.dP[i * PC + j] = j <= i ? s.dP[i * PC + j] * G : 0.f;
         }
         __syncthreads();
-        {
-            // dK += (M + M^T) K + H^T Q, dQ += H K
-            const int i = own_r;
-#pragma unroll 2
-            for (int j = 0; j < kC; ++j) {
-                // M_ij + M_ji with M strictly lower (its diagonal is zero)
-                const float mk = j <= i ? s.dA[i * PC + j] : s.dA[j * PC + i];
-                const float hq = s.dP[j * PC + i], hk = s.dP[i * PC + j];
+        if (kwarp) {
+            // dK_hat += (M + M^T) K_hat + H^T Q_hat: the column scales rk_j, rq_j go into the
+            // left operand so that the raw rows (exact) are the right one
+            const int mt = w & 3;
+#pragma unroll 1
+            for (int kt = 0; kt < 8; ++kt) {
+                const int k0 = 8 * kt;
+                uint32_t mh[4], mr[4];
+                frag_a_split([&](int i, int j) { return (j <= i ? s.dA[i * PC + j] : s.dA[j * PC + i]) * s.rk[j]; }, om0, k0,
+                             g, t, mh, mr);
 #pragma unroll
-                for (int e = 0; e < KSL; e += 4) {
-                    const float4 kj = ld4(&s.Kh[j * PK + colp<KD>(own_c0 + e)]);
-                    const float4 qj = ld4(&s.Qh[j * PK + colp<KD>(own_c0 + e)]);
-                    dKacc[e + 0] = fmaf(mk, kj.x, fmaf(hq, qj.x, dKacc[e + 0]));
-                    dKacc[e + 1] = fmaf(mk, kj.y, fmaf(hq, qj.y, dKacc[e + 1]));
-                    dKacc[e + 2] = fmaf(mk, kj.z, fmaf(hq, qj.z, dKacc[e + 2]));
-                    dKacc[e + 3] = fmaf(mk, kj.w, fmaf(hq, qj.w, dKacc[e + 3]));
-                    dQacc[e + 0] = fmaf(hk, kj.x, dQacc[e + 0]);
-                    dQacc[e + 1] = fmaf(hk, kj.y, dQacc[e + 1]);
-                    dQacc[e + 2] = fmaf(hk, kj.z, dQacc[e + 2]);
-                    dQacc[e + 3] = fmaf(hk, kj.w, dQacc[e + 3]);
+                for (int nd = 0; nd < NT; ++nd) {
+                    const int dp = colp<KD>(8 * nd) + g;
+                    const uint32_t b[2] = {fbits(s.Kr[(k0 + t) * PK + dp]), fbits(s.Kr[(k0 + t + 4) * PK + dp])};
+                    mma2b(acc[nd], mh, mr, b);
+                }
+            }
+#pragma unroll 1
+            for (int kt = 2 * mt; kt < 8; ++kt) {
+                const int k0 = 8 * kt;
+                uint32_t hh[4], hr[4];
+                frag_a_split([&](int i, int j) { return s.dP[j * PC + i] * s.rq[j]; }, om0, k0, g, t, hh, hr);
+#pragma unroll
+                for (int nd = 0; nd < NT; ++nd) {
+                    const int dp = colp<KD>(8 * nd) + g;
+                    const uint32_t b[2] = {fbits(s.Qr[(k0 + t) * PK + dp]), fbits(s.Qr[(k0 + t + 4) * PK + dp])};
+                    mma2b(acc[nd], hh, hr, b);
+                }
+            }
+        } else {
+            // dQ_hat += H K_hat
+            const int mt = w & 3;
+#pragma unroll 1
+            for (int kt = 0; kt <= 2 * mt + 1; ++kt) {
+                const int k0 = 8 * kt;
+                uint32_t hh[4], hr[4];
+                frag_a_split([&](int i, int j) { return s.dP[i * PC + j] * s.rk[j]; }, om0, k0, g, t, hh, hr);
+#pragma unroll
+                for (int nd = 0; nd < NT; ++nd) {
+                    const int dp = colp<KD>(8 * nd) + g;
+                    const uint32_t b[2] = {fbits(s.Kr[(k0 + t) * PK + dp]), fbits(s.Kr[(k0 + t + 4) * PK + dp])};
+                    mma2b(acc[nd], hh, hr, b);
                 }
             }
         }
-        __syncthreads();
-        if (tid < kC) {
-            // dg_j = sum_{i >= j} db_i within the chunk
-            const int j = tid;
-            float acc = 0.f;
-            for (int i = j; i < n; ++i) acc += s.db[i];
-            if (j < n) {
-                a.dg[(t0 + j) * a.dg_st + h * a.dg_sh] = acc;
-                a.dbeta[(t0 + j) * a.db_st + h * a.db_sh] = s.dbeta[j];
-            }
-        }
         {
-            // L2-norm backward of row own_r: dx = r dy - r^3 (x . dy) x on the raw row
-            const int i = own_r;
-            float pk = 0.f, pq = 0.f;
+            // L2-norm backward of rows om0 + g and om0 + g + 8: with the raw row x and r = 1 / |x|,
+            // dx = r (dy - r^2 (x . dy) x)
+            const float* Xr = kwarp ? s.Kr : s.Qr;
+            const float* rr = kwarp ? s.rk : s.rq;
+            float pr[2] = {0.f, 0.f};
 #pragma unroll
-            for (int e = 0; e < KSL; ++e) {
-                pk = fmaf(s.Kh[i * PK + colp<KD>(own_c0 + e)], dKacc[e], pk);
-                pq = fmaf(s.Qh[i * PK + colp<KD>(own_c0 + e)], dQacc[e], pq);
+            for (int nd = 0; nd < NT; ++nd) {
+                const int dp = colp<KD>(8 * nd) + 2 * t;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const float* xr = Xr + (om0 + g + 8 * hh) * PK + dp;
+                    pr[hh] = fmaf(xr[0], acc[nd][2 * hh], fmaf(xr[1], acc[nd][2 * hh + 1], pr[hh]));
+                }
             }
-            pk += __shfl_xor_sync(0xffffffffu, pk, 1);
-            pk += __shfl_xor_sync(0xffffffffu, pk, 2);
-            pq += __shfl_xor_sync(0xffffffffu, pq, 1);
-            pq += __shfl_xor_sync(0xffffffffu, pq, 2);
-            if (i < n) {
-                // with the normalised row x_hat = r x: r^3 (x . dy) x = r (x_hat . dy) x_hat
-                const float rkk = s.rk[i], rqq = s.rq[i];
 #pragma unroll
-                for (int e = 0; e < KSL; ++e) {
+            for (int hh = 0; hh < 2; ++hh) {
+                pr[hh] += __shfl_xor_sync(0xffffffffu, pr[hh], 1);
+                pr[hh] += __shfl_xor_sync(0xffffffffu, pr[hh], 2);
+            }
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int i = om0 + g + 8 * hh;
+                if (i >= n) continue;
+                const float r = rr[i], f = r * r * pr[hh];
+                const int64_t tok = t0 + i;
+                uint16_t* orow = nullptr;
+                float* hrow = nullptr;
+                if (a.group == 1) orow = kwarp ? a.dk + tok * a.dk_st + hk * a.dk_sh : a.dq + tok * a.dq_st + hk * a.dq_sh;
+                else hrow = (kwarp ? a.dkh : a.dqh) + (tok * HO + h) * KD;
+#pragma unroll
+                for (int nd = 0; nd < NT; ++nd) {
+                    const int d = 8 * nd + 2 * t;
+                    float v0 = acc[nd][2 * hh], v1 = acc[nd][2 * hh + 1];
                     if (a.l2norm) {
-                        dKacc[e] = rkk * (dKacc[e] - pk * s.Kh[i * PK + colp<KD>(own_c0 + e)]);
-                        dQacc[e] = rqq * (dQacc[e] - pq * s.Qh[i * PK + colp<KD>(own_c0 + e)]);
+                        const float* xr = Xr + i * PK + colp<KD>(8 * nd) + 2 * t;
+                        v0 = r * (v0 - f * xr[0]);
+                        v1 = r * (v1 - f * xr[1]);
                     }
-                }
-                const int64_t t = t0 + i;
-                if (a.group == 1 && a.vec_out) {
-                    // 8 bf16 per 16-byte store (dq, dk rows 16-byte aligned)
-                    uint4* kd = reinterpret_cast<uint4*>(a.dk + t * a.dk_st + hk * a.dk_sh + own_c0);
-                    uint4* qd = reinterpret_cast<uint4*>(a.dq + t * a.dq_st + hk * a.dq_sh + own_c0);
-#pragma unroll
-                    for (int e = 0; e < KSL; e += 8) {
-                        uint32_t kw[4], qw[4];
-#pragma unroll
-                        for (int x = 0; x < 4; ++x) {
-                            kw[x] = static_cast<uint32_t>(f2b(dKacc[e + 2 * x])) | (static_cast<uint32_t>(f2b(dKacc[e + 2 * x + 1])) << 16);
-                            qw[x] = static_cast<uint32_t>(f2b(dQacc[e + 2 * x])) | (static_cast<uint32_t>(f2b(dQacc[e + 2 * x + 1])) << 16);
-                        }
-                        kd[e / 8] = make_uint4(kw[0], kw[1], kw[2], kw[3]);
-                        qd[e / 8] = make_uint4(qw[0], qw[1], qw[2], qw[3]);
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < KSL; ++e) {
-                        const int d = own_c0 + e;
-                        if (a.group == 1) {
-                            a.dk[t * a.dk_st + hk * a.dk_sh + d] = f2b(dKacc[e]);
-                            a.dq[t * a.dq_st + hk * a.dq_sh + d] = f2b(dQacc[e]);
+                    if (a.group == 1) {
+                        if (a.vec_out) {
+                            *reinterpret_cast<uint32_t*>(orow + d) =
+                                static_cast<uint32_t>(f2b(v0)) | (static_cast<uint32_t>(f2b(v1)) << 16);
                         } else {
-                            a.dkh[(t * HO + h) * KD + d] = dKacc[e];
-                            a.dqh[(t * HO + h) * KD + d] = dQacc[e];
+                            orow[d] = f2b(v0);
+                            orow[d + 1] = f2b(v1);
                         }
+                    } else {
+                        *reinterpret_cast<float2*>(hrow + d) = make_float2(v0, v1);
                     }
                 }
             }
