@@ -96,10 +96,12 @@ __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
-// x = head + rest, both tf32 (the head rounded to nearest, the rest the rounded remainder).
+// x = head + rest: the head is x with its 13 low mantissa bits cleared (a tf32 value), the rest
+// x - head exactly (|rest| < 2^-10 |x|); the tensor core reads the rest's top 19 bits, so the
+// split represents x to about 2^-20 relative.
 __device__ __forceinline__ void split_tf32(float x, uint32_t& hd, uint32_t& rs) {
-    hd = to_tf32(x);
-    rs = to_tf32(x - __uint_as_float(hd));
+    hd = __float_as_uint(x) & 0xFFFFE000u;
+    rs = __float_as_uint(x - __uint_as_float(hd));
 }
 // A fragment (16 x 8, rows m0.., columns k0..) of an element function, split in two.
 template <class F>
@@ -133,6 +135,14 @@ __device__ __forceinline__ void mma2b(float (&c)[4], const uint32_t (&ah)[4], co
     mma_tf32_16x8x8(c, ah, b);
 }
 __device__ __forceinline__ uint32_t fbits(float x) { return __float_as_uint(x); }
+// The same three products with the head x head term in c and the two rest terms in r
+// (two independent accumulation chains; the caller adds r to c at the end).
+__device__ __forceinline__ void mma3s(float (&c)[4], float (&r)[4], const uint32_t (&ah)[4], const uint32_t (&ar)[4],
+                                      const uint32_t (&bh)[2], const uint32_t (&br)[2]) {
+    mma_tf32_16x8x8(r, ar, bh);
+    mma_tf32_16x8x8(r, ah, br);
+    mma_tf32_16x8x8(c, ah, bh);
+}
 
 // The 20 lower (16-row, 8-column) output tiles of a 64 x 64 lower-triangular product, in order.
 __device__ __forceinline__ void lower_tile(int p, int& mt, int& nt) {
@@ -402,7 +412,9 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
             const int mt = w & 3, m0 = 16 * mt, n0 = 8 * (w >> 2);  // this warp's 16 x 8 tile
             {
                 // x = K S_J, Q S_J, K dS_J (rows scaled by rk / rq afterwards); V, dO into the tiles
+                // head and rest products accumulate separately (independent MMA chains)
                 float cx4[4] = {0.f, 0.f, 0.f, 0.f}, cq4[4] = {0.f, 0.f, 0.f, 0.f}, cd4[4] = {0.f, 0.f, 0.f, 0.f};
+                float rx4[4] = {0.f, 0.f, 0.f, 0.f}, rq4[4] = {0.f, 0.f, 0.f, 0.f}, rd4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 2
                 for (int k0 = 0; k0 < KD; k0 += 8) {
                     const int kp = colp<KD>(k0) + t;
@@ -415,9 +427,18 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
                     split_tf32(SJ[(n0 + g) * PK + kp + 4], sh[1], sr[1]);
                     split_tf32(dSJ[(n0 + g) * PK + kp], dh[0], dr[0]);
                     split_tf32(dSJ[(n0 + g) * PK + kp + 4], dh[1], dr[1]);
-                    mma2a(cx4, ak, sh, sr);
-                    mma2a(cq4, aq, sh, sr);
-                    mma2a(cd4, ak, dh, dr);
+                    mma_tf32_16x8x8(rx4, ak, sr);
+                    mma_tf32_16x8x8(rq4, aq, sr);
+                    mma_tf32_16x8x8(rd4, ak, dr);
+                    mma_tf32_16x8x8(cx4, ak, sh);
+                    mma_tf32_16x8x8(cq4, aq, sh);
+                    mma_tf32_16x8x8(cd4, ak, dh);
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    cx4[e] += rx4[e];
+                    cq4[e] += rq4[e];
+                    cd4[e] += rd4[e];
                 }
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -440,43 +461,46 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
             {
                 // D = T Y (T lower: column tiles up to the diagonal);  dD = scale P^T dO + Gamma_C (K dS_J)
                 float cD[4] = {0.f, 0.f, 0.f, 0.f}, cE[4] = {0.f, 0.f, 0.f, 0.f};
+                float rD[4] = {0.f, 0.f, 0.f, 0.f}, rE[4] = {0.f, 0.f, 0.f, 0.f};
                 for (int kt = 0; kt <= 2 * mt + 1; ++kt) {
                     const int k0 = 8 * kt;
                     uint32_t ah[4], ar[4], bh[2], br[2];
                     frag_a_split([&](int i, int m) { return s.Tm[i * PC + m]; }, m0, k0, g, t, ah, ar);
                     frag_b_split([&](int m, int cc) { return s.Y[cc * PC + m]; }, k0, n0, g, t, bh, br);
-                    mma3(cD, ah, ar, bh, br);
+                    mma3s(cD, rD, ah, ar, bh, br);
                 }
                 for (int kt = 2 * mt; kt < 8; ++kt) {
                     const int k0 = 8 * kt;
                     uint32_t ah[4], ar[4];
                     frag_a_split([&](int i, int m) { return s.Pm[m * PC + i]; }, m0, k0, g, t, ah, ar);
                     const uint32_t b[2] = {fbits(s.OJ[(n0 + g) * PC + k0 + t]), fbits(s.OJ[(n0 + g) * PC + k0 + t + 4])};
-                    mma2b(cE, ah, ar, b);
+                    mma_tf32_16x8x8(rE, ar, b);
+                    mma_tf32_16x8x8(cE, ah, b);
                 }
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int i = m0 + g + 8 * (e >> 1), cc = n0 + 2 * t + (e & 1);
-                    s.D[cc * PC + i] = cD[e];
-                    s.dD[cc * PC + i] = a.scale * cE[e] + s.GC[i] * s.KdS[cc * PC + i];
+                    s.D[cc * PC + i] = cD[e] + rD[e];
+                    s.dD[cc * PC + i] = a.scale * (cE[e] + rE[e]) + s.GC[i] * s.KdS[cc * PC + i];
                 }
             }
             __syncthreads();
             {
                 // dY = T^T dD (T^T upper: column tiles from the diagonal); dV = beta dY (final)
-                float cY[4] = {0.f, 0.f, 0.f, 0.f};
+                float cY[4] = {0.f, 0.f, 0.f, 0.f}, rY[4] = {0.f, 0.f, 0.f, 0.f};
                 for (int kt = 2 * mt; kt < 8; ++kt) {
                     const int k0 = 8 * kt;
                     uint32_t ah[4], ar[4], bh[2], br[2];
                     frag_a_split([&](int i, int m) { return s.Tm[m * PC + i]; }, m0, k0, g, t, ah, ar);
                     frag_b_split([&](int m, int cc) { return s.dD[cc * PC + m]; }, k0, n0, g, t, bh, br);
-                    mma3(cY, ah, ar, bh, br);
+                    mma3s(cY, rY, ah, ar, bh, br);
                 }
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int i = m0 + g + 8 * (e >> 1), cc = n0 + 2 * t + (e & 1);
-                    s.dY[cc * PC + i] = cY[e];
-                    if (i < n) a.dv[(t0 + i) * a.dv_st + h * a.dv_sh + j0 + cc] = f2b(s.beta[i] * cY[e]);
+                    const float dy = cY[e] + rY[e];
+                    s.dY[cc * PC + i] = dy;
+                    if (i < n) a.dv[(t0 + i) * a.dv_st + h * a.dv_sh + j0 + cc] = f2b(s.beta[i] * dy);
                 }
             }
             __syncthreads();
