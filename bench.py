@@ -498,7 +498,7 @@ def run_decode(args, world, rank, local):
 
 
 BWD_METRIC = "GDN bwd tokens/s (T=65536,H=32,K=V=128; gradients of q,k,v,g,beta,initial state)"
-FP32_LANES_PER_SM = 128  # FP32 FMA lanes per SM (4 partitions x 32)
+TF32_PER_BF16 = 1.1 / 2.25  # nominal dense tf32 / bf16 tensor rates of the part
 
 
 def bwd_algorithmic_flops(lengths, HO, K, V, C=64):
@@ -562,14 +562,8 @@ def run_bwd_bench(args, world, rank, local):
     kern_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in k_ev)
     assert la.read_status(status) == 0
     flops = bwd_algorithmic_flops(w.lengths(), HV, K, V)
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    peaks = {}
-    try:
-        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
-    except (OSError, ValueError):
-        pass
-    sm_mhz = float(peaks.get("sm_max_mhz", 2070.0))
-    alu_peak = sms * FP32_LANES_PER_SM * 2 * sm_mhz * 1e6 / 1e12  # TFLOP/s, fp32 FMA
+    _, bf16_peak, peak_src = load_peaks()
+    tf32_peak = bf16_peak * TF32_PER_BF16  # TFLOP/s: the products run on tf32 tensor-core MMAs
     achieved = flops / (kern_ms * 1e-3) / 1e12
 
     # end to end: the step's inputs, cotangents and checkpoints copied from pinned host memory,
@@ -624,9 +618,10 @@ def run_bwd_bench(args, world, rank, local):
                        "global_batch": N * world, "seq_len": 8192,
                        "parallelism": "single GPU" if world == 1 else f"independent batches per GPU x{world}",
                        "l2": "inputs larger than L2 (1.6 GB of q/k/v + 2.1 GB of checkpoints per step); no flush"},
-            "roofline": {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
-                         "frac": achieved / alu_peak, "traffic": None,
-                         "peak_source": f"{sms} SMs x {FP32_LANES_PER_SM} fp32 FMA lanes x 2 FLOP x {sm_mhz:.0f} MHz",
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": tf32_peak, "unit": "TFLOP/s",
+                         "frac": achieved / tf32_peak, "traffic": None,
+                         "peak_source": f"{peak_src} bf16 x {TF32_PER_BF16:.3f} (nominal dense tf32 / bf16); "
+                                        "each fp32 product is 2-3 tf32 MMAs (head and remainder splits)",
                          "kernel": "gdn_bwd_kernel<128, 128>", "kernel_ms": kern_ms, "algorithmic_flops": flops},
             "cpu_baseline": cpu,
             "e2e": {"value": T * world / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
@@ -816,6 +811,106 @@ def run_summary_bench(args, world, rank, local):
     return 0
 
 
+SUM_BWD_METRIC = ("GDN summary_bwd tokens/s (state gradient entering each span; one 131072-token sequence, "
+                  "8 spans, H=16, K=V=128)")
+
+
+def summary_bwd_algorithmic_flops(lengths, HO, K, V, C=64):
+    """Arithmetic of the state-gradient recursion per (chunk, head): K K^T and Q K^T (lower
+    halves), the triangular inverse, K dS, P^T dO, T^T dD and the dS update K^T dx + Q^T dO."""
+    per = (2 * (C * (C + 1) // 2) * K * 2 + C ** 3 // 3 * 2 + C * K * V * 2 + 2 * (C * (C + 1) // 2) * V * 2
+           + 2 * K * C * V * 2)
+    chunks = sum((int(L) + C - 1) // C for L in lengths)
+    return int(per * chunks * HO)
+
+
+def run_summary_bwd_bench(args, world, rank, local):
+    """gdn_summary_bwd over the context-parallel workload: one 131072-token sequence cut into 8
+    spans of 16384, 16 heads, K = V = 128: per span and head the gradient of the span's outputs
+    with respect to the state entering it (zero exit cotangent)."""
+    import gated_delta_rule_29_gb300 as la
+    from gated_delta_rule_29_gb300 import binding as B
+    from gated_delta_rule_29_gb300 import workloads as W
+
+    assert torch.cuda.is_available(), "bench needs a CUDA device (there is no CPU fallback)"
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lib = B.load()
+    w = W.config(5)
+    T, HK, HV, K, V = w.T, w.HK, w.HV, w.K, w.V
+    gen = torch.Generator().manual_seed(1013)
+    do_h = torch.randn(T, HV, V, generator=gen).to(torch.bfloat16)
+    q, k, g, b, spans, do = (x.to(dev) for x in (w.q, w.k, w.g, w.beta, w.spans, do_h))
+    S = spans.numel() - 1
+    ws = torch.empty(lib.la_gdn_summary_bwd_workspace_bytes(S, HV, K, V), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def step():
+        return la.gdn_summary_bwd(q, k, g, b, spans, do, workspace=ws, status=status)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert la.read_status(status) == 0
+    stream = torch.cuda.current_stream()
+    k_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a_, b_ in k_ev:
+        a_.record(stream)
+        b_.record(stream)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(args.steps):
+            lib.la_set_kernel_timing_events(k_ev[i][0].cuda_event, k_ev[i][1].cuda_event)
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    ms = max_over_ranks(e0.elapsed_time(e1) / args.steps, world)
+    kern_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in k_ev)
+    assert la.read_status(status) == 0
+    alg = T * (2 * HK * K + HV * V) * 2 + 2 * T * HV * 4 + S * HV * K * V * 4 + (S + 1) * 4
+    flops = summary_bwd_algorithmic_flops([T // S] * S, HV, K, V)
+    hbm_peak, bf16_peak, peak_src = load_peaks()
+    tf32_peak = bf16_peak * TF32_PER_BF16
+    tflops = flops / (kern_ms * 1e-3) / 1e12
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle  # CPU baseline only
+        n_tok = 4096
+        t0 = time.perf_counter()
+        oracle.gdn_summary_bwd(w.q[:n_tok, :1], w.k[:n_tok, :1], w.g[:n_tok, :1], w.beta[:n_tok, :1],
+                               np.array([0, n_tok]), do_h[:n_tok, :1])
+        dt = time.perf_counter() - t0
+        cpu = {"value": n_tok / HV / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+               "sample": f"1 head x the first {n_tok} tokens of span 0 ({dt:.1f} s), fp64 token-by-token "
+                         f"reverse recursion of the state gradient (numpy, one thread)"}
+    if rank == 0:
+        line = {
+            "metric": SUM_BWD_METRIC, "value": T * world / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "summary_bwd: one sequence of 131072 tokens, 8 spans of 16384, H=16, K=V=128, "
+                                   "zero exit cotangent", "global_batch": 1, "seq_len": T, "parallelism": "single GPU",
+                       "l2": "inputs larger than L2 (1.1 GB of q/k/dO per step); no flush"},
+            "roofline": {"bound": "tensor", "achieved": tflops, "peak": tf32_peak, "unit": "TFLOP/s",
+                         "frac": tflops / tf32_peak, "traffic": None,
+                         "peak_source": f"{peak_src} bf16 x {TF32_PER_BF16:.3f} (nominal dense tf32 / bf16)",
+                         "kernel": "gdn_bwd_kernel<128, 128> (state-gradient mode)", "kernel_ms": kern_ms,
+                         "algorithmic_flops": flops, "algorithmic_bytes": alg,
+                         "hbm_frac": alg / (kern_ms * 1e-3) / 1e9 / hbm_peak},
+            "cpu_baseline": cpu,
+            "e2e": None,
+            "gpu_launches": 2 * args.steps,
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -828,10 +923,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--e2e-groups", type=int, default=8, help="sequence groups pipelined by gdn_fwd_host")
-    ap.add_argument("--workload", choices=["dense", "decode", "bwd", "gdp", "summary"], default="dense",
+    ap.add_argument("--workload", choices=["dense", "decode", "bwd", "gdp", "summary", "summary_bwd"],
+                    default="dense",
                     help="dense: the chunked forward over the dense batch (the headline); "
                          "decode: one decode step against a state pool; bwd: the backward of the dense batch; "
-                         "gdp: Gated DeltaProduct with 2 updates per token; summary: gdn_summary over 8 spans")
+                         "gdp: Gated DeltaProduct with 2 updates per token; summary: gdn_summary over 8 spans; "
+                         "summary_bwd: the summary's state-gradient mirror over the same spans")
     ap.add_argument("--seq-len", type=int, default=8192,
                     help="tokens per sequence of the dense batch (8192 is the benchmark workload)")
     args = ap.parse_args()
@@ -849,6 +946,8 @@ def main():
             return run_gdp_bench(args, world, rank, local)
         if args.workload == "summary":
             return run_summary_bench(args, world, rank, local)
+        if args.workload == "summary_bwd":
+            return run_summary_bwd_bench(args, world, rank, local)
         return run_ours(args, world, rank, local)
     finally:
         if world > 1:

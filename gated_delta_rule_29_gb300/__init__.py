@@ -2,11 +2,12 @@
 
 The computation lives in liblinattn.so (C ABI: include/liblinattn.h), built
 in-tree from csrc/ by ``_build.build()``.  This package is its thin Python
-binding: ``gdn_fwd``, ``gdn_bwd``, ``gdn_summary`` and ``gdn_decode`` marshal torch tensors
+binding: ``gdn_fwd``, ``gdn_bwd``, ``gdn_summary``, ``gdn_summary_bwd`` and ``gdn_decode`` marshal torch tensors
 into the C structs and launch on the current CUDA stream.  There is no CPU fallback.
 """
-from .api import (checkpoint_rows, gdn_bwd, gdn_decode, gdn_fwd, gdn_fwd_host, gdn_summary, read_status,  # noqa: F401
-                  workspace_bytes)
+from .api import (checkpoint_rows, gdn_bwd, gdn_decode, gdn_fwd, gdn_fwd_host, gdn_summary,  # noqa: F401
+                  gdn_summary_bwd, read_status, workspace_bytes)
 from . import binding  # noqa: F401
 
-__all__ = ["gdn_fwd", "gdn_fwd_host", "gdn_summary", "gdn_decode", "gdn_bwd", "read_status", "checkpoint_rows", "workspace_bytes", "binding"]
+__all__ = ["gdn_fwd", "gdn_fwd_host", "gdn_summary", "gdn_summary_bwd", "gdn_decode", "gdn_bwd", "read_status",
+           "checkpoint_rows", "workspace_bytes", "binding"]

@@ -291,6 +291,48 @@ def gdn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
     return dq, dk, dv, dg, db, ds0
 
 
+def gdn_summary_bwd(q: torch.Tensor, k: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
+                    cu_seqlens: torch.Tensor, d_o: torch.Tensor, *, scale: Optional[float] = None,
+                    use_qk_l2norm: bool = True, d_final_state: Optional[torch.Tensor] = None,
+                    workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
+                    stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """State-gradient mirror of gdn_summary: for each span (sequence) the gradient of
+    sum(d_o * o) + sum(d_final_state * end_state) with respect to the state entering the span,
+    [N, HO, K, V] fp32.  It depends on neither that state nor v; with gdn_summary's transition,
+    d_enter = einsum('ab,bv->av', transition, d_exit) + (the value for d_exit = 0)."""
+    _check_thd("q", q, torch.bfloat16)
+    _check_thd("k", k, torch.bfloat16)
+    _check_thd("g", g, torch.float32, heads_dim=False)
+    _check_thd("beta", beta, torch.float32, heads_dim=False)
+    _check_thd("d_o", d_o, torch.bfloat16)
+    T, HK, K = k.shape
+    HV, V = d_o.shape[1], d_o.shape[2]
+    N = cu_seqlens.numel() - 1
+    dev = q.device
+    d_state = torch.empty(N, HV, K, V, dtype=torch.float32, device=dev)
+    lib = B.load()
+    if workspace is None:
+        workspace = torch.empty(lib.la_gdn_summary_bwd_workspace_bytes(N, HV, K, V), dtype=torch.uint8, device=dev)
+    if d_final_state is not None:
+        d_final_state = d_final_state.contiguous().float()
+    p = B.GdnSummaryBwdParams()
+    p.q, p.q_stride_t, p.q_stride_h = q.data_ptr(), q.stride(0), q.stride(1)
+    p.k, p.k_stride_t, p.k_stride_h = k.data_ptr(), k.stride(0), k.stride(1)
+    p.g, p.g_stride_t, p.g_stride_h = g.data_ptr(), g.stride(0), g.stride(1)
+    p.beta, p.beta_stride_t, p.beta_stride_h = beta.data_ptr(), beta.stride(0), beta.stride(1)
+    p.cu_seqlens, p.cu_seqlens_bits = cu_seqlens.data_ptr(), _cu_bits(cu_seqlens)
+    p.T, p.N, p.HK, p.HV, p.K, p.V = T, N, HK, HV, K, V
+    p.scale = float(scale) if scale is not None else 1.0 / math.sqrt(K)
+    p.use_qk_l2norm = int(bool(use_qk_l2norm))
+    p.d_o, p.d_o_stride_t, p.d_o_stride_h = d_o.data_ptr(), d_o.stride(0), d_o.stride(1)
+    p.d_final_state = d_final_state.data_ptr() if d_final_state is not None else None
+    p.d_state = d_state.data_ptr()
+    p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel()
+    p.status = status.data_ptr() if status is not None else None
+    B.check(lib.gdn_summary_bwd(ctypes.byref(p), _stream_ptr(stream)), "gdn_summary_bwd")
+    return d_state
+
+
 def gdn_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
                state_pool: torch.Tensor, *, state_indices: Optional[torch.Tensor] = None,
                scale: Optional[float] = None, use_qk_l2norm: bool = True, o: Optional[torch.Tensor] = None,

@@ -41,6 +41,8 @@ EXPORTED_SYMBOLS = (
     "gdn_bwd",
     "la_gdn_bwd_workspace_bytes",
     "la_gdp_workspace_bytes",
+    "gdn_summary_bwd",
+    "la_gdn_summary_bwd_workspace_bytes",
 )
 
 _i64 = ctypes.c_int64
@@ -118,6 +120,10 @@ def load(build_if_missing: bool = True):
         lib.gdn_fwd.argtypes = [ctypes.POINTER(GdnFwdParams), _vp]
         lib.gdn_bwd.restype = ctypes.c_int
         lib.gdn_bwd.argtypes = [ctypes.POINTER(GdnBwdParams), _vp]
+        lib.gdn_summary_bwd.restype = ctypes.c_int
+        lib.gdn_summary_bwd.argtypes = [ctypes.POINTER(GdnSummaryBwdParams), _vp]
+        lib.la_gdn_summary_bwd_workspace_bytes.restype = ctypes.c_size_t
+        lib.la_gdn_summary_bwd_workspace_bytes.argtypes = [_i32, _i32, _i32, _i32]
         lib.la_gdp_workspace_bytes.restype = ctypes.c_size_t
         lib.la_gdp_workspace_bytes.argtypes = [_i64, _i32, _i32, _i32, _i32, _i32, _i32]
         lib.la_gdn_bwd_workspace_bytes.restype = ctypes.c_size_t
@@ -185,6 +191,25 @@ class GdnBwdParams(ctypes.Structure):
         ("dg", _vp), ("dg_stride_t", _i64), ("dg_stride_h", _i64),
         ("dbeta", _vp), ("dbeta_stride_t", _i64), ("dbeta_stride_h", _i64),
         ("d_initial_state", _vp),
+        ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
+        ("status", _vp),
+    ]
+
+
+class GdnSummaryBwdParams(ctypes.Structure):
+    """Mirror of la_gdn_summary_bwd_params (same field order and types)."""
+    _fields_ = [
+        ("q", _vp), ("q_stride_t", _i64), ("q_stride_h", _i64),
+        ("k", _vp), ("k_stride_t", _i64), ("k_stride_h", _i64),
+        ("g", _vp), ("g_stride_t", _i64), ("g_stride_h", _i64),
+        ("beta", _vp), ("beta_stride_t", _i64), ("beta_stride_h", _i64),
+        ("cu_seqlens", _vp), ("cu_seqlens_bits", _i32),
+        ("T", _i64),
+        ("N", _i32), ("HK", _i32), ("HV", _i32), ("K", _i32), ("V", _i32),
+        ("scale", ctypes.c_float), ("use_qk_l2norm", _i32),
+        ("d_o", _vp), ("d_o_stride_t", _i64), ("d_o_stride_h", _i64),
+        ("d_final_state", _vp),
+        ("d_state", _vp),
         ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
         ("status", _vp),
     ]

@@ -9,9 +9,10 @@ composes the state entering its span,
 
 then runs gdn_fwd on its span from that state (cuDNN Linear Attention page,
 "Summaries": the summaries compose across spans to give context parallelism).
-The backward mirrors it: each rank's state gradient from its own outputs, one
-all-gather, and the reverse composition dS_enter = transition dS_exit give every
-rank the cotangent of its span's end state for gdn_bwd.
+The backward mirrors it: each rank's state gradient from its own outputs
+(gdn_summary_bwd, the summary's mirror for the state gradient), one all-gather, and
+the reverse composition dS_enter = transition dS_exit + dS_H give every rank the
+cotangent of its span's end state for gdn_bwd.
 The composition is a handful of small fp32 products per rank and runs on
 whatever device the tensors live on; the exchange is the only collective.
 """
@@ -49,7 +50,8 @@ def compose_grads(transitions: List[torch.Tensor], local_grads: List[torch.Tenso
     The gradients are linear in the final-state cotangent, and through a span the state gradient
     moves as dS_enter = einsum('ab,bv->av', transition, dS_exit) (the transpose of the forward
     composition).  local_grads[r] is the entering-state gradient of span r from its own outputs
-    alone (gdn_bwd with a zero final-state cotangent); d_final the cotangent of the state after
+    alone (gdn_summary_bwd, or gdn_bwd with a zero final-state cotangent); d_final the cotangent
+    of the state after
     the last span.  Returns len(spans) + 1 tensors: the gradient leaving each span (dS_exit_r,
     the final-state cotangent to use for span r), then the gradient entering span 0.
     """
@@ -66,8 +68,8 @@ def exit_state_grad(transition: torch.Tensor, local_grad: torch.Tensor,
                     d_final: Optional[torch.Tensor] = None, group=None) -> torch.Tensor:
     """Final-state cotangent for this rank's span in the context-parallel backward.
 
-    Ranks hold consecutive spans in rank order.  Each rank first runs gdn_bwd on its span with a
-    zero final-state cotangent (local_grad = its d_initial_state), then one all-gather of
+    Ranks hold consecutive spans in rank order.  Each rank first takes its span's own state
+    gradient (local_grad: gdn_summary_bwd, zero exit cotangent), then one all-gather of
     (transition, local_grad) lets every rank compose the gradient arriving at its span's end;
     running gdn_bwd again with that cotangent (or adding the contribution of the second run, the
     gradients being linear in it) completes the rank's gradients.  `d_final` is the cotangent

@@ -180,6 +180,7 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
     __syncthreads();
 
     constexpr int KSL = KD / 4;
+    const bool so = a.state_only != 0;  // the entering-state gradient alone
 
     // Asynchronous fetch of one value tile (chunk cc, columns j0..j0+15) into buffer pb: the
     // S and dS columns (4-byte copies, transposed into the tile layout) and the raw V and dO
@@ -187,10 +188,15 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
     auto fetch_tile = [&](int cc, int j0, int pb) {
         const int64_t ft0 = ts + static_cast<int64_t>(cc) * kC;
         const int fn = static_cast<int>(L - static_cast<int64_t>(cc) * kC < kC ? L - static_cast<int64_t>(cc) * kC : kC);
-        const float* Sf = a.ckpt + ((a.ckpt_off[seq] + cc) * HO + h) * KV;
+        if (!so) {
+            const float* Sf = a.ckpt + ((a.ckpt_off[seq] + cc) * HO + h) * KV;
+            for (int e = tid; e < KD * kVT; e += kBT) {
+                const int r = e / kVT, col = e % kVT;
+                cp_async4(&s.SJ[pb][col * PK + colp<KD>(r)], Sf + r * VD + j0 + col);
+            }
+        }
         for (int e = tid; e < KD * kVT; e += kBT) {
             const int r = e / kVT, col = e % kVT;
-            cp_async4(&s.SJ[pb][col * PK + colp<KD>(r)], Sf + r * VD + j0 + col);
             cp_async4(&s.dSJ[pb][col * PK + colp<KD>(r)], dSg + r * VD + j0 + col);
         }
         for (int e = tid; e < kC * kVT / 2; e += kBT) {
@@ -201,16 +207,19 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
                 *reinterpret_cast<uint32_t*>(vd) = 0u;
                 *reinterpret_cast<uint32_t*>(od) = 0u;
             } else {
-                const uint16_t* vs = a.v + (ft0 + i) * a.v_st + h * a.v_sh + j0 + c2;
                 const uint16_t* os = a.dout + (ft0 + i) * a.do_st + h * a.do_sh + j0 + c2;
-                if (a.vo_async) {
-                    cp_async4(vd, vs);
-                    cp_async4(od, os);
-                } else {
-                    vd[0] = vs[0];
-                    vd[1] = vs[1];
+                if (a.vo_async) cp_async4(od, os);
+                else {
                     od[0] = os[0];
                     od[1] = os[1];
+                }
+                if (!so) {
+                    const uint16_t* vs = a.v + (ft0 + i) * a.v_st + h * a.v_sh + j0 + c2;
+                    if (a.vo_async) cp_async4(vd, vs);
+                    else {
+                        vd[0] = vs[0];
+                        vd[1] = vs[1];
+                    }
                 }
             }
         }
@@ -400,7 +409,7 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
         for (int j0 = 0; j0 < VD; j0 += kVT) {
             cp_async_wait_all();
             __syncthreads();  // this tile's S, dS, V, dO have landed; the previous tile is done
-            if (tid == 0 && j0 > 0) {
+            if (tid == 0 && j0 > 0 && !so) {
                 // the previous tile's Gamma_C terms of S_next and the decay of S into S_next
                 float p = 0.f, wsum = 0.f;
                 for (int x = 0; x < kBT / 32; ++x) p += s.red[x];
@@ -410,7 +419,27 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
             const float* SJ = s.SJ[pb];
             const float* dSJ = s.dSJ[pb];
             const int mt = w & 3, m0 = 16 * mt, n0 = 8 * (w >> 2);  // this warp's 16 x 8 tile
-            {
+            if (so) {
+                // K dS_J alone (rows scaled by rk afterwards); dO into its tile
+                float cd4[4] = {0.f, 0.f, 0.f, 0.f}, rd4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+                for (int k0 = 0; k0 < KD; k0 += 8) {
+                    const int kp = colp<KD>(k0) + t;
+                    const uint32_t ak[4] = {fbits(s.Kr[(m0 + g) * PK + kp]), fbits(s.Kr[(m0 + g + 8) * PK + kp]),
+                                            fbits(s.Kr[(m0 + g) * PK + kp + 4]), fbits(s.Kr[(m0 + g + 8) * PK + kp + 4])};
+                    uint32_t dh[2], dr[2];
+                    split_tf32(dSJ[(n0 + g) * PK + kp], dh[0], dr[0]);
+                    split_tf32(dSJ[(n0 + g) * PK + kp + 4], dh[1], dr[1]);
+                    mma_tf32_16x8x8(rd4, ak, dr);
+                    mma_tf32_16x8x8(cd4, ak, dh);
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int i = m0 + g + 8 * (e >> 1), cc = n0 + 2 * t + (e & 1);
+                    s.KdS[cc * PC + i] = s.rk[i] * (cd4[e] + rd4[e]);
+                    s.OJ[cc * PC + i] = b2f(s.Ob[i * kVT + cc]);
+                }
+            } else {
                 // x = K S_J, Q S_J, K dS_J (rows scaled by rk / rq afterwards); V, dO into the tiles
                 // head and rest products accumulate separately (independent MMA chains)
                 float cx4[4] = {0.f, 0.f, 0.f, 0.f}, cq4[4] = {0.f, 0.f, 0.f, 0.f}, cd4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -462,7 +491,7 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
                 // D = T Y (T lower: column tiles up to the diagonal);  dD = scale P^T dO + Gamma_C (K dS_J)
                 float cD[4] = {0.f, 0.f, 0.f, 0.f}, cE[4] = {0.f, 0.f, 0.f, 0.f};
                 float rD[4] = {0.f, 0.f, 0.f, 0.f}, rE[4] = {0.f, 0.f, 0.f, 0.f};
-                for (int kt = 0; kt <= 2 * mt + 1; ++kt) {
+                for (int kt = 0; kt <= (so ? -1 : 2 * mt + 1); ++kt) {
                     const int k0 = 8 * kt;
                     uint32_t ah[4], ar[4], bh[2], br[2];
                     frag_a_split([&](int i, int m) { return s.Tm[i * PC + m]; }, m0, k0, g, t, ah, ar);
@@ -500,11 +529,11 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
                     const int i = m0 + g + 8 * (e >> 1), cc = n0 + 2 * t + (e & 1);
                     const float dy = cY[e] + rY[e];
                     s.dY[cc * PC + i] = dy;
-                    if (i < n) a.dv[(t0 + i) * a.dv_st + h * a.dv_sh + j0 + cc] = f2b(s.beta[i] * dy);
+                    if (i < n && !so) a.dv[(t0 + i) * a.dv_st + h * a.dv_sh + j0 + cc] = f2b(s.beta[i] * dy);
                 }
             }
             __syncthreads();
-            {
+            if (!so) {
                 // gamma_last <dS_J, S_J>: the decay of the entering state into S_next
                 float p = 0.f;
                 for (int e = tid; e < KD * kVT; e += kBT) {
@@ -515,7 +544,7 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
                 for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
                 if (lane == 0) s.red[w] = p;
             }
-            if (kwarp) {
+            if (kwarp && !so) {
                 // dK_hat += dx S_J^T + Gamma_C D dS_J^T,  dx = -beta gamma dY
 #pragma unroll
                 for (int kt = 0; kt < 2; ++kt) {
@@ -561,8 +590,8 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
                         if (j <= i) s.dP[i * PC + j] += a.scale * cp[e];
                     }
                 }
-            } else {
-                if (tid < 128 + kC) {
+            } else if (!kwarp) {
+                if (tid < 128 + kC && !so) {
                     // per-row sums: dbeta (Y's beta), db (Y's gamma, O's gamma); the Gamma_Cj terms
                     // of S_next, w_j = Gamma_Cj sum_v (K dS_J)_jv D_jv, move from b_j to b_last
                     const int i = tid - 128;
@@ -581,7 +610,7 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
                 }
                 // dQ_hat sum += dO S_J^T (the row factor scale gamma_i is applied after the tiles)
 #pragma unroll
-                for (int kt = 0; kt < 2; ++kt) {
+                for (int kt = 0; kt < (so ? 0 : 2); ++kt) {
                     const int k0 = 8 * kt;
                     const uint32_t ao[4] = {fbits(s.OJ[(k0 + t) * PC + om0 + g]), fbits(s.OJ[(k0 + t) * PC + om0 + g + 8]),
                                             fbits(s.OJ[(k0 + t + 4) * PC + om0 + g]),
@@ -648,6 +677,7 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
             pb ^= 1;
         }
         __syncthreads();
+        if (so) continue;  // the state gradient is all this mode computes
         if (tid == 0) {
             float p = 0.f, wsum = 0.f;
             for (int x = 0; x < kBT / 32; ++x) p += s.red[x];
@@ -847,7 +877,7 @@ cudaError_t launch_bwd_kv(const BwdArgs& a, cudaStream_t s) {
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    if (a.group > 1 && a.T > 0) {
+    if (a.group > 1 && a.T > 0 && !a.state_only) {
         gdn_bwd_group_sum_kernel<<<1024, 256, 0, s>>>(a);
         return cudaGetLastError();
     }

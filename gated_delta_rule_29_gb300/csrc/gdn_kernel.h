@@ -157,6 +157,8 @@ struct BwdArgs {
     float* dkh;
     int32_t vec_out;                 // dq, dk rows 16-byte aligned: 16-byte stores
     int32_t vo_async;                // v, dO pairs 4-byte aligned: asynchronous 4-byte copies
+    int32_t state_only;              // only the entering-state gradient (gdn_summary_bwd): no
+                                     // checkpoints, v, dq, dk, dv, dg, dbeta
 };
 
 // Gated DeltaProduct: the update timeline for the chunk kernel, and the per-token outputs.

@@ -489,9 +489,25 @@ BwdLayout bwd_layout(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, in
     L.total = off;
     return L;
 }
+// gdn_summary_bwd: the prologue's area, then the carried state gradient of every (sequence, head).
+struct SumBwdLayout {
+    size_t pro, ds, total;
+};
+SumBwdLayout sum_bwd_layout(int32_t N, int32_t HV, int32_t K, int32_t V) {
+    SumBwdLayout L{};
+    L.pro = 0;
+    L.ds = up256(la::ws_layout(N).total);
+    L.total = L.ds + up256(static_cast<size_t>(N) * HV * K * V * sizeof(float));
+    return L;
+}
 }  // namespace
 
 extern "C" {
+
+size_t la_gdn_summary_bwd_workspace_bytes(int32_t N, int32_t HV, int32_t K, int32_t V) {
+    if (N < 0 || HV <= 0 || K <= 0 || V <= 0) return 0;
+    return sum_bwd_layout(N, HV, K, V).total;
+}
 
 size_t la_gdn_bwd_workspace_bytes(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, int32_t V,
                                   int32_t checkpoints_given) {
@@ -597,6 +613,67 @@ la_status gdn_bwd(const la_gdn_bwd_params* p, void* stream) {
         b.dqh = reinterpret_cast<float*>(wb + BL.gh);
         b.dkh = b.dqh + static_cast<size_t>(p->T) * p->HV * p->K;
     }
+    cudaEvent_t ev0 = t_timing_start, ev1 = t_timing_stop;
+    t_timing_start = t_timing_stop = nullptr;
+    if (ev0 && cudaEventRecord(ev0, s) != cudaSuccess) return LA_ERR_CUDA;
+    if (la::launch_bwd(b, s) != cudaSuccess) return LA_ERR_CUDA;
+    if (ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return LA_ERR_CUDA;
+    return LA_OK;
+}
+
+la_status gdn_summary_bwd(const la_gdn_summary_bwd_params* p, void* stream) {
+    if (!p) return LA_ERR_INVALID_ARG;
+    Common c{p->T, p->N, p->HK, p->HV, p->K, p->V, p->cu_seqlens, p->cu_seqlens_bits, p->g, p->beta, 4};
+    la_status st = check_common(c);
+    if (st != LA_OK) return st;
+    if (!p->d_state || !aligned(p->d_state, 4)) return LA_ERR_INVALID_ARG;
+    if (p->d_final_state && !aligned(p->d_final_state, 4)) return LA_ERR_INVALID_ARG;
+    if (p->T > 0) {
+        if ((st = check_tma_operand(p->q, p->q_stride_t, p->q_stride_h, p->HK)) != LA_OK) return st;
+        if ((st = check_tma_operand(p->k, p->k_stride_t, p->k_stride_h, p->HK)) != LA_OK) return st;
+        if (!p->d_o || !aligned(p->d_o, 2)) return LA_ERR_INVALID_ARG;
+    }
+    const SumBwdLayout SL = sum_bwd_layout(p->N, p->HV, p->K, p->V);
+    void* ws = p->workspace;
+    if (ws) {
+        if (p->workspace_bytes < SL.total || !aligned(ws, 256)) return LA_ERR_WORKSPACE;
+    } else if ((st = internal_workspace(SL.total, &ws)) != LA_OK) {
+        return st;
+    }
+    uint8_t* wb = static_cast<uint8_t*>(ws);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const la::WorkspaceLayout PL = la::ws_layout(p->N);
+    // the prologue validates cu_seqlens into the status word the kernel reads first
+    PrologueArgs pa;
+    pa.cu = p->cu_seqlens;
+    pa.cu64 = p->cu_seqlens_bits == 64;
+    pa.T = p->T;
+    pa.N = p->N;
+    pa.ckpt_n = la::kChunk;
+    pa.hdr = reinterpret_cast<la::WsHeader*>(wb + SL.pro);
+    pa.order = reinterpret_cast<int32_t*>(wb + SL.pro + PL.order);
+    pa.ckpt_off = reinterpret_cast<int64_t*>(wb + SL.pro + PL.ckpt_off);
+    pa.keys = reinterpret_cast<uint64_t*>(wb + SL.pro + PL.keys);
+    pa.user_status = p->status;
+    if (la::launch_prologue(pa, s) != cudaSuccess) return LA_ERR_CUDA;
+    la::BwdArgs b;
+    std::memset(&b, 0, sizeof(b));
+    b.q = static_cast<const uint16_t*>(p->q); b.q_st = p->q_stride_t; b.q_sh = p->q_stride_h;
+    b.k = static_cast<const uint16_t*>(p->k); b.k_st = p->k_stride_t; b.k_sh = p->k_stride_h;
+    b.g = p->g; b.g_st = p->g_stride_t; b.g_sh = p->g_stride_h;
+    b.beta = p->beta; b.b_st = p->beta_stride_t; b.b_sh = p->beta_stride_h;
+    b.cu = p->cu_seqlens; b.cu64 = p->cu_seqlens_bits == 64;
+    b.T = p->T; b.N = p->N; b.HK = p->HK; b.HV = p->HV; b.K = p->K; b.V = p->V; b.group = p->HV / p->HK;
+    b.scale = p->scale > 0.f ? p->scale : 1.0f / std::sqrt(static_cast<float>(p->K));
+    b.l2norm = p->use_qk_l2norm != 0;
+    b.dout = static_cast<const uint16_t*>(p->d_o); b.do_st = p->d_o_stride_t; b.do_sh = p->d_o_stride_h;
+    b.dfinal = p->d_final_state;
+    b.ckpt_off = reinterpret_cast<const int64_t*>(wb + SL.pro + PL.ckpt_off);
+    b.hdr = reinterpret_cast<const la::WsHeader*>(wb + SL.pro);
+    b.dS_work = reinterpret_cast<float*>(wb + SL.ds);
+    b.ds0 = p->d_state;
+    b.vo_async = aligned(p->d_o, 4) && p->d_o_stride_t % 2 == 0 && (p->HV == 1 || p->d_o_stride_h % 2 == 0);
+    b.state_only = 1;
     cudaEvent_t ev0 = t_timing_start, ev1 = t_timing_stop;
     t_timing_start = t_timing_stop = nullptr;
     if (ev0 && cudaEventRecord(ev0, s) != cudaSuccess) return LA_ERR_CUDA;

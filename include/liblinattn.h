@@ -299,6 +299,46 @@ la_status gdn_bwd(const la_gdn_bwd_params* p, void* stream);
 size_t la_gdn_bwd_workspace_bytes(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, int32_t V,
                                   int32_t checkpoints_given);
 
+/* Parameters of gdn_summary_bwd.  Strides are in elements. */
+typedef struct la_gdn_summary_bwd_params {
+    const void* q;    int64_t q_stride_t, q_stride_h;       /* [T, HK, K] bf16 */
+    const void* k;    int64_t k_stride_t, k_stride_h;       /* [T, HK, K] bf16 */
+    const float* g;   int64_t g_stride_t, g_stride_h;       /* [T, HO] fp32, natural-log gate */
+    const float* beta; int64_t beta_stride_t, beta_stride_h; /* [T, HO] fp32 */
+    const void* cu_seqlens;                                 /* [N + 1]: one span per entry */
+    int32_t cu_seqlens_bits;
+    int64_t T;
+    int32_t N, HK, HV, K, V;
+    float scale;                 /* <= 0: 1 / sqrt(K) */
+    int32_t use_qk_l2norm;
+    const void* d_o;  int64_t d_o_stride_t, d_o_stride_h;   /* [T, HO, V] bf16: the outputs' cotangent */
+    const float* d_final_state;  /* [N, HO, K, V] fp32 cotangent of each span's end state, or NULL (zero) */
+    float* d_state;              /* [N, HO, K, V] fp32 out: gradient w.r.t. the state entering each span */
+    void* workspace;             /* >= la_gdn_summary_bwd_workspace_bytes(...), 256-byte aligned, or NULL */
+    size_t workspace_bytes;
+    int32_t* status;
+} la_gdn_summary_bwd_params;
+
+/*
+ * gdn_summary_bwd -- the state-gradient mirror of gdn_summary.
+ *
+ * Page: the summary ops come in pairs, <op>_summary and <op>_summary_bwd, the latter "the
+ * mirror for the state gradient"; together they give context parallelism over spans.  Read
+ * here as: for each span (sequence) and head, the gradient of L = sum(d_o * o) +
+ * sum(d_final_state * S_end) with respect to the state entering the span,
+ *
+ *   d_state = transition applied to d_final_state + dS_H,   dS_H = the same with d_final_state = 0,
+ *
+ * i.e. dS_enter[a][v] = sum_b transition[a][b] dS_exit[b][v] + dS_H[a][v] with gdn_summary's
+ * transition.  That gradient does not depend on the entering state or on v (the map from the
+ * state to the outputs is affine), so neither is an input and no forward pass runs.  Errors and
+ * ownership as gdn_summary; the gate and beta transforms of gdn_fwd are forward-only.
+ */
+la_status gdn_summary_bwd(const la_gdn_summary_bwd_params* p, void* stream);
+
+/* Bytes of device workspace gdn_summary_bwd needs. */
+size_t la_gdn_summary_bwd_workspace_bytes(int32_t N, int32_t HV, int32_t K, int32_t V);
+
 /* Bytes of device workspace gdn_fwd needs with num_householder = n > 1 (the update timeline's
    query, gate and output rows plus the chunk kernel's scratch); n <= 1: la_gdn_workspace_bytes. */
 size_t la_gdp_workspace_bytes(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, int32_t V, int32_t n);
@@ -323,8 +363,9 @@ la_status la_read_status(const int32_t* device_status, void* stream, int32_t* ou
 /*
  * Profiling hook: record `start_event` and `stop_event` (cudaEvent_t handles) on
  * the launch stream immediately before and after the fused chunk kernel of the
- * next gdn_fwd / gdn_summary call (or the decode kernel of the next gdn_decode
- * call) made by this host thread, so a caller can time
+ * next gdn_fwd / gdn_summary call (the decode kernel of the next gdn_decode call,
+ * the backward kernels of the next gdn_bwd / gdn_summary_bwd call) made by this
+ * host thread, so a caller can time
  * that kernel alone with CUDA events.  The hook is consumed by that one call;
  * pass NULL, NULL to clear it.  Not part of the computation; no citation.
  */

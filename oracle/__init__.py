@@ -1,9 +1,10 @@
 """Parity oracle -- TEST INFRASTRUCTURE ONLY.
 
 A plain fp64 CPU restatement of the Gated DeltaNet forward (``gdn_fwd``), of
-the span summary (``gdn_summary``) and of the forward's backward (``gdn_bwd``,
-reverse-mode differentiation of the token recurrence), following the cuDNN "Linear Attention"
-operations page (sections "Layout" and "Semantics worth knowing").  The
+the span summary (``gdn_summary``), of the forward's backward (``gdn_bwd``,
+reverse-mode differentiation of the token recurrence) and of the summary's
+state-gradient mirror (``gdn_summary_bwd``), following the cuDNN "Linear Attention"
+operations page (sections "Layout", "Semantics worth knowing" and "Summaries").  The
 arithmetic lives in ``gdn_oracle.c`` (token-by-token recurrence, fp64); this
 module only compiles it with gcc, converts inputs to fp64 and marshals
 arguments.  The optional in-kernel input transforms of cudnn-frontend PR #616
@@ -57,6 +58,7 @@ MUTATIONS = {
     # planted in the backward
     14: "backward: decay gradient misses the erase path (uses dS instead of dS')",
     15: "backward: key gradient misses the S' dx term",
+    18: "summary backward: a token's output term added after its erase step instead of before",
 }
 
 
@@ -302,6 +304,49 @@ def gdn_bwd(q, k, v, g, beta, cu_seqlens, do, *, scale=None, use_qk_l2norm=True,
     dq = dqh.reshape(T, HK, grp, K).sum(axis=2)
     dk = dkh.reshape(T, HK, grp, K).sum(axis=2)
     return {"dq": dq, "dk": dk, "dv": dv, "dg": dg, "dbeta": db, "d_initial_state": ds0}
+
+
+def gdn_summary_bwd(q, k, g, beta, cu_seqlens, do, *, scale=None, use_qk_l2norm=True, d_final_state=None,
+                    mutation=0):
+    """fp64 state-gradient mirror of the summary (cuDNN Linear Attention page, "Summaries":
+    <op>_summary_bwd is the mirror for the state gradient).  For each span (sequence) and output
+    head: the gradient of L = sum(do * o) + sum(d_final_state * S_end) with respect to the state
+    entering the span, [N, HO, K, V].
+
+    Walking the span backwards with G the gradient with respect to the state after token t:
+    G <- G + scale q_t do_t^T (from o_t = scale S_t^T q_t), then G <- exp(g_t)(I - beta_t k_t k_t^T) G,
+    the transposed Jacobian of S_t = exp(g_t)(I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T
+    (the factor is symmetric).  G after the span's first token is the result; it involves neither
+    v nor any state value.  q, k are L2-normalised first when use_qk_l2norm is set.
+    """
+    q, k, g, beta, do = (_f64(x) for x in (q, k, g, beta, do))
+    cu = _i64(cu_seqlens)
+    T, HK, K = k.shape
+    HO, V = do.shape[1], do.shape[2]
+    N = cu.shape[0] - 1
+    grp = HO // HK
+    if scale is None:
+        scale = 1.0 / np.sqrt(K)
+    if use_qk_l2norm:
+        q = q / np.sqrt((q * q).sum(axis=-1, keepdims=True) + 1e-6)
+        k = k / np.sqrt((k * k).sum(axis=-1, keepdims=True) + 1e-6)
+    out = np.zeros((N, HO, K, V))
+    if d_final_state is not None:
+        out[:] = _f64(d_final_state)
+    for i in range(N):
+        G = out[i].copy()
+        for t in range(int(cu[i + 1]) - 1, int(cu[i]) - 1, -1):
+            qh = np.repeat(q[t], grp, axis=0)  # [HO, K]: head h reads q/k head h // grp
+            kh = np.repeat(k[t], grp, axis=0)
+            out_term = scale * qh[:, :, None] * do[t][:, None, :]
+            if mutation != 18:
+                G = G + out_term
+            kG = np.einsum("hk,hkv->hv", kh, G)
+            G = np.exp(g[t])[:, None, None] * (G - beta[t][:, None, None] * kh[:, :, None] * kG[:, None, :])
+            if mutation == 18:
+                G = G + out_term
+        out[i] = G
+    return out
 
 
 def gdn_summary(k, v, g, beta, cu_seqlens, *, use_qk_l2norm=True, start_state=None,

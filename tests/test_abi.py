@@ -49,7 +49,8 @@ def _c_layout(struct_name, fields):
 @pytest.mark.parametrize("cls,cname", [(B.GdnFwdParams, "la_gdn_fwd_params"),
                                        (B.GdnSummaryParams, "la_gdn_summary_params"),
                                        (B.GdnDecodeParams, "la_gdn_decode_params"),
-                                       (B.GdnBwdParams, "la_gdn_bwd_params")])
+                                       (B.GdnBwdParams, "la_gdn_bwd_params"),
+                                       (B.GdnSummaryBwdParams, "la_gdn_summary_bwd_params")])
 def test_ctypes_mirror_matches_c_layout(cls, cname):
     names = [f[0] for f in cls._fields_]
     size, offs = _c_layout(cname, names)
@@ -204,6 +205,52 @@ def test_null_params():
     assert lib.gdn_summary(None, None) == B.LA_ERR_INVALID_ARG
     assert lib.gdn_decode(None, None) == B.LA_ERR_INVALID_ARG
     assert lib.gdn_bwd(None, None) == B.LA_ERR_INVALID_ARG
+    assert lib.gdn_summary_bwd(None, None) == B.LA_ERR_INVALID_ARG
+
+
+def _summary_bwd(**over):
+    p = B.GdnSummaryBwdParams()
+    T, N, HK, HV, K, V = 256, 2, 2, 4, 128, 128
+    p.q, p.q_stride_t, p.q_stride_h = FAKE, HK * K, K
+    p.k, p.k_stride_t, p.k_stride_h = FAKE, HK * K, K
+    p.g, p.g_stride_t, p.g_stride_h = FAKE, HV, 1
+    p.beta, p.beta_stride_t, p.beta_stride_h = FAKE, HV, 1
+    p.cu_seqlens, p.cu_seqlens_bits = FAKE, 32
+    p.T, p.N, p.HK, p.HV, p.K, p.V = T, N, HK, HV, K, V
+    p.d_o, p.d_o_stride_t, p.d_o_stride_h = FAKE, HV * V, V
+    p.d_state = FAKE
+    for k, v in over.items():
+        setattr(p, k, v)
+    return p
+
+
+SUM_BWD_ERRORS = [
+    ("K not 64/128", dict(K=96), B.LA_ERR_UNSUPPORTED),
+    ("HV not a multiple of HK", dict(HK=3), B.LA_ERR_UNSUPPORTED),
+    ("null d_state", dict(d_state=None), B.LA_ERR_INVALID_ARG),
+    ("misaligned d_state", dict(d_state=FAKE + 2), B.LA_ERR_INVALID_ARG),
+    ("misaligned d_final_state", dict(d_final_state=FAKE + 2), B.LA_ERR_INVALID_ARG),
+    ("null q", dict(q=None), B.LA_ERR_INVALID_ARG),
+    ("q not 16-byte aligned", dict(q=FAKE + 8), B.LA_ERR_INVALID_ARG),
+    ("null d_o", dict(d_o=None), B.LA_ERR_INVALID_ARG),
+    ("negative N", dict(N=-1), B.LA_ERR_INVALID_ARG),
+    ("small workspace", dict(workspace=FAKE, workspace_bytes=16), B.LA_ERR_WORKSPACE),
+]
+
+
+@pytest.mark.parametrize("name,over,code", SUM_BWD_ERRORS, ids=[e[0] for e in SUM_BWD_ERRORS])
+def test_gdn_summary_bwd_rejects(name, over, code):
+    lib = B.load()
+    p = _summary_bwd(**over)
+    assert lib.gdn_summary_bwd(ctypes.byref(p), None) == code
+
+
+def test_summary_bwd_workspace_bytes():
+    lib = B.load()
+    a = lib.la_gdn_summary_bwd_workspace_bytes(8, 32, 128, 128)
+    b = lib.la_gdn_summary_bwd_workspace_bytes(16, 32, 128, 128)
+    assert b > a >= 8 * 32 * 128 * 128 * 4
+    assert lib.la_gdn_summary_bwd_workspace_bytes(-1, 32, 128, 128) == 0
 
 
 def test_checkpoint_rows_host_helper():

@@ -114,10 +114,10 @@ def _bwd_worker(rank, world, port, results):
         tr = torch.from_numpy(summ["transition"][0])
         s_in = cp.entering_state(tr, torch.from_numpy(summ["end_state"][0]),
                                  initial_state=torch.from_numpy(s0[0]) if rank == 0 else None)
-        # local backward (zero final cotangent), then the composed exit cotangent
-        loc = oracle.gdn_bwd(q[sl], k[sl], v[sl], g[sl], beta[sl], cu, do[sl], initial_state=s_in.numpy()[None],
-                             nthreads=1)
-        d_exit = cp.exit_state_grad(tr, torch.from_numpy(loc["d_initial_state"][0]),
+        # the span's own state gradient (the summary's mirror: zero exit cotangent), then the
+        # composed exit cotangent
+        loc = oracle.gdn_summary_bwd(q[sl], k[sl], g[sl], beta[sl], cu, do[sl])
+        d_exit = cp.exit_state_grad(tr, torch.from_numpy(loc[0]),
                                     d_final=torch.from_numpy(dfin[0]) if rank == world - 1 else None)
         full = oracle.gdn_bwd(q[sl], k[sl], v[sl], g[sl], beta[sl], cu, do[sl], initial_state=s_in.numpy()[None],
                               d_final_state=d_exit.numpy()[None], nthreads=1)
@@ -128,9 +128,9 @@ def _bwd_worker(rank, world, port, results):
 
 @pytest.mark.timeout(300)
 def test_two_rank_backward_composition_matches_unsplit():
-    """Context-parallel backward on two gloo ranks: local backwards, one all-gather, the reverse
-    composition of the state gradient, and the span backwards from it reproduce the unsplit
-    backward of the whole sequence."""
+    """Context-parallel backward on two gloo ranks: each span's own state gradient (the summary's
+    mirror), one all-gather, the reverse composition of the state gradient, and the span
+    backwards from it reproduce the unsplit backward of the whole sequence."""
     world = 2
     mgr = mp.Manager()
     results = mgr.dict()

@@ -1,0 +1,160 @@
+"""gdn_summary_bwd (the state-gradient mirror of the span summary) vs the fp64 oracle, through
+the C ABI.
+
+Tolerance (max|x - ref| / max|ref| per tensor): 2e-3, as for the fp32 states.  The loss is
+sum(d_o * o) + sum(d_final_state * end_state) with seeded N(0,1) cotangents; the result is its
+gradient with respect to the state entering each span."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import gated_delta_rule_29_gb300 as la
+from gated_delta_rule_29_gb300 import context_parallel as CP
+from gated_delta_rule_29_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+F32_TOL = 2e-3
+
+
+def dev():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return torch.device("cuda:0")
+
+
+def rel(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    den = np.abs(ref).max()
+    assert den > 0, "reference is all zero: the comparison would be vacuous"
+    return float(np.abs(got - ref).max() / den)
+
+
+def cotangents(w, seed, with_final=True):
+    gen = torch.Generator().manual_seed(seed)
+    do = torch.randn(w.T, w.HV, w.V, generator=gen).to(torch.bfloat16)
+    dfin = torch.randn(w.N, w.HV, w.K, w.V, generator=gen) if with_final else None
+    return do, dfin
+
+
+def run(w, do, dfin, l2=True, scale=None, cu=None):
+    d = dev()
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    cu = w.cu_seqlens if cu is None else cu
+    out = la.gdn_summary_bwd(w.q.to(d), w.k.to(d), w.g.to(d), w.beta.to(d), cu.to(d), do.to(d),
+                             use_qk_l2norm=l2, scale=scale, d_final_state=None if dfin is None else dfin.to(d),
+                             status=status)
+    assert la.read_status(status) == 0
+    return out
+
+
+def check(w, got, ref, label):
+    e = rel(got.cpu().numpy(), ref)
+    print(f"[parity] summary_bwd {w.name}{label}: d_state {e:.2e}")
+    assert e <= F32_TOL
+    return e
+
+
+@pytest.mark.parametrize("K,V", [(64, 64), (128, 128), (64, 128), (128, 64)])
+def test_summary_bwd_ragged_grouped_heads(K, V):
+    """Ragged spans (one token, one chunk +- 1, several chunks, an empty span), grouped heads,
+    a final-state cotangent, slow decay so that every chunk reaches the span start."""
+    w = W.draw("sbwd ragged", [1, 63, 64, 0, 65, 200], 2, 4, K, V, seed=501 + K + V, slow_decay=True)
+    do, dfin = cotangents(w, 502)
+    got = run(w, do, dfin)
+    ref = oracle.gdn_summary_bwd(w.q, w.k, w.g, w.beta, w.cu_seqlens, do, d_final_state=dfin)
+    check(w, got, ref, f" K={K} V={V}")
+    # the empty span passes the exit cotangent through unchanged
+    assert torch.equal(got[3].cpu(), dfin[3].float())
+
+
+def test_summary_bwd_page_distributions_no_final():
+    """The pages' gate and beta distributions (fast decay) and no exit cotangent."""
+    w = W.draw("sbwd page", [300, 129, 1000], 4, 4, 128, 128, seed=511)
+    do, _ = cotangents(w, 512, with_final=False)
+    got = run(w, do, None)
+    ref = oracle.gdn_summary_bwd(w.q, w.k, w.g, w.beta, w.cu_seqlens, do)
+    check(w, got, ref, "")
+
+
+def test_summary_bwd_without_l2norm():
+    """Keys and queries scaled to unit-order norms by hand, the kernel's norm off, explicit scale."""
+    w = W.draw("sbwd no-norm", [150, 70], 1, 2, 64, 64, seed=521, slow_decay=True)
+    w.q = (w.q.float() / 8.0).to(torch.bfloat16)
+    w.k = (w.k.float() / 8.0).to(torch.bfloat16)
+    do, dfin = cotangents(w, 522)
+    got = run(w, do, dfin, l2=False, scale=0.5)
+    ref = oracle.gdn_summary_bwd(w.q, w.k, w.g, w.beta, w.cu_seqlens, do, scale=0.5, use_qk_l2norm=False,
+                                 d_final_state=dfin)
+    check(w, got, ref, "")
+
+
+def test_summary_bwd_equals_backward_state_gradient_bitwise():
+    """The mirror is bitwise the entering-state gradient of the full backward (same recursion)."""
+    w = W.draw("sbwd vs bwd", [130, 64, 257], 2, 2, 128, 128, seed=531, initial_state=True, slow_decay=True)
+    do, dfin = cotangents(w, 532)
+    d = dev()
+    a = run(w, do, dfin)
+    b = la.gdn_bwd(w.q.to(d), w.k.to(d), w.v.to(d), w.g.to(d), w.beta.to(d), w.cu_seqlens.to(d), do.to(d),
+                   initial_state=w.initial_state.to(d), d_final_state=dfin.to(d))[5]
+    assert torch.equal(a, b)
+
+
+def test_summary_bwd_batch_invariant():
+    """A span's state gradient is bitwise the same alone and inside a batch."""
+    w = W.draw("sbwd batch", [90, 200, 33, 128], 2, 2, 64, 64, seed=541, slow_decay=True)
+    do, dfin = cotangents(w, 542)
+    full = run(w, do, dfin)
+    cu = w.cu_seqlens.numpy().astype(np.int64)
+    i = 1
+    sl = slice(cu[i], cu[i + 1])
+    sub = W.Workload(name="one", cu_seqlens=torch.tensor([0, cu[i + 1] - cu[i]]), q=w.q[sl], k=w.k[sl], v=w.v[sl],
+                     g=w.g[sl].contiguous(), beta=w.beta[sl].contiguous())
+    alone = run(sub, do[sl], dfin[i:i + 1])
+    assert torch.equal(full[i], alone[0])
+
+
+def test_summary_bwd_span_composition():
+    """Context-parallel backward on one GPU: per-span state gradients (zero exit cotangent),
+    composed right to left with gdn_summary's transitions, equal the whole sequence's."""
+    L = 2048
+    w = W.draw("sbwd spans", [L], 4, 4, 128, 128, seed=551, slow_decay=True)
+    do, dfin = cotangents(w, 552)
+    spans = torch.tensor([0, 512, 1024, 1536, L], dtype=torch.int32)
+    d = dev()
+    loc = run(w, do, None, cu=spans)
+    _, trs = la.gdn_summary(w.k.to(d), w.v.to(d), w.g.to(d), w.beta.to(d), spans.to(d))
+    full = run(w, do, dfin)
+    composed = CP.compose_grads(list(trs), list(loc), dfin[0].to(d))[-1]
+    e = rel(composed.cpu().numpy(), full[0].cpu().numpy())
+    print(f"[parity] summary_bwd span composition: {e:.2e}")
+    assert e <= F32_TOL
+
+
+def test_summary_bwd_long_spans_sampled():
+    """The long-sequence span workload (131072 tokens, 8 spans of 16384, H = 16, K = V = 128): the
+    oracle recomputes two sampled (span, head) units."""
+    w = W.config(5)
+    do, _ = cotangents(w, 561, with_final=False)
+    got = run(w, do, None, cu=w.spans).cpu().numpy()
+    cu = w.spans.numpy().astype(np.int64)
+    errs = []
+    for i, h in [(0, 0), (7, 11)]:
+        sl = slice(cu[i], cu[i + 1])
+        ref = oracle.gdn_summary_bwd(w.q[sl, h:h + 1], w.k[sl, h:h + 1], w.g[sl, h:h + 1], w.beta[sl, h:h + 1],
+                                     np.array([0, cu[i + 1] - cu[i]]), do[sl, h:h + 1])
+        errs.append(rel(got[i, h], ref[0, 0]))
+    print("[parity] summary_bwd long spans sampled: " + ", ".join(f"{e:.2e}" for e in errs))
+    assert max(errs) <= F32_TOL
+
+
+def test_summary_bwd_bad_cu_seqlens_sets_status():
+    """A decreasing cu_seqlens is a value error: the status word says so and nothing is computed."""
+    d = dev()
+    w = W.draw("sbwd bad", [64, 64], 1, 1, 64, 64, seed=571)
+    do, _ = cotangents(w, 572, with_final=False)
+    bad = torch.tensor([0, 100, 64], dtype=torch.int32, device=d)
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    la.gdn_summary_bwd(w.q.to(d), w.k.to(d), w.g.to(d), w.beta.to(d), bad, do.to(d), status=status)
+    assert la.read_status(status) != 0

@@ -473,6 +473,81 @@ def check_gdp_dense_products(mutation=0):
     return worst
 
 
+def check_summary_bwd(mutation=0):
+    """The summary's state-gradient mirror against (1) the entering-state gradient of the
+    (finite-difference pinned) backward, with and without a final-state cotangent, grouped heads,
+    the L2 norm on and off and an empty sequence; (2) the closed form with beta = 0,
+    G = exp(b_L) dS_exit + sum_t exp(b_t) scale q_t do_t^T (b_t the cumulative gate from the span
+    start); (3) span composition: the whole sequence's gradient equals the per-span gradients
+    composed right to left with the summary's transitions, d_enter = transition d_exit + (the
+    span's own value)."""
+    worst = 0.0
+    rng = np.random.default_rng(121)
+    cu = np.array([0, 5, 5, 12])
+    T, HK, HV, K, V = 12, 1, 2, 3, 4
+    q = rng.standard_normal((T, HK, K))
+    k = rng.standard_normal((T, HK, K))
+    v = rng.standard_normal((T, HV, V))
+    g = -0.4 * rng.random((T, HV))
+    beta = rng.random((T, HV))
+    do = rng.standard_normal((T, HV, V))
+    S0 = rng.standard_normal((3, HV, K, V))
+    dfin = rng.standard_normal((3, HV, K, V))
+    for l2 in (True, False):
+        for df in (None, dfin):
+            ref = oracle.gdn_bwd(q, k, v, g, beta, cu, do, scale=0.7, use_qk_l2norm=l2, initial_state=S0,
+                                 d_final_state=df, nthreads=1)["d_initial_state"]
+            got = oracle.gdn_summary_bwd(q, k, g, beta, cu, do, scale=0.7, use_qk_l2norm=l2, d_final_state=df,
+                                         mutation=mutation)
+            worst = max(worst, _rel(got, ref))
+    # (2) beta = 0 closed form (no L2 norm)
+    b0 = np.zeros_like(beta)
+    got = oracle.gdn_summary_bwd(q, k, g, b0, cu, do, scale=0.7, use_qk_l2norm=False, d_final_state=dfin,
+                                 mutation=mutation)
+    for i in range(3):
+        for h in range(HV):
+            s_, e_ = cu[i], cu[i + 1]
+            G = np.exp(g[s_:e_, h].sum()) * dfin[i, h]
+            for t in range(s_, e_):
+                G = G + np.exp(g[s_:t + 1, h].sum()) * 0.7 * np.outer(q[t, h // (HV // HK)], do[t, h])
+            worst = max(worst, _rel(got[i, h], G))
+    # (3) span composition of the state gradient
+    L = 11
+    whole = np.array([0, L])
+    spans = np.array([0, 4, 7, L])
+    qs, ks, gs, bs, ds = q[:L], k[:L], g[:L], beta[:L], do[:L]
+    dF = dfin[:1]
+    full = oracle.gdn_summary_bwd(qs, ks, gs, bs, whole, ds, scale=0.7, d_final_state=dF, mutation=mutation)
+    loc = oracle.gdn_summary_bwd(qs, ks, gs, bs, spans, ds, scale=0.7, mutation=mutation)
+    trs = oracle.gdn_summary(ks, v[:L], gs, bs, spans)["transition"]
+    d = dF[0]
+    for r in range(2, -1, -1):
+        d = loc[r] + np.einsum("hab,hbv->hav", trs[r], d)
+    return max(worst, _rel(d, full[0]))
+
+
+def check_summary_bwd_finite_differences(mutation=0):
+    """The summary's state-gradient mirror against central differences of the (pinned) forward's
+    loss sum(do * o) + sum(dS_T * S_final) in the start state."""
+    x, cu, do, dfin, l2 = _fd_case(True, 131)
+    got = oracle.gdn_summary_bwd(x["q"], x["k"], x["g"], x["beta"], cu, do, scale=0.8, use_qk_l2norm=l2,
+                                 d_final_state=dfin, mutation=mutation)
+
+    def loss(S0):
+        r = oracle.gdn_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], cu, scale=0.8, use_qk_l2norm=l2,
+                           initial_state=S0, nthreads=1)
+        return float((r["o"] * do).sum() + (r["final_state"] * dfin).sum())
+
+    eps = 1e-6
+    fd = np.zeros_like(x["S0"])
+    for idx in np.ndindex(x["S0"].shape):
+        sp, sm = x["S0"].copy(), x["S0"].copy()
+        sp[idx] += eps
+        sm[idx] -= eps
+        fd[idx] = (loss(sp) - loss(sm)) / (2 * eps)
+    return _rel(got, fd)
+
+
 CHECKS = {
     "golden": (check_golden, 1e-12),
     "brute_force": (check_brute_force, 1e-12),
@@ -492,6 +567,8 @@ CHECKS = {
     "state_pool": (check_state_pool, 1e-13),
     "backward_finite_differences": (check_backward_finite_differences, 1e-6),
     "gdp_dense_products": (check_gdp_dense_products, 1e-12),
+    "summary_bwd": (check_summary_bwd, 1e-12),
+    "summary_bwd_finite_differences": (check_summary_bwd_finite_differences, 1e-6),
 }
 
 
