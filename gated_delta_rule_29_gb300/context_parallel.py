@@ -10,7 +10,7 @@ composes the state entering its span,
 then runs gdn_fwd on its span from that state (cuDNN Linear Attention page,
 "Summaries": the summaries compose across spans to give context parallelism).
 The backward mirrors it: each rank's state gradient from its own outputs
-(gdn_summary_bwd, the summary's mirror for the state gradient), one all-gather, and
+(gdn_summary_bwd, the summary's counterpart on the gradient side), one all-gather, and
 the reverse composition dS_enter = transition dS_exit + dS_H give every rank the
 cotangent of its span's end state for gdn_bwd.
 The composition is a handful of small fp32 products per rank and runs on

@@ -308,8 +308,8 @@ def gdn_bwd(q, k, v, g, beta, cu_seqlens, do, *, scale=None, use_qk_l2norm=True,
 
 def gdn_summary_bwd(q, k, g, beta, cu_seqlens, do, *, scale=None, use_qk_l2norm=True, d_final_state=None,
                     mutation=0):
-    """fp64 state-gradient mirror of the summary (cuDNN Linear Attention page, "Summaries":
-    <op>_summary_bwd is the mirror for the state gradient).  For each span (sequence) and output
+    """fp64 state-gradient counterpart of the summary (cuDNN Linear Attention page, "Summaries":
+    each summary op has a backward partner acting on the state gradient).  For each span (sequence) and output
     head: the gradient of L = sum(do * o) + sum(d_final_state * S_end) with respect to the state
     entering the span, [N, HO, K, V].
 
