@@ -103,6 +103,15 @@ __device__ __forceinline__ void split_tf32(float x, uint32_t& hd, uint32_t& rs) 
     hd = __float_as_uint(x) & 0xFFFFE000u;
     rs = __float_as_uint(x - __uint_as_float(hd));
 }
+// A fragment (16 x 8, rows m0.., columns k0..) of an element function, rounded to tf32 (for the
+// products that only feed the bf16 gradients dq and dk: one MMA, ~2^-11 relative per operand).
+template <class F>
+__device__ __forceinline__ void frag_a_round(F f, int m0, int k0, int g, int t, uint32_t (&a)[4]) {
+    a[0] = to_tf32(f(m0 + g, k0 + t));
+    a[1] = to_tf32(f(m0 + g + 8, k0 + t));
+    a[2] = to_tf32(f(m0 + g, k0 + t + 4));
+    a[3] = to_tf32(f(m0 + g + 8, k0 + t + 4));
+}
 // A fragment (16 x 8, rows m0.., columns k0..) of an element function, split in two.
 template <class F>
 __device__ __forceinline__ void frag_a_split(F f, int m0, int k0, int g, int t, uint32_t (&hd)[4], uint32_t (&rs)[4]) {
@@ -117,7 +126,7 @@ __device__ __forceinline__ void frag_b_split(F f, int k0, int n0, int g, int t, 
     split_tf32(f(k0 + t, n0 + g), hd[0], rs[0]);
     split_tf32(f(k0 + t + 4, n0 + g), hd[1], rs[1]);
 }
-// c += A B with both operands split (three products), or with one exact operand (two).
+// c += A B with both operands split (three products), or with an exact A operand (two).
 __device__ __forceinline__ void mma3(float (&c)[4], const uint32_t (&ah)[4], const uint32_t (&ar)[4],
                                      const uint32_t (&bh)[2], const uint32_t (&br)[2]) {
     mma_tf32_16x8x8(c, ar, bh);
@@ -128,11 +137,6 @@ __device__ __forceinline__ void mma2a(float (&c)[4], const uint32_t (&a)[4], con
                                       const uint32_t (&br)[2]) {
     mma_tf32_16x8x8(c, a, br);
     mma_tf32_16x8x8(c, a, bh);
-}
-__device__ __forceinline__ void mma2b(float (&c)[4], const uint32_t (&ah)[4], const uint32_t (&ar)[4],
-                                      const uint32_t (&b)[2]) {
-    mma_tf32_16x8x8(c, ar, b);
-    mma_tf32_16x8x8(c, ah, b);
 }
 __device__ __forceinline__ uint32_t fbits(float x) { return __float_as_uint(x); }
 // The same three products with the head x head term in c and the two rest terms in r
@@ -545,24 +549,22 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
                 if (lane == 0) s.red[w] = p;
             }
             if (kwarp && !so) {
-                // dK_hat += dx S_J^T + Gamma_C D dS_J^T,  dx = -beta gamma dY
+                // dK_hat += dx S_J^T + Gamma_C D dS_J^T,  dx = -beta gamma dY (rounded tf32 operands:
+                // these sums only reach the bf16 dk)
 #pragma unroll
                 for (int kt = 0; kt < 2; ++kt) {
                     const int k0 = 8 * kt;
-                    uint32_t xh[4], xr[4], dh[4], dr[4];
-                    frag_a_split([&](int i, int cc) { return -s.beta[i] * s.gam[i] * s.dY[cc * PC + i]; }, om0, k0, g, t,
-                                 xh, xr);
-                    frag_a_split([&](int i, int cc) { return s.GC[i] * s.D[cc * PC + i]; }, om0, k0, g, t, dh, dr);
+                    uint32_t xa[4], da[4];
+                    frag_a_round([&](int i, int cc) { return -s.beta[i] * s.gam[i] * s.dY[cc * PC + i]; }, om0, k0, g, t,
+                                 xa);
+                    frag_a_round([&](int i, int cc) { return s.GC[i] * s.D[cc * PC + i]; }, om0, k0, g, t, da);
 #pragma unroll
                     for (int nd = 0; nd < NT; ++nd) {
                         const int dp = colp<KD>(8 * nd) + g;
-                        uint32_t sh[2], sr[2], th[2], tr[2];
-                        split_tf32(SJ[(k0 + t) * PK + dp], sh[0], sr[0]);
-                        split_tf32(SJ[(k0 + t + 4) * PK + dp], sh[1], sr[1]);
-                        split_tf32(dSJ[(k0 + t) * PK + dp], th[0], tr[0]);
-                        split_tf32(dSJ[(k0 + t + 4) * PK + dp], th[1], tr[1]);
-                        mma3(acc[nd], xh, xr, sh, sr);
-                        mma3(acc[nd], dh, dr, th, tr);
+                        const uint32_t sb[2] = {to_tf32(SJ[(k0 + t) * PK + dp]), to_tf32(SJ[(k0 + t + 4) * PK + dp])};
+                        const uint32_t tb[2] = {to_tf32(dSJ[(k0 + t) * PK + dp]), to_tf32(dSJ[(k0 + t + 4) * PK + dp])};
+                        mma_tf32_16x8x8(acc[nd], xa, sb);
+                        mma_tf32_16x8x8(acc[nd], da, tb);
                     }
                 }
                 // dA -= dY D^T (strict), dP += scale dO D^T (incl.) on the lower 16 x 8 tiles
@@ -618,10 +620,8 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
 #pragma unroll
                     for (int nd = 0; nd < NT; ++nd) {
                         const int dp = colp<KD>(8 * nd) + g;
-                        uint32_t sh[2], sr[2];
-                        split_tf32(SJ[(k0 + t) * PK + dp], sh[0], sr[0]);
-                        split_tf32(SJ[(k0 + t + 4) * PK + dp], sh[1], sr[1]);
-                        mma2a(acc[nd], ao, sh, sr);
+                        const uint32_t sb[2] = {to_tf32(SJ[(k0 + t) * PK + dp]), to_tf32(SJ[(k0 + t + 4) * PK + dp])};
+                        mma_tf32_16x8x8(acc[nd], ao, sb);
                     }
                 }
                 // dS_J <- gamma_last dS_J + K^T (cx (.) dY) + Q^T (co (.) dO): key rows
@@ -746,26 +746,26 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
 #pragma unroll 1
             for (int kt = 0; kt < 8; ++kt) {
                 const int k0 = 8 * kt;
-                uint32_t mh[4], mr[4];
-                frag_a_split([&](int i, int j) { return (j <= i ? s.dA[i * PC + j] : s.dA[j * PC + i]) * s.rk[j]; }, om0, k0,
-                             g, t, mh, mr);
+                uint32_t ma[4];
+                frag_a_round([&](int i, int j) { return (j <= i ? s.dA[i * PC + j] : s.dA[j * PC + i]) * s.rk[j]; }, om0, k0,
+                             g, t, ma);
 #pragma unroll
                 for (int nd = 0; nd < NT; ++nd) {
                     const int dp = colp<KD>(8 * nd) + g;
                     const uint32_t b[2] = {fbits(s.Kr[(k0 + t) * PK + dp]), fbits(s.Kr[(k0 + t + 4) * PK + dp])};
-                    mma2b(acc[nd], mh, mr, b);
+                    mma_tf32_16x8x8(acc[nd], ma, b);
                 }
             }
 #pragma unroll 1
             for (int kt = 2 * mt; kt < 8; ++kt) {
                 const int k0 = 8 * kt;
-                uint32_t hh[4], hr[4];
-                frag_a_split([&](int i, int j) { return s.dP[j * PC + i] * s.rq[j]; }, om0, k0, g, t, hh, hr);
+                uint32_t ha[4];
+                frag_a_round([&](int i, int j) { return s.dP[j * PC + i] * s.rq[j]; }, om0, k0, g, t, ha);
 #pragma unroll
                 for (int nd = 0; nd < NT; ++nd) {
                     const int dp = colp<KD>(8 * nd) + g;
                     const uint32_t b[2] = {fbits(s.Qr[(k0 + t) * PK + dp]), fbits(s.Qr[(k0 + t + 4) * PK + dp])};
-                    mma2b(acc[nd], hh, hr, b);
+                    mma_tf32_16x8x8(acc[nd], ha, b);
                 }
             }
         } else {
@@ -774,13 +774,13 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
 #pragma unroll 1
             for (int kt = 0; kt <= 2 * mt + 1; ++kt) {
                 const int k0 = 8 * kt;
-                uint32_t hh[4], hr[4];
-                frag_a_split([&](int i, int j) { return s.dP[i * PC + j] * s.rk[j]; }, om0, k0, g, t, hh, hr);
+                uint32_t ha[4];
+                frag_a_round([&](int i, int j) { return s.dP[i * PC + j] * s.rk[j]; }, om0, k0, g, t, ha);
 #pragma unroll
                 for (int nd = 0; nd < NT; ++nd) {
                     const int dp = colp<KD>(8 * nd) + g;
                     const uint32_t b[2] = {fbits(s.Kr[(k0 + t) * PK + dp]), fbits(s.Kr[(k0 + t + 4) * PK + dp])};
-                    mma2b(acc[nd], hh, hr, b);
+                    mma_tf32_16x8x8(acc[nd], ha, b);
                 }
             }
         }
