@@ -522,8 +522,13 @@ def run_bwd_bench(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     lib = B.load()
-    w = W.config(3)
+    if args.seq_len == 8192:
+        w = W.config(3)
+    else:  # a smaller dense batch of the same shape family (profiling captures)
+        w = W.draw(f"dense batch N=8 x {args.seq_len}", [args.seq_len] * 8, 32, 32, 128, 128, seed=1003,
+                   initial_state=True)
     T, N, HK, HV, K, V = w.T, w.N, w.HK, w.HV, w.K, w.V
+    L = args.seq_len
     gen = torch.Generator().manual_seed(1009)
     do_h = torch.randn(T, HV, V, generator=gen).to(torch.bfloat16)
     dfin_h = torch.randn(N, HV, K, V, generator=gen)
@@ -583,16 +588,20 @@ def run_bwd_bench(args, world, rank, local):
         for hbuf, dbuf in zip(host_out, r):
             hbuf.copy_(dbuf, non_blocking=True)
 
-    e2e_step()
-    torch.cuda.synchronize()
-    x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2e_steps = max(3, min(args.steps, 5))
-    x0.record(stream)
-    for _ in range(e2e_steps):
+    e2e = None
+    if not args.no_e2e:
         e2e_step()
-    x1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(x0.elapsed_time(x1) / e2e_steps, world)
+        torch.cuda.synchronize()
+        x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e2e_steps = max(3, min(args.steps, 5))
+        x0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        x1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(x0.elapsed_time(x1) / e2e_steps, world)
+        e2e = {"value": T * world / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -606,16 +615,16 @@ def run_bwd_bench(args, world, rank, local):
         oracle.gdn_bwd(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, do_h, initial_state=w.initial_state,
                        d_final_state=dfin_h, unit_mask=mask, nthreads=cores)
         dt = time.perf_counter() - t0
-        cpu = {"value": len(units) * 8192 / HV / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-               "sample": f"{len(units)} of {N * HV} (sequence, head) units x 8192 tokens ({dt:.1f} s), fp64 reverse "
+        cpu = {"value": len(units) * L / HV / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{len(units)} of {N * HV} (sequence, head) units x {L} tokens ({dt:.1f} s), fp64 reverse "
                          f"mode of the token recurrence, up to {cores} threads (one per unit)"}
     if rank == 0:
         line = {
             "metric": BWD_METRIC, "value": T * world / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD + "; bwd with the forward's fp32 checkpoints every 64 tokens",
-                       "global_batch": N * world, "seq_len": 8192,
+            "config": {"workload": (WORKLOAD if L == 8192 else w.name) + "; bwd with the forward's fp32 checkpoints "
+                                   "every 64 tokens", "global_batch": N * world, "seq_len": L,
                        "parallelism": "single GPU" if world == 1 else f"independent batches per GPU x{world}",
                        "l2": "inputs larger than L2 (1.6 GB of q/k/v + 2.1 GB of checkpoints per step); no flush"},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": tf32_peak, "unit": "TFLOP/s",
@@ -624,8 +633,7 @@ def run_bwd_bench(args, world, rank, local):
                                         "each fp32 product is 2-3 tf32 MMAs (head and remainder splits)",
                          "kernel": "gdn_bwd_kernel<128, 128>", "kernel_ms": kern_ms, "algorithmic_flops": flops},
             "cpu_baseline": cpu,
-            "e2e": {"value": T * world / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+            "e2e": e2e,
             "gpu_launches": args.steps * 2,
             "clocks": clk.summary(),
         }
