@@ -61,11 +61,14 @@ __device__ __forceinline__ int colp(int d) { return d + (d / (KD / 4)) * 4; }
 template <int KD>
 struct BwdSmem {
     static constexpr int PK = KD + 12;  // row stride of K / Q / S^T / dS^T
-    static constexpr int PC = kC + 4;   // row stride of the 64 x 64 matrices and of the tiles
+    static constexpr int PC = kC + 4;   // row stride of the 64 x 64 matrices and of the tiles read
+                                        // along the token index (4 mod 32 words)
+    static constexpr int PT = kC + 8;   // row stride of the tiles read along the value column
+                                        // (8 mod 32 words): both fragment patterns conflict free
     float Kr[kC * PK];      // raw keys (rows past the end are zero); k_hat = rk k
     float Qr[kC * PK];      // raw queries; q_hat = rq q
     float Tm[kC * PC];      // T = (I + A)^{-1}
-    float Pm[kC * PC];      // P (lower incl.)
+    float Pt[kC * PC];      // P transposed: Pt[j][i] = P_ij (P lower incl.)
     // strictly lower part: dA accumulated over the tiles, then M; strictly upper part: the
     // transpose of Gk_ij = (k_hat_i . k_hat_j) Gamma_ij (j < i) stored at [j][i]; diagonal zero
     float dA[kC * PC];
@@ -74,9 +77,14 @@ struct BwdSmem {
     // S and dS are double buffered so that the next tile streams in while this one is computed
     float SJ[2][kVT * PK];  // S[:, tile]^T
     float dSJ[2][kVT * PK]; // dS_next[:, tile]^T
-    float X[kVT * PC], Y[kVT * PC], D[kVT * PC], dD[kVT * PC], dY[kVT * PC];
-    float VJ[kVT * PC], OJ[kVT * PC], QS[kVT * PC], KdS[kVT * PC];
+    // per tile, [cc][i]: Y, dD, dY, dO with stride PC (MMA operands along the tokens), D and
+    // copies of dY and dO with stride PT (MMA operands along the value columns)
+    float Y[kVT * PC], dD[kVT * PC], dY[kVT * PC], OJ[kVT * PC];
+    float D[kVT * PT], dYc[kVT * PT], OJc[kVT * PT];
     uint16_t Vb[kC * kVT], Ob[kC * kVT];  // the next tile's raw V and dO rows (bf16, token-major)
+    // per-row partial sums over each 8-column half of the tile, formed in the MMA epilogues:
+    // [0] sum dY (V - gamma x), [1] sum dY x, [2] sum dO (Q S), [3] sum (K dS) D
+    float part[4][2][kC];
     float beta[kC], b[kC], gam[kC], GC[kC], rk[kC], rq[kC];
     float cx[kC], co[kC];   // -rk beta gamma (K^T dx) and scale rq gamma (Q^T dO) row factors
     float dbeta[kC], db[kC], wv[kC];
@@ -148,6 +156,12 @@ __device__ __forceinline__ void mma3s(float (&c)[4], float (&r)[4], const uint32
     mma_tf32_16x8x8(c, ah, bh);
 }
 
+// Sum over the four lanes of a quad (the accumulator fragment's column pairs of one row).
+__device__ __forceinline__ float quad_sum(float x) {
+    x += __shfl_xor_sync(0xffffffffu, x, 1);
+    return x + __shfl_xor_sync(0xffffffffu, x, 2);
+}
+
 // The 20 lower (16-row, 8-column) output tiles of a 64 x 64 lower-triangular product, in order.
 __device__ __forceinline__ void lower_tile(int p, int& mt, int& nt) {
     mt = p < 2 ? 0 : (p < 6 ? 1 : (p < 12 ? 2 : 3));
@@ -160,6 +174,7 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
     BwdSmem<KD>& s = *reinterpret_cast<BwdSmem<KD>*>(smem_raw);
     constexpr int PK = BwdSmem<KD>::PK;
     constexpr int PC = BwdSmem<KD>::PC;
+    constexpr int PT = BwdSmem<KD>::PT;
     constexpr int NT = KD / 8;    // 8-column key tiles of the dK / dQ rows
     constexpr int MTW = KD / 64;  // 16-row key tiles of dS per warp in the dS update
     const int tid = threadIdx.x;
@@ -333,7 +348,7 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
                 const int i = m0 + g + 8 * (e >> 1), j = n0 + 2 * t + (e & 1);
                 const float G = j <= i ? expf(s.b[i] - s.b[j]) : 0.f;
                 if (isP) {
-                    s.Pm[i * PC + j] = s.rq[i] * s.rk[j] * cf[e] * G;
+                    s.Pt[j * PC + i] = s.rq[i] * s.rk[j] * cf[e] * G;
                     s.dP[i * PC + j] = 0.f;
                 } else {
                     if (j <= i) s.dA[i * PC + j] = 0.f;                             // dA accumulator, diagonal
@@ -423,6 +438,9 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
             const float* SJ = s.SJ[pb];
             const float* dSJ = s.dSJ[pb];
             const int mt = w & 3, m0 = 16 * mt, n0 = 8 * (w >> 2);  // this warp's 16 x 8 tile
+            const int nh = w >> 2;                                 // its 8-column half
+            // values of this thread's four (row, column) elements kept from one phase to the next
+            float kds[4], xs[4], zs[4];
             if (so) {
                 // K dS_J alone (rows scaled by rk afterwards); dO into its tile
                 float cd4[4] = {0.f, 0.f, 0.f, 0.f}, rd4[4] = {0.f, 0.f, 0.f, 0.f};
@@ -440,8 +458,10 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int i = m0 + g + 8 * (e >> 1), cc = n0 + 2 * t + (e & 1);
-                    s.KdS[cc * PC + i] = s.rk[i] * (cd4[e] + rd4[e]);
-                    s.OJ[cc * PC + i] = b2f(s.Ob[i * kVT + cc]);
+                    kds[e] = s.rk[i] * (cd4[e] + rd4[e]);
+                    const float ov = b2f(s.Ob[i * kVT + cc]);
+                    s.OJ[cc * PC + i] = ov;
+                    s.OJc[cc * PT + i] = ov;
                 }
             } else {
                 // x = K S_J, Q S_J, K dS_J (rows scaled by rk / rq afterwards); V, dO into the tiles
@@ -473,17 +493,25 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
                     cq4[e] += rq4[e];
                     cd4[e] += rd4[e];
                 }
+                float sop[2] = {0.f, 0.f};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int i = m0 + g + 8 * (e >> 1), cc = n0 + 2 * t + (e & 1);
                     const float x = s.rk[i] * cx4[e];
                     const float vv = b2f(s.Vb[i * kVT + cc]);
-                    s.X[cc * PC + i] = x;
-                    s.VJ[cc * PC + i] = vv;
-                    s.Y[cc * PC + i] = s.beta[i] * (vv - s.gam[i] * x);
-                    s.QS[cc * PC + i] = s.rq[i] * cq4[e];
-                    s.KdS[cc * PC + i] = s.rk[i] * cd4[e];
-                    s.OJ[cc * PC + i] = b2f(s.Ob[i * kVT + cc]);
+                    const float ov = b2f(s.Ob[i * kVT + cc]);
+                    xs[e] = x;
+                    zs[e] = vv - s.gam[i] * x;
+                    kds[e] = s.rk[i] * cd4[e];
+                    s.Y[cc * PC + i] = s.beta[i] * zs[e];
+                    s.OJ[cc * PC + i] = ov;
+                    s.OJc[cc * PT + i] = ov;
+                    sop[e >> 1] = fmaf(ov, s.rq[i] * cq4[e], sop[e >> 1]);
+                }
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const float v_ = quad_sum(sop[hh]);
+                    if (t == 0) s.part[2][nh][m0 + g + 8 * hh] = v_;
                 }
             }
             __syncthreads();
@@ -505,16 +533,26 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
                 for (int kt = 2 * mt; kt < 8; ++kt) {
                     const int k0 = 8 * kt;
                     uint32_t ah[4], ar[4];
-                    frag_a_split([&](int i, int m) { return s.Pm[m * PC + i]; }, m0, k0, g, t, ah, ar);
+                    frag_a_split([&](int i, int m) { return s.Pt[i * PC + m]; }, m0, k0, g, t, ah, ar);
                     const uint32_t b[2] = {fbits(s.OJ[(n0 + g) * PC + k0 + t]), fbits(s.OJ[(n0 + g) * PC + k0 + t + 4])};
                     mma_tf32_16x8x8(rE, ar, b);
                     mma_tf32_16x8x8(cE, ah, b);
                 }
+                float wp[2] = {0.f, 0.f};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int i = m0 + g + 8 * (e >> 1), cc = n0 + 2 * t + (e & 1);
-                    s.D[cc * PC + i] = cD[e] + rD[e];
-                    s.dD[cc * PC + i] = a.scale * (cE[e] + rE[e]) + s.GC[i] * s.KdS[cc * PC + i];
+                    const float dv_ = cD[e] + rD[e];
+                    s.D[cc * PT + i] = dv_;
+                    s.dD[cc * PC + i] = a.scale * (cE[e] + rE[e]) + s.GC[i] * kds[e];
+                    wp[e >> 1] = fmaf(kds[e], dv_, wp[e >> 1]);
+                }
+                if (!so) {
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const float v_ = quad_sum(wp[hh]);
+                        if (t == 0) s.part[3][nh][m0 + g + 8 * hh] = v_;
+                    }
                 }
             }
             __syncthreads();
@@ -528,12 +566,28 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
                     frag_b_split([&](int m, int cc) { return s.dD[cc * PC + m]; }, k0, n0, g, t, bh, br);
                     mma3s(cY, rY, ah, ar, bh, br);
                 }
+                float sbp[2] = {0.f, 0.f}, sgp[2] = {0.f, 0.f};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int i = m0 + g + 8 * (e >> 1), cc = n0 + 2 * t + (e & 1);
                     const float dy = cY[e] + rY[e];
                     s.dY[cc * PC + i] = dy;
-                    if (i < n && !so) a.dv[(t0 + i) * a.dv_st + h * a.dv_sh + j0 + cc] = f2b(s.beta[i] * dy);
+                    s.dYc[cc * PT + i] = dy;
+                    if (!so) {
+                        if (i < n) a.dv[(t0 + i) * a.dv_st + h * a.dv_sh + j0 + cc] = f2b(s.beta[i] * dy);
+                        sbp[e >> 1] = fmaf(dy, zs[e], sbp[e >> 1]);
+                        sgp[e >> 1] = fmaf(dy, xs[e], sgp[e >> 1]);
+                    }
+                }
+                if (!so) {
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const float b_ = quad_sum(sbp[hh]), g_ = quad_sum(sgp[hh]);
+                        if (t == 0) {
+                            s.part[0][nh][m0 + g + 8 * hh] = b_;
+                            s.part[1][nh][m0 + g + 8 * hh] = g_;
+                        }
+                    }
                 }
             }
             __syncthreads();
@@ -555,9 +609,9 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
                 for (int kt = 0; kt < 2; ++kt) {
                     const int k0 = 8 * kt;
                     uint32_t xa[4], da[4];
-                    frag_a_round([&](int i, int cc) { return -s.beta[i] * s.gam[i] * s.dY[cc * PC + i]; }, om0, k0, g, t,
-                                 xa);
-                    frag_a_round([&](int i, int cc) { return s.GC[i] * s.D[cc * PC + i]; }, om0, k0, g, t, da);
+                    frag_a_round([&](int i, int cc) { return -s.beta[i] * s.gam[i] * s.dYc[cc * PT + i]; }, om0, k0, g,
+                                 t, xa);
+                    frag_a_round([&](int i, int cc) { return s.GC[i] * s.D[cc * PT + i]; }, om0, k0, g, t, da);
 #pragma unroll
                     for (int nd = 0; nd < NT; ++nd) {
                         const int dp = colp<KD>(8 * nd) + g;
@@ -577,11 +631,11 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
                     for (int kt = 0; kt < 2; ++kt) {
                         const int k0 = 8 * kt;
                         uint32_t yh[4], yr[4], bh[2], br[2];
-                        frag_a_split([&](int i, int cc) { return s.dY[cc * PC + i]; }, p0, k0, g, t, yh, yr);
-                        frag_b_split([&](int cc, int j) { return s.D[cc * PC + j]; }, k0, q0, g, t, bh, br);
-                        const uint32_t ao[4] = {fbits(s.OJ[(k0 + t) * PC + p0 + g]), fbits(s.OJ[(k0 + t) * PC + p0 + g + 8]),
-                                                fbits(s.OJ[(k0 + t + 4) * PC + p0 + g]),
-                                                fbits(s.OJ[(k0 + t + 4) * PC + p0 + g + 8])};
+                        frag_a_split([&](int i, int cc) { return s.dYc[cc * PT + i]; }, p0, k0, g, t, yh, yr);
+                        frag_b_split([&](int cc, int j) { return s.D[cc * PT + j]; }, k0, q0, g, t, bh, br);
+                        const uint32_t ao[4] = {fbits(s.OJc[(k0 + t) * PT + p0 + g]), fbits(s.OJc[(k0 + t) * PT + p0 + g + 8]),
+                                                fbits(s.OJc[(k0 + t + 4) * PT + p0 + g]),
+                                                fbits(s.OJc[(k0 + t + 4) * PT + p0 + g + 8])};
                         mma3(ca, yh, yr, bh, br);
                         mma2a(cp, ao, bh, br);
                     }
@@ -597,26 +651,19 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
                     // per-row sums: dbeta (Y's beta), db (Y's gamma, O's gamma); the Gamma_Cj terms
                     // of S_next, w_j = Gamma_Cj sum_v (K dS_J)_jv D_jv, move from b_j to b_last
                     const int i = tid - 128;
-                    float sb = 0.f, sg = 0.f, so = 0.f, wj = 0.f;
-#pragma unroll
-                    for (int cc = 0; cc < kVT; ++cc) {
-                        const float dy = s.dY[cc * PC + i], xv = s.X[cc * PC + i];
-                        sb = fmaf(dy, s.VJ[cc * PC + i] - s.gam[i] * xv, sb);
-                        sg = fmaf(dy, xv, sg);
-                        so = fmaf(s.OJ[cc * PC + i], s.QS[cc * PC + i], so);
-                        wj = fmaf(s.KdS[cc * PC + i], s.D[cc * PC + i], wj);
-                    }
+                    const float sb = s.part[0][0][i] + s.part[0][1][i], sg = s.part[1][0][i] + s.part[1][1][i];
+                    const float so_ = s.part[2][0][i] + s.part[2][1][i], wj = s.part[3][0][i] + s.part[3][1][i];
                     s.dbeta[i] += sb;
-                    s.db[i] += s.gam[i] * (a.scale * so - s.beta[i] * sg) - wj * s.GC[i];
+                    s.db[i] += s.gam[i] * (a.scale * so_ - s.beta[i] * sg) - wj * s.GC[i];
                     s.wv[i] = wj * s.GC[i];
                 }
                 // dQ_hat sum += dO S_J^T (the row factor scale gamma_i is applied after the tiles)
 #pragma unroll
                 for (int kt = 0; kt < (so ? 0 : 2); ++kt) {
                     const int k0 = 8 * kt;
-                    const uint32_t ao[4] = {fbits(s.OJ[(k0 + t) * PC + om0 + g]), fbits(s.OJ[(k0 + t) * PC + om0 + g + 8]),
-                                            fbits(s.OJ[(k0 + t + 4) * PC + om0 + g]),
-                                            fbits(s.OJ[(k0 + t + 4) * PC + om0 + g + 8])};
+                    const uint32_t ao[4] = {fbits(s.OJc[(k0 + t) * PT + om0 + g]), fbits(s.OJc[(k0 + t) * PT + om0 + g + 8]),
+                                            fbits(s.OJc[(k0 + t + 4) * PT + om0 + g]),
+                                            fbits(s.OJc[(k0 + t + 4) * PT + om0 + g + 8])};
 #pragma unroll
                     for (int nd = 0; nd < NT; ++nd) {
                         const int dp = colp<KD>(8 * nd) + g;
@@ -704,9 +751,9 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
                     sb += x;
                     rowsum = fmaf(x, s.beta[i], rowsum);
                 }
-                if (j <= i) rowsum = fmaf(s.dP[i * PC + j], s.Pm[i * PC + j], rowsum);
+                if (j <= i) rowsum = fmaf(s.dP[i * PC + j], s.Pt[j * PC + i], rowsum);
                 if (j > i) colsum = fmaf(s.dA[j * PC + i] * s.beta[j], s.dA[i * PC + j], colsum);  // Gk_ji at [i][j]
-                if (j >= i) colsum = fmaf(s.dP[j * PC + i], s.Pm[j * PC + i], colsum);
+                if (j >= i) colsum = fmaf(s.dP[j * PC + i], s.Pt[i * PC + j], colsum);
             }
 #pragma unroll
             for (int off = 1; off < 4; off <<= 1) {
