@@ -232,15 +232,19 @@ def gdn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
             use_qk_l2norm: bool = True, initial_state: Optional[torch.Tensor] = None,
             d_final_state: Optional[torch.Tensor] = None, checkpoints: Optional[torch.Tensor] = None,
             workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
-            stream: Optional[torch.cuda.Stream] = None):
+            stream: Optional[torch.cuda.Stream] = None, a_log: Optional[torch.Tensor] = None,
+            dt_bias: Optional[torch.Tensor] = None, gate_lower_bound: Optional[float] = None,
+            beta_sigmoid: bool = False):
     """Backward of gdn_fwd: returns (dq, dk, dv, dg, dbeta, d_initial_state or None) for the loss
     sum(d_o * o) + sum(d_final_state * final_state).  `checkpoints`, if given, are the forward's
-    fp32 checkpoints every 64 tokens; otherwise the forward is re-run for them."""
+    fp32 checkpoints every 64 tokens; otherwise the forward is re-run for them.  With the input
+    transforms of gdn_fwd, dg and dbeta are the gradients of the raw inputs, and the softplus
+    gate (a_log, dt_bias) appends (d_a_log, d_dt_bias) [HO] fp32 to the tuple."""
     _check_thd("q", q, torch.bfloat16)
     _check_thd("k", k, torch.bfloat16)
     _check_thd("v", v, torch.bfloat16)
     _check_thd("g", g, torch.float32, heads_dim=False)
-    _check_thd("beta", beta, torch.float32, heads_dim=False)
+    _check_beta(beta, beta_sigmoid)
     _check_thd("d_o", d_o, torch.bfloat16)
     T, HK, K = k.shape
     HV, V = v.shape[1], v.shape[2]
@@ -287,23 +291,33 @@ def gdn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
     p.d_initial_state = ds0.data_ptr() if ds0 is not None else None
     p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel()
     p.status = status.data_ptr() if status is not None else None
+    keep = _set_transforms(p, HV, dev, a_log, dt_bias, gate_lower_bound, beta_sigmoid, beta)  # noqa: F841
+    extra = ()
+    if a_log is not None:
+        da = torch.empty(HV, dtype=torch.float32, device=dev)
+        ddt = torch.empty(HV, dtype=torch.float32, device=dev)
+        p.d_a_log, p.d_dt_bias = da.data_ptr(), ddt.data_ptr()
+        extra = (da, ddt)
     B.check(lib.gdn_bwd(ctypes.byref(p), _stream_ptr(stream)), "gdn_bwd")
-    return dq, dk, dv, dg, db, ds0
+    return (dq, dk, dv, dg, db, ds0) + extra
 
 
 def gdn_summary_bwd(q: torch.Tensor, k: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
                     cu_seqlens: torch.Tensor, d_o: torch.Tensor, *, scale: Optional[float] = None,
                     use_qk_l2norm: bool = True, d_final_state: Optional[torch.Tensor] = None,
                     workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
-                    stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+                    stream: Optional[torch.cuda.Stream] = None, a_log: Optional[torch.Tensor] = None,
+                    dt_bias: Optional[torch.Tensor] = None, gate_lower_bound: Optional[float] = None,
+                    beta_sigmoid: bool = False) -> torch.Tensor:
     """State-gradient mirror of gdn_summary: for each span (sequence) the gradient of
     sum(d_o * o) + sum(d_final_state * end_state) with respect to the state entering the span,
     [N, HO, K, V] fp32.  It depends on neither that state nor v; with gdn_summary's transition,
-    d_enter = einsum('ab,bv->av', transition, d_exit) + (the value for d_exit = 0)."""
+    d_enter = einsum('ab,bv->av', transition, d_exit) + (the value for d_exit = 0).  Gate and
+    beta transforms as in gdn_fwd."""
     _check_thd("q", q, torch.bfloat16)
     _check_thd("k", k, torch.bfloat16)
     _check_thd("g", g, torch.float32, heads_dim=False)
-    _check_thd("beta", beta, torch.float32, heads_dim=False)
+    _check_beta(beta, beta_sigmoid)
     _check_thd("d_o", d_o, torch.bfloat16)
     T, HK, K = k.shape
     HV, V = d_o.shape[1], d_o.shape[2]
@@ -329,6 +343,7 @@ def gdn_summary_bwd(q: torch.Tensor, k: torch.Tensor, g: torch.Tensor, beta: tor
     p.d_state = d_state.data_ptr()
     p.workspace, p.workspace_bytes = workspace.data_ptr(), workspace.numel()
     p.status = status.data_ptr() if status is not None else None
+    keep = _set_transforms(p, HV, dev, a_log, dt_bias, gate_lower_bound, beta_sigmoid, beta)  # noqa: F841
     B.check(lib.gdn_summary_bwd(ctypes.byref(p), _stream_ptr(stream)), "gdn_summary_bwd")
     return d_state
 

@@ -193,6 +193,9 @@ class GdnBwdParams(ctypes.Structure):
         ("d_initial_state", _vp),
         ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
         ("status", _vp),
+        ("gate_mode", _i32), ("a_log", _vp), ("dt_bias", _vp), ("gate_lower_bound", ctypes.c_float),
+        ("beta_sigmoid", _i32), ("beta_bf16", _i32),
+        ("d_a_log", _vp), ("d_dt_bias", _vp),
     ]
 
 
@@ -212,6 +215,8 @@ class GdnSummaryBwdParams(ctypes.Structure):
         ("d_state", _vp),
         ("workspace", _vp), ("workspace_bytes", ctypes.c_size_t),
         ("status", _vp),
+        ("gate_mode", _i32), ("a_log", _vp), ("dt_bias", _vp), ("gate_lower_bound", ctypes.c_float),
+        ("beta_sigmoid", _i32), ("beta_bf16", _i32),
     ]
 
 

@@ -88,6 +88,7 @@ struct BwdSmem {
     float beta[kC], b[kC], gam[kC], GC[kC], rk[kC], rq[kC];
     float cx[kC], co[kC];   // -rk beta gamma (K^T dx) and scale rq gamma (Q^T dO) row factors
     float dbeta[kC], db[kC], wv[kC];
+    float gt[kC];           // the chunk's log decays (after the gate transform)
     float red[kBT / 32];
 };
 static_assert(sizeof(BwdSmem<128>) <= 227 * 1024, "backward shared memory exceeds the per-CTA limit");
@@ -154,6 +155,24 @@ __device__ __forceinline__ void mma3s(float (&c)[4], float (&r)[4], const uint32
     mma_tf32_16x8x8(r, ar, bh);
     mma_tf32_16x8x8(r, ah, br);
     mma_tf32_16x8x8(c, ah, bh);
+}
+
+// The recurrence's log decay and beta from the raw inputs (the forward's input transforms:
+// softplus gate gA softplus(g + gdt) with gA = -exp(a_log[h]), bounded gate lb sigmoid(g), beta
+// sigmoid of fp32 or bf16 logits).
+__device__ __forceinline__ float raw_gate(const BwdArgs& a, int64_t t, int h) { return a.g[t * a.g_st + h * a.g_sh]; }
+__device__ __forceinline__ float raw_beta(const BwdArgs& a, int64_t t, int h) {
+    const int64_t i = t * a.b_st + h * a.b_sh;
+    return a.beta_bf16 ? b2f(reinterpret_cast<const uint16_t*>(a.beta)[i]) : a.beta[i];
+}
+__device__ __forceinline__ float sigmoidf_(float x) { return 1.f / (1.f + expf(-x)); }
+__device__ __forceinline__ float gate_of(const BwdArgs& a, float x, float gA, float gdt) {
+    if (a.gate_mode == LA_GATE_SOFTPLUS) {
+        const float z = x + gdt;
+        return gA * (z > 20.f ? z : log1pf(expf(z)));
+    }
+    if (a.gate_mode == LA_GATE_SIGMOID_BOUND) return a.gate_lb * sigmoidf_(x);
+    return x;
 }
 
 // Sum over the four lanes of a quad (the accumulator fragment's column pairs of one row).
@@ -249,6 +268,9 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
 
     const bool kwarp = w < 4;  // owns dK_hat rows (else dQ_hat rows) 16 (w % 4) .. + 15
     const int om0 = 16 * (w & 3);
+    const float gA = a.gate_mode == LA_GATE_SOFTPLUS ? -expf(a.a_log[h]) : 0.f;
+    const float gdt = a.gate_mode == LA_GATE_SOFTPLUS ? a.dt_bias[h] : 0.f;
+    float pa_log = 0.f, pa_dt = 0.f;  // this token slot's sums for d_a_log and d_dt_bias (tid < 64)
 
     for (int c = nch - 1; c >= 0; --c) {
         const int64_t t0 = ts + static_cast<int64_t>(c) * kC;
@@ -276,8 +298,15 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
         }
         if (tid < kC) {
             const int i = tid;
-            s.beta[i] = i < n ? a.beta[(t0 + i) * a.b_st + h * a.b_sh] : 0.f;
-            s.b[i] = i < n ? a.g[(t0 + i) * a.g_st + h * a.g_sh] : 0.f;
+            float bt = 0.f, gt = 0.f;
+            if (i < n) {
+                bt = raw_beta(a, t0 + i, h);
+                if (a.beta_sigmoid) bt = sigmoidf_(bt);
+                gt = gate_of(a, raw_gate(a, t0 + i, h), gA, gdt);
+            }
+            s.beta[i] = bt;
+            s.b[i] = gt;
+            s.gt[i] = gt;
         }
         __syncthreads();
         {
@@ -773,8 +802,20 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
             float sacc = 0.f;
             for (int i = j; i < n; ++i) sacc += s.db[i];
             if (j < n) {
-                a.dg[(t0 + j) * a.dg_st + h * a.dg_sh] = sacc;
-                a.dbeta[(t0 + j) * a.db_st + h * a.db_sh] = s.dbeta[j];
+                // chain rule through the input transforms: dg, dbeta of the raw inputs
+                float dgr = sacc, dbr = s.dbeta[j];
+                if (a.gate_mode == LA_GATE_SOFTPLUS) {
+                    const float sz = sigmoidf_(raw_gate(a, t0 + j, h) + gdt);
+                    dgr = sacc * gA * sz;
+                    pa_log = fmaf(sacc, s.gt[j], pa_log);
+                    pa_dt += dgr;
+                } else if (a.gate_mode == LA_GATE_SIGMOID_BOUND) {
+                    const float sx = sigmoidf_(raw_gate(a, t0 + j, h));
+                    dgr = sacc * a.gate_lb * sx * (1.f - sx);
+                }
+                if (a.beta_sigmoid) dbr *= s.beta[j] * (1.f - s.beta[j]);
+                a.dg[(t0 + j) * a.dg_st + h * a.dg_sh] = dgr;
+                a.dbeta[(t0 + j) * a.db_st + h * a.db_sh] = dbr;
             }
         }
         // M = dA (.) beta_i Gamma (strictly lower part; the upper part keeps Gk), H = dP (.) Gamma
@@ -887,9 +928,39 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
         __syncthreads();
     }
     cp_async_wait_all();  // nothing is in flight here (the last tile fetches nothing)
+    if (a.gpart && tid < kC) {
+        // this unit's d_a_log and d_dt_bias sums: a fixed-order reduction over the 64 token slots
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            pa_log += __shfl_xor_sync(0xffffffffu, pa_log, off);
+            pa_dt += __shfl_xor_sync(0xffffffffu, pa_dt, off);
+        }
+        if (lane == 0) {
+            s.red[2 * w] = pa_log;
+            s.red[2 * w + 1] = pa_dt;
+        }
+    }
+    __syncthreads();
+    if (a.gpart && tid == 0) {
+        a.gpart[2 * unit] = s.red[0] + s.red[2];
+        a.gpart[2 * unit + 1] = s.red[1] + s.red[3];
+    }
     if (a.ds0) {
         for (int64_t e = tid; e < KV; e += kBT) a.ds0[unit * KV + e] = dSg[e];
     }
+}
+
+// d_a_log and d_dt_bias of a head: the per-sequence sums added in sequence order.
+__global__ void gdn_bwd_gate_param_kernel(const BwdArgs a) {
+    const int h = blockIdx.x * blockDim.x + threadIdx.x;
+    if (h >= a.HV) return;
+    float sa = 0.f, sd = 0.f;
+    for (int i = 0; i < a.N; ++i) {
+        sa += a.gpart[2 * (static_cast<int64_t>(i) * a.HV + h)];
+        sd += a.gpart[2 * (static_cast<int64_t>(i) * a.HV + h) + 1];
+    }
+    if (a.d_a_log) a.d_a_log[h] = sa;
+    if (a.d_dt_bias) a.d_dt_bias[h] = sd;
 }
 
 // dq, dk of a q/k head: the sum over its group of value heads (fixed order), rounded to bf16.
@@ -926,6 +997,11 @@ cudaError_t launch_bwd_kv(const BwdArgs& a, cudaStream_t s) {
     }
     if (a.group > 1 && a.T > 0 && !a.state_only) {
         gdn_bwd_group_sum_kernel<<<1024, 256, 0, s>>>(a);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    if (a.gpart && !a.state_only) {
+        gdn_bwd_gate_param_kernel<<<(a.HV + 127) / 128, 128, 0, s>>>(a);
         return cudaGetLastError();
     }
     return cudaSuccess;

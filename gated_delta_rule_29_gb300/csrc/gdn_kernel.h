@@ -159,6 +159,16 @@ struct BwdArgs {
     int32_t vo_async;                // v, dO pairs 4-byte aligned: asynchronous 4-byte copies
     int32_t state_only;              // only the entering-state gradient (gdn_summary_bwd): no
                                      // checkpoints, v, dq, dk, dv, dg, dbeta
+    // input transforms as in the forward; dg, dbeta then refer to the raw inputs
+    int32_t gate_mode;               // la_gate_mode
+    const float* a_log;              // [HO] (LA_GATE_SOFTPLUS)
+    const float* dt_bias;            // [HO] (LA_GATE_SOFTPLUS)
+    float gate_lb;                   // (LA_GATE_SIGMOID_BOUND)
+    int32_t beta_sigmoid;            // beta holds logits
+    int32_t beta_bf16;               // beta is bf16
+    float* gpart;                    // [N * HO][2] per-unit sums for d_a_log, d_dt_bias, or null
+    float* d_a_log;                  // [HO] or null
+    float* d_dt_bias;                // [HO] or null
 };
 
 // Gated DeltaProduct: the update timeline for the chunk kernel, and the per-token outputs.

@@ -139,6 +139,22 @@ la_status set_transforms(ChunkArgs& ka, int32_t gate_mode, const float* a_log, c
     return LA_OK;
 }
 
+// The same transforms for the backward kernel's arguments.
+la_status set_bwd_transforms(la::BwdArgs& b, int32_t gate_mode, const float* a_log, const float* dt_bias, float lb,
+                             int32_t beta_sigmoid, int32_t beta_bf16) {
+    ChunkArgs ka;
+    std::memset(&ka, 0, sizeof(ka));
+    const la_status st = set_transforms(ka, gate_mode, a_log, dt_bias, lb, beta_sigmoid, beta_bf16);
+    if (st != LA_OK) return st;
+    b.gate_mode = ka.gate_mode;
+    b.a_log = ka.a_log;
+    b.dt_bias = ka.dt_bias;
+    b.gate_lb = ka.gate_lb;
+    b.beta_sigmoid = ka.beta_sigmoid;
+    b.beta_bf16 = ka.beta_bf16;
+    return LA_OK;
+}
+
 la_status check_common(const Common& c) {
     if (c.T < 0 || c.N < 0 || c.HK <= 0 || c.HV <= 0) return LA_ERR_INVALID_ARG;
     if (c.cu_bits != 32 && c.cu_bits != 64) return LA_ERR_INVALID_ARG;
@@ -470,7 +486,7 @@ la_status gdp_fwd(const la_gdn_fwd_params* p, void* stream) {
 }
 
 struct BwdLayout {
-    size_t pro, ck, o, ds, gh, total;
+    size_t pro, ck, o, ds, gh, gp, total;
 };
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 BwdLayout bwd_layout(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, int32_t V, bool ck_given) {
@@ -486,6 +502,8 @@ BwdLayout bwd_layout(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, in
     off += up256(static_cast<size_t>(N) * HV * K * V * sizeof(float));
     L.gh = off;
     if (HV != HK) off += up256(2 * static_cast<size_t>(T) * HV * K * sizeof(float));
+    L.gp = off;  // per (sequence, head) sums for the softplus gate's parameter gradients
+    off += up256(2 * static_cast<size_t>(N) * HV * sizeof(float));
     L.total = off;
     return L;
 }
@@ -517,9 +535,16 @@ size_t la_gdn_bwd_workspace_bytes(int64_t T, int32_t N, int32_t HK, int32_t HV, 
 
 la_status gdn_bwd(const la_gdn_bwd_params* p, void* stream) {
     if (!p) return LA_ERR_INVALID_ARG;
-    Common c{p->T, p->N, p->HK, p->HV, p->K, p->V, p->cu_seqlens, p->cu_seqlens_bits, p->g, p->beta, 4};
+    Common c{p->T, p->N, p->HK, p->HV, p->K, p->V, p->cu_seqlens, p->cu_seqlens_bits, p->g, p->beta,
+             p->beta_bf16 ? 2 : 4};
     la_status st = check_common(c);
     if (st != LA_OK) return st;
+    la::BwdArgs b;
+    std::memset(&b, 0, sizeof(b));
+    if ((st = set_bwd_transforms(b, p->gate_mode, p->a_log, p->dt_bias, p->gate_lower_bound, p->beta_sigmoid,
+                                 p->beta_bf16)) != LA_OK)
+        return st;
+    if ((p->d_a_log && !aligned(p->d_a_log, 4)) || (p->d_dt_bias && !aligned(p->d_dt_bias, 4))) return LA_ERR_INVALID_ARG;
     if (p->T > 0) {
         if ((st = check_tma_operand(p->q, p->q_stride_t, p->q_stride_h, p->HK)) != LA_OK) return st;
         if ((st = check_tma_operand(p->k, p->k_stride_t, p->k_stride_h, p->HK)) != LA_OK) return st;
@@ -561,6 +586,8 @@ la_status gdn_bwd(const la_gdn_bwd_params* p, void* stream) {
         f.T = p->T; f.N = p->N; f.HK = p->HK; f.HV = p->HV; f.K = p->K; f.V = p->V;
         f.scale = p->scale; f.use_qk_l2norm = p->use_qk_l2norm;
         f.initial_state = p->initial_state; f.initial_state_dtype = p->initial_state_dtype;
+        f.gate_mode = p->gate_mode; f.a_log = p->a_log; f.dt_bias = p->dt_bias;
+        f.gate_lower_bound = p->gate_lower_bound; f.beta_sigmoid = p->beta_sigmoid; f.beta_bf16 = p->beta_bf16;
         f.o = wb + BL.o; f.o_stride_t = static_cast<int64_t>(p->HV) * p->V; f.o_stride_h = p->V;
         f.checkpoints = wb + BL.ck; f.checkpoint_dtype = LA_DTYPE_F32; f.checkpoint_every_n = la::kChunk;
         f.workspace = wb + BL.pro; f.workspace_bytes = PL.total;
@@ -582,8 +609,6 @@ la_status gdn_bwd(const la_gdn_bwd_params* p, void* stream) {
         pa.user_status = p->status;
         if (la::launch_prologue(pa, s) != cudaSuccess) return LA_ERR_CUDA;
     }
-    la::BwdArgs b;
-    std::memset(&b, 0, sizeof(b));
     b.q = static_cast<const uint16_t*>(p->q); b.q_st = p->q_stride_t; b.q_sh = p->q_stride_h;
     b.k = static_cast<const uint16_t*>(p->k); b.k_st = p->k_stride_t; b.k_sh = p->k_stride_h;
     b.v = static_cast<const uint16_t*>(p->v); b.v_st = p->v_stride_t; b.v_sh = p->v_stride_h;
@@ -613,6 +638,11 @@ la_status gdn_bwd(const la_gdn_bwd_params* p, void* stream) {
         b.dqh = reinterpret_cast<float*>(wb + BL.gh);
         b.dkh = b.dqh + static_cast<size_t>(p->T) * p->HV * p->K;
     }
+    if (b.gate_mode == LA_GATE_SOFTPLUS && (p->d_a_log || p->d_dt_bias)) {
+        b.gpart = reinterpret_cast<float*>(wb + BL.gp);
+        b.d_a_log = p->d_a_log;
+        b.d_dt_bias = p->d_dt_bias;
+    }
     cudaEvent_t ev0 = t_timing_start, ev1 = t_timing_stop;
     t_timing_start = t_timing_stop = nullptr;
     if (ev0 && cudaEventRecord(ev0, s) != cudaSuccess) return LA_ERR_CUDA;
@@ -623,9 +653,15 @@ la_status gdn_bwd(const la_gdn_bwd_params* p, void* stream) {
 
 la_status gdn_summary_bwd(const la_gdn_summary_bwd_params* p, void* stream) {
     if (!p) return LA_ERR_INVALID_ARG;
-    Common c{p->T, p->N, p->HK, p->HV, p->K, p->V, p->cu_seqlens, p->cu_seqlens_bits, p->g, p->beta, 4};
+    Common c{p->T, p->N, p->HK, p->HV, p->K, p->V, p->cu_seqlens, p->cu_seqlens_bits, p->g, p->beta,
+             p->beta_bf16 ? 2 : 4};
     la_status st = check_common(c);
     if (st != LA_OK) return st;
+    la::BwdArgs b;
+    std::memset(&b, 0, sizeof(b));
+    if ((st = set_bwd_transforms(b, p->gate_mode, p->a_log, p->dt_bias, p->gate_lower_bound, p->beta_sigmoid,
+                                 p->beta_bf16)) != LA_OK)
+        return st;
     if (!p->d_state || !aligned(p->d_state, 4)) return LA_ERR_INVALID_ARG;
     if (p->d_final_state && !aligned(p->d_final_state, 4)) return LA_ERR_INVALID_ARG;
     if (p->T > 0) {
@@ -656,8 +692,6 @@ la_status gdn_summary_bwd(const la_gdn_summary_bwd_params* p, void* stream) {
     pa.keys = reinterpret_cast<uint64_t*>(wb + SL.pro + PL.keys);
     pa.user_status = p->status;
     if (la::launch_prologue(pa, s) != cudaSuccess) return LA_ERR_CUDA;
-    la::BwdArgs b;
-    std::memset(&b, 0, sizeof(b));
     b.q = static_cast<const uint16_t*>(p->q); b.q_st = p->q_stride_t; b.q_sh = p->q_stride_h;
     b.k = static_cast<const uint16_t*>(p->k); b.k_st = p->k_stride_t; b.k_sh = p->k_stride_h;
     b.g = p->g; b.g_st = p->g_stride_t; b.g_sh = p->g_stride_h;

@@ -280,6 +280,15 @@ typedef struct la_gdn_bwd_params {
     void* workspace;             /* >= la_gdn_bwd_workspace_bytes(...), 256-byte aligned, or NULL */
     size_t workspace_bytes;
     int32_t* status;
+    /* ---- optional input transforms, as in gdn_fwd (zero-initialised: none) ---- */
+    int32_t gate_mode;           /* la_gate_mode */
+    const float* a_log;          /* [HO] fp32 (LA_GATE_SOFTPLUS) */
+    const float* dt_bias;        /* [HO] fp32 (LA_GATE_SOFTPLUS) */
+    float gate_lower_bound;      /* < 0 (LA_GATE_SIGMOID_BOUND) */
+    int32_t beta_sigmoid;        /* beta holds logits */
+    int32_t beta_bf16;           /* beta is bf16 (values, or logits with beta_sigmoid) */
+    float* d_a_log;              /* [HO] fp32 out (LA_GATE_SOFTPLUS), or NULL */
+    float* d_dt_bias;            /* [HO] fp32 out (LA_GATE_SOFTPLUS), or NULL */
 } la_gdn_bwd_params;
 
 /*
@@ -291,7 +300,9 @@ typedef struct la_gdn_bwd_params {
  * sum the contributions of its value heads.  When `checkpoints` is NULL the library first
  * re-runs the forward with fp32 checkpoints every 64 tokens into the workspace.  Each
  * (sequence, head) runs in a fixed order, so results do not depend on the batch around a
- * sequence.  The gate and beta transforms of gdn_fwd are forward-only.
+ * sequence.  With gdn_fwd's input transforms (cudnn-frontend PR #616 fusions) dg and dbeta are
+ * the gradients of the raw inputs (the gate input, the beta logits), and the softplus gate also
+ * gives d_a_log and d_dt_bias, summed over the batch in sequence order (deterministic).
  */
 la_status gdn_bwd(const la_gdn_bwd_params* p, void* stream);
 
@@ -317,6 +328,13 @@ typedef struct la_gdn_summary_bwd_params {
     void* workspace;             /* >= la_gdn_summary_bwd_workspace_bytes(...), 256-byte aligned, or NULL */
     size_t workspace_bytes;
     int32_t* status;
+    /* ---- optional input transforms, as in gdn_fwd / gdn_summary (zero-initialised: none) ---- */
+    int32_t gate_mode;
+    const float* a_log;
+    const float* dt_bias;
+    float gate_lower_bound;
+    int32_t beta_sigmoid;
+    int32_t beta_bf16;
 } la_gdn_summary_bwd_params;
 
 /*
@@ -332,7 +350,7 @@ typedef struct la_gdn_summary_bwd_params {
  * i.e. dS_enter[a][v] = sum_b transition[a][b] dS_exit[b][v] + dS_H[a][v] with gdn_summary's
  * transition.  That gradient does not depend on the entering state or on v (the map from the
  * state to the outputs is affine), so neither is an input and no forward pass runs.  Errors and
- * ownership as gdn_summary; the gate and beta transforms of gdn_fwd are forward-only.
+ * ownership as gdn_summary; g and beta go through gdn_fwd's input transforms when named.
  */
 la_status gdn_summary_bwd(const la_gdn_summary_bwd_params* p, void* stream);
 

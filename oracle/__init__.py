@@ -59,6 +59,8 @@ MUTATIONS = {
     14: "backward: decay gradient misses the erase path (uses dS instead of dS')",
     15: "backward: key gradient misses the S' dx term",
     18: "summary backward: a token's output term added after its erase step instead of before",
+    19: "backward of the softplus gate: d_dt_bias without the sigmoid factor",
+    20: "backward of the beta sigmoid: the logit gradient scaled by beta instead of beta (1 - beta)",
 }
 
 
@@ -265,15 +267,25 @@ def gdp_fwd(q, k, v, g, beta, cu_seqlens, num_householder, *, scale=None, use_qk
 
 
 def gdn_bwd(q, k, v, g, beta, cu_seqlens, do, *, scale=None, use_qk_l2norm=True, initial_state=None,
-            d_final_state=None, unit_mask=None, nthreads=None, mutation=0):
-    """fp64 backward of gdn_fwd (natural-log gate, beta as given) by reverse-mode differentiation
-    of the token recurrence: the gradients of L = sum(do * o) + sum(d_final_state * S_final).
+            d_final_state=None, unit_mask=None, nthreads=None, mutation=0,
+            gate="log", a_log=None, dt_bias=None, gate_lower_bound=None, beta_sigmoid=False):
+    """fp64 backward of gdn_fwd by reverse-mode differentiation of the token recurrence: the
+    gradients of L = sum(do * o) + sum(d_final_state * S_final).
 
     Returns dict(dq [T,HK,K], dk [T,HK,K], dv [T,HV,V], dg [T,HO], dbeta [T,HO],
     d_initial_state [N,HO,K,V]).  Grouped heads: dq, dk sum the contributions of every value
-    head of the group.
+    head of the group.  With the input transforms of gdn_fwd, dg and dbeta are the gradients of
+    the raw inputs (the chain rule through the transform, applied to the gradients of the
+    recurrence's log decay and beta), and the softplus gate adds d_a_log, d_dt_bias [HO]:
+    with z = g_raw + dt_bias and A = -exp(a_log), g = A softplus(z) gives dg_raw = dg A sigmoid(z),
+    d_dt_bias = sum_t dg_raw and d_a_log = sum_t dg g (since dg/da_log = g); the bounded gate
+    g = lb sigmoid(x) gives dx = dg lb sigmoid(x) (1 - sigmoid(x)); beta = sigmoid(y) gives
+    dy = dbeta beta (1 - beta).
     """
-    q, k, v, g, beta, do = (_f64(x) for x in (q, k, v, g, beta, do))
+    g_raw, beta_raw = _f64(g), _f64(beta)
+    g = gate_transform(g_raw, gate=gate, a_log=a_log, dt_bias=dt_bias, gate_lower_bound=gate_lower_bound)
+    beta = beta_transform(beta_raw, beta_sigmoid=beta_sigmoid)
+    q, k, v, do = (_f64(x) for x in (q, k, v, do))
     cu = _i64(cu_seqlens)
     T, HK, K = k.shape
     HV, V = v.shape[1], v.shape[2]
@@ -297,17 +309,31 @@ def gdn_bwd(q, k, v, g, beta, cu_seqlens, do, *, scale=None, use_qk_l2norm=True,
         T, N, HK, HV, K, V, float(scale), int(bool(use_qk_l2norm)), _ptr(s0),
         _ptr(do), _ptr(dfin),
         _ptr(dqh), _ptr(dkh), _ptr(dv), _ptr(dg), _ptr(db), _ptr(ds0),
-        mask.ctypes.data if mask is not None else None, int(nthreads or _default_threads()), int(mutation))
+        mask.ctypes.data if mask is not None else None, int(nthreads or _default_threads()),
+        int(mutation if mutation < 19 else 0))
     if rc != 0:
         raise ValueError("oracle rejected its arguments (cu_seqlens or shapes)")
     grp = HV // HK
     dq = dqh.reshape(T, HK, grp, K).sum(axis=2)
     dk = dkh.reshape(T, HK, grp, K).sum(axis=2)
-    return {"dq": dq, "dk": dk, "dv": dv, "dg": dg, "dbeta": db, "d_initial_state": ds0}
+    out = {"dq": dq, "dk": dk, "dv": dv, "dg": dg, "dbeta": db, "d_initial_state": ds0}
+    if gate == "softplus":
+        z = g_raw + _f64(dt_bias).reshape(1, -1)
+        A = -np.exp(_f64(a_log)).reshape(1, -1)
+        dg_raw = dg * A * (1.0 if mutation == 19 else sigmoid(z))
+        out["d_a_log"] = (dg * g).sum(axis=0)
+        out["d_dt_bias"] = dg_raw.sum(axis=0)
+        out["dg"] = dg_raw
+    elif gate == "sigmoid_bound":
+        sx = sigmoid(g_raw)
+        out["dg"] = dg * float(gate_lower_bound) * sx * (1.0 - sx)
+    if beta_sigmoid:
+        out["dbeta"] = db * (beta if mutation == 20 else beta * (1.0 - beta))
+    return out
 
 
 def gdn_summary_bwd(q, k, g, beta, cu_seqlens, do, *, scale=None, use_qk_l2norm=True, d_final_state=None,
-                    mutation=0):
+                    mutation=0, gate="log", a_log=None, dt_bias=None, gate_lower_bound=None, beta_sigmoid=False):
     """fp64 state-gradient counterpart of the summary (cuDNN Linear Attention page, "Summaries":
     each summary op has a backward partner acting on the state gradient).  For each span (sequence) and output
     head: the gradient of L = sum(do * o) + sum(d_final_state * S_end) with respect to the state
@@ -317,8 +343,11 @@ def gdn_summary_bwd(q, k, g, beta, cu_seqlens, do, *, scale=None, use_qk_l2norm=
     G <- G + scale q_t do_t^T (from o_t = scale S_t^T q_t), then G <- exp(g_t)(I - beta_t k_t k_t^T) G,
     the transposed Jacobian of S_t = exp(g_t)(I - beta_t k_t k_t^T) S_{t-1} + beta_t k_t v_t^T
     (the factor is symmetric).  G after the span's first token is the result; it involves neither
-    v nor any state value.  q, k are L2-normalised first when use_qk_l2norm is set.
+    v nor any state value.  q, k are L2-normalised first when use_qk_l2norm is set; the input
+    transforms of gdn_fwd apply to g and beta as there.
     """
+    g = gate_transform(g, gate=gate, a_log=a_log, dt_bias=dt_bias, gate_lower_bound=gate_lower_bound)
+    beta = beta_transform(beta, beta_sigmoid=beta_sigmoid)
     q, k, g, beta, do = (_f64(x) for x in (q, k, g, beta, do))
     cu = _i64(cu_seqlens)
     T, HK, K = k.shape

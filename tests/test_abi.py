@@ -245,6 +245,50 @@ def test_gdn_summary_bwd_rejects(name, over, code):
     assert lib.gdn_summary_bwd(ctypes.byref(p), None) == code
 
 
+def _bwd(**over):
+    p = B.GdnBwdParams()
+    T, N, HK, HV, K, V = 256, 2, 2, 4, 128, 128
+    p.q, p.q_stride_t, p.q_stride_h = FAKE, HK * K, K
+    p.k, p.k_stride_t, p.k_stride_h = FAKE, HK * K, K
+    p.v, p.v_stride_t, p.v_stride_h = FAKE, HV * V, V
+    p.g, p.g_stride_t, p.g_stride_h = FAKE, HV, 1
+    p.beta, p.beta_stride_t, p.beta_stride_h = FAKE, HV, 1
+    p.cu_seqlens, p.cu_seqlens_bits = FAKE, 32
+    p.T, p.N, p.HK, p.HV, p.K, p.V = T, N, HK, HV, K, V
+    p.d_o, p.d_o_stride_t, p.d_o_stride_h = FAKE, HV * V, V
+    p.dq, p.dq_stride_t, p.dq_stride_h = FAKE, HK * K, K
+    p.dk, p.dk_stride_t, p.dk_stride_h = FAKE, HK * K, K
+    p.dv, p.dv_stride_t, p.dv_stride_h = FAKE, HV * V, V
+    p.dg, p.dg_stride_t, p.dg_stride_h = FAKE, HV, 1
+    p.dbeta, p.dbeta_stride_t, p.dbeta_stride_h = FAKE, HV, 1
+    p.workspace, p.workspace_bytes = FAKE, 16  # too small: reached only after every argument check
+    for k, v in over.items():
+        setattr(p, k, v)
+    return p
+
+
+BWD_ERRORS = [
+    ("valid arguments reach the workspace check", dict(), B.LA_ERR_WORKSPACE),
+    ("K not 64/128", dict(K=96), B.LA_ERR_UNSUPPORTED),
+    ("null dg", dict(dg=None), B.LA_ERR_INVALID_ARG),
+    ("softplus gate without a_log", dict(gate_mode=B.LA_GATE_SOFTPLUS, dt_bias=FAKE), B.LA_ERR_INVALID_ARG),
+    ("bounded gate with a positive bound", dict(gate_mode=B.LA_GATE_SIGMOID_BOUND, gate_lower_bound=1.0),
+     B.LA_ERR_INVALID_ARG),
+    ("unknown gate mode", dict(gate_mode=7), B.LA_ERR_INVALID_ARG),
+    ("misaligned d_a_log", dict(gate_mode=B.LA_GATE_SOFTPLUS, a_log=FAKE, dt_bias=FAKE, d_a_log=FAKE + 2),
+     B.LA_ERR_INVALID_ARG),
+    ("softplus gate with outputs reaches the workspace check",
+     dict(gate_mode=B.LA_GATE_SOFTPLUS, a_log=FAKE, dt_bias=FAKE, d_a_log=FAKE, d_dt_bias=FAKE), B.LA_ERR_WORKSPACE),
+]
+
+
+@pytest.mark.parametrize("name,over,code", BWD_ERRORS, ids=[e[0] for e in BWD_ERRORS])
+def test_gdn_bwd_rejects(name, over, code):
+    lib = B.load()
+    p = _bwd(**over)
+    assert lib.gdn_bwd(ctypes.byref(p), None) == code
+
+
 def test_summary_bwd_workspace_bytes():
     lib = B.load()
     a = lib.la_gdn_summary_bwd_workspace_bytes(8, 32, 128, 128)

@@ -153,3 +153,49 @@ def test_bwd_dense_batch_sampled():
     print("[parity] bwd dense batch sampled: " + ", ".join(f"{k_} {v_:.2e}" for k_, v_ in errs.items()))
     for name, e in errs.items():
         assert e <= (BF16_TOL if name in ("dq", "dk", "dv") else F32_TOL), errs
+
+
+def test_bwd_softplus_gate_and_beta_sigmoid():
+    """The backward through the forward's input transforms: softplus gate with a_log, dt_bias
+    (raw gate inputs N(0,1), rates exp(a_log) in [0.02, 0.1] so that state crosses chunks) and
+    beta logits through the sigmoid; gradients of the raw inputs, d_a_log and d_dt_bias."""
+    w = W.draw("bwd softplus", [1, 100, 64, 250], 2, 4, 128, 128, seed=461, initial_state=True)
+    gen = torch.Generator().manual_seed(462)
+    g_raw = torch.randn(w.T, w.HV, generator=gen)
+    b_logit = torch.randn(w.T, w.HV, generator=gen)
+    a_log = torch.log(0.02 + 0.08 * torch.rand(w.HV, generator=gen))
+    dt_bias = 0.5 * torch.randn(w.HV, generator=gen)
+    do, dfin = cotangents(w, 463)
+    d = dev()
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    out = la.gdn_bwd(w.q.to(d), w.k.to(d), w.v.to(d), g_raw.to(d), b_logit.to(d), w.cu_seqlens.to(d), do.to(d),
+                     initial_state=w.initial_state.to(d), d_final_state=dfin.to(d), status=status,
+                     a_log=a_log.to(d), dt_bias=dt_bias.to(d), beta_sigmoid=True)
+    assert la.read_status(status) == 0
+    assert len(out) == 8
+    got = [x.float().cpu().numpy() for x in out]
+    ref = oracle.gdn_bwd(w.q, w.k, w.v, g_raw, b_logit, w.cu_seqlens, do, initial_state=w.initial_state,
+                         d_final_state=dfin, gate="softplus", a_log=a_log, dt_bias=dt_bias, beta_sigmoid=True)
+    compare(w, got[:6], ref, label=" softplus gate + beta sigmoid")
+    errs = {name: rel(x, ref[name]) for name, x in zip(["d_a_log", "d_dt_bias"], got[6:])}
+    print("[parity] bwd gate parameters: " + ", ".join(f"{k_} {v_:.2e}" for k_, v_ in errs.items()))
+    assert max(errs.values()) <= F32_TOL, errs
+
+
+def test_bwd_bounded_gate_bf16_beta_logits():
+    """The bounded sigmoid gate (lower bound -0.1) and bf16 beta logits through the sigmoid."""
+    w = W.draw("bwd bounded", [70, 129], 1, 2, 64, 64, seed=471, initial_state=True)
+    gen = torch.Generator().manual_seed(472)
+    g_raw = torch.randn(w.T, w.HV, generator=gen)
+    b_logit = torch.randn(w.T, w.HV, generator=gen).to(torch.bfloat16)
+    do, dfin = cotangents(w, 473)
+    d = dev()
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    out = la.gdn_bwd(w.q.to(d), w.k.to(d), w.v.to(d), g_raw.to(d), b_logit.to(d), w.cu_seqlens.to(d), do.to(d),
+                     initial_state=w.initial_state.to(d), d_final_state=dfin.to(d), status=status,
+                     gate_lower_bound=-0.1, beta_sigmoid=True)
+    assert la.read_status(status) == 0
+    got = [x.float().cpu().numpy() for x in out]
+    ref = oracle.gdn_bwd(w.q, w.k, w.v, g_raw, b_logit.float(), w.cu_seqlens, do, initial_state=w.initial_state,
+                         d_final_state=dfin, gate="sigmoid_bound", gate_lower_bound=-0.1, beta_sigmoid=True)
+    compare(w, got, ref, label=" bounded gate + bf16 beta logits")

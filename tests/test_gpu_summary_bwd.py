@@ -158,3 +158,23 @@ def test_summary_bwd_bad_cu_seqlens_sets_status():
     status = torch.zeros(1, dtype=torch.int32, device=d)
     la.gdn_summary_bwd(w.q.to(d), w.k.to(d), w.g.to(d), w.beta.to(d), bad, do.to(d), status=status)
     assert la.read_status(status) != 0
+
+
+def test_summary_bwd_with_input_transforms():
+    """The forward's input transforms on g and beta (softplus gate, beta sigmoid) apply here too."""
+    w = W.draw("sbwd transforms", [300, 64, 129], 2, 2, 128, 128, seed=581)
+    gen = torch.Generator().manual_seed(582)
+    g_raw = torch.randn(w.T, w.HV, generator=gen)
+    b_logit = torch.randn(w.T, w.HV, generator=gen)
+    a_log = torch.log(0.02 + 0.08 * torch.rand(w.HV, generator=gen))
+    dt_bias = 0.5 * torch.randn(w.HV, generator=gen)
+    do, dfin = cotangents(w, 583)
+    d = dev()
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    got = la.gdn_summary_bwd(w.q.to(d), w.k.to(d), g_raw.to(d), b_logit.to(d), w.cu_seqlens.to(d), do.to(d),
+                             d_final_state=dfin.to(d), status=status, a_log=a_log.to(d), dt_bias=dt_bias.to(d),
+                             beta_sigmoid=True)
+    assert la.read_status(status) == 0
+    ref = oracle.gdn_summary_bwd(w.q, w.k, g_raw, b_logit, w.cu_seqlens, do, d_final_state=dfin, gate="softplus",
+                                 a_log=a_log, dt_bias=dt_bias, beta_sigmoid=True)
+    check(w, got, ref, " softplus gate + beta sigmoid")

@@ -433,6 +433,47 @@ def check_backward_finite_differences(mutation=0):
     return worst
 
 
+def check_backward_transforms_finite_differences(mutation=0):
+    """The backward through the input transforms (softplus gate with a_log and dt_bias, bounded
+    sigmoid gate, beta sigmoid) against central differences of the (pinned) forward with the same
+    transforms: the raw gate and beta inputs, a_log and dt_bias."""
+    worst = 0.0
+    x, cu, do, dfin, l2 = _fd_case(True, 141)
+    rng = np.random.default_rng(142)
+    HV = x["g"].shape[1]
+    x["g"] = rng.standard_normal(x["g"].shape)          # raw gate inputs
+    x["beta"] = rng.standard_normal(x["beta"].shape)    # beta logits
+    x["a_log"] = 0.3 * rng.standard_normal(HV)
+    x["dt_bias"] = 0.5 * rng.standard_normal(HV)
+    for kw, names in ((dict(gate="softplus", beta_sigmoid=True), ("g", "beta", "a_log", "dt_bias")),
+                      (dict(gate="sigmoid_bound", gate_lower_bound=-2.5), ("g",))):
+        def fw(xx):
+            extra = dict(kw)
+            if kw["gate"] == "softplus":
+                extra.update(a_log=xx["a_log"], dt_bias=xx["dt_bias"])
+            return extra
+
+        def loss(xx):
+            r = oracle.gdn_fwd(xx["q"], xx["k"], xx["v"], xx["g"], xx["beta"], cu, scale=0.8, use_qk_l2norm=l2,
+                               initial_state=xx["S0"], nthreads=1, **fw(xx))
+            return float((r["o"] * do).sum() + (r["final_state"] * dfin).sum())
+
+        grads = oracle.gdn_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], cu, do, scale=0.8, use_qk_l2norm=l2,
+                               initial_state=x["S0"], d_final_state=dfin, nthreads=1, mutation=mutation, **fw(x))
+        gname = {"g": "dg", "beta": "dbeta", "a_log": "d_a_log", "dt_bias": "d_dt_bias"}
+        eps = 1e-6
+        for name in names:
+            fd = np.zeros_like(x[name])
+            for idx in np.ndindex(x[name].shape):
+                xp = {kk: vv.copy() for kk, vv in x.items()}
+                xm = {kk: vv.copy() for kk, vv in x.items()}
+                xp[name][idx] += eps
+                xm[name][idx] -= eps
+                fd[idx] = (loss(xp) - loss(xm)) / (2 * eps)
+            worst = max(worst, _rel(grads[gname[name]], fd))
+    return worst
+
+
 def check_gdp_dense_products(mutation=0):
     """GDP against its definition written as dense products: per token, S_t = exp(g_t) H_t S_{t-1}
     + sum_j (prod_{i > j} (I - beta_i k_i k_i^T)) beta_j k_j v_j^T with H_t the product of the
@@ -566,6 +607,7 @@ CHECKS = {
     "beta_sigmoid": (check_beta_sigmoid, 1e-14),
     "state_pool": (check_state_pool, 1e-13),
     "backward_finite_differences": (check_backward_finite_differences, 1e-6),
+    "backward_transforms_finite_differences": (check_backward_transforms_finite_differences, 1e-6),
     "gdp_dense_products": (check_gdp_dense_products, 1e-12),
     "summary_bwd": (check_summary_bwd, 1e-12),
     "summary_bwd_finite_differences": (check_summary_bwd_finite_differences, 1e-6),
