@@ -715,11 +715,11 @@ def run_gdp_bench(args, world, rank, local):
                        "l2": "inputs larger than L2; no flush"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak, "traffic": None, "peak_source": peak_src,
-                         "kernel": "update-timeline build + gdn_chunk_kernel<128, fwd> + gather (whole step)",
+                         "kernel": "gdn_chunk_kernel<128, gdp> (whole step: prologue + kernel)",
                          "algorithmic_bytes": alg},
             "cpu_baseline": cpu,
             "e2e": None,
-            "gpu_launches": 4 * args.steps,
+            "gpu_launches": 2 * args.steps,
             "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)

@@ -117,6 +117,13 @@ __device__ __forceinline__ float gate_at(const ChunkArgs& a, int64_t t, int h, f
     if (a.gate_mode == LA_GATE_SIGMOID_BOUND) return a.gate_lb / (1.f + expf(-x));
     return x;
 }
+// The log decay of update row r: on the update timeline of Gated DeltaProduct (gdp_n > 1 rows
+// per token) a token's gate enters at its first update and the others carry no decay.
+template <bool kGdp>
+__device__ __forceinline__ float gate_row(const ChunkArgs& a, int64_t r, int h, float gA, float gdt) {
+    if (kGdp) return (r % a.gdp_n == 0) ? gate_at(a, r / a.gdp_n, h, gA, gdt) : 0.f;
+    return gate_at(a, r, h, gA, gdt);
+}
 __device__ __forceinline__ float beta_at(const ChunkArgs& a, int64_t t, int h) {
     const int64_t i = t * a.b_st + h * a.b_sh;
     const float x = a.beta_bf16 ? __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const uint16_t*>(a.beta)[i]) << 16)
@@ -355,8 +362,13 @@ __global__ void __launch_bounds__(kCta, 2)
     gdn_chunk_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
                      const ChunkArgs a) {
-    constexpr bool kFwd = MODE == kModeFwd;
+    constexpr bool kFwd = MODE != kModeSummary;  // queries and outputs (the forward, or GDP's)
+    constexpr bool kGdp = MODE == kModeGdp;
     constexpr int KP = KD / 16;  // 16-column pieces of the state
+    // GDP: a chunk of 64 update rows holds QR tokens; their queries fill rows 0 .. QR-1 of the
+    // query half of the K/Q tile (the other rows stay zero) and their outputs columns 0 .. QR-1
+    const int NH = kGdp ? a.gdp_n : 1;
+    const int QR = kChunk / NH;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Scalars& sc = *reinterpret_cast<Scalars*>(sm + SM_SC);
@@ -405,12 +417,22 @@ __global__ void __launch_bounds__(kCta, 2)
     const uint64_t d_pb = sdesc_sw128(smem_u32(PB), 16, 1024);
     const uint64_t d_slo = kFwd ? 0 : sdesc_sw128(smem_u32(SLO), 16, 1024);
 
+    if (kGdp) {
+        // the query rows past a chunk's QR tokens are never written by the tile loads: zero them once
+        for (int e = tid; e < (KD / 64) * (64 - QR) * 8; e += kCta) {
+            const int rg = e / ((64 - QR) * 8), rem = e % ((64 - QR) * 8);
+            *reinterpret_cast<uint4*>(KQ + rg * 16384 + 8192 + (QR + rem / 8) * 128 + (rem % 8) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+    }
     uint32_t ph_kq = 0, ph_v = 0, ph_mma = 0, ph_o = 0;  // parity of the next wait on each barrier
     bool pend_kq = false, pend_v = false, pend_mma = false, pend_o = false;
     bool failed = false;
     const uint64_t budget = a.wait_budget_ns;
     const int64_t per_seq = static_cast<int64_t>(HO) * a.tiles_per_head;
-    const uint32_t kq_bytes = (kFwd ? 2u : 1u) * KD * 128u;
+    const uint32_t kq_bytes = KD * 128u + (kFwd ? static_cast<uint32_t>(KD / 64) * QR * 128u : 0u);
     const uint32_t v_bytes = static_cast<uint32_t>(a.V) * 128u;
 
     for (;;) {
@@ -429,8 +451,10 @@ __global__ void __launch_bounds__(kCta, 2)
         const int tile = rem % a.tiles_per_head;
         const int hk = h / a.group;
         const bool value_tile = kFwd || tile == kTileValue;
-        const int64_t ts = cu_get(a.cu, a.cu64, seq);
-        const int64_t L = cu_get(a.cu, a.cu64, seq + 1) - ts;
+        // update rows (GDP: NH per token); tok_s is the sequence's first token
+        const int64_t tok_s = cu_get(a.cu, a.cu64, seq);
+        const int64_t ts = tok_s * NH;
+        const int64_t L = (cu_get(a.cu, a.cu64, seq + 1) - tok_s) * NH;
         const int nchunks = static_cast<int>((L + kChunk - 1) / kChunk);
         const int64_t unit_state = static_cast<int64_t>(seq) * HO + h;
         // the start state's slot, and where the end state goes (the same pool slot when a state
@@ -458,7 +482,7 @@ __global__ void __launch_bounds__(kCta, 2)
             gdt = a.dt_bias[h];
         }
         if (tid < 64 && tid < L) {
-            g_nx = gate_at(a, ts + tid, h, gA, gdt);
+            g_nx = gate_row<kGdp>(a, ts + tid, h, gA, gdt);
             b_nx = beta_at(a, ts + tid, h);
         }
         if (tid < 64) {
@@ -536,7 +560,8 @@ __global__ void __launch_bounds__(kCta, 2)
 #pragma unroll
                 for (int rg = 0; rg < KD / 64; ++rg) {
                     tma_load_3d(KQ + rg * 16384, &kmap, &sc.bar_kq, rg * 64, hk, static_cast<int>(ts));
-                    if (kFwd) tma_load_3d(KQ + rg * 16384 + 8192, &qmap, &sc.bar_kq, rg * 64, hk, static_cast<int>(ts));
+                    if (kFwd)
+                        tma_load_3d(KQ + rg * 16384 + 8192, &qmap, &sc.bar_kq, rg * 64, hk, static_cast<int>(ts / NH));
                 }
             }
             if (tid == 0) {
@@ -555,11 +580,12 @@ __global__ void __launch_bounds__(kCta, 2)
             const int n = left < kChunk ? static_cast<int>(left) : kChunk;
             const bool last = c + 1 == nchunks;
             const bool o_tma_chunk = kFwd && a.o_tma && n == kChunk;
+            const int64_t tok0 = t0 / NH;  // the chunk's first token (its query and output rows)
             const float g_cur = g_nx, b_cur = b_nx;
             if (!last) {
                 g_nx = b_nx = 0.f;
                 if (tid < 64 && tid < left - kChunk) {
-                    g_nx = gate_at(a, t0 + kChunk + tid, h, gA, gdt);
+                    g_nx = gate_row<kGdp>(a, t0 + kChunk + tid, h, gA, gdt);
                     b_nx = beta_at(a, t0 + kChunk + tid, h);
                 }
             }
@@ -625,7 +651,8 @@ __global__ void __launch_bounds__(kCta, 2)
                     for (int e = 0; e < 32; ++e) nrm = (e == lane) ? d32[e] : nrm;
                 }
                 const int row = r & 63;
-                const float inv = (row < n) ? (a.l2norm ? 1.0f / sqrtf(nrm + 1e-6f) : 1.f) : 0.f;
+                const int nvalid = (r < 64) ? n : n / NH;  // key rows, or the chunk's query tokens
+                const float inv = (row < nvalid) ? (a.l2norm ? 1.0f / sqrtf(nrm + 1e-6f) : 1.f) : 0.f;
                 if (r < 64) sc.rk[row] = inv;
                 else sc.rq[row] = inv;
             }
@@ -665,11 +692,19 @@ __global__ void __launch_bounds__(kCta, 2)
                 sc.b[i] = bi;
                 sc.bet[i] = bet;
                 sc.sx[i] = bet * gam * rk;
-                sc.sq[i] = a.scale * rq * gam;
                 sc.sd[i] = exp2f(bC - bi) * rk;
                 sc.u[i] = rk * exp2f(b31 - bi);
                 sc.cA[i] = bet * rk * e;
-                sc.cP[i] = a.scale * rq * e;
+                if (kGdp) {
+                    // query row i is token i of the chunk, read after its last update row ri
+                    const int ri = i * NH + NH - 1;
+                    const float bq = ri < 64 ? sc.bw[ri] + (ri >= 32 ? sc.bw[31] : 0.f) : 0.f;
+                    sc.sq[i] = ri < 64 ? a.scale * rq * exp2f(bq) : 0.f;
+                    sc.cP[i] = ri < 64 ? a.scale * rq * exp2f(bq - b31) : 0.f;
+                } else {
+                    sc.sq[i] = a.scale * rq * gam;
+                    sc.cP[i] = a.scale * rq * e;
+                }
                 in_range = fabsf(bi - b31) <= kFastRange;
             }
             const bool fast = __syncthreads_and(in_range) != 0;
@@ -679,7 +714,10 @@ __global__ void __launch_bounds__(kCta, 2)
                 const int i = r & 63;
                 const bool is_a = r < 64;
                 const float ci = fast ? (is_a ? sc.cA[i] : sc.cP[i]) : (is_a ? sc.bet[i] * sc.rk[i] : a.scale * sc.rq[i]);
-                const float bi = sc.b[i];
+                // the row's position on the update timeline (GDP query rows: the token's last update;
+                // rows past the chunk's tokens are zero and fully masked)
+                const int ip = (kGdp && !is_a) ? (i < QR ? i * NH + NH - 1 : -1) : i;
+                const float bi = sc.b[ip < 0 ? 0 : ip];
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
                     float* gv = &g64[16 * p];
@@ -693,7 +731,7 @@ __global__ void __launch_bounds__(kCta, 2)
 #pragma unroll
                         for (int e = 0; e < 16; ++e) {
                             const int j = 16 * p + e;
-                            const float dec = (j <= i) ? exp2f(bi - sc.b[j]) : 0.f;
+                            const float dec = (j <= ip) ? exp2f(bi - sc.b[j]) : 0.f;
                             gv[e] *= ci * sc.rk[j] * dec;
                         }
                     }
@@ -711,7 +749,7 @@ __global__ void __launch_bounds__(kCta, 2)
                     } else {
 #pragma unroll
                         for (int e = 0; e < 16; ++e)
-                            if (16 * p + e > i) gv[e] = 0.f;
+                            if (16 * p + e > ip) gv[e] = 0.f;
                         store8_split(PB + sw128_off(i, 2 * p), nullptr, &gv[0]);
                         store8_split(PB + sw128_off(i, 2 * p + 1), nullptr, &gv[8]);
                     }
@@ -905,20 +943,22 @@ __global__ void __launch_bounds__(kCta, 2)
                         const uint32_t vchunk = (r & 63) >> 3;
 #pragma unroll
                         for (int i = 0; i < 64; ++i)
-                            *reinterpret_cast<uint16_t*>(col + sw128_off(i, vchunk)) = f_to_bf16_bits(o64[i]);
+                            if (!kGdp || i < QR)
+                                *reinterpret_cast<uint16_t*>(col + sw128_off(i, vchunk)) = f_to_bf16_bits(o64[i]);
                     }
                     fence_proxy_async_smem();
                     __syncthreads();
                     if (tid == 0) {
                         for (int rg = 0; rg < a.V / 64; ++rg)
-                            tma_store_3d(&omap, OST + rg * 8192, rg * 64, h, static_cast<int>(t0));
+                            tma_store_3d(&omap, OST + rg * 8192, rg * 64, h, static_cast<int>(tok0));
                         bulk_commit_group();
                     }
                 } else if (r < a.V) {
-                    uint16_t* op = a.o + t0 * a.o_st + static_cast<int64_t>(h) * a.o_sh + r;
+                    uint16_t* op = a.o + tok0 * a.o_st + static_cast<int64_t>(h) * a.o_sh + r;
+                    const int nq = n / NH;
 #pragma unroll
                     for (int i = 0; i < 64; ++i)
-                        if (i < n) op[static_cast<int64_t>(i) * a.o_st] = f_to_bf16_bits(o64[i]);
+                        if (i < nq) op[static_cast<int64_t>(i) * a.o_st] = f_to_bf16_bits(o64[i]);
                 }
             }
             {
@@ -937,7 +977,7 @@ __global__ void __launch_bounds__(kCta, 2)
 #pragma unroll
                 for (int rg = 0; rg < KD / 64; ++rg) {
                     tma_load_3d(KQ + rg * 16384, &kmap, &sc.bar_kq, rg * 64, hk, t1);
-                    if (kFwd) tma_load_3d(KQ + rg * 16384 + 8192, &qmap, &sc.bar_kq, rg * 64, hk, t1);
+                    if (kFwd) tma_load_3d(KQ + rg * 16384 + 8192, &qmap, &sc.bar_kq, rg * 64, hk, t1 / NH);
                 }
             }
             if (!last) pend_kq = true;
@@ -1074,8 +1114,12 @@ cudaError_t launch_chunk_kernel(const ChunkArgs& a, const CUtensorMap& qm, const
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (a.K == 128) return mode == kModeFwd ? launch_one<128, kModeFwd>(a, qm, km, vm, om, dev, s)
-                                            : launch_one<128, kModeSummary>(a, qm, km, vm, om, dev, s);
+    if (a.K == 128) {
+        if (mode == kModeGdp) return launch_one<128, kModeGdp>(a, qm, km, vm, om, dev, s);
+        return mode == kModeFwd ? launch_one<128, kModeFwd>(a, qm, km, vm, om, dev, s)
+                                : launch_one<128, kModeSummary>(a, qm, km, vm, om, dev, s);
+    }
+    if (mode == kModeGdp) return launch_one<64, kModeGdp>(a, qm, km, vm, om, dev, s);
     return mode == kModeFwd ? launch_one<64, kModeFwd>(a, qm, km, vm, om, dev, s)
                             : launch_one<64, kModeSummary>(a, qm, km, vm, om, dev, s);
 }

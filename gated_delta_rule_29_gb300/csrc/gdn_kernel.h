@@ -11,7 +11,9 @@ constexpr int kChunk = 64;          // tokens per chunk; the chunk grid restarts
 constexpr int kThreads = 256;       // threads of the fused chunk kernel
 constexpr int kPrologueThreads = 1024;
 
-enum Mode : int { kModeFwd = 0, kModeSummary = 1 };
+// kModeGdp: the forward of Gated DeltaProduct (n delta updates per token) on the update timeline,
+// with q, g and o on the token timeline
+enum Mode : int { kModeFwd = 0, kModeSummary = 1, kModeGdp = 2 };
 enum TileKind : int { kTileValue = 0, kTileTransition = 1 };
 
 // Workspace layout (bytes from the 256-aligned workspace base).
@@ -97,6 +99,7 @@ struct ChunkArgs {
     float gate_lb;
     int32_t beta_sigmoid;
     int32_t beta_bf16;
+    int32_t gdp_n;                   // kModeGdp: updates per token (divides 64); k, v, beta have n rows per token
     // state pool: sequence i reads and writes back slot state_idx[i] of s0 (then final_state
     // aliases s0 and final_bf16 follows the pool's dtype)
     const int32_t* state_idx;

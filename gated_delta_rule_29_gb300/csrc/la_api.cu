@@ -48,13 +48,14 @@ thread_local cudaEvent_t t_timing_stop = nullptr;
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // [T, H, D] bf16 view with 64 x 1 x 64 boxes (64 features of one head, 64 tokens), 128-byte swizzle.
-la_status make_map(CUtensorMap* m, const void* base, int64_t T, int64_t H, int64_t D, int64_t st, int64_t sh) {
+la_status make_map(CUtensorMap* m, const void* base, int64_t T, int64_t H, int64_t D, int64_t st, int64_t sh,
+                   uint32_t box_rows = 64) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return LA_ERR_CUDA;
     if (H == 1) sh = D;  // the stride of a size-1 axis is never used
     cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(T)};
     cuuint64_t strides[2] = {static_cast<cuuint64_t>(sh) * 2, static_cast<cuuint64_t>(st) * 2};
-    cuuint32_t box[3] = {64, 1, 64};
+    cuuint32_t box[3] = {64, 1, box_rows};
     cuuint32_t es[3] = {1, 1, 1};
     CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -166,9 +167,11 @@ la_status check_common(const Common& c) {
     return LA_OK;
 }
 
+// gdp_n > 1 (mode kModeGdp): k, v (and beta) have gdp_n rows per token, q, g and o one; the q and
+// o tiles then hold 64 / gdp_n token rows per 64-row chunk.
 la_status run(const Common& c, ChunkArgs& ka, const void* q, int64_t q_st, int64_t q_sh, const void* k, int64_t k_st,
               int64_t k_sh, const void* v, int64_t v_st, int64_t v_sh, int64_t ckpt_n, void* workspace,
-              size_t workspace_bytes, int32_t* user_status, int mode, cudaStream_t stream) {
+              size_t workspace_bytes, int32_t* user_status, int mode, cudaStream_t stream, int32_t gdp_n = 1) {
     void* ws = nullptr;
     la_status st = resolve_workspace(workspace, workspace_bytes, c.N, &ws);
     if (st != LA_OK) return st;
@@ -222,11 +225,13 @@ la_status run(const Common& c, ChunkArgs& ka, const void* q, int64_t q_st, int64
     std::memset(&vm, 0, sizeof(vm));
     std::memset(&om, 0, sizeof(om));
     const int64_t Tm = c.T > 0 ? c.T : 1;  // descriptors need a non-empty extent
+    const uint32_t qrows = static_cast<uint32_t>(la::kChunk / gdp_n);
+    ka.gdp_n = gdp_n;
     if (c.T > 0) {
-        if ((st = make_map(&km, k, Tm, c.HK, c.K, k_st, k_sh)) != LA_OK) return st;
-        if ((st = make_map(&vm, v, Tm, c.HV, c.V, v_st, v_sh)) != LA_OK) return st;
+        if ((st = make_map(&km, k, Tm * gdp_n, c.HK, c.K, k_st, k_sh)) != LA_OK) return st;
+        if ((st = make_map(&vm, v, Tm * gdp_n, c.HV, c.V, v_st, v_sh)) != LA_OK) return st;
         if (q) {
-            if ((st = make_map(&qm, q, Tm, c.HK, c.K, q_st, q_sh)) != LA_OK) return st;
+            if ((st = make_map(&qm, q, Tm, c.HK, c.K, q_st, q_sh, qrows)) != LA_OK) return st;
         } else {
             qm = km;
         }
@@ -234,7 +239,7 @@ la_status run(const Common& c, ChunkArgs& ka, const void* q, int64_t q_st, int64
         // the kernel stores it element by element
         ka.o_tma = 0;
         if (ka.o && aligned(ka.o, 16) && ka.o_st % 8 == 0 && (c.HV == 1 || ka.o_sh % 8 == 0) &&
-            make_map(&om, ka.o, Tm, c.HV, c.V, ka.o_st, ka.o_sh) == LA_OK)
+            make_map(&om, ka.o, Tm, c.HV, c.V, ka.o_st, ka.o_sh, qrows) == LA_OK)
             ka.o_tma = 1;
     }
     cudaEvent_t ev0 = t_timing_start, ev1 = t_timing_stop;
@@ -283,6 +288,7 @@ la_status static_scratch_address(void** out) {
 
 namespace {
 la_status gdp_fwd(const la_gdn_fwd_params* p, void* stream);  // Gated DeltaProduct, below
+la_status fwd_impl(const la_gdn_fwd_params* p, void* stream, int32_t gdp_n);
 }  // namespace
 
 extern "C" {
@@ -291,6 +297,14 @@ la_status gdn_fwd(const la_gdn_fwd_params* p, void* stream) {
     if (!p) return LA_ERR_INVALID_ARG;
     if (p->num_householder > 1) return gdp_fwd(p, stream);
     if (p->num_householder < 0) return LA_ERR_INVALID_ARG;
+    return fwd_impl(p, stream, 1);
+}
+
+}  // extern "C"
+
+namespace {
+// The forward (gdp_n = 1) or Gated DeltaProduct natively on the update timeline (gdp_n = 2, 4, 8).
+la_status fwd_impl(const la_gdn_fwd_params* p, void* stream, int32_t gdp_n) {
     Common c{p->T, p->N, p->HK, p->HV, p->K, p->V, p->cu_seqlens, p->cu_seqlens_bits, p->g, p->beta,
              p->beta_bf16 ? 2 : 4};
     la_status st = check_common(c);
@@ -308,10 +322,12 @@ la_status gdn_fwd(const la_gdn_fwd_params* p, void* stream) {
     }
     if (p->final_state && !aligned(p->final_state, 4)) return LA_ERR_INVALID_ARG;
     if (p->checkpoints) {
-        if (p->checkpoint_every_n <= 0 || p->checkpoint_every_n % la::kChunk != 0) return LA_ERR_INVALID_ARG;
+        // a multiple of the chunk on the timeline the kernel walks (GDP: n update rows per token)
+        if (p->checkpoint_every_n <= 0 || (p->checkpoint_every_n * gdp_n) % la::kChunk != 0) return LA_ERR_INVALID_ARG;
         if (p->checkpoint_dtype != LA_DTYPE_F32 && p->checkpoint_dtype != LA_DTYPE_BF16) return LA_ERR_UNSUPPORTED;
         if (!aligned(p->checkpoints, p->checkpoint_dtype == LA_DTYPE_F32 ? 4 : 2)) return LA_ERR_INVALID_ARG;
     }
+    if (gdp_n > 1 && p->T > 0 && p->T * gdp_n >= (int64_t(1) << 31) - 64) return LA_ERR_UNSUPPORTED;
     ChunkArgs ka;
     std::memset(&ka, 0, sizeof(ka));
     ka.g_st = p->g_stride_t;
@@ -328,7 +344,7 @@ la_status gdn_fwd(const la_gdn_fwd_params* p, void* stream) {
     ka.final_state = p->final_state;
     ka.ckpt = p->checkpoints;
     ka.ckpt_bf16 = p->checkpoint_dtype == LA_DTYPE_BF16;
-    ka.ckpt_n = p->checkpoints ? p->checkpoint_every_n : 0;
+    ka.ckpt_n = p->checkpoints ? p->checkpoint_every_n * gdp_n : 0;  // on the update timeline
     ka.transition = nullptr;
     ka.tiles_per_head = 1;
     if ((st = set_transforms(ka, p->gate_mode, p->a_log, p->dt_bias, p->gate_lower_bound, p->beta_sigmoid,
@@ -345,9 +361,12 @@ la_status gdn_fwd(const la_gdn_fwd_params* p, void* stream) {
         ka.final_bf16 = p->initial_state_dtype == LA_DTYPE_BF16;
     }
     return run(c, ka, p->q, p->q_stride_t, p->q_stride_h, p->k, p->k_stride_t, p->k_stride_h, p->v, p->v_stride_t,
-               p->v_stride_h, ka.ckpt_n, p->workspace, p->workspace_bytes, p->status, la::kModeFwd,
-               static_cast<cudaStream_t>(stream));
+               p->v_stride_h, p->checkpoints ? p->checkpoint_every_n : 0, p->workspace, p->workspace_bytes,
+               p->status, gdp_n > 1 ? la::kModeGdp : la::kModeFwd, static_cast<cudaStream_t>(stream), gdp_n);
 }
+}  // namespace
+
+extern "C" {
 
 la_status gdn_decode(const la_gdn_decode_params* p, void* stream) {
     if (!p) return LA_ERR_INVALID_ARG;
@@ -431,6 +450,10 @@ namespace {
 // per-token outputs.
 la_status gdp_fwd(const la_gdn_fwd_params* p, void* stream) {
     const int32_t n = p->num_householder;
+    // n = 2, 4, 8: natively on the update timeline (q, g, o read and written on the token
+    // timeline by the chunk kernel); other n: the timeline's query, gate and output rows are
+    // materialised below and the plain forward runs on it
+    if (n == 2 || n == 4 || n == 8) return fwd_impl(p, stream, n);
     if (p->N < 0 || p->HK <= 0 || p->HV <= 0 || p->T < 0) return LA_ERR_INVALID_ARG;
     if ((p->K != 64 && p->K != 128) || (p->V != 64 && p->V != 128)) return LA_ERR_UNSUPPORTED;
     if (p->HV % p->HK != 0) return LA_ERR_UNSUPPORTED;

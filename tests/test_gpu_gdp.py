@@ -59,6 +59,48 @@ def test_gdp_two_updates_checkpoints_grouped_heads():
     assert errs["o"] <= O_TOL and errs["final"] <= S_TOL and errs["ckpt"] <= S_TOL, errs
 
 
+@pytest.mark.parametrize("n,K,V", [(4, 128, 128), (8, 64, 128), (4, 64, 64)])
+def test_gdp_native_timeline_ragged(n, K, V):
+    """n = 4, 8 (the chunk kernel reads the queries and gates per token and writes the outputs per
+    token; 64 / n tokens per chunk): ragged sequences that end inside a chunk, a one-token
+    sequence, grouped heads, checkpoints every 16 tokens, a start state."""
+    c = gdp_case([1, 15, 16, 17, 70], n, 2, 4, K, V, seed=521 + n + K + V)
+    d = dev()
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    ck_n = 64 // n
+    o, fin, ck = la.gdn_fwd(c["q"].to(d), c["k"].to(d), c["v"].to(d), c["g"].to(d), c["beta"].to(d), c["cu"].to(d),
+                            initial_state=c["s0"].to(d), checkpoint_every_n=ck_n, checkpoint_dtype=torch.float32,
+                            num_householder=n, status=status)
+    assert la.read_status(status) == 0
+    ref = oracle.gdp_fwd(c["q"], c["k"], c["v"], c["g"], c["beta"], c["cu"], n, initial_state=c["s0"],
+                         checkpoint_every_n=ck_n)
+    errs = {"o": rel(o.float().cpu(), ref["o"]), "final": rel(fin.cpu(), ref["final_state"]),
+            "ckpt": rel(ck.cpu(), ref["checkpoints"])}
+    print(f"[parity] gdp n={n} K={K} V={V}: " + ", ".join(f"{k_} {v_:.2e}" for k_, v_ in errs.items()))
+    assert errs["o"] <= O_TOL and errs["final"] <= S_TOL and errs["ckpt"] <= S_TOL, errs
+
+
+def test_gdp_native_bounded_gate_beta_logits_page_distributions():
+    """n = 2 with the pages' fast decay, the bounded sigmoid gate and beta logits."""
+    n = 2
+    c = gdp_case([200, 64, 33], n, 1, 1, 128, 128, seed=531, slow=False)
+    gen = torch.Generator().manual_seed(532)
+    g_raw = torch.randn(c["q"].shape[0], 1, generator=gen)
+    b_raw = torch.randn(c["k"].shape[0], 1, generator=gen)
+    d = dev()
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    o, fin, _ = la.gdn_fwd(c["q"].to(d), c["k"].to(d), c["v"].to(d), g_raw.to(d), b_raw.to(d), c["cu"].to(d),
+                           initial_state=c["s0"].to(d), num_householder=n, gate_lower_bound=-3.0,
+                           beta_sigmoid=True, status=status)
+    assert la.read_status(status) == 0
+    g_log = oracle.gate_transform(g_raw, gate="sigmoid_bound", gate_lower_bound=-3.0)
+    b = oracle.beta_transform(b_raw, beta_sigmoid=True)
+    ref = oracle.gdp_fwd(c["q"], c["k"], c["v"], g_log, b, c["cu"], n, initial_state=c["s0"])
+    errs = {"o": rel(o.float().cpu(), ref["o"]), "final": rel(fin.cpu(), ref["final_state"])}
+    print("[parity] gdp n=2 bounded gate: " + ", ".join(f"{k_} {v_:.2e}" for k_, v_ in errs.items()))
+    assert errs["o"] <= O_TOL and errs["final"] <= S_TOL, errs
+
+
 def test_gdp_three_updates_token_major_transforms():
     """n = 3 (chunks end inside tokens), token-major [T, n, H, D] inputs, the softplus gate and
     beta logits in the kernel."""
