@@ -69,7 +69,9 @@ def compare(w, got, ref, units=None, label=""):
 
 @pytest.mark.parametrize("K,V", [(64, 64), (128, 128), (64, 128), (128, 64)])
 def test_bwd_ragged_grouped_heads(K, V):
-    w = W.draw("bwd ragged", [1, 63, 64, 65, 200], 2, 4, K, V, seed=401 + K + V, initial_state=True,
+    """Ragged sequences (one token, a chunk +- 1, an empty one, several chunks), grouped heads,
+    a start state and a final-state cotangent, slow decay."""
+    w = W.draw("bwd ragged", [1, 63, 0, 64, 65, 200], 2, 4, K, V, seed=401 + K + V, initial_state=True,
                slow_decay=True)
     do, dfin = cotangents(w, 402)
     got = run_bwd(w, do, dfin)
