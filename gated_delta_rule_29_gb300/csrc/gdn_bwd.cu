@@ -29,10 +29,17 @@
 // Every product runs on warp-level tensor-core MMAs (m16n8k8, tf32 operands, fp32
 // accumulation) with each inexact fp32 operand split into a tf32 head and a tf32 remainder:
 // three products per MMA (head x head, head x rest, rest x head), two when one operand is an
-// exact bf16 input (k, q, dO), which keeps fp32-level accuracy.  The dK and dQ rows stay in
-// the warps' accumulator fragments for the whole chunk: warps 0-3 own dK rows 16 w .. 16 w +
-// 15, warps 4-7 the same dQ rows.  The chunk entering states come from the forward kernel run
-// with fp32 checkpoints every 64 tokens.
+// exact bf16 input (k, q, dO), which keeps fp32-level accuracy; the products that reach only
+// the bf16 dq and dk take one MMA on rounded operands.  The dK and dQ rows stay in the warps'
+// accumulator fragments for the whole chunk: warps 0-3 own dK rows 16 w .. 16 w + 15, warps 4-7
+// the same dQ rows.  The chunk entering states come from the forward kernel run with fp32
+// checkpoints every 64 tokens.  With the forward's input transforms the gate and beta are
+// transformed as they are loaded and dg, dbeta go back through the chain rule (d_a_log and
+// d_dt_bias are per-unit sums added in sequence order by a second small kernel).
+//
+// State-only mode (gdn_summary_bwd): the recursion of dS needs no forward state, so only
+// K dS, dD, dY and the dS update run per tile, no checkpoints are read, and the gradient
+// entering the span is the result.
 #include <cuda_bf16.h>
 
 #include "../../include/liblinattn.h"
