@@ -201,3 +201,15 @@ def test_bwd_bounded_gate_bf16_beta_logits():
     ref = oracle.gdn_bwd(w.q, w.k, w.v, g_raw, b_logit.float(), w.cu_seqlens, do, initial_state=w.initial_state,
                          d_final_state=dfin, gate="sigmoid_bound", gate_lower_bound=-0.1, beta_sigmoid=True)
     compare(w, got, ref, label=" bounded gate + bf16 beta logits")
+
+
+def test_bwd_bf16_start_state_regenerated_checkpoints():
+    """A bf16 start state: the regenerated forward reads it as given, and the gradient with
+    respect to it comes back in fp32."""
+    w = W.draw("bwd bf16 s0", [96, 200], 2, 2, 128, 64, seed=481, initial_state=True, slow_decay=True)
+    w.initial_state = w.initial_state.to(torch.bfloat16)
+    do, dfin = cotangents(w, 482)
+    got = run_bwd(w, do, dfin)
+    ref = oracle.gdn_bwd(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, do, initial_state=w.initial_state.float(),
+                         d_final_state=dfin)
+    compare(w, got, ref, label=" bf16 start state")

@@ -132,3 +132,27 @@ def test_gdp_one_update_is_gdn_bitwise():
     o1, f1, _ = la.gdn_fwd(*args, initial_state=c["s0"].to(d))
     o2, f2, _ = la.gdn_fwd(*args, initial_state=c["s0"].to(d), num_householder=1)
     assert torch.equal(o1, o2) and torch.equal(f1, f2)
+
+
+def test_gdp_native_with_state_pool():
+    """n = 2 natively with a state pool: each sequence starts from its slot and its end state goes
+    back into that slot (the other slots untouched)."""
+    n = 2
+    c = gdp_case([40, 1, 97], n, 1, 2, 128, 128, seed=541)
+    d = dev()
+    gen = torch.Generator().manual_seed(542)
+    P = 6
+    pool = 0.1 * torch.randn(P, 2, 128, 128, generator=gen)
+    idx = torch.tensor([4, 0, 2], dtype=torch.int32)
+    pool_d = pool.to(d)
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    o, _, _ = la.gdn_fwd(c["q"].to(d), c["k"].to(d), c["v"].to(d), c["g"].to(d), c["beta"].to(d), c["cu"].to(d),
+                         initial_state=pool_d, state_indices=idx.to(d), num_householder=n, status=status)
+    assert la.read_status(status) == 0
+    ref = oracle.gdp_fwd(c["q"], c["k"], c["v"], c["g"], c["beta"], c["cu"], n, initial_state=pool[idx.long()])
+    got_pool = pool_d.cpu()
+    errs = {"o": rel(o.float().cpu(), ref["o"]), "slots": rel(got_pool[idx.long()], ref["final_state"])}
+    print("[parity] gdp n=2 state pool: " + ", ".join(f"{k_} {v_:.2e}" for k_, v_ in errs.items()))
+    assert errs["o"] <= O_TOL and errs["slots"] <= S_TOL, errs
+    untouched = [i for i in range(P) if i not in idx.tolist()]
+    assert torch.equal(got_pool[untouched], pool[untouched])
