@@ -235,11 +235,13 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
         const int fn = static_cast<int>(L - static_cast<int64_t>(cc) * kC < kC ? L - static_cast<int64_t>(cc) * kC : kC);
         if (!so) {
             const float* Sf = a.ckpt + ((a.ckpt_off[seq] + cc) * HO + h) * KV;
+#pragma unroll
             for (int e = tid; e < KD * kVT; e += kBT) {
                 const int r = e / kVT, col = e % kVT;
                 cp_async4(&s.SJ[pb][col * PK + colp<KD>(r)], Sf + r * VD + j0 + col);
             }
         }
+#pragma unroll
         for (int e = tid; e < KD * kVT; e += kBT) {
             const int r = e / kVT, col = e % kVT;
             cp_async4(&s.dSJ[pb][col * PK + colp<KD>(r)], dSg + r * VD + j0 + col);
@@ -284,23 +286,35 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
         const int n = static_cast<int>(L - static_cast<int64_t>(c) * kC < kC ? L - static_cast<int64_t>(c) * kC : kC);
 
         // ---- chunk-level quantities: raw rows, norms, decays, Gk, P, T
-        for (int e = tid; e < kC * KD / 8; e += kBT) {
-            // 8 bf16 (16 bytes) per load: k and q rows are 16-byte aligned (TMA operand rules)
-            const int i = e / (KD / 8), d = (e % (KD / 8)) * 8;
-            uint4 kw = make_uint4(0u, 0u, 0u, 0u), qw = kw;
-            if (i < n) {
-                kw = *reinterpret_cast<const uint4*>(a.k + (t0 + i) * a.k_st + hk * a.k_sh + d);
-                qw = *reinterpret_cast<const uint4*>(a.q + (t0 + i) * a.q_st + hk * a.q_sh + d);
-            }
-            float* kd = &s.Kr[i * PK + colp<KD>(d)];
-            float* qd = &s.Qr[i * PK + colp<KD>(d)];
-            const uint32_t kk[4] = {kw.x, kw.y, kw.z, kw.w}, qq[4] = {qw.x, qw.y, qw.z, qw.w};
+        {
+            // 8 bf16 (16 bytes) per load (k and q rows are 16-byte aligned: TMA operand rules);
+            // every load of the thread is issued before the first is used
+            constexpr int LPT = kC * KD / 8 / kBT;  // 16-byte pieces per thread and matrix
+            uint4 kw[LPT], qw[LPT];
 #pragma unroll
-            for (int x = 0; x < 4; ++x) {
-                kd[2 * x] = __uint_as_float(kk[x] << 16);
-                kd[2 * x + 1] = __uint_as_float(kk[x] & 0xFFFF0000u);
-                qd[2 * x] = __uint_as_float(qq[x] << 16);
-                qd[2 * x + 1] = __uint_as_float(qq[x] & 0xFFFF0000u);
+            for (int x = 0; x < LPT; ++x) {
+                const int e = tid + x * kBT;
+                const int i = e / (KD / 8), d = (e % (KD / 8)) * 8;
+                kw[x] = qw[x] = make_uint4(0u, 0u, 0u, 0u);
+                if (i < n) {
+                    kw[x] = *reinterpret_cast<const uint4*>(a.k + (t0 + i) * a.k_st + hk * a.k_sh + d);
+                    qw[x] = *reinterpret_cast<const uint4*>(a.q + (t0 + i) * a.q_st + hk * a.q_sh + d);
+                }
+            }
+#pragma unroll
+            for (int x = 0; x < LPT; ++x) {
+                const int e = tid + x * kBT;
+                const int i = e / (KD / 8), d = (e % (KD / 8)) * 8;
+                float* kd = &s.Kr[i * PK + colp<KD>(d)];
+                float* qd = &s.Qr[i * PK + colp<KD>(d)];
+                const uint32_t kk[4] = {kw[x].x, kw[x].y, kw[x].z, kw[x].w}, qq[4] = {qw[x].x, qw[x].y, qw[x].z, qw[x].w};
+#pragma unroll
+                for (int y = 0; y < 4; ++y) {
+                    kd[2 * y] = __uint_as_float(kk[y] << 16);
+                    kd[2 * y + 1] = __uint_as_float(kk[y] & 0xFFFF0000u);
+                    qd[2 * y] = __uint_as_float(qq[y] << 16);
+                    qd[2 * y + 1] = __uint_as_float(qq[y] & 0xFFFF0000u);
+                }
             }
         }
         if (tid < kC) {
@@ -364,7 +378,9 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
         }
         // Gk = rk_i rk_j (k_i . k_j) Gamma_ij and P = rq_i rk_j (q_i . k_j) Gamma_ij on the
         // lower 16 x 8 tiles (the raw rows are exact in tf32: one product per MMA)
-        for (int job = w; job < 40; job += 8) {
+#pragma unroll
+        for (int jx = 0; jx < 5; ++jx) {  // five of the 40 (tile, product) jobs per warp
+            const int job = w + 8 * jx;
             int mt, nt;
             lower_tile(job >> 1, mt, nt);
             const bool isP = job & 1;
