@@ -21,6 +21,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -76,11 +77,18 @@ def load_peaks():
 TRAFFIC_SOURCES = ("gdn_chunk.cu", "gdn_prologue.cu", "ptx.cuh", "la_api.cu")
 
 
+def _code_only(text):
+    """C++ source without comments or blank lines (a comment edit does not change the kernel)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = [re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines()]
+    return "\n".join(ln for ln in lines if ln.strip())
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     d = os.path.join(ROOT, "gated_delta_rule_29_gb300", "csrc")
     for name in TRAFFIC_SOURCES:
-        h.update(open(os.path.join(d, name), "rb").read())
+        h.update(_code_only(open(os.path.join(d, name)).read()).encode())
     return h.hexdigest()[:16]
 
 

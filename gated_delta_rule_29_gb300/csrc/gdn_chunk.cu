@@ -30,6 +30,13 @@
 // Tiles: a forward unit has one value tile.  A summary unit has a value tile
 // (the span end state from the given start) and a transition tile: the same
 // recurrence on P with v = 0 and P0 = I, stored transposed.
+//
+// Gated DeltaProduct (mode kModeGdp, n = 2, 4, 8 updates per token): the same
+// recurrence walked on the update timeline (n rows per token of k, v, beta; a
+// token's gate at its first update, no decay at the others).  A 64-row chunk holds
+// 64 / n tokens, whose queries occupy the first rows of the query half of the K/Q
+// tile; query row i is read after its token's last update row i n + n - 1, and the
+// output tile's 64 / n rows go to the token rows of o.
 #include <cuda_bf16.h>
 
 #include "../../include/liblinattn.h"
