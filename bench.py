@@ -814,10 +814,14 @@ def run_summary_bench(args, world, rank, local):
             "config": {"workload": "summary: one sequence of 131072 tokens, 8 spans of 16384, H=16, K=V=128, zero start",
                        "global_batch": 1, "seq_len": T, "parallelism": "single GPU",
                        "l2": "inputs larger than L2 (1.07 GB of k/v per step); no flush"},
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": None, "peak_source": peak_src,
-                         "kernel": "gdn_chunk_kernel<128, summary>", "kernel_ms": kern_ms, "algorithmic_bytes": alg,
-                         "tensor_tflops": tflops, "tensor_frac": tflops / tc_peak, "algorithmic_flops": flops},
+            # the binding roof: bytes at the copy bandwidth or the products at the bf16 rate
+            "roofline": ({"bound": "tensor", "achieved": tflops, "peak": tc_peak, "unit": "TFLOP/s",
+                          "frac": tflops / tc_peak, "hbm_gbs": achieved, "hbm_frac": achieved / hbm_peak}
+                         if flops / (tc_peak * 1e12) > alg / (hbm_peak * 1e9) else
+                         {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                          "frac": achieved / hbm_peak, "tensor_tflops": tflops, "tensor_frac": tflops / tc_peak})
+                        | {"traffic": None, "peak_source": peak_src, "kernel": "gdn_chunk_kernel<128, summary>",
+                           "kernel_ms": kern_ms, "algorithmic_bytes": alg, "algorithmic_flops": flops},
             "cpu_baseline": cpu,
             "e2e": None,
             "gpu_launches": 2 * args.steps,
