@@ -8,6 +8,7 @@ into the C structs and launch on the current CUDA stream.  There is no CPU fallb
 from .api import (checkpoint_rows, gdn_bwd, gdn_decode, gdn_fwd, gdn_fwd_host, gdn_summary,  # noqa: F401
                   gdn_summary_bwd, read_status, workspace_bytes)
 from . import binding  # noqa: F401
+from .autograd import gdn_attention  # noqa: F401
 
-__all__ = ["gdn_fwd", "gdn_fwd_host", "gdn_summary", "gdn_summary_bwd", "gdn_decode", "gdn_bwd", "read_status",
-           "checkpoint_rows", "workspace_bytes", "binding"]
+__all__ = ["gdn_fwd", "gdn_fwd_host", "gdn_summary", "gdn_summary_bwd", "gdn_decode", "gdn_bwd", "gdn_attention",
+           "read_status", "checkpoint_rows", "workspace_bytes", "binding"]
