@@ -372,10 +372,12 @@ __global__ void __launch_bounds__(kCta, 2)
     constexpr bool kFwd = MODE != kModeSummary;  // queries and outputs (the forward, or GDP's)
     constexpr bool kGdp = MODE == kModeGdp;
     constexpr int KP = KD / 16;  // 16-column pieces of the state
-    // GDP: a chunk of 64 update rows holds QR tokens; their queries fill rows 0 .. QR-1 of the
-    // query half of the K/Q tile (the other rows stay zero) and their outputs columns 0 .. QR-1
+    // GDP: the tokens whose last update row falls in a chunk of 64 update rows (at most QR of
+    // them) have their queries in rows 0 .. QR-1 of the query half of the K/Q tile (the other
+    // rows stay zero) and their outputs in columns 0 .. QR-1; when n does not divide 64 a chunk
+    // begins or ends inside a token
     const int NH = kGdp ? a.gdp_n : 1;
-    const int QR = kChunk / NH;
+    const int QR = (kChunk + NH - 1) / NH;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Scalars& sc = *reinterpret_cast<Scalars*>(sm + SM_SC);
@@ -587,7 +589,9 @@ __global__ void __launch_bounds__(kCta, 2)
             const int n = left < kChunk ? static_cast<int>(left) : kChunk;
             const bool last = c + 1 == nchunks;
             const bool o_tma_chunk = kFwd && a.o_tma && n == kChunk;
-            const int64_t tok0 = t0 / NH;  // the chunk's first token (its query and output rows)
+            // the chunk's query tokens: tok0 .. tok0 + nq - 1, those whose last update row is in it
+            const int64_t tok0 = t0 / NH;
+            const int nq = kGdp ? static_cast<int>((t0 + n) / NH - tok0) : n;
             const float g_cur = g_nx, b_cur = b_nx;
             if (!last) {
                 g_nx = b_nx = 0.f;
@@ -658,7 +662,7 @@ __global__ void __launch_bounds__(kCta, 2)
                     for (int e = 0; e < 32; ++e) nrm = (e == lane) ? d32[e] : nrm;
                 }
                 const int row = r & 63;
-                const int nvalid = (r < 64) ? n : n / NH;  // key rows, or the chunk's query tokens
+                const int nvalid = (r < 64) ? n : nq;  // key rows, or the chunk's query tokens
                 const float inv = (row < nvalid) ? (a.l2norm ? 1.0f / sqrtf(nrm + 1e-6f) : 1.f) : 0.f;
                 if (r < 64) sc.rk[row] = inv;
                 else sc.rq[row] = inv;
@@ -703,11 +707,11 @@ __global__ void __launch_bounds__(kCta, 2)
                 sc.u[i] = rk * exp2f(b31 - bi);
                 sc.cA[i] = bet * rk * e;
                 if (kGdp) {
-                    // query row i is token i of the chunk, read after its last update row ri
-                    const int ri = i * NH + NH - 1;
-                    const float bq = ri < 64 ? sc.bw[ri] + (ri >= 32 ? sc.bw[31] : 0.f) : 0.f;
-                    sc.sq[i] = ri < 64 ? a.scale * rq * exp2f(bq) : 0.f;
-                    sc.cP[i] = ri < 64 ? a.scale * rq * exp2f(bq - b31) : 0.f;
+                    // query row i is token tok0 + i, read after its last update row ri of the chunk
+                    const int ri = i < nq ? static_cast<int>((tok0 + i) * NH + NH - 1 - t0) : -1;
+                    const float bq = ri >= 0 ? sc.bw[ri] + (ri >= 32 ? sc.bw[31] : 0.f) : 0.f;
+                    sc.sq[i] = ri >= 0 ? a.scale * rq * exp2f(bq) : 0.f;
+                    sc.cP[i] = ri >= 0 ? a.scale * rq * exp2f(bq - b31) : 0.f;
                 } else {
                     sc.sq[i] = a.scale * rq * gam;
                     sc.cP[i] = a.scale * rq * e;
@@ -723,7 +727,7 @@ __global__ void __launch_bounds__(kCta, 2)
                 const float ci = fast ? (is_a ? sc.cA[i] : sc.cP[i]) : (is_a ? sc.bet[i] * sc.rk[i] : a.scale * sc.rq[i]);
                 // the row's position on the update timeline (GDP query rows: the token's last update;
                 // rows past the chunk's tokens are zero and fully masked)
-                const int ip = (kGdp && !is_a) ? (i < QR ? i * NH + NH - 1 : -1) : i;
+                const int ip = (kGdp && !is_a) ? (i < nq ? static_cast<int>((tok0 + i) * NH + NH - 1 - t0) : -1) : i;
                 const float bi = sc.b[ip < 0 ? 0 : ip];
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
@@ -950,7 +954,7 @@ __global__ void __launch_bounds__(kCta, 2)
                         const uint32_t vchunk = (r & 63) >> 3;
 #pragma unroll
                         for (int i = 0; i < 64; ++i)
-                            if (!kGdp || i < QR)
+                            if (!kGdp || i < QR)  // (the bulk store needs 64 / n whole tokens: n divides 64)
                                 *reinterpret_cast<uint16_t*>(col + sw128_off(i, vchunk)) = f_to_bf16_bits(o64[i]);
                     }
                     fence_proxy_async_smem();
@@ -962,7 +966,6 @@ __global__ void __launch_bounds__(kCta, 2)
                     }
                 } else if (r < a.V) {
                     uint16_t* op = a.o + tok0 * a.o_st + static_cast<int64_t>(h) * a.o_sh + r;
-                    const int nq = n / NH;
 #pragma unroll
                     for (int i = 0; i < 64; ++i)
                         if (i < nq) op[static_cast<int64_t>(i) * a.o_st] = f_to_bf16_bits(o64[i]);

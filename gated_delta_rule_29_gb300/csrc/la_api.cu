@@ -225,7 +225,7 @@ la_status run(const Common& c, ChunkArgs& ka, const void* q, int64_t q_st, int64
     std::memset(&vm, 0, sizeof(vm));
     std::memset(&om, 0, sizeof(om));
     const int64_t Tm = c.T > 0 ? c.T : 1;  // descriptors need a non-empty extent
-    const uint32_t qrows = static_cast<uint32_t>(la::kChunk / gdp_n);
+    const uint32_t qrows = static_cast<uint32_t>((la::kChunk + gdp_n - 1) / gdp_n);
     ka.gdp_n = gdp_n;
     if (c.T > 0) {
         if ((st = make_map(&km, k, Tm * gdp_n, c.HK, c.K, k_st, k_sh)) != LA_OK) return st;
@@ -237,9 +237,10 @@ la_status run(const Common& c, ChunkArgs& ka, const void* q, int64_t q_st, int64
         }
         // o goes out by TMA stores when its layout allows (16-byte base and strides); otherwise
         // the kernel stores it element by element
+        // (GDP: only when n divides 64, so that every full chunk holds 64 / n whole tokens)
         ka.o_tma = 0;
         if (ka.o && aligned(ka.o, 16) && ka.o_st % 8 == 0 && (c.HV == 1 || ka.o_sh % 8 == 0) &&
-            make_map(&om, ka.o, Tm, c.HV, c.V, ka.o_st, ka.o_sh, qrows) == LA_OK)
+            la::kChunk % gdp_n == 0 && make_map(&om, ka.o, Tm, c.HV, c.V, ka.o_st, ka.o_sh, qrows) == LA_OK)
             ka.o_tma = 1;
     }
     cudaEvent_t ev0 = t_timing_start, ev1 = t_timing_stop;
@@ -303,7 +304,7 @@ la_status gdn_fwd(const la_gdn_fwd_params* p, void* stream) {
 }  // extern "C"
 
 namespace {
-// The forward (gdp_n = 1) or Gated DeltaProduct natively on the update timeline (gdp_n = 2, 4, 8).
+// The forward (gdp_n = 1) or Gated DeltaProduct natively on the update timeline (2 <= gdp_n <= 64).
 la_status fwd_impl(const la_gdn_fwd_params* p, void* stream, int32_t gdp_n) {
     Common c{p->T, p->N, p->HK, p->HV, p->K, p->V, p->cu_seqlens, p->cu_seqlens_bits, p->g, p->beta,
              p->beta_bf16 ? 2 : 4};
@@ -450,10 +451,10 @@ namespace {
 // per-token outputs.
 la_status gdp_fwd(const la_gdn_fwd_params* p, void* stream) {
     const int32_t n = p->num_householder;
-    // n = 2, 4, 8: natively on the update timeline (q, g, o read and written on the token
-    // timeline by the chunk kernel); other n: the timeline's query, gate and output rows are
+    // n <= 64: natively on the update timeline (q, g, o read and written on the token timeline
+    // by the chunk kernel); larger n: the timeline's query, gate and output rows are
     // materialised below and the plain forward runs on it
-    if (n == 2 || n == 4 || n == 8) return fwd_impl(p, stream, n);
+    if (n <= la::kChunk) return fwd_impl(p, stream, n);
     if (p->N < 0 || p->HK <= 0 || p->HV <= 0 || p->T < 0) return LA_ERR_INVALID_ARG;
     if ((p->K != 64 && p->K != 128) || (p->V != 64 && p->V != 128)) return LA_ERR_UNSUPPORTED;
     if (p->HV % p->HK != 0) return LA_ERR_UNSUPPORTED;

@@ -59,15 +59,17 @@ def test_gdp_two_updates_checkpoints_grouped_heads():
     assert errs["o"] <= O_TOL and errs["final"] <= S_TOL and errs["ckpt"] <= S_TOL, errs
 
 
-@pytest.mark.parametrize("n,K,V", [(4, 128, 128), (8, 64, 128), (4, 64, 64)])
+@pytest.mark.parametrize("n,K,V", [(4, 128, 128), (8, 64, 128), (4, 64, 64), (3, 128, 128), (5, 64, 64),
+                                   (7, 128, 64)])
 def test_gdp_native_timeline_ragged(n, K, V):
-    """n = 4, 8 (the chunk kernel reads the queries and gates per token and writes the outputs per
-    token; 64 / n tokens per chunk): ragged sequences that end inside a chunk, a one-token
-    sequence, grouped heads, checkpoints every 16 tokens, a start state."""
+    """The chunk kernel reads the queries and gates per token and writes the outputs per token
+    (n = 4, 8: 64 / n tokens per chunk; n = 3, 5, 7: chunks begin and end inside tokens): ragged
+    sequences that end inside a chunk, a one-token sequence, grouped heads, checkpoints, a start
+    state."""
     c = gdp_case([1, 15, 16, 17, 70], n, 2, 4, K, V, seed=521 + n + K + V)
     d = dev()
     status = torch.zeros(1, dtype=torch.int32, device=d)
-    ck_n = 64 // n
+    ck_n = 64 // n if 64 % n == 0 else 64
     o, fin, ck = la.gdn_fwd(c["q"].to(d), c["k"].to(d), c["v"].to(d), c["g"].to(d), c["beta"].to(d), c["cu"].to(d),
                             initial_state=c["s0"].to(d), checkpoint_every_n=ck_n, checkpoint_dtype=torch.float32,
                             num_householder=n, status=status)
