@@ -31,12 +31,12 @@
 // (the span end state from the given start) and a transition tile: the same
 // recurrence on P with v = 0 and P0 = I, stored transposed.
 //
-// Gated DeltaProduct (mode kModeGdp, n = 2, 4, 8 updates per token): the same
+// Gated DeltaProduct (mode kModeGdp, 2 <= n <= 64 updates per token): the same
 // recurrence walked on the update timeline (n rows per token of k, v, beta; a
-// token's gate at its first update, no decay at the others).  A 64-row chunk holds
-// 64 / n tokens, whose queries occupy the first rows of the query half of the K/Q
-// tile; query row i is read after its token's last update row i n + n - 1, and the
-// output tile's 64 / n rows go to the token rows of o.
+// token's gate at its first update, no decay at the others).  A 64-row chunk's
+// query tokens are those whose last update row lies in it; their queries occupy
+// the first rows of the query half of the K/Q tile, each read after its token's
+// last update row, and the outputs go to the token rows of o.
 #include <cuda_bf16.h>
 
 #include "../../include/liblinattn.h"

@@ -5,9 +5,10 @@
 // Per token t the state decays once, takes the token's n delta updates in order, and the
 // output reads the state after the last one.  That is the GDN recurrence on the update
 // timeline (T * n steps) with the log decay g_t at each token's first update and 0 at the
-// others, and the query at each token's last update.  These kernels build that timeline
-// (query rows, gate rows, sequence boundaries) so the chunk kernel runs it unchanged, and
-// gather the per-token outputs afterwards.
+// others, and the query at each token's last update.  The chunk kernel walks that timeline
+// natively for n <= 64; for larger n these kernels build it (query rows, gate rows, sequence
+// boundaries) so the plain forward runs it unchanged, and gather the per-token outputs
+// afterwards.
 #include <cuda_bf16.h>
 
 #include "../../include/liblinattn.h"
