@@ -590,8 +590,11 @@ __global__ void __launch_bounds__(kCta, 2)
             const bool last = c + 1 == nchunks;
             const bool o_tma_chunk = kFwd && a.o_tma && n == kChunk;
             // the chunk's query tokens: tok0 .. tok0 + nq - 1, those whose last update row is in it
-            const int64_t tok0 = t0 / NH;
-            const int nq = kGdp ? static_cast<int>((t0 + n) / NH - tok0) : n;
+            // (32-bit arithmetic relative to the sequence start, which is a token boundary)
+            const int rel0 = c * kChunk;
+            const int tq0 = kGdp ? rel0 / NH : rel0;
+            const int64_t tok0 = tok_s + tq0;
+            const int nq = kGdp ? (rel0 + n) / NH - tq0 : n;
             const float g_cur = g_nx, b_cur = b_nx;
             if (!last) {
                 g_nx = b_nx = 0.f;
@@ -708,7 +711,7 @@ __global__ void __launch_bounds__(kCta, 2)
                 sc.cA[i] = bet * rk * e;
                 if (kGdp) {
                     // query row i is token tok0 + i, read after its last update row ri of the chunk
-                    const int ri = i < nq ? static_cast<int>((tok0 + i) * NH + NH - 1 - t0) : -1;
+                    const int ri = i < nq ? (tq0 + i) * NH + NH - 1 - rel0 : -1;
                     const float bq = ri >= 0 ? sc.bw[ri] + (ri >= 32 ? sc.bw[31] : 0.f) : 0.f;
                     sc.sq[i] = ri >= 0 ? a.scale * rq * exp2f(bq) : 0.f;
                     sc.cP[i] = ri >= 0 ? a.scale * rq * exp2f(bq - b31) : 0.f;
@@ -727,7 +730,7 @@ __global__ void __launch_bounds__(kCta, 2)
                 const float ci = fast ? (is_a ? sc.cA[i] : sc.cP[i]) : (is_a ? sc.bet[i] * sc.rk[i] : a.scale * sc.rq[i]);
                 // the row's position on the update timeline (GDP query rows: the token's last update;
                 // rows past the chunk's tokens are zero and fully masked)
-                const int ip = (kGdp && !is_a) ? (i < nq ? static_cast<int>((tok0 + i) * NH + NH - 1 - t0) : -1) : i;
+                const int ip = (kGdp && !is_a) ? (i < nq ? (tq0 + i) * NH + NH - 1 - rel0 : -1) : i;
                 const float bi = sc.b[ip < 0 ? 0 : ip];
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
