@@ -60,6 +60,19 @@ def _check_beta(beta, beta_sigmoid):
         _check_thd("beta", beta, torch.float32, heads_dim=False)
 
 
+def _out(name, x, shape, dtype, dev, contiguous=False):
+    """A caller-provided output buffer, or a new one when x is None."""
+    if x is None:
+        return torch.empty(*shape, dtype=dtype, device=dev)
+    if not isinstance(x, torch.Tensor) or x.device != dev or x.dtype != dtype or tuple(x.shape) != tuple(shape):
+        raise ValueError(f"{name} must be a {dtype} tensor of shape {tuple(shape)} on {dev}")
+    if contiguous and not x.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if len(shape) == 3 and shape[-1] > 1 and x.stride(-1) != 1:
+        raise ValueError(f"{name} must have a contiguous innermost axis")
+    return x
+
+
 def _cu_bits(cu: torch.Tensor) -> int:
     if cu.dtype == torch.int32:
         return 32
@@ -234,12 +247,15 @@ def gdn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
             workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
             stream: Optional[torch.cuda.Stream] = None, a_log: Optional[torch.Tensor] = None,
             dt_bias: Optional[torch.Tensor] = None, gate_lower_bound: Optional[float] = None,
-            beta_sigmoid: bool = False):
+            beta_sigmoid: bool = False, out: Optional[Tuple[Optional[torch.Tensor], ...]] = None):
     """Backward of gdn_fwd: returns (dq, dk, dv, dg, dbeta, d_initial_state or None) for the loss
     sum(d_o * o) + sum(d_final_state * final_state).  `checkpoints`, if given, are the forward's
     fp32 checkpoints every 64 tokens; otherwise the forward is re-run for them.  With the input
     transforms of gdn_fwd, dg and dbeta are the gradients of the raw inputs, and the softplus
-    gate (a_log, dt_bias) appends (d_a_log, d_dt_bias) [HO] fp32 to the tuple."""
+    gate (a_log, dt_bias) appends (d_a_log, d_dt_bias) [HO] fp32 to the tuple.
+
+    out: optional preallocated (dq, dk, dv, dg, dbeta, d_initial_state) buffers (any entry None
+    is allocated); dq/dk/dv/dg/dbeta may be strided views, d_initial_state is contiguous."""
     _check_thd("q", q, torch.bfloat16)
     _check_thd("k", k, torch.bfloat16)
     _check_thd("v", v, torch.bfloat16)
@@ -250,12 +266,16 @@ def gdn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
     HV, V = v.shape[1], v.shape[2]
     N = cu_seqlens.numel() - 1
     dev = q.device
-    dq = torch.empty(T, HK, K, dtype=torch.bfloat16, device=dev)
-    dk = torch.empty(T, HK, K, dtype=torch.bfloat16, device=dev)
-    dv = torch.empty(T, HV, V, dtype=torch.bfloat16, device=dev)
-    dg = torch.empty(T, HV, dtype=torch.float32, device=dev)
-    db = torch.empty(T, HV, dtype=torch.float32, device=dev)
-    ds0 = torch.empty(N, HV, K, V, dtype=torch.float32, device=dev) if initial_state is not None else None
+    o6 = tuple(out) + (None,) * (6 - len(out)) if out is not None else (None,) * 6
+    if len(o6) != 6:
+        raise ValueError("out holds at most (dq, dk, dv, dg, dbeta, d_initial_state)")
+    dq = _out("dq", o6[0], (T, HK, K), torch.bfloat16, dev)
+    dk = _out("dk", o6[1], (T, HK, K), torch.bfloat16, dev)
+    dv = _out("dv", o6[2], (T, HV, V), torch.bfloat16, dev)
+    dg = _out("dg", o6[3], (T, HV), torch.float32, dev)
+    db = _out("dbeta", o6[4], (T, HV), torch.float32, dev)
+    ds0 = _out("d_initial_state", o6[5], (N, HV, K, V), torch.float32, dev, contiguous=True) \
+        if initial_state is not None else None
     lib = B.load()
     if workspace is None:
         need = lib.la_gdn_bwd_workspace_bytes(T, N, HK, HV, K, V, int(checkpoints is not None))
@@ -308,12 +328,12 @@ def gdn_summary_bwd(q: torch.Tensor, k: torch.Tensor, g: torch.Tensor, beta: tor
                     workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
                     stream: Optional[torch.cuda.Stream] = None, a_log: Optional[torch.Tensor] = None,
                     dt_bias: Optional[torch.Tensor] = None, gate_lower_bound: Optional[float] = None,
-                    beta_sigmoid: bool = False) -> torch.Tensor:
+                    beta_sigmoid: bool = False, d_state: Optional[torch.Tensor] = None) -> torch.Tensor:
     """State-gradient mirror of gdn_summary: for each span (sequence) the gradient of
     sum(d_o * o) + sum(d_final_state * end_state) with respect to the state entering the span,
     [N, HO, K, V] fp32.  It depends on neither that state nor v; with gdn_summary's transition,
     d_enter = einsum('ab,bv->av', transition, d_exit) + (the value for d_exit = 0).  Gate and
-    beta transforms as in gdn_fwd."""
+    beta transforms as in gdn_fwd.  d_state: optional preallocated contiguous output."""
     _check_thd("q", q, torch.bfloat16)
     _check_thd("k", k, torch.bfloat16)
     _check_thd("g", g, torch.float32, heads_dim=False)
@@ -323,7 +343,7 @@ def gdn_summary_bwd(q: torch.Tensor, k: torch.Tensor, g: torch.Tensor, beta: tor
     HV, V = d_o.shape[1], d_o.shape[2]
     N = cu_seqlens.numel() - 1
     dev = q.device
-    d_state = torch.empty(N, HV, K, V, dtype=torch.float32, device=dev)
+    d_state = _out("d_state", d_state, (N, HV, K, V), torch.float32, dev, contiguous=True)
     lib = B.load()
     if workspace is None:
         workspace = torch.empty(lib.la_gdn_summary_bwd_workspace_bytes(N, HV, K, V), dtype=torch.uint8, device=dev)

@@ -234,3 +234,48 @@ def test_autograd_matches_oracle_gradients(save_checkpoints):
                          d_final_state=wf)
     got = [x.grad.float().cpu().numpy() for x in leaves]
     compare(w, got, ref, label=f" autograd (saved checkpoints: {save_checkpoints})")
+
+
+def test_bwd_fused_projection_views_int64_cu_single_key_head():
+    """q, k, v as column slices of one fused projection, gradients written into column slices of
+    one fused gradient buffer (the layout a fused projection's backward consumes), int64
+    cu_seqlens, one key head shared by four value heads, explicit scale, K != V."""
+    w = W.draw("bwd fused views", [150, 64, 1, 93], 1, 4, 128, 64, seed=451, initial_state=True, slow_decay=True)
+    do, dfin = cotangents(w, 452)
+    d = dev()
+    T = w.T
+    a, b = w.HK * w.K, 2 * w.HK * w.K
+    fused = torch.cat([w.q.reshape(T, -1), w.k.reshape(T, -1), w.v.reshape(T, -1)], dim=1).to(d)
+    q, k, v = fused[:, :a].view(T, w.HK, w.K), fused[:, a:b].view(T, w.HK, w.K), fused[:, b:].view(T, w.HV, w.V)
+    assert not q.is_contiguous() and not v.is_contiguous()
+    grad = torch.full_like(fused, float("nan"))
+    gb = torch.full((T, 2 * w.HV), float("nan"), dtype=torch.float32, device=d)
+    out = (grad[:, :a].view(T, w.HK, w.K), grad[:, a:b].view(T, w.HK, w.K), grad[:, b:].view(T, w.HV, w.V),
+           gb[:, :w.HV], gb[:, w.HV:], None)
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    res = la.gdn_bwd(q, k, v, w.g.to(d), w.beta.to(d), w.cu_seqlens.to(torch.int64).to(d), do.to(d), scale=0.3,
+                     initial_state=w.initial_state.to(d), d_final_state=dfin.to(d), status=status, out=out)
+    assert la.read_status(status) == 0
+    for x, y in zip(res[:5], out[:5]):
+        assert x.data_ptr() == y.data_ptr()
+    assert not torch.isnan(grad).any() and not torch.isnan(gb).any()
+    got = [x.float().cpu().numpy() for x in res[:6]]
+    ref = oracle.gdn_bwd(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, do, scale=0.3, initial_state=w.initial_state,
+                         d_final_state=dfin)
+    compare(w, got, ref)
+    # the same gradients as through freshly allocated contiguous outputs, bitwise
+    plain = run_bwd(w, do, dfin, scale=0.3)
+    for name, x, y in zip(["dq", "dk", "dv", "dg", "dbeta", "d_initial_state"], got, plain):
+        assert np.array_equal(x, y), name
+
+
+def test_bwd_out_buffers_rejected_when_mismatched():
+    """A preallocated output of the wrong shape or dtype is an argument error, raised before launch."""
+    w = W.draw("bwd out check", [64], 1, 1, 64, 64, seed=461)
+    do, _ = cotangents(w, 462, with_final=False)
+    d = dev()
+    args = [x.to(d) for x in (w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, do)]
+    with pytest.raises(ValueError):
+        la.gdn_bwd(*args, out=(torch.empty(w.T, w.HK, w.K + 1, dtype=torch.bfloat16, device=d),))
+    with pytest.raises(ValueError):
+        la.gdn_bwd(*args, out=(None, None, None, torch.empty(w.T, w.HV, dtype=torch.float64, device=d)))

@@ -173,3 +173,91 @@ def test_forward_and_summary_write_only_their_outputs(K, V):
                          checkpoint_every_n=64)
     assert rel(o.float().cpu(), ref["o"]) <= 1e-2
     assert rel(ck.cpu(), ref["checkpoints"]) <= 2e-3
+
+
+def test_backward_writes_only_its_outputs_and_replays_in_a_graph():
+    """The backward with the forward's checkpoints, grouped heads and ragged sequences (an empty
+    one, one token, chunk +- 1): the guard regions around dq, dk, dv, dg, dbeta and the
+    start-state gradient keep their sentinel, and the same call captured in a CUDA graph (caller
+    workspace and outputs) replays bitwise and reads new cotangents at replay time."""
+    lengths = [65, 0, 1, 63, 200]
+    w = W.draw("bwd guards", lengths, 2, 4, 128, 64, seed=631, initial_state=True, slow_decay=True)
+    d = dev()
+    ins = [x.to(d) for x in (w.q, w.k, w.v, w.g, w.beta)]
+    cu = w.cu_seqlens.to(d)
+    s0 = w.initial_state.to(d)
+    gen = torch.Generator().manual_seed(632)
+    do1 = torch.randn(w.T, w.HV, w.V, generator=gen).to(torch.bfloat16)
+    do2 = torch.randn(w.T, w.HV, w.V, generator=gen).to(torch.bfloat16)
+    dfin = torch.randn(w.N, w.HV, w.K, w.V, generator=gen)
+    _, _, ck = la.gdn_fwd(*ins, cu, initial_state=s0, checkpoint_every_n=64, checkpoint_dtype=torch.float32)
+    s = -77.0
+    shapes = [((w.T, w.HK, w.K), torch.bfloat16), ((w.T, w.HK, w.K), torch.bfloat16),
+              ((w.T, w.HV, w.V), torch.bfloat16), ((w.T, w.HV), torch.float32), ((w.T, w.HV), torch.float32),
+              ((w.N, w.HV, w.K, w.V), torch.float32)]
+    bigs, outs = zip(*[guarded(shape, dt, s, d) for shape, dt in shapes])
+    d_o = do1.to(d)
+    dfin_d = dfin.to(d)
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    import gated_delta_rule_29_gb300.binding as B
+    ws = torch.empty(B.load().la_gdn_bwd_workspace_bytes(w.T, w.N, w.HK, w.HV, w.K, w.V, 1), dtype=torch.uint8,
+                     device=d)
+    scratch = [torch.empty_like(x) for x in outs]
+
+    def call(warm=False):
+        la.gdn_bwd(*ins, cu, d_o, initial_state=s0, d_final_state=dfin_d, checkpoints=ck, workspace=ws,
+                   status=status, out=tuple(scratch) if warm else outs)
+
+    call()
+    torch.cuda.synchronize()
+    assert la.read_status(status) == 0
+    for name, big in zip(("dq", "dk", "dv", "dg", "dbeta", "d_initial_state"), bigs):
+        assert intact(big, s), f"{name}: a write outside the buffer"
+    ref = oracle.gdn_bwd(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, do1, initial_state=w.initial_state,
+                         d_final_state=dfin)
+    for name, x in zip(("dq", "dk", "dv", "dg", "dbeta", "d_initial_state"), outs):
+        assert rel(x.float().cpu(), ref[name]) <= (1e-2 if name in ("dq", "dk", "dv") else 2e-3), name
+    eager = [x.clone() for x in outs]
+    g = capture(call)
+    for x in outs:
+        x.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert la.read_status(status) == 0
+    for x, y in zip(outs, eager):
+        assert torch.equal(x, y)
+    # new cotangent contents: the replay reads them at replay time
+    d_o.copy_(do2.to(d))
+    g.replay()
+    torch.cuda.synchronize()
+    replayed = [x.clone() for x in outs]
+    call()
+    torch.cuda.synchronize()
+    for x, y in zip(replayed, outs):
+        assert torch.equal(x, y)
+    ref2 = oracle.gdn_bwd(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, do2, initial_state=w.initial_state,
+                          d_final_state=dfin)
+    e = rel(replayed[2].float().cpu(), ref2["dv"])
+    print(f"[parity] backward graph replay, new cotangent: dv {e:.2e}")
+    assert e <= 1e-2
+    for name, big in zip(("dq", "dk", "dv", "dg", "dbeta", "d_initial_state"), bigs):
+        assert intact(big, s), f"{name}: a write outside the buffer (graph replay)"
+
+
+def test_summary_bwd_writes_only_its_output():
+    """gdn_summary_bwd into a caller buffer with guard regions: ragged spans, an empty one."""
+    w = W.draw("sbwd guards", [1, 130, 0, 64], 2, 2, 64, 128, seed=641, slow_decay=True)
+    d = dev()
+    gen = torch.Generator().manual_seed(642)
+    do = torch.randn(w.T, w.HV, w.V, generator=gen).to(torch.bfloat16)
+    dfin = torch.randn(w.N, w.HV, w.K, w.V, generator=gen)
+    s = -77.0
+    big, out = guarded((w.N, w.HV, w.K, w.V), torch.float32, s, d)
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    res = la.gdn_summary_bwd(w.q.to(d), w.k.to(d), w.g.to(d), w.beta.to(d), w.cu_seqlens.to(d), do.to(d),
+                             d_final_state=dfin.to(d), status=status, d_state=out)
+    assert la.read_status(status) == 0
+    assert res.data_ptr() == out.data_ptr()
+    assert intact(big, s)
+    ref = oracle.gdn_summary_bwd(w.q, w.k, w.g, w.beta, w.cu_seqlens, do, d_final_state=dfin)
+    assert rel(out.cpu(), ref) <= 2e-3
