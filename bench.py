@@ -322,7 +322,8 @@ def run_ours(args, world, rank, local):
 
     # end to end through the public API with host buffers: gdn_fwd_host copies the step's inputs
     # from pinned host memory, runs the forward and copies o, the final state and the checkpoints
-    # back, pipelined by sequence groups; all of it inside the timed region
+    # back, pipelined over token ranges (long sequences cut into pieces that hand their fp32
+    # state on); all of it inside the timed region
     host_in = [x.pin_memory() for x in (w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, w.initial_state)]
     host_out = (torch.empty(o.shape, dtype=o.dtype).pin_memory(), torch.empty(fin.shape).pin_memory(),
                 torch.empty(ck.shape, dtype=ck.dtype).pin_memory())
@@ -354,6 +355,7 @@ def run_ours(args, world, rank, local):
         e2e = {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "groups": args.e2e_groups}
         assert torch.equal(host_out[0].view(torch.int16), o.cpu().view(torch.int16)), "e2e output differs"
+        assert torch.equal(host_out[1], fin.cpu()) and torch.equal(host_out[2], ck.cpu()), "e2e states differ"
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -942,7 +944,7 @@ def main():
     ap.add_argument("--ref-units", type=int, default=2, help="units per step of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
-    ap.add_argument("--e2e-groups", type=int, default=8, help="sequence groups pipelined by gdn_fwd_host")
+    ap.add_argument("--e2e-groups", type=int, default=16, help="token ranges pipelined by gdn_fwd_host")
     ap.add_argument("--workload", choices=["dense", "decode", "bwd", "gdp", "summary", "summary_bwd"],
                     default="dense",
                     help="dense: the chunked forward over the dense batch (the headline); "

@@ -419,17 +419,41 @@ def read_status(status: torch.Tensor, stream: Optional[torch.cuda.Stream] = None
     return int(out.value)
 
 
-def _groups_by_tokens(lengths, parts):
-    """Consecutive sequence groups with roughly equal token counts (at least one sequence each)."""
+def _host_parts(lengths, groups, n):
+    """The token ranges gdn_fwd_host pipelines, in packed order: runs of consecutive whole
+    sequences of at most P tokens, and every sequence longer than P cut into pieces of P tokens,
+    each piece a range of its own.  P is about total / groups, rounded up to a multiple of 64
+    and of the checkpoint cadence n, so a cut falls on a chunk and checkpoint boundary.
+
+    Returns (P, parts) with parts as tuples (t_a, t_b, a, b, piece, last): tokens t_a..t_b of
+    the packed batch; a run holds sequences a..b-1 (piece = -1, last = True); a piece belongs to
+    sequence a (b = a + 1), piece is its index within the sequence and last says whether it
+    ends the sequence."""
     total = int(sum(lengths))
-    parts = max(1, min(parts, len(lengths)))
-    bounds, acc, target = [0], 0, total / parts
+    unit = 64 if not n else 64 * int(n) // math.gcd(64, int(n))
+    target = -(-total // max(1, int(groups))) if total else 1
+    P = max(unit, -(-target // unit) * unit)
+    parts = []
+    t = 0
+    run_a, run_t = 0, 0
     for i, L in enumerate(lengths):
-        acc += int(L)
-        if len(bounds) < parts and acc >= target * len(bounds) and i + 1 < len(lengths):
-            bounds.append(i + 1)
-    bounds.append(len(lengths))
-    return [(bounds[j], bounds[j + 1]) for j in range(len(bounds) - 1) if bounds[j + 1] > bounds[j]]
+        L = int(L)
+        if L > P:
+            if i > run_a:
+                parts.append((run_t, t, run_a, i, -1, True))
+            npc = -(-L // P)
+            for pc in range(npc):
+                parts.append((t + pc * P, t + min(L, (pc + 1) * P), i, i + 1, pc, pc == npc - 1))
+            t += L
+            run_a, run_t = i + 1, t
+            continue
+        if t + L - run_t > P and i > run_a:
+            parts.append((run_t, t, run_a, i, -1, True))
+            run_a, run_t = i, t
+        t += L
+    if len(lengths) > run_a:
+        parts.append((run_t, t, run_a, len(lengths), -1, True))
+    return P, parts
 
 
 def gdn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
@@ -437,19 +461,25 @@ def gdn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Ten
                  initial_state: Optional[torch.Tensor] = None, output_final_state: bool = True,
                  checkpoint_every_n: int = 0, checkpoint_dtype: torch.dtype = torch.bfloat16,
                  out: Optional[Tuple[torch.Tensor, Optional[torch.Tensor], Optional[torch.Tensor]]] = None,
-                 device: Optional[torch.device] = None, groups: int = 4, staging: Optional[dict] = None):
-    """gdn_fwd on HOST tensors: copies in, computes, copies out, pipelined by sequence groups.
+                 device: Optional[torch.device] = None, groups: int = 4, staging: Optional[dict] = None,
+                 compute_streams: int = 8):
+    """gdn_fwd on HOST tensors: copies in, computes, copies out, pipelined over token ranges.
 
     q, k, v, g, beta, cu_seqlens (and initial_state) are contiguous CPU tensors (pin them for
-    asynchronous copies).  The batch is cut into `groups` consecutive sequence groups of similar
-    token counts; each group's host-to-device copy, forward and device-to-host copy run on their
-    own streams, so copies overlap computation and the group kernels share the GPU.  Outputs are
-    CPU tensors (pinned when `out` is not given).  Returns (o, final_state, checkpoints) once every
-    copy is enqueued; the current stream is made to wait for them, so synchronise it (or an event
-    recorded on it) before reading the outputs on the host.  Because every sequence's results are
-    independent of the batch, the grouped run gives the same bits as one gdn_fwd call.  `staging`
-    may carry device buffers and streams from an earlier call of the same shapes to avoid
-    reallocation.
+    asynchronous copies).  The packed batch is cut into ranges of about T / groups tokens (see
+    _host_parts): runs of whole sequences, and long sequences cut into pieces at chunk and
+    checkpoint boundaries, a piece starting from the state the previous piece ended in (fp32,
+    on the device).  Each range's host-to-device copy, forward and device-to-host copy are
+    ordered by events across a copy-in stream, `compute_streams` compute streams (the pieces of
+    one sequence stay on one) and a copy-out stream, so copies overlap computation and the
+    forward of a range starts as soon as its inputs have arrived.  Outputs are CPU tensors
+    (pinned when `out` is not given).  Returns (o, final_state, checkpoints) once every copy is
+    enqueued; the current stream is made to wait for them, so synchronise it (or an event
+    recorded on it) before reading the outputs on the host.  The result is bitwise that of one
+    gdn_fwd call: every sequence's results are independent of the batch around it, and a cut
+    at a chunk boundary hands the exact fp32 state to the next piece, which continues the
+    same chunk sequence with the same arithmetic.  `staging` may carry device buffers and
+    streams from an earlier call of the same shapes to avoid reallocation.
     """
     dev = device or torch.device("cuda", torch.cuda.current_device())
     T, HK, K = k.shape
@@ -468,56 +498,85 @@ def gdn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Ten
         o_h, fin_h, ck_h = out
     st = staging if staging is not None else {}
 
-    def dbuf(name, like, dtype=None):
+    def dbuf(name, shape, dtype):
         t = st.get(name)
-        if t is None or t.shape != like.shape:
-            t = torch.empty(like.shape, dtype=dtype or like.dtype, device=dev)
+        if t is None or tuple(t.shape) != tuple(shape) or t.dtype != dtype:
+            t = torch.empty(*shape, dtype=dtype, device=dev)
             st[name] = t
         return t
 
-    qd, kd, vd = dbuf("q", q), dbuf("k", k), dbuf("v", v)
-    gd, bd = dbuf("g", g), dbuf("beta", beta)
-    s0d = dbuf("s0", initial_state) if initial_state is not None else None
-    od = dbuf("o", o_h)
-    find = dbuf("fin", fin_h) if fin_h is not None else None
-    ckd = dbuf("ck", ck_h) if ck_h is not None else None
+    qd, kd, vd = dbuf("q", q.shape, q.dtype), dbuf("k", k.shape, k.dtype), dbuf("v", v.shape, v.dtype)
+    gd, bd = dbuf("g", g.shape, g.dtype), dbuf("beta", beta.shape, beta.dtype)
+    s0d = dbuf("s0", initial_state.shape, initial_state.dtype) if initial_state is not None else None
+    od = dbuf("o", o_h.shape, o_h.dtype)
+    find = dbuf("fin", fin_h.shape, fin_h.dtype) if fin_h is not None else None
+    ckd = dbuf("ck", ck_h.shape, ck_h.dtype) if ck_h is not None else None
+    _, parts = _host_parts(lengths, groups, n)
+    long_seqs = sorted({a for (_, _, a, _, pc, _) in parts if pc >= 0})
+    # the state between two pieces of a long sequence: two fp32 slots per such sequence
+    mid = dbuf("mid", (max(1, len(long_seqs)), 2, HO, K, V), torch.float32) if long_seqs else None
+    slot = {j: x for x, j in enumerate(long_seqs)}
     cur = torch.cuda.current_stream(dev)
     h2d = st.setdefault("h2d_stream", torch.cuda.Stream(dev))
     d2h = st.setdefault("d2h_stream", torch.cuda.Stream(dev))
+    ncs = max(1, int(compute_streams))
+    css = [st.setdefault(f"compute_stream{x}", torch.cuda.Stream(dev)) for x in range(ncs)]
     h2d.wait_stream(cur)
     d2h.wait_stream(cur)
+    for cs in css:
+        cs.wait_stream(cur)
     row_off = [0]
     for r_ in rows:
         row_off.append(row_off[-1] + r_)
-    for gi, (a, b) in enumerate(_groups_by_tokens(lengths, groups)):
-        t_a, t_b = int(cu[a]), int(cu[b])
-        cu_g = (cu[a:b + 1] - t_a).to(torch.int32)
-        cs = st.setdefault(f"compute_stream{gi}", torch.cuda.Stream(dev))
+    # every range's cu_seqlens in one pinned buffer and one copy ahead of the inputs (a copy from
+    # pageable memory would make the host wait for the copies already queued)
+    cu_list, cu_at = [], []
+    for (t_a, t_b, a, b, pc, _) in parts:
+        cu_at.append(len(cu_list))
+        cu_list += (cu[a:b + 1] - int(cu[a])).tolist() if pc < 0 else [0, t_b - t_a]
+    with torch.cuda.stream(h2d):
+        cu_all = torch.tensor(cu_list, dtype=torch.int32).pin_memory().to(dev, non_blocking=True) \
+            if cu_list else None
+    seq_stream = {}
+    for pi, (t_a, t_b, a, b, pc, last) in enumerate(parts):
         with torch.cuda.stream(h2d):
             for dst, src in ((qd, q), (kd, k), (vd, v), (gd, g), (bd, beta)):
                 dst[t_a:t_b].copy_(src[t_a:t_b], non_blocking=True)
-            if s0d is not None:
+            if s0d is not None and pc <= 0:
                 s0d[a:b].copy_(initial_state[a:b], non_blocking=True)
-            cu_d = cu_g.to(dev, non_blocking=True)
             ev_in = torch.cuda.Event()
             ev_in.record(h2d)
+        cu_d = cu_all[cu_at[pi]:cu_at[pi] + (b - a + 1 if pc < 0 else 2)]
+        cs = css[seq_stream.setdefault(a, len(seq_stream) % ncs)] if pc >= 0 else css[pi % ncs]
         cs.wait_event(ev_in)
+        if pc < 0:
+            s_in = s0d[a:b] if s0d is not None else None
+            s_out = find[a:b] if find is not None else None
+            r_a, r_b = row_off[a], row_off[b]
+        else:
+            m = mid[slot[a]]
+            s_in = (s0d[a:b] if s0d is not None else None) if pc == 0 else m[(pc - 1) % 2:(pc - 1) % 2 + 1]
+            s_out = (find[a:b] if find is not None else None) if last else m[pc % 2:pc % 2 + 1]
+            off = int(cu[a])
+            r_a = row_off[a] + ((t_a - off) // n if n else 0)
+            r_b = row_off[a] + ((t_b - off + n - 1) // n if n else 0)
         with torch.cuda.stream(cs):
             gdn_fwd(qd[t_a:t_b], kd[t_a:t_b], vd[t_a:t_b], gd[t_a:t_b], bd[t_a:t_b], cu_d, scale=scale,
-                    use_qk_l2norm=use_qk_l2norm, initial_state=s0d[a:b] if s0d is not None else None,
-                    output_final_state=find is not None, checkpoint_every_n=n,
-                    checkpoint_dtype=checkpoint_dtype, checkpoint_rows_hint=row_off[b] - row_off[a],
-                    o=od[t_a:t_b], final_state=find[a:b] if find is not None else None,
-                    checkpoints=ckd[row_off[a]:row_off[b]] if ckd is not None else None, stream=cs)
-            cu_d.record_stream(cs)
+                    use_qk_l2norm=use_qk_l2norm, initial_state=s_in, output_final_state=s_out is not None,
+                    checkpoint_every_n=n, checkpoint_dtype=checkpoint_dtype, checkpoint_rows_hint=r_b - r_a,
+                    o=od[t_a:t_b], final_state=s_out, checkpoints=ckd[r_a:r_b] if ckd is not None else None,
+                    stream=cs)
+            cu_all.record_stream(cs)
             ev_c = torch.cuda.Event()
             ev_c.record(cs)
         d2h.wait_event(ev_c)
         with torch.cuda.stream(d2h):
             o_h[t_a:t_b].copy_(od[t_a:t_b], non_blocking=True)
-            if fin_h is not None:
+            if fin_h is not None and last:
                 fin_h[a:b].copy_(find[a:b], non_blocking=True)
-            if ck_h is not None and row_off[b] > row_off[a]:
-                ck_h[row_off[a]:row_off[b]].copy_(ckd[row_off[a]:row_off[b]], non_blocking=True)
+            if ck_h is not None and r_b > r_a:
+                ck_h[r_a:r_b].copy_(ckd[r_a:r_b], non_blocking=True)
     cur.wait_stream(d2h)
+    for cs in css:
+        cur.wait_stream(cs)
     return o_h, fin_h, ck_h

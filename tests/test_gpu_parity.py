@@ -322,9 +322,10 @@ def test_summary_start_state_and_empty_spans():
         assert np.array_equal(tr[i].cpu().numpy(), np.stack([eye, eye]).astype(np.float32))
 
 
-@pytest.mark.parametrize("groups", [1, 3])
+@pytest.mark.parametrize("groups", [1, 3, 8])
 def test_host_pipeline_matches_device_call(groups):
-    """gdn_fwd_host (host buffers, pipelined by sequence groups) gives the same bits as gdn_fwd."""
+    """gdn_fwd_host (host buffers, pipelined over token ranges: 3 and 8 ranges cut the longer
+    sequences into pieces that hand their fp32 state on) gives the same bits as gdn_fwd."""
     w = small([300, 1, 0, 200, 129, 64], HK=2, HV=4, K=128, V=128, seed=37, initial_state=True,
               checkpoint_every_n=64, checkpoint_dtype=torch.float32, slow_decay=True)
     o_d, f_d, c_d = gpu_fwd(w)
@@ -403,3 +404,31 @@ def test_transform_arguments_rejected():
         la.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu"], gate_lower_bound=0.5)
     with pytest.raises(ValueError):
         la.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu"], a_log=torch.zeros(2, device=d))
+
+
+@pytest.mark.parametrize("cut", [128, 200])
+def test_state_round_trip_split_run(cut):
+    """Running tokens [0, m) and then [m, L) from the first part's fp32 final state equals the
+    unsplit run: bitwise when m is a chunk boundary (the second run continues the same chunk
+    sequence from the exact state), within tolerance of the oracle otherwise (the chunk grid
+    restarts at m)."""
+    L = 450
+    w = small([L], HK=2, HV=4, K=128, V=128, seed=41, initial_state=True, slow_decay=True)
+    d = dev()
+    t = to_dev(w, d)
+    o, fin, _ = la.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu"], initial_state=t["s0"])
+    parts = []
+    s_in = t["s0"]
+    for a, b in ((0, cut), (cut, L)):
+        cu = torch.tensor([0, b - a], dtype=torch.int32, device=d)
+        oo, ff, _ = la.gdn_fwd(t["q"][a:b], t["k"][a:b], t["v"][a:b], t["g"][a:b], t["beta"][a:b], cu,
+                               initial_state=s_in)
+        parts.append(oo)
+        s_in = ff
+    o2 = torch.cat(parts)
+    if cut % 64 == 0:
+        assert torch.equal(o2, o) and torch.equal(s_in, fin)
+    ref = oracle_fwd(w)
+    e_o, e_f = rel(o2.float().cpu().numpy(), ref["o"]), rel(s_in.cpu().numpy(), ref["final_state"])
+    print(f"[parity] split run at {cut}: o {e_o:.2e}, final {e_f:.2e}")
+    assert e_o <= O_TOL and e_f <= S_TOL
