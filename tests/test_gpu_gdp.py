@@ -60,12 +60,12 @@ def test_gdp_two_updates_checkpoints_grouped_heads():
 
 
 @pytest.mark.parametrize("n,K,V", [(4, 128, 128), (8, 64, 128), (4, 64, 64), (3, 128, 128), (5, 64, 64),
-                                   (7, 128, 64)])
+                                   (7, 128, 64), (16, 128, 128), (33, 64, 128), (64, 64, 64), (65, 64, 64)])
 def test_gdp_native_timeline_ragged(n, K, V):
     """The chunk kernel reads the queries and gates per token and writes the outputs per token
-    (n = 4, 8: 64 / n tokens per chunk; n = 3, 5, 7: chunks begin and end inside tokens): ragged
-    sequences that end inside a chunk, a one-token sequence, grouped heads, checkpoints, a start
-    state."""
+    (n = 4, 8, 16, 64: 64 / n tokens per chunk; n = 3, 5, 7, 33: chunks begin and end inside
+    tokens; n = 65: the timeline build, one token longer than a chunk): ragged sequences that end
+    inside a chunk, a one-token sequence, grouped heads, checkpoints, a start state."""
     c = gdp_case([1, 15, 16, 17, 70], n, 2, 4, K, V, seed=521 + n + K + V)
     d = dev()
     status = torch.zeros(1, dtype=torch.int32, device=d)

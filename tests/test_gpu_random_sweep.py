@@ -55,6 +55,7 @@ def draw_case(seed, backward=False):
     c["gate"] = str(rng.choice(["log_fast", "log_slow", "softplus", "bound"]))
     c["beta"] = str(rng.choice(["plain", "logit_f32", "logit_bf16"]))
     c["cu64"] = bool(rng.random() < 0.5)
+    c["gb_fused"] = bool(rng.random() < 0.3)
     q = torch.randn(T, HK, K, generator=gen)
     k = torch.randn(T, HK, K, generator=gen)
     if not c["l2"]:
@@ -85,6 +86,11 @@ def draw_case(seed, backward=False):
         c["b"] = braw.to(torch.bfloat16) if c["beta"] == "logit_bf16" else braw
         okw.update(beta_sigmoid=True)
         kw.update(beta_sigmoid=True)
+    if c["gb_fused"] and c["b"].dtype == torch.float32:
+        # g and beta as column slices of one [T, 2 HV] projection output (strided views)
+        c["gb"] = torch.cat([c["g"].reshape(T, HV), c["b"].reshape(T, HV)], dim=1)
+    else:
+        c["gb_fused"] = False
     s0 = None
     if c["s0"] != "none":
         s0 = 0.1 * torch.randn(N, HV, K, V, generator=gen)
@@ -97,8 +103,19 @@ def draw_case(seed, backward=False):
     return c
 
 
+def gate_beta_on(c, d):
+    """g and beta on the device: two tensors, or two column slices of one fused buffer."""
+    if c["gb_fused"]:
+        gb = c["gb"].to(d)
+        HV = c["HV"]
+        g, b = gb[:, :HV], gb[:, HV:]
+        assert not g.is_contiguous() and g.stride(0) == 2 * HV
+        return g, b
+    return c["g"].to(d), c["b"].to(d)
+
+
 def label(c):
-    keys = ("seed", "lengths", "HK", "HV", "K", "V", "l2", "scale", "s0", "ck", "gate", "beta", "cu64")
+    keys = ("seed", "lengths", "HK", "HV", "K", "V", "l2", "scale", "s0", "ck", "gate", "beta", "cu64", "gb_fused")
     return " ".join(f"{x}={c[x]}" for x in keys) + (f" ck_dtype={c['ck_dtype']}" if c["ck"] else "")
 
 
@@ -108,7 +125,7 @@ def test_forward_random_case(case):
     d = dev()
     status = torch.zeros(1, dtype=torch.int32, device=d)
     kw = {x: (y.to(d) if isinstance(y, torch.Tensor) else y) for x, y in c["kw"].items()}
-    o, fin, ck = la.gdn_fwd(c["q"].to(d), c["k"].to(d), c["v"].to(d), c["g"].to(d), c["b"].to(d), c["cu"].to(d),
+    o, fin, ck = la.gdn_fwd(c["q"].to(d), c["k"].to(d), c["v"].to(d), *gate_beta_on(c, d), c["cu"].to(d),
                             scale=c["scale"], use_qk_l2norm=c["l2"],
                             initial_state=None if c["s0t"] is None else c["s0t"].to(d),
                             checkpoint_every_n=c["ck"], checkpoint_dtype=c["ck_dtype"], status=status, **kw)
@@ -137,7 +154,7 @@ def test_backward_random_case(case):
     dfin = torch.randn(N, c["HV"], c["K"], c["V"], generator=gen) if case % 2 == 0 else None
     status = torch.zeros(1, dtype=torch.int32, device=d)
     kw = {x: (y.to(d) if isinstance(y, torch.Tensor) else y) for x, y in c["kw"].items()}
-    out = la.gdn_bwd(c["q"].to(d), c["k"].to(d), c["v"].to(d), c["g"].to(d), c["b"].to(d), c["cu"].to(d), do.to(d),
+    out = la.gdn_bwd(c["q"].to(d), c["k"].to(d), c["v"].to(d), *gate_beta_on(c, d), c["cu"].to(d), do.to(d),
                      scale=c["scale"], use_qk_l2norm=c["l2"],
                      initial_state=None if c["s0t"] is None else c["s0t"].to(d),
                      d_final_state=None if dfin is None else dfin.to(d), status=status, **kw)
