@@ -420,40 +420,30 @@ def read_status(status: torch.Tensor, stream: Optional[torch.cuda.Stream] = None
 
 
 def _host_parts(lengths, groups, n):
-    """The token ranges gdn_fwd_host pipelines, in packed order: runs of consecutive whole
-    sequences of at most P tokens, and every sequence longer than P cut into pieces of P tokens,
-    each piece a range of its own.  P is about total / groups, rounded up to a multiple of 64
-    and of the checkpoint cadence n, so a cut falls on a chunk and checkpoint boundary.
+    """The token ranges gdn_fwd_host pipelines (the library's plan, la_gdn_fwd_host_plan): runs
+    of whole sequences of at most P tokens, and sequences longer than P cut into pieces of P
+    tokens, P about total / groups rounded up to a multiple of 64 and of the checkpoint cadence
+    n.  Returns (P, parts), parts as tuples (t_a, t_b, a, b, piece, last)."""
+    acc, cu = 0, [0]
+    for L in lengths:
+        acc += int(L)
+        cu.append(acc)
+    cu_t = torch.tensor(cu, dtype=torch.int64)
+    lib = B.load()
+    P = ctypes.c_int64(0)
+    args = (cu_t.data_ptr(), 64, len(lengths), max(1, int(groups)), int(n or 0))
+    cnt = lib.la_gdn_fwd_host_plan(*args, None, 0, ctypes.byref(P))
+    if cnt < 0:
+        raise ValueError("invalid lengths, groups or checkpoint cadence")
+    rows = (ctypes.c_int64 * (6 * max(cnt, 1)))()
+    lib.la_gdn_fwd_host_plan(*args, rows, cnt, ctypes.byref(P))
+    parts = [tuple(int(rows[6 * i + j]) for j in range(5)) + (bool(rows[6 * i + 5]),) for i in range(cnt)]
+    return int(P.value), parts
 
-    Returns (P, parts) with parts as tuples (t_a, t_b, a, b, piece, last): tokens t_a..t_b of
-    the packed batch; a run holds sequences a..b-1 (piece = -1, last = True); a piece belongs to
-    sequence a (b = a + 1), piece is its index within the sequence and last says whether it
-    ends the sequence."""
-    total = int(sum(lengths))
-    unit = 64 if not n else 64 * int(n) // math.gcd(64, int(n))
-    target = -(-total // max(1, int(groups))) if total else 1
-    P = max(unit, -(-target // unit) * unit)
-    parts = []
-    t = 0
-    run_a, run_t = 0, 0
-    for i, L in enumerate(lengths):
-        L = int(L)
-        if L > P:
-            if i > run_a:
-                parts.append((run_t, t, run_a, i, -1, True))
-            npc = -(-L // P)
-            for pc in range(npc):
-                parts.append((t + pc * P, t + min(L, (pc + 1) * P), i, i + 1, pc, pc == npc - 1))
-            t += L
-            run_a, run_t = i + 1, t
-            continue
-        if t + L - run_t > P and i > run_a:
-            parts.append((run_t, t, run_a, i, -1, True))
-            run_a, run_t = i, t
-        t += L
-    if len(lengths) > run_a:
-        parts.append((run_t, t, run_a, len(lengths), -1, True))
-    return P, parts
+
+def _check_host(name, x, dtype, dims):
+    if not isinstance(x, torch.Tensor) or x.is_cuda or x.dtype != dtype or x.dim() != dims or not x.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous CPU {dtype} tensor of rank {dims} (pinned for overlap)")
 
 
 def gdn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
@@ -461,122 +451,93 @@ def gdn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Ten
                  initial_state: Optional[torch.Tensor] = None, output_final_state: bool = True,
                  checkpoint_every_n: int = 0, checkpoint_dtype: torch.dtype = torch.bfloat16,
                  out: Optional[Tuple[torch.Tensor, Optional[torch.Tensor], Optional[torch.Tensor]]] = None,
-                 device: Optional[torch.device] = None, groups: int = 4, staging: Optional[dict] = None,
-                 compute_streams: int = 8):
-    """gdn_fwd on HOST tensors: copies in, computes, copies out, pipelined over token ranges.
+                 device: Optional[torch.device] = None, groups: int = 16, staging: Optional[dict] = None,
+                 status: Optional[torch.Tensor] = None, stream: Optional[torch.cuda.Stream] = None,
+                 a_log: Optional[torch.Tensor] = None, dt_bias: Optional[torch.Tensor] = None,
+                 gate_lower_bound: Optional[float] = None, beta_sigmoid: bool = False):
+    """gdn_fwd on HOST tensors through the library's gdn_fwd_host: copy in, forward, copy out,
+    pipelined over about `groups` token ranges on the library's own streams.
 
-    q, k, v, g, beta, cu_seqlens (and initial_state) are contiguous CPU tensors (pin them for
-    asynchronous copies).  The packed batch is cut into ranges of about T / groups tokens (see
-    _host_parts): runs of whole sequences, and long sequences cut into pieces at chunk and
-    checkpoint boundaries, a piece starting from the state the previous piece ended in (fp32,
-    on the device).  Each range's host-to-device copy, forward and device-to-host copy are
-    ordered by events across a copy-in stream, `compute_streams` compute streams (the pieces of
-    one sequence stay on one) and a copy-out stream, so copies overlap computation and the
-    forward of a range starts as soon as its inputs have arrived.  Outputs are CPU tensors
-    (pinned when `out` is not given).  Returns (o, final_state, checkpoints) once every copy is
-    enqueued; the current stream is made to wait for them, so synchronise it (or an event
-    recorded on it) before reading the outputs on the host.  The result is bitwise that of one
-    gdn_fwd call: every sequence's results are independent of the batch around it, and a cut
-    at a chunk boundary hands the exact fp32 state to the next piece, which continues the
-    same chunk sequence with the same arithmetic.  `staging` may carry device buffers and
-    streams from an earlier call of the same shapes to avoid reallocation.
-    """
+    q, k, v, g, beta, initial_state are contiguous CPU tensors (pin them so the copies run
+    asynchronously), cu_seqlens a CPU int32/int64 tensor; a_log and dt_bias, with the softplus
+    gate, CPU float32 [HO].  Outputs (o, final_state, checkpoints) are CPU tensors (pinned when
+    `out` is not given).  Returns once everything is enqueued, with the stream made to wait for
+    the last copy out: synchronise it before reading the outputs, and keep the inputs alive and
+    unchanged until then.  The result is bitwise that of one gdn_fwd call.  `staging` (a dict)
+    keeps the device staging buffer from one call to the next; the status word, if given, is a
+    device int32 tensor as for gdn_fwd."""
     dev = device or torch.device("cuda", torch.cuda.current_device())
+    _check_host("q", q, torch.bfloat16, 3)
+    _check_host("k", k, torch.bfloat16, 3)
+    _check_host("v", v, torch.bfloat16, 3)
+    _check_host("g", g, torch.float32, 2)
+    beta_bf16 = beta_sigmoid and beta.dtype == torch.bfloat16
+    _check_host("beta", beta, torch.bfloat16 if beta_bf16 else torch.float32, 2)
     T, HK, K = k.shape
     HV, V = v.shape[1], v.shape[2]
     HO = HV
-    N = cu_seqlens.numel() - 1
-    cu = cu_seqlens.to(torch.int64)
-    lengths = (cu[1:] - cu[:-1]).tolist()
+    cu = cu_seqlens.detach().to("cpu").contiguous()
+    N = cu.numel() - 1
     n = int(checkpoint_every_n or 0)
-    rows = [(int(L) + n - 1) // n for L in lengths] if n else [0] * N
+    R = checkpoint_rows(cu, n) if n else 0
     if out is None:
         o_h = torch.empty(T, HO, V, dtype=torch.bfloat16).pin_memory()
         fin_h = torch.empty(N, HO, K, V, dtype=torch.float32).pin_memory() if output_final_state else None
-        ck_h = torch.empty(sum(rows), HO, K, V, dtype=checkpoint_dtype).pin_memory() if n else None
+        ck_h = torch.empty(R, HO, K, V, dtype=checkpoint_dtype).pin_memory() if n else None
     else:
         o_h, fin_h, ck_h = out
+    _check_host("o", o_h, torch.bfloat16, 3)
+    if fin_h is not None:
+        _check_host("final_state", fin_h, torch.float32, 4)
+    if ck_h is not None:
+        _check_host("checkpoints", ck_h, checkpoint_dtype, 4)
+    hp = B.GdnFwdHostParams()
+    p = hp.fwd
+    p.q, p.q_stride_t, p.q_stride_h = q.data_ptr(), HK * K, K
+    p.k, p.k_stride_t, p.k_stride_h = k.data_ptr(), HK * K, K
+    p.v, p.v_stride_t, p.v_stride_h = v.data_ptr(), HV * V, V
+    p.g, p.g_stride_t, p.g_stride_h = g.data_ptr(), HO, 1
+    p.beta, p.beta_stride_t, p.beta_stride_h = beta.data_ptr(), HO, 1
+    p.cu_seqlens, p.cu_seqlens_bits = cu.data_ptr(), _cu_bits(cu)
+    p.T, p.N, p.HK, p.HV, p.K, p.V = T, N, HK, HV, K, V
+    p.scale = float(scale) if scale is not None else 1.0 / math.sqrt(K)
+    p.use_qk_l2norm = int(bool(use_qk_l2norm))
+    if initial_state is not None:
+        _check_host("initial_state", initial_state, initial_state.dtype, 4)
+        p.initial_state = initial_state.data_ptr()
+        p.initial_state_dtype = B.LA_DTYPE_BF16 if initial_state.dtype == torch.bfloat16 else B.LA_DTYPE_F32
+    p.o, p.o_stride_t, p.o_stride_h = o_h.data_ptr(), HO * V, V
+    p.final_state = fin_h.data_ptr() if fin_h is not None else None
+    if ck_h is not None:
+        p.checkpoints = ck_h.data_ptr()
+        p.checkpoint_dtype = B.LA_DTYPE_BF16 if ck_h.dtype == torch.bfloat16 else B.LA_DTYPE_F32
+        p.checkpoint_every_n = n
+    p.status = status.data_ptr() if status is not None else None
+    if (a_log is None) != (dt_bias is None):
+        raise ValueError("the softplus gate needs both a_log and dt_bias")
+    if a_log is not None:
+        if gate_lower_bound is not None:
+            raise ValueError("choose one gate transform: (a_log, dt_bias) or gate_lower_bound")
+        for name, x in (("a_log", a_log), ("dt_bias", dt_bias)):
+            _check_host(name, x, torch.float32, 1)
+            if x.numel() != HO:
+                raise ValueError(f"{name} must hold {HO} elements")
+        p.gate_mode, p.a_log, p.dt_bias = B.LA_GATE_SOFTPLUS, a_log.data_ptr(), dt_bias.data_ptr()
+    elif gate_lower_bound is not None:
+        p.gate_mode, p.gate_lower_bound = B.LA_GATE_SIGMOID_BOUND, float(gate_lower_bound)
+    p.beta_sigmoid = int(bool(beta_sigmoid))
+    p.beta_bf16 = int(beta_bf16)
+    hp.ranges = max(1, int(groups))
+    lib = B.load()
+    need = int(lib.la_gdn_fwd_host_staging_bytes(ctypes.byref(hp)))
+    if need == 0:
+        raise ValueError("gdn_fwd_host: invalid arguments (shapes, cu_seqlens or options)")
     st = staging if staging is not None else {}
-
-    def dbuf(name, shape, dtype):
-        t = st.get(name)
-        if t is None or tuple(t.shape) != tuple(shape) or t.dtype != dtype:
-            t = torch.empty(*shape, dtype=dtype, device=dev)
-            st[name] = t
-        return t
-
-    qd, kd, vd = dbuf("q", q.shape, q.dtype), dbuf("k", k.shape, k.dtype), dbuf("v", v.shape, v.dtype)
-    gd, bd = dbuf("g", g.shape, g.dtype), dbuf("beta", beta.shape, beta.dtype)
-    s0d = dbuf("s0", initial_state.shape, initial_state.dtype) if initial_state is not None else None
-    od = dbuf("o", o_h.shape, o_h.dtype)
-    find = dbuf("fin", fin_h.shape, fin_h.dtype) if fin_h is not None else None
-    ckd = dbuf("ck", ck_h.shape, ck_h.dtype) if ck_h is not None else None
-    _, parts = _host_parts(lengths, groups, n)
-    long_seqs = sorted({a for (_, _, a, _, pc, _) in parts if pc >= 0})
-    # the state between two pieces of a long sequence: two fp32 slots per such sequence
-    mid = dbuf("mid", (max(1, len(long_seqs)), 2, HO, K, V), torch.float32) if long_seqs else None
-    slot = {j: x for x, j in enumerate(long_seqs)}
-    cur = torch.cuda.current_stream(dev)
-    h2d = st.setdefault("h2d_stream", torch.cuda.Stream(dev))
-    d2h = st.setdefault("d2h_stream", torch.cuda.Stream(dev))
-    ncs = max(1, int(compute_streams))
-    css = [st.setdefault(f"compute_stream{x}", torch.cuda.Stream(dev)) for x in range(ncs)]
-    h2d.wait_stream(cur)
-    d2h.wait_stream(cur)
-    for cs in css:
-        cs.wait_stream(cur)
-    row_off = [0]
-    for r_ in rows:
-        row_off.append(row_off[-1] + r_)
-    # every range's cu_seqlens in one pinned buffer and one copy ahead of the inputs (a copy from
-    # pageable memory would make the host wait for the copies already queued)
-    cu_list, cu_at = [], []
-    for (t_a, t_b, a, b, pc, _) in parts:
-        cu_at.append(len(cu_list))
-        cu_list += (cu[a:b + 1] - int(cu[a])).tolist() if pc < 0 else [0, t_b - t_a]
-    with torch.cuda.stream(h2d):
-        cu_all = torch.tensor(cu_list, dtype=torch.int32).pin_memory().to(dev, non_blocking=True) \
-            if cu_list else None
-    seq_stream = {}
-    for pi, (t_a, t_b, a, b, pc, last) in enumerate(parts):
-        with torch.cuda.stream(h2d):
-            for dst, src in ((qd, q), (kd, k), (vd, v), (gd, g), (bd, beta)):
-                dst[t_a:t_b].copy_(src[t_a:t_b], non_blocking=True)
-            if s0d is not None and pc <= 0:
-                s0d[a:b].copy_(initial_state[a:b], non_blocking=True)
-            ev_in = torch.cuda.Event()
-            ev_in.record(h2d)
-        cu_d = cu_all[cu_at[pi]:cu_at[pi] + (b - a + 1 if pc < 0 else 2)]
-        cs = css[seq_stream.setdefault(a, len(seq_stream) % ncs)] if pc >= 0 else css[pi % ncs]
-        cs.wait_event(ev_in)
-        if pc < 0:
-            s_in = s0d[a:b] if s0d is not None else None
-            s_out = find[a:b] if find is not None else None
-            r_a, r_b = row_off[a], row_off[b]
-        else:
-            m = mid[slot[a]]
-            s_in = (s0d[a:b] if s0d is not None else None) if pc == 0 else m[(pc - 1) % 2:(pc - 1) % 2 + 1]
-            s_out = (find[a:b] if find is not None else None) if last else m[pc % 2:pc % 2 + 1]
-            off = int(cu[a])
-            r_a = row_off[a] + ((t_a - off) // n if n else 0)
-            r_b = row_off[a] + ((t_b - off + n - 1) // n if n else 0)
-        with torch.cuda.stream(cs):
-            gdn_fwd(qd[t_a:t_b], kd[t_a:t_b], vd[t_a:t_b], gd[t_a:t_b], bd[t_a:t_b], cu_d, scale=scale,
-                    use_qk_l2norm=use_qk_l2norm, initial_state=s_in, output_final_state=s_out is not None,
-                    checkpoint_every_n=n, checkpoint_dtype=checkpoint_dtype, checkpoint_rows_hint=r_b - r_a,
-                    o=od[t_a:t_b], final_state=s_out, checkpoints=ckd[r_a:r_b] if ckd is not None else None,
-                    stream=cs)
-            cu_all.record_stream(cs)
-            ev_c = torch.cuda.Event()
-            ev_c.record(cs)
-        d2h.wait_event(ev_c)
-        with torch.cuda.stream(d2h):
-            o_h[t_a:t_b].copy_(od[t_a:t_b], non_blocking=True)
-            if fin_h is not None and last:
-                fin_h[a:b].copy_(find[a:b], non_blocking=True)
-            if ck_h is not None and r_b > r_a:
-                ck_h[r_a:r_b].copy_(ckd[r_a:r_b], non_blocking=True)
-    cur.wait_stream(d2h)
-    for cs in css:
-        cur.wait_stream(cs)
+    buf = st.get("staging")
+    if buf is None or buf.numel() < need or buf.device != dev:
+        with torch.cuda.stream(stream if stream is not None else torch.cuda.current_stream(dev)):
+            buf = torch.empty(need, dtype=torch.uint8, device=dev)
+        st["staging"] = buf
+    hp.staging, hp.staging_bytes = buf.data_ptr(), buf.numel()
+    B.check(lib.gdn_fwd_host(ctypes.byref(hp), _stream_ptr(stream)), "gdn_fwd_host")
     return o_h, fin_h, ck_h

@@ -43,6 +43,9 @@ EXPORTED_SYMBOLS = (
     "la_gdp_workspace_bytes",
     "gdn_summary_bwd",
     "la_gdn_summary_bwd_workspace_bytes",
+    "gdn_fwd_host",
+    "la_gdn_fwd_host_staging_bytes",
+    "la_gdn_fwd_host_plan",
 )
 
 _i64 = ctypes.c_int64
@@ -73,6 +76,12 @@ class GdnFwdParams(ctypes.Structure):
         ("state_indices", _vp), ("state_pool_size", _i64),
         ("num_householder", _i32),
     ]
+
+
+class GdnFwdHostParams(ctypes.Structure):
+    """Mirror of la_gdn_fwd_host_params: gdn_fwd's parameters with host data pointers, the
+    device staging buffer and the number of token ranges."""
+    _fields_ = [("fwd", GdnFwdParams), ("staging", _vp), ("staging_bytes", ctypes.c_size_t), ("ranges", _i32)]
 
 
 class GdnSummaryParams(ctypes.Structure):
@@ -144,6 +153,13 @@ def load(build_if_missing: bool = True):
         lib.la_version.argtypes = []
         lib.la_set_kernel_timing_events.restype = ctypes.c_int
         lib.la_set_kernel_timing_events.argtypes = [_vp, _vp]
+        lib.gdn_fwd_host.restype = ctypes.c_int
+        lib.gdn_fwd_host.argtypes = [ctypes.POINTER(GdnFwdHostParams), _vp]
+        lib.la_gdn_fwd_host_staging_bytes.restype = ctypes.c_size_t
+        lib.la_gdn_fwd_host_staging_bytes.argtypes = [ctypes.POINTER(GdnFwdHostParams)]
+        lib.la_gdn_fwd_host_plan.restype = _i32
+        lib.la_gdn_fwd_host_plan.argtypes = [_vp, _i32, _i32, _i32, _i64, ctypes.POINTER(_i64), _i32,
+                                             ctypes.POINTER(_i64)]
         lib.gdn_fwd_static_workspace.restype = ctypes.c_int
         lib.gdn_fwd_static_workspace.argtypes = [ctypes.POINTER(GdnFwdParams), _vp]
         _lib = lib

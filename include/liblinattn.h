@@ -55,7 +55,7 @@ typedef enum la_status {
     LA_ERR_INVALID_ARG = 1,  /* null pointer, bad shape/stride/alignment, N < 0, ... */
     LA_ERR_UNSUPPORTED = 2,  /* K or V not in {64,128}, HV % HK != 0, HK > HV, dtype */
     LA_ERR_CUDA = 3,         /* a CUDA runtime or driver call failed (launch, encode) */
-    LA_ERR_BAD_SEQLENS = 4,  /* device-side: cu_seqlens not 0-based, decreasing or != T at N */
+    LA_ERR_BAD_SEQLENS = 4,  /* cu_seqlens not 0-based, decreasing or != T at N (device-side; returned by gdn_fwd_host) */
     LA_ERR_TIMEOUT = 5,      /* device-side: a bounded wait in a kernel gave up */
     LA_ERR_WORKSPACE = 6,    /* workspace smaller than la_gdn_workspace_bytes() */
     LA_ERR_BAD_STATE_INDEX = 7 /* device-side: a state_indices entry outside [0, state_pool_size) */
@@ -167,6 +167,69 @@ la_status gdn_fwd(const la_gdn_fwd_params* p, void* stream);
  *     race on the array and give undefined results.
  */
 la_status gdn_fwd_static_workspace(const la_gdn_fwd_params* p, void* stream);
+
+/*
+ * gdn_fwd_host -- gdn_fwd on HOST buffers: copy in, forward, copy out, pipelined.
+ *
+ * Computes exactly what gdn_fwd computes (bitwise the same o, final state and
+ * checkpoints) for inputs and outputs that live in host memory.  The packed
+ * batch is cut into about `ranges` token ranges (la_gdn_fwd_host_plan): runs
+ * of whole sequences, and sequences longer than a range cut into pieces at
+ * multiples of the range length P (a multiple of the 64-token chunk and of
+ * checkpoint_every_n), each piece starting from the exact fp32 state the
+ * previous piece ended in.  A range's host-to-device copies, its forward and
+ * its device-to-host copies are chained by events across one copy-in stream,
+ * eight compute streams (the pieces of one sequence share one) and one
+ * copy-out stream, owned by the library per device, so copies of some ranges
+ * overlap the forwards of others.
+ *
+ *   fwd: the gdn_fwd parameters with HOST pointers for q, k, v, g, beta,
+ *     cu_seqlens, initial_state, a_log, dt_bias, o, final_state and
+ *     checkpoints.  q, k, v, g, beta and o must be contiguous ([T, H, D] with
+ *     token stride H * D and head stride D; [T, HO] with stride HO, 1).
+ *     Page-locked (pinned) host memory lets the copies run asynchronously;
+ *     pageable memory is accepted but serialises the copies with the host.
+ *     fwd.status, if set, is a DEVICE int32 as in gdn_fwd; fwd.workspace is
+ *     ignored; state_indices must be NULL and num_householder <= 1.
+ *   staging: DEVICE memory of at least la_gdn_fwd_host_staging_bytes(p)
+ *     bytes, 256-byte aligned, owned by the caller (the device copies of every
+ *     input and output plus per-stream scratch).  Two calls sharing a staging
+ *     buffer must be ordered on one stream.
+ *   ranges: >= 1.
+ * Stream semantics: every copy and kernel is ordered after the work already
+ * enqueued on `stream`, and `stream` is made to wait for the last copy out;
+ * the call returns once everything is enqueued (host buffers must stay valid
+ * and the outputs must not be read until `stream` has been synchronised).
+ * The host may block while the previous call's small metadata copy is still
+ * pending.  Not capturable in a CUDA graph (use gdn_fwd on device buffers).
+ * Errors: argument checks as gdn_fwd, plus LA_ERR_BAD_SEQLENS for a host
+ * cu_seqlens that is not 0, nondecreasing, T; LA_ERR_WORKSPACE for a staging
+ * buffer that is too small or misaligned; LA_ERR_UNSUPPORTED for a state pool
+ * or Gated DeltaProduct.
+ */
+typedef struct la_gdn_fwd_host_params {
+    la_gdn_fwd_params fwd;
+    void* staging;
+    size_t staging_bytes;
+    int32_t ranges;
+} la_gdn_fwd_host_params;
+
+la_status gdn_fwd_host(const la_gdn_fwd_host_params* p, void* stream);
+
+/* Device staging bytes gdn_fwd_host needs for these parameters (reads the host
+ * cu_seqlens); 0 if the parameters are invalid. */
+size_t la_gdn_fwd_host_staging_bytes(const la_gdn_fwd_host_params* p);
+
+/* The token ranges of gdn_fwd_host for a host cu_seqlens [N + 1] (idx_bits 32 or
+ * 64), `ranges` and the checkpoint cadence n (0: none).  Writes up to
+ * max_ranges rows of six int64 (t_a, t_b, a, b, piece, last) into out: tokens
+ * t_a .. t_b of the packed batch; a run of whole sequences a .. b-1 has
+ * piece = -1 and last = 1; a piece of sequence a (b = a + 1) has its index
+ * within the sequence and last = 1 when it ends the sequence.  *piece_tokens
+ * receives P.  Returns the number of ranges (which may exceed max_ranges: call
+ * again with room), or -1 for invalid arguments. */
+int32_t la_gdn_fwd_host_plan(const void* cu_seqlens_host, int32_t idx_bits, int32_t N, int32_t ranges,
+                             int64_t checkpoint_every_n, int64_t* out, int32_t max_ranges, int64_t* piece_tokens);
 
 /* Parameters of gdn_summary.  Strides are in elements. */
 typedef struct la_gdn_summary_params {

@@ -50,7 +50,8 @@ def _c_layout(struct_name, fields):
                                        (B.GdnSummaryParams, "la_gdn_summary_params"),
                                        (B.GdnDecodeParams, "la_gdn_decode_params"),
                                        (B.GdnBwdParams, "la_gdn_bwd_params"),
-                                       (B.GdnSummaryBwdParams, "la_gdn_summary_bwd_params")])
+                                       (B.GdnSummaryBwdParams, "la_gdn_summary_bwd_params"),
+                                       (B.GdnFwdHostParams, "la_gdn_fwd_host_params")])
 def test_ctypes_mirror_matches_c_layout(cls, cname):
     names = [f[0] for f in cls._fields_]
     size, offs = _c_layout(cname, names)
@@ -325,3 +326,70 @@ def test_workspace_bytes_grows_with_batch():
     assert small >= 256 and small % 256 == 0
     assert big > small and big % 256 == 0
     assert big >= 256 + 4 * 100000 + 8 * 100000 + 8 * 131072
+
+
+def _host(cu, **over):
+    """gdn_fwd_host parameters over a real host cu_seqlens (the call reads it on the host)."""
+    hp = B.GdnFwdHostParams()
+    p = _fwd()
+    p.cu_seqlens, p.cu_seqlens_bits = ctypes.addressof(cu), 32
+    p.T, p.N = cu[len(cu) - 1], len(cu) - 1
+    for k, v in over.items():
+        if k in ("staging", "staging_bytes", "ranges"):
+            setattr(hp, k, v)
+        else:
+            setattr(p, k, v)
+    hp.fwd = p
+    if "staging" not in over:
+        hp.staging = FAKE
+    if "staging_bytes" not in over:
+        hp.staging_bytes = 1 << 40
+    if "ranges" not in over:
+        hp.ranges = 4
+    return hp
+
+
+HOST_ERRORS = [
+    ("decreasing cu_seqlens", [0, 200, 100, 256], {}, B.LA_ERR_BAD_SEQLENS),
+    ("cu_seqlens not ending at T", [0, 100, 256], dict(T=300), B.LA_ERR_BAD_SEQLENS),
+    ("cu_seqlens not starting at 0", [4, 100, 256], {}, B.LA_ERR_BAD_SEQLENS),
+    ("zero ranges", [0, 100, 256], dict(ranges=0), B.LA_ERR_INVALID_ARG),
+    ("Gated DeltaProduct", [0, 100, 256], dict(num_householder=2), B.LA_ERR_UNSUPPORTED),
+    ("state pool", [0, 100, 256], dict(state_indices=FAKE, state_pool_size=4), B.LA_ERR_UNSUPPORTED),
+    ("HV not a multiple of HK", [0, 100, 256], dict(HK=3, HV=4), B.LA_ERR_UNSUPPORTED),
+    ("K not 64/128", [0, 100, 256], dict(K=96), B.LA_ERR_UNSUPPORTED),
+    ("strided q", [0, 100, 256], dict(q_stride_t=256), B.LA_ERR_INVALID_ARG),
+    ("strided g", [0, 100, 256], dict(g_stride_t=4), B.LA_ERR_INVALID_ARG),
+    ("null o", [0, 100, 256], dict(o=None), B.LA_ERR_INVALID_ARG),
+    ("checkpoint n not a multiple of 64", [0, 100, 256], dict(checkpoints=FAKE, checkpoint_every_n=100),
+     B.LA_ERR_INVALID_ARG),
+    ("softplus gate without dt_bias", [0, 100, 256], dict(gate_mode=1, a_log=FAKE), B.LA_ERR_INVALID_ARG),
+    ("staging too small", [0, 100, 256], dict(staging_bytes=1024), B.LA_ERR_WORKSPACE),
+    ("staging misaligned", [0, 100, 256], dict(staging=FAKE + 16), B.LA_ERR_WORKSPACE),
+    ("no staging", [0, 100, 256], dict(staging=None), B.LA_ERR_WORKSPACE),
+]
+
+
+@pytest.mark.parametrize("name,cu,over,code", HOST_ERRORS, ids=[e[0] for e in HOST_ERRORS])
+def test_gdn_fwd_host_rejects(name, cu, over, code):
+    """Every rejection of the host-buffer entry happens on the host, before any CUDA call."""
+    lib = B.load()
+    cu_arr = (ctypes.c_int32 * len(cu))(*cu)
+    hp = _host(cu_arr, **over)
+    assert lib.gdn_fwd_host(ctypes.byref(hp), None) == code
+
+
+def test_gdn_fwd_host_staging_bytes():
+    """The staging size covers the device copies of every input and output: it grows with the
+    checkpoints and the start state, and is 0 for invalid parameters."""
+    lib = B.load()
+    cu = (ctypes.c_int32 * 3)(0, 100, 256)
+    base = lib.la_gdn_fwd_host_staging_bytes(ctypes.byref(_host(cu)))
+    T, HK, HV, K, V = 256, 2, 2, 64, 64
+    assert base >= T * (2 * HK * K + 2 * HV * V) * 2 + 2 * T * HV * 4
+    ck = lib.la_gdn_fwd_host_staging_bytes(ctypes.byref(_host(cu, checkpoints=FAKE, checkpoint_every_n=64,
+                                                                   checkpoint_dtype=1)))
+    assert ck >= base + (2 + 3) * HV * K * V * 4
+    s0 = lib.la_gdn_fwd_host_staging_bytes(ctypes.byref(_host(cu, initial_state=FAKE, initial_state_dtype=1)))
+    assert s0 >= base + 2 * HV * K * V * 4
+    assert lib.la_gdn_fwd_host_staging_bytes(ctypes.byref(_host(cu, K=96))) == 0

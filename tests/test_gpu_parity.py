@@ -406,6 +406,29 @@ def test_transform_arguments_rejected():
         la.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu"], a_log=torch.zeros(2, device=d))
 
 
+def test_host_pipeline_transforms_and_options_bitwise():
+    """gdn_fwd_host with the softplus gate (host a_log, dt_bias), bf16 beta logits, a bf16 start
+    state, bf16 checkpoints every 128 tokens, no final state, int64 cu_seqlens and 7 ranges: the
+    same bits as gdn_fwd on device buffers."""
+    w = small([700, 64, 1, 0, 389, 129], HK=1, HV=4, K=128, V=64, seed=43, initial_state=True)
+    g_raw, beta_raw = _raw_gate_inputs(w, 44, torch.bfloat16)
+    a_log = torch.log(torch.tensor([0.02, 0.05, 0.1, 0.5]))
+    dt_bias = torch.tensor([-3.0, -1.0, 0.0, 0.5])
+    s0 = w.initial_state.to(torch.bfloat16)
+    d = dev()
+    t = to_dev(w, d)
+    kw = dict(checkpoint_every_n=128, checkpoint_dtype=torch.bfloat16, output_final_state=False, beta_sigmoid=True)
+    o_d, _, c_d = la.gdn_fwd(t["q"], t["k"], t["v"], g_raw.to(d), beta_raw.to(d), t["cu"], initial_state=s0.to(d),
+                             a_log=a_log.to(d), dt_bias=dt_bias.to(d), **kw)
+    pin = lambda x: x.contiguous().pin_memory()
+    o_h, f_h, c_h = la.gdn_fwd_host(pin(w.q), pin(w.k), pin(w.v), pin(g_raw), pin(beta_raw),
+                                    w.cu_seqlens.to(torch.int64), initial_state=pin(s0), a_log=a_log, dt_bias=dt_bias,
+                                    groups=7, **kw)
+    torch.cuda.synchronize()
+    assert f_h is None
+    assert torch.equal(o_h, o_d.cpu()) and torch.equal(c_h, c_d.cpu())
+
+
 @pytest.mark.parametrize("cut", [128, 200])
 def test_state_round_trip_split_run(cut):
     """Running tokens [0, m) and then [m, L) from the first part's fp32 final state equals the
