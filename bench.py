@@ -329,13 +329,17 @@ def run_ours(args, world, rank, local):
                 torch.empty(ck.shape, dtype=ck.dtype).pin_memory())
     h2d = sum(x.numel() * x.element_size() for x in host_in)
     d2h = sum(x.numel() * x.element_size() for x in host_out)
-    staging = {}
+    # two staging buffers used in turn: a step's copies in only wait for the step before last
+    # (the one that used the same buffer), so they run under the previous step's last forward
+    staging = ({}, {})
+    e2e_count = [0]
 
     def e2e_step():
         hq, hk, hv, hg, hb, hcu, hs0 = host_in
         la.gdn_fwd_host(hq, hk, hv, hg, hb, hcu, initial_state=hs0, checkpoint_every_n=n_ck,
                         checkpoint_dtype=torch.float32, out=host_out, device=dev, groups=args.e2e_groups,
-                        staging=staging)
+                        staging=staging[e2e_count[0] % 2])
+        e2e_count[0] += 1
 
     e2e = None
     if not args.no_e2e:

@@ -464,8 +464,10 @@ def gdn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Ten
     `out` is not given).  Returns once everything is enqueued, with the stream made to wait for
     the last copy out: synchronise it before reading the outputs, and keep the inputs alive and
     unchanged until then.  The result is bitwise that of one gdn_fwd call.  `staging` (a dict)
-    keeps the device staging buffer from one call to the next; the status word, if given, is a
-    device int32 tensor as for gdn_fwd."""
+    keeps the device staging buffer from one call to the next: a call with the same buffer is
+    ordered after the previous call that used it rather than after the stream, so alternating two
+    dicts lets one call's copies run under the previous call's last forwards.  The status word, if
+    given, is a device int32 tensor as for gdn_fwd."""
     dev = device or torch.device("cuda", torch.cuda.current_device())
     _check_host("q", q, torch.bfloat16, 3)
     _check_host("k", k, torch.bfloat16, 3)

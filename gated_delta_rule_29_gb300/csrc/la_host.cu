@@ -156,6 +156,8 @@ struct HostPipe {
     size_t meta_cap = 0;
     cudaEvent_t meta_ev = nullptr;
     bool meta_pending = false;
+    // the end of the last call that used each staging buffer
+    std::vector<std::pair<const void*, cudaEvent_t>> done;
 };
 std::mutex g_host_mutex;
 HostPipe g_host[128];
@@ -281,10 +283,26 @@ la_status gdn_fwd_host(const la_gdn_fwd_host_params* hp, void* stream) {
             std::memcpy(m + P.cu_count + HV, f.dt_bias, HV * sizeof(float));
         }
     }
-    // every stream starts after the caller's stream
-    if ((st = chain(s, pipe->h2d)) != LA_OK || (st = chain(s, pipe->d2h)) != LA_OK) return st;
-    for (int x = 0; x < kHostStreams; ++x)
-        if ((st = chain(s, pipe->cs[x])) != LA_OK) return st;
+    // The copies in wait for the end of the last call that used this staging buffer (its device
+    // copies, scratch and hand-over slots are about to be overwritten); a staging buffer not seen
+    // before orders the call after the caller's stream.  Everything else follows from the copies
+    // in by events, and the internal streams are FIFO across calls.
+    cudaEvent_t* done_ev = nullptr;
+    for (auto& e : pipe->done)
+        if (e.first == hp->staging) done_ev = &e.second;
+    if (done_ev) {
+        if (cudaStreamWaitEvent(pipe->h2d, *done_ev, 0) != cudaSuccess) return LA_ERR_CUDA;
+    } else {
+        if (pipe->done.size() >= 64) {  // forget the oldest (a call on it is ordered by its caller's stream)
+            cudaEventDestroy(pipe->done.front().second);
+            pipe->done.erase(pipe->done.begin());
+        }
+        cudaEvent_t e;
+        if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return LA_ERR_CUDA;
+        pipe->done.emplace_back(hp->staging, e);
+        done_ev = &pipe->done.back().second;
+        if ((st = chain(s, pipe->h2d)) != LA_OK) return st;
+    }
     if ((st = copy(dev + P.meta, pipe->meta, P.meta_bytes, cudaMemcpyHostToDevice, pipe->h2d)) != LA_OK) return st;
     if (cudaEventRecord(pipe->meta_ev, pipe->h2d) != cudaSuccess) return LA_ERR_CUDA;
     pipe->meta_pending = true;
@@ -376,7 +394,8 @@ la_status gdn_fwd_host(const la_gdn_fwd_host_params* hp, void* stream) {
             return st;
     }
     // the caller's stream continues after the last copy out (which follows every forward)
-    return chain(pipe->d2h, s);
+    if (cudaEventRecord(*done_ev, pipe->d2h) != cudaSuccess) return LA_ERR_CUDA;
+    return cudaStreamWaitEvent(s, *done_ev, 0) == cudaSuccess ? LA_OK : LA_ERR_CUDA;
 }
 
 }  // extern "C"

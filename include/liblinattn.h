@@ -193,13 +193,16 @@ la_status gdn_fwd_static_workspace(const la_gdn_fwd_params* p, void* stream);
  *     ignored; state_indices must be NULL and num_householder <= 1.
  *   staging: DEVICE memory of at least la_gdn_fwd_host_staging_bytes(p)
  *     bytes, 256-byte aligned, owned by the caller (the device copies of every
- *     input and output plus per-stream scratch).  Two calls sharing a staging
- *     buffer must be ordered on one stream.
+ *     input and output plus per-stream scratch).
  *   ranges: >= 1.
- * Stream semantics: every copy and kernel is ordered after the work already
- * enqueued on `stream`, and `stream` is made to wait for the last copy out;
- * the call returns once everything is enqueued (host buffers must stay valid
- * and the outputs must not be read until `stream` has been synchronised).
+ * Ordering: the first call with a given staging buffer is ordered after the
+ * work already enqueued on `stream`; a later call with the same buffer is
+ * ordered after the previous call that used it (not after `stream`: its
+ * inputs are host memory), so a caller that alternates two staging buffers
+ * lets the copies of one call run under the last forwards of the one before.
+ * `stream` is made to wait for the call's last copy out.  The call returns
+ * once everything is enqueued (host buffers must stay valid and the outputs
+ * must not be read until `stream` has been synchronised).
  * The host may block while the previous call's small metadata copy is still
  * pending.  Not capturable in a CUDA graph (use gdn_fwd on device buffers).
  * Errors: argument checks as gdn_fwd, plus LA_ERR_BAD_SEQLENS for a host

@@ -429,6 +429,30 @@ def test_host_pipeline_transforms_and_options_bitwise():
     assert torch.equal(o_h, o_d.cpu()) and torch.equal(c_h, c_d.cpu())
 
 
+@pytest.mark.parametrize("nstaging", [1, 2])
+def test_host_pipeline_back_to_back_calls(nstaging):
+    """Four gdn_fwd_host calls enqueued without a host synchronisation, on two different input
+    sets and into four output sets, with one staging buffer or two used in turn (a call is then
+    ordered only after the last call on its buffer): every output equals its device call."""
+    lengths = [300, 1, 129, 450]
+    ws = [small(lengths, HK=2, HV=2, K=128, V=128, seed=51 + i, initial_state=True, checkpoint_every_n=64,
+                checkpoint_dtype=torch.float32, slow_decay=True) for i in range(2)]
+    pin = lambda x: x.contiguous().pin_memory()
+    host = [[pin(x) for x in (w.q, w.k, w.v, w.g, w.beta, w.initial_state)] for w in ws]
+    refs = [gpu_fwd(w) for w in ws]
+    stagings = [{} for _ in range(nstaging)]
+    outs = []
+    for call in range(4):
+        q, k, v, g, b, s0 = host[call % 2]
+        outs.append(la.gdn_fwd_host(q, k, v, g, b, ws[0].cu_seqlens, initial_state=s0, checkpoint_every_n=64,
+                                    checkpoint_dtype=torch.float32, groups=5, staging=stagings[call % nstaging]))
+    torch.cuda.synchronize()
+    for call, (o_h, f_h, c_h) in enumerate(outs):
+        o_d, f_d, c_d = refs[call % 2]
+        assert np.array_equal(o_h.float().numpy(), o_d), call
+        assert np.array_equal(f_h.numpy(), f_d) and np.array_equal(c_h.numpy(), c_d), call
+
+
 @pytest.mark.parametrize("cut", [128, 200])
 def test_state_round_trip_split_run(cut):
     """Running tokens [0, m) and then [m, L) from the first part's fp32 final state equals the
