@@ -357,7 +357,8 @@ def run_ours(args, world, rank, local):
         barrier(world)
         e2e_ms = max_over_ranks(x0.elapsed_time(x1) / e2e_steps, world)
         e2e = {"value": tokens / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "groups": args.e2e_groups}
+               "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "ranges": args.e2e_groups,
+               "staging_buffers": 2, "entry": "gdn_fwd_host (C ABI, host buffers)"}
         assert torch.equal(host_out[0].view(torch.int16), o.cpu().view(torch.int16)), "e2e output differs"
         assert torch.equal(host_out[1], fin.cpu()) and torch.equal(host_out[2], ck.cpu()), "e2e states differ"
 
