@@ -223,7 +223,9 @@ def run_reference(args, world, rank):
     from gated_delta_rule_29_gb300 import workloads as W
     w = W.config(3)
     cores = os.cpu_count() or 1
-    units = cpu_units(w, args.ref_units)
+    # one (sequence, head) unit per host core per step unless told otherwise: every core works
+    units = cpu_units(w, args.ref_units if args.ref_units else min(cores, w.N * w.HV))
+    cores = min(cores, len(units))  # threads that actually run
     for _ in range(args.warmup):
         oracle_sample(w, units[:1], cores)
     times, th = [], 0
@@ -946,7 +948,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-units", type=int, default=256,
                     help="(sequence, head) units in the CPU-baseline sample (256 = the whole batch)")
-    ap.add_argument("--ref-units", type=int, default=2, help="units per step of the reference arm")
+    ap.add_argument("--ref-units", type=int, default=0,
+                    help="(sequence, head) units per step of the reference arm (0: one per host core)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--e2e-groups", type=int, default=16, help="token ranges pipelined by gdn_fwd_host")
