@@ -480,6 +480,8 @@ def gdn_fwd_host(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Ten
     HO = HV
     cu = cu_seqlens.detach().to("cpu").contiguous()
     N = cu.numel() - 1
+    if N < 0 or int(cu[0]) != 0 or int(cu[-1]) != T or bool((cu[1:] < cu[:-1]).any()):
+        raise ValueError("cu_seqlens must start at 0, be nondecreasing and end at T")
     n = int(checkpoint_every_n or 0)
     R = checkpoint_rows(cu, n) if n else 0
     if out is None:

@@ -453,6 +453,35 @@ def test_host_pipeline_back_to_back_calls(nstaging):
         assert np.array_equal(f_h.numpy(), f_d) and np.array_equal(c_h.numpy(), c_d), call
 
 
+def test_host_pipeline_pageable_buffers_and_two_threads():
+    """gdn_fwd_host on pageable (not pinned) host tensors, outputs included, and two host
+    threads calling it at once with their own staging buffers: the same bits as gdn_fwd."""
+    import threading
+    ws = [small([260, 64, 3], HK=1, HV=2, K=64, V=128, seed=61 + i, initial_state=True, checkpoint_every_n=64,
+                checkpoint_dtype=torch.float32, slow_decay=True) for i in range(2)]
+    refs = [gpu_fwd(w) for w in ws]
+
+    def run(w, out):
+        o = torch.empty(w.T, w.HV, w.V, dtype=torch.bfloat16)
+        f = torch.empty(w.N, w.HV, w.K, w.V)
+        c = torch.empty(la.checkpoint_rows(w.cu_seqlens, 64), w.HV, w.K, w.V)
+        s = torch.cuda.Stream()
+        la.gdn_fwd_host(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, initial_state=w.initial_state, checkpoint_every_n=64,
+                        checkpoint_dtype=torch.float32, out=(o, f, c), groups=3, staging={}, stream=s)
+        s.synchronize()
+        out.extend([o, f, c])
+
+    outs = [[], []]
+    threads = [threading.Thread(target=run, args=(w, out)) for w, out in zip(ws, outs)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    for (o, f, c), (o_d, f_d, c_d) in zip(outs, refs):
+        assert np.array_equal(o.float().numpy(), o_d) and np.array_equal(f.numpy(), f_d)
+        assert np.array_equal(c.numpy(), c_d)
+
+
 @pytest.mark.parametrize("cut", [128, 200])
 def test_state_round_trip_split_run(cut):
     """Running tokens [0, m) and then [m, L) from the first part's fp32 final state equals the

@@ -64,3 +64,20 @@ def test_plan_checkpoint_cadence_sets_the_cut():
     """With checkpoints every 192 tokens the cut is a multiple of lcm(64, 192) = 192."""
     P, _ = check_plan([1000, 1000], 8, 192)
     assert P % math.lcm(64, 192) == 0
+
+
+def test_host_entry_rejects_bad_seqlens_before_any_device_work():
+    """A cu_seqlens that is not 0, nondecreasing, T makes gdn_fwd_host raise on the host before
+    any device work (the library's own entry returns LA_ERR_BAD_SEQLENS for it too, see
+    test_abi)."""
+    import torch
+
+    import gated_delta_rule_29_gb300 as la
+    T, H, D = 128, 1, 64
+    q = torch.zeros(T, H, D, dtype=torch.bfloat16)
+    v = torch.zeros(T, H, D, dtype=torch.bfloat16)
+    g = torch.zeros(T, H)
+    b = torch.zeros(T, H)
+    for cu in ([0, 100, 64, 128], [0, 64, 100], [8, 64, 128]):
+        with pytest.raises(ValueError):
+            la.gdn_fwd_host(q, q, v, g, b, torch.tensor(cu, dtype=torch.int32), device=torch.device("cuda", 0))
