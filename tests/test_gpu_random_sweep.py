@@ -119,7 +119,7 @@ def label(c):
     return " ".join(f"{x}={c[x]}" for x in keys) + (f" ck_dtype={c['ck_dtype']}" if c["ck"] else "")
 
 
-@pytest.mark.parametrize("case", range(24))
+@pytest.mark.parametrize("case", range(64))
 def test_forward_random_case(case):
     c = draw_case(7000 + case)
     d = dev()
@@ -144,7 +144,7 @@ def test_forward_random_case(case):
     assert errs["o"] <= O_TOL and errs["final"] <= S_TOL and errs.get("ckpt", 0.0) <= ck_tol, (label(c), errs)
 
 
-@pytest.mark.parametrize("case", range(10))
+@pytest.mark.parametrize("case", range(20))
 def test_backward_random_case(case):
     c = draw_case(7500 + case, backward=True)
     d = dev()
