@@ -482,6 +482,29 @@ def test_host_pipeline_pageable_buffers_and_two_threads():
         assert np.array_equal(c.numpy(), c_d)
 
 
+@pytest.mark.parametrize("K,V", [(128, 128), (64, 64)])
+def test_extreme_but_valid_values(K, V):
+    """Gates from 0 down to -30 (decays spanning far more than fp32's range within a chunk: the
+    kernel's factorised decays must fall back to direct ones), beta exactly 0 or 1, all-zero q
+    and k rows under the L2 norm (the norm's epsilon keeps them zero), and a start state."""
+    w = small([300, 77, 64], HK=2, HV=2, K=K, V=V, seed=71 + K, initial_state=True, checkpoint_every_n=64,
+              checkpoint_dtype=torch.float32)
+    gen = torch.Generator().manual_seed(72)
+    T = w.T
+    u = torch.rand(T, w.HV, generator=gen)
+    g = torch.where(u < 0.1, torch.full_like(u, -30.0), torch.where(u < 0.5, torch.zeros_like(u), -0.01 * u))
+    r = torch.rand(T, w.HV, generator=gen)
+    beta = torch.where(r < 0.2, torch.zeros_like(r), torch.where(r < 0.4, torch.ones_like(r), r))
+    q, k = w.q.clone(), w.k.clone()
+    zq = torch.rand(T, generator=gen) < 0.05
+    zk = torch.rand(T, generator=gen) < 0.05
+    q[zq] = 0
+    k[zk] = 0
+    w.q, w.k, w.g, w.beta = q, k, g.contiguous(), beta.contiguous()
+    got = gpu_fwd(w)
+    compare_units(w, got, oracle_fwd(w), all_units(w))
+
+
 @pytest.mark.parametrize("cut", [128, 200])
 def test_state_round_trip_split_run(cut):
     """Running tokens [0, m) and then [m, L) from the first part's fp32 final state equals the
