@@ -279,3 +279,28 @@ def test_bwd_out_buffers_rejected_when_mismatched():
         la.gdn_bwd(*args, out=(torch.empty(w.T, w.HK, w.K + 1, dtype=torch.bfloat16, device=d),))
     with pytest.raises(ValueError):
         la.gdn_bwd(*args, out=(None, None, None, torch.empty(w.T, w.HV, dtype=torch.float64, device=d)))
+
+
+def test_bwd_extreme_but_valid_values():
+    """Gates from 0 down to -30, beta exactly 0 or 1, all-zero q and k rows under the norm, a
+    start state and a final-state cotangent: finite gradients within tolerance of the oracle."""
+    w = W.draw("bwd extreme", [200, 77, 64], 2, 2, 128, 128, seed=471, initial_state=True)
+    gen = torch.Generator().manual_seed(472)
+    T = w.T
+    u = torch.rand(T, w.HV, generator=gen)
+    w.g = torch.where(u < 0.1, torch.full_like(u, -30.0), torch.where(u < 0.5, torch.zeros_like(u), -0.01 * u))
+    r = torch.rand(T, w.HV, generator=gen)
+    w.beta = torch.where(r < 0.2, torch.zeros_like(r), torch.where(r < 0.4, torch.ones_like(r), r)).contiguous()
+    w.g = w.g.contiguous()
+    q, k = w.q.clone(), w.k.clone()
+    q[torch.rand(T, generator=gen) < 0.05] = 0
+    k[torch.rand(T, generator=gen) < 0.05] = 0
+    w.q, w.k = q, k
+    do, dfin = cotangents(w, 473)
+    got = run_bwd(w, do, dfin)
+    for x in got:
+        if x is not None:
+            assert np.isfinite(x).all()
+    ref = oracle.gdn_bwd(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, do, initial_state=w.initial_state,
+                         d_final_state=dfin)
+    compare(w, got, ref)
