@@ -142,3 +142,30 @@ def test_bad_state_index_sets_status():
     run = la.gdn_decode(w.q.to(d), w.k.to(d), w.v.to(d), w.g.to(d), w.beta.to(d), pool.to(d),
                         state_indices=idx.to(d), status=status)
     assert la.read_status(status) == 0 and torch.isfinite(run.float()).all()
+
+
+def test_decode_fused_projection_views_and_strided_output():
+    """q, k, v as column slices of one fused [N, 2 HK K + HV V] projection, g and beta as slices
+    of one [N, 2 HV] buffer, o written into a column slice of a wider buffer: the same bits as
+    with contiguous tensors, and within tolerance of the oracle."""
+    N, HK, HV, K, V, P = 48, 2, 4, 128, 64, 64
+    w, pool, idx = decode_case(N, HK, HV, K, V, P, seed=351)
+    d = dev()
+    a, b = HK * K, 2 * HK * K
+    fused = torch.cat([w.q.reshape(N, -1), w.k.reshape(N, -1), w.v.reshape(N, -1)], dim=1).to(d)
+    q, k, v = fused[:, :a].view(N, HK, K), fused[:, a:b].view(N, HK, K), fused[:, b:].view(N, HV, V)
+    gb = torch.cat([w.g, w.beta], dim=1).to(d)
+    g, beta = gb[:, :HV], gb[:, HV:]
+    assert not q.is_contiguous() and not g.is_contiguous()
+    wide = torch.full((N, HV, V + 32), 7.0, dtype=torch.bfloat16, device=d)
+    o = wide[:, :, :V]
+    pool_s = pool.to(d)
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    la.gdn_decode(q, k, v, g, beta, pool_s, state_indices=idx.to(d), o=o, status=status)
+    assert la.read_status(status) == 0
+    assert bool((wide[:, :, V:] == 7.0).all()), "a write outside the output view"
+    o_c, pool_c = run_decode(w, pool, idx)
+    assert np.array_equal(o.float().cpu().numpy(), o_c)
+    assert np.array_equal(pool_s.float().cpu().numpy(), pool_c)
+    ref = oracle.gdn_fwd(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, initial_state=pool, state_indices=idx)
+    check_pool(w, pool, idx, o_c, pool_c, ref, S_TOL)
