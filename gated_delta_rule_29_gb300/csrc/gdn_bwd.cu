@@ -21,7 +21,11 @@
 // inverse norms as row or column scales of the other operand.
 //
 // Mapping.  One CTA of 256 threads (8 warps) per (sequence, head) walks the chunks in reverse
-// and carries dS in a global per-unit buffer.  The value columns are independent chains (each
+// and carries dS in a global per-unit buffer.  When the units outnumber the CTAs that fit on the
+// GPU at once, each unit's chunks are cut into four consecutive ranges: launch after launch, one
+// wave each, the work items are the units' last ranges, then the ranges before them, so that a
+// range's dS comes from the previous launch through the global buffer (exact fp32), the results
+// are the same bits as one walk, and the units fill 1.75 waves instead of 2 (e.g. 256 on 152).  The value columns are independent chains (each
 // column of S evolves on its own), so a chunk is processed in 16-column tiles of S, dS, V and
 // dO; the tile-independent parts (K, Q, A, T, P, the decays) are formed once per chunk in
 // shared memory and the cross-column sums (dA, dP, dK, dQ, dbeta, db) accumulate over the
@@ -210,18 +214,25 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
     if (__float_as_int(s.red[0]) != LA_OK) return;  // bad cu_seqlens: the forward ran nothing
     __syncthreads();
     const int HO = a.HV;
-    const int unit = blockIdx.x;
+    const int U = a.N * HO;
+    const int item = a.item_base + static_cast<int>(blockIdx.x);
+    const int P = a.pieces;
+    const int piece = P - 1 - item / U;  // the unit's chunk range, counted from its start
+    const int unit = item % U;
     const int seq = unit / HO, h = unit % HO;
     const int hk = h / a.group;
     const int64_t ts = a.cu64 ? static_cast<const int64_t*>(a.cu)[seq] : static_cast<const int32_t*>(a.cu)[seq];
     const int64_t te = a.cu64 ? static_cast<const int64_t*>(a.cu)[seq + 1] : static_cast<const int32_t*>(a.cu)[seq + 1];
     const int64_t L = te - ts;
     const int nch = static_cast<int>((L + kC - 1) / kC);
+    const int lo = static_cast<int>(static_cast<int64_t>(piece) * nch / P);  // chunks lo .. hi - 1
+    const int hi = static_cast<int>(static_cast<int64_t>(piece + 1) * nch / P);
     const int64_t KV = static_cast<int64_t>(KD) * VD;
     float* dSg = a.dS_work + static_cast<int64_t>(unit) * KV;  // carried dS (global, L2 resident)
 
-    // dS after the last token: d_final_state or zero
-    for (int64_t e = tid; e < KV; e += kBT) dSg[e] = a.dfinal ? a.dfinal[unit * KV + e] : 0.f;
+    // dS after the last token: d_final_state or zero (set by the last range, which runs first)
+    if (piece == P - 1)
+        for (int64_t e = tid; e < KV; e += kBT) dSg[e] = a.dfinal ? a.dfinal[unit * KV + e] : 0.f;
     __syncthreads();
 
     constexpr int KSL = KD / 4;
@@ -273,7 +284,7 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
         cp_async_commit();
     };
     int pb = 0;  // buffer of the current tile
-    if (nch > 0) fetch_tile(nch - 1, 0, 0);
+    if (hi > lo) fetch_tile(hi - 1, 0, 0);
 
     const bool kwarp = w < 4;  // owns dK_hat rows (else dQ_hat rows) 16 (w % 4) .. + 15
     const int om0 = 16 * (w & 3);
@@ -281,7 +292,7 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
     const float gdt = a.gate_mode == LA_GATE_SOFTPLUS ? a.dt_bias[h] : 0.f;
     float pa_log = 0.f, pa_dt = 0.f;  // this token slot's sums for d_a_log and d_dt_bias (tid < 64)
 
-    for (int c = nch - 1; c >= 0; --c) {
+    for (int c = hi - 1; c >= lo; --c) {
         const int64_t t0 = ts + static_cast<int64_t>(c) * kC;
         const int n = static_cast<int>(L - static_cast<int64_t>(c) * kC < kC ? L - static_cast<int64_t>(c) * kC : kC);
 
@@ -570,7 +581,7 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
             // the next tile (this chunk's next columns, else the previous chunk's first) streams
             // into the other buffer; the staged V / dO rows have been read above
             if (j0 + kVT < VD) fetch_tile(c, j0 + kVT, pb ^ 1);
-            else if (c > 0) fetch_tile(c - 1, 0, pb ^ 1);
+            else if (c > lo) fetch_tile(c - 1, 0, pb ^ 1);
             {
                 // D = T Y (T lower: column tiles up to the diagonal);  dD = scale P^T dO + Gamma_C (K dS_J)
                 float cD[4] = {0.f, 0.f, 0.f, 0.f}, cE[4] = {0.f, 0.f, 0.f, 0.f};
@@ -965,23 +976,26 @@ __global__ void __launch_bounds__(kBT, 1) gdn_bwd_kernel(const BwdArgs a) {
     }
     __syncthreads();
     if (a.gpart && tid == 0) {
-        a.gpart[2 * unit] = s.red[0] + s.red[2];
-        a.gpart[2 * unit + 1] = s.red[1] + s.red[3];
+        const int64_t slot = static_cast<int64_t>(unit) * P + piece;
+        a.gpart[2 * slot] = s.red[0] + s.red[2];
+        a.gpart[2 * slot + 1] = s.red[1] + s.red[3];
     }
-    if (a.ds0) {
+    if (a.ds0 && piece == 0) {
         for (int64_t e = tid; e < KV; e += kBT) a.ds0[unit * KV + e] = dSg[e];
     }
 }
 
-// d_a_log and d_dt_bias of a head: the per-sequence sums added in sequence order.
+// d_a_log and d_dt_bias of a head: the per-range sums added in sequence and range order.
 __global__ void gdn_bwd_gate_param_kernel(const BwdArgs a) {
     const int h = blockIdx.x * blockDim.x + threadIdx.x;
     if (h >= a.HV) return;
     float sa = 0.f, sd = 0.f;
-    for (int i = 0; i < a.N; ++i) {
-        sa += a.gpart[2 * (static_cast<int64_t>(i) * a.HV + h)];
-        sd += a.gpart[2 * (static_cast<int64_t>(i) * a.HV + h) + 1];
-    }
+    for (int i = 0; i < a.N; ++i)
+        for (int pc = 0; pc < a.pieces; ++pc) {
+            const int64_t slot = (static_cast<int64_t>(i) * a.HV + h) * a.pieces + pc;
+            sa += a.gpart[2 * slot];
+            sd += a.gpart[2 * slot + 1];
+        }
     if (a.d_a_log) a.d_a_log[h] = sa;
     if (a.d_dt_bias) a.d_dt_bias[h] = sd;
 }
@@ -1006,17 +1020,42 @@ __global__ void gdn_bwd_group_sum_kernel(const BwdArgs a) {
     }
 }
 
+// CTAs of the backward kernel resident on the whole GPU at once (one wave), per device and
+// head-dimension pair; looked up on the first launch (outside any stream capture).
+int g_bwd_wave[128][4];
+
 template <int KD, int VD>
-cudaError_t launch_bwd_kv(const BwdArgs& a, cudaStream_t s) {
+cudaError_t launch_bwd_kv(const BwdArgs& a0, cudaStream_t s) {
+    BwdArgs a = a0;
     const int units = a.N * a.HV;
+    a.pieces = 1;
+    a.item_base = 0;
     if (units > 0) {
         auto* fn = gdn_bwd_kernel<KD, VD>;
         const int smem = static_cast<int>(sizeof(BwdSmem<KD>));
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
-        fn<<<units, kBT, smem, s>>>(a);
-        e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
+        int dev = 0;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+        int& wave = g_bwd_wave[dev & 127][(KD == 128 ? 2 : 0) + (VD == 128 ? 1 : 0)];
+        if (wave == 0) {
+            int sms = 0, per_sm = 0;
+            if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+            if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kBT, smem)) != cudaSuccess) return e;
+            wave = sms * (per_sm > 0 ? per_sm : 1);
+        }
+        // more units than one wave: four ranges per unit, launched range by range in waves (a
+        // range's successor in the unit is at least `units` >= `wave` items earlier, so in an
+        // earlier launch)
+        if (units > wave) a.pieces = kBwdPieces;
+        const int items = units * a.pieces;
+        const int grid = a.pieces == 1 ? units : wave;
+        for (int base = 0; base < items; base += grid) {
+            a.item_base = base;
+            fn<<<items - base < grid ? items - base : grid, kBT, smem, s>>>(a);
+            e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+        }
     }
     if (a.group > 1 && a.T > 0 && !a.state_only) {
         gdn_bwd_group_sum_kernel<<<1024, 256, 0, s>>>(a);

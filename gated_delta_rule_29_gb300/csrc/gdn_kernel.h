@@ -169,10 +169,15 @@ struct BwdArgs {
     float gate_lb;                   // (LA_GATE_SIGMOID_BOUND)
     int32_t beta_sigmoid;            // beta holds logits
     int32_t beta_bf16;               // beta is bf16
-    float* gpart;                    // [N * HO][2] per-unit sums for d_a_log, d_dt_bias, or null
+    float* gpart;                    // [N * HO][pieces][2] per-piece sums for d_a_log, d_dt_bias, or null
     float* d_a_log;                  // [HO] or null
     float* d_dt_bias;                // [HO] or null
+    // A unit's chunks are cut into `pieces` consecutive ranges run in reverse order by successive
+    // launches; this launch's CTA b runs work item item_base + b (pieces 1: one item per unit).
+    int32_t pieces;
+    int32_t item_base;
 };
+constexpr int kBwdPieces = 4;
 
 // Gated DeltaProduct: the update timeline for the chunk kernel, and the per-token outputs.
 struct GdpArgs {

@@ -526,8 +526,8 @@ BwdLayout bwd_layout(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, in
     off += up256(static_cast<size_t>(N) * HV * K * V * sizeof(float));
     L.gh = off;
     if (HV != HK) off += up256(2 * static_cast<size_t>(T) * HV * K * sizeof(float));
-    L.gp = off;  // per (sequence, head) sums for the softplus gate's parameter gradients
-    off += up256(2 * static_cast<size_t>(N) * HV * sizeof(float));
+    L.gp = off;  // per (sequence, head, chunk range) sums for the softplus gate's parameter gradients
+    off += up256(2 * static_cast<size_t>(N) * HV * la::kBwdPieces * sizeof(float));
     L.total = off;
     return L;
 }
