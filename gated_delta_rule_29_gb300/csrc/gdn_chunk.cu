@@ -29,7 +29,11 @@
 //
 // Tiles: a forward unit has one value tile.  A summary unit has a value tile
 // (the span end state from the given start) and a transition tile: the same
-// recurrence on P with v = 0 and P0 = I, stored transposed.
+// recurrence on P with v = 0 and P0 = I, stored transposed.  When the summary's
+// units outnumber one wave (it runs one CTA per SM), each unit's chunks run as
+// four consecutive ranges in successive launches, a range starting from the
+// exact fp32 state the previous one left in the outputs: the same bits as one
+// walk, in fewer waves.
 //
 // Gated DeltaProduct (mode kModeGdp, 2 <= n <= 64 updates per token): the same
 // recurrence walked on the update timeline (n rows per token of k, v, beta; a
@@ -46,6 +50,7 @@
 namespace la {
 
 constexpr int kCta = 128;  // threads per CTA
+constexpr int kSumPieces = 4;  // chunk ranges per summary unit when the units outnumber one wave
 
 // ------------------------------------------------------------------ shared memory map
 constexpr uint32_t SM_KQ = 0;        // [region 0..1][128 rows: K 0-63, Q 64-127][128 B]
@@ -371,6 +376,7 @@ __global__ void __launch_bounds__(kCta, 2)
                      const ChunkArgs a) {
     constexpr bool kFwd = MODE != kModeSummary;  // queries and outputs (the forward, or GDP's)
     constexpr bool kGdp = MODE == kModeGdp;
+    constexpr bool kSum = MODE == kModeSummary;
     constexpr int KP = KD / 16;  // 16-column pieces of the state
     // GDP: the tokens whose last update row falls in a chunk of 64 update rows (at most QR of
     // them) have their queries in rows 0 .. QR-1 of the query half of the K/Q tile (the other
@@ -444,16 +450,22 @@ __global__ void __launch_bounds__(kCta, 2)
     const uint32_t kq_bytes = KD * 128u + (kFwd ? static_cast<uint32_t>(KD / 64) * QR * 128u : 0u);
     const uint32_t v_bytes = static_cast<uint32_t>(a.V) * 128u;
 
-    for (;;) {
+    const bool ranged = kSum && a.pieces > 1;  // one range item per CTA, from blockIdx
+    for (int iter = 0;; ++iter) {
         if (tid == 0) {
-            const unsigned long long u = atomicAdd(reinterpret_cast<unsigned long long*>(&a.hdr->ticket), 1ull);
+            const unsigned long long u =
+                ranged ? (iter == 0 ? static_cast<unsigned long long>(blockIdx.x) : 0x7FFFFFFFFFFFFFFFull)
+                       : atomicAdd(reinterpret_cast<unsigned long long*>(&a.hdr->ticket), 1ull);
             sc.unit_lo = static_cast<int32_t>(u & 0xFFFFFFFFull);
             sc.unit_hi = static_cast<int32_t>(u >> 32);
         }
         __syncthreads();
-        const int64_t unit = (static_cast<int64_t>(sc.unit_hi) << 32) | static_cast<uint32_t>(sc.unit_lo);
+        const int64_t taken = (static_cast<int64_t>(sc.unit_hi) << 32) | static_cast<uint32_t>(sc.unit_lo);
         __syncthreads();  // every thread has read the ticket before thread 0 may take the next one
-        if (unit >= a.num_units) break;
+        if (taken >= (ranged ? a.items : a.num_units)) break;
+        const int64_t item = ranged ? a.item_base + taken : taken;
+        const int rng = ranged ? static_cast<int>(item / a.num_units) : 0;  // the chunk range
+        const int64_t unit = ranged ? item % a.num_units : item;
         const int seq = a.order[unit / per_seq];
         const int rem = static_cast<int>(unit % per_seq);
         const int h = rem / a.tiles_per_head;
@@ -465,6 +477,11 @@ __global__ void __launch_bounds__(kCta, 2)
         const int64_t ts = tok_s * NH;
         const int64_t L = (cu_get(a.cu, a.cu64, seq + 1) - tok_s) * NH;
         const int nchunks = static_cast<int>((L + kChunk - 1) / kChunk);
+        // this item's chunks lo .. hi - 1 (all of them unless ranged)
+        const int lo = ranged ? static_cast<int>(static_cast<int64_t>(rng) * nchunks / a.pieces) : 0;
+        const int hi = ranged ? static_cast<int>(static_cast<int64_t>(rng + 1) * nchunks / a.pieces) : nchunks;
+        if (lo == hi && rng > 0) continue;  // an empty later range: the state stays where it is
+        const int64_t tlo = static_cast<int64_t>(lo) * kChunk;  // first update row of the range
         const int64_t unit_state = static_cast<int64_t>(seq) * HO + h;
         // the start state's slot, and where the end state goes (the same pool slot when a state
         // pool is used: written back in place)
@@ -490,9 +507,9 @@ __global__ void __launch_bounds__(kCta, 2)
             gA = -expf(a.a_log[h]);
             gdt = a.dt_bias[h];
         }
-        if (tid < 64 && tid < L) {
-            g_nx = gate_row<kGdp>(a, ts + tid, h, gA, gdt);
-            b_nx = beta_at(a, ts + tid, h);
+        if (tid < 64 && tid < L - tlo) {
+            g_nx = gate_row<kGdp>(a, ts + tlo + tid, h, gA, gdt);
+            b_nx = beta_at(a, ts + tlo + tid, h);
         }
         if (tid < 64) {
             float x = g_nx * kLog2e;
@@ -501,7 +518,7 @@ __global__ void __launch_bounds__(kCta, 2)
             if ((tid & 31) == 0) sc.gsum[tid >> 5] = x;
         }
         __syncthreads();
-        const float gam0 = nchunks > 0 ? exp2f(sc.gsum[0] + sc.gsum[1]) : 1.f;
+        const float gam0 = hi > lo ? exp2f(sc.gsum[0] + sc.gsum[1]) : 1.f;
 
         // ---- initial state -> TMEM (fp32 2^{b_C} S^T), WB (bf16 S^T, the A operand of K S),
         // checkpoint entry 0, and the end state of an empty sequence
@@ -509,6 +526,9 @@ __global__ void __launch_bounds__(kCta, 2)
             const int64_t base = s0_unit * KD * a.V + r;
             const int64_t fbase0 = fin_unit * KD * a.V + r;
             const bool ckpt0 = kFwd && a.ckpt && nchunks > 0 && r < a.V;
+            // a later range starts from what the previous range left in the outputs: the end
+            // state (fp32, value tile) or the transition (stored transposed: lane r reads row r)
+            const bool from_out = ranged && rng > 0;
             const int64_t cbase = ckpt0 ? ((a.ckpt_off[seq] * HO + h) * KD) * a.V + r : 0;
 #pragma unroll 1
             for (int p = 0; p < KP; ++p) {
@@ -517,7 +537,13 @@ __global__ void __launch_bounds__(kCta, 2)
                 for (int e = 0; e < 16; ++e) {
                     const int k = 16 * p + e;
                     float val = 0.f;
-                    if (value_tile) {
+                    if (from_out) {
+                        if (value_tile) {
+                            if (r < a.V) val = a.final_state[fbase0 + static_cast<int64_t>(k) * a.V];
+                        } else if (r < KD) {
+                            val = a.transition[(unit_state * KD + r) * KD + k];
+                        }
+                    } else if (value_tile) {
                         if (a.s0 && r < a.V) {
                             const int64_t idx = base + static_cast<int64_t>(k) * a.V;
                             val = a.s0_bf16 ? bf16_bits_to_f(static_cast<const uint16_t*>(a.s0)[idx])
@@ -542,7 +568,7 @@ __global__ void __launch_bounds__(kCta, 2)
                         else static_cast<float*>(a.ckpt)[idx] = x[e];
                     }
                 }
-                if (nchunks == 0) {  // empty sequence: the start state is the end state
+                if (hi == lo) {  // no chunks (an empty sequence, or an empty first range): start = end
                     if (value_tile) {
                         if (a.final_state && r < a.V)
 #pragma unroll
@@ -563,31 +589,32 @@ __global__ void __launch_bounds__(kCta, 2)
         }
 
         // ---- first chunk's tiles and per-token scalars
-        if (nchunks > 0) {
+        if (hi > lo) {
+            const int64_t tf = ts + tlo;
             if (tid == 0 && !a.test_skip_tile_load) {
                 mbar_arrive_expect_tx(&sc.bar_kq, kq_bytes);
 #pragma unroll
                 for (int rg = 0; rg < KD / 64; ++rg) {
-                    tma_load_3d(KQ + rg * 16384, &kmap, &sc.bar_kq, rg * 64, hk, static_cast<int>(ts));
+                    tma_load_3d(KQ + rg * 16384, &kmap, &sc.bar_kq, rg * 64, hk, static_cast<int>(tf));
                     if (kFwd)
-                        tma_load_3d(KQ + rg * 16384 + 8192, &qmap, &sc.bar_kq, rg * 64, hk, static_cast<int>(ts / NH));
+                        tma_load_3d(KQ + rg * 16384 + 8192, &qmap, &sc.bar_kq, rg * 64, hk, static_cast<int>(tf / NH));
                 }
             }
             if (tid == 0) {
                 if (value_tile) {
                     mbar_arrive_expect_tx(&sc.bar_v, v_bytes);
                     for (int rg = 0; rg < a.V / 64; ++rg)
-                        tma_load_3d(VT + rg * 8192, &vmap, &sc.bar_v, rg * 64, h, static_cast<int>(ts));
+                        tma_load_3d(VT + rg * 8192, &vmap, &sc.bar_v, rg * 64, h, static_cast<int>(tf));
                 }
             }
             pend_kq = !a.test_skip_tile_load;
             pend_v = value_tile;
         }
-        for (int c = 0; c < nchunks; ++c) {
+        for (int c = lo; c < hi; ++c) {
             const int64_t t0 = ts + static_cast<int64_t>(c) * kChunk;
             const int64_t left = L - static_cast<int64_t>(c) * kChunk;
             const int n = left < kChunk ? static_cast<int>(left) : kChunk;
-            const bool last = c + 1 == nchunks;
+            const bool last = c + 1 == hi;
             const bool o_tma_chunk = kFwd && a.o_tma && n == kChunk;
             // the chunk's query tokens: tok0 .. tok0 + nq - 1, those whose last update row is in it
             // (32-bit arithmetic relative to the sequence start, which is a token boundary)
@@ -1116,9 +1143,27 @@ static cudaError_t launch_one(const ChunkArgs& a, const CUtensorMap& qm, const C
     }
     if (per_sm < 1) per_sm = 1;
     const int64_t slots = static_cast<int64_t>(per_sm) * sms;
-    const int grid = static_cast<int>(a.num_units < slots ? a.num_units : slots);
+    ChunkArgs b = a;
+    b.pieces = 1;
+    b.item_base = 0;
+    b.items = 0;
+    if (MODE == kModeSummary && b.num_units > slots) {
+        // four ranges per unit, one wave per launch: item r * units + u's predecessor (u, r - 1)
+        // is `units` > `slots` items earlier, so it ran in an earlier launch
+        b.pieces = kSumPieces;
+        const int64_t items = b.num_units * b.pieces;
+        for (int64_t base = 0; base < items; base += slots) {
+            b.item_base = base;
+            b.items = items - base < slots ? items - base : slots;
+            fn<<<static_cast<int>(b.items), kCta, smem, s>>>(qm, km, vm, om, b);
+            e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
+    }
+    const int grid = static_cast<int>(b.num_units < slots ? b.num_units : slots);
     if (grid <= 0) return cudaSuccess;
-    fn<<<grid, kCta, smem, s>>>(qm, km, vm, om, a);
+    fn<<<grid, kCta, smem, s>>>(qm, km, vm, om, b);
     return cudaGetLastError();
 }
 

@@ -86,6 +86,13 @@ struct ChunkArgs {
     float* transition;               // summary: [N, HO, K, K]
     int32_t tiles_per_head;          // fwd 1; summary 2 (value tile, transition tile)
     int64_t num_units;               // N * HO * tiles_per_head
+    // Summary with more units than one wave: each unit's chunks run as `pieces` consecutive
+    // ranges in successive launches (items r * num_units + u, range r of unit u); this launch's CTA
+    // b runs item item_base + b.  A range starts from the state the previous range left in the
+    // outputs (end state, transition).  pieces 1: one persistent launch over the units.
+    int32_t pieces;
+    int64_t item_base;
+    int64_t items;                   // items of this launch
     WsHeader* hdr;
     const int32_t* order;
     const int64_t* ckpt_off;
