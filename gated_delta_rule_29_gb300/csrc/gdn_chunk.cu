@@ -432,7 +432,7 @@ __global__ void __launch_bounds__(kCta, 2)
     const uint64_t d_pb = sdesc_sw128(smem_u32(PB), 16, 1024);
     const uint64_t d_slo = kFwd ? 0 : sdesc_sw128(smem_u32(SLO), 16, 1024);
 
-    if (kGdp) {
+    if constexpr (kGdp) {
         // the query rows past a chunk's QR tokens are never written by the tile loads: zero them once
         for (int e = tid; e < (KD / 64) * (64 - QR) * 8; e += kCta) {
             const int rg = e / ((64 - QR) * 8), rem = e % ((64 - QR) * 8);
