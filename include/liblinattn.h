@@ -273,6 +273,11 @@ typedef struct la_gdn_summary_params {
  * which is the page's S_init * transition with states read V-major, and the
  * orientation a backward applies (dS_0 = P^T dS_L).  An empty span returns the
  * identity and its start state.
+ * When the (span, head, tile) units outnumber the CTAs the GPU holds at once,
+ * the call enqueues several launches that walk each span in four chunk ranges
+ * and keep the state between ranges in end_state and transition themselves
+ * (each unit reads only its own rows there); the results are the same bits as
+ * one walk.
  */
 la_status gdn_summary(const la_gdn_summary_params* p, void* stream);
 
@@ -366,9 +371,12 @@ typedef struct la_gdn_bwd_params {
  * sum the contributions of its value heads.  When `checkpoints` is NULL the library first
  * re-runs the forward with fp32 checkpoints every 64 tokens into the workspace.  Each
  * (sequence, head) runs in a fixed order, so results do not depend on the batch around a
- * sequence.  With gdn_fwd's input transforms (cudnn-frontend PR #616 fusions) dg and dbeta are
- * the gradients of the raw inputs (the gate input, the beta logits), and the softplus gate also
- * gives d_a_log and d_dt_bias, summed over the batch in sequence order (deterministic).
+ * sequence.  When the (sequence, head) units outnumber the CTAs the GPU holds at once, the
+ * call enqueues several launches that walk each unit in four chunk ranges, the state gradient
+ * handed from range to range exactly (the same bits as one walk).  With gdn_fwd's input
+ * transforms (cudnn-frontend PR #616 fusions) dg and dbeta are the gradients of the raw inputs
+ * (the gate input, the beta logits), and the softplus gate also gives d_a_log and d_dt_bias,
+ * summed over the batch in a fixed order (deterministic).
  */
 la_status gdn_bwd(const la_gdn_bwd_params* p, void* stream);
 
