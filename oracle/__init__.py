@@ -61,6 +61,9 @@ MUTATIONS = {
     18: "summary backward: a token's output term added after its erase step instead of before",
     19: "backward of the softplus gate: d_dt_bias without the sigmoid factor",
     20: "backward of the beta sigmoid: the logit gradient scaled by beta instead of beta (1 - beta)",
+    # planted in the negative-argument branches of the two scalar functions below
+    21: "sigmoid at x < 0 evaluated as 1 / (1 + e^x), the positive branch's formula",
+    22: "softplus at x < 0 evaluated as x + log1p(e^-|x|), dropping the max(x, 0)",
 }
 
 
@@ -145,17 +148,20 @@ def _default_threads():
     return max(1, os.cpu_count() or 1)
 
 
-def softplus(x):
+def softplus(x, mutation=0):
     """log(1 + e^x) in fp64, evaluated as max(x, 0) + log1p(e^-|x|) so it never overflows."""
     x = np.asarray(x, dtype=np.float64)
-    return np.maximum(x, 0.0) + np.log1p(np.exp(-np.abs(x)))
+    head = x if mutation == 22 else np.maximum(x, 0.0)
+    return head + np.log1p(np.exp(-np.abs(x)))
 
 
-def sigmoid(x):
-    """1 / (1 + e^-x) in fp64, evaluated without overflow for either sign of x."""
+def sigmoid(x, mutation=0):
+    """1 / (1 + e^-x) in fp64, evaluated without overflow for either sign of x: with
+    e = e^-|x|, 1 / (1 + e) for x >= 0 and e / (1 + e) = 1 / (1 + e^-x) for x < 0."""
     x = np.asarray(x, dtype=np.float64)
     e = np.exp(-np.abs(x))
-    return np.where(x >= 0, 1.0 / (1.0 + e), e / (1.0 + e))
+    neg = 1.0 / (1.0 + e) if mutation == 21 else e / (1.0 + e)
+    return np.where(x >= 0, 1.0 / (1.0 + e), neg)
 
 
 def gate_transform(g, *, gate="log", a_log=None, dt_bias=None, gate_lower_bound=None, mutation=0):
@@ -173,10 +179,10 @@ def gate_transform(g, *, gate="log", a_log=None, dt_bias=None, gate_lower_bound=
         a = _f64(a_log).reshape(1, -1)
         dt = _f64(dt_bias).reshape(1, -1)
         rate = a if mutation == 10 else np.exp(a)
-        return -rate * softplus(g if mutation == 9 else g + dt)
+        return -rate * softplus(g if mutation == 9 else g + dt, mutation)
     if gate == "sigmoid_bound":
         lb = float(gate_lower_bound)
-        return lb * (g if mutation == 12 else sigmoid(g))
+        return lb * (g if mutation == 12 else sigmoid(g, mutation))
     raise ValueError(f"unknown gate mode {gate!r}")
 
 
@@ -185,7 +191,7 @@ def beta_transform(beta, *, beta_sigmoid=False, mutation=0):
     beta = _f64(beta)
     if not beta_sigmoid:
         return beta
-    return sigmoid(-beta if mutation == 11 else beta)
+    return sigmoid(-beta if mutation == 11 else beta, mutation)
 
 
 def gdn_fwd(q, k, v, g, beta, cu_seqlens, *, scale=None, use_qk_l2norm=True,

@@ -302,63 +302,74 @@ def check_gate_softplus(mutation=0):
     Head 0: a_log = 0, dt_bias = 0, g = 0 gives log decay -ln 2 per token (softplus(0) = ln 2).
     Head 1: a_log = ln 3, dt_bias = ln(e - 1), g = 0 gives -3 per token (softplus = ln e = 1).
     Head 2: a_log = -3, g = 50 checks the large-argument branch: softplus(50) = 50 + log1p(e^-50).
+    Head 3: a_log = 0, dt_bias = -ln 3, g = 0 checks the negative branch: softplus(-ln 3) =
+    ln(1 + 1/3) = ln(4/3), a decay of exactly 3/4 per token.
+    Head 4: a_log = 0, g = -5: softplus(-5) = ln(1 + e^-5).
     The state after L tokens is exp(sum of log decays) S0, and the transition that factor times I.
     """
-    L, K, V = 5, 3, 2
+    L, K, V, H = 5, 3, 2, 5
     rng = np.random.default_rng(91)
     q = rng.standard_normal((L, 1, K))
     k = rng.standard_normal((L, 1, K))
-    v = rng.standard_normal((L, 3, V))
-    S0 = rng.standard_normal((1, 3, K, V))
-    g_raw = np.zeros((L, 3))
+    v = rng.standard_normal((L, H, V))
+    S0 = rng.standard_normal((1, H, K, V))
+    g_raw = np.zeros((L, H))
     g_raw[:, 2] = 50.0
-    a_log = np.array([0.0, math.log(3.0), -3.0])
-    dt_bias = np.array([0.0, math.log(math.e - 1.0), 0.0])
-    beta = np.zeros((L, 3))
+    g_raw[:, 4] = -5.0
+    a_log = np.array([0.0, math.log(3.0), -3.0, 0.0, 0.0])
+    dt_bias = np.array([0.0, math.log(math.e - 1.0), 0.0, -math.log(3.0), 0.0])
+    beta = np.zeros((L, H))
     cu = np.array([0, L])
     kw = dict(gate="softplus", a_log=a_log, dt_bias=dt_bias, mutation=mutation)
     r = oracle.gdn_fwd(q, k, v, g_raw, beta, cu, initial_state=S0, **kw)
     s = oracle.gdn_summary(k, v, g_raw, beta, cu, **kw)
-    per_token = np.array([-math.log(2.0), -3.0, -math.exp(-3.0) * (50.0 + math.log1p(math.exp(-50.0)))])
+    per_token = np.array([-math.log(2.0), -3.0, -math.exp(-3.0) * (50.0 + math.log1p(math.exp(-50.0))),
+                          math.log(0.75), -math.log1p(math.exp(-5.0))])
     factor = np.exp(L * per_token)
-    errs = [_rel(r["final_state"][0, h], factor[h] * S0[0, h]) for h in range(3)]
-    errs += [_rel(s["transition"][0, h], factor[h] * np.eye(K)) for h in range(3)]
+    errs = [_rel(r["final_state"][0, h], factor[h] * S0[0, h]) for h in range(H)]
+    errs += [_rel(s["transition"][0, h], factor[h] * np.eye(K)) for h in range(H)]
     return max(errs)
 
 
 def check_gate_sigmoid_bound(mutation=0):
     """Bounded gate lower_bound * sigmoid(g) with lower_bound = -2 ln 2 and beta = 0:
     g = 0 gives sigmoid 1/2, a decay of exactly 1/2 per token; g = ln 3 gives sigmoid 3/4,
-    a decay of 2^-1.5."""
+    a decay of 2^-1.5; g = -ln 3 (the negative branch) gives sigmoid 1/4, a decay of 2^-0.5."""
     L, K, V = 4, 2, 3
     rng = np.random.default_rng(92)
     q = rng.standard_normal((L, 1, K))
     k = rng.standard_normal((L, 1, K))
-    v = rng.standard_normal((L, 2, V))
-    S0 = rng.standard_normal((1, 2, K, V))
-    g_raw = np.zeros((L, 2))
+    v = rng.standard_normal((L, 3, V))
+    S0 = rng.standard_normal((1, 3, K, V))
+    g_raw = np.zeros((L, 3))
     g_raw[:, 1] = math.log(3.0)
-    beta = np.zeros((L, 2))
+    g_raw[:, 2] = -math.log(3.0)
+    beta = np.zeros((L, 3))
     r = oracle.gdn_fwd(q, k, v, g_raw, beta, np.array([0, L]), initial_state=S0, gate="sigmoid_bound",
                        gate_lower_bound=-2.0 * math.log(2.0), mutation=mutation)
     return max(_rel(r["final_state"][0, 0], 0.5 ** L * S0[0, 0]),
-               _rel(r["final_state"][0, 1], 2.0 ** (-1.5 * L) * S0[0, 1]))
+               _rel(r["final_state"][0, 1], 2.0 ** (-1.5 * L) * S0[0, 1]),
+               _rel(r["final_state"][0, 2], 2.0 ** (-0.5 * L) * S0[0, 2]))
 
 
 def check_beta_sigmoid(mutation=0):
-    """beta given as logits: beta_raw = ln 3 is beta = 3/4.  One token from a zero start with
-    k = q = e_0, no norm, scale 1: S_1 = beta e_0 v^T and o_0 = beta v."""
+    """beta given as logits: beta_raw = ln 3 is beta = 3/4 (head 0) and beta_raw = -ln 3, the
+    negative branch, is beta = 1/4 (head 1).  One token from a zero start with k = q = e_0, no
+    norm, scale 1: S_1 = beta e_0 v^T and o_0 = beta v."""
     K, V = 3, 2
     k = np.zeros((1, 1, K))
     k[0, 0, 0] = 1.0
-    v = np.array([[[1.0, -2.0]]])
-    g = np.array([[-0.3]])
-    beta_raw = np.array([[math.log(3.0)]])
+    v = np.array([[[1.0, -2.0], [3.0, 0.5]]])
+    g = np.array([[-0.3, -0.7]])
+    beta_raw = np.array([[math.log(3.0), -math.log(3.0)]])
     r = oracle.gdn_fwd(k, k, v, g, beta_raw, np.array([0, 1]), scale=1.0, use_qk_l2norm=False,
                        beta_sigmoid=True, mutation=mutation)
-    expect_S = np.zeros((K, V))
-    expect_S[0] = 0.75 * v[0, 0]
-    return max(_rel(r["o"][0, 0], 0.75 * v[0, 0]), _rel(r["final_state"][0, 0], expect_S))
+    errs = []
+    for h, b in ((0, 0.75), (1, 0.25)):
+        expect_S = np.zeros((K, V))
+        expect_S[0] = b * v[0, h]
+        errs += [_rel(r["o"][0, h], b * v[0, h]), _rel(r["final_state"][0, h], expect_S)]
+    return max(errs)
 
 
 def check_state_pool(mutation=0):
