@@ -125,37 +125,58 @@ def test_dense_batch_full_size_sampled(slow):
     assert np.isfinite(got[0]).all() and np.isfinite(got[1]).all()
 
 
+def _ck_offsets(lengths, n):
+    rows = [-(-int(L) // n) for L in lengths]
+    return np.concatenate([[0], np.cumsum(rows)]).astype(np.int64)
+
+
+def _fwd_dev(w, ckpt_n, d):
+    """gdn_fwd on the device, results kept on the device (o bf16, final and checkpoints fp32)."""
+    t = to_dev(w, d)
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    o, fin, ck = la.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu"], use_qk_l2norm=True,
+                            initial_state=t["s0"], output_final_state=True, checkpoint_every_n=ckpt_n,
+                            checkpoint_dtype=torch.float32, status=status)
+    assert la.read_status(status) == 0
+    return o, fin, ck
+
+
 def test_skewed_gva_sampled_and_batch_invariant():
+    """The skewed grouped-head batch: parity on sampled units, then bitwise batch invariance of
+    EVERY sequence (page, "Semantics worth knowing": batch_invariant): each of the 64 sequences
+    run alone and inside three shuffled copies of the whole batch gives the same bits in o, the
+    final state and its fp32 checkpoints as in the original batch."""
     w = W.config(4)
-    got = gpu_fwd(w)
+    d = dev()
     lens = w.lengths()
     order = np.argsort(lens)
     picks = [int(order[0]), int(order[len(order) // 2]), int(order[-1])]
     units = [(i, h) for i in picks for h in (0, 1, 31)]
-    compare_units(w, got, oracle_fwd(w, units), units)
-    # bitwise batch invariance: each picked sequence alone and inside shuffled batches
+    n = 512
+    full = _fwd_dev(w, n, d)
+    host = (full[0].float().cpu().numpy(), full[1].cpu().numpy(), None)
+    compare_units(w, host, oracle_fwd(w, units), units)
+    del host
     cu = w.cu_seqlens.numpy().astype(np.int64)
-    rng = np.random.default_rng(7)
-    for trial in range(4):
-        if trial == 0:
-            seqs = [picks[0]]
-        elif trial == 1:
-            seqs = [picks[2]]
-        else:
-            seqs = list(rng.permutation(w.N)[: 20 + 10 * trial])
-            for p_ in picks:
-                if p_ not in seqs:
-                    seqs.insert(int(rng.integers(0, len(seqs) + 1)), p_)
+    off = _ck_offsets(lens, n)
+
+    def check_batch(seqs, tag):
         idx = np.concatenate([np.arange(cu[i], cu[i + 1]) for i in seqs])
-        sub = W.Workload(name="sub", cu_seqlens=W._cu([lens[i] for i in seqs]), q=w.q[idx], k=w.k[idx],
+        sub = W.Workload(name=tag, cu_seqlens=W._cu([lens[i] for i in seqs]), q=w.q[idx], k=w.k[idx],
                          v=w.v[idx], g=w.g[idx].contiguous(), beta=w.beta[idx].contiguous())
-        o2, f2, _ = gpu_fwd(sub)
+        o2, f2, c2 = _fwd_dev(sub, n, d)
         cu2 = sub.cu_seqlens.numpy().astype(np.int64)
+        off2 = _ck_offsets([lens[i] for i in seqs], n)
         for j, i in enumerate(seqs):
-            if i not in picks:
-                continue
-            assert np.array_equal(o2[cu2[j]:cu2[j + 1]], got[0][cu[i]:cu[i + 1]]), (trial, i)
-            assert np.array_equal(f2[j], got[1][i]), (trial, i)
+            assert torch.equal(o2[cu2[j]:cu2[j + 1]], full[0][cu[i]:cu[i + 1]]), (tag, i, "o")
+            assert torch.equal(f2[j], full[1][i]), (tag, i, "final")
+            assert torch.equal(c2[off2[j]:off2[j + 1]], full[2][off[i]:off[i + 1]]), (tag, i, "ckpt")
+
+    for i in range(w.N):
+        check_batch([i], f"alone {i}")
+    rng = np.random.default_rng(7)
+    for trial in range(3):
+        check_batch([int(x) for x in rng.permutation(w.N)], f"shuffle {trial}")
 
 
 @pytest.mark.parametrize("slow", [False, True])
@@ -166,19 +187,25 @@ def test_summary_span_composition(slow):
     d = dev()
     t = to_dev(w, d)
     spans = w.spans.to(d)
+    # a nonzero state entering the sequence, S_init ~ 0.1 N(0, 1), so that the first span's
+    # transition is applied to a state (page, "Summaries": S_final = S_init * transition + S_H)
+    gen = torch.Generator().manual_seed(5005)
+    S_init = 0.1 * torch.randn((1, w.HV, w.K, w.V), generator=gen, dtype=torch.float32)
     status = torch.zeros(1, dtype=torch.int32, device=d)
     end, tr = la.gdn_summary(t["k"], t["v"], t["g"], t["beta"], spans, use_qk_l2norm=True, status=status)
     assert la.read_status(status) == 0
-    _, fin, _ = la.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu"], use_qk_l2norm=True)
+    _, fin, _ = la.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu"], use_qk_l2norm=True,
+                           initial_state=S_init.to(d))
     end = end.double().cpu().numpy()
     tr = tr.double().cpu().numpy()
-    S = np.zeros_like(end[0])
+    S = S_init.double().numpy()[0]
     for j in range(end.shape[0]):
         S = np.einsum("hab,hav->hbv", tr[j], S) + end[j]
     fin = fin.double().cpu().numpy()[0]
     errs = {"composed_vs_unsplit": rel(S, fin)}
     assert errs["composed_vs_unsplit"] <= S_TOL
-    # the oracle on two sampled heads: span end states, transitions and the composed state
+    # the oracle on two sampled heads: span end states, transitions, the composed state and the
+    # unsplit run from the same start
     heads = [0, 11]
     mask = np.zeros((8, w.HV), dtype=bool)
     mask[:, heads] = True
@@ -186,10 +213,16 @@ def test_summary_span_composition(slow):
     errs["end_state"] = rel(end[:, heads], ref["end_state"][:, heads])
     if slow:
         errs["transition"] = rel(tr[:, heads], ref["transition"][:, heads])
-    refS = np.zeros_like(ref["end_state"][0])
+    refS = S_init.double().numpy()[0].copy()
     for j in range(8):
         refS = np.einsum("hab,hav->hbv", ref["transition"][j], refS) + ref["end_state"][j]
     errs["composed_vs_oracle"] = rel(S[heads], refS[heads])
+    umask = np.zeros((1, w.HV), dtype=bool)
+    umask[0, heads] = True
+    unsplit = oracle.gdn_fwd(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, initial_state=S_init, want_o=False,
+                             unit_mask=umask)["final_state"][0]
+    errs["oracle_composed_vs_oracle_unsplit"] = rel(refS[heads], unsplit[heads])
+    errs["unsplit_vs_oracle"] = rel(fin[heads], unsplit[heads])
     print(f"[parity] summary slow={slow}: " + ", ".join(f"{k_} {v_:.2e}" for k_, v_ in errs.items()))
     assert max(errs.values()) <= S_TOL, errs
 
@@ -275,21 +308,22 @@ def test_bad_cu_seqlens_sets_status():
     assert la.read_status(status) == 0
 
 
-def test_bounded_wait_timeout_reports_and_context_survives(monkeypatch):
-    """The failure path of the bounded waits, made on the host: a test switch stops the
-    K/Q tile loads, so every CTA's first wait runs out after a 20 ms budget.  The kernel
+def test_bounded_wait_timeout_reports_and_context_survives():
+    """The failure path of the bounded waits, made on the host: the library's test hook stops
+    the K/Q tile loads, so every CTA's first wait runs out after a 20 ms budget.  The kernel
     must report LA_ERR_TIMEOUT and return; the next normal call on the same context must
     succeed and match the oracle."""
     w = small([100, 156, 64], seed=37)
     d = dev()
     t = to_dev(w, d)
     status = torch.zeros(1, dtype=torch.int32, device=d)
-    monkeypatch.setenv("LA_TEST_SKIP_TILE_LOAD", "1")
-    monkeypatch.setenv("LA_TEST_WAIT_BUDGET_NS", "20000000")
-    la.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu"], status=status)
-    assert la.read_status(status) == la.binding.LA_ERR_TIMEOUT
-    monkeypatch.delenv("LA_TEST_SKIP_TILE_LOAD")
-    monkeypatch.delenv("LA_TEST_WAIT_BUDGET_NS")
+    lib = la.binding.load()
+    assert lib.la_test_set_wait_hooks(1, 20000000) == 0
+    try:
+        la.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu"], status=status)
+        assert la.read_status(status) == la.binding.LA_ERR_TIMEOUT
+    finally:
+        assert lib.la_test_set_wait_hooks(0, 0) == 0
     torch.cuda.synchronize()
     status.zero_()
     o, fin, _ = la.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu"], status=status)
