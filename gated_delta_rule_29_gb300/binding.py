@@ -36,6 +36,7 @@ EXPORTED_SYMBOLS = (
     "la_status_string",
     "la_version",
     "la_set_kernel_timing_events",
+    "la_test_set_wait_hooks",
     "gdn_fwd_static_workspace",
     "gdn_decode",
     "gdn_bwd",
@@ -153,6 +154,8 @@ def load(build_if_missing: bool = True):
         lib.la_version.argtypes = []
         lib.la_set_kernel_timing_events.restype = ctypes.c_int
         lib.la_set_kernel_timing_events.argtypes = [_vp, _vp]
+        lib.la_test_set_wait_hooks.restype = ctypes.c_int
+        lib.la_test_set_wait_hooks.argtypes = [_i32, ctypes.c_uint64]
         lib.gdn_fwd_host.restype = ctypes.c_int
         lib.gdn_fwd_host.argtypes = [ctypes.POINTER(GdnFwdHostParams), _vp]
         lib.la_gdn_fwd_host_staging_bytes.restype = ctypes.c_size_t

@@ -46,6 +46,8 @@
 // entering the span is the result.
 #include <cuda_bf16.h>
 
+#include <atomic>
+
 #include "../../include/liblinattn.h"
 #include "gdn_kernel.h"
 #include "ptx.cuh"
@@ -1021,8 +1023,10 @@ __global__ void gdn_bwd_group_sum_kernel(const BwdArgs a) {
 }
 
 // CTAs of the backward kernel resident on the whole GPU at once (one wave), per device and
-// head-dimension pair; looked up on the first launch (outside any stream capture).
-int g_bwd_wave[128][4];
+// head-dimension pair; looked up on the first launch (outside any stream capture).  Host
+// threads may launch concurrently: each slot is written atomically (every writer stores the
+// same value).
+std::atomic<int> g_bwd_wave[128][4];
 
 template <int KD, int VD>
 cudaError_t launch_bwd_kv(const BwdArgs& a0, cudaStream_t s) {
@@ -1037,12 +1041,14 @@ cudaError_t launch_bwd_kv(const BwdArgs& a0, cudaStream_t s) {
         if (e != cudaSuccess) return e;
         int dev = 0;
         if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-        int& wave = g_bwd_wave[dev & 127][(KD == 128 ? 2 : 0) + (VD == 128 ? 1 : 0)];
+        std::atomic<int>& slot = g_bwd_wave[dev & 127][(KD == 128 ? 2 : 0) + (VD == 128 ? 1 : 0)];
+        int wave = slot.load(std::memory_order_relaxed);
         if (wave == 0) {
             int sms = 0, per_sm = 0;
             if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
             if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kBT, smem)) != cudaSuccess) return e;
             wave = sms * (per_sm > 0 ? per_sm : 1);
+            slot.store(wave, std::memory_order_relaxed);
         }
         // more units than one wave: four ranges per unit, launched range by range in waves (a
         // range's successor in the unit is at least `units` >= `wave` items earlier, so in an

@@ -11,6 +11,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 
 #include "../../include/liblinattn.h"
@@ -79,35 +80,47 @@ struct DeviceWorkspace {
 std::mutex g_ws_mutex;
 DeviceWorkspace g_ws[128];
 
-// Internal per-device workspace, grown on demand (growth synchronises the device once).
-la_status internal_workspace(size_t need, void** out) {
+// Internal per-device workspace, grown on demand without synchronising anything: a larger
+// buffer replaces the current one and the old buffer is kept allocated until the process exits
+// (kernels enqueued earlier, on any stream, may still be reading it, and freeing it safely would
+// need a device-wide synchronisation).  Sizes at least double, so the kept buffers add up to
+// less than the current one.  Growth allocates, which a stream capture does not allow: a call
+// on a capturing stream that would need a larger buffer returns LA_ERR_WORKSPACE (nothing is
+// launched; pass a workspace, or make one call of that size before capturing).
+la_status internal_workspace(size_t need, cudaStream_t stream, void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return LA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_ws_mutex);
     DeviceWorkspace& w = g_ws[dev];
     if (w.bytes < need) {
-        if (w.ptr) {
-            if (cudaDeviceSynchronize() != cudaSuccess) return LA_ERR_CUDA;
-            cudaFree(w.ptr);
-            w.ptr = nullptr;
-            w.bytes = 0;
-        }
-        size_t grow = need < (1u << 20) ? (1u << 20) : need;
-        if (cudaMalloc(&w.ptr, grow) != cudaSuccess) return LA_ERR_CUDA;
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess) return LA_ERR_CUDA;
+        if (cs != cudaStreamCaptureStatusNone) return LA_ERR_WORKSPACE;
+        size_t grow = 2 * w.bytes;
+        if (grow < need) grow = need;
+        if (grow < (size_t(1) << 20)) grow = size_t(1) << 20;
+        void* p = nullptr;
+        if (cudaMalloc(&p, grow) != cudaSuccess) return LA_ERR_CUDA;
+        w.ptr = p;  // the previous buffer, if any, stays allocated (see above)
         w.bytes = grow;
     }
     *out = w.ptr;
     return LA_OK;
 }
 
-la_status resolve_workspace(void* user, size_t user_bytes, int32_t N, void** out) {
+// Failure-path test hooks, set only through la_test_set_wait_hooks (never from the
+// environment): skip the forward's K/Q tile loads, and replace the bounded waits' budget.
+std::atomic<int32_t> g_test_skip_tile_load{0};
+std::atomic<uint64_t> g_test_wait_budget_ns{0};
+
+la_status resolve_workspace(void* user, size_t user_bytes, int32_t N, cudaStream_t stream, void** out) {
     const size_t need = la::ws_layout(N).total;
     if (user) {
         if (user_bytes < need || !aligned(user, 256)) return LA_ERR_WORKSPACE;
         *out = user;
         return LA_OK;
     }
-    return internal_workspace(need, out);
+    return internal_workspace(need, stream, out);
 }
 
 struct Common {
@@ -173,7 +186,7 @@ la_status run(const Common& c, ChunkArgs& ka, const void* q, int64_t q_st, int64
               int64_t k_sh, const void* v, int64_t v_st, int64_t v_sh, int64_t ckpt_n, void* workspace,
               size_t workspace_bytes, int32_t* user_status, int mode, cudaStream_t stream, int32_t gdp_n = 1) {
     void* ws = nullptr;
-    la_status st = resolve_workspace(workspace, workspace_bytes, c.N, &ws);
+    la_status st = resolve_workspace(workspace, workspace_bytes, c.N, stream, &ws);
     if (st != LA_OK) return st;
     const la::WorkspaceLayout L = la::ws_layout(c.N);
     uint8_t* wsb = static_cast<uint8_t*>(ws);
@@ -209,14 +222,9 @@ la_status run(const Common& c, ChunkArgs& ka, const void* q, int64_t q_st, int64
     ka.ckpt_off = pa.ckpt_off;
     ka.user_status = user_status;
     ka.wait_budget_ns = kWaitBudgetNs;
-    // Test hooks for the failure path (read on every call): LA_TEST_SKIP_TILE_LOAD=1 makes the
-    // chunk kernel skip its K/Q tile loads so its first bounded wait runs out and it reports
-    // LA_ERR_TIMEOUT; LA_TEST_WAIT_BUDGET_NS shortens the bounded waits.
-    if (const char* e = std::getenv("LA_TEST_SKIP_TILE_LOAD")) ka.test_skip_tile_load = std::atoi(e) != 0;
-    if (const char* e = std::getenv("LA_TEST_WAIT_BUDGET_NS")) {
-        const long long b = std::atoll(e);
-        if (b > 0) ka.wait_budget_ns = static_cast<uint64_t>(b);
-    }
+    // failure-path test hooks (off unless a test set them with la_test_set_wait_hooks)
+    ka.test_skip_tile_load = g_test_skip_tile_load.load(std::memory_order_relaxed) != 0;
+    if (const uint64_t b = g_test_wait_budget_ns.load(std::memory_order_relaxed)) ka.wait_budget_ns = b;
     if (ka.num_units == 0) return LA_OK;
 
     CUtensorMap qm, km, vm, om;
@@ -471,7 +479,7 @@ la_status gdp_fwd(const la_gdn_fwd_params* p, void* stream) {
     la_status st;
     if (ws) {
         if (p->workspace_bytes < GL.total || !aligned(ws, 256)) return LA_ERR_WORKSPACE;
-    } else if ((st = internal_workspace(GL.total, &ws)) != LA_OK) {
+    } else if ((st = internal_workspace(GL.total, static_cast<cudaStream_t>(stream), &ws)) != LA_OK) {
         return st;
     }
     uint8_t* wb = static_cast<uint8_t*>(ws);
@@ -590,7 +598,7 @@ la_status gdn_bwd(const la_gdn_bwd_params* p, void* stream) {
     void* ws = p->workspace;
     if (ws) {
         if (p->workspace_bytes < BL.total || !aligned(ws, 256)) return LA_ERR_WORKSPACE;
-    } else if ((st = internal_workspace(BL.total, &ws)) != LA_OK) {
+    } else if ((st = internal_workspace(BL.total, static_cast<cudaStream_t>(stream), &ws)) != LA_OK) {
         return st;
     }
     uint8_t* wb = static_cast<uint8_t*>(ws);
@@ -697,7 +705,7 @@ la_status gdn_summary_bwd(const la_gdn_summary_bwd_params* p, void* stream) {
     void* ws = p->workspace;
     if (ws) {
         if (p->workspace_bytes < SL.total || !aligned(ws, 256)) return LA_ERR_WORKSPACE;
-    } else if ((st = internal_workspace(SL.total, &ws)) != LA_OK) {
+    } else if ((st = internal_workspace(SL.total, static_cast<cudaStream_t>(stream), &ws)) != LA_OK) {
         return st;
     }
     uint8_t* wb = static_cast<uint8_t*>(ws);
@@ -780,6 +788,8 @@ la_status gdn_fwd_static_workspace(const la_gdn_fwd_params* p, void* stream) {
     if (!p) return LA_ERR_INVALID_ARG;
     if (p->workspace) return LA_ERR_INVALID_ARG;  // the scratch is the library's own array
     if (p->N < 0) return LA_ERR_INVALID_ARG;
+    // GDP beyond 64 updates per token materialises its timeline in a scratch that grows with T
+    if (p->num_householder > la::kChunk) return LA_ERR_UNSUPPORTED;
     if (p->N > kStaticMaxSeqs || la::ws_layout(p->N).total > kStaticScratchBytes) return LA_ERR_WORKSPACE;
     void* scratch = nullptr;
     la_status st = static_scratch_address(&scratch);
@@ -819,6 +829,12 @@ la_status la_read_status(const int32_t* device_status, void* stream, int32_t* ou
     if (!device_status || !out) return LA_ERR_INVALID_ARG;
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return LA_ERR_CUDA;
     if (cudaMemcpy(out, device_status, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess) return LA_ERR_CUDA;
+    return LA_OK;
+}
+
+la_status la_test_set_wait_hooks(int32_t skip_tile_load, uint64_t wait_budget_ns) {
+    g_test_skip_tile_load.store(skip_tile_load != 0 ? 1 : 0, std::memory_order_relaxed);
+    g_test_wait_budget_ns.store(wait_budget_ns, std::memory_order_relaxed);
     return LA_OK;
 }
 

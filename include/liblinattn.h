@@ -140,7 +140,15 @@ typedef struct la_gdn_fwd_params {
  *                      sequence order: sequence i owns ceil(L_i / n) rows
  *                      starting at sum_{j<i} ceil(L_j / n).
  * Workspace: if `workspace` is NULL an internal per-device buffer is used;
- * overlapping calls on different streams must then each pass their own.
+ * overlapping calls on different streams must then each pass their own.  That
+ * buffer grows on demand (every entry point that takes a workspace shares it)
+ * without any synchronisation: a larger buffer replaces it and the old one
+ * stays allocated until the process exits, since earlier kernels may still
+ * read it (sizes at least double, so the kept buffers total less than the
+ * current one).  Growth allocates, which stream capture forbids: a call on a
+ * capturing stream that would need to grow the buffer returns
+ * LA_ERR_WORKSPACE and launches nothing (pass a workspace, or make a call of
+ * that size before capturing).
  * Returns LA_OK once the work is enqueued.
  */
 la_status gdn_fwd(const la_gdn_fwd_params* p, void* stream);
@@ -157,9 +165,14 @@ la_status gdn_fwd(const la_gdn_fwd_params* p, void* stream);
  *   - p->workspace must be NULL (LA_ERR_INVALID_ARG otherwise);
  *   - N may be at most 8192 sequences; larger batches return LA_ERR_WORKSPACE
  *     and launch nothing;
+ *   - Gated DeltaProduct with num_householder > 64 is not available here (its
+ *     timeline scratch grows with T): LA_ERR_UNSUPPORTED, nothing launched;
  *   - no call allocates or frees device memory.  The first call on a device
  *     looks up the array's device address (once, with that device current);
- *     make that first call before any stream capture.
+ *     make that first call before any stream capture.  The address is kept
+ *     for the life of the process: after the application resets a device
+ *     (cudaDeviceReset) it is stale, and this entry point must not be used
+ *     on that device again.
  *   - every call on a device shares the one array.  Each call re-initialises
  *     what must start at zero (status word, unit ticket) in its own prologue
  *     kernel, so leftovers from an earlier call are harmless, but calls whose
@@ -462,6 +475,17 @@ la_status la_read_status(const int32_t* device_status, void* stream, int32_t* ou
  * pass NULL, NULL to clear it.  Not part of the computation; no citation.
  */
 la_status la_set_kernel_timing_events(void* start_event, void* stop_event);
+
+/*
+ * Failure-path test hook, not for production use (no counterpart on the pages).
+ * skip_tile_load != 0 makes the forward's chunk kernel issue no K/Q tile loads,
+ * so its first bounded wait can never complete and it reports LA_ERR_TIMEOUT in
+ * the status word; wait_budget_ns > 0 replaces the 1 s budget of every bounded
+ * wait of the forward.  The settings are process-wide and apply to every later
+ * gdn_fwd call from any thread until cleared with (0, 0); nothing else sets
+ * them (the library reads no environment variables).
+ */
+la_status la_test_set_wait_hooks(int32_t skip_tile_load, uint64_t wait_budget_ns);
 
 /* Static description of a status code. */
 const char* la_status_string(la_status s);
