@@ -840,6 +840,133 @@ def run_summary_bench(args, world, rank, local):
     return 0
 
 
+def run_table(args, world, rank, local):
+    """One line per workload of the survey's table: the forward on the tiny, varlen, dense-batch
+    and skewed grouped-head workloads, and the summary on the span workload.  For each, the GPU
+    call's and the fused kernel's time (CUDA events, mean over --steps after --warmup), tokens/s,
+    the algorithmic bytes and FLOPs over the kernel time against the measured peaks, and the fp64
+    oracle's rate on the host cores at one thread and at all cores, each on a bounded sample of
+    the workload's (sequence, head) units, with the whole-workload oracle time those rates imply."""
+    import oracle  # the CPU baseline columns only
+    import gated_delta_rule_29_gb300 as la
+    from gated_delta_rule_29_gb300 import binding as B
+    from gated_delta_rule_29_gb300 import workloads as W
+
+    assert torch.cuda.is_available(), "bench needs a CUDA device (there is no CPU fallback)"
+    if rank != 0:
+        return 0
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    lib = B.load()
+    hbm_peak, tc_peak, peak_src = load_peaks()
+    cores = os.cpu_count() or 1
+    stream = torch.cuda.current_stream()
+
+    def timed(step):
+        for _ in range(args.warmup):
+            step()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for a_, b_ in evs:
+            a_.record(stream)
+            b_.record(stream)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.steps):
+            lib.la_set_kernel_timing_events(evs[i][0].cuda_event, evs[i][1].cuda_event)
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / args.steps, statistics.mean(a_.elapsed_time(b_) for a_, b_ in evs)
+
+    def oracle_rates(w, units_1t, units_all, summary=False):
+        def one(units, nthreads):
+            if not summary:
+                dt, th = oracle_sample(w, units, nthreads)
+                return th / dt
+            mask = np.zeros((w.N, w.HV), dtype=bool)
+            for i, h in units:
+                mask[i, h] = True
+            t0 = time.perf_counter()
+            oracle.gdn_summary(w.k, w.v, w.g, w.beta, w.cu_seqlens, unit_mask=mask, nthreads=nthreads)
+            dt = time.perf_counter() - t0
+            lens = w.lengths()
+            return sum(int(lens[i]) for i, _ in units) / dt
+        r1 = one(units_1t, 1)
+        ra = one(units_all, cores)
+        total = sum(int(L) for L in w.lengths()) * w.HV  # token-heads of the whole workload
+        return {"tokens_per_s_1_thread": r1 / w.HV, "tokens_per_s_all_cores": ra / w.HV, "cores": cores,
+                "sample_1_thread": f"{len(units_1t)} (sequence, head) units",
+                "sample_all_cores": f"{len(units_all)} (sequence, head) units",
+                "workload_s_1_thread": total / r1, "workload_s_all_cores": total / ra}
+
+    def spread(w, count):
+        """`count` (sequence, head) units spread over the batch (sequences of every length)."""
+        units = [(i, h) for i in range(w.N) for h in range(w.HV) if w.lengths()[i] > 0]
+        step_ = max(1, len(units) // count)
+        return units[::step_][:count]
+
+    rows = []
+    for cfg in (1, 2, 3, 4):
+        w = W.config(cfg)
+        T, N, HK, HV, K, V = w.T, w.N, w.HK, w.HV, w.K, w.V
+        t = [x.to(dev) for x in (w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens)]
+        s0 = None if w.initial_state is None else w.initial_state.to(dev)
+        n_ck = w.checkpoint_every_n
+        R = la.checkpoint_rows(w.cu_seqlens, n_ck) if n_ck else 0
+        o = torch.empty(T, HV, V, dtype=torch.bfloat16, device=dev)
+        fin = torch.empty(N, HV, K, V, dtype=torch.float32, device=dev)
+        ck = torch.empty(R, HV, K, V, dtype=torch.float32, device=dev) if n_ck else None
+        ws = torch.empty(la.workspace_bytes(N), dtype=torch.uint8, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+        def step():
+            la.gdn_fwd(*t, initial_state=s0, checkpoint_every_n=n_ck, checkpoint_dtype=torch.float32,
+                       checkpoint_rows_hint=R, o=o, final_state=fin, checkpoints=ck, workspace=ws, status=status)
+
+        call_ms, kern_ms = timed(step)
+        assert la.read_status(status) == 0
+        alg = algorithmic_bytes(T, N, HK, HV, K, V, R, s0=s0 is not None, final=True)
+        flops = algorithmic_flops(w.lengths(), HV, K, V)
+        units = [(i, h) for i in range(N) for h in range(HV) if w.lengths()[i] > 0]
+        n1 = {1: len(units), 2: 8, 3: 2, 4: 8}[cfg]
+        na = {1: len(units), 2: len(units), 3: 32, 4: 64}[cfg]
+        rows.append({"workload": w.name, "op": "gdn_fwd", "T": T, "N": N, "HK": HK, "HV": HV, "K": K, "V": V,
+                     "call_ms": call_ms, "kernel_ms": kern_ms, "tokens_per_s": T / (call_ms * 1e-3),
+                     "algorithmic_bytes": alg, "hbm_gbs": alg / (kern_ms * 1e-3) / 1e9,
+                     "hbm_frac": alg / (kern_ms * 1e-3) / 1e9 / hbm_peak,
+                     "tensor_tflops": flops / (kern_ms * 1e-3) / 1e12,
+                     "tensor_frac": flops / (kern_ms * 1e-3) / 1e12 / tc_peak,
+                     "oracle": oracle_rates(w, spread(w, n1), spread(w, na))})
+        del t, o, fin, ck
+    w = W.config(5)
+    T, HK, HV, K, V = w.T, w.HK, w.HV, w.K, w.V
+    k, v, g, b, spans = (x.to(dev) for x in (w.k, w.v, w.g, w.beta, w.spans))
+    S = spans.numel() - 1
+    end = torch.empty(S, HV, K, V, dtype=torch.float32, device=dev)
+    tr = torch.empty(S, HV, K, K, dtype=torch.float32, device=dev)
+    ws = torch.empty(la.workspace_bytes(S, True), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    call_ms, kern_ms = timed(lambda: la.gdn_summary(k, v, g, b, spans, end_state=end, transition=tr, workspace=ws,
+                                                    status=status))
+    assert la.read_status(status) == 0
+    alg = T * (HK * K + HV * V) * 2 + 2 * T * HV * 4 + S * HV * (K * V + K * K) * 4 + (S + 1) * 4
+    C = 64
+    flops = 2 * (2 * C * C * K + 2 * C * K * V + 2 * C * C * V + 2 * C * K * V) * (T // C) * HV
+    ws5 = W.Workload(name=w.name + " (span summaries)", cu_seqlens=w.spans, q=w.k, k=w.k, v=w.v, g=w.g, beta=w.beta)
+    rows.append({"workload": w.name, "op": "gdn_summary (8 spans)", "T": T, "N": S, "HK": HK, "HV": HV, "K": K,
+                 "V": V, "call_ms": call_ms, "kernel_ms": kern_ms, "tokens_per_s": T / (call_ms * 1e-3),
+                 "algorithmic_bytes": alg, "hbm_gbs": alg / (kern_ms * 1e-3) / 1e9,
+                 "hbm_frac": alg / (kern_ms * 1e-3) / 1e9 / hbm_peak,
+                 "tensor_tflops": flops / (kern_ms * 1e-3) / 1e12, "tensor_frac": flops / (kern_ms * 1e-3) / 1e12 / tc_peak,
+                 "oracle": oracle_rates(ws5, [(0, 0)], [(0, h) for h in range(min(HV, cores))], summary=True)})
+    for r_ in rows:
+        r_["peak_source"] = peak_src
+        print(json.dumps(r_), flush=True)
+    return 0
+
+
 SUM_BWD_METRIC = ("GDN summary_bwd tokens/s (state gradient entering each span; one 131072-token sequence, "
                   "8 spans, H=16, K=V=128)")
 
@@ -953,12 +1080,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
     ap.add_argument("--e2e-groups", type=int, default=16, help="token ranges pipelined by gdn_fwd_host")
-    ap.add_argument("--workload", choices=["dense", "decode", "bwd", "gdp", "summary", "summary_bwd"],
+    ap.add_argument("--workload", choices=["dense", "decode", "bwd", "gdp", "summary", "summary_bwd", "table"],
                     default="dense",
                     help="dense: the chunked forward over the dense batch (the headline); "
                          "decode: one decode step against a state pool; bwd: the backward of the dense batch; "
                          "gdp: Gated DeltaProduct with 2 updates per token; summary: gdn_summary over 8 spans; "
-                         "summary_bwd: the summary's state-gradient mirror over the same spans")
+                         "summary_bwd: the summary's state-gradient mirror over the same spans; "
+                         "table: one line per workload of the five configurations, with the oracle at one "
+                         "thread and at all cores")
     ap.add_argument("--seq-len", type=int, default=8192,
                     help="tokens per sequence of the dense batch (8192 is the benchmark workload)")
     args = ap.parse_args()
@@ -978,6 +1107,8 @@ def main():
             return run_summary_bench(args, world, rank, local)
         if args.workload == "summary_bwd":
             return run_summary_bwd_bench(args, world, rank, local)
+        if args.workload == "table":
+            return run_table(args, world, rank, local)
         return run_ours(args, world, rank, local)
     finally:
         if world > 1:

@@ -310,6 +310,9 @@ __global__ void __launch_bounds__(kCta, 2)
     constexpr bool kFwd = MODE != kModeSummary;  // queries and outputs (the forward, or GDP's)
     constexpr bool kGdp = MODE == kModeGdp;
     constexpr bool kSum = MODE == kModeSummary;
+    // waits sleep in hardware when another CTA shares the SM (the forward runs two per SM; the
+    // summary, with its larger shared-memory footprint, one)
+    constexpr bool kSleep = !kSum;
     constexpr int KP = KD / 16;  // 16-column pieces of the state
     // GDP: the tokens whose last update row falls in a chunk of 64 update rows (at most QR of
     // them) have their queries in rows 0 .. QR-1 of the query half of the K/Q tile (the other
@@ -566,7 +569,7 @@ __global__ void __launch_bounds__(kCta, 2)
 
             // ---- S1: K/Q tile; G = [K; Q] [K; Q]^T on the tensor core while the gate scan runs.
             // Its diagonal holds the squared row norms of K (lanes 0-63) and Q (lanes 64-127).
-            bool ok = mbar_wait(&sc.bar_kq, ph_kq, budget);
+            bool ok = mbar_wait(&sc.bar_kq, ph_kq, budget, kSleep);
             if (ok) {
                 ph_kq ^= 1u;
                 pend_kq = false;
@@ -592,7 +595,7 @@ __global__ void __launch_bounds__(kCta, 2)
                 sc.bw[tid] = x;
             }
             {
-                const bool okg = mbar_wait(&sc.bar_mma, ph_mma, budget);
+                const bool okg = mbar_wait(&sc.bar_mma, ph_mma, budget, kSleep);
                 if (okg) {
                     ph_mma ^= 1u;
                     pend_mma = false;
@@ -734,13 +737,13 @@ __global__ void __launch_bounds__(kCta, 2)
             if (__syncthreads_or(!ok)) { failed = true; break; }
 
             // ---- S4: X^T = beta V^T - sx (K S)^T (hi + lo); then T = (I + A)^{-1} in the V tile's space
-            ok = mbar_wait(&sc.bar_mma, ph_mma, budget);
+            ok = mbar_wait(&sc.bar_mma, ph_mma, budget, kSleep);
             if (ok) {
                 ph_mma ^= 1u;
                 pend_mma = false;
             }
             if (value_tile) {
-                const bool okv = mbar_wait(&sc.bar_v, ph_v, budget);
+                const bool okv = mbar_wait(&sc.bar_v, ph_v, budget, kSleep);
                 if (okv) {
                     ph_v ^= 1u;
                     pend_v = false;
@@ -844,7 +847,7 @@ __global__ void __launch_bounds__(kCta, 2)
                 for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
                 if ((tid & 31) == 0) sc.gsum[tid >> 5] = x;
             }
-            ok = mbar_wait(&sc.bar_mma, ph_mma, budget);
+            ok = mbar_wait(&sc.bar_mma, ph_mma, budget, kSleep);
             if (ok) {
                 ph_mma ^= 1u;
                 pend_mma = false;
@@ -898,7 +901,7 @@ __global__ void __launch_bounds__(kCta, 2)
             pend_o = kFwd;
             if (kFwd) {
                 // O is complete before the state update: store it while the update runs
-                const bool oko = mbar_wait(&sc.bar_o, ph_o, budget);
+                const bool oko = mbar_wait(&sc.bar_o, ph_o, budget, kSleep);
                 if (oko) {
                     ph_o ^= 1u;
                     pend_o = false;
@@ -935,7 +938,7 @@ __global__ void __launch_bounds__(kCta, 2)
                 }
             }
             {
-                const bool okm = mbar_wait(&sc.bar_mma, ph_mma, budget);
+                const bool okm = mbar_wait(&sc.bar_mma, ph_mma, budget, kSleep);
                 if (okm) {
                     ph_mma ^= 1u;
                     pend_mma = false;

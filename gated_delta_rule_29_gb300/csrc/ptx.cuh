@@ -59,12 +59,19 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
     return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete; false after budget_ns.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t budget_ns) {
+// Waits for the phase with the given parity to complete; false after budget_ns.  sleep: the
+// waiting thread is suspended between polls, which leaves the issue slots to another CTA on the
+// same SM (a gain when two CTAs share it, a wake-up cost when the CTA has the SM to itself).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t budget_ns, bool sleep = false) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
-        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if (sleep) {
+            if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        } else {
+            for (int i = 0; i < 64; ++i)
+                if (mbar_try_wait(bar, parity)) return true;
+        }
         if (globaltimer_ns() - t0 > budget_ns) return false;
     }
 }
