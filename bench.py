@@ -551,13 +551,20 @@ def run_bwd_bench(args, world, rank, local):
     dfin_h = torch.randn(N, HV, K, V, generator=gen)
     q, k, v, g, b, cu, s0, do, dfin = (x.to(dev) for x in (w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens,
                                                             w.initial_state, do_h, dfin_h))
-    _, _, ck = la.gdn_fwd(q, k, v, g, b, cu, initial_state=s0, checkpoint_every_n=64, checkpoint_dtype=torch.float32)
-    ws = torch.empty(lib.la_gdn_bwd_workspace_bytes(T, N, HK, HV, K, V, 1), dtype=torch.uint8, device=dev)
+    # the checkpoints the backward is given: the forward's fp32 rows every --bwd-ckpt tokens (64:
+    # the chunk cadence, read directly; larger: the dense series is regenerated segment by segment)
+    # or none (the whole forward re-runs)
+    ck_n = 0 if args.bwd_ckpt == "none" else int(args.bwd_ckpt)
+    ck = None
+    if ck_n:
+        _, _, ck = la.gdn_fwd(q, k, v, g, b, cu, initial_state=s0, checkpoint_every_n=ck_n,
+                              checkpoint_dtype=torch.float32)
+    ws = torch.empty(lib.la_gdn_bwd_workspace_bytes_ckpt(T, N, HK, HV, K, V, ck_n, 0), dtype=torch.uint8, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def step():
         return la.gdn_bwd(q, k, v, g, b, cu, do, initial_state=s0, d_final_state=dfin, checkpoints=ck,
-                          workspace=ws, status=status)
+                          checkpoint_every_n=ck_n if ck_n else 64, workspace=ws, status=status)
 
     for _ in range(args.warmup):
         step()
@@ -591,17 +598,17 @@ def run_bwd_bench(args, world, rank, local):
     # end to end: the step's inputs, cotangents and checkpoints copied from pinned host memory,
     # the gradients copied back, all inside the timed region
     host_in = [x.pin_memory() for x in (w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, w.initial_state, do_h, dfin_h)]
-    host_ck = ck.cpu().pin_memory()
+    host_ck = ck.cpu().pin_memory() if ck is not None else None
     outs = step()
     host_out = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in outs]
-    h2d = sum(x.numel() * x.element_size() for x in host_in) + host_ck.numel() * 4
+    h2d = sum(x.numel() * x.element_size() for x in host_in) + (host_ck.numel() * 4 if host_ck is not None else 0)
     d2h = sum(x.numel() * x.element_size() for x in host_out)
 
     def e2e_step():
         xs = [x.to(dev, non_blocking=True) for x in host_in]
-        ckd = host_ck.to(dev, non_blocking=True)
+        ckd = host_ck.to(dev, non_blocking=True) if host_ck is not None else None
         r = la.gdn_bwd(xs[0], xs[1], xs[2], xs[3], xs[4], xs[5], xs[7], initial_state=xs[6], d_final_state=xs[8],
-                       checkpoints=ckd, workspace=ws, status=status)
+                       checkpoints=ckd, checkpoint_every_n=ck_n if ck_n else 64, workspace=ws, status=status)
         for hbuf, dbuf in zip(host_out, r):
             hbuf.copy_(dbuf, non_blocking=True)
 
@@ -640,8 +647,9 @@ def run_bwd_bench(args, world, rank, local):
             "metric": BWD_METRIC, "value": T * world / (ms * 1e-3), "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": (WORKLOAD if L == 8192 else w.name) + "; bwd with the forward's fp32 checkpoints "
-                                   "every 64 tokens", "global_batch": N * world, "seq_len": L,
+            "config": {"workload": (WORKLOAD if L == 8192 else w.name) + (
+                           f"; bwd with the forward's fp32 checkpoints every {ck_n} tokens" if ck_n else
+                           "; bwd without checkpoints (the forward re-runs)"), "global_batch": N * world, "seq_len": L,
                        "parallelism": "single GPU" if world == 1 else f"independent batches per GPU x{world}",
                        "l2": "inputs larger than L2 (1.6 GB of q/k/v + 2.1 GB of checkpoints per step); no flush"},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": tf32_peak, "unit": "TFLOP/s",
@@ -1088,6 +1096,8 @@ def main():
                          "summary_bwd: the summary's state-gradient mirror over the same spans; "
                          "table: one line per workload of the five configurations, with the oracle at one "
                          "thread and at all cores")
+    ap.add_argument("--bwd-ckpt", choices=["64", "128", "256", "512", "1024", "none"], default="64",
+                    help="bwd: cadence of the forward's fp32 checkpoints the backward is given (none: re-run)")
     ap.add_argument("--seq-len", type=int, default=8192,
                     help="tokens per sequence of the dense batch (8192 is the benchmark workload)")
     args = ap.parse_args()

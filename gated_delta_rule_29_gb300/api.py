@@ -247,10 +247,13 @@ def gdn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
             workspace: Optional[torch.Tensor] = None, status: Optional[torch.Tensor] = None,
             stream: Optional[torch.cuda.Stream] = None, a_log: Optional[torch.Tensor] = None,
             dt_bias: Optional[torch.Tensor] = None, gate_lower_bound: Optional[float] = None,
-            beta_sigmoid: bool = False, out: Optional[Tuple[Optional[torch.Tensor], ...]] = None):
+            beta_sigmoid: bool = False, out: Optional[Tuple[Optional[torch.Tensor], ...]] = None,
+            checkpoint_every_n: int = 64):
     """Backward of gdn_fwd: returns (dq, dk, dv, dg, dbeta, d_initial_state or None) for the loss
     sum(d_o * o) + sum(d_final_state * final_state).  `checkpoints`, if given, are the forward's
-    fp32 checkpoints every 64 tokens; otherwise the forward is re-run for them.  With the input
+    checkpoints (fp32 or bf16) every `checkpoint_every_n` tokens (a multiple of 64): rows every 64
+    tokens are used directly (bf16 widened), sparser rows regenerate the states entering every
+    chunk segment by segment; without them the forward is re-run.  With the input
     transforms of gdn_fwd, dg and dbeta are the gradients of the raw inputs, and the softplus
     gate (a_log, dt_bias) appends (d_a_log, d_dt_bias) [HO] fp32 to the tuple.
 
@@ -277,16 +280,20 @@ def gdn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
     ds0 = _out("d_initial_state", o6[5], (N, HV, K, V), torch.float32, dev, contiguous=True) \
         if initial_state is not None else None
     lib = B.load()
+    ck_n = int(checkpoint_every_n) if checkpoints is not None else 0
+    ck_bf16 = checkpoints is not None and checkpoints.dtype == torch.bfloat16
+    if checkpoints is not None:
+        if checkpoints.dtype not in (torch.float32, torch.bfloat16) or not checkpoints.is_contiguous():
+            raise ValueError("checkpoints must be the forward's contiguous fp32 or bf16 rows")
+        if ck_n <= 0 or ck_n % 64 != 0:
+            raise ValueError("checkpoint_every_n must be a positive multiple of 64")
     if workspace is None:
-        need = lib.la_gdn_bwd_workspace_bytes(T, N, HK, HV, K, V, int(checkpoints is not None))
+        need = lib.la_gdn_bwd_workspace_bytes_ckpt(T, N, HK, HV, K, V, ck_n, int(ck_bf16))
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     if initial_state is not None:
         initial_state = initial_state.contiguous()
     if d_final_state is not None:
         d_final_state = d_final_state.contiguous().float()
-    if checkpoints is not None:
-        if checkpoints.dtype != torch.float32 or not checkpoints.is_contiguous():
-            raise ValueError("checkpoints must be the forward's contiguous fp32 rows every 64 tokens")
     p = B.GdnBwdParams()
     p.q, p.q_stride_t, p.q_stride_h = q.data_ptr(), q.stride(0), q.stride(1)
     p.k, p.k_stride_t, p.k_stride_h = k.data_ptr(), k.stride(0), k.stride(1)
@@ -301,6 +308,7 @@ def gdn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
         p.initial_state = initial_state.data_ptr()
         p.initial_state_dtype = B.LA_DTYPE_BF16 if initial_state.dtype == torch.bfloat16 else B.LA_DTYPE_F32
     p.checkpoints = checkpoints.data_ptr() if checkpoints is not None else None
+    p.checkpoint_every_n, p.checkpoint_bf16 = ck_n, int(ck_bf16)
     p.d_o, p.d_o_stride_t, p.d_o_stride_h = d_o.data_ptr(), d_o.stride(0), d_o.stride(1)
     p.d_final_state = d_final_state.data_ptr() if d_final_state is not None else None
     p.dq, p.dq_stride_t, p.dq_stride_h = dq.data_ptr(), dq.stride(0), dq.stride(1)

@@ -41,6 +41,7 @@ EXPORTED_SYMBOLS = (
     "gdn_decode",
     "gdn_bwd",
     "la_gdn_bwd_workspace_bytes",
+    "la_gdn_bwd_workspace_bytes_ckpt",
     "la_gdp_workspace_bytes",
     "gdn_summary_bwd",
     "la_gdn_summary_bwd_workspace_bytes",
@@ -138,6 +139,8 @@ def load(build_if_missing: bool = True):
         lib.la_gdp_workspace_bytes.argtypes = [_i64, _i32, _i32, _i32, _i32, _i32, _i32]
         lib.la_gdn_bwd_workspace_bytes.restype = ctypes.c_size_t
         lib.la_gdn_bwd_workspace_bytes.argtypes = [_i64, _i32, _i32, _i32, _i32, _i32, _i32]
+        lib.la_gdn_bwd_workspace_bytes_ckpt.restype = ctypes.c_size_t
+        lib.la_gdn_bwd_workspace_bytes_ckpt.argtypes = [_i64, _i32, _i32, _i32, _i32, _i32, _i64, _i32]
         lib.gdn_decode.restype = ctypes.c_int
         lib.gdn_decode.argtypes = [ctypes.POINTER(GdnDecodeParams), _vp]
         lib.gdn_summary.restype = ctypes.c_int
@@ -215,6 +218,7 @@ class GdnBwdParams(ctypes.Structure):
         ("gate_mode", _i32), ("a_log", _vp), ("dt_bias", _vp), ("gate_lower_bound", ctypes.c_float),
         ("beta_sigmoid", _i32), ("beta_bf16", _i32),
         ("d_a_log", _vp), ("d_dt_bias", _vp),
+        ("checkpoint_every_n", _i64), ("checkpoint_bf16", _i32),
     ]
 
 

@@ -45,7 +45,7 @@ __host__ __device__ inline WorkspaceLayout ws_layout(int32_t N) {
 
 struct WsHeader {
     int32_t status;     // LA_OK or a device-side error code
-    int32_t reserved;
+    int32_t ckpt_rows;  // sum_i ceil(L_i / n) when the prologue computed checkpoint offsets
     uint64_t ticket;    // next unit to hand out (8-byte aligned for the 64-bit atomic)
 };
 
@@ -204,6 +204,31 @@ struct GdpArgs {
     const uint16_t* oe;              // [T * n, HO, V] contiguous
     uint16_t* o; int64_t o_st, o_sh;
 };
+
+// Checkpoint rows for the backward (gdn_ckpt.cu).  widen: the first hdr->ckpt_rows rows (at most
+// max_rows) of bf16 checkpoints to fp32.  segments: the pseudo-sequences that cut every sequence
+// at multiples of n (cu_seg [max_seg + 1], int64; trailing entries empty) and their start states
+// (s0_seg [max_seg][row_elems] fp32: the given rows, zero beyond them), from the cadence-n
+// checkpoint offsets a prologue wrote (ckpt_off_n, hdr_n).
+struct CkptArgs {
+    const void* src;        // given checkpoint rows (fp32 or bf16)
+    int32_t src_bf16;
+    int64_t row_elems;      // HO * K * V
+    const WsHeader* hdr;    // rows and status from the prologue
+    int64_t max_rows;
+    float* dst;             // widen: fp32 rows
+    const void* cu;         // segments: the batch's cu_seqlens
+    int32_t cu64;
+    int32_t N;
+    int64_t T;
+    int64_t n;
+    const int64_t* ckpt_off_n;
+    int64_t* cu_seg;
+    float* s0_seg;
+    int64_t max_seg;
+};
+cudaError_t launch_ckpt_widen(const CkptArgs& a, cudaStream_t s);
+cudaError_t launch_ckpt_segments(const CkptArgs& a, cudaStream_t s);
 
 // Launchers (return cudaError_t of the launch).
 cudaError_t launch_gdp_expand(const GdpArgs& a, cudaStream_t s);

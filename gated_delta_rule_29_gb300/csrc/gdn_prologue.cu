@@ -85,6 +85,7 @@ __global__ void __launch_bounds__(kPrologueThreads) gdn_prologue_kernel(Prologue
             if (i < N) a.ckpt_off[i] = carry + ex;
             carry += total;
         }
+        if (tid == 0) a.hdr->ckpt_rows = static_cast<int32_t>(carry);
     }
 
     const uint32_t P = next_pow2(static_cast<uint32_t>(N > 0 ? N : 1));

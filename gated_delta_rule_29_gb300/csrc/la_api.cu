@@ -517,25 +517,52 @@ la_status gdp_fwd(const la_gdn_fwd_params* p, void* stream) {
     return LA_OK;
 }
 
+// How the backward gets the fp32 states entering every chunk.
+enum BwdCkpt : int {
+    kCkNone = 0,     // regenerated by a forward pass over the batch
+    kCkDirect = 1,   // given: fp32 rows every 64 tokens
+    kCkWiden = 2,    // given: bf16 rows every 64 tokens, widened to fp32
+    kCkSegments = 3  // given: rows every n > 64 tokens; the forward over the n-token segments
+};
+int bwd_ckpt_mode(bool given, int64_t n, bool bf16) {
+    if (!given) return kCkNone;
+    if (n == 0 || n == la::kChunk) return bf16 ? kCkWiden : kCkDirect;
+    return kCkSegments;
+}
+// the segments of a batch cut at multiples of n: at most ceil(T / n) + N of them
+int64_t max_segments(int64_t T, int32_t N, int64_t n) { return (T + n - 1) / n + N; }
+
 struct BwdLayout {
-    size_t pro, ck, o, ds, gh, gp, total;
+    size_t pro, ck, o, ds, gh, gp, pro_n, pro_seg, cu_seg, s0_seg, total;
 };
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
-BwdLayout bwd_layout(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, int32_t V, bool ck_given) {
+BwdLayout bwd_layout(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, int32_t V, int mode, int64_t n = 0) {
     BwdLayout L{};
     size_t off = up256(la::ws_layout(N).total);
     const size_t rows = static_cast<size_t>((T + la::kChunk - 1) / la::kChunk + N);  // >= sum ceil(L_i / 64)
     L.pro = 0;
     L.ck = off;
-    if (!ck_given) off += up256(rows * HV * K * V * sizeof(float));
+    if (mode != kCkDirect) off += up256(rows * HV * K * V * sizeof(float));
     L.o = off;
-    if (!ck_given) off += up256(static_cast<size_t>(T) * HV * V * 2);
+    if (mode == kCkNone || mode == kCkSegments) off += up256(static_cast<size_t>(T) * HV * V * 2);
     L.ds = off;
     off += up256(static_cast<size_t>(N) * HV * K * V * sizeof(float));
     L.gh = off;
     if (HV != HK) off += up256(2 * static_cast<size_t>(T) * HV * K * sizeof(float));
     L.gp = off;  // per (sequence, head, chunk range) sums for the softplus gate's parameter gradients
     off += up256(2 * static_cast<size_t>(N) * HV * la::kBwdPieces * sizeof(float));
+    if (mode == kCkSegments) {
+        // the cadence-n row offsets, the segments' own prologue area, boundaries and start states
+        const int64_t S = max_segments(T, N, n);
+        L.pro_n = off;
+        off += up256(la::ws_layout(N).total);
+        L.pro_seg = off;
+        off += up256(la::ws_layout(static_cast<int32_t>(S)).total);
+        L.cu_seg = off;
+        off += up256(static_cast<size_t>(S + 1) * sizeof(int64_t));
+        L.s0_seg = off;
+        off += up256(static_cast<size_t>(S) * HV * K * V * sizeof(float));
+    }
     L.total = off;
     return L;
 }
@@ -562,7 +589,15 @@ size_t la_gdn_summary_bwd_workspace_bytes(int32_t N, int32_t HV, int32_t K, int3
 size_t la_gdn_bwd_workspace_bytes(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, int32_t V,
                                   int32_t checkpoints_given) {
     if (T < 0 || N < 0 || HK <= 0 || HV <= 0) return 0;
-    return bwd_layout(T, N, HK, HV, K, V, checkpoints_given != 0).total;
+    return bwd_layout(T, N, HK, HV, K, V, checkpoints_given != 0 ? kCkDirect : kCkNone).total;
+}
+
+size_t la_gdn_bwd_workspace_bytes_ckpt(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, int32_t V,
+                                       int64_t checkpoint_every_n, int32_t checkpoint_bf16) {
+    if (T < 0 || N < 0 || HK <= 0 || HV <= 0 || checkpoint_every_n < 0 || checkpoint_every_n % la::kChunk != 0)
+        return 0;
+    const int mode = bwd_ckpt_mode(checkpoint_every_n > 0, checkpoint_every_n, checkpoint_bf16 != 0);
+    return bwd_layout(T, N, HK, HV, K, V, mode, checkpoint_every_n).total;
 }
 
 la_status gdn_bwd(const la_gdn_bwd_params* p, void* stream) {
@@ -590,11 +625,14 @@ la_status gdn_bwd(const la_gdn_bwd_params* p, void* stream) {
         if (p->initial_state_dtype != LA_DTYPE_F32 && p->initial_state_dtype != LA_DTYPE_BF16) return LA_ERR_UNSUPPORTED;
         if (!aligned(p->initial_state, p->initial_state_dtype == LA_DTYPE_F32 ? 4 : 2)) return LA_ERR_INVALID_ARG;
     }
-    if (p->checkpoints && !aligned(p->checkpoints, 4)) return LA_ERR_INVALID_ARG;
+    if (p->checkpoint_every_n < 0 || p->checkpoint_every_n % la::kChunk != 0) return LA_ERR_INVALID_ARG;
+    const bool ck_bf16 = p->checkpoint_bf16 != 0;
+    if (p->checkpoints && !aligned(p->checkpoints, ck_bf16 ? 2 : 4)) return LA_ERR_INVALID_ARG;
     if ((p->d_final_state && !aligned(p->d_final_state, 4)) || (p->d_initial_state && !aligned(p->d_initial_state, 4)))
         return LA_ERR_INVALID_ARG;
-    const bool ck_given = p->checkpoints != nullptr;
-    const BwdLayout BL = bwd_layout(p->T, p->N, p->HK, p->HV, p->K, p->V, ck_given);
+    const int mode = bwd_ckpt_mode(p->checkpoints != nullptr, p->checkpoint_every_n, ck_bf16);
+    const int64_t ck_n = mode == kCkSegments ? p->checkpoint_every_n : la::kChunk;
+    const BwdLayout BL = bwd_layout(p->T, p->N, p->HK, p->HV, p->K, p->V, mode, ck_n);
     void* ws = p->workspace;
     if (ws) {
         if (p->workspace_bytes < BL.total || !aligned(ws, 256)) return LA_ERR_WORKSPACE;
@@ -603,11 +641,12 @@ la_status gdn_bwd(const la_gdn_bwd_params* p, void* stream) {
     }
     uint8_t* wb = static_cast<uint8_t*>(ws);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const float* ck = p->checkpoints;
+    const float* ck = static_cast<const float*>(p->checkpoints);
     const la::WorkspaceLayout PL = la::ws_layout(p->N);
-    if (!ck_given) {
-        // states entering every chunk: the forward with fp32 checkpoints every 64 tokens
-        la_gdn_fwd_params f;
+    const int64_t row_elems = static_cast<int64_t>(p->HV) * p->K * p->V;
+    const int64_t rows64 = (p->T + la::kChunk - 1) / la::kChunk + p->N;  // the regenerated rows' capacity
+    // the forward over the batch (or over its segments), writing fp32 states every 64 tokens
+    auto regen_fwd = [&](la_gdn_fwd_params& f) {
         std::memset(&f, 0, sizeof(f));
         f.q = p->q; f.q_stride_t = p->q_stride_t; f.q_stride_h = p->q_stride_h;
         f.k = p->k; f.k_stride_t = p->k_stride_t; f.k_stride_h = p->k_stride_h;
@@ -624,22 +663,75 @@ la_status gdn_bwd(const la_gdn_bwd_params* p, void* stream) {
         f.checkpoints = wb + BL.ck; f.checkpoint_dtype = LA_DTYPE_F32; f.checkpoint_every_n = la::kChunk;
         f.workspace = wb + BL.pro; f.workspace_bytes = PL.total;
         f.status = p->status;
-        if ((st = gdn_fwd(&f, stream)) != LA_OK) return st;
-        ck = reinterpret_cast<const float*>(wb + BL.ck);
-    } else {
-        // only the prologue: validation and the chunk-row offsets of the caller's checkpoints
+    };
+    // a prologue over the batch: validation and the checkpoint-row offsets at cadence n
+    auto prologue = [&](size_t area, int64_t n) {
         PrologueArgs pa;
         pa.cu = p->cu_seqlens;
         pa.cu64 = p->cu_seqlens_bits == 64;
         pa.T = p->T;
         pa.N = p->N;
-        pa.ckpt_n = la::kChunk;
-        pa.hdr = reinterpret_cast<la::WsHeader*>(wb + BL.pro);
-        pa.order = reinterpret_cast<int32_t*>(wb + BL.pro + PL.order);
-        pa.ckpt_off = reinterpret_cast<int64_t*>(wb + BL.pro + PL.ckpt_off);
-        pa.keys = reinterpret_cast<uint64_t*>(wb + BL.pro + PL.keys);
+        pa.ckpt_n = n;
+        pa.hdr = reinterpret_cast<la::WsHeader*>(wb + area);
+        pa.order = reinterpret_cast<int32_t*>(wb + area + PL.order);
+        pa.ckpt_off = reinterpret_cast<int64_t*>(wb + area + PL.ckpt_off);
+        pa.keys = reinterpret_cast<uint64_t*>(wb + area + PL.keys);
         pa.user_status = p->status;
-        if (la::launch_prologue(pa, s) != cudaSuccess) return LA_ERR_CUDA;
+        return la::launch_prologue(pa, s) == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+    };
+    if (mode == kCkNone) {
+        // states entering every chunk: the forward with fp32 checkpoints every 64 tokens
+        la_gdn_fwd_params f;
+        regen_fwd(f);
+        if ((st = gdn_fwd(&f, stream)) != LA_OK) return st;
+        ck = reinterpret_cast<const float*>(wb + BL.ck);
+    } else if (mode == kCkDirect) {
+        // only the prologue: validation and the chunk-row offsets of the caller's checkpoints
+        if ((st = prologue(BL.pro, la::kChunk)) != LA_OK) return st;
+    } else if (mode == kCkWiden) {
+        // bf16 rows at the chunk cadence: widened to fp32
+        if ((st = prologue(BL.pro, la::kChunk)) != LA_OK) return st;
+        la::CkptArgs ca;
+        std::memset(&ca, 0, sizeof(ca));
+        ca.src = p->checkpoints;
+        ca.src_bf16 = 1;
+        ca.row_elems = row_elems;
+        ca.hdr = reinterpret_cast<const la::WsHeader*>(wb + BL.pro);
+        ca.max_rows = rows64;
+        ca.dst = reinterpret_cast<float*>(wb + BL.ck);
+        if (la::launch_ckpt_widen(ca, s) != cudaSuccess) return LA_ERR_CUDA;
+        ck = reinterpret_cast<const float*>(wb + BL.ck);
+    } else {
+        // rows every n > 64 tokens: the forward over the n-token segments, each from its row,
+        // writes the states entering every chunk in the order the backward reads them
+        if ((st = prologue(BL.pro_n, ck_n)) != LA_OK) return st;
+        const int64_t S = max_segments(p->T, p->N, ck_n);
+        la::CkptArgs ca;
+        std::memset(&ca, 0, sizeof(ca));
+        ca.src = p->checkpoints;
+        ca.src_bf16 = ck_bf16;
+        ca.row_elems = row_elems;
+        ca.hdr = reinterpret_cast<const la::WsHeader*>(wb + BL.pro_n);
+        ca.cu = p->cu_seqlens;
+        ca.cu64 = p->cu_seqlens_bits == 64;
+        ca.N = p->N;
+        ca.T = p->T;
+        ca.n = ck_n;
+        ca.ckpt_off_n = reinterpret_cast<const int64_t*>(wb + BL.pro_n + PL.ckpt_off);
+        ca.cu_seg = reinterpret_cast<int64_t*>(wb + BL.cu_seg);
+        ca.s0_seg = reinterpret_cast<float*>(wb + BL.s0_seg);
+        ca.max_seg = S;
+        if (la::launch_ckpt_segments(ca, s) != cudaSuccess) return LA_ERR_CUDA;
+        la_gdn_fwd_params f;
+        regen_fwd(f);
+        f.cu_seqlens = wb + BL.cu_seg; f.cu_seqlens_bits = 64;
+        f.N = static_cast<int32_t>(S);
+        f.initial_state = wb + BL.s0_seg; f.initial_state_dtype = LA_DTYPE_F32;
+        f.workspace = wb + BL.pro_seg; f.workspace_bytes = la::ws_layout(static_cast<int32_t>(S)).total;
+        if ((st = gdn_fwd(&f, stream)) != LA_OK) return st;
+        // the backward's own chunk-row offsets over the batch
+        if ((st = prologue(BL.pro, la::kChunk)) != LA_OK) return st;
+        ck = reinterpret_cast<const float*>(wb + BL.ck);
     }
     b.q = static_cast<const uint16_t*>(p->q); b.q_st = p->q_stride_t; b.q_sh = p->q_stride_h;
     b.k = static_cast<const uint16_t*>(p->k); b.k_st = p->k_stride_t; b.k_sh = p->k_stride_h;

@@ -348,9 +348,10 @@ typedef struct la_gdn_bwd_params {
     int32_t use_qk_l2norm;
     const void* initial_state;   /* [N, HO, K, V] or NULL */
     int32_t initial_state_dtype;
-    /* states entering every chunk, as gdn_fwd writes them with checkpoint_every_n = 64 and
-       fp32 checkpoints ([sum ceil(L_i / 64), HO, K, V]); NULL: regenerated by a forward pass */
-    const float* checkpoints;
+    /* the forward's checkpoints, as gdn_fwd writes them ([sum ceil(L_i / n), HO, K, V]: the
+       states entering offsets 0, n, 2n, ... of each sequence), with n = checkpoint_every_n and the
+       dtype of checkpoint_bf16 below; NULL: regenerated by a forward pass */
+    const void* checkpoints;
     /* ---- incoming gradients ---- */
     const void* d_o;  int64_t d_o_stride_t, d_o_stride_h;   /* [T, HO, V] bf16 */
     const float* d_final_state;  /* [N, HO, K, V] fp32 or NULL (zero) */
@@ -373,6 +374,9 @@ typedef struct la_gdn_bwd_params {
     int32_t beta_bf16;           /* beta is bf16 (values, or logits with beta_sigmoid) */
     float* d_a_log;              /* [HO] fp32 out (LA_GATE_SOFTPLUS), or NULL */
     float* d_dt_bias;            /* [HO] fp32 out (LA_GATE_SOFTPLUS), or NULL */
+    /* ---- the given checkpoints' cadence and dtype (zero-initialised: every 64 tokens, fp32) ---- */
+    int64_t checkpoint_every_n;  /* 0 or 64: the chunk cadence; else a multiple of 64 */
+    int32_t checkpoint_bf16;     /* the rows are bf16 (as gdn_fwd writes with checkpoint_dtype bf16) */
 } la_gdn_bwd_params;
 
 /*
@@ -381,8 +385,17 @@ typedef struct la_gdn_bwd_params {
  * Page: every variant has "a full backward", which reuses the forward's checkpoints at the
  * chunk cadence.  Gradients of L = sum(d_o * o) + sum(d_final_state * final_state) with
  * respect to q, k, v, g, beta and the initial state; grouped heads: dq and dk of a q/k head
- * sum the contributions of its value heads.  When `checkpoints` is NULL the library first
- * re-runs the forward with fp32 checkpoints every 64 tokens into the workspace.  Each
+ * sum the contributions of its value heads.  The backward walks each chunk from the state
+ * entering it (page, "States and checkpoints": it reuses rows at the chunk cadence and
+ * regenerates the dense series from any other rows):
+ *   - fp32 rows every 64 tokens are read as they are;
+ *   - bf16 rows every 64 tokens are widened to fp32 in the workspace;
+ *   - rows every n > 64 tokens (fp32 or bf16): every sequence is cut at multiples of n into
+ *     segments that each start from their row, and one forward launch over all the segments
+ *     (independent, so they run side by side) regenerates the states entering every chunk.
+ *     From fp32 rows these are bitwise the states the full forward produced;
+ *   - no rows: the library re-runs the forward with fp32 checkpoints every 64 tokens.
+ * Each
  * (sequence, head) runs in a fixed order, so results do not depend on the batch around a
  * sequence.  When the (sequence, head) units outnumber the CTAs the GPU holds at once, the
  * call enqueues several launches that walk each unit in four chunk ranges, the state gradient
@@ -393,9 +406,15 @@ typedef struct la_gdn_bwd_params {
  */
 la_status gdn_bwd(const la_gdn_bwd_params* p, void* stream);
 
-/* Bytes of device workspace gdn_bwd needs (checkpoints_given = 0 when they are regenerated). */
+/* Bytes of device workspace gdn_bwd needs (checkpoints_given = 0 when they are regenerated,
+   1 for fp32 rows every 64 tokens). */
 size_t la_gdn_bwd_workspace_bytes(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, int32_t V,
                                   int32_t checkpoints_given);
+
+/* Bytes of device workspace gdn_bwd needs with given checkpoint rows every checkpoint_every_n
+   tokens (0: none given), fp32 or bf16 (checkpoint_bf16). */
+size_t la_gdn_bwd_workspace_bytes_ckpt(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, int32_t V,
+                                       int64_t checkpoint_every_n, int32_t checkpoint_bf16);
 
 /* Parameters of gdn_summary_bwd.  Strides are in elements. */
 typedef struct la_gdn_summary_bwd_params {

@@ -280,6 +280,11 @@ BWD_ERRORS = [
      B.LA_ERR_INVALID_ARG),
     ("softplus gate with outputs reaches the workspace check",
      dict(gate_mode=B.LA_GATE_SOFTPLUS, a_log=FAKE, dt_bias=FAKE, d_a_log=FAKE, d_dt_bias=FAKE), B.LA_ERR_WORKSPACE),
+    ("checkpoint cadence not a multiple of 64", dict(checkpoints=FAKE, checkpoint_every_n=100), B.LA_ERR_INVALID_ARG),
+    ("negative checkpoint cadence", dict(checkpoints=FAKE, checkpoint_every_n=-64), B.LA_ERR_INVALID_ARG),
+    ("misaligned fp32 checkpoints", dict(checkpoints=FAKE + 2), B.LA_ERR_INVALID_ARG),
+    ("bf16 checkpoints every 1024 tokens reach the workspace check",
+     dict(checkpoints=FAKE + 2, checkpoint_bf16=1, checkpoint_every_n=1024), B.LA_ERR_WORKSPACE),
 ]
 
 
@@ -288,6 +293,23 @@ def test_gdn_bwd_rejects(name, over, code):
     lib = B.load()
     p = _bwd(**over)
     assert lib.gdn_bwd(ctypes.byref(p), None) == code
+
+
+def test_bwd_workspace_bytes_by_checkpoint_kind():
+    """Given fp32 rows every 64 tokens need the least; bf16 rows add the widened copy; sparse
+    rows also the regenerating forward's output, segment boundaries and start states."""
+    lib = B.load()
+    args = (65536, 8, 32, 32, 128, 128)
+    none = lib.la_gdn_bwd_workspace_bytes(*args, 0)
+    direct = lib.la_gdn_bwd_workspace_bytes(*args, 1)
+    assert lib.la_gdn_bwd_workspace_bytes_ckpt(*args, 0, 0) == none
+    assert lib.la_gdn_bwd_workspace_bytes_ckpt(*args, 64, 0) == direct
+    widen = lib.la_gdn_bwd_workspace_bytes_ckpt(*args, 64, 1)
+    sparse = lib.la_gdn_bwd_workspace_bytes_ckpt(*args, 1024, 0)
+    assert direct < widen < none < sparse
+    rows = 65536 // 64 + 8
+    assert widen - direct >= rows * 32 * 128 * 128 * 4
+    assert lib.la_gdn_bwd_workspace_bytes_ckpt(*args, 100, 0) == 0
 
 
 def test_summary_bwd_workspace_bytes():

@@ -38,18 +38,19 @@ def cotangents(w, seed, with_final=True):
     return do, dfin
 
 
-def run_bwd(w, do, dfin, l2=True, checkpoints=None, scale=None):
+def run_bwd(w, do, dfin, l2=True, checkpoints=None, scale=None, checkpoint_every_n=64):
     d = dev()
     status = torch.zeros(1, dtype=torch.int32, device=d)
     out = la.gdn_bwd(w.q.to(d), w.k.to(d), w.v.to(d), w.g.to(d), w.beta.to(d), w.cu_seqlens.to(d), do.to(d),
                      use_qk_l2norm=l2, scale=scale,
                      initial_state=None if w.initial_state is None else w.initial_state.to(d),
-                     d_final_state=None if dfin is None else dfin.to(d), checkpoints=checkpoints, status=status)
+                     d_final_state=None if dfin is None else dfin.to(d), checkpoints=checkpoints, status=status,
+                     checkpoint_every_n=checkpoint_every_n)
     assert la.read_status(status) == 0
     return [None if x is None else x.float().cpu().numpy() for x in out]
 
 
-def compare(w, got, ref, units=None, label=""):
+def compare(w, got, ref, units=None, label="", f32_tol=F32_TOL):
     names = ["dq", "dk", "dv", "dg", "dbeta", "d_initial_state"]
     errs = {}
     for name, x in zip(names, got):
@@ -63,7 +64,7 @@ def compare(w, got, ref, units=None, label=""):
         errs[name] = rel(x, r)
     print(f"[parity] bwd {w.name}{label}: " + ", ".join(f"{k_} {v_:.2e}" for k_, v_ in errs.items()))
     for name, e in errs.items():
-        assert e <= (BF16_TOL if name in ("dq", "dk", "dv") else F32_TOL), errs
+        assert e <= (BF16_TOL if name in ("dq", "dk", "dv") else f32_tol), errs
     return errs
 
 
@@ -113,6 +114,56 @@ def test_bwd_reuses_forward_checkpoints_bitwise():
     b = run_bwd(w, do, dfin, checkpoints=ck)
     for x, y in zip(a, b):
         assert np.array_equal(x, y)
+
+
+def fwd_checkpoints(w, n, dtype):
+    d = dev()
+    _, _, ck = la.gdn_fwd(w.q.to(d), w.k.to(d), w.v.to(d), w.g.to(d), w.beta.to(d), w.cu_seqlens.to(d),
+                          initial_state=None if w.initial_state is None else w.initial_state.to(d),
+                          checkpoint_every_n=n, checkpoint_dtype=dtype)
+    return ck
+
+
+@pytest.mark.parametrize("n", [128, 256])
+def test_bwd_sparse_fp32_checkpoints_regenerate_the_same_bits(n):
+    """Page, "States and checkpoints": the backward regenerates the states entering every chunk
+    from sparser rows.  The segments start from the forward's exact fp32 states, so the
+    gradients are bitwise those computed from the rows every 64 tokens (and from a full re-run).
+    Ragged lengths: partial last segments and chunks, an empty sequence, one-chunk sequences."""
+    w = W.draw("bwd sparse ckpt", [300, 0, 64, 1000, 129, 1, 520], 2, 4, 128, 128, seed=471, initial_state=True,
+               slow_decay=True)
+    do, dfin = cotangents(w, 472)
+    dense = run_bwd(w, do, dfin, checkpoints=fwd_checkpoints(w, 64, torch.float32))
+    sparse = run_bwd(w, do, dfin, checkpoints=fwd_checkpoints(w, n, torch.float32), checkpoint_every_n=n)
+    regen = run_bwd(w, do, dfin)
+    for name, x, y, z in zip(["dq", "dk", "dv", "dg", "dbeta", "d_initial_state"], dense, sparse, regen):
+        assert np.array_equal(x, y), name
+        assert np.array_equal(x, z), name
+
+
+@pytest.mark.parametrize("n", [64, 192])
+def test_bwd_bf16_checkpoints_against_oracle(n):
+    """bf16 rows (the io dtype) at the chunk cadence are widened; at n = 192 the dense series is
+    regenerated from them.  The states then carry bf16's 2^-9 relative rounding before the
+    backward starts, so every gradient is held to the bf16 bound 1e-2 (as bf16 checkpoints are);
+    the oracle differentiates the exact recurrence."""
+    w = W.draw("bwd bf16 ckpt", [200, 64, 450, 77], 2, 2, 64, 64, seed=481, initial_state=True, slow_decay=True)
+    do, dfin = cotangents(w, 482)
+    got = run_bwd(w, do, dfin, checkpoints=fwd_checkpoints(w, n, torch.bfloat16), checkpoint_every_n=n)
+    ref = oracle.gdn_bwd(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, do, initial_state=w.initial_state,
+                         d_final_state=dfin)
+    compare(w, got, ref, label=f" bf16 rows every {n}", f32_tol=BF16_TOL)
+
+
+def test_bwd_dense_batch_reuses_its_1024_token_checkpoints_bitwise():
+    """The dense batch's forward keeps fp32 rows every 1024 tokens; the backward from them equals
+    the backward from rows every 64 tokens bit for bit."""
+    w = W.config(3, slow_decay=True)
+    do, dfin = cotangents(w, 491)
+    a = run_bwd(w, do, dfin, checkpoints=fwd_checkpoints(w, 64, torch.float32))
+    b = run_bwd(w, do, dfin, checkpoints=fwd_checkpoints(w, 1024, torch.float32), checkpoint_every_n=1024)
+    for name, x, y in zip(["dq", "dk", "dv", "dg", "dbeta", "d_initial_state"], a, b):
+        assert np.array_equal(x, y), name
 
 
 def test_bwd_batch_invariant():
