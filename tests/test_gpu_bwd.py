@@ -266,11 +266,12 @@ def test_bwd_bf16_start_state_regenerated_checkpoints():
     compare(w, got, ref, label=" bf16 start state")
 
 
-@pytest.mark.parametrize("save_checkpoints", [True, False])
-def test_autograd_matches_oracle_gradients(save_checkpoints):
+@pytest.mark.parametrize("save_checkpoints,n", [(True, 64), (True, 128), (False, 64)])
+def test_autograd_matches_oracle_gradients(save_checkpoints, n):
     """gdn_attention under torch.autograd: a scalar loss of o and the final state, backward through
-    the library's kernels, gradients of every input against the oracle's reverse mode."""
-    w = W.draw("autograd", [70, 129, 1], 2, 4, 64, 64, seed=491, initial_state=True, slow_decay=True)
+    the library's kernels, gradients of every input against the oracle's reverse mode (the forward
+    keeping fp32 states every 64 or 128 tokens, or none)."""
+    w = W.draw("autograd", [70, 129, 1, 300], 2, 4, 64, 64, seed=491, initial_state=True, slow_decay=True)
     d = dev()
     gen = torch.Generator().manual_seed(492)
     wo = torch.randn(w.T, w.HV, w.V, generator=gen).to(torch.bfloat16)
@@ -278,13 +279,13 @@ def test_autograd_matches_oracle_gradients(save_checkpoints):
     leaves = [x.to(d).requires_grad_(True) for x in (w.q, w.k, w.v, w.g, w.beta, w.initial_state)]
     q, k, v, g, beta, s0 = leaves
     o, fin = la.gdn_attention(q, k, v, g, beta, w.cu_seqlens.to(d), initial_state=s0,
-                              save_checkpoints=save_checkpoints)
+                              save_checkpoints=save_checkpoints, checkpoint_every_n=n)
     loss = (o.float() * wo.to(d).float()).sum() + (fin * wf.to(d)).sum()
     loss.backward()
     ref = oracle.gdn_bwd(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, wo, initial_state=w.initial_state,
                          d_final_state=wf)
     got = [x.grad.float().cpu().numpy() for x in leaves]
-    compare(w, got, ref, label=f" autograd (saved checkpoints: {save_checkpoints})")
+    compare(w, got, ref, label=f" autograd (saved checkpoints: {save_checkpoints}, every {n})")
 
 
 def test_bwd_fused_projection_views_int64_cu_single_key_head():
