@@ -37,6 +37,7 @@ EXPORTED_SYMBOLS = (
     "la_version",
     "la_set_kernel_timing_events",
     "la_test_set_wait_hooks",
+    "la_test_set_fwd_pieces",
     "gdn_fwd_static_workspace",
     "gdn_decode",
     "gdn_bwd",
@@ -159,6 +160,8 @@ def load(build_if_missing: bool = True):
         lib.la_set_kernel_timing_events.argtypes = [_vp, _vp]
         lib.la_test_set_wait_hooks.restype = ctypes.c_int
         lib.la_test_set_wait_hooks.argtypes = [_i32, ctypes.c_uint64]
+        lib.la_test_set_fwd_pieces.restype = ctypes.c_int
+        lib.la_test_set_fwd_pieces.argtypes = [_i32]
         lib.gdn_fwd_host.restype = ctypes.c_int
         lib.gdn_fwd_host.argtypes = [ctypes.POINTER(GdnFwdHostParams), _vp]
         lib.la_gdn_fwd_host_staging_bytes.restype = ctypes.c_size_t

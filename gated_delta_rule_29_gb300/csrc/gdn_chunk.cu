@@ -33,7 +33,10 @@
 // units outnumber one wave (it runs one CTA per SM), each unit's chunks run as
 // four consecutive ranges in successive launches, a range starting from the
 // exact fp32 state the previous one left in the outputs: the same bits as one
-// walk, in fewer waves.
+// walk, in fewer waves.  The forward does the same when its units fill between
+// one and four waves and the final state is kept in fp32 (the hand-over goes
+// through it): a range ending inside its sequence writes the state it reached
+// there, and the checkpoint row if the boundary is one.
 //
 // Gated DeltaProduct (mode kModeGdp, 2 <= n <= 64 updates per token): the same
 // recurrence walked on the update timeline (n rows per token of k, v, beta; a
@@ -92,6 +95,7 @@ struct __align__(16) Scalars {
     uint32_t tmem_base;
     int32_t unit_lo, unit_hi;
     int32_t status0;
+    int32_t ranges_ok;
 };
 static_assert(sizeof(Scalars) <= 7168, "scalar area");
 
@@ -338,10 +342,18 @@ __global__ void __launch_bounds__(kCta, 2)
     const int r = tid;  // TMEM lane, value column, stacked token row
     const int HO = a.HV;
 
-    // one read of the status word for the whole CTA (another CTA may set it meanwhile)
-    if (tid == 0) sc.status0 = *reinterpret_cast<volatile int32_t*>(&a.hdr->status);
+    // one read of the status word for the whole CTA (another CTA may set it meanwhile), and of
+    // the prologue's verdict on forward ranges
+    if (tid == 0) {
+        sc.status0 = *reinterpret_cast<volatile int32_t*>(&a.hdr->status);
+        sc.ranges_ok = a.hdr->ranges_ok;
+    }
     __syncthreads();
     if (sc.status0 != LA_OK) return;
+    // chunk ranges: the summary's whenever launched so, the forward's unless the prologue found
+    // the sequence lengths spread, in which case launch 0 walks whole units and the rest return
+    const bool ranged = !kGdp && a.pieces > 1 && (kSum || a.pieces_request > 1 || sc.ranges_ok != 0);
+    if (!kGdp && a.pieces > 1 && !ranged && a.item_base > 0) return;
 
     if (tid < 32) {
         tmem_alloc(&sc.tmem_base, TMEM_COLS);
@@ -386,7 +398,6 @@ __global__ void __launch_bounds__(kCta, 2)
     const uint32_t kq_bytes = KD * 128u + (kFwd ? static_cast<uint32_t>(KD / 64) * QR * 128u : 0u);
     const uint32_t v_bytes = static_cast<uint32_t>(a.V) * 128u;
 
-    const bool ranged = kSum && a.pieces > 1;  // one range item per CTA, from blockIdx
     for (int iter = 0;; ++iter) {
         if (tid == 0) {
             const unsigned long long u =
@@ -461,10 +472,10 @@ __global__ void __launch_bounds__(kCta, 2)
         {
             const int64_t base = s0_unit * KD * a.V + r;
             const int64_t fbase0 = fin_unit * KD * a.V + r;
-            const bool ckpt0 = kFwd && a.ckpt && nchunks > 0 && r < a.V;
             // a later range starts from what the previous range left in the outputs: the end
             // state (fp32, value tile) or the transition (stored transposed: lane r reads row r)
             const bool from_out = ranged && rng > 0;
+            const bool ckpt0 = kFwd && a.ckpt && nchunks > 0 && r < a.V && !from_out;
             const int64_t cbase = ckpt0 ? ((a.ckpt_off[seq] * HO + h) * KD) * a.V + r : 0;
 #pragma unroll 1
             for (int p = 0; p < KP; ++p) {
@@ -962,8 +973,9 @@ __global__ void __launch_bounds__(kCta, 2)
                 // then pre-multiplied by the next chunk's decay for its state update
                 const float gnext = last ? 1.f : exp2f(sc.gsum[0] + sc.gsum[1]);
                 const int64_t fbase = fin_unit * KD * a.V + r;
-                const bool ckpt = kFwd && a.ckpt && !last && (static_cast<int64_t>(c + 1) * kChunk) % a.ckpt_n == 0 &&
-                                  r < a.V;
+                // (a range that ends inside its sequence writes the checkpoint row at its end too)
+                const bool ckpt = kFwd && a.ckpt && c + 1 < nchunks &&
+                                  (static_cast<int64_t>(c + 1) * kChunk) % a.ckpt_n == 0 && r < a.V;
                 const int64_t cbase =
                     ckpt ? (((a.ckpt_off[seq] + static_cast<int64_t>(c + 1) * kChunk / a.ckpt_n) * HO + h) * KD) * a.V + r
                          : 0;
@@ -992,6 +1004,14 @@ __global__ void __launch_bounds__(kCta, 2)
 #pragma unroll
                                     for (int e = 0; e < 16; ++e)
                                         store_state(a, fbase + static_cast<int64_t>(16 * p + e) * a.V, x[e]);
+                                if (ckpt) {
+#pragma unroll
+                                    for (int e = 0; e < 16; ++e) {
+                                        const int64_t idx = cbase + static_cast<int64_t>(16 * p + e) * a.V;
+                                        if (a.ckpt_bf16) static_cast<uint16_t*>(a.ckpt)[idx] = f_to_bf16_bits(x[e]);
+                                        else static_cast<float*>(a.ckpt)[idx] = x[e];
+                                    }
+                                }
                             } else if (r < KD) {
                                 // transition[j][k] = P[k][j]: lane r = j holds column j of P
                                 float* tp = a.transition + (unit_state * KD + r) * KD + 16 * p;
@@ -1043,6 +1063,27 @@ __global__ void __launch_bounds__(kCta, 2)
 }
 
 // ------------------------------------------------------------------ host side
+// Ranges per unit for a forward whose units fill between one and four waves: the count in
+// 2..8 that minimises the estimated time, waves x (chunks per range + two chunks for a
+// launch's start and drain, as measured), against whole units (ceil(units / slots) waves of
+// `chunks`), from the mean sequence length.  1 when no count saves at least 5 %.  The kernel
+// still walks whole units when the lengths turn out spread (the prologue's verdict).
+static int fwd_pieces(int64_t units, int64_t slots, int64_t chunks) {
+    if (chunks < 2) return 1;
+    const double whole = static_cast<double>((units + slots - 1) / slots) * static_cast<double>(chunks);
+    int best = 1;
+    double best_t = whole;
+    for (int p = 2; p <= 8 && p <= chunks; ++p) {
+        const int64_t waves = (units * p + slots - 1) / slots;
+        const double t = static_cast<double>(waves) * (static_cast<double>(chunks) / p + 2.0);
+        if (t < best_t) {
+            best_t = t;
+            best = p;
+        }
+    }
+    return best_t < 0.95 * whole ? best : 1;
+}
+
 template <int KD, int MODE>
 static cudaError_t launch_one(const ChunkArgs& a, const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm,
                               const CUtensorMap& om, int device, cudaStream_t s) {
@@ -1083,10 +1124,15 @@ static cudaError_t launch_one(const ChunkArgs& a, const CUtensorMap& qm, const C
     b.pieces = 1;
     b.item_base = 0;
     b.items = 0;
-    if (MODE == kModeSummary && b.num_units > slots) {
-        // four ranges per unit, one wave per launch: item r * units + u's predecessor (u, r - 1)
+    if (MODE == kModeSummary && b.num_units > slots) b.pieces = kSumPieces;
+    if (MODE == kModeFwd && b.final_state && !b.final_bf16 && b.num_units > slots) {
+        if (a.pieces_request > 0) b.pieces = a.pieces_request;
+        else if (b.num_units <= 4 * slots)
+            b.pieces = fwd_pieces(b.num_units, slots, (b.T / (b.N > 0 ? b.N : 1) + kChunk - 1) / kChunk);
+    }
+    if (b.pieces > 1) {
+        // ranges of every unit, one wave per launch: item r * units + u's predecessor (u, r - 1)
         // is `units` > `slots` items earlier, so it ran in an earlier launch
-        b.pieces = kSumPieces;
         const int64_t items = b.num_units * b.pieces;
         for (int64_t base = 0; base < items; base += slots) {
             b.item_base = base;

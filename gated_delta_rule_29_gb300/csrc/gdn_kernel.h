@@ -47,7 +47,10 @@ struct WsHeader {
     int32_t status;     // LA_OK or a device-side error code
     int32_t ckpt_rows;  // sum_i ceil(L_i / n) when the prologue computed checkpoint offsets
     uint64_t ticket;    // next unit to hand out (8-byte aligned for the 64-bit atomic)
+    int32_t ranges_ok;  // the sequences' chunk counts are within 1/8 of each other (forward ranges pay)
+    int32_t reserved;
 };
+static_assert(sizeof(WsHeader) <= 256, "the header lives in the workspace's first 256 bytes");
 
 struct PrologueArgs {
     const void* cu;
@@ -86,11 +89,16 @@ struct ChunkArgs {
     float* transition;               // summary: [N, HO, K, K]
     int32_t tiles_per_head;          // fwd 1; summary 2 (value tile, transition tile)
     int64_t num_units;               // N * HO * tiles_per_head
-    // Summary with more units than one wave: each unit's chunks run as `pieces` consecutive
-    // ranges in successive launches (items r * num_units + u, range r of unit u); this launch's CTA
-    // b runs item item_base + b.  A range starts from the state the previous range left in the
-    // outputs (end state, transition).  pieces 1: one persistent launch over the units.
+    // Summary with more units than one wave, or a forward (fp32 final state) with one to four
+    // waves of units: each unit's chunks run as `pieces` consecutive ranges in successive
+    // launches (items r * num_units + u, range r of unit u); this launch's CTA b runs item
+    // item_base + b.  A range starts from the state the previous range left in the outputs (end
+    // or final state, transition).  pieces 1: one persistent launch over the units.
     int32_t pieces;
+    int32_t pieces_request;          // forward: 0 automatic, 1 whole walks, >= 2 that many ranges (test hook)
+    // A forward launched in automatic ranges still walks whole sequences when the prologue found
+    // their lengths spread (WsHeader::ranges_ok = 0): the first launch then runs the persistent
+    // walk over whole units and the later launches return at once.
     int64_t item_base;
     int64_t items;                   // items of this launch
     WsHeader* hdr;

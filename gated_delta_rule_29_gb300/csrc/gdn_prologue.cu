@@ -9,7 +9,9 @@
 //   * orders sequences longest-first (ties by index) so the persistent kernel
 //     hands out the longest (sequence, head) units first.  The order only decides
 //     which unit starts when, never how a unit is computed, so results stay
-//     bitwise independent of the batch.
+//     bitwise independent of the batch;
+//   * records whether the sequences' chunk counts are close enough for the
+//     forward's range launches to pay (the same bits either way).
 #include "gdn_kernel.h"
 #include "../../include/liblinattn.h"
 
@@ -117,6 +119,13 @@ __global__ void __launch_bounds__(kPrologueThreads) gdn_prologue_kernel(Prologue
         }
     }
     for (int i = tid; i < N; i += blockDim.x) a.order[i] = static_cast<int32_t>(keys[i] & 0xFFFFFFFFull);
+    if (tid == 0) {
+        // the forward's chunk ranges are cut at the longest range of each wave: they pay only
+        // when the sequences' chunk counts are within 1/8 of each other
+        const uint64_t cmax = N > 0 ? 0xFFFFFFFFull - (keys[0] >> 32) : 0;
+        const uint64_t cmin = N > 0 ? 0xFFFFFFFFull - (keys[N - 1] >> 32) : 0;
+        a.hdr->ranges_ok = (N > 0 && cmin * 8 >= cmax * 7) ? 1 : 0;
+    }
 }
 
 cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t s) {

@@ -112,6 +112,8 @@ la_status internal_workspace(size_t need, cudaStream_t stream, void** out) {
 // environment): skip the forward's K/Q tile loads, and replace the bounded waits' budget.
 std::atomic<int32_t> g_test_skip_tile_load{0};
 std::atomic<uint64_t> g_test_wait_budget_ns{0};
+// Scheduling test hook, set only through la_test_set_fwd_pieces: 0 automatic chunk ranges.
+std::atomic<int32_t> g_test_fwd_pieces{0};
 
 la_status resolve_workspace(void* user, size_t user_bytes, int32_t N, cudaStream_t stream, void** out) {
     const size_t need = la::ws_layout(N).total;
@@ -225,6 +227,7 @@ la_status run(const Common& c, ChunkArgs& ka, const void* q, int64_t q_st, int64
     // failure-path test hooks (off unless a test set them with la_test_set_wait_hooks)
     ka.test_skip_tile_load = g_test_skip_tile_load.load(std::memory_order_relaxed) != 0;
     if (const uint64_t b = g_test_wait_budget_ns.load(std::memory_order_relaxed)) ka.wait_budget_ns = b;
+    ka.pieces_request = g_test_fwd_pieces.load(std::memory_order_relaxed);
     if (ka.num_units == 0) return LA_OK;
 
     CUtensorMap qm, km, vm, om;
@@ -927,6 +930,12 @@ la_status la_read_status(const int32_t* device_status, void* stream, int32_t* ou
 la_status la_test_set_wait_hooks(int32_t skip_tile_load, uint64_t wait_budget_ns) {
     g_test_skip_tile_load.store(skip_tile_load != 0 ? 1 : 0, std::memory_order_relaxed);
     g_test_wait_budget_ns.store(wait_budget_ns, std::memory_order_relaxed);
+    return LA_OK;
+}
+
+la_status la_test_set_fwd_pieces(int32_t pieces) {
+    if (pieces < 0 || pieces > 16) return LA_ERR_INVALID_ARG;
+    g_test_fwd_pieces.store(pieces, std::memory_order_relaxed);
     return LA_OK;
 }
 

@@ -149,6 +149,14 @@ typedef struct la_gdn_fwd_params {
  * capturing stream that would need to grow the buffer returns
  * LA_ERR_WORKSPACE and launches nothing (pass a workspace, or make a call of
  * that size before capturing).
+ * Scheduling: each (sequence, head) is one serial walk over its chunks.  When
+ * the walks fill between one and four waves of the CTAs the GPU holds at once
+ * and final_state is fp32 (or the state pool is), the call may instead enqueue
+ * several launches that walk every sequence in 2 to 8 chunk ranges, handing the
+ * exact fp32 state from range to range through final_state (each walk reads
+ * and writes only its own rows there, and a range ending on a checkpoint
+ * boundary writes that row): the results are the same bits as one walk, with
+ * a shorter tail when the last wave would be partly empty.
  * Returns LA_OK once the work is enqueued.
  */
 la_status gdn_fwd(const la_gdn_fwd_params* p, void* stream);
@@ -505,6 +513,18 @@ la_status la_set_kernel_timing_events(void* start_event, void* stop_event);
  * them (the library reads no environment variables).
  */
 la_status la_test_set_wait_hooks(int32_t skip_tile_load, uint64_t wait_budget_ns);
+
+/*
+ * Scheduling test hook, not for production use (no counterpart on the pages).
+ * pieces = 0 restores the automatic choice of gdn_fwd's chunk ranges (see
+ * gdn_fwd, "Scheduling"); 1 makes every later gdn_fwd call walk whole
+ * sequences; 2..16 makes it walk every sequence in that many ranges whenever
+ * the walks outnumber one wave and final_state is fp32 (or the pool is), so
+ * that tests can compare ranged and whole walks bitwise on any batch.
+ * Process-wide, like la_test_set_wait_hooks.  LA_ERR_INVALID_ARG for pieces
+ * outside 0..16.
+ */
+la_status la_test_set_fwd_pieces(int32_t pieces);
 
 /* Static description of a status code. */
 const char* la_status_string(la_status s);

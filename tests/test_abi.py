@@ -312,6 +312,16 @@ def test_bwd_workspace_bytes_by_checkpoint_kind():
     assert lib.la_gdn_bwd_workspace_bytes_ckpt(*args, 100, 0) == 0
 
 
+def test_fwd_pieces_hook_range():
+    """The scheduling test hook takes 0 (automatic) .. 16 and rejects the rest; it only stores
+    the setting (no device work), so it is callable without a GPU."""
+    lib = B.load()
+    for bad in (-1, 17):
+        assert lib.la_test_set_fwd_pieces(bad) == B.LA_ERR_INVALID_ARG
+    for ok in (16, 1, 0):
+        assert lib.la_test_set_fwd_pieces(ok) == B.LA_OK
+
+
 def test_summary_bwd_workspace_bytes():
     lib = B.load()
     a = lib.la_gdn_summary_bwd_workspace_bytes(8, 32, 128, 128)
