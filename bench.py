@@ -278,7 +278,7 @@ def run_ours(args, world, rank, local):
     o = torch.empty(T, HO, V, dtype=torch.bfloat16, device=dev)
     fin = torch.empty(N, HO, K, V, dtype=torch.float32, device=dev)
     ck = torch.empty(R, HO, K, V, dtype=torch.float32, device=dev)
-    ws = torch.empty(la.workspace_bytes(N), dtype=torch.uint8, device=dev)
+    ws = torch.empty(la.api.split_workspace_bytes(T, N, HV), dtype=torch.uint8, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def step(qq=q, kk=k, vv=v, gg=g, bb=beta, cc=cu, ss=s0, oo=o, ff=fin, kc=ck):
@@ -926,7 +926,7 @@ def run_table(args, world, rank, local):
         o = torch.empty(T, HV, V, dtype=torch.bfloat16, device=dev)
         fin = torch.empty(N, HV, K, V, dtype=torch.float32, device=dev)
         ck = torch.empty(R, HV, K, V, dtype=torch.float32, device=dev) if n_ck else None
-        ws = torch.empty(la.workspace_bytes(N), dtype=torch.uint8, device=dev)
+        ws = torch.empty(la.api.split_workspace_bytes(T, N, HV), dtype=torch.uint8, device=dev)
         status = torch.zeros(1, dtype=torch.int32, device=dev)
 
         def step():

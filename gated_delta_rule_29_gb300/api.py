@@ -94,6 +94,11 @@ def workspace_bytes(N: int, summary: bool = False) -> int:
     return int(B.load().la_gdn_workspace_bytes(int(N), int(bool(summary))))
 
 
+def split_workspace_bytes(T: int, N: int, HV: int) -> int:
+    """Workspace with which gdn_fwd may run as two passes (the same bits as the fused kernel)."""
+    return int(B.load().la_gdn_fwd_split_workspace_bytes(int(T), int(N), int(HV)))
+
+
 def gdn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
             cu_seqlens: torch.Tensor, *, scale: Optional[float] = None, use_qk_l2norm: bool = True,
             initial_state: Optional[torch.Tensor] = None, output_final_state: bool = True,
@@ -159,7 +164,7 @@ def gdn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
         R = checkpoint_rows_hint if checkpoint_rows_hint is not None else checkpoint_rows(cu_seqlens, checkpoint_every_n)
         checkpoints = torch.empty(R, HO, K, V, dtype=checkpoint_dtype, device=dev)
     if workspace is None:
-        need = workspace_bytes(N) if n <= 1 else B.load().la_gdp_workspace_bytes(T, N, HK, HV, K, V, n)
+        need = split_workspace_bytes(T, N, HV) if n <= 1 else B.load().la_gdp_workspace_bytes(T, N, HK, HV, K, V, n)
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     if initial_state is not None and state_indices is None:
         initial_state = initial_state.contiguous()

@@ -31,6 +31,7 @@ EXPORTED_SYMBOLS = (
     "gdn_fwd",
     "gdn_summary",
     "la_gdn_workspace_bytes",
+    "la_gdn_fwd_split_workspace_bytes",
     "la_checkpoint_rows",
     "la_read_status",
     "la_status_string",
@@ -38,6 +39,7 @@ EXPORTED_SYMBOLS = (
     "la_set_kernel_timing_events",
     "la_test_set_wait_hooks",
     "la_test_set_fwd_pieces",
+    "la_test_set_fwd_passes",
     "gdn_fwd_static_workspace",
     "gdn_decode",
     "gdn_bwd",
@@ -148,6 +150,8 @@ def load(build_if_missing: bool = True):
         lib.gdn_summary.argtypes = [ctypes.POINTER(GdnSummaryParams), _vp]
         lib.la_gdn_workspace_bytes.restype = ctypes.c_size_t
         lib.la_gdn_workspace_bytes.argtypes = [_i32, _i32]
+        lib.la_gdn_fwd_split_workspace_bytes.restype = ctypes.c_size_t
+        lib.la_gdn_fwd_split_workspace_bytes.argtypes = [_i64, _i32, _i32]
         lib.la_checkpoint_rows.restype = ctypes.c_int
         lib.la_checkpoint_rows.argtypes = [_vp, _i32, _i32, _i64, ctypes.POINTER(_i64)]
         lib.la_read_status.restype = ctypes.c_int
@@ -162,6 +166,8 @@ def load(build_if_missing: bool = True):
         lib.la_test_set_wait_hooks.argtypes = [_i32, ctypes.c_uint64]
         lib.la_test_set_fwd_pieces.restype = ctypes.c_int
         lib.la_test_set_fwd_pieces.argtypes = [_i32]
+        lib.la_test_set_fwd_passes.restype = ctypes.c_int
+        lib.la_test_set_fwd_passes.argtypes = [_i32]
         lib.gdn_fwd_host.restype = ctypes.c_int
         lib.gdn_fwd_host.argtypes = [ctypes.POINTER(GdnFwdHostParams), _vp]
         lib.la_gdn_fwd_host_staging_bytes.restype = ctypes.c_size_t

@@ -89,15 +89,16 @@ struct __align__(16) Scalars {
     float u[64];    // rk_j 2^{b_31 - b_j}           (factorised decay, column factor)
     float cA[64];   // beta_i rk_i 2^{b_i - b_31}    (row factor of A)
     float cP[64];   // scale rq_i 2^{b_i - b_31}     (row factor of P)
-    float Y[4][256];  // per-warp 16 x 16 solve scratch
     float gsum[2];    // per-warp sums of the next chunk's g * log2(e)
-    uint64_t bar_kq, bar_v, bar_mma, bar_o;
+    uint64_t bar_kq, bar_v, bar_mma, bar_o, bar_f;
     uint32_t tmem_base;
     int32_t unit_lo, unit_hi;
     int32_t status0;
     int32_t ranges_ok;
+    float Y[4][256];  // per-warp 16 x 16 solve scratch (last: the WY pass keeps it elsewhere)
 };
 static_assert(sizeof(Scalars) <= 7168, "scalar area");
+constexpr uint32_t kScalarsNoY = static_cast<uint32_t>(sizeof(Scalars) - sizeof(float[4][256]));
 
 // fp32 64 x 64 tiles (A, T): 16-byte chunks XOR-swizzled by row to spread rows over the banks.
 __device__ __forceinline__ int midx(int r, int c) { return r * 64 + ((((c >> 2) ^ (r & 15)) << 2) | (c & 3)); }
@@ -306,14 +307,177 @@ __device__ void solve_unit_lower(const float* M, float* Tf, float (*Ys)[256], in
     __syncthreads();
 }
 
+// ------------------------------------------------------------------ state-independent phases
+// (shared by the fused kernel and the WY pass, so both compute the same bits)
+
+// Rows of G = [K; Q] [K; Q]^T (at TMEM column col) into g64 (thread r: row r's first 64
+// columns, the products with the key rows), and the inverse row norms from G's diagonal: rk (key
+// rows, threads 0-63) and rq (query rows, threads 64-127; the forward only); rows past the
+// chunk's tokens get 0.
+template <bool kFwd>
+__device__ __forceinline__ void g_rows_and_norms(uint32_t trow, uint32_t col, int r, int n, int nq, int l2norm,
+                                                 float (&g64)[64], Scalars& sc) {
+    const int lane = r & 31;
+    if (r < 64 || kFwd) {
+#pragma unroll
+        for (int p = 0; p < 4; ++p) tmem_ld16(trow + col + 16 * p, *reinterpret_cast<float(*)[16]>(&g64[16 * p]));
+        float nrm = 0.f;
+        if (r < 64) {
+            tmem_wait_ld();
+            if (r < 32) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) nrm = (e == lane) ? g64[e] : nrm;
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) nrm = (e == lane) ? g64[32 + e] : nrm;
+            }
+        } else {
+            float d32[32];
+            const uint32_t cbase = col + (r & ~31);
+            tmem_ld16(trow + cbase, *reinterpret_cast<float(*)[16]>(&d32[0]));
+            tmem_ld16(trow + cbase + 16, *reinterpret_cast<float(*)[16]>(&d32[16]));
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) nrm = (e == lane) ? d32[e] : nrm;
+        }
+        const int row = r & 63;
+        const int nvalid = (r < 64) ? n : nq;  // key rows, or the chunk's query tokens
+        const float inv = (row < nvalid) ? (l2norm ? 1.0f / sqrtf(nrm + 1e-6f) : 1.f) : 0.f;
+        if (r < 64) sc.rk[row] = inv;
+        else sc.rq[row] = inv;
+    }
+}
+
+// Per-token factors of a chunk from the per-warp gate scans (sc.bw), the norms and beta
+// (b_cur: this thread's row); returns, block-wide, whether the factorised decays are in range.
+template <bool kFwd, bool kGdp>
+__device__ __forceinline__ bool chunk_scalars(Scalars& sc, int tid, int n, int nq, int tq0, int rel0, int NH,
+                                              float b_cur, float scale) {
+    bool in_range = true;
+    if (tid < 64) {
+        const int i = tid;
+        const float bi = sc.bw[i] + (i >= 32 ? sc.bw[31] : 0.f);
+        const float b31 = sc.bw[31];
+        const float bC = sc.bw[31] + sc.bw[63];
+        const float rk = sc.rk[i], rq = kFwd ? sc.rq[i] : 0.f;
+        const float bet = i < n ? b_cur : 0.f;
+        const float gam = exp2f(bi);
+        const float e = exp2f(bi - b31);
+        sc.b[i] = bi;
+        sc.bet[i] = bet;
+        sc.sx[i] = bet * gam * rk;
+        sc.sd[i] = exp2f(bC - bi) * rk;
+        sc.u[i] = rk * exp2f(b31 - bi);
+        sc.cA[i] = bet * rk * e;
+        if (kGdp) {
+            // query row i is token tok0 + i, read after its last update row ri of the chunk
+            const int ri = i < nq ? (tq0 + i) * NH + NH - 1 - rel0 : -1;
+            const float bq = ri >= 0 ? sc.bw[ri] + (ri >= 32 ? sc.bw[31] : 0.f) : 0.f;
+            sc.sq[i] = ri >= 0 ? scale * rq * exp2f(bq) : 0.f;
+            sc.cP[i] = ri >= 0 ? scale * rq * exp2f(bq - b31) : 0.f;
+        } else {
+            sc.sq[i] = scale * rq * gam;
+            sc.cP[i] = scale * rq * e;
+        }
+        in_range = fabsf(bi - b31) <= kFastRange;
+    }
+    return __syncthreads_and(in_range) != 0;
+}
+
+// A (fp32, strictly lower, into M for the solve) and P (bf16, lower with the diagonal, into PB)
+// from this thread's row of G.
+template <bool kFwd, bool kGdp>
+__device__ __forceinline__ void build_a_p(float (&g64)[64], const Scalars& sc, float* M, uint8_t* PB, bool fast, int r,
+                                          int nq, int tq0, int rel0, int NH, float scale) {
+    if (r < 64 || kFwd) {
+        const int i = r & 63;
+        const bool is_a = r < 64;
+        const float ci = fast ? (is_a ? sc.cA[i] : sc.cP[i]) : (is_a ? sc.bet[i] * sc.rk[i] : scale * sc.rq[i]);
+        // the row's position on the update timeline (GDP query rows: the token's last update;
+        // rows past the chunk's tokens are zero and fully masked)
+        const int ip = (kGdp && !is_a) ? (i < nq ? (tq0 + i) * NH + NH - 1 - rel0 : -1) : i;
+        const float bi = sc.b[ip < 0 ? 0 : ip];
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            float* gv = &g64[16 * p];
+            if (fast) {
+                float uv[16];
+                ld8(uv, &sc.u[16 * p]);
+                ld8(uv + 8, &sc.u[16 * p + 8]);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) gv[e] *= ci * uv[e];
+            } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int j = 16 * p + e;
+                    const float dec = (j <= ip) ? exp2f(bi - sc.b[j]) : 0.f;
+                    gv[e] *= ci * sc.rk[j] * dec;
+                }
+            }
+            if (is_a) {
+#pragma unroll
+                for (int j4 = 0; j4 < 4; ++j4) {
+                    const int j = 16 * p + 4 * j4;
+                    float4 w;
+                    w.x = (j + 0 < i) ? gv[4 * j4 + 0] : 0.f;
+                    w.y = (j + 1 < i) ? gv[4 * j4 + 1] : 0.f;
+                    w.z = (j + 2 < i) ? gv[4 * j4 + 2] : 0.f;
+                    w.w = (j + 3 < i) ? gv[4 * j4 + 3] : 0.f;
+                    *reinterpret_cast<float4*>(&M[midx(i, j)]) = w;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    if (16 * p + e > ip) gv[e] = 0.f;
+                store8_split(PB + sw128_off(i, 2 * p), nullptr, &gv[0]);
+                store8_split(PB + sw128_off(i, 2 * p + 1), nullptr, &gv[8]);
+            }
+        }
+    }
+}
+
+// T (fp32, from the solve) -> bf16, K-major (128-byte swizzle), into TB; zeros above the
+// diagonal blocks.
+__device__ __forceinline__ void t_to_bf16(const float* Tf, uint8_t* TB, int tid) {
+    const int i = tid >> 1;
+#pragma unroll
+    for (int cc4 = 0; cc4 < 4; ++cc4) {
+        const int cc = (tid & 1) * 4 + cc4;
+        if ((cc >> 1) > (i >> 4)) {
+            // a block above the diagonal: zeros
+            *reinterpret_cast<uint4*>(TB + sw128_off(i, cc)) = make_uint4(0u, 0u, 0u, 0u);
+            continue;
+        }
+        const float4 lo4 = *reinterpret_cast<const float4*>(&Tf[midx(i, 8 * cc)]);
+        const float4 hi4 = *reinterpret_cast<const float4*>(&Tf[midx(i, 8 * cc + 4)]);
+        const float x[8] = {lo4.x, lo4.y, lo4.z, lo4.w, hi4.x, hi4.y, hi4.z, hi4.w};
+        store8_split(TB + sw128_off(i, cc), nullptr, x);
+    }
+}
+
+// One WY record into shared memory, on bar_f: T (bf16, into TB's place), P (into PB) and the
+// factors beta, sx, sq, sd (into sc.bet .. sc.sd, contiguous).  One thread.
+__device__ __forceinline__ void load_wy(const ChunkArgs& a, const CUtensorMap& wymap, int64_t chunk, int h,
+                                        void* TBdst, void* PBdst, Scalars& sc) {
+    const int64_t item = chunk * a.HV + h;
+    mbar_arrive_expect_tx(&sc.bar_f, static_cast<uint32_t>(kWyRecordBytes));
+    tma_load_3d(TBdst, &wymap, &sc.bar_f, 0, static_cast<int>(item), 0);
+    tma_load_3d(PBdst, &wymap, &sc.bar_f, 0, static_cast<int>(item), 64);
+    bulk_load(sc.bet, a.wy + item * static_cast<int64_t>(kWyRecordBytes) + 2 * kWyTileBytes,
+              static_cast<uint32_t>(kWyFactorBytes), &sc.bar_f);
+}
+
 template <int KD, int MODE>
 __global__ void __launch_bounds__(kCta, 2)
     gdn_chunk_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
-                     const ChunkArgs a) {
+                     const __grid_constant__ CUtensorMap wymap, const ChunkArgs a) {
     constexpr bool kFwd = MODE != kModeSummary;  // queries and outputs (the forward, or GDP's)
     constexpr bool kGdp = MODE == kModeGdp;
     constexpr bool kSum = MODE == kModeSummary;
+    // the state pass of the two-pass forward: T, P and the factors of every chunk come from the
+    // WY pass's records instead of being formed here
+    constexpr bool kSplit = MODE == kModeFwdSplit;
     // waits sleep in hardware when another CTA shares the SM (the forward runs two per SM; the
     // summary, with its larger shared-memory footprint, one)
     constexpr bool kSleep = !kSum;
@@ -364,6 +528,7 @@ __global__ void __launch_bounds__(kCta, 2)
         mbar_init(&sc.bar_v, 1);
         mbar_init(&sc.bar_mma, 1);
         mbar_init(&sc.bar_o, 1);
+        mbar_init(&sc.bar_f, 1);
         fence_mbar_init();
     }
     tc_fence_before();
@@ -390,8 +555,8 @@ __global__ void __launch_bounds__(kCta, 2)
         fence_proxy_async_smem();
         __syncthreads();
     }
-    uint32_t ph_kq = 0, ph_v = 0, ph_mma = 0, ph_o = 0;  // parity of the next wait on each barrier
-    bool pend_kq = false, pend_v = false, pend_mma = false, pend_o = false;
+    uint32_t ph_kq = 0, ph_v = 0, ph_mma = 0, ph_o = 0, ph_f = 0;  // parity of the next wait on each barrier
+    bool pend_kq = false, pend_v = false, pend_mma = false, pend_o = false, pend_f = false;
     bool failed = false;
     const uint64_t budget = a.wait_budget_ns;
     const int64_t per_seq = static_cast<int64_t>(HO) * a.tiles_per_head;
@@ -556,6 +721,10 @@ __global__ void __launch_bounds__(kCta, 2)
             }
             pend_kq = !a.test_skip_tile_load;
             pend_v = value_tile;
+            if (kSplit) {
+                if (tid == 0) load_wy(a, wymap, a.chunk_off[seq] + lo, h, M, PB, sc);
+                pend_f = true;
+            }
         }
         for (int c = lo; c < hi; ++c) {
             const int64_t t0 = ts + static_cast<int64_t>(c) * kChunk;
@@ -585,7 +754,7 @@ __global__ void __launch_bounds__(kCta, 2)
                 ph_kq ^= 1u;
                 pend_kq = false;
             }
-            if (tid == 0 && ok) {
+            if (!kSplit && tid == 0 && ok) {
                 tc_fence_after();
                 const uint32_t idesc = idesc_bf16_f32(128, kFwd ? 128 : 64, false, false);
 #pragma unroll
@@ -595,154 +764,76 @@ __global__ void __launch_bounds__(kCta, 2)
                 }
                 umma_commit(&sc.bar_mma);
             }
-            pend_mma = ok;
-            if (tid < 64) {
-                float x = (tid < n) ? g_cur * kLog2e : 0.f;
-#pragma unroll
-                for (int off = 1; off < 32; off <<= 1) {
-                    const float y = __shfl_up_sync(0xffffffffu, x, off);
-                    if ((tid & 31) >= off) x += y;
-                }
-                sc.bw[tid] = x;
-            }
-            {
-                const bool okg = mbar_wait(&sc.bar_mma, ph_mma, budget, kSleep);
-                if (okg) {
-                    ph_mma ^= 1u;
-                    pend_mma = false;
-                }
-                ok = ok && okg;
-            }
-            tc_fence_after();
-            const int lane = r & 31;
             float g64[64];
-            if (r < 64 || kFwd) {
-#pragma unroll
-                for (int p = 0; p < 4; ++p) tmem_ld16(trow + COL_R1 + 16 * p, *reinterpret_cast<float(*)[16]>(&g64[16 * p]));
-                float nrm = 0.f;
-                if (r < 64) {
-                    tmem_wait_ld();
-                    if (r < 32) {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) nrm = (e == lane) ? g64[e] : nrm;
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) nrm = (e == lane) ? g64[32 + e] : nrm;
-                    }
-                } else {
-                    float d32[32];
-                    const uint32_t cbase = COL_R1 + (r & ~31);
-                    tmem_ld16(trow + cbase, *reinterpret_cast<float(*)[16]>(&d32[0]));
-                    tmem_ld16(trow + cbase + 16, *reinterpret_cast<float(*)[16]>(&d32[16]));
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) nrm = (e == lane) ? d32[e] : nrm;
+            bool fast = true;
+            if constexpr (kSplit) {
+                // no G: (K S)^T and (Q S)^T are issued as soon as the tile is in (at a range's first
+                // chunk once every thread has written its row of the start state's bf16 copy)
+                if (c == lo) {
+                    fence_proxy_async_smem();
+                    tc_fence_before();
+                    if (__syncthreads_or(!ok)) { failed = true; break; }
                 }
-                const int row = r & 63;
-                const int nvalid = (r < 64) ? n : nq;  // key rows, or the chunk's query tokens
-                const float inv = (row < nvalid) ? (a.l2norm ? 1.0f / sqrtf(nrm + 1e-6f) : 1.f) : 0.f;
-                if (r < 64) sc.rk[row] = inv;
-                else sc.rq[row] = inv;
-            }
-            tc_fence_before();
-            if (__syncthreads_or(!ok)) { failed = true; break; }
-            // ---- S3: (K S)^T and (Q S)^T = S^T [K; Q]^T, issued as soon as every thread holds its row of
-            // G (the product reuses G's columns); it runs while the scalars and A / P are formed
-            if (tid == 0) {
-                tc_fence_after();
-                const uint32_t idesc = idesc_bf16_f32(128, kFwd ? 128 : 64, false, false);
-#pragma unroll
-                for (int kk = 0; kk < KD / 16; ++kk) {
-                    const uint64_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                    umma_bf16(tmem + COL_R1, d_wb + off, d_kq + off, idesc, kk > 0);
-                }
-                if (!kFwd) {
+                if (tid == 0 && ok) {
+                    tc_fence_after();
+                    const uint32_t idesc = idesc_bf16_f32(128, 128, false, false);
 #pragma unroll
                     for (int kk = 0; kk < KD / 16; ++kk) {
                         const uint64_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                        umma_bf16(tmem + COL_R1, d_slo + off, d_kq + off, idesc, 1u);
+                        umma_bf16(tmem + COL_R1, d_wb + off, d_kq + off, idesc, kk > 0);
                     }
+                    umma_commit(&sc.bar_mma);
                 }
-                umma_commit(&sc.bar_mma);
-            }
-            pend_mma = true;
-
-            bool in_range = true;
-            if (tid < 64) {
-                const int i = tid;
-                const float bi = sc.bw[i] + (i >= 32 ? sc.bw[31] : 0.f);
-                const float b31 = sc.bw[31];
-                const float bC = sc.bw[31] + sc.bw[63];
-                const float rk = sc.rk[i], rq = kFwd ? sc.rq[i] : 0.f;
-                const float bet = i < n ? b_cur : 0.f;
-                const float gam = exp2f(bi);
-                const float e = exp2f(bi - b31);
-                sc.b[i] = bi;
-                sc.bet[i] = bet;
-                sc.sx[i] = bet * gam * rk;
-                sc.sd[i] = exp2f(bC - bi) * rk;
-                sc.u[i] = rk * exp2f(b31 - bi);
-                sc.cA[i] = bet * rk * e;
-                if (kGdp) {
-                    // query row i is token tok0 + i, read after its last update row ri of the chunk
-                    const int ri = i < nq ? (tq0 + i) * NH + NH - 1 - rel0 : -1;
-                    const float bq = ri >= 0 ? sc.bw[ri] + (ri >= 32 ? sc.bw[31] : 0.f) : 0.f;
-                    sc.sq[i] = ri >= 0 ? a.scale * rq * exp2f(bq) : 0.f;
-                    sc.cP[i] = ri >= 0 ? a.scale * rq * exp2f(bq - b31) : 0.f;
-                } else {
-                    sc.sq[i] = a.scale * rq * gam;
-                    sc.cP[i] = a.scale * rq * e;
+                pend_mma = true;
+            } else {
+                pend_mma = ok;
+                if (tid < 64) {
+                    float x = (tid < n) ? g_cur * kLog2e : 0.f;
+#pragma unroll
+                    for (int off = 1; off < 32; off <<= 1) {
+                        const float y = __shfl_up_sync(0xffffffffu, x, off);
+                        if ((tid & 31) >= off) x += y;
+                    }
+                    sc.bw[tid] = x;
                 }
-                in_range = fabsf(bi - b31) <= kFastRange;
-            }
-            const bool fast = __syncthreads_and(in_range) != 0;
-
-            // ---- S2: A (fp32, for the solve) and P (bf16) from G
-            if (r < 64 || kFwd) {
-                const int i = r & 63;
-                const bool is_a = r < 64;
-                const float ci = fast ? (is_a ? sc.cA[i] : sc.cP[i]) : (is_a ? sc.bet[i] * sc.rk[i] : a.scale * sc.rq[i]);
-                // the row's position on the update timeline (GDP query rows: the token's last update;
-                // rows past the chunk's tokens are zero and fully masked)
-                const int ip = (kGdp && !is_a) ? (i < nq ? (tq0 + i) * NH + NH - 1 - rel0 : -1) : i;
-                const float bi = sc.b[ip < 0 ? 0 : ip];
+                {
+                    const bool okg = mbar_wait(&sc.bar_mma, ph_mma, budget, kSleep);
+                    if (okg) {
+                        ph_mma ^= 1u;
+                        pend_mma = false;
+                    }
+                    ok = ok && okg;
+                }
+                tc_fence_after();
+                g_rows_and_norms<kFwd>(trow, COL_R1, r, n, nq, a.l2norm, g64, sc);
+                tc_fence_before();
+                if (__syncthreads_or(!ok)) { failed = true; break; }
+                // ---- S3: (K S)^T and (Q S)^T = S^T [K; Q]^T, issued as soon as every thread holds its row of
+                // G (the product reuses G's columns); it runs while the scalars and A / P are formed
+                if (tid == 0) {
+                    tc_fence_after();
+                    const uint32_t idesc = idesc_bf16_f32(128, kFwd ? 128 : 64, false, false);
 #pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    float* gv = &g64[16 * p];
-                    if (fast) {
-                        float uv[16];
-                        ld8(uv, &sc.u[16 * p]);
-                        ld8(uv + 8, &sc.u[16 * p + 8]);
+                    for (int kk = 0; kk < KD / 16; ++kk) {
+                        const uint64_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                        umma_bf16(tmem + COL_R1, d_wb + off, d_kq + off, idesc, kk > 0);
+                    }
+                    if (!kFwd) {
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) gv[e] *= ci * uv[e];
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const int j = 16 * p + e;
-                            const float dec = (j <= ip) ? exp2f(bi - sc.b[j]) : 0.f;
-                            gv[e] *= ci * sc.rk[j] * dec;
+                        for (int kk = 0; kk < KD / 16; ++kk) {
+                            const uint64_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                            umma_bf16(tmem + COL_R1, d_slo + off, d_kq + off, idesc, 1u);
                         }
                     }
-                    if (is_a) {
-#pragma unroll
-                        for (int j4 = 0; j4 < 4; ++j4) {
-                            const int j = 16 * p + 4 * j4;
-                            float4 w;
-                            w.x = (j + 0 < i) ? gv[4 * j4 + 0] : 0.f;
-                            w.y = (j + 1 < i) ? gv[4 * j4 + 1] : 0.f;
-                            w.z = (j + 2 < i) ? gv[4 * j4 + 2] : 0.f;
-                            w.w = (j + 3 < i) ? gv[4 * j4 + 3] : 0.f;
-                            *reinterpret_cast<float4*>(&M[midx(i, j)]) = w;
-                        }
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 16; ++e)
-                            if (16 * p + e > ip) gv[e] = 0.f;
-                        store8_split(PB + sw128_off(i, 2 * p), nullptr, &gv[0]);
-                        store8_split(PB + sw128_off(i, 2 * p + 1), nullptr, &gv[8]);
-                    }
+                    umma_commit(&sc.bar_mma);
                 }
-            }
+                pend_mma = true;
+
+                fast = chunk_scalars<kFwd, kGdp>(sc, tid, n, nq, tq0, rel0, NH, b_cur, a.scale);
+
+                // ---- S2: A (fp32, for the solve) and P (bf16) from G
+                build_a_p<kFwd, kGdp>(g64, sc, M, PB, fast, r, nq, tq0, rel0, NH, a.scale);
+            }  // !kSplit
             fence_proxy_async_smem();
             tc_fence_before();
             if (__syncthreads_or(!ok)) { failed = true; break; }
@@ -760,6 +851,14 @@ __global__ void __launch_bounds__(kCta, 2)
                     pend_v = false;
                 }
                 ok = ok && okv;
+            }
+            if (kSplit) {
+                const bool okf = mbar_wait(&sc.bar_f, ph_f, budget, kSleep);
+                if (okf) {
+                    ph_f ^= 1u;
+                    pend_f = false;
+                }
+                ok = ok && okf;
             }
             tc_fence_after();
             {
@@ -809,23 +908,9 @@ __global__ void __launch_bounds__(kCta, 2)
                 tc_fence_before();
             }
             __syncthreads();  // every V read is done before T takes the tile's space
-            solve_unit_lower(M, Tf, sc.Y, tid);
-            {
-                // T (fp32) -> bf16, K-major, into the A buffer's space (A is no longer needed)
-                const int i = tid >> 1;
-#pragma unroll
-                for (int cc4 = 0; cc4 < 4; ++cc4) {
-                    const int cc = (tid & 1) * 4 + cc4;
-                    if ((cc >> 1) > (i >> 4)) {
-                        // a block above the diagonal: zeros
-                        *reinterpret_cast<uint4*>(TB + sw128_off(i, cc)) = make_uint4(0u, 0u, 0u, 0u);
-                        continue;
-                    }
-                    const float4 lo4 = *reinterpret_cast<const float4*>(&Tf[midx(i, 8 * cc)]);
-                    const float4 hi4 = *reinterpret_cast<const float4*>(&Tf[midx(i, 8 * cc + 4)]);
-                    const float x[8] = {lo4.x, lo4.y, lo4.z, lo4.w, hi4.x, hi4.y, hi4.z, hi4.w};
-                    store8_split(TB + sw128_off(i, cc), nullptr, x);
-                }
+            if (!kSplit) {
+                solve_unit_lower(M, Tf, sc.Y, tid);
+                t_to_bf16(Tf, TB, tid);
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -968,6 +1053,15 @@ __global__ void __launch_bounds__(kCta, 2)
                 }
             }
             if (!last) pend_kq = true;
+            if (kSplit && !last) {
+                // P, the factors and the O staging buffer (the next T's place) are free: fetch the
+                // next chunk's record once the bulk store of O has read its staging buffer
+                if (tid == 0 && ok) {
+                    bulk_wait_read_all();
+                    load_wy(a, wymap, a.chunk_off[seq] + c + 1, h, M, PB, sc);
+                }
+                pend_f = true;
+            }
             {
                 // new state: bf16 copy for the next K S product, end state or checkpoint entry,
                 // then pre-multiplied by the next chunk's decay for its state update
@@ -1052,6 +1146,7 @@ __global__ void __launch_bounds__(kCta, 2)
         if (pend_v) mbar_wait(&sc.bar_v, ph_v, budget);
         if (pend_mma) mbar_wait(&sc.bar_mma, ph_mma, budget);
         if (pend_o) mbar_wait(&sc.bar_o, ph_o, budget);
+        if (pend_f) mbar_wait(&sc.bar_f, ph_f, budget);
         if (tid == 0) {
             atomicCAS(&a.hdr->status, LA_OK, LA_ERR_TIMEOUT);
             if (a.user_status) atomicCAS(a.user_status, LA_OK, LA_ERR_TIMEOUT);
@@ -1062,7 +1157,224 @@ __global__ void __launch_bounds__(kCta, 2)
     if (tid < 32) tmem_dealloc(tmem, TMEM_COLS);
 }
 
+// ------------------------------------------------------------------ WY pass of the two-pass forward
+// Every (chunk, head) item of the batch is independent of the state: G, the norms, the
+// per-token factors, A, P and T = (I + A)^{-1} are formed exactly as the fused kernel forms them
+// (the same functions, so the same bits), and written out as one record per item: T and P as
+// bf16 64 x 64 tiles by TMA stores, the factors beta, sx, sq, sd by a bulk copy.  The state pass
+// (kModeFwdSplit) then walks each sequence with only the state-dependent products on its chain.
+// CTAs of 128 threads, four per SM (52 KB of shared memory, 128 TMEM columns for G, at most 128
+// registers a thread); CTA b takes items b, b + grid, ...  Once G is formed the K/Q tile's space
+// holds T (fp32), P (bf16) and the solve's scratch; the next item's indices, gates and betas
+// are fetched while the current one is formed.
+constexpr uint32_t WY_KQ = 0;       // K/Q tile [region][128 rows][128 B] | T fp32 [64][64], P, solve scratch
+constexpr uint32_t WY_PB = 16384;   // P bf16 [64][128 B] (in the K/Q tile's space)
+constexpr uint32_t WY_Y = 24576;    // solve scratch [4][256] fp32 (in the K/Q tile's space)
+constexpr uint32_t WY_M = 32768;    // A fp32 [64][64] | T bf16 [64][128 B]
+constexpr uint32_t WY_SC = 49152;   // Scalars without the solve scratch
+constexpr uint32_t WY_SMEM = WY_SC + ((kScalarsNoY + 127) & ~127u) + 1024;
+constexpr uint32_t WY_TMEM_COLS = 128;
+
+template <int KD>
+__global__ void __launch_bounds__(kCta, 4)
+    gdn_wy_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                  const __grid_constant__ CUtensorMap wymap, const ChunkArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    Scalars& sc = *reinterpret_cast<Scalars*>(sm + WY_SC);  // (its solve scratch is not used here)
+    uint8_t* KQ = sm + WY_KQ;
+    float* Tf = reinterpret_cast<float*>(sm + WY_KQ);
+    uint8_t* PB = sm + WY_PB;
+    float (*Y)[256] = reinterpret_cast<float(*)[256]>(sm + WY_Y);
+    float* M = reinterpret_cast<float*>(sm + WY_M);
+    uint8_t* TB = sm + WY_M;
+    const int tid = threadIdx.x;
+    const int r = tid;
+    const int HO = a.HV;
+
+    if (tid == 0) sc.status0 = *reinterpret_cast<volatile int32_t*>(&a.hdr->status);
+    __syncthreads();
+    if (sc.status0 != LA_OK) return;
+    const int64_t items = a.hdr->total_chunks * HO;
+    if (static_cast<int64_t>(blockIdx.x) >= items) return;
+
+    if (tid < 32) {
+        tmem_alloc(&sc.tmem_base, WY_TMEM_COLS);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&sc.bar_kq, 1);
+        mbar_init(&sc.bar_mma, 1);
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sc.tmem_base;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(r & ~31) << 16);
+    const uint64_t d_kq = sdesc_sw128(smem_u32(KQ), 16, 1024);
+    const uint32_t kq_bytes = KD * 128u * 2u;
+    const uint64_t budget = a.wait_budget_ns;
+    uint32_t ph_kq = 0, ph_mma = 0;
+    bool pend_kq = false, pend_mma = false, failed = false;
+
+    // an item's rows: chunk c of sequence seq, head h; first token t0, n valid rows
+    auto rows_of = [&](int64_t item, int seq, int64_t& t0, int& n) {
+        const int64_t chunk = item / HO;
+        const int c = static_cast<int>(chunk - a.chunk_off[seq]);
+        const int64_t tok_s = cu_get(a.cu, a.cu64, seq);
+        const int64_t left = cu_get(a.cu, a.cu64, seq + 1) - tok_s - static_cast<int64_t>(c) * kChunk;
+        n = left < kChunk ? static_cast<int>(left) : kChunk;
+        t0 = tok_s + static_cast<int64_t>(c) * kChunk;
+    };
+    // a row's gate and beta (threads 0-63)
+    auto gates_of = [&](int64_t t0, int n, int h, float& g, float& b) {
+        g = b = 0.f;
+        if (tid < 64 && tid < n) {
+            float gA = 0.f, gdt = 0.f;
+            if (a.gate_mode == LA_GATE_SOFTPLUS) {
+                gA = -expf(a.a_log[h]);
+                gdt = a.dt_bias[h];
+            }
+            g = gate_row<false>(a, t0 + tid, h, gA, gdt);
+            b = beta_at(a, t0 + tid, h);
+        }
+    };
+
+    int64_t item = blockIdx.x;
+    int64_t t0;
+    int n;
+    rows_of(item, a.chunk_seq[item / HO], t0, n);
+    float g_cur, b_cur;
+    gates_of(t0, n, static_cast<int>(item % HO), g_cur, b_cur);
+    for (; item < items; item += gridDim.x) {
+        const int h = static_cast<int>(item % HO);
+        if (tid == 0 && !a.test_skip_tile_load) {
+            // the previous item's T, P and scratch in this space are dead (the loop ended with a
+            // barrier) and its record stores have read their sources
+            bulk_wait_read_all();
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&sc.bar_kq, kq_bytes);
+            const int hk = h / a.group;
+#pragma unroll
+            for (int rg = 0; rg < KD / 64; ++rg) {
+                tma_load_3d(KQ + rg * 16384, &kmap, &sc.bar_kq, rg * 64, hk, static_cast<int>(t0));
+                tma_load_3d(KQ + rg * 16384 + 8192, &qmap, &sc.bar_kq, rg * 64, hk, static_cast<int>(t0));
+            }
+        }
+        pend_kq = !a.test_skip_tile_load;
+        // the next item's sequence (its load completes while this item is formed)
+        const int64_t nitem = item + gridDim.x;
+        const bool has_next = nitem < items;
+        const int nseq = has_next ? a.chunk_seq[nitem / HO] : 0;
+
+        bool ok = mbar_wait(&sc.bar_kq, ph_kq, budget, true);
+        if (ok) {
+            ph_kq ^= 1u;
+            pend_kq = false;
+        }
+        if (tid == 0 && ok) {
+            tc_fence_after();
+            const uint32_t idesc = idesc_bf16_f32(128, 128, false, false);
+#pragma unroll
+            for (int kk = 0; kk < KD / 16; ++kk) {
+                const uint64_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                umma_bf16(tmem, d_kq + off, d_kq + off, idesc, kk > 0);
+            }
+            umma_commit(&sc.bar_mma);
+        }
+        pend_mma = ok;
+        if (tid < 64) {
+            float x = (tid < n) ? g_cur * kLog2e : 0.f;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, x, off);
+                if ((tid & 31) >= off) x += y;
+            }
+            sc.bw[tid] = x;
+        }
+        {
+            const bool okg = mbar_wait(&sc.bar_mma, ph_mma, budget, true);
+            if (okg) {
+                ph_mma ^= 1u;
+                pend_mma = false;
+            }
+            ok = ok && okg;
+        }
+        tc_fence_after();
+        float g64[64];
+        g_rows_and_norms<true>(trow, 0, r, n, n, a.l2norm, g64, sc);
+        tc_fence_before();
+        if (__syncthreads_or(!ok)) { failed = true; break; }
+        const bool fast = chunk_scalars<true, false>(sc, tid, n, n, 0, 0, 1, b_cur, a.scale);
+        build_a_p<true, false>(g64, sc, M, PB, fast, r, n, 0, 0, 1, a.scale);
+        // the next item's rows, gates and betas (in flight during the solve)
+        int64_t nt0 = t0;
+        int nn = 0;
+        float g_nx = 0.f, b_nx = 0.f;
+        if (has_next) {
+            rows_of(nitem, nseq, nt0, nn);
+            gates_of(nt0, nn, static_cast<int>(nitem % HO), g_nx, b_nx);
+        }
+        __syncthreads();  // A and P complete; the K/Q tile (read by the finished G product) becomes T's space
+        solve_unit_lower(M, Tf, Y, tid);
+        t_to_bf16(Tf, TB, tid);
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            tma_store_3d(&wymap, TB, 0, static_cast<int>(item), 0);
+            tma_store_3d(&wymap, PB, 0, static_cast<int>(item), 64);
+            bulk_store(a.wy + item * static_cast<int64_t>(kWyRecordBytes) + 2 * kWyTileBytes, sc.bet,
+                       static_cast<uint32_t>(kWyFactorBytes));
+            bulk_commit_group();
+        }
+        __syncthreads();  // T (fp32) and the scratch are read: the next item's tile may land in their space
+        t0 = nt0;
+        n = nn;
+        g_cur = g_nx;
+        b_cur = b_nx;
+    }
+    if (tid == 0) bulk_wait_all();
+    if (failed) {
+        if (pend_kq) mbar_wait(&sc.bar_kq, ph_kq, budget);
+        if (pend_mma) mbar_wait(&sc.bar_mma, ph_mma, budget);
+        if (tid == 0) {
+            atomicCAS(&a.hdr->status, LA_OK, LA_ERR_TIMEOUT);
+            if (a.user_status) atomicCAS(a.user_status, LA_OK, LA_ERR_TIMEOUT);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (tid < 32) tmem_dealloc(tmem, WY_TMEM_COLS);
+}
+
 // ------------------------------------------------------------------ host side
+// CTAs of kCta threads resident per SM, at most `cap`: the occupancy API's answer or the one
+// from the hardware limits (registers allocated per warp in units of 256, shared memory per SM
+// minus the per-block reserve), whichever is larger.  A CTA that cannot be resident yet simply
+// starts later and finds no work left, so overestimating costs nothing.
+static cudaError_t resident_per_sm(const void* fn, uint32_t smem, int cap, int device, int* out) {
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kCta, smem);
+    if (e != cudaSuccess) return e;
+    cudaFuncAttributes fa;
+    int smem_sm = 0, reserve = 0, regs_sm = 0;
+    if (cudaFuncGetAttributes(&fa, fn) == cudaSuccess &&
+        cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device) == cudaSuccess &&
+        cudaDeviceGetAttribute(&reserve, cudaDevAttrReservedSharedMemoryPerBlock, device) == cudaSuccess &&
+        cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, device) == cudaSuccess) {
+        const int regs_cta = ((fa.numRegs * 32 + 255) / 256) * 256 * (kCta / 32);
+        const int by_regs = regs_cta > 0 ? regs_sm / regs_cta : 1;
+        const int by_smem = smem_sm / (static_cast<int>(smem) + reserve);
+        const int hw = by_regs < by_smem ? by_regs : by_smem;
+        if (hw > per_sm) per_sm = hw;
+    }
+    if (per_sm > cap) per_sm = cap;
+    if (per_sm < 1) per_sm = 1;
+    *out = per_sm;
+    return cudaSuccess;
+}
+
 // Ranges per unit for a forward whose units fill between one and four waves: the count in
 // 2..8 that minimises the estimated time, waves x (chunks per range + two chunks for a
 // launch's start and drain, as measured), against whole units (ceil(units / slots) waves of
@@ -1086,7 +1398,7 @@ static int fwd_pieces(int64_t units, int64_t slots, int64_t chunks) {
 
 template <int KD, int MODE>
 static cudaError_t launch_one(const ChunkArgs& a, const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm,
-                              const CUtensorMap& om, int device, cudaStream_t s) {
+                              const CUtensorMap& om, const CUtensorMap& wm, int device, cudaStream_t s) {
     auto* fn = gdn_chunk_kernel<KD, MODE>;
     constexpr uint32_t smem = smem_alloc(MODE);
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -1095,37 +1407,17 @@ static cudaError_t launch_one(const ChunkArgs& a, const CUtensorMap& qm, const C
     e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     int per_sm = 0, sms = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kCta, smem);
+    e = resident_per_sm(reinterpret_cast<const void*>(fn), smem, 2, device, &per_sm);
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
     if (e != cudaSuccess) return e;
-    {
-        // Residency from the hardware limits (registers are allocated per warp in units of
-        // 256, shared memory per SM minus the per-block reserve); the larger of the two
-        // answers is used.  A CTA that cannot be resident yet simply starts later and finds
-        // the ticket exhausted, so overestimating costs nothing.
-        cudaFuncAttributes fa;
-        int smem_sm = 0, reserve = 0, regs_sm = 0;
-        if (cudaFuncGetAttributes(&fa, fn) == cudaSuccess &&
-            cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device) == cudaSuccess &&
-            cudaDeviceGetAttribute(&reserve, cudaDevAttrReservedSharedMemoryPerBlock, device) == cudaSuccess &&
-            cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, device) == cudaSuccess) {
-            const int regs_cta = ((fa.numRegs * 32 + 255) / 256) * 256 * (kCta / 32);
-            const int by_regs = regs_cta > 0 ? regs_sm / regs_cta : 1;
-            const int by_smem = smem_sm / (static_cast<int>(smem) + reserve);
-            int hw = by_regs < by_smem ? by_regs : by_smem;
-            if (hw > 2) hw = 2;
-            if (hw > per_sm) per_sm = hw;
-        }
-    }
-    if (per_sm < 1) per_sm = 1;
     const int64_t slots = static_cast<int64_t>(per_sm) * sms;
     ChunkArgs b = a;
     b.pieces = 1;
     b.item_base = 0;
     b.items = 0;
     if (MODE == kModeSummary && b.num_units > slots) b.pieces = kSumPieces;
-    if (MODE == kModeFwd && b.final_state && !b.final_bf16 && b.num_units > slots) {
+    if ((MODE == kModeFwd || MODE == kModeFwdSplit) && b.final_state && !b.final_bf16 && b.num_units > slots) {
         if (a.pieces_request > 0) b.pieces = a.pieces_request;
         else if (b.num_units <= 4 * slots)
             b.pieces = fwd_pieces(b.num_units, slots, (b.T / (b.N > 0 ? b.N : 1) + kChunk - 1) / kChunk);
@@ -1137,7 +1429,7 @@ static cudaError_t launch_one(const ChunkArgs& a, const CUtensorMap& qm, const C
         for (int64_t base = 0; base < items; base += slots) {
             b.item_base = base;
             b.items = items - base < slots ? items - base : slots;
-            fn<<<static_cast<int>(b.items), kCta, smem, s>>>(qm, km, vm, om, b);
+            fn<<<static_cast<int>(b.items), kCta, smem, s>>>(qm, km, vm, om, wm, b);
             e = cudaGetLastError();
             if (e != cudaSuccess) return e;
         }
@@ -1145,23 +1437,62 @@ static cudaError_t launch_one(const ChunkArgs& a, const CUtensorMap& qm, const C
     }
     const int grid = static_cast<int>(b.num_units < slots ? b.num_units : slots);
     if (grid <= 0) return cudaSuccess;
-    fn<<<grid, kCta, smem, s>>>(qm, km, vm, om, b);
+    fn<<<grid, kCta, smem, s>>>(qm, km, vm, om, wm, b);
     return cudaGetLastError();
 }
 
 cudaError_t launch_chunk_kernel(const ChunkArgs& a, const CUtensorMap& qm, const CUtensorMap& km,
-                                const CUtensorMap& vm, const CUtensorMap& om, int mode, cudaStream_t s) {
+                                const CUtensorMap& vm, const CUtensorMap& om, const CUtensorMap& wm, int mode,
+                                cudaStream_t s) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (a.K == 128) {
-        if (mode == kModeGdp) return launch_one<128, kModeGdp>(a, qm, km, vm, om, dev, s);
-        return mode == kModeFwd ? launch_one<128, kModeFwd>(a, qm, km, vm, om, dev, s)
-                                : launch_one<128, kModeSummary>(a, qm, km, vm, om, dev, s);
+        switch (mode) {
+            case kModeGdp: return launch_one<128, kModeGdp>(a, qm, km, vm, om, wm, dev, s);
+            case kModeFwdSplit: return launch_one<128, kModeFwdSplit>(a, qm, km, vm, om, wm, dev, s);
+            case kModeSummary: return launch_one<128, kModeSummary>(a, qm, km, vm, om, wm, dev, s);
+            default: return launch_one<128, kModeFwd>(a, qm, km, vm, om, wm, dev, s);
+        }
     }
-    if (mode == kModeGdp) return launch_one<64, kModeGdp>(a, qm, km, vm, om, dev, s);
-    return mode == kModeFwd ? launch_one<64, kModeFwd>(a, qm, km, vm, om, dev, s)
-                            : launch_one<64, kModeSummary>(a, qm, km, vm, om, dev, s);
+    switch (mode) {
+        case kModeGdp: return launch_one<64, kModeGdp>(a, qm, km, vm, om, wm, dev, s);
+        case kModeFwdSplit: return launch_one<64, kModeFwdSplit>(a, qm, km, vm, om, wm, dev, s);
+        case kModeSummary: return launch_one<64, kModeSummary>(a, qm, km, vm, om, wm, dev, s);
+        default: return launch_one<64, kModeFwd>(a, qm, km, vm, om, wm, dev, s);
+    }
+}
+
+template <int KD>
+static cudaError_t launch_wy(const ChunkArgs& a, const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& wm,
+                             int device, cudaStream_t s) {
+    auto* fn = gdn_wy_kernel<KD>;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, WY_SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0, sms = 0;
+    // four per SM: their 512 TMEM columns fill the SM's, and registers and shared memory allow it
+    e = resident_per_sm(reinterpret_cast<const void*>(fn), WY_SMEM, 4, device, &per_sm);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    if (e != cudaSuccess) return e;
+    // whole waves, at most one CTA per item of the host's bound (a.num_units); the kernel reads
+    // the item count the prologue wrote, and CTAs past it return at once
+    const int64_t bound = a.num_units;
+    int64_t grid = static_cast<int64_t>(per_sm) * sms;
+    if (grid > bound) grid = bound;
+    if (grid <= 0) return cudaSuccess;
+    fn<<<static_cast<int>(grid), kCta, WY_SMEM, s>>>(qm, km, wm, a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_wy_kernel(const ChunkArgs& a, const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& wm,
+                             cudaStream_t s) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    return a.K == 128 ? launch_wy<128>(a, qm, km, wm, dev, s) : launch_wy<64>(a, qm, km, wm, dev, s);
 }
 
 }  // namespace la

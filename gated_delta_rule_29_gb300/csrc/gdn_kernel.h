@@ -12,8 +12,9 @@ constexpr int kThreads = 256;       // threads of the fused chunk kernel
 constexpr int kPrologueThreads = 1024;
 
 // kModeGdp: the forward of Gated DeltaProduct (n delta updates per token) on the update timeline,
-// with q, g and o on the token timeline
-enum Mode : int { kModeFwd = 0, kModeSummary = 1, kModeGdp = 2 };
+// with q, g and o on the token timeline.  kModeFwdSplit: the forward's state pass, reading each
+// chunk's T, P and per-token factors from the records the WY pass (gdn_wy_kernel) wrote.
+enum Mode : int { kModeFwd = 0, kModeSummary = 1, kModeGdp = 2, kModeFwdSplit = 3 };
 enum TileKind : int { kTileValue = 0, kTileTransition = 1 };
 
 // Workspace layout (bytes from the 256-aligned workspace base).
@@ -43,12 +44,39 @@ __host__ __device__ inline WorkspaceLayout ws_layout(int32_t N) {
     return L;
 }
 
+// The two-pass forward's extra workspace, after ws_layout(N): chunk_off[N + 1] (each
+// sequence's first chunk in the batch-wide chunk numbering, and the total), chunk_seq[chunks]
+// (the sequence of each chunk), then one WY record
+// per (chunk, head) item, item = chunk * HV + h: T (bf16 [64][64], row-major), P (bf16
+// [64][64]) and the factors beta, sx, sq, sd (fp32 [4][64]).  A batch has at most T / 64 + N
+// chunks.
+constexpr size_t kWyTileBytes = 64 * 64 * 2;
+constexpr size_t kWyFactorBytes = 4 * 64 * 4;
+constexpr size_t kWyRecordBytes = 2 * kWyTileBytes + kWyFactorBytes;  // 17408: 136 rows of 128 B
+struct SplitLayout {
+    size_t chunk_off, chunk_seq, wy, total;
+    int64_t chunks, items;
+};
+__host__ __device__ inline SplitLayout split_layout(int64_t T, int32_t N, int32_t HV) {
+    SplitLayout L;
+    const size_t n = N > 0 ? static_cast<size_t>(N) : 1;
+    L.chunks = T / kChunk + (N > 0 ? N : 0);
+    L.items = L.chunks * static_cast<int64_t>(HV > 0 ? HV : 0);
+    L.chunk_off = ws_layout(N).total;
+    L.chunk_seq = ws_align(L.chunk_off + 8 * (n + 1));
+    L.wy = ws_align(L.chunk_seq + 4 * static_cast<size_t>(L.chunks > 0 ? L.chunks : 1));
+    L.total = ws_align(L.wy + static_cast<size_t>(L.items) * kWyRecordBytes);
+    return L;
+}
+
 struct WsHeader {
     int32_t status;     // LA_OK or a device-side error code
     int32_t ckpt_rows;  // sum_i ceil(L_i / n) when the prologue computed checkpoint offsets
     uint64_t ticket;    // next unit to hand out (8-byte aligned for the 64-bit atomic)
     int32_t ranges_ok;  // the sequences' chunk counts are within 1/8 of each other (forward ranges pay)
     int32_t reserved;
+    int64_t total_chunks;  // sum_i ceil(L_i / 64) when the prologue computed chunk offsets
+    uint64_t wy_ticket;    // next WY item to hand out
 };
 static_assert(sizeof(WsHeader) <= 256, "the header lives in the workspace's first 256 bytes");
 
@@ -63,6 +91,8 @@ struct PrologueArgs {
     int64_t* ckpt_off;
     uint64_t* keys;       // global sort scratch (N > kSmemSortMax)
     int32_t* user_status; // nullable
+    int64_t* chunk_off;   // nullable: [N + 1] first chunk of each sequence, then the total
+    int32_t* chunk_seq;   // with chunk_off: [total] the sequence of each chunk
 };
 
 struct ChunkArgs {
@@ -120,6 +150,10 @@ struct ChunkArgs {
     const int32_t* state_idx;
     int64_t pool_size;
     int32_t final_bf16;
+    // the two-pass forward (kModeFwdSplit and the WY pass): chunk offsets and the WY records
+    const int64_t* chunk_off;
+    const int32_t* chunk_seq;
+    uint8_t* wy;
 };
 
 // One recurrence step per sequence against a state pool (gdn_decode).
@@ -244,8 +278,13 @@ cudaError_t launch_gdp_gather(const GdpArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t s);
+// The WY pass of the two-pass forward: one record per (chunk, head) item (wymap: the records as
+// [items][136 rows][64] bf16).
+cudaError_t launch_wy_kernel(const ChunkArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
+                             const CUtensorMap& wymap, cudaStream_t s);
 cudaError_t launch_chunk_kernel(const ChunkArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
-                                const CUtensorMap& vmap, const CUtensorMap& omap, int mode, cudaStream_t s);
+                                const CUtensorMap& vmap, const CUtensorMap& omap, const CUtensorMap& wymap, int mode,
+                                cudaStream_t s);
 int chunk_kernel_grid(int device, int64_t num_units);
 
 }  // namespace la

@@ -5,7 +5,9 @@
 //     status word (the chunk kernel does nothing when it is non-zero);
 //   * resets the unit ticket of the persistent chunk kernel;
 //   * computes each sequence's first checkpoint row, an exclusive prefix sum of
-//     ceil(L_i / n) (entries are the states entering offsets 0, n, 2n, ... < L_i);
+//     ceil(L_i / n) (entries are the states entering offsets 0, n, 2n, ... < L_i),
+//     and for the two-pass forward each sequence's first chunk, the same sum with
+//     n = 64;
 //   * orders sequences longest-first (ties by index) so the persistent kernel
 //     hands out the longest (sequence, head) units first.  The order only decides
 //     which unit starts when, never how a unit is computed, so results stay
@@ -89,6 +91,24 @@ __global__ void __launch_bounds__(kPrologueThreads) gdn_prologue_kernel(Prologue
         }
         if (tid == 0) a.hdr->ckpt_rows = static_cast<int32_t>(carry);
     }
+    if (a.chunk_off) {
+        // the two-pass forward numbers the batch's chunks sequence by sequence
+        int64_t carry = 0;
+        for (int base = 0; base < N; base += blockDim.x) {
+            const int i = base + tid;
+            int64_t nch = 0;
+            if (i < N) nch = (cu_at(a.cu, a.cu64, i + 1) - cu_at(a.cu, a.cu64, i) + kChunk - 1) / kChunk;
+            int64_t total;
+            const int64_t ex = block_exclusive_scan(nch, warp_sums, total);
+            if (i < N) a.chunk_off[i] = carry + ex;
+            carry += total;
+        }
+        if (tid == 0) {
+            a.chunk_off[N] = carry;
+            a.hdr->total_chunks = carry;
+            a.hdr->wy_ticket = 0ull;
+        }
+    }
 
     const uint32_t P = next_pow2(static_cast<uint32_t>(N > 0 ? N : 1));
     volatile uint64_t* keys = P <= kSmemSortMax ? skeys : a.keys;
@@ -125,6 +145,29 @@ __global__ void __launch_bounds__(kPrologueThreads) gdn_prologue_kernel(Prologue
         const uint64_t cmax = N > 0 ? 0xFFFFFFFFull - (keys[0] >> 32) : 0;
         const uint64_t cmin = N > 0 ? 0xFFFFFFFFull - (keys[N - 1] >> 32) : 0;
         a.hdr->ranges_ok = (N > 0 && cmin * 8 >= cmax * 7) ? 1 : 0;
+    }
+    if (a.chunk_off && N > 0) {
+        // chunk_seq[g] = the sequence whose chunks include g: the last i with chunk_off[i] <= g
+        // (empty sequences share their successor's offset), by binary search over the offsets,
+        // staged in the sort keys' shared memory when they fit
+        __syncthreads();
+        const int64_t* off = a.chunk_off;
+        if (P <= kSmemSortMax) {
+            int64_t* soff = reinterpret_cast<int64_t*>(skeys);
+            for (int i = tid; i < N; i += blockDim.x) soff[i] = a.chunk_off[i];
+            __syncthreads();
+            off = soff;
+        }
+        const int64_t total = a.chunk_off[N];
+        for (int64_t gch = tid; gch < total; gch += blockDim.x) {
+            int lo = 0, hi = N - 1;
+            while (lo < hi) {
+                const int mid = (lo + hi + 1) >> 1;
+                if (off[mid] <= gch) lo = mid;
+                else hi = mid - 1;
+            }
+            a.chunk_seq[gch] = lo;
+        }
     }
 }
 

@@ -100,7 +100,10 @@ la_status internal_workspace(size_t need, cudaStream_t stream, void** out) {
         if (grow < need) grow = need;
         if (grow < (size_t(1) << 20)) grow = size_t(1) << 20;
         void* p = nullptr;
-        if (cudaMalloc(&p, grow) != cudaSuccess) return LA_ERR_CUDA;
+        if (cudaMalloc(&p, grow) != cudaSuccess) {
+            (void)cudaGetLastError();  // an allocation failure must not surface as a later launch error
+            return LA_ERR_CUDA;
+        }
         w.ptr = p;  // the previous buffer, if any, stays allocated (see above)
         w.bytes = grow;
     }
@@ -112,8 +115,10 @@ la_status internal_workspace(size_t need, cudaStream_t stream, void** out) {
 // environment): skip the forward's K/Q tile loads, and replace the bounded waits' budget.
 std::atomic<int32_t> g_test_skip_tile_load{0};
 std::atomic<uint64_t> g_test_wait_budget_ns{0};
-// Scheduling test hook, set only through la_test_set_fwd_pieces: 0 automatic chunk ranges.
+// Scheduling test hooks, set only through la_test_set_fwd_pieces / la_test_set_fwd_passes:
+// 0 automatic chunk ranges; 0 automatic choice of the fused or the two-pass forward.
 std::atomic<int32_t> g_test_fwd_pieces{0};
+std::atomic<int32_t> g_test_fwd_passes{0};
 
 la_status resolve_workspace(void* user, size_t user_bytes, int32_t N, cudaStream_t stream, void** out) {
     const size_t need = la::ws_layout(N).total;
@@ -188,13 +193,29 @@ la_status run(const Common& c, ChunkArgs& ka, const void* q, int64_t q_st, int64
               int64_t k_sh, const void* v, int64_t v_st, int64_t v_sh, int64_t ckpt_n, void* workspace,
               size_t workspace_bytes, int32_t* user_status, int mode, cudaStream_t stream, int32_t gdp_n = 1) {
     void* ws = nullptr;
-    la_status st = resolve_workspace(workspace, workspace_bytes, c.N, stream, &ws);
-    if (st != LA_OK) return st;
+    // The forward runs as two passes (the WY pass over every (chunk, head), then the state pass)
+    // when the workspace has room for the WY records; otherwise as the fused kernel.  Both give
+    // the same bits.
+    const int32_t passes = g_test_fwd_passes.load(std::memory_order_relaxed);
+    const la::SplitLayout SL = la::split_layout(c.T, c.N, c.HV);
+    bool split = mode == la::kModeFwd && c.T > 0 && passes != 1 && SL.items < (int64_t(1) << 31);
+    la_status st = LA_OK;
+    if (split) {
+        if (workspace) {
+            split = workspace_bytes >= SL.total && aligned(workspace, 256);
+            if (split) ws = workspace;
+        } else {
+            split = internal_workspace(SL.total, stream, &ws) == LA_OK;
+        }
+    }
+    if (!split && (st = resolve_workspace(workspace, workspace_bytes, c.N, stream, &ws)) != LA_OK) return st;
     const la::WorkspaceLayout L = la::ws_layout(c.N);
     uint8_t* wsb = static_cast<uint8_t*>(ws);
 
     PrologueArgs pa;
     pa.cu = c.cu;
+    pa.chunk_off = split ? reinterpret_cast<int64_t*>(wsb + SL.chunk_off) : nullptr;
+    pa.chunk_seq = split ? reinterpret_cast<int32_t*>(wsb + SL.chunk_seq) : nullptr;
     pa.cu64 = c.cu_bits == 64;
     pa.T = c.T;
     pa.N = c.N;
@@ -228,13 +249,21 @@ la_status run(const Common& c, ChunkArgs& ka, const void* q, int64_t q_st, int64
     ka.test_skip_tile_load = g_test_skip_tile_load.load(std::memory_order_relaxed) != 0;
     if (const uint64_t b = g_test_wait_budget_ns.load(std::memory_order_relaxed)) ka.wait_budget_ns = b;
     ka.pieces_request = g_test_fwd_pieces.load(std::memory_order_relaxed);
+    ka.chunk_off = pa.chunk_off;
+    ka.chunk_seq = pa.chunk_seq;
+    ka.wy = split ? wsb + SL.wy : nullptr;
     if (ka.num_units == 0) return LA_OK;
 
-    CUtensorMap qm, km, vm, om;
+    CUtensorMap qm, km, vm, om, wm;
     std::memset(&qm, 0, sizeof(qm));
     std::memset(&km, 0, sizeof(km));
     std::memset(&vm, 0, sizeof(vm));
     std::memset(&om, 0, sizeof(om));
+    std::memset(&wm, 0, sizeof(wm));
+    // the WY records as [items][136 rows][64] bf16: T at row 0, P at row 64 (the factors follow)
+    if (split && (st = make_map(&wm, ka.wy, 136, SL.items, 64, 64, static_cast<int64_t>(la::kWyRecordBytes / 2))) !=
+                     LA_OK)
+        return st;
     const int64_t Tm = c.T > 0 ? c.T : 1;  // descriptors need a non-empty extent
     const uint32_t qrows = static_cast<uint32_t>((la::kChunk + gdp_n - 1) / gdp_n);
     ka.gdp_n = gdp_n;
@@ -257,7 +286,13 @@ la_status run(const Common& c, ChunkArgs& ka, const void* q, int64_t q_st, int64
     cudaEvent_t ev0 = t_timing_start, ev1 = t_timing_stop;
     t_timing_start = t_timing_stop = nullptr;
     if (ev0 && cudaEventRecord(ev0, stream) != cudaSuccess) return LA_ERR_CUDA;
-    if (la::launch_chunk_kernel(ka, qm, km, vm, om, mode, stream) != cudaSuccess) return LA_ERR_CUDA;
+    if (split) {
+        ChunkArgs kw = ka;
+        kw.num_units = SL.items;  // the bound on (chunk, head) items
+        if (la::launch_wy_kernel(kw, qm, km, wm, stream) != cudaSuccess) return LA_ERR_CUDA;
+    }
+    if (la::launch_chunk_kernel(ka, qm, km, vm, om, wm, split ? la::kModeFwdSplit : mode, stream) != cudaSuccess)
+        return LA_ERR_CUDA;
     if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess) return LA_ERR_CUDA;
     return LA_OK;
 }
@@ -671,6 +706,7 @@ la_status gdn_bwd(const la_gdn_bwd_params* p, void* stream) {
     auto prologue = [&](size_t area, int64_t n) {
         PrologueArgs pa;
         pa.cu = p->cu_seqlens;
+        pa.chunk_off = nullptr;
         pa.cu64 = p->cu_seqlens_bits == 64;
         pa.T = p->T;
         pa.N = p->N;
@@ -809,6 +845,7 @@ la_status gdn_summary_bwd(const la_gdn_summary_bwd_params* p, void* stream) {
     // the prologue validates cu_seqlens into the status word the kernel reads first
     PrologueArgs pa;
     pa.cu = p->cu_seqlens;
+    pa.chunk_off = nullptr;
     pa.cu64 = p->cu_seqlens_bits == 64;
     pa.T = p->T;
     pa.N = p->N;
@@ -900,6 +937,11 @@ size_t la_gdn_workspace_bytes(int32_t N, int32_t summary) {
     return la::ws_layout(N).total;
 }
 
+size_t la_gdn_fwd_split_workspace_bytes(int64_t T, int32_t N, int32_t HV) {
+    if (T < 0 || N < 0 || HV <= 0) return 0;
+    return la::split_layout(T, N, HV).total;
+}
+
 la_status la_checkpoint_rows(const void* cu_seqlens_host, int32_t idx_bits, int32_t N, int64_t n, int64_t* rows_out) {
     if (!cu_seqlens_host || !rows_out || n <= 0 || N < 0 || (idx_bits != 32 && idx_bits != 64))
         return LA_ERR_INVALID_ARG;
@@ -930,6 +972,12 @@ la_status la_read_status(const int32_t* device_status, void* stream, int32_t* ou
 la_status la_test_set_wait_hooks(int32_t skip_tile_load, uint64_t wait_budget_ns) {
     g_test_skip_tile_load.store(skip_tile_load != 0 ? 1 : 0, std::memory_order_relaxed);
     g_test_wait_budget_ns.store(wait_budget_ns, std::memory_order_relaxed);
+    return LA_OK;
+}
+
+la_status la_test_set_fwd_passes(int32_t passes) {
+    if (passes < 0 || passes > 2) return LA_ERR_INVALID_ARG;
+    g_test_fwd_passes.store(passes, std::memory_order_relaxed);
     return LA_OK;
 }
 

@@ -97,7 +97,8 @@ typedef struct la_gdn_fwd_params {
     int32_t checkpoint_dtype; /* la_dtype of the checkpoint rows */
     int64_t checkpoint_every_n; /* > 0 and a multiple of 64 when checkpoints != NULL */
     /* ---- scratch and status ---- */
-    void* workspace;          /* >= la_gdn_workspace_bytes(N, 0) bytes, 256-byte aligned, or NULL */
+    void* workspace;          /* >= la_gdn_workspace_bytes(N, 0) bytes, 256-byte aligned, or NULL;
+                                 >= la_gdn_fwd_split_workspace_bytes(T, N, HV) allows two passes */
     size_t workspace_bytes;
     int32_t* status;          /* optional device int32; receives LA_OK or a device-side error */
     /* ---- optional input transforms (all zero = off; PR #616 in-kernel fusions) ---- */
@@ -149,6 +150,14 @@ typedef struct la_gdn_fwd_params {
  * capturing stream that would need to grow the buffer returns
  * LA_ERR_WORKSPACE and launches nothing (pass a workspace, or make a call of
  * that size before capturing).
+ * Two passes: half of each chunk's work does not depend on the state (the
+ * gates' cumulative sums, the row norms, A, P and T = (I + A)^{-1}).  When the
+ * workspace has room for it (la_gdn_fwd_split_workspace_bytes; with workspace
+ * = NULL the internal buffer grows to that size, and a failed allocation or a
+ * capturing stream falls back), gdn_fwd first forms that half for every
+ * (chunk, head) of the batch at once, then walks each sequence with only the
+ * state-dependent products on its serial chain; otherwise one fused kernel
+ * does both on the chain.  The two compute the same bits.
  * Scheduling: each (sequence, head) is one serial walk over its chunks.  When
  * the walks fill between one and four waves of the CTAs the GPU holds at once
  * and final_state is fp32 (or the state pool is), the call may instead enqueue
@@ -478,6 +487,12 @@ size_t la_gdp_workspace_bytes(int64_t T, int32_t N, int32_t HK, int32_t HV, int3
 /* Bytes of device workspace gdn_fwd (summary = 0) or gdn_summary (summary = 1) needs. */
 size_t la_gdn_workspace_bytes(int32_t N, int32_t summary);
 
+/* Bytes of device workspace with which gdn_fwd (num_householder <= 1) may run as two passes
+   (see gdn_fwd, "Two passes"): la_gdn_workspace_bytes(N, 0) plus per-chunk tables and one
+   17408-byte record per (chunk, head), at most (T / 64 + N) * HV of them (0.57 GB for
+   T = 65536, N = 8, HV = 32). */
+size_t la_gdn_fwd_split_workspace_bytes(int64_t T, int32_t N, int32_t HV);
+
 /*
  * Host helper: total checkpoint rows R = sum_i ceil(L_i / n) for a HOST copy of
  * cu_seqlens (idx_bits 32 or 64).  Returns LA_ERR_INVALID_ARG for n <= 0 or a
@@ -525,6 +540,15 @@ la_status la_test_set_wait_hooks(int32_t skip_tile_load, uint64_t wait_budget_ns
  * outside 0..16.
  */
 la_status la_test_set_fwd_pieces(int32_t pieces);
+
+/*
+ * Scheduling test hook, not for production use (no counterpart on the pages).
+ * passes = 0 restores the automatic choice between the fused and the two-pass
+ * forward (see gdn_fwd, "Two passes"); 1 makes every later gdn_fwd call use
+ * the fused kernel; 2 the two passes wherever the workspace allows them.
+ * Process-wide.  LA_ERR_INVALID_ARG for passes outside 0..2.
+ */
+la_status la_test_set_fwd_passes(int32_t passes);
 
 /* Static description of a status code. */
 const char* la_status_string(la_status s);

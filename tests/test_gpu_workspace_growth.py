@@ -4,8 +4,10 @@ A call with workspace = NULL uses one buffer per device that the library grows o
 The header promises that no call synchronises: growth must not wait for work already on the
 GPU (here a spin kernel on another stream), and inside a stream capture, where allocation is
 not allowed, a call that would need a larger buffer must return LA_ERR_WORKSPACE and launch
-nothing.  The scenario runs in a fresh process so that the buffer starts empty whatever the
-other tests did.
+nothing.  The growth itself is checked on the fused forward (whose workspace depends on N
+alone); then, with the automatic choice back, a captured call whose two-pass workspace does
+not fit the buffer but whose fused one does falls back to the fused kernel and succeeds.  The
+scenario runs in a fresh process so that the buffer starts empty whatever the other tests did.
 """
 import os
 import subprocess
@@ -26,6 +28,7 @@ SCRIPT = textwrap.dedent(r"""
     from gated_delta_rule_29_gb300 import binding as B
 
     lib = B.load()
+    assert lib.la_test_set_fwd_passes(1) == 0  # the fused forward: a workspace of N alone
     d = torch.device("cuda:0")
     gen = torch.Generator(device=d).manual_seed(3)
 
@@ -98,6 +101,20 @@ SCRIPT = textwrap.dedent(r"""
     assert call(huge, main.cuda_stream) == B.LA_OK
     torch.cuda.synchronize()
     assert int(huge[7].item()) == B.LA_OK
+
+    # automatic choice: the two-pass workspace of `big` (about 1.8 GB) is beyond the buffer, so
+    # under capture the call takes the fused kernel, whose workspace fits, and succeeds
+    assert lib.la_test_set_fwd_passes(0) == 0
+    need = lib.la_gdn_fwd_split_workspace_bytes(100000, 100000, 1)
+    assert need > 1 << 30
+    big[7].fill_(-1)
+    graph2 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph2, stream=cap):
+        rc_fallback = call(big, cap.cuda_stream)
+    assert rc_fallback == B.LA_OK, rc_fallback
+    graph2.replay()
+    torch.cuda.synchronize()
+    assert int(big[7].item()) == B.LA_OK
     print("growth ok", round(dt * 1e3, 2), "ms")
 """)
 
