@@ -73,7 +73,7 @@ def load_peaks():
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
-# the sources that decide the forward chunk kernel's code and launch (its DRAM traffic)
+# the sources that decide the forward's two kernels' code and launch (their DRAM traffic)
 TRAFFIC_SOURCES = ("gdn_chunk.cu", "gdn_prologue.cu", "ptx.cuh", "la_api.cu")
 
 
@@ -93,9 +93,9 @@ def kernel_source_hash():
 
 
 def profiled_traffic():
-    """DRAM bytes per launch of the fused kernel from the committed ncu summary, if it
-    was taken from the current kernel sources (else None)."""
-    p = os.path.join(ROOT, "profiles", "gdn_chunk_kernel_dense_batch.json")
+    """DRAM bytes per call of the forward's two passes (the WY pass and the state pass) from the
+    committed ncu summary, if it was taken from the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "gdn_fwd_two_pass_dense_batch.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
@@ -384,13 +384,16 @@ def run_ours(args, world, rank, local):
                        "parallelism": f"independent batches per GPU x{world}" if world > 1 else "single GPU",
                        "l2": f"inputs larger than L2 ({qkv_bytes / 1e9:.2f} GB of q/k/v per step); no flush"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                         "frac": achieved / hbm_peak, "traffic": profiled_traffic(),
-                         "peak_source": peak_src, "kernel": "gdn_chunk_kernel<128, fwd>",
+                         "frac": achieved / hbm_peak,
+                         "traffic": None if args.fwd_passes == "fused" else profiled_traffic(),
+                         "peak_source": peak_src,
+                         "kernel": ("gdn_chunk_kernel<128, fwd> (fused)" if args.fwd_passes == "fused" else
+                                    "gdn_wy_kernel<128> + gdn_chunk_kernel<128, state pass> (timed together)"),
                          "kernel_ms": kern_ms, "algorithmic_bytes": alg_bytes,
                          "tensor_tflops": tflops, "tensor_frac": tflops / tc_peak},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": 2 * args.steps,
+            "gpu_launches": (2 if args.fwd_passes == "fused" else 3) * args.steps,  # prologue, (WY pass,) state pass
             "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)
@@ -1098,12 +1101,18 @@ def main():
                          "thread and at all cores")
     ap.add_argument("--bwd-ckpt", choices=["64", "128", "256", "512", "1024", "none"], default="64",
                     help="bwd: cadence of the forward's fp32 checkpoints the backward is given (none: re-run)")
+    ap.add_argument("--fwd-passes", choices=["auto", "fused", "two"], default="auto",
+                    help="forward schedule: the automatic choice (two passes when the workspace allows), "
+                         "the fused kernel, or the two passes (the same bits either way)")
     ap.add_argument("--seq-len", type=int, default=8192,
                     help="tokens per sequence of the dense batch (8192 is the benchmark workload)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
     world, rank, local = dist_setup()
+    if args.impl == "ours" and args.fwd_passes != "auto":
+        from gated_delta_rule_29_gb300 import binding as B
+        B.load().la_test_set_fwd_passes({"fused": 1, "two": 2}[args.fwd_passes])
     try:
         if args.impl == "reference":
             return run_reference(args, world, rank)
