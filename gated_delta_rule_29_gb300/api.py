@@ -425,6 +425,39 @@ def gdn_decode(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tenso
     return o
 
 
+def compose_spans(transitions: torch.Tensor, terms: torch.Tensor, start: Optional[torch.Tensor] = None, *,
+                  backward: bool = False, out: Optional[torch.Tensor] = None,
+                  stream: Optional[torch.cuda.Stream] = None) -> torch.Tensor:
+    """Composition of span summaries on the GPU (gdn_compose_spans).  transitions [R, HO, K, K]
+    and terms [R, HO, K, V] fp32 on one CUDA device; start [HO, K, V] or None (zeros).
+    Forward: returns [R + 1, HO, K, V], the state entering each span and the final state.
+    Backward (terms = each span's own entering-state gradient, start = the cotangent after the
+    last span): the cotangent leaving each span, then the gradient entering span 0."""
+    if transitions.dim() != 4 or terms.dim() != 4:
+        raise ValueError("transitions [R, HO, K, K] and terms [R, HO, K, V] expected")
+    R, HO, K, V = terms.shape
+    if tuple(transitions.shape) != (R, HO, K, K):
+        raise ValueError(f"transitions must be [{R}, {HO}, {K}, {K}], got {tuple(transitions.shape)}")
+    dev = terms.device
+    for name, x in (("transitions", transitions), ("terms", terms), ("start", start)):
+        if x is not None and (x.dtype != torch.float32 or x.device != dev or dev.type != "cuda"):
+            raise ValueError(f"{name} must be fp32 on the CUDA device of terms")
+    if start is not None and tuple(start.shape) != (HO, K, V):
+        raise ValueError(f"start must be [{HO}, {K}, {V}]")
+    transitions, terms = transitions.contiguous(), terms.contiguous()
+    start = start.contiguous() if start is not None else None
+    if out is None:
+        out = torch.empty(R + 1, HO, K, V, dtype=torch.float32, device=dev)
+    p = B.GdnComposeParams()
+    p.R, p.HO, p.K, p.V = R, HO, K, V
+    p.transitions, p.terms = transitions.data_ptr(), terms.data_ptr()
+    p.start = start.data_ptr() if start is not None else None
+    p.out = out.data_ptr()
+    p.backward = int(bool(backward))
+    B.check(B.load().gdn_compose_spans(ctypes.byref(p), _stream_ptr(stream)), "gdn_compose_spans")
+    return out
+
+
 def read_status(status: torch.Tensor, stream: Optional[torch.cuda.Stream] = None) -> int:
     """Synchronises the stream and returns the device status word (an la_status code)."""
     out = ctypes.c_int32(0)

@@ -40,6 +40,7 @@ EXPORTED_SYMBOLS = (
     "la_test_set_wait_hooks",
     "la_test_set_fwd_pieces",
     "la_test_set_fwd_passes",
+    "gdn_compose_spans",
     "gdn_fwd_static_workspace",
     "gdn_decode",
     "gdn_bwd",
@@ -110,6 +111,15 @@ class GdnSummaryParams(ctypes.Structure):
     ]
 
 
+class GdnComposeParams(ctypes.Structure):
+    """Mirror of la_gdn_compose_params (same field order and types)."""
+    _fields_ = [
+        ("R", _i32), ("HO", _i32), ("K", _i32), ("V", _i32),
+        ("transitions", _vp), ("terms", _vp), ("start", _vp), ("out", _vp),
+        ("backward", _i32),
+    ]
+
+
 _lock = threading.Lock()
 _lib = None
 
@@ -168,6 +178,8 @@ def load(build_if_missing: bool = True):
         lib.la_test_set_fwd_pieces.argtypes = [_i32]
         lib.la_test_set_fwd_passes.restype = ctypes.c_int
         lib.la_test_set_fwd_passes.argtypes = [_i32]
+        lib.gdn_compose_spans.restype = ctypes.c_int
+        lib.gdn_compose_spans.argtypes = [ctypes.POINTER(GdnComposeParams), _vp]
         lib.gdn_fwd_host.restype = ctypes.c_int
         lib.gdn_fwd_host.argtypes = [ctypes.POINTER(GdnFwdHostParams), _vp]
         lib.la_gdn_fwd_host_staging_bytes.restype = ctypes.c_size_t

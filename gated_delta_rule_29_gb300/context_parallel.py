@@ -13,14 +13,19 @@ The backward mirrors it: each rank's state gradient from its own outputs
 (gdn_summary_bwd, the summary's counterpart on the gradient side), one all-gather, and
 the reverse composition dS_enter = transition dS_exit + dS_H give every rank the
 cotangent of its span's end state for gdn_bwd.
-The composition is a handful of small fp32 products per rank and runs on
-whatever device the tensors live on; the exchange is the only collective.
+The composition runs in the library's kernel (gdn_compose_spans: a handful of
+small fp32 products per rank, on the CUDA device of the summaries); the exchange
+is the only collective.  `entering_state` and `exit_state_grad` take an optional
+`composer` with the signature of `compose` / `compose_grads` for callers whose
+tensors are not on a GPU.
 """
 from __future__ import annotations
 
-from typing import List, Optional
+from typing import Callable, List, Optional
 
 import torch
+
+from . import api
 
 
 def compose(transitions: List[torch.Tensor], end_states: List[torch.Tensor],
@@ -32,15 +37,13 @@ def compose(transitions: List[torch.Tensor], end_states: List[torch.Tensor],
     shaped like `like` / the first end state), entering span 1, ..., and the state after the
     last span.
     """
-    if initial_state is not None:
-        S = initial_state
-    else:
-        S = torch.zeros_like(like if like is not None else end_states[0])
-    out = [S]
-    for tr, sh in zip(transitions, end_states):
-        S = torch.einsum("...ab,...av->...bv", tr, S) + sh
-        out.append(S)
-    return out
+    if not transitions:
+        if initial_state is not None:
+            return [initial_state]
+        return [torch.zeros_like(like if like is not None else end_states[0])]
+    trs, shs = torch.stack(list(transitions)), torch.stack(list(end_states))
+    out = api.compose_spans(trs, shs, initial_state, backward=False)
+    return list(out.unbind(0))
 
 
 def compose_grads(transitions: List[torch.Tensor], local_grads: List[torch.Tensor],
@@ -55,17 +58,16 @@ def compose_grads(transitions: List[torch.Tensor], local_grads: List[torch.Tenso
     the last span.  Returns len(spans) + 1 tensors: the gradient leaving each span (dS_exit_r,
     the final-state cotangent to use for span r), then the gradient entering span 0.
     """
-    S = len(transitions)
-    d_exit = [None] * S
-    d = d_final if d_final is not None else torch.zeros_like(local_grads[-1])
-    for r in range(S - 1, -1, -1):
-        d_exit[r] = d
-        d = local_grads[r] + torch.einsum("...ab,...bv->...av", transitions[r], d)
-    return d_exit + [d]
+    if not transitions:
+        return [d_final]
+    trs, loc = torch.stack(list(transitions)), torch.stack(list(local_grads))
+    out = api.compose_spans(trs, loc, d_final, backward=True)
+    return list(out.unbind(0))
 
 
 def exit_state_grad(transition: torch.Tensor, local_grad: torch.Tensor,
-                    d_final: Optional[torch.Tensor] = None, group=None) -> torch.Tensor:
+                    d_final: Optional[torch.Tensor] = None, group=None,
+                    composer: Optional[Callable] = None) -> torch.Tensor:
     """Final-state cotangent for this rank's span in the context-parallel backward.
 
     Ranks hold consecutive spans in rank order.  Each rank first takes its span's own state
@@ -86,11 +88,12 @@ def exit_state_grad(transition: torch.Tensor, local_grad: torch.Tensor,
     dfin = d_final.contiguous().clone() if d_final is not None else torch.zeros_like(local_grad)
     last = dist.get_global_rank(group, world - 1) if group is not None else world - 1
     dist.broadcast(dfin, src=last, group=group)
-    return compose_grads(trs, lgs, dfin)[rank]
+    return (composer or compose_grads)(trs, lgs, dfin)[rank]
 
 
 def entering_state(transition: torch.Tensor, end_state: torch.Tensor,
-                   initial_state: Optional[torch.Tensor] = None, group=None) -> torch.Tensor:
+                   initial_state: Optional[torch.Tensor] = None, group=None,
+                   composer: Optional[Callable] = None) -> torch.Tensor:
     """State entering this rank's span, given this rank's span summary.
 
     Ranks hold consecutive spans in rank order.  One all-gather of (transition, end_state);
@@ -108,4 +111,4 @@ def entering_state(transition: torch.Tensor, end_state: torch.Tensor,
     # every rank takes part in the broadcast (a rank without a start state sends zeros)
     s0 = initial_state.contiguous().clone() if initial_state is not None else torch.zeros_like(end_state)
     dist.broadcast(s0, src=dist.get_global_rank(group, 0) if group is not None else 0, group=group)
-    return compose(trs[:rank], shs[:rank], s0, like=end_state)[rank]
+    return (composer or compose)(trs[:rank], shs[:rank], s0, like=end_state)[rank]

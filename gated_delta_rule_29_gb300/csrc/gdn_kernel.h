@@ -278,6 +278,17 @@ cudaError_t launch_gdp_gather(const GdpArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t s);
+// Composition of span summaries (gdn_compose_spans): out [R + 1, HO, K, V].
+struct ComposeArgs {
+    int32_t R, HO, K, V;
+    const float* transitions;  // [R, HO, K, K]
+    const float* terms;        // [R, HO, K, V]
+    const float* start;        // [HO, K, V] or null (zeros)
+    float* out;
+    int32_t backward;
+};
+cudaError_t launch_compose(const ComposeArgs& a, cudaStream_t s);
+
 // The WY pass of the two-pass forward: one record per (chunk, head) item (wymap: the records as
 // [items][136 rows][64] bf16).
 cudaError_t launch_wy_kernel(const ChunkArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,

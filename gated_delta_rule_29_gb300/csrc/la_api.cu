@@ -880,6 +880,25 @@ la_status gdn_summary_bwd(const la_gdn_summary_bwd_params* p, void* stream) {
     return LA_OK;
 }
 
+la_status gdn_compose_spans(const la_gdn_compose_params* p, void* stream) {
+    if (!p || !p->out || p->R < 0 || p->HO < 1) return LA_ERR_INVALID_ARG;
+    if ((p->K != 64 && p->K != 128) || (p->V != 64 && p->V != 128)) return LA_ERR_UNSUPPORTED;
+    if (p->R > 0 && (!p->transitions || !p->terms)) return LA_ERR_INVALID_ARG;
+    if (!aligned(p->out, 4) || !aligned(p->transitions, 4) || !aligned(p->terms, 4) || !aligned(p->start, 4))
+        return LA_ERR_INVALID_ARG;
+    la::ComposeArgs a;
+    a.R = p->R;
+    a.HO = p->HO;
+    a.K = p->K;
+    a.V = p->V;
+    a.transitions = p->transitions;
+    a.terms = p->terms;
+    a.start = p->start;
+    a.out = p->out;
+    a.backward = p->backward != 0;
+    return la::launch_compose(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? LA_OK : LA_ERR_CUDA;
+}
+
 la_status gdn_summary(const la_gdn_summary_params* p, void* stream) {
     if (!p) return LA_ERR_INVALID_ARG;
     Common c{p->T, p->N, p->HK, p->HV, p->K, p->V, p->cu_seqlens, p->cu_seqlens_bits, p->g, p->beta,

@@ -311,6 +311,38 @@ typedef struct la_gdn_summary_params {
  */
 la_status gdn_summary(const la_gdn_summary_params* p, void* stream);
 
+/* ---- composition of span summaries ---------------------------------------------------- */
+typedef struct la_gdn_compose_params {
+    int32_t R;                /* spans, >= 0 */
+    int32_t HO, K, V;         /* heads (>= 1); K, V in {64, 128} */
+    const float* transitions; /* [R, HO, K, K] fp32 contiguous: gdn_summary's transition per span */
+    const float* terms;       /* [R, HO, K, V] fp32 contiguous: forward, each span's end state from a
+                                 zero start; backward, each span's own entering-state gradient */
+    const float* start;       /* [HO, K, V] fp32 contiguous, or NULL for zeros: forward, the state
+                                 entering span 0; backward, the cotangent of the state after span R-1 */
+    float* out;               /* [R + 1, HO, K, V] fp32 contiguous, written */
+    int32_t backward;         /* 0 forward, 1 backward */
+} la_gdn_compose_params;
+
+/*
+ * gdn_compose_spans -- context parallelism over sequence spans: compose span summaries.
+ *
+ * Page: "Summaries" (the end state and the transition of consecutive spans compose as
+ * S_final = S_init * transition + S_H, which is how the summaries give context
+ * parallelism).  In the library's orientation (states [K][V], transition = P^T):
+ *   forward:  out[0] = start; out[r + 1][b][v] = sum_a transitions[r][a][b] out[r][a][v]
+ *             + terms[r][b][v]: the state entering span r + 1, out[R] the final state;
+ *   backward: d = start; for r = R - 1 down to 0: out[r] = d (the cotangent of the state
+ *             leaving span r), d[a][v] <- terms[r][a][v] + sum_b transitions[r][a][b] d[b][v];
+ *             out[R] = d, the gradient of the state entering span 0.
+ * fp32 throughout; each output is a K-term dot product in ascending order (no dependence on
+ * the launch shape).  out must not overlap the inputs.  Asynchronous on `stream`; no
+ * workspace, no synchronisation.  Errors: LA_ERR_INVALID_ARG (null params or out, null
+ * transitions or terms with R > 0, R < 0, HO < 1, pointers not 4-byte aligned),
+ * LA_ERR_UNSUPPORTED (K or V not in {64, 128}), LA_ERR_CUDA (launch failure).
+ */
+la_status gdn_compose_spans(const la_gdn_compose_params* p, void* stream);
+
 /* Parameters of gdn_decode: one new token for each of N sequences.  Strides are in elements. */
 typedef struct la_gdn_decode_params {
     const void* q;    int64_t q_stride_n, q_stride_h;       /* [N, HK, K] bf16 */

@@ -16,6 +16,9 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  The CUDA library never does, and this
 package imports nothing from the library: the two share no code.
 
+``compose_spans`` / ``compose_span_grads`` restate the page's composition of span summaries
+(numpy products, fp64); they serve the context-parallel tests.
+
 Parity pins: every entry point is pinned in ``tests/test_oracle_pins.py``
 (brute-force dense products, closed forms, linearity, span composition,
 hand-derived golden values in ``tests/golden/``; the backward against central
@@ -64,6 +67,9 @@ MUTATIONS = {
     # planted in the negative-argument branches of the two scalar functions below
     21: "sigmoid at x < 0 evaluated as 1 / (1 + e^x), the positive branch's formula",
     22: "softplus at x < 0 evaluated as x + log1p(e^-|x|), dropping the max(x, 0)",
+    # planted in the span composition below
+    23: "span composition applies the transition untransposed",
+    24: "backward span composition adds the span's own gradient after moving through the span",
 }
 
 
@@ -406,6 +412,38 @@ def gdn_summary(k, v, g, beta, cu_seqlens, *, use_qk_l2norm=True, start_state=No
              want_transition=True, unit_mask=unit_mask, nthreads=nthreads,
              mutation=mutation)
     return {"end_state": r["final_state"], "transition": r["transition"]}
+
+
+def compose_spans(transitions, end_states, start, mutation=0):
+    """States entering consecutive spans from their summaries (page, "Summaries": the state after
+    a span is the state before it times the span's transition plus the span's own end state,
+    S_final = S_init * transition + S_H).  With states [.., K, V] and transition = P^T
+    [.., K, K] as gdn_summary returns them: S_{r+1}[b][v] = sum_a transition_r[a][b] S_r[a][v]
+    + end_r[b][v].  Returns [S_0 = start, S_1, ..., S_R] (fp64)."""
+    S = np.asarray(start, dtype=np.float64)
+    out = [S]
+    for tr, sh in zip(transitions, end_states):
+        tr = np.asarray(tr, dtype=np.float64)
+        M = np.swapaxes(tr, -1, -2) if mutation != 23 else tr
+        S = M @ S + np.asarray(sh, dtype=np.float64)
+        out.append(S)
+    return out
+
+
+def compose_span_grads(transitions, local_grads, d_final, mutation=0):
+    """The reverse of compose_spans for a state gradient: leaving span r the cotangent is d_r;
+    through the span it becomes d_enter = transition_r d_r + g_r, g_r the span's own
+    entering-state gradient (the state is linear in the entering state with Jacobian
+    transition^T).  Returns [d leaving span 0, ..., d leaving span R-1, d entering span 0]."""
+    d = np.asarray(d_final, dtype=np.float64)
+    R = len(transitions)
+    leaving = [None] * R
+    for r in range(R - 1, -1, -1):
+        leaving[r] = d
+        tr = np.asarray(transitions[r], dtype=np.float64)
+        loc = np.asarray(local_grads[r], dtype=np.float64)
+        d = loc + tr @ d if mutation != 24 else tr @ (d + loc)
+    return leaving + [d]
 
 
 def _run(q, k, v, g, beta, cu_seqlens, *, scale, use_qk_l2norm, s0, want_final,

@@ -51,7 +51,8 @@ def _c_layout(struct_name, fields):
                                        (B.GdnDecodeParams, "la_gdn_decode_params"),
                                        (B.GdnBwdParams, "la_gdn_bwd_params"),
                                        (B.GdnSummaryBwdParams, "la_gdn_summary_bwd_params"),
-                                       (B.GdnFwdHostParams, "la_gdn_fwd_host_params")])
+                                       (B.GdnFwdHostParams, "la_gdn_fwd_host_params"),
+                                       (B.GdnComposeParams, "la_gdn_compose_params")])
 def test_ctypes_mirror_matches_c_layout(cls, cname):
     names = [f[0] for f in cls._fields_]
     size, offs = _c_layout(cname, names)
@@ -310,6 +311,30 @@ def test_bwd_workspace_bytes_by_checkpoint_kind():
     rows = 65536 // 64 + 8
     assert widen - direct >= rows * 32 * 128 * 128 * 4
     assert lib.la_gdn_bwd_workspace_bytes_ckpt(*args, 100, 0) == 0
+
+
+def _compose(**over):
+    p = B.GdnComposeParams()
+    p.R, p.HO, p.K, p.V = 3, 2, 128, 64
+    p.transitions, p.terms, p.start, p.out = FAKE, FAKE, FAKE, FAKE
+    for k_, v_ in over.items():
+        setattr(p, k_, v_)
+    return p
+
+
+@pytest.mark.parametrize("name,over,code", [
+    ("no out", dict(out=None), B.LA_ERR_INVALID_ARG),
+    ("negative spans", dict(R=-1), B.LA_ERR_INVALID_ARG),
+    ("no heads", dict(HO=0), B.LA_ERR_INVALID_ARG),
+    ("no transitions", dict(transitions=None), B.LA_ERR_INVALID_ARG),
+    ("no terms", dict(terms=None), B.LA_ERR_INVALID_ARG),
+    ("misaligned out", dict(out=FAKE + 2), B.LA_ERR_INVALID_ARG),
+    ("misaligned start", dict(start=FAKE + 1), B.LA_ERR_INVALID_ARG),
+    ("K = 96", dict(K=96), B.LA_ERR_UNSUPPORTED),
+    ("V = 32", dict(V=32), B.LA_ERR_UNSUPPORTED),
+])
+def test_gdn_compose_rejects(name, over, code):
+    assert B.load().gdn_compose_spans(ctypes.byref(_compose(**over)), None) == code, name
 
 
 def test_fwd_pieces_hook_range():

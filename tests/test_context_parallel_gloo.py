@@ -1,6 +1,8 @@
 """Multi-rank path on CPU: span-parallel composition over gloo (world size 2), and the
-benchmark's rank helpers.  The span summaries and forwards come from the fp64 oracle, so
-no GPU is involved; the exchange and the composition are the code under test."""
+benchmark's rank helpers.  The span summaries, forwards and the composition itself come from
+the fp64 oracle (passed to the exchange as its `composer`; the library's composition kernel is
+tested on the GPU), so no GPU is involved; the exchange, the choice of spans each rank composes
+and the broadcasts of the start state and the final cotangent are the code under test."""
 import os
 import socket
 
@@ -26,6 +28,16 @@ def _case():
     return q, k, v, g, beta, s0
 
 
+def _oracle_compose(trs, shs, s0, like=None):
+    return [torch.from_numpy(x) for x in oracle.compose_spans([t.numpy() for t in trs], [s.numpy() for s in shs],
+                                                              s0.numpy())]
+
+
+def _oracle_compose_grads(trs, lgs, dfin):
+    return [torch.from_numpy(x) for x in oracle.compose_span_grads([t.numpy() for t in trs],
+                                                                   [x.numpy() for x in lgs], dfin.numpy())]
+
+
 def _free_port():
     with socket.socket() as s:
         s.bind(("127.0.0.1", 0))
@@ -45,7 +57,7 @@ def _worker(rank, world, port, results):
         tr = torch.from_numpy(summ["transition"][0])
         sh = torch.from_numpy(summ["end_state"][0])
         s_in = cp.entering_state(tr, sh, initial_state=torch.from_numpy(s0[0]) if rank == 0 else
-                                 torch.zeros_like(torch.from_numpy(s0[0])))
+                                 torch.zeros_like(torch.from_numpy(s0[0])), composer=_oracle_compose)
         fw = oracle.gdn_fwd(q[sl], k[sl], v[sl], g[sl], beta[sl], np.array([0, b - a]),
                             initial_state=s_in.numpy()[None], nthreads=1)
         # the benchmark's rank helpers: barrier and max over ranks
@@ -92,9 +104,11 @@ def test_compose_single_process():
         s = oracle.gdn_summary(k[a:b], v[a:b], g[a:b], beta[a:b], np.array([0, b - a]), nthreads=1)
         trs.append(torch.from_numpy(s["transition"][0]))
         shs.append(torch.from_numpy(s["end_state"][0]))
-    states = cp.compose(trs, shs, torch.from_numpy(s0[0]))
-    full = oracle.gdn_fwd(q, k, v, g, beta, np.array([0, L]), initial_state=s0, nthreads=1)
+    states = _oracle_compose(trs, shs, torch.from_numpy(s0[0]))
+    full = oracle.gdn_fwd(q, k, v, g, beta, np.array([0, L]), initial_state=s0, checkpoint_every_n=1, nthreads=1)
     np.testing.assert_allclose(states[-1].numpy(), full["final_state"][0], rtol=1e-10, atol=1e-12)
+    for j, c in enumerate(cuts[:-1]):  # the state entering span j is the unsplit run's state at its cut
+        np.testing.assert_allclose(states[j].numpy(), full["checkpoints"][c], rtol=1e-10, atol=1e-12)
 
 
 def _bwd_worker(rank, world, port, results):
@@ -113,12 +127,14 @@ def _bwd_worker(rank, world, port, results):
         summ = oracle.gdn_summary(k[sl], v[sl], g[sl], beta[sl], cu, nthreads=1)
         tr = torch.from_numpy(summ["transition"][0])
         s_in = cp.entering_state(tr, torch.from_numpy(summ["end_state"][0]),
-                                 initial_state=torch.from_numpy(s0[0]) if rank == 0 else None)
+                                 initial_state=torch.from_numpy(s0[0]) if rank == 0 else None,
+                                 composer=_oracle_compose)
         # the span's own state gradient (the summary's mirror: zero exit cotangent), then the
         # composed exit cotangent
         loc = oracle.gdn_summary_bwd(q[sl], k[sl], g[sl], beta[sl], cu, do[sl])
         d_exit = cp.exit_state_grad(tr, torch.from_numpy(loc[0]),
-                                    d_final=torch.from_numpy(dfin[0]) if rank == world - 1 else None)
+                                    d_final=torch.from_numpy(dfin[0]) if rank == world - 1 else None,
+                                    composer=_oracle_compose_grads)
         full = oracle.gdn_bwd(q[sl], k[sl], v[sl], g[sl], beta[sl], cu, do[sl], initial_state=s_in.numpy()[None],
                               d_final_state=d_exit.numpy()[None], nthreads=1)
         results[rank] = {k_: full[k_] for k_ in ("dq", "dk", "dv", "dg", "dbeta", "d_initial_state")}

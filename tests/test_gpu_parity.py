@@ -13,6 +13,7 @@ import torch
 
 import oracle
 import gated_delta_rule_29_gb300 as la
+from gated_delta_rule_29_gb300 import context_parallel as cp
 from gated_delta_rule_29_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -181,8 +182,9 @@ def test_skewed_gva_sampled_and_batch_invariant():
 
 @pytest.mark.parametrize("slow", [False, True])
 def test_summary_span_composition(slow):
-    """One 131072-token sequence cut into 8 spans: composing the span summaries
-    (S <- transition^T S + S_H) reproduces the unsplit forward's final state."""
+    """One 131072-token sequence cut into 8 spans: composing the span summaries with the
+    library's kernel (S <- transition^T S + S_H, gdn_compose_spans) reproduces the unsplit
+    forward's final state."""
     w = W.config(5, slow_decay=slow)
     d = dev()
     t = to_dev(w, d)
@@ -196,11 +198,9 @@ def test_summary_span_composition(slow):
     assert la.read_status(status) == 0
     _, fin, _ = la.gdn_fwd(t["q"], t["k"], t["v"], t["g"], t["beta"], t["cu"], use_qk_l2norm=True,
                            initial_state=S_init.to(d))
+    S = cp.compose(list(tr), list(end), S_init[0].to(d))[-1].double().cpu().numpy()
     end = end.double().cpu().numpy()
     tr = tr.double().cpu().numpy()
-    S = S_init.double().numpy()[0]
-    for j in range(end.shape[0]):
-        S = np.einsum("hab,hav->hbv", tr[j], S) + end[j]
     fin = fin.double().cpu().numpy()[0]
     errs = {"composed_vs_unsplit": rel(S, fin)}
     assert errs["composed_vs_unsplit"] <= S_TOL
@@ -213,9 +213,7 @@ def test_summary_span_composition(slow):
     errs["end_state"] = rel(end[:, heads], ref["end_state"][:, heads])
     if slow:
         errs["transition"] = rel(tr[:, heads], ref["transition"][:, heads])
-    refS = S_init.double().numpy()[0].copy()
-    for j in range(8):
-        refS = np.einsum("hab,hav->hbv", ref["transition"][j], refS) + ref["end_state"][j]
+    refS = oracle.compose_spans(ref["transition"], ref["end_state"], S_init.double().numpy()[0])[-1]
     errs["composed_vs_oracle"] = rel(S[heads], refS[heads])
     umask = np.zeros((1, w.HV), dtype=bool)
     umask[0, heads] = True

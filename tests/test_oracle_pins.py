@@ -232,10 +232,9 @@ def check_span_composition(mutation=0):
     full = oracle.gdn_fwd(q, k, v, g, beta, whole_cu, initial_state=S_init, mutation=mutation)
     s = oracle.gdn_summary(k, v, g, beta, span_cu, mutation=mutation)
     sw = oracle.gdn_summary(k, v, g, beta, whole_cu, mutation=mutation)
-    S = S_init[0].copy()
+    S = oracle.compose_spans(s["transition"], s["end_state"], S_init[0], mutation=mutation)[-1]
     tr_prod = np.stack([np.eye(4)] * 2)
     for j in range(len(lengths)):
-        S = np.einsum("hab,hav->hbv", s["transition"][j], S) + s["end_state"][j]
         tr_prod = np.einsum("hab,hbc->hac", tr_prod, s["transition"][j])
     err = max(_rel(S, full["final_state"][0]), _rel(tr_prod, sw["transition"][0]))
     # summary from a non-zero start equals transition applied to the start plus S_H
@@ -572,9 +571,7 @@ def check_summary_bwd(mutation=0):
     full = oracle.gdn_summary_bwd(qs, ks, gs, bs, whole, ds, scale=0.7, d_final_state=dF, mutation=mutation)
     loc = oracle.gdn_summary_bwd(qs, ks, gs, bs, spans, ds, scale=0.7, mutation=mutation)
     trs = oracle.gdn_summary(ks, v[:L], gs, bs, spans)["transition"]
-    d = dF[0]
-    for r in range(2, -1, -1):
-        d = loc[r] + np.einsum("hab,hbv->hav", trs[r], d)
+    d = oracle.compose_span_grads(trs, loc, dF[0], mutation=mutation)[-1]
     return max(worst, _rel(d, full[0]))
 
 
