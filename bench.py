@@ -775,7 +775,7 @@ def run_summary_bench(args, world, rank, local):
     S = spans.numel() - 1
     end = torch.empty(S, HV, K, V, dtype=torch.float32, device=dev)
     tr = torch.empty(S, HV, K, K, dtype=torch.float32, device=dev)
-    ws = torch.empty(la.workspace_bytes(S, True), dtype=torch.uint8, device=dev)
+    ws = torch.empty(la.api.split_workspace_bytes(T, S, HV), dtype=torch.uint8, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def step():
@@ -840,7 +840,8 @@ def run_summary_bench(args, world, rank, local):
                          if flops / (tc_peak * 1e12) > alg / (hbm_peak * 1e9) else
                          {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                           "frac": achieved / hbm_peak, "tensor_tflops": tflops, "tensor_frac": tflops / tc_peak})
-                        | {"traffic": None, "peak_source": peak_src, "kernel": "gdn_chunk_kernel<128, summary>",
+                        | {"traffic": None, "peak_source": peak_src, "kernel": ("gdn_chunk_kernel<128, summary> (fused)" if args.fwd_passes == "fused" else
+                                              "gdn_wy_kernel<128, summary> + gdn_chunk_kernel<128, summary state pass>"),
                            "kernel_ms": kern_ms, "algorithmic_bytes": alg, "algorithmic_flops": flops},
             "cpu_baseline": cpu,
             "e2e": None,
@@ -957,7 +958,7 @@ def run_table(args, world, rank, local):
     S = spans.numel() - 1
     end = torch.empty(S, HV, K, V, dtype=torch.float32, device=dev)
     tr = torch.empty(S, HV, K, K, dtype=torch.float32, device=dev)
-    ws = torch.empty(la.workspace_bytes(S, True), dtype=torch.uint8, device=dev)
+    ws = torch.empty(la.api.split_workspace_bytes(T, S, HV), dtype=torch.uint8, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     call_ms, kern_ms = timed(lambda: la.gdn_summary(k, v, g, b, spans, end_state=end, transition=tr, workspace=ws,
                                                     status=status))

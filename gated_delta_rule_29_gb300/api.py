@@ -222,7 +222,7 @@ def gdn_summary(k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.T
     if transition is None:
         transition = torch.empty(N, HO, K, K, dtype=torch.float32, device=dev)
     if workspace is None:
-        workspace = torch.empty(workspace_bytes(N, True), dtype=torch.uint8, device=dev)
+        workspace = torch.empty(split_workspace_bytes(k.shape[0], N, v.shape[1]), dtype=torch.uint8, device=dev)
     if start_state is not None:
         start_state = start_state.contiguous()
     p = B.GdnSummaryParams()

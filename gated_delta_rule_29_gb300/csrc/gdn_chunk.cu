@@ -57,15 +57,24 @@ constexpr int kCta = 128;  // threads per CTA
 constexpr int kSumPieces = 4;  // chunk ranges per summary unit when the units outnumber one wave
 
 // ------------------------------------------------------------------ shared memory map
-constexpr uint32_t SM_KQ = 0;        // [region 0..1][128 rows: K 0-63, Q 64-127][128 B]
-constexpr uint32_t SM_V = 32768;     // V tile [region 0..1][64 rows][128 B] | later T fp32 [64][64]
-constexpr uint32_t SM_WB = 49152;    // S^T bf16 [2][128][128 B] | X^T hi,lo | Ddec^T hi,lo
-constexpr uint32_t SM_M = 81920;     // A fp32 [64][64] | T bf16 [64][128 B] | D^T bf16 [128][128 B]
-constexpr uint32_t SM_PB = 98304;    // P bf16 [64][128 B]
-constexpr uint32_t SM_SC = 106496;   // Scalars (7 KB)
-constexpr uint32_t SM_SLO = 114688;  // summary only: S^T bf16 residual (lo part), same layout as WB
-__host__ __device__ constexpr uint32_t smem_alloc(int mode) {
-    return (mode == kModeSummary ? SM_SLO + 32768 : SM_SC + 7168) + 1024;
+// Byte offsets from the 1024-aligned base, per mode:
+//   kq   [region 0..1][128 rows: K 0-63, Q 64-127][128 B], regions kq_region bytes apart
+//   v    V tile [region 0..1][64 rows][128 B] | later T fp32 [64][64]
+//   wb   S^T bf16 [2][128][128 B] | X^T hi,lo | Ddec^T hi,lo
+//   m    A fp32 [64][64] | T bf16 [64][128 B] | D^T bf16 [128][128 B]
+//   pb   P bf16 [64][128 B]
+//   sc   Scalars (7 KB; without the solve's scratch in the summary's state pass)
+//   slo  summary only: S^T bf16 residual (lo part), same layout as wb
+// The summary's state pass loads only K (two 8 KB regions), keeps only T (bf16) in m and has no
+// P: 109 KB, so two CTAs share an SM.
+struct SmemMap {
+    uint32_t kq, kq_region, v, wb, m, pb, sc, slo, total;
+};
+__host__ __device__ constexpr SmemMap smem_map(int mode) {
+    return mode == kModeSummarySplit
+               ? SmemMap{0u, 8192u, 16384u, 32768u, 65536u, 0u, 73728u, 77824u, 77824u + 32768u + 1024u}
+               : SmemMap{0u, 16384u, 32768u, 49152u, 81920u, 98304u, 106496u, 114688u,
+                         (mode == kModeSummary ? 114688u + 32768u : 106496u + 7168u) + 1024u};
 }
 
 // TMEM columns (fp32, 128 lanes)
@@ -99,6 +108,8 @@ struct __align__(16) Scalars {
 };
 static_assert(sizeof(Scalars) <= 7168, "scalar area");
 constexpr uint32_t kScalarsNoY = static_cast<uint32_t>(sizeof(Scalars) - sizeof(float[4][256]));
+static_assert(smem_map(kModeSummarySplit).sc + kScalarsNoY <= smem_map(kModeSummarySplit).slo,
+              "the summary state pass's scalars overlap its residual buffer");
 
 // fp32 64 x 64 tiles (A, T): 16-byte chunks XOR-swizzled by row to spread rows over the banks.
 __device__ __forceinline__ int midx(int r, int c) { return r * 64 + ((((c >> 2) ^ (r & 15)) << 2) | (c & 3)); }
@@ -455,14 +466,15 @@ __device__ __forceinline__ void t_to_bf16(const float* Tf, uint8_t* TB, int tid)
     }
 }
 
-// One WY record into shared memory, on bar_f: T (bf16, into TB's place), P (into PB) and the
-// factors beta, sx, sq, sd (into sc.bet .. sc.sd, contiguous).  One thread.
+// One WY record into shared memory, on bar_f: T (bf16, into TB's place), P (into PB; the
+// summary has none: PBdst null) and the factors beta, sx, sq, sd (into sc.bet .. sc.sd,
+// contiguous).  One thread.
 __device__ __forceinline__ void load_wy(const ChunkArgs& a, const CUtensorMap& wymap, int64_t chunk, int h,
                                         void* TBdst, void* PBdst, Scalars& sc) {
     const int64_t item = chunk * a.HV + h;
-    mbar_arrive_expect_tx(&sc.bar_f, static_cast<uint32_t>(kWyRecordBytes));
+    mbar_arrive_expect_tx(&sc.bar_f, static_cast<uint32_t>(PBdst ? kWyRecordBytes : kWyRecordBytes - kWyTileBytes));
     tma_load_3d(TBdst, &wymap, &sc.bar_f, 0, static_cast<int>(item), 0);
-    tma_load_3d(PBdst, &wymap, &sc.bar_f, 0, static_cast<int>(item), 64);
+    if (PBdst) tma_load_3d(PBdst, &wymap, &sc.bar_f, 0, static_cast<int>(item), 64);
     bulk_load(sc.bet, a.wy + item * static_cast<int64_t>(kWyRecordBytes) + 2 * kWyTileBytes,
               static_cast<uint32_t>(kWyFactorBytes), &sc.bar_f);
 }
@@ -472,15 +484,17 @@ __global__ void __launch_bounds__(kCta, 2)
     gdn_chunk_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
                      const __grid_constant__ CUtensorMap wymap, const ChunkArgs a) {
-    constexpr bool kFwd = MODE != kModeSummary;  // queries and outputs (the forward, or GDP's)
+    constexpr bool kSum = MODE == kModeSummary || MODE == kModeSummarySplit;
+    constexpr bool kFwd = !kSum;  // queries and outputs (the forward, or GDP's)
     constexpr bool kGdp = MODE == kModeGdp;
-    constexpr bool kSum = MODE == kModeSummary;
-    // the state pass of the two-pass forward: T, P and the factors of every chunk come from the
-    // WY pass's records instead of being formed here
-    constexpr bool kSplit = MODE == kModeFwdSplit;
-    // waits sleep in hardware when another CTA shares the SM (the forward runs two per SM; the
-    // summary, with its larger shared-memory footprint, one)
-    constexpr bool kSleep = !kSum;
+    // the state pass of the two-pass forward or summary: T (P) and the factors of every chunk come
+    // from the WY pass's records instead of being formed here
+    constexpr bool kSplit = MODE == kModeFwdSplit || MODE == kModeSummarySplit;
+    constexpr SmemMap L = smem_map(MODE);
+    constexpr uint32_t RQ = L.kq_region;
+    // waits sleep in hardware when another CTA shares the SM (the forward and the summary's state
+    // pass run two per SM; the fused summary, with its larger shared-memory footprint, one)
+    constexpr bool kSleep = !kSum || kSplit;
     constexpr int KP = KD / 16;  // 16-column pieces of the state
     // GDP: the tokens whose last update row falls in a chunk of 64 update rows (at most QR of
     // them) have their queries in rows 0 .. QR-1 of the query half of the K/Q tile (the other
@@ -490,17 +504,17 @@ __global__ void __launch_bounds__(kCta, 2)
     const int QR = (kChunk + NH - 1) / NH;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    Scalars& sc = *reinterpret_cast<Scalars*>(sm + SM_SC);
-    uint8_t* KQ = sm + SM_KQ;
-    uint8_t* VT = sm + SM_V;
-    uint8_t* WB = sm + SM_WB;
-    float* M = reinterpret_cast<float*>(sm + SM_M);   // A (fp32) -> T bf16 (TB) -> D^T bf16 (DT)
-    uint8_t* TB = sm + SM_M;
-    uint8_t* DT = sm + SM_M;
-    float* Tf = reinterpret_cast<float*>(sm + SM_V);  // T fp32, in the V tile's space after X
-    uint8_t* PB = sm + SM_PB;
-    uint8_t* SLO = kFwd ? nullptr : sm + SM_SLO;
-    uint8_t* OST = sm + SM_M;  // O staging for the bulk store, once the O product has read D^T
+    Scalars& sc = *reinterpret_cast<Scalars*>(sm + L.sc);  // (no solve scratch in the summary's state pass)
+    uint8_t* KQ = sm + L.kq;
+    uint8_t* VT = sm + L.v;
+    uint8_t* WB = sm + L.wb;
+    float* M = reinterpret_cast<float*>(sm + L.m);   // A (fp32) -> T bf16 (TB) -> D^T bf16 (DT)
+    uint8_t* TB = sm + L.m;
+    uint8_t* DT = sm + L.m;
+    float* Tf = reinterpret_cast<float*>(sm + L.v);  // T fp32, in the V tile's space after X
+    uint8_t* PB = kFwd ? sm + L.pb : nullptr;
+    uint8_t* SLO = kFwd ? nullptr : sm + L.slo;
+    uint8_t* OST = sm + L.m;  // O staging for the bulk store, once the O product has read D^T
 
     const int tid = threadIdx.x;
     const int r = tid;  // TMEM lane, value column, stacked token row
@@ -539,17 +553,38 @@ __global__ void __launch_bounds__(kCta, 2)
     // shared-memory matrix descriptors of the operand buffers; an operand at byte offset off
     // from a buffer uses base + (off >> 4) (the start-address field counts 16-byte units)
     const uint64_t d_kq = sdesc_sw128(smem_u32(KQ), 16, 1024);
-    const uint64_t d_kq_mn = sdesc_sw128(smem_u32(KQ), 16384, 1024);  // K read MN-major
+    const uint64_t d_kq_mn = sdesc_sw128(smem_u32(KQ), RQ, 1024);  // K read MN-major
     const uint64_t d_wb = sdesc_sw128(smem_u32(WB), 16, 1024);
-    const uint64_t d_m = sdesc_sw128(smem_u32(sm + SM_M), 16, 1024);   // T bf16, then D^T bf16
-    const uint64_t d_pb = sdesc_sw128(smem_u32(PB), 16, 1024);
+    const uint64_t d_m = sdesc_sw128(smem_u32(sm + L.m), 16, 1024);   // T bf16, then D^T bf16
+    const uint64_t d_pb = kFwd ? sdesc_sw128(smem_u32(PB), 16, 1024) : 0;
     const uint64_t d_slo = kFwd ? 0 : sdesc_sw128(smem_u32(SLO), 16, 1024);
+    // (K S)^T and, in the forward, (Q S)^T = S^T [K; Q]^T, one M = 128 product per 16 keys (the
+    // summary adds the product with the state's lo part); one thread
+    auto issue_state_products = [&]() {
+        tc_fence_after();
+        const uint32_t idesc = idesc_bf16_f32(128, kFwd ? 128 : 64, false, false);
+#pragma unroll
+        for (int kk = 0; kk < KD / 16; ++kk) {
+            const uint64_t ow = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+            const uint64_t oq = ((kk >> 2) * RQ + (kk & 3) * 32) >> 4;
+            umma_bf16(tmem + COL_R1, d_wb + ow, d_kq + oq, idesc, kk > 0);
+        }
+        if (!kFwd) {
+#pragma unroll
+            for (int kk = 0; kk < KD / 16; ++kk) {
+                const uint64_t ow = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                const uint64_t oq = ((kk >> 2) * RQ + (kk & 3) * 32) >> 4;
+                umma_bf16(tmem + COL_R1, d_slo + ow, d_kq + oq, idesc, 1u);
+            }
+        }
+        umma_commit(&sc.bar_mma);
+    };
 
     if constexpr (kGdp) {
         // the query rows past a chunk's QR tokens are never written by the tile loads: zero them once
         for (int e = tid; e < (KD / 64) * (64 - QR) * 8; e += kCta) {
             const int rg = e / ((64 - QR) * 8), rem = e % ((64 - QR) * 8);
-            *reinterpret_cast<uint4*>(KQ + rg * 16384 + 8192 + (QR + rem / 8) * 128 + (rem % 8) * 16) =
+            *reinterpret_cast<uint4*>(KQ + rg * RQ + 8192 + (QR + rem / 8) * 128 + (rem % 8) * 16) =
                 make_uint4(0u, 0u, 0u, 0u);
         }
         fence_proxy_async_smem();
@@ -707,9 +742,9 @@ __global__ void __launch_bounds__(kCta, 2)
                 mbar_arrive_expect_tx(&sc.bar_kq, kq_bytes);
 #pragma unroll
                 for (int rg = 0; rg < KD / 64; ++rg) {
-                    tma_load_3d(KQ + rg * 16384, &kmap, &sc.bar_kq, rg * 64, hk, static_cast<int>(tf));
+                    tma_load_3d(KQ + rg * RQ, &kmap, &sc.bar_kq, rg * 64, hk, static_cast<int>(tf));
                     if (kFwd)
-                        tma_load_3d(KQ + rg * 16384 + 8192, &qmap, &sc.bar_kq, rg * 64, hk, static_cast<int>(tf / NH));
+                        tma_load_3d(KQ + rg * RQ + 8192, &qmap, &sc.bar_kq, rg * 64, hk, static_cast<int>(tf / NH));
                 }
             }
             if (tid == 0) {
@@ -759,7 +794,7 @@ __global__ void __launch_bounds__(kCta, 2)
                 const uint32_t idesc = idesc_bf16_f32(128, kFwd ? 128 : 64, false, false);
 #pragma unroll
                 for (int kk = 0; kk < KD / 16; ++kk) {
-                    const uint64_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
+                    const uint64_t off = ((kk >> 2) * RQ + (kk & 3) * 32) >> 4;
                     umma_bf16(tmem + COL_R1, d_kq + off, d_kq + off, idesc, kk > 0);
                 }
                 umma_commit(&sc.bar_mma);
@@ -774,16 +809,7 @@ __global__ void __launch_bounds__(kCta, 2)
                     tc_fence_before();
                     if (__syncthreads_or(!ok)) { failed = true; break; }
                 }
-                if (tid == 0 && ok) {
-                    tc_fence_after();
-                    const uint32_t idesc = idesc_bf16_f32(128, 128, false, false);
-#pragma unroll
-                    for (int kk = 0; kk < KD / 16; ++kk) {
-                        const uint64_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                        umma_bf16(tmem + COL_R1, d_wb + off, d_kq + off, idesc, kk > 0);
-                    }
-                    umma_commit(&sc.bar_mma);
-                }
+                if (tid == 0 && ok) issue_state_products();
                 pend_mma = true;
             } else {
                 pend_mma = ok;
@@ -810,23 +836,7 @@ __global__ void __launch_bounds__(kCta, 2)
                 if (__syncthreads_or(!ok)) { failed = true; break; }
                 // ---- S3: (K S)^T and (Q S)^T = S^T [K; Q]^T, issued as soon as every thread holds its row of
                 // G (the product reuses G's columns); it runs while the scalars and A / P are formed
-                if (tid == 0) {
-                    tc_fence_after();
-                    const uint32_t idesc = idesc_bf16_f32(128, kFwd ? 128 : 64, false, false);
-#pragma unroll
-                    for (int kk = 0; kk < KD / 16; ++kk) {
-                        const uint64_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                        umma_bf16(tmem + COL_R1, d_wb + off, d_kq + off, idesc, kk > 0);
-                    }
-                    if (!kFwd) {
-#pragma unroll
-                        for (int kk = 0; kk < KD / 16; ++kk) {
-                            const uint64_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
-                            umma_bf16(tmem + COL_R1, d_slo + off, d_kq + off, idesc, 1u);
-                        }
-                    }
-                    umma_commit(&sc.bar_mma);
-                }
+                if (tid == 0) issue_state_products();
                 pend_mma = true;
 
                 fast = chunk_scalars<kFwd, kGdp>(sc, tid, n, nq, tq0, rel0, NH, b_cur, a.scale);
@@ -1048,8 +1058,8 @@ __global__ void __launch_bounds__(kCta, 2)
                 mbar_arrive_expect_tx(&sc.bar_kq, kq_bytes);
 #pragma unroll
                 for (int rg = 0; rg < KD / 64; ++rg) {
-                    tma_load_3d(KQ + rg * 16384, &kmap, &sc.bar_kq, rg * 64, hk, t1);
-                    if (kFwd) tma_load_3d(KQ + rg * 16384 + 8192, &qmap, &sc.bar_kq, rg * 64, hk, t1 / NH);
+                    tma_load_3d(KQ + rg * RQ, &kmap, &sc.bar_kq, rg * 64, hk, t1);
+                    if (kFwd) tma_load_3d(KQ + rg * RQ + 8192, &qmap, &sc.bar_kq, rg * 64, hk, t1 / NH);
                 }
             }
             if (!last) pend_kq = true;
@@ -1175,7 +1185,9 @@ constexpr uint32_t WY_SC = 49152;   // Scalars without the solve scratch
 constexpr uint32_t WY_SMEM = WY_SC + ((kScalarsNoY + 127) & ~127u) + 1024;
 constexpr uint32_t WY_TMEM_COLS = 128;
 
-template <int KD>
+// kQ: the forward's records (queries: P and the query factors); else the summary's (T and the
+// key factors only, G over the keys alone as the fused summary forms it).
+template <int KD, bool kQ>
 __global__ void __launch_bounds__(kCta, 4)
     gdn_wy_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap wymap, const ChunkArgs a) {
@@ -1213,7 +1225,7 @@ __global__ void __launch_bounds__(kCta, 4)
     const uint32_t tmem = sc.tmem_base;
     const uint32_t trow = tmem + (static_cast<uint32_t>(r & ~31) << 16);
     const uint64_t d_kq = sdesc_sw128(smem_u32(KQ), 16, 1024);
-    const uint32_t kq_bytes = KD * 128u * 2u;
+    const uint32_t kq_bytes = KD * 128u * (kQ ? 2u : 1u);
     const uint64_t budget = a.wait_budget_ns;
     uint32_t ph_kq = 0, ph_mma = 0;
     bool pend_kq = false, pend_mma = false, failed = false;
@@ -1259,7 +1271,7 @@ __global__ void __launch_bounds__(kCta, 4)
 #pragma unroll
             for (int rg = 0; rg < KD / 64; ++rg) {
                 tma_load_3d(KQ + rg * 16384, &kmap, &sc.bar_kq, rg * 64, hk, static_cast<int>(t0));
-                tma_load_3d(KQ + rg * 16384 + 8192, &qmap, &sc.bar_kq, rg * 64, hk, static_cast<int>(t0));
+                if (kQ) tma_load_3d(KQ + rg * 16384 + 8192, &qmap, &sc.bar_kq, rg * 64, hk, static_cast<int>(t0));
             }
         }
         pend_kq = !a.test_skip_tile_load;
@@ -1275,7 +1287,7 @@ __global__ void __launch_bounds__(kCta, 4)
         }
         if (tid == 0 && ok) {
             tc_fence_after();
-            const uint32_t idesc = idesc_bf16_f32(128, 128, false, false);
+            const uint32_t idesc = idesc_bf16_f32(128, kQ ? 128 : 64, false, false);
 #pragma unroll
             for (int kk = 0; kk < KD / 16; ++kk) {
                 const uint64_t off = ((kk >> 2) * 16384 + (kk & 3) * 32) >> 4;
@@ -1303,11 +1315,11 @@ __global__ void __launch_bounds__(kCta, 4)
         }
         tc_fence_after();
         float g64[64];
-        g_rows_and_norms<true>(trow, 0, r, n, n, a.l2norm, g64, sc);
+        g_rows_and_norms<kQ>(trow, 0, r, n, n, a.l2norm, g64, sc);
         tc_fence_before();
         if (__syncthreads_or(!ok)) { failed = true; break; }
-        const bool fast = chunk_scalars<true, false>(sc, tid, n, n, 0, 0, 1, b_cur, a.scale);
-        build_a_p<true, false>(g64, sc, M, PB, fast, r, n, 0, 0, 1, a.scale);
+        const bool fast = chunk_scalars<kQ, false>(sc, tid, n, n, 0, 0, 1, b_cur, a.scale);
+        build_a_p<kQ, false>(g64, sc, M, PB, fast, r, n, 0, 0, 1, a.scale);
         // the next item's rows, gates and betas (in flight during the solve)
         int64_t nt0 = t0;
         int nn = 0;
@@ -1323,7 +1335,7 @@ __global__ void __launch_bounds__(kCta, 4)
         __syncthreads();
         if (tid == 0) {
             tma_store_3d(&wymap, TB, 0, static_cast<int>(item), 0);
-            tma_store_3d(&wymap, PB, 0, static_cast<int>(item), 64);
+            if (kQ) tma_store_3d(&wymap, PB, 0, static_cast<int>(item), 64);
             bulk_store(a.wy + item * static_cast<int64_t>(kWyRecordBytes) + 2 * kWyTileBytes, sc.bet,
                        static_cast<uint32_t>(kWyFactorBytes));
             bulk_commit_group();
@@ -1400,7 +1412,7 @@ template <int KD, int MODE>
 static cudaError_t launch_one(const ChunkArgs& a, const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm,
                               const CUtensorMap& om, const CUtensorMap& wm, int device, cudaStream_t s) {
     auto* fn = gdn_chunk_kernel<KD, MODE>;
-    constexpr uint32_t smem = smem_alloc(MODE);
+    constexpr uint32_t smem = smem_map(MODE).total;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     // Ask for the largest shared-memory carveout so two CTAs fit per SM.
@@ -1416,7 +1428,7 @@ static cudaError_t launch_one(const ChunkArgs& a, const CUtensorMap& qm, const C
     b.pieces = 1;
     b.item_base = 0;
     b.items = 0;
-    if (MODE == kModeSummary && b.num_units > slots) b.pieces = kSumPieces;
+    if ((MODE == kModeSummary || MODE == kModeSummarySplit) && b.num_units > slots) b.pieces = kSumPieces;
     if ((MODE == kModeFwd || MODE == kModeFwdSplit) && b.final_state && !b.final_bf16 && b.num_units > slots) {
         if (a.pieces_request > 0) b.pieces = a.pieces_request;
         else if (b.num_units <= 4 * slots)
@@ -1452,6 +1464,7 @@ cudaError_t launch_chunk_kernel(const ChunkArgs& a, const CUtensorMap& qm, const
             case kModeGdp: return launch_one<128, kModeGdp>(a, qm, km, vm, om, wm, dev, s);
             case kModeFwdSplit: return launch_one<128, kModeFwdSplit>(a, qm, km, vm, om, wm, dev, s);
             case kModeSummary: return launch_one<128, kModeSummary>(a, qm, km, vm, om, wm, dev, s);
+            case kModeSummarySplit: return launch_one<128, kModeSummarySplit>(a, qm, km, vm, om, wm, dev, s);
             default: return launch_one<128, kModeFwd>(a, qm, km, vm, om, wm, dev, s);
         }
     }
@@ -1459,14 +1472,15 @@ cudaError_t launch_chunk_kernel(const ChunkArgs& a, const CUtensorMap& qm, const
         case kModeGdp: return launch_one<64, kModeGdp>(a, qm, km, vm, om, wm, dev, s);
         case kModeFwdSplit: return launch_one<64, kModeFwdSplit>(a, qm, km, vm, om, wm, dev, s);
         case kModeSummary: return launch_one<64, kModeSummary>(a, qm, km, vm, om, wm, dev, s);
+        case kModeSummarySplit: return launch_one<64, kModeSummarySplit>(a, qm, km, vm, om, wm, dev, s);
         default: return launch_one<64, kModeFwd>(a, qm, km, vm, om, wm, dev, s);
     }
 }
 
-template <int KD>
+template <int KD, bool kQ>
 static cudaError_t launch_wy(const ChunkArgs& a, const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& wm,
                              int device, cudaStream_t s) {
-    auto* fn = gdn_wy_kernel<KD>;
+    auto* fn = gdn_wy_kernel<KD, kQ>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, WY_SMEM);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
@@ -1488,11 +1502,12 @@ static cudaError_t launch_wy(const ChunkArgs& a, const CUtensorMap& qm, const CU
 }
 
 cudaError_t launch_wy_kernel(const ChunkArgs& a, const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& wm,
-                             cudaStream_t s) {
+                             bool summary, cudaStream_t s) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    return a.K == 128 ? launch_wy<128>(a, qm, km, wm, dev, s) : launch_wy<64>(a, qm, km, wm, dev, s);
+    if (summary) return a.K == 128 ? launch_wy<128, false>(a, qm, km, wm, dev, s) : launch_wy<64, false>(a, qm, km, wm, dev, s);
+    return a.K == 128 ? launch_wy<128, true>(a, qm, km, wm, dev, s) : launch_wy<64, true>(a, qm, km, wm, dev, s);
 }
 
 }  // namespace la

@@ -12,9 +12,10 @@ constexpr int kThreads = 256;       // threads of the fused chunk kernel
 constexpr int kPrologueThreads = 1024;
 
 // kModeGdp: the forward of Gated DeltaProduct (n delta updates per token) on the update timeline,
-// with q, g and o on the token timeline.  kModeFwdSplit: the forward's state pass, reading each
-// chunk's T, P and per-token factors from the records the WY pass (gdn_wy_kernel) wrote.
-enum Mode : int { kModeFwd = 0, kModeSummary = 1, kModeGdp = 2, kModeFwdSplit = 3 };
+// with q, g and o on the token timeline.  kModeFwdSplit / kModeSummarySplit: the forward's or
+// the summary's state pass, reading each chunk's T (and P) and per-token factors from the
+// records the WY pass (gdn_wy_kernel) wrote.
+enum Mode : int { kModeFwd = 0, kModeSummary = 1, kModeGdp = 2, kModeFwdSplit = 3, kModeSummarySplit = 4 };
 enum TileKind : int { kTileValue = 0, kTileTransition = 1 };
 
 // Workspace layout (bytes from the 256-aligned workspace base).
@@ -289,10 +290,10 @@ struct ComposeArgs {
 };
 cudaError_t launch_compose(const ComposeArgs& a, cudaStream_t s);
 
-// The WY pass of the two-pass forward: one record per (chunk, head) item (wymap: the records as
-// [items][136 rows][64] bf16).
+// The WY pass of the two-pass forward or summary: one record per (chunk, head) item (wymap: the
+// records as [items][136 rows][64] bf16); summary: the records without P.
 cudaError_t launch_wy_kernel(const ChunkArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
-                             const CUtensorMap& wymap, cudaStream_t s);
+                             const CUtensorMap& wymap, bool summary, cudaStream_t s);
 cudaError_t launch_chunk_kernel(const ChunkArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
                                 const CUtensorMap& vmap, const CUtensorMap& omap, const CUtensorMap& wymap, int mode,
                                 cudaStream_t s);

@@ -193,12 +193,13 @@ la_status run(const Common& c, ChunkArgs& ka, const void* q, int64_t q_st, int64
               int64_t k_sh, const void* v, int64_t v_st, int64_t v_sh, int64_t ckpt_n, void* workspace,
               size_t workspace_bytes, int32_t* user_status, int mode, cudaStream_t stream, int32_t gdp_n = 1) {
     void* ws = nullptr;
-    // The forward runs as two passes (the WY pass over every (chunk, head), then the state pass)
-    // when the workspace has room for the WY records; otherwise as the fused kernel.  Both give
-    // the same bits.
+    // The forward and the summary run as two passes (the WY pass over every (chunk, head), then
+    // the state pass) when the workspace has room for the WY records; otherwise as the fused
+    // kernel.  Both give the same bits.
     const int32_t passes = g_test_fwd_passes.load(std::memory_order_relaxed);
     const la::SplitLayout SL = la::split_layout(c.T, c.N, c.HV);
-    bool split = mode == la::kModeFwd && c.T > 0 && passes != 1 && SL.items < (int64_t(1) << 31);
+    bool split = (mode == la::kModeFwd || mode == la::kModeSummary) && c.T > 0 && passes != 1 &&
+                 SL.items < (int64_t(1) << 31);
     la_status st = LA_OK;
     if (split) {
         if (workspace) {
@@ -289,10 +290,10 @@ la_status run(const Common& c, ChunkArgs& ka, const void* q, int64_t q_st, int64
     if (split) {
         ChunkArgs kw = ka;
         kw.num_units = SL.items;  // the bound on (chunk, head) items
-        if (la::launch_wy_kernel(kw, qm, km, wm, stream) != cudaSuccess) return LA_ERR_CUDA;
+        if (la::launch_wy_kernel(kw, qm, km, wm, mode == la::kModeSummary, stream) != cudaSuccess) return LA_ERR_CUDA;
     }
-    if (la::launch_chunk_kernel(ka, qm, km, vm, om, wm, split ? la::kModeFwdSplit : mode, stream) != cudaSuccess)
-        return LA_ERR_CUDA;
+    const int kmode = !split ? mode : (mode == la::kModeSummary ? la::kModeSummarySplit : la::kModeFwdSplit);
+    if (la::launch_chunk_kernel(ka, qm, km, vm, om, wm, kmode, stream) != cudaSuccess) return LA_ERR_CUDA;
     if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess) return LA_ERR_CUDA;
     return LA_OK;
 }

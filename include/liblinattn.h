@@ -303,6 +303,11 @@ typedef struct la_gdn_summary_params {
  * which is the page's S_init * transition with states read V-major, and the
  * orientation a backward applies (dS_0 = P^T dS_L).  An empty span returns the
  * identity and its start state.
+ * Two passes as in gdn_fwd ("Two passes"), when the workspace has room for them
+ * (la_gdn_fwd_split_workspace_bytes; with workspace = NULL the internal buffer
+ * grows to that size): the WY pass forms each (chunk, head)'s T once for both
+ * tiles, and the state pass, which then needs less shared memory, runs two
+ * units per SM; the same bits as the fused kernel.
  * When the (span, head, tile) units outnumber the CTAs the GPU holds at once,
  * the call enqueues several launches that walk each span in four chunk ranges
  * and keep the state between ranges in end_state and transition themselves
@@ -519,10 +524,10 @@ size_t la_gdp_workspace_bytes(int64_t T, int32_t N, int32_t HK, int32_t HV, int3
 /* Bytes of device workspace gdn_fwd (summary = 0) or gdn_summary (summary = 1) needs. */
 size_t la_gdn_workspace_bytes(int32_t N, int32_t summary);
 
-/* Bytes of device workspace with which gdn_fwd (num_householder <= 1) may run as two passes
-   (see gdn_fwd, "Two passes"): la_gdn_workspace_bytes(N, 0) plus per-chunk tables and one
-   17408-byte record per (chunk, head), at most (T / 64 + N) * HV of them (0.57 GB for
-   T = 65536, N = 8, HV = 32). */
+/* Bytes of device workspace with which gdn_fwd (num_householder <= 1) or gdn_summary may run
+   as two passes (see gdn_fwd, "Two passes"; N counts the spans for gdn_summary):
+   la_gdn_workspace_bytes(N, 0) plus per-chunk tables and one 17408-byte record per
+   (chunk, head), at most (T / 64 + N) * HV of them (0.57 GB for T = 65536, N = 8, HV = 32). */
 size_t la_gdn_fwd_split_workspace_bytes(int64_t T, int32_t N, int32_t HV);
 
 /*
@@ -576,8 +581,9 @@ la_status la_test_set_fwd_pieces(int32_t pieces);
 /*
  * Scheduling test hook, not for production use (no counterpart on the pages).
  * passes = 0 restores the automatic choice between the fused and the two-pass
- * forward (see gdn_fwd, "Two passes"); 1 makes every later gdn_fwd call use
- * the fused kernel; 2 the two passes wherever the workspace allows them.
+ * forward and summary (see gdn_fwd, "Two passes"); 1 makes every later
+ * gdn_fwd and gdn_summary call use the fused kernel; 2 the two passes wherever
+ * the workspace allows them.
  * Process-wide.  LA_ERR_INVALID_ARG for passes outside 0..2.
  */
 la_status la_test_set_fwd_passes(int32_t passes);

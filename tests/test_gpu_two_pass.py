@@ -140,3 +140,60 @@ def test_minimal_workspace_takes_the_fused_kernel():
     ws = torch.empty(la.workspace_bytes(w.N), dtype=torch.uint8, device=d)
     assert la.api.split_workspace_bytes(w.T, w.N, w.HV) > ws.numel()
     same(run(w, d, 2, workspace=ws), run(w, d, 2), "minimal workspace")
+
+
+# ---------------------------------------------------------------- summary
+
+
+def summary(w, d, passes, start=None, **kw):
+    lib = la.binding.load()
+    assert lib.la_test_set_fwd_passes(passes) == 0
+    try:
+        status = torch.zeros(1, dtype=torch.int32, device=d)
+        end, tr = la.gdn_summary(w.k.to(d), w.v.to(d), w.g.to(d), w.beta.to(d), w.cu_seqlens.to(d),
+                                 start_state=None if start is None else start.to(d), status=status, **kw)
+        assert la.read_status(status) == 0
+    finally:
+        assert lib.la_test_set_fwd_passes(0) == 0
+    return end, tr
+
+
+SUMMARY_CASES = {
+    "ragged spans K=V=128": dict(lengths=RAGGED, HK=2, HV=2, K=128, V=128),
+    "ragged spans K=V=64": dict(lengths=RAGGED, HK=1, HV=3, K=64, V=64),
+    "K=128 V=64 grouped 2:4": dict(lengths=[700, 64, 1, 2000], HK=2, HV=4, K=128, V=64),
+    "K=64 V=128": dict(lengths=[130, 1500], HK=2, HV=2, K=64, V=128),
+}
+
+
+@pytest.mark.parametrize("name", list(SUMMARY_CASES))
+@pytest.mark.parametrize("slow", [False, True])
+def test_two_pass_summary_equals_fused(name, slow):
+    """End states (from a nonzero start) and transitions: the same bits."""
+    c = SUMMARY_CASES[name]
+    d = dev()
+    w = W.draw(name, c["lengths"], c["HK"], c["HV"], c["K"], c["V"], seed=751 + len(name), initial_state=True,
+               slow_decay=slow)
+    for start in (None, w.initial_state):
+        a, b = summary(w, d, 1, start), summary(w, d, 2, start)
+        assert torch.equal(bits(a[0]), bits(b[0])), (name, "end state")
+        assert torch.equal(bits(a[1]), bits(b[1])), (name, "transition")
+
+
+def test_two_pass_summary_transforms_and_ranges():
+    """The gate and beta transforms, and a batch of spans whose (span, head, tile) units exceed
+    a wave even at two CTAs per SM (the range launches on top of the two passes)."""
+    d = dev()
+    w = W.draw("sum transforms", [300, 64, 0, 129], 2, 4, 128, 128, seed=761, initial_state=True)
+    g_raw, beta_logit, a_log, dt_bias = raw_gates(w, 762)
+    w.g, w.beta = g_raw, beta_logit
+    kw = dict(a_log=a_log.to(d), dt_bias=dt_bias.to(d), beta_sigmoid=True)
+    a, b = summary(w, d, 1, w.initial_state, **kw), summary(w, d, 2, w.initial_state, **kw)
+    assert torch.equal(bits(a[0]), bits(b[0])) and torch.equal(bits(a[1]), bits(b[1]))
+    lengths = [0, 1, 63, 64, 65, 127, 128, 129, 191, 192, 0, 700, 255, 256, 257, 3, 511, 640,
+               130, 0, 65, 200, 1000, 64, 2, 450, 129, 320, 0, 190, 66, 777,
+               128, 1, 256, 380, 0, 193, 64, 900, 40, 129, 600, 192, 5, 333, 70, 128]
+    w = W.draw("sum ranges", lengths, 8, 8, 64, 64, seed=763, initial_state=True, slow_decay=True)
+    assert w.N * w.HV * 2 > 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    a, b = summary(w, d, 1, w.initial_state), summary(w, d, 2, w.initial_state)
+    assert torch.equal(bits(a[0]), bits(b[0])) and torch.equal(bits(a[1]), bits(b[1]))
