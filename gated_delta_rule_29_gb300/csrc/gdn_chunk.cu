@@ -486,10 +486,10 @@ __global__ void __launch_bounds__(kCta, 2)
                      const __grid_constant__ CUtensorMap wymap, const ChunkArgs a) {
     constexpr bool kSum = MODE == kModeSummary || MODE == kModeSummarySplit;
     constexpr bool kFwd = !kSum;  // queries and outputs (the forward, or GDP's)
-    constexpr bool kGdp = MODE == kModeGdp;
-    // the state pass of the two-pass forward or summary: T (P) and the factors of every chunk come
-    // from the WY pass's records instead of being formed here
-    constexpr bool kSplit = MODE == kModeFwdSplit || MODE == kModeSummarySplit;
+    constexpr bool kGdp = MODE == kModeGdp || MODE == kModeGdpSplit;
+    // the state pass of the two-pass forward, summary or GDP: T (P) and the factors of every chunk
+    // come from the WY pass's records instead of being formed here
+    constexpr bool kSplit = MODE == kModeFwdSplit || MODE == kModeSummarySplit || MODE == kModeGdpSplit;
     constexpr SmemMap L = smem_map(MODE);
     constexpr uint32_t RQ = L.kq_region;
     // waits sleep in hardware when another CTA shares the SM (the forward and the summary's state
@@ -1185,12 +1185,16 @@ constexpr uint32_t WY_SC = 49152;   // Scalars without the solve scratch
 constexpr uint32_t WY_SMEM = WY_SC + ((kScalarsNoY + 127) & ~127u) + 1024;
 constexpr uint32_t WY_TMEM_COLS = 128;
 
-// kQ: the forward's records (queries: P and the query factors); else the summary's (T and the
-// key factors only, G over the keys alone as the fused summary forms it).
-template <int KD, bool kQ>
+// KIND kWyFwd: the forward's records (queries: P and the query factors); kWySummary: the
+// summary's (T and the key factors only, G over the keys alone as the fused summary forms it);
+// kWyGdp: Gated DeltaProduct's, chunks of 64 update rows whose query tokens are those whose last
+// update row lies in the chunk (at most ceil(64 / n), in the first rows of the query half).
+template <int KD, int KIND>
 __global__ void __launch_bounds__(kCta, 4)
     gdn_wy_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                   const __grid_constant__ CUtensorMap wymap, const ChunkArgs a) {
+    constexpr bool kQ = KIND != kWySummary;
+    constexpr bool kG = KIND == kWyGdp;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     Scalars& sc = *reinterpret_cast<Scalars*>(sm + WY_SC);  // (its solve scratch is not used here)
@@ -1203,6 +1207,8 @@ __global__ void __launch_bounds__(kCta, 4)
     const int tid = threadIdx.x;
     const int r = tid;
     const int HO = a.HV;
+    const int NH = kG ? a.gdp_n : 1;            // rows per token on the update timeline
+    const int QR = (kChunk + NH - 1) / NH;      // query rows a chunk can hold
 
     if (tid == 0) sc.status0 = *reinterpret_cast<volatile int32_t*>(&a.hdr->status);
     __syncthreads();
@@ -1225,19 +1231,24 @@ __global__ void __launch_bounds__(kCta, 4)
     const uint32_t tmem = sc.tmem_base;
     const uint32_t trow = tmem + (static_cast<uint32_t>(r & ~31) << 16);
     const uint64_t d_kq = sdesc_sw128(smem_u32(KQ), 16, 1024);
-    const uint32_t kq_bytes = KD * 128u * (kQ ? 2u : 1u);
+    const uint32_t kq_bytes = KD * 128u + (kQ ? static_cast<uint32_t>(KD / 64) * QR * 128u : 0u);
     const uint64_t budget = a.wait_budget_ns;
     uint32_t ph_kq = 0, ph_mma = 0;
     bool pend_kq = false, pend_mma = false, failed = false;
 
-    // an item's rows: chunk c of sequence seq, head h; first token t0, n valid rows
-    auto rows_of = [&](int64_t item, int seq, int64_t& t0, int& n) {
+    // an item's rows: chunk c of sequence seq, head h; first (update) row t0, n valid rows; its
+    // query tokens tq0 .. tq0 + nq - 1 relative to the sequence start (GDP), rel0 = 64 c
+    auto rows_of = [&](int64_t item, int seq, int64_t& t0, int& n, int& rel0, int& tq0, int& nq) {
         const int64_t chunk = item / HO;
         const int c = static_cast<int>(chunk - a.chunk_off[seq]);
         const int64_t tok_s = cu_get(a.cu, a.cu64, seq);
-        const int64_t left = cu_get(a.cu, a.cu64, seq + 1) - tok_s - static_cast<int64_t>(c) * kChunk;
+        const int64_t rows = (cu_get(a.cu, a.cu64, seq + 1) - tok_s) * NH;
+        const int64_t left = rows - static_cast<int64_t>(c) * kChunk;
         n = left < kChunk ? static_cast<int>(left) : kChunk;
-        t0 = tok_s + static_cast<int64_t>(c) * kChunk;
+        rel0 = c * kChunk;
+        t0 = tok_s * NH + rel0;
+        tq0 = kG ? rel0 / NH : rel0;
+        nq = kG ? (rel0 + n) / NH - tq0 : n;
     };
     // a row's gate and beta (threads 0-63)
     auto gates_of = [&](int64_t t0, int n, int h, float& g, float& b) {
@@ -1248,19 +1259,30 @@ __global__ void __launch_bounds__(kCta, 4)
                 gA = -expf(a.a_log[h]);
                 gdt = a.dt_bias[h];
             }
-            g = gate_row<false>(a, t0 + tid, h, gA, gdt);
+            g = gate_row<kG>(a, t0 + tid, h, gA, gdt);
             b = beta_at(a, t0 + tid, h);
         }
     };
 
     int64_t item = blockIdx.x;
     int64_t t0;
-    int n;
-    rows_of(item, a.chunk_seq[item / HO], t0, n);
+    int n, rel0, tq0, nq;
+    rows_of(item, a.chunk_seq[item / HO], t0, n, rel0, tq0, nq);
     float g_cur, b_cur;
     gates_of(t0, n, static_cast<int>(item % HO), g_cur, b_cur);
     for (; item < items; item += gridDim.x) {
         const int h = static_cast<int>(item % HO);
+        if (kG && QR < kChunk) {
+            // query rows QR .. 63 of the tile get no load: zero them (the space held the previous
+            // item's T and scratch), as the fused kernel has them
+            for (int e = tid; e < (KD / 64) * (kChunk - QR) * 8; e += kCta) {
+                const int rg = e / ((kChunk - QR) * 8), rem = e % ((kChunk - QR) * 8);
+                *reinterpret_cast<uint4*>(KQ + rg * 16384 + 8192 + (QR + rem / 8) * 128 + (rem % 8) * 16) =
+                    make_uint4(0u, 0u, 0u, 0u);
+            }
+            fence_proxy_async_smem();  // the G product reads them through the async proxy
+            __syncthreads();
+        }
         if (tid == 0 && !a.test_skip_tile_load) {
             // the previous item's T, P and scratch in this space are dead (the loop ended with a
             // barrier) and its record stores have read their sources
@@ -1271,7 +1293,8 @@ __global__ void __launch_bounds__(kCta, 4)
 #pragma unroll
             for (int rg = 0; rg < KD / 64; ++rg) {
                 tma_load_3d(KQ + rg * 16384, &kmap, &sc.bar_kq, rg * 64, hk, static_cast<int>(t0));
-                if (kQ) tma_load_3d(KQ + rg * 16384 + 8192, &qmap, &sc.bar_kq, rg * 64, hk, static_cast<int>(t0));
+                if (kQ)
+                    tma_load_3d(KQ + rg * 16384 + 8192, &qmap, &sc.bar_kq, rg * 64, hk, static_cast<int>(t0 / NH));
             }
         }
         pend_kq = !a.test_skip_tile_load;
@@ -1315,17 +1338,17 @@ __global__ void __launch_bounds__(kCta, 4)
         }
         tc_fence_after();
         float g64[64];
-        g_rows_and_norms<kQ>(trow, 0, r, n, n, a.l2norm, g64, sc);
+        g_rows_and_norms<kQ>(trow, 0, r, n, nq, a.l2norm, g64, sc);
         tc_fence_before();
         if (__syncthreads_or(!ok)) { failed = true; break; }
-        const bool fast = chunk_scalars<kQ, false>(sc, tid, n, n, 0, 0, 1, b_cur, a.scale);
-        build_a_p<kQ, false>(g64, sc, M, PB, fast, r, n, 0, 0, 1, a.scale);
+        const bool fast = chunk_scalars<kQ, kG>(sc, tid, n, nq, tq0, rel0, NH, b_cur, a.scale);
+        build_a_p<kQ, kG>(g64, sc, M, PB, fast, r, nq, tq0, rel0, NH, a.scale);
         // the next item's rows, gates and betas (in flight during the solve)
         int64_t nt0 = t0;
-        int nn = 0;
+        int nn = 0, nrel0 = 0, ntq0 = 0, nnq = 0;
         float g_nx = 0.f, b_nx = 0.f;
         if (has_next) {
-            rows_of(nitem, nseq, nt0, nn);
+            rows_of(nitem, nseq, nt0, nn, nrel0, ntq0, nnq);
             gates_of(nt0, nn, static_cast<int>(nitem % HO), g_nx, b_nx);
         }
         __syncthreads();  // A and P complete; the K/Q tile (read by the finished G product) becomes T's space
@@ -1343,6 +1366,9 @@ __global__ void __launch_bounds__(kCta, 4)
         __syncthreads();  // T (fp32) and the scratch are read: the next item's tile may land in their space
         t0 = nt0;
         n = nn;
+        rel0 = nrel0;
+        tq0 = ntq0;
+        nq = nnq;
         g_cur = g_nx;
         b_cur = b_nx;
     }
@@ -1465,6 +1491,7 @@ cudaError_t launch_chunk_kernel(const ChunkArgs& a, const CUtensorMap& qm, const
             case kModeFwdSplit: return launch_one<128, kModeFwdSplit>(a, qm, km, vm, om, wm, dev, s);
             case kModeSummary: return launch_one<128, kModeSummary>(a, qm, km, vm, om, wm, dev, s);
             case kModeSummarySplit: return launch_one<128, kModeSummarySplit>(a, qm, km, vm, om, wm, dev, s);
+            case kModeGdpSplit: return launch_one<128, kModeGdpSplit>(a, qm, km, vm, om, wm, dev, s);
             default: return launch_one<128, kModeFwd>(a, qm, km, vm, om, wm, dev, s);
         }
     }
@@ -1473,14 +1500,15 @@ cudaError_t launch_chunk_kernel(const ChunkArgs& a, const CUtensorMap& qm, const
         case kModeFwdSplit: return launch_one<64, kModeFwdSplit>(a, qm, km, vm, om, wm, dev, s);
         case kModeSummary: return launch_one<64, kModeSummary>(a, qm, km, vm, om, wm, dev, s);
         case kModeSummarySplit: return launch_one<64, kModeSummarySplit>(a, qm, km, vm, om, wm, dev, s);
+        case kModeGdpSplit: return launch_one<64, kModeGdpSplit>(a, qm, km, vm, om, wm, dev, s);
         default: return launch_one<64, kModeFwd>(a, qm, km, vm, om, wm, dev, s);
     }
 }
 
-template <int KD, bool kQ>
+template <int KD, int KIND>
 static cudaError_t launch_wy(const ChunkArgs& a, const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& wm,
                              int device, cudaStream_t s) {
-    auto* fn = gdn_wy_kernel<KD, kQ>;
+    auto* fn = gdn_wy_kernel<KD, KIND>;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, WY_SMEM);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
@@ -1502,12 +1530,15 @@ static cudaError_t launch_wy(const ChunkArgs& a, const CUtensorMap& qm, const CU
 }
 
 cudaError_t launch_wy_kernel(const ChunkArgs& a, const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& wm,
-                             bool summary, cudaStream_t s) {
+                             int kind, cudaStream_t s) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (summary) return a.K == 128 ? launch_wy<128, false>(a, qm, km, wm, dev, s) : launch_wy<64, false>(a, qm, km, wm, dev, s);
-    return a.K == 128 ? launch_wy<128, true>(a, qm, km, wm, dev, s) : launch_wy<64, true>(a, qm, km, wm, dev, s);
+    if (kind == kWySummary)
+        return a.K == 128 ? launch_wy<128, kWySummary>(a, qm, km, wm, dev, s) : launch_wy<64, kWySummary>(a, qm, km, wm, dev, s);
+    if (kind == kWyGdp)
+        return a.K == 128 ? launch_wy<128, kWyGdp>(a, qm, km, wm, dev, s) : launch_wy<64, kWyGdp>(a, qm, km, wm, dev, s);
+    return a.K == 128 ? launch_wy<128, kWyFwd>(a, qm, km, wm, dev, s) : launch_wy<64, kWyFwd>(a, qm, km, wm, dev, s);
 }
 
 }  // namespace la

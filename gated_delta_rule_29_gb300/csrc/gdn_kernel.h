@@ -12,10 +12,12 @@ constexpr int kThreads = 256;       // threads of the fused chunk kernel
 constexpr int kPrologueThreads = 1024;
 
 // kModeGdp: the forward of Gated DeltaProduct (n delta updates per token) on the update timeline,
-// with q, g and o on the token timeline.  kModeFwdSplit / kModeSummarySplit: the forward's or
-// the summary's state pass, reading each chunk's T (and P) and per-token factors from the
-// records the WY pass (gdn_wy_kernel) wrote.
-enum Mode : int { kModeFwd = 0, kModeSummary = 1, kModeGdp = 2, kModeFwdSplit = 3, kModeSummarySplit = 4 };
+// with q, g and o on the token timeline.  kModeFwdSplit / kModeSummarySplit / kModeGdpSplit:
+// the forward's, the summary's or GDP's state pass, reading each chunk's T (and P) and per-token
+// factors from the records the WY pass (gdn_wy_kernel) wrote.
+enum Mode : int {
+    kModeFwd = 0, kModeSummary = 1, kModeGdp = 2, kModeFwdSplit = 3, kModeSummarySplit = 4, kModeGdpSplit = 5
+};
 enum TileKind : int { kTileValue = 0, kTileTransition = 1 };
 
 // Workspace layout (bytes from the 256-aligned workspace base).
@@ -93,6 +95,7 @@ struct PrologueArgs {
     uint64_t* keys;       // global sort scratch (N > kSmemSortMax)
     int32_t* user_status; // nullable
     int64_t* chunk_off;   // nullable: [N + 1] first chunk of each sequence, then the total
+    int32_t chunk_rows;   // rows per token on the chunked timeline (GDP: its updates per token; else 1)
     int32_t* chunk_seq;   // with chunk_off: [total] the sequence of each chunk
 };
 
@@ -292,8 +295,9 @@ cudaError_t launch_compose(const ComposeArgs& a, cudaStream_t s);
 
 // The WY pass of the two-pass forward or summary: one record per (chunk, head) item (wymap: the
 // records as [items][136 rows][64] bf16); summary: the records without P.
+enum WyKind : int { kWyFwd = 0, kWySummary = 1, kWyGdp = 2 };
 cudaError_t launch_wy_kernel(const ChunkArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
-                             const CUtensorMap& wymap, bool summary, cudaStream_t s);
+                             const CUtensorMap& wymap, int kind, cudaStream_t s);
 cudaError_t launch_chunk_kernel(const ChunkArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
                                 const CUtensorMap& vmap, const CUtensorMap& omap, const CUtensorMap& wymap, int mode,
                                 cudaStream_t s);

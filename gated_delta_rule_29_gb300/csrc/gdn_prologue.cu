@@ -92,12 +92,13 @@ __global__ void __launch_bounds__(kPrologueThreads) gdn_prologue_kernel(Prologue
         if (tid == 0) a.hdr->ckpt_rows = static_cast<int32_t>(carry);
     }
     if (a.chunk_off) {
-        // the two-pass forward numbers the batch's chunks sequence by sequence
+        // the two-pass schedule numbers the batch's chunks sequence by sequence (GDP's on the
+        // update timeline, chunk_rows rows per token)
         int64_t carry = 0;
         for (int base = 0; base < N; base += blockDim.x) {
             const int i = base + tid;
             int64_t nch = 0;
-            if (i < N) nch = (cu_at(a.cu, a.cu64, i + 1) - cu_at(a.cu, a.cu64, i) + kChunk - 1) / kChunk;
+            if (i < N) nch = ((cu_at(a.cu, a.cu64, i + 1) - cu_at(a.cu, a.cu64, i)) * a.chunk_rows + kChunk - 1) / kChunk;
             int64_t total;
             const int64_t ex = block_exclusive_scan(nch, warp_sums, total);
             if (i < N) a.chunk_off[i] = carry + ex;

@@ -197,9 +197,9 @@ la_status run(const Common& c, ChunkArgs& ka, const void* q, int64_t q_st, int64
     // the state pass) when the workspace has room for the WY records; otherwise as the fused
     // kernel.  Both give the same bits.
     const int32_t passes = g_test_fwd_passes.load(std::memory_order_relaxed);
-    const la::SplitLayout SL = la::split_layout(c.T, c.N, c.HV);
-    bool split = (mode == la::kModeFwd || mode == la::kModeSummary) && c.T > 0 && passes != 1 &&
-                 SL.items < (int64_t(1) << 31);
+    const la::SplitLayout SL = la::split_layout(c.T * gdp_n, c.N, c.HV);
+    bool split = (mode == la::kModeFwd || mode == la::kModeSummary || mode == la::kModeGdp) && c.T > 0 &&
+                 passes != 1 && SL.items < (int64_t(1) << 31);
     la_status st = LA_OK;
     if (split) {
         if (workspace) {
@@ -217,6 +217,7 @@ la_status run(const Common& c, ChunkArgs& ka, const void* q, int64_t q_st, int64
     pa.cu = c.cu;
     pa.chunk_off = split ? reinterpret_cast<int64_t*>(wsb + SL.chunk_off) : nullptr;
     pa.chunk_seq = split ? reinterpret_cast<int32_t*>(wsb + SL.chunk_seq) : nullptr;
+    pa.chunk_rows = gdp_n;
     pa.cu64 = c.cu_bits == 64;
     pa.T = c.T;
     pa.N = c.N;
@@ -290,9 +291,12 @@ la_status run(const Common& c, ChunkArgs& ka, const void* q, int64_t q_st, int64
     if (split) {
         ChunkArgs kw = ka;
         kw.num_units = SL.items;  // the bound on (chunk, head) items
-        if (la::launch_wy_kernel(kw, qm, km, wm, mode == la::kModeSummary, stream) != cudaSuccess) return LA_ERR_CUDA;
+        const int kind = mode == la::kModeSummary ? la::kWySummary : mode == la::kModeGdp ? la::kWyGdp : la::kWyFwd;
+        if (la::launch_wy_kernel(kw, qm, km, wm, kind, stream) != cudaSuccess) return LA_ERR_CUDA;
     }
-    const int kmode = !split ? mode : (mode == la::kModeSummary ? la::kModeSummarySplit : la::kModeFwdSplit);
+    const int kmode = !split ? mode
+                             : (mode == la::kModeSummary ? la::kModeSummarySplit
+                                                         : mode == la::kModeGdp ? la::kModeGdpSplit : la::kModeFwdSplit);
     if (la::launch_chunk_kernel(ka, qm, km, vm, om, wm, kmode, stream) != cudaSuccess) return LA_ERR_CUDA;
     if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess) return LA_ERR_CUDA;
     return LA_OK;
@@ -490,6 +494,8 @@ extern "C" size_t la_gdp_workspace_bytes(int64_t T, int32_t N, int32_t HK, int32
                                          int32_t n) {
     if (T < 0 || N < 0 || HK <= 0 || HV <= 0 || n < 1) return 0;
     if (n == 1) return la::ws_layout(N).total;
+    // n <= 64 runs natively on the update timeline: the two-pass workspace of that timeline
+    if (n <= la::kChunk) return la::split_layout(T * n, N, HV).total;
     return gdp_layout(T, N, HK, HV, K, V, n).total;
 }
 
@@ -708,6 +714,7 @@ la_status gdn_bwd(const la_gdn_bwd_params* p, void* stream) {
         PrologueArgs pa;
         pa.cu = p->cu_seqlens;
         pa.chunk_off = nullptr;
+        pa.chunk_rows = 1;
         pa.cu64 = p->cu_seqlens_bits == 64;
         pa.T = p->T;
         pa.N = p->N;
@@ -847,6 +854,7 @@ la_status gdn_summary_bwd(const la_gdn_summary_bwd_params* p, void* stream) {
     PrologueArgs pa;
     pa.cu = p->cu_seqlens;
     pa.chunk_off = nullptr;
+    pa.chunk_rows = 1;
     pa.cu64 = p->cu_seqlens_bits == 64;
     pa.T = p->T;
     pa.N = p->N;

@@ -517,8 +517,11 @@ la_status gdn_summary_bwd(const la_gdn_summary_bwd_params* p, void* stream);
 /* Bytes of device workspace gdn_summary_bwd needs. */
 size_t la_gdn_summary_bwd_workspace_bytes(int32_t N, int32_t HV, int32_t K, int32_t V);
 
-/* Bytes of device workspace gdn_fwd needs with num_householder = n > 1 (the update timeline's
-   query, gate and output rows plus the chunk kernel's scratch); n <= 1: la_gdn_workspace_bytes. */
+/* Bytes of device workspace gdn_fwd needs with num_householder = n > 1: for n <= 64 (run
+   natively on the update timeline) the two-pass workspace of that timeline (T * n rows; a
+   smaller workspace of at least la_gdn_workspace_bytes(N, 0) takes the fused kernel, the same
+   bits); for n > 64 the timeline's query, gate and output rows plus the chunk kernel's scratch.
+   n <= 1: la_gdn_workspace_bytes. */
 size_t la_gdp_workspace_bytes(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, int32_t V, int32_t n);
 
 /* Bytes of device workspace gdn_fwd (summary = 0) or gdn_summary (summary = 1) needs. */

@@ -197,3 +197,33 @@ def test_two_pass_summary_transforms_and_ranges():
     assert w.N * w.HV * 2 > 2 * torch.cuda.get_device_properties(0).multi_processor_count
     a, b = summary(w, d, 1, w.initial_state), summary(w, d, 2, w.initial_state)
     assert torch.equal(bits(a[0]), bits(b[0])) and torch.equal(bits(a[1]), bits(b[1]))
+
+
+# ---------------------------------------------------------------- Gated DeltaProduct
+
+
+@pytest.mark.parametrize("n", [2, 3, 5, 16, 64])
+def test_two_pass_gdp_equals_fused(n):
+    """GDP natively on the update timeline (n updates per token): two passes and the fused kernel
+    give the same outputs, final states and checkpoints (every 64 tokens)."""
+    d = dev()
+    lengths = [0, 1, 33, 64, 100, 257]
+    w = W.draw(f"gdp {n}", lengths, 2, 4, 64, 64, seed=771 + n, initial_state=True, slow_decay=True)
+    gen = torch.Generator().manual_seed(772 + n)
+    T = w.T
+    k = torch.randn(T * n, w.HK, w.K, generator=gen).to(torch.bfloat16)
+    v = torch.randn(T * n, w.HV, w.V, generator=gen).to(torch.bfloat16)
+    beta = (0.1 * torch.rand(T * n, w.HV, generator=gen)).contiguous()
+    outs = []
+    lib = la.binding.load()
+    for passes in (1, 2):
+        assert lib.la_test_set_fwd_passes(passes) == 0
+        try:
+            status = torch.zeros(1, dtype=torch.int32, device=d)
+            outs.append(la.gdn_fwd(w.q.to(d), k.to(d), v.to(d), w.g.to(d), beta.to(d), w.cu_seqlens.to(d),
+                                   initial_state=w.initial_state.to(d), checkpoint_every_n=64,
+                                   checkpoint_dtype=torch.float32, num_householder=n, status=status))
+            assert la.read_status(status) == 0
+        finally:
+            assert lib.la_test_set_fwd_passes(0) == 0
+    same(outs[0], outs[1], f"GDP n={n}")
