@@ -592,6 +592,7 @@ __global__ void __launch_bounds__(kCta, 2)
     }
     uint32_t ph_kq = 0, ph_v = 0, ph_mma = 0, ph_o = 0, ph_f = 0;  // parity of the next wait on each barrier
     bool pend_kq = false, pend_v = false, pend_mma = false, pend_o = false, pend_f = false;
+    bool pend_st = false;  // the state's write-back to TMEM, waited for before the next state update
     bool failed = false;
     const uint64_t budget = a.wait_budget_ns;
     const int64_t per_seq = static_cast<int64_t>(HO) * a.tiles_per_head;
@@ -848,19 +849,36 @@ __global__ void __launch_bounds__(kCta, 2)
             tc_fence_before();
             if (__syncthreads_or(!ok)) { failed = true; break; }
 
-            // ---- S4: X^T = beta V^T - sx (K S)^T (hi + lo); then T = (I + A)^{-1} in the V tile's space
-            ok = mbar_wait(&sc.bar_mma, ph_mma, budget, kSleep);
-            if (ok) {
-                ph_mma ^= 1u;
-                pend_mma = false;
-            }
-            if (value_tile) {
-                const bool okv = mbar_wait(&sc.bar_v, ph_v, budget, kSleep);
-                if (okv) {
-                    ph_v ^= 1u;
-                    pend_v = false;
+            // ---- S4: X^T = beta V^T - sx (K S)^T (hi + lo); then T = (I + A)^{-1} in the V tile's space.
+            // This thread's column of V (64 bf16, packed in pairs) is read while the K S product runs.
+            uint32_t vpk[32];
+            {
+                bool okv = true;
+                if (value_tile) {
+                    okv = mbar_wait(&sc.bar_v, ph_v, budget, kSleep);
+                    if (okv) {
+                        ph_v ^= 1u;
+                        pend_v = false;
+                    }
+                }
+                const bool has_v = value_tile && okv && r < a.V;
+                const uint8_t* vcol = VT + (r >> 6) * 8192 + (r & 7) * 2;
+                const uint32_t vchunk = (r & 63) >> 3;
+#pragma unroll
+                for (int j2 = 0; j2 < 32; ++j2) {
+                    const uint32_t lo16 = has_v ? *reinterpret_cast<const uint16_t*>(vcol + sw128_off(2 * j2, vchunk)) : 0u;
+                    const uint32_t hi16 = has_v ? *reinterpret_cast<const uint16_t*>(vcol + sw128_off(2 * j2 + 1, vchunk)) : 0u;
+                    vpk[j2] = lo16 | (hi16 << 16);
                 }
                 ok = ok && okv;
+            }
+            {
+                const bool okk = mbar_wait(&sc.bar_mma, ph_mma, budget, kSleep);
+                if (okk) {
+                    ph_mma ^= 1u;
+                    pend_mma = false;
+                }
+                ok = ok && okk;
             }
             if (kSplit) {
                 const bool okf = mbar_wait(&sc.bar_f, ph_f, budget, kSleep);
@@ -873,9 +891,6 @@ __global__ void __launch_bounds__(kCta, 2)
             tc_fence_after();
             {
                 const int v = r;
-                const bool has_v = value_tile && v < a.V;
-                const uint8_t* vcol = VT + (v >> 6) * 8192 + (v & 7) * 2;
-                const uint32_t vchunk = (v & 63) >> 3;
                 float k64[64];
 #pragma unroll
                 for (int p = 0; p < 4; ++p) tmem_ld16(trow + COL_R1 + 16 * p, *reinterpret_cast<float(*)[16]>(&k64[16 * p]));
@@ -892,9 +907,7 @@ __global__ void __launch_bounds__(kCta, 2)
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
                             const int j = 8 * cc + e;
-                            const float vv = has_v
-                                ? bf16_bits_to_f(*reinterpret_cast<const uint16_t*>(vcol + sw128_off(j, vchunk)))
-                                : 0.f;
+                            const float vv = __uint_as_float((j & 1) ? (vpk[j >> 1] & 0xFFFF0000u) : (vpk[j >> 1] << 16));
                             x[e] = bt[e] * vv - sxv[e] * ks[8 * hh + e];
                         }
                         store8_split(WB + sw128_off(v, cc), WB + 16384 + sw128_off(v, cc), x);
@@ -979,6 +992,10 @@ __global__ void __launch_bounds__(kCta, 2)
                         store8_split(WB + sw128_off(v, cc), WB + 16384 + sw128_off(v, cc), x);
                     }
                 }
+            }
+            if (pend_st) {
+                tmem_wait_st();  // the previous chunk's state write-back, which the update accumulates onto
+                pend_st = false;
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -1138,7 +1155,7 @@ __global__ void __launch_bounds__(kCta, 2)
                         }
                     }
                 }
-                if (!last) tmem_wait_st();
+                pend_st = !last;
             }
             // the O staging buffer is the next chunk's A: the bulk store must have read it
             if (kFwd && tid == 0) bulk_wait_read_all();
@@ -1157,6 +1174,7 @@ __global__ void __launch_bounds__(kCta, 2)
         if (pend_mma) mbar_wait(&sc.bar_mma, ph_mma, budget);
         if (pend_o) mbar_wait(&sc.bar_o, ph_o, budget);
         if (pend_f) mbar_wait(&sc.bar_f, ph_f, budget);
+        tmem_wait_st();
         if (tid == 0) {
             atomicCAS(&a.hdr->status, LA_OK, LA_ERR_TIMEOUT);
             if (a.user_status) atomicCAS(a.user_status, LA_OK, LA_ERR_TIMEOUT);
