@@ -143,7 +143,13 @@ la_status make_host_plan(const la_gdn_fwd_host_params* hp, HostPlan& P) {
     P.mid = take(static_cast<size_t>(P.nlong) * 2 * state * 4);
     P.meta_bytes = P.cu_count * 4 + (f.gate_mode == LA_GATE_SOFTPLUS ? 2 * HV * 4 : 0);
     P.meta = take(P.meta_bytes);
+    // each compute stream's workspace has room for the two-pass forward of the largest range
     P.ws_each = up256(la_gdn_workspace_bytes(f.N, 0));
+    for (const Range& r : P.parts) {
+        const int32_t nr = r.piece < 0 ? r.b - r.a : 1;
+        const size_t need = la_gdn_fwd_split_workspace_bytes(r.t_b - r.t_a, nr, f.HV);
+        if (up256(need) > P.ws_each) P.ws_each = up256(need);
+    }
     P.ws = take(P.ws_each * kHostStreams);
     P.total = off;
     return LA_OK;
