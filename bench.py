@@ -1010,7 +1010,8 @@ def run_summary_bwd_bench(args, world, rank, local):
     do_h = torch.randn(T, HV, V, generator=gen).to(torch.bfloat16)
     q, k, g, b, spans, do = (x.to(dev) for x in (w.q, w.k, w.g, w.beta, w.spans, do_h))
     S = spans.numel() - 1
-    ws = torch.empty(lib.la_gdn_summary_bwd_workspace_bytes(S, HV, K, V), dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(lib.la_gdn_summary_bwd_workspace_bytes(S, HV, K, V), la.api.split_workspace_bytes(T, S, HV)),
+                     dtype=torch.uint8, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
 
     def step():

@@ -359,7 +359,9 @@ def gdn_summary_bwd(q: torch.Tensor, k: torch.Tensor, g: torch.Tensor, beta: tor
     d_state = _out("d_state", d_state, (N, HV, K, V), torch.float32, dev, contiguous=True)
     lib = B.load()
     if workspace is None:
-        workspace = torch.empty(lib.la_gdn_summary_bwd_workspace_bytes(N, HV, K, V), dtype=torch.uint8, device=dev)
+        # room for the tensor-core path (the forward's WY records), else the tile kernel's minimum
+        need = max(int(lib.la_gdn_summary_bwd_workspace_bytes(N, HV, K, V)), split_workspace_bytes(q.shape[0], N, HV))
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
     if d_final_state is not None:
         d_final_state = d_final_state.contiguous().float()
     p = B.GdnSummaryBwdParams()

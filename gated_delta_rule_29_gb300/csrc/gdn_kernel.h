@@ -295,6 +295,10 @@ cudaError_t launch_compose(const ComposeArgs& a, cudaStream_t s);
 
 // The WY pass of the two-pass forward or summary: one record per (chunk, head) item (wymap: the
 // records as [items][136 rows][64] bf16); summary: the records without P.
+// The state-gradient pass of gdn_summary_bwd on the WY records (a.s0: the gradient leaving each
+// span or null, a.final_state: the gradient entering it; domap: dO as [T][HV][V] bf16).
+cudaError_t launch_grad(const ChunkArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
+                        const CUtensorMap& domap, const CUtensorMap& wymap, cudaStream_t s);
 enum WyKind : int { kWyFwd = 0, kWySummary = 1, kWyGdp = 2 };
 cudaError_t launch_wy_kernel(const ChunkArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
                              const CUtensorMap& wymap, int kind, cudaStream_t s);

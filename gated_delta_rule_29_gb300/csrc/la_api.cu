@@ -822,6 +822,85 @@ la_status gdn_bwd(const la_gdn_bwd_params* p, void* stream) {
     return LA_OK;
 }
 
+namespace {
+// gdn_summary_bwd on the tensor cores: the prologue (validation, longest-first order, chunk
+// numbering), the forward's WY pass over every (chunk, head), and the state-gradient pass.
+la_status summary_bwd_two_pass(const la_gdn_summary_bwd_params* p, const la::SplitLayout& GL, uint8_t* wb,
+                               cudaStream_t s) {
+    la_status st;
+    const la::WorkspaceLayout PL = la::ws_layout(p->N);
+    PrologueArgs pa;
+    pa.cu = p->cu_seqlens;
+    pa.chunk_off = reinterpret_cast<int64_t*>(wb + GL.chunk_off);
+    pa.chunk_seq = reinterpret_cast<int32_t*>(wb + GL.chunk_seq);
+    pa.chunk_rows = 1;
+    pa.cu64 = p->cu_seqlens_bits == 64;
+    pa.T = p->T;
+    pa.N = p->N;
+    pa.ckpt_n = 0;
+    pa.hdr = reinterpret_cast<la::WsHeader*>(wb);
+    pa.order = reinterpret_cast<int32_t*>(wb + PL.order);
+    pa.ckpt_off = reinterpret_cast<int64_t*>(wb + PL.ckpt_off);
+    pa.keys = reinterpret_cast<uint64_t*>(wb + PL.keys);
+    pa.user_status = p->status;
+    if (la::launch_prologue(pa, s) != cudaSuccess) return LA_ERR_CUDA;
+
+    ChunkArgs ka;
+    std::memset(&ka, 0, sizeof(ka));
+    if ((st = set_transforms(ka, p->gate_mode, p->a_log, p->dt_bias, p->gate_lower_bound, p->beta_sigmoid,
+                             p->beta_bf16)) != LA_OK)
+        return st;
+    ka.g = p->g;
+    ka.g_st = p->g_stride_t;
+    ka.g_sh = p->g_stride_h;
+    ka.beta = p->beta;
+    ka.b_st = p->beta_stride_t;
+    ka.b_sh = p->beta_stride_h;
+    ka.cu = p->cu_seqlens;
+    ka.cu64 = p->cu_seqlens_bits == 64;
+    ka.T = p->T;
+    ka.N = p->N;
+    ka.HK = p->HK;
+    ka.HV = p->HV;
+    ka.K = p->K;
+    ka.V = p->V;
+    ka.group = p->HV / p->HK;
+    ka.scale = p->scale > 0.f ? p->scale : 1.0f / std::sqrt(static_cast<float>(p->K));
+    ka.l2norm = p->use_qk_l2norm != 0;
+    ka.s0 = p->d_final_state;
+    ka.final_state = p->d_state;
+    ka.tiles_per_head = 1;
+    ka.num_units = static_cast<int64_t>(p->N) * p->HV;
+    ka.hdr = pa.hdr;
+    ka.order = pa.order;
+    ka.ckpt_off = pa.ckpt_off;
+    ka.chunk_off = pa.chunk_off;
+    ka.chunk_seq = pa.chunk_seq;
+    ka.wy = wb + GL.wy;
+    ka.user_status = p->status;
+    ka.wait_budget_ns = kWaitBudgetNs;
+    ka.gdp_n = 1;
+    if (const uint64_t b = g_test_wait_budget_ns.load(std::memory_order_relaxed)) ka.wait_budget_ns = b;
+    if (ka.num_units == 0) return LA_OK;
+
+    CUtensorMap qm, km, dom, wm;
+    if ((st = make_map(&km, p->k, p->T, p->HK, p->K, p->k_stride_t, p->k_stride_h)) != LA_OK) return st;
+    if ((st = make_map(&qm, p->q, p->T, p->HK, p->K, p->q_stride_t, p->q_stride_h)) != LA_OK) return st;
+    if ((st = make_map(&dom, p->d_o, p->T, p->HV, p->V, p->d_o_stride_t, p->d_o_stride_h)) != LA_OK) return st;
+    if ((st = make_map(&wm, ka.wy, 136, GL.items, 64, 64, static_cast<int64_t>(la::kWyRecordBytes / 2))) != LA_OK)
+        return st;
+    cudaEvent_t ev0 = t_timing_start, ev1 = t_timing_stop;
+    t_timing_start = t_timing_stop = nullptr;
+    if (ev0 && cudaEventRecord(ev0, s) != cudaSuccess) return LA_ERR_CUDA;
+    ChunkArgs kw = ka;
+    kw.num_units = GL.items;  // the bound on (chunk, head) items
+    if (la::launch_wy_kernel(kw, qm, km, wm, la::kWyFwd, s) != cudaSuccess) return LA_ERR_CUDA;
+    if (la::launch_grad(ka, qm, km, dom, wm, s) != cudaSuccess) return LA_ERR_CUDA;
+    if (ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return LA_ERR_CUDA;
+    return LA_OK;
+}
+}  // namespace
+
 la_status gdn_summary_bwd(const la_gdn_summary_bwd_params* p, void* stream) {
     if (!p) return LA_ERR_INVALID_ARG;
     Common c{p->T, p->N, p->HK, p->HV, p->K, p->V, p->cu_seqlens, p->cu_seqlens_bits, p->g, p->beta,
@@ -839,6 +918,24 @@ la_status gdn_summary_bwd(const la_gdn_summary_bwd_params* p, void* stream) {
         if ((st = check_tma_operand(p->q, p->q_stride_t, p->q_stride_h, p->HK)) != LA_OK) return st;
         if ((st = check_tma_operand(p->k, p->k_stride_t, p->k_stride_h, p->HK)) != LA_OK) return st;
         if (!p->d_o || !aligned(p->d_o, 2)) return LA_ERR_INVALID_ARG;
+    }
+    // On the tensor cores when the workspace has room for the forward's WY records: the WY pass,
+    // then the state-gradient pass (gdn_grad.cu); otherwise the tile kernel's state-only mode.
+    {
+        const int32_t passes = g_test_fwd_passes.load(std::memory_order_relaxed);
+        const la::SplitLayout GL = la::split_layout(p->T, p->N, p->HV);
+        bool two = passes != 1 && p->T > 0 && GL.items < (int64_t(1) << 31) && aligned(p->d_o, 16) &&
+                   p->d_o_stride_t % 8 == 0 && (p->HV == 1 || p->d_o_stride_h % 8 == 0);
+        void* w2 = nullptr;
+        if (two) {
+            if (p->workspace) {
+                two = p->workspace_bytes >= GL.total && aligned(p->workspace, 256);
+                w2 = p->workspace;
+            } else {
+                two = internal_workspace(GL.total, static_cast<cudaStream_t>(stream), &w2) == LA_OK;
+            }
+        }
+        if (two) return summary_bwd_two_pass(p, GL, static_cast<uint8_t*>(w2), static_cast<cudaStream_t>(stream));
     }
     const SumBwdLayout SL = sum_bwd_layout(p->N, p->HV, p->K, p->V);
     void* ws = p->workspace;

@@ -511,10 +511,17 @@ typedef struct la_gdn_summary_bwd_params {
  * transition.  That gradient does not depend on the entering state or on v (the map from the
  * state to the outputs is affine), so neither is an input and no forward pass runs.  Errors and
  * ownership as gdn_summary; g and beta go through gdn_fwd's input transforms when named.
+ * Two paths: when the workspace has room for the forward's WY records
+ * (la_gdn_fwd_split_workspace_bytes(T, N, HV); with workspace = NULL the internal buffer grows to
+ * it) and d_o is 16-byte aligned with strides in 16-byte units, the WY pass and a state-gradient
+ * pass on the tensor cores (the state gradient in TMEM, bf16 hi + lo operands); otherwise a tile
+ * kernel on warp-level MMAs (split tf32 operands), whose result equals gdn_bwd's d_initial_state
+ * bit for bit.  The two agree to fp32-level tolerance; each is bitwise independent of the batch.
  */
 la_status gdn_summary_bwd(const la_gdn_summary_bwd_params* p, void* stream);
 
-/* Bytes of device workspace gdn_summary_bwd needs. */
+/* Bytes of device workspace gdn_summary_bwd needs (the tile kernel's path; the tensor-core path
+   needs la_gdn_fwd_split_workspace_bytes(T, N, HV)). */
 size_t la_gdn_summary_bwd_workspace_bytes(int32_t N, int32_t HV, int32_t K, int32_t V);
 
 /* Bytes of device workspace gdn_fwd needs with num_householder = n > 1: for n <= 64 (run

@@ -38,14 +38,21 @@ def cotangents(w, seed, with_final=True):
     return do, dfin
 
 
-def run(w, do, dfin, l2=True, scale=None, cu=None):
+def run(w, do, dfin, l2=True, scale=None, cu=None, passes=0):
+    """passes 0: the automatic path (the tensor-core state-gradient pass when the workspace has
+    room, as the API's default workspace does); 1: the tile kernel's state-only mode."""
     d = dev()
     status = torch.zeros(1, dtype=torch.int32, device=d)
     cu = w.cu_seqlens if cu is None else cu
-    out = la.gdn_summary_bwd(w.q.to(d), w.k.to(d), w.g.to(d), w.beta.to(d), cu.to(d), do.to(d),
-                             use_qk_l2norm=l2, scale=scale, d_final_state=None if dfin is None else dfin.to(d),
-                             status=status)
-    assert la.read_status(status) == 0
+    lib = la.binding.load()
+    assert lib.la_test_set_fwd_passes(passes) == 0
+    try:
+        out = la.gdn_summary_bwd(w.q.to(d), w.k.to(d), w.g.to(d), w.beta.to(d), cu.to(d), do.to(d),
+                                 use_qk_l2norm=l2, scale=scale, d_final_state=None if dfin is None else dfin.to(d),
+                                 status=status)
+        assert la.read_status(status) == 0
+    finally:
+        assert lib.la_test_set_fwd_passes(0) == 0
     return out
 
 
@@ -91,14 +98,20 @@ def test_summary_bwd_without_l2norm():
 
 
 def test_summary_bwd_equals_backward_state_gradient_bitwise():
-    """The mirror is bitwise the entering-state gradient of the full backward (same recursion)."""
+    """The tile kernel's state-only mode is bitwise the entering-state gradient of the full
+    backward (same recursion, same kernel); the tensor-core pass agrees with both to fp32-level
+    tolerance."""
     w = W.draw("sbwd vs bwd", [130, 64, 257], 2, 2, 128, 128, seed=531, initial_state=True, slow_decay=True)
     do, dfin = cotangents(w, 532)
     d = dev()
-    a = run(w, do, dfin)
+    a = run(w, do, dfin, passes=1)
     b = la.gdn_bwd(w.q.to(d), w.k.to(d), w.v.to(d), w.g.to(d), w.beta.to(d), w.cu_seqlens.to(d), do.to(d),
                    initial_state=w.initial_state.to(d), d_final_state=dfin.to(d))[5]
     assert torch.equal(a, b)
+    c = run(w, do, dfin)
+    e = rel(c.cpu().numpy(), a.cpu().numpy())
+    print(f"[parity] summary_bwd tensor-core pass vs tile kernel: {e:.2e}")
+    assert e <= F32_TOL
 
 
 def test_summary_bwd_batch_invariant():
