@@ -480,7 +480,8 @@ GdpLayout gdp_layout(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, in
         off += (bytes + 255) & ~size_t(255);
         return at;
     };
-    L.pro = take(la::ws_layout(N).total);
+    // the forward on the timeline (T n rows) gets room for its two-pass schedule
+    L.pro = take(la::split_layout(T * n, N, HV).total);
     L.qe = take(static_cast<size_t>(T) * n * HK * K * 2);
     L.ge = take(static_cast<size_t>(T) * n * HV * sizeof(float));
     L.cue = take(static_cast<size_t>(N + 1) * sizeof(int64_t));
@@ -556,7 +557,7 @@ la_status gdp_fwd(const la_gdn_fwd_params* p, void* stream) {
     f.T = p->T * n;
     f.o = wb + GL.oe; f.o_stride_t = static_cast<int64_t>(p->HV) * p->V; f.o_stride_h = p->V;
     f.checkpoint_every_n = p->checkpoints ? p->checkpoint_every_n * n : 0;
-    f.workspace = wb + GL.pro; f.workspace_bytes = la::ws_layout(p->N).total;
+    f.workspace = wb + GL.pro; f.workspace_bytes = la::split_layout(p->T * n, p->N, p->HV).total;
     if ((st = gdn_fwd(&f, stream)) != LA_OK) return st;
     if (la::launch_gdp_gather(g, s) != cudaSuccess) return LA_ERR_CUDA;
     return LA_OK;
