@@ -191,3 +191,27 @@ def test_summary_bwd_with_input_transforms():
     ref = oracle.gdn_summary_bwd(w.q, w.k, g_raw, b_logit, w.cu_seqlens, do, d_final_state=dfin, gate="softplus",
                                  a_log=a_log, dt_bias=dt_bias, beta_sigmoid=True)
     check(w, got, ref, " softplus gate + beta sigmoid")
+
+
+def test_summary_bwd_tensor_core_pass_many_units_per_cta():
+    """More (span, head) units than SMs (one state-gradient CTA per SM), so CTAs walk several
+    units in turn, ragged spans included: the tensor-core pass against the tile kernel, and every
+    span bitwise the same alone as inside the batch."""
+    lengths = [0, 1, 63, 64, 65, 127, 128, 129, 191, 192, 0, 700, 255, 256, 257, 3, 511, 640,
+               130, 0, 65, 200, 1000, 64, 2, 450, 129, 320, 0, 190, 66, 777,
+               128, 1, 256, 380, 0, 193, 64, 900, 40, 129, 600, 192, 5, 333, 70, 128]
+    w = W.draw("sbwd many units", lengths, 4, 8, 64, 64, seed=561, slow_decay=True)
+    assert w.N * w.HV > torch.cuda.get_device_properties(0).multi_processor_count
+    do, dfin = cotangents(w, 562)
+    tc = run(w, do, dfin)
+    tile = run(w, do, dfin, passes=1)
+    e = rel(tc.cpu().numpy(), tile.cpu().numpy())
+    print(f"[parity] summary_bwd many units: tensor-core pass vs tile kernel {e:.2e}")
+    assert e <= F32_TOL
+    cu = w.cu_seqlens.numpy().astype(np.int64)
+    for i in (2, 11, 22, 39):
+        sl = slice(cu[i], cu[i + 1])
+        sub = W.Workload(name="one", cu_seqlens=torch.tensor([0, cu[i + 1] - cu[i]]), q=w.q[sl], k=w.k[sl], v=w.v[sl],
+                         g=w.g[sl].contiguous(), beta=w.beta[sl].contiguous())
+        alone = run(sub, do[sl], dfin[i:i + 1])
+        assert torch.equal(tc[i], alone[0]), i
