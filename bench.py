@@ -853,7 +853,7 @@ def run_summary_bench(args, world, rank, local):
 
 
 def run_table(args, world, rank, local):
-    """One line per workload of the survey's table: the forward on the tiny, varlen, dense-batch
+    """One line per configuration of the benchmark table: the forward on the tiny, varlen, dense-batch
     and skewed grouped-head workloads, and the summary on the span workload.  For each, the GPU
     call's and the fused kernel's time (CUDA events, mean over --steps after --warmup), tokens/s,
     the algorithmic bytes and FLOPs over the kernel time against the measured peaks, and the fp64

@@ -521,7 +521,7 @@ __global__ void __launch_bounds__(kCta, 2)
     const int HO = a.HV;
 
     // one read of the status word for the whole CTA (another CTA may set it meanwhile), and of
-    // the prologue's verdict on forward ranges
+    // the prologue's decision on forward ranges
     if (tid == 0) {
         sc.status0 = *reinterpret_cast<volatile int32_t*>(&a.hdr->status);
         sc.ranges_ok = a.hdr->ranges_ok;
@@ -1435,7 +1435,7 @@ static cudaError_t resident_per_sm(const void* fn, uint32_t smem, int cap, int d
 // 2..8 that minimises the estimated time, waves x (chunks per range + two chunks for a
 // launch's start and drain, as measured), against whole units (ceil(units / slots) waves of
 // `chunks`), from the mean sequence length.  1 when no count saves at least 5 %.  The kernel
-// still walks whole units when the lengths turn out spread (the prologue's verdict).
+// still walks whole units when the lengths turn out spread (the prologue's decision).
 static int fwd_pieces(int64_t units, int64_t slots, int64_t chunks) {
     if (chunks < 2) return 1;
     const double whole = static_cast<double>((units + slots - 1) / slots) * static_cast<double>(chunks);
