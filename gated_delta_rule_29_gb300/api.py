@@ -99,6 +99,16 @@ def split_workspace_bytes(T: int, N: int, HV: int) -> int:
     return int(B.load().la_gdn_fwd_split_workspace_bytes(int(T), int(N), int(HV)))
 
 
+def _workspace(preferred: int, minimum: int, dev: torch.device) -> torch.Tensor:
+    """A device workspace of `preferred` bytes (room for the two-pass schedules, about 272 bytes
+    per token and head), or of `minimum` bytes when that allocation fails: the library then takes
+    its single-kernel path, as it does for any smaller workspace."""
+    try:
+        return torch.empty(preferred, dtype=torch.uint8, device=dev)
+    except torch.cuda.OutOfMemoryError:
+        return torch.empty(minimum, dtype=torch.uint8, device=dev)
+
+
 def gdn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.Tensor,
             cu_seqlens: torch.Tensor, *, scale: Optional[float] = None, use_qk_l2norm: bool = True,
             initial_state: Optional[torch.Tensor] = None, output_final_state: bool = True,
@@ -165,7 +175,8 @@ def gdn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
         checkpoints = torch.empty(R, HO, K, V, dtype=checkpoint_dtype, device=dev)
     if workspace is None:
         need = split_workspace_bytes(T, N, HV) if n <= 1 else B.load().la_gdp_workspace_bytes(T, N, HK, HV, K, V, n)
-        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        # n > 64 needs its whole timeline workspace; otherwise the minimum is the prologue's tables
+        workspace = _workspace(need, workspace_bytes(N) if n <= 64 else need, dev)
     if initial_state is not None and state_indices is None:
         initial_state = initial_state.contiguous()
     p = B.GdnFwdParams()
@@ -222,7 +233,7 @@ def gdn_summary(k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, beta: torch.T
     if transition is None:
         transition = torch.empty(N, HO, K, K, dtype=torch.float32, device=dev)
     if workspace is None:
-        workspace = torch.empty(split_workspace_bytes(k.shape[0], N, v.shape[1]), dtype=torch.uint8, device=dev)
+        workspace = _workspace(split_workspace_bytes(k.shape[0], N, v.shape[1]), workspace_bytes(N, True), dev)
     if start_state is not None:
         start_state = start_state.contiguous()
     p = B.GdnSummaryParams()
@@ -360,8 +371,8 @@ def gdn_summary_bwd(q: torch.Tensor, k: torch.Tensor, g: torch.Tensor, beta: tor
     lib = B.load()
     if workspace is None:
         # room for the tensor-core path (the forward's WY records), else the tile kernel's minimum
-        need = max(int(lib.la_gdn_summary_bwd_workspace_bytes(N, HV, K, V)), split_workspace_bytes(q.shape[0], N, HV))
-        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        tile = int(lib.la_gdn_summary_bwd_workspace_bytes(N, HV, K, V))
+        workspace = _workspace(max(tile, split_workspace_bytes(q.shape[0], N, HV)), tile, dev)
     if d_final_state is not None:
         d_final_state = d_final_state.contiguous().float()
     p = B.GdnSummaryBwdParams()

@@ -227,3 +227,12 @@ def test_two_pass_gdp_equals_fused(n):
         finally:
             assert lib.la_test_set_fwd_passes(0) == 0
     same(outs[0], outs[1], f"GDP n={n}")
+
+
+def test_api_workspace_falls_back_when_the_two_pass_room_cannot_be_allocated():
+    """The wrappers allocate room for the two passes (about 272 bytes per token and head); when
+    that allocation fails they hand the library the minimal workspace, which takes the fused
+    kernel, instead of failing the call."""
+    d = dev()
+    ws = la.api._workspace(1 << 50, 4096, d)  # a petabyte: refused by the allocator, nothing launched
+    assert ws.numel() == 4096
