@@ -215,3 +215,20 @@ def test_summary_bwd_tensor_core_pass_many_units_per_cta():
                          g=w.g[sl].contiguous(), beta=w.beta[sl].contiguous())
         alone = run(sub, do[sl], dfin[i:i + 1])
         assert torch.equal(tc[i], alone[0]), i
+
+
+def test_summary_bwd_unaligned_d_o_takes_the_tile_kernel():
+    """d_o whose rows are not in 16-byte units cannot be read by TMA: the call takes the tile
+    kernel, with the tile kernel's exact result."""
+    w = W.draw("sbwd odd d_o", [70, 129], 2, 2, 64, 64, seed=571, slow_decay=True)
+    do, dfin = cotangents(w, 572)
+    d = dev()
+    wide = torch.zeros(w.T, w.HV, w.V + 1, dtype=torch.bfloat16)
+    wide[:, :, :w.V] = do
+    view = wide.to(d)[:, :, :w.V]  # row stride HV * (V + 1) elements: not a multiple of 8
+    assert view.stride(0) % 8 != 0
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    got = la.gdn_summary_bwd(w.q.to(d), w.k.to(d), w.g.to(d), w.beta.to(d), w.cu_seqlens.to(d), view,
+                             d_final_state=dfin.to(d), status=status)
+    assert la.read_status(status) == 0
+    assert torch.equal(got, run(w, do, dfin, passes=1))
