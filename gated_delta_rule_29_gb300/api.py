@@ -304,8 +304,8 @@ def gdn_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor, 
         if ck_n <= 0 or ck_n % 64 != 0:
             raise ValueError("checkpoint_every_n must be a positive multiple of 64")
     if workspace is None:
-        need = lib.la_gdn_bwd_workspace_bytes_ckpt(T, N, HK, HV, K, V, ck_n, int(ck_bf16))
-        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        workspace = _workspace(lib.la_gdn_bwd_workspace_bytes_ckpt(T, N, HK, HV, K, V, ck_n, int(ck_bf16)),
+                               lib.la_gdn_bwd_workspace_bytes_min(T, N, HK, HV, K, V, ck_n, int(ck_bf16)), dev)
     if initial_state is not None:
         initial_state = initial_state.contiguous()
     if d_final_state is not None:

@@ -46,6 +46,7 @@ EXPORTED_SYMBOLS = (
     "gdn_bwd",
     "la_gdn_bwd_workspace_bytes",
     "la_gdn_bwd_workspace_bytes_ckpt",
+    "la_gdn_bwd_workspace_bytes_min",
     "la_gdp_workspace_bytes",
     "gdn_summary_bwd",
     "la_gdn_summary_bwd_workspace_bytes",
@@ -154,6 +155,8 @@ def load(build_if_missing: bool = True):
         lib.la_gdn_bwd_workspace_bytes.argtypes = [_i64, _i32, _i32, _i32, _i32, _i32, _i32]
         lib.la_gdn_bwd_workspace_bytes_ckpt.restype = ctypes.c_size_t
         lib.la_gdn_bwd_workspace_bytes_ckpt.argtypes = [_i64, _i32, _i32, _i32, _i32, _i32, _i64, _i32]
+        lib.la_gdn_bwd_workspace_bytes_min.restype = ctypes.c_size_t
+        lib.la_gdn_bwd_workspace_bytes_min.argtypes = [_i64, _i32, _i32, _i32, _i32, _i32, _i64, _i32]
         lib.gdn_decode.restype = ctypes.c_int
         lib.gdn_decode.argtypes = [ctypes.POINTER(GdnDecodeParams), _vp]
         lib.gdn_summary.restype = ctypes.c_int

@@ -1077,6 +1077,19 @@ cudaError_t launch_bwd_kv(const BwdArgs& a0, cudaStream_t s) {
 
 }  // namespace
 
+cudaError_t launch_bwd_finish(const BwdArgs& a, cudaStream_t s) {
+    if (a.group > 1 && a.T > 0) {
+        gdn_bwd_group_sum_kernel<<<1024, 256, 0, s>>>(a);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    if (a.gpart) {
+        gdn_bwd_gate_param_kernel<<<(a.HV + 127) / 128, 128, 0, s>>>(a);
+        return cudaGetLastError();
+    }
+    return cudaSuccess;
+}
+
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t s) {
     if (a.K == 128) return a.V == 128 ? launch_bwd_kv<128, 128>(a, s) : launch_bwd_kv<128, 64>(a, s);
     return a.V == 128 ? launch_bwd_kv<64, 128>(a, s) : launch_bwd_kv<64, 64>(a, s);

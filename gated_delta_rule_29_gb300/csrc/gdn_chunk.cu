@@ -466,6 +466,31 @@ __device__ __forceinline__ void t_to_bf16(const float* Tf, uint8_t* TB, int tid)
     }
 }
 
+// The bf16 residual T - bf16(T) of the same tile (the lo part the full backward's products add),
+// in the 128-byte swizzled byte order of a [64][128 B] tile, so that a bulk copy into a
+// 1024-aligned buffer lands it as a swizzled TMA load would; into global memory at dst.
+__device__ __forceinline__ void t_lo_store(const float* Tf, uint8_t* dst, int tid) {
+    const int i = tid >> 1;
+#pragma unroll
+    for (int cc4 = 0; cc4 < 4; ++cc4) {
+        const int cc = (tid & 1) * 4 + cc4;
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if ((cc >> 1) <= (i >> 4)) {
+            const float4 lo4 = *reinterpret_cast<const float4*>(&Tf[midx(i, 8 * cc)]);
+            const float4 hi4 = *reinterpret_cast<const float4*>(&Tf[midx(i, 8 * cc + 4)]);
+            const float x[8] = {lo4.x, lo4.y, lo4.z, lo4.w, hi4.x, hi4.y, hi4.z, hi4.w};
+            uint32_t l[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t h = pack_bf16(x[2 * e], x[2 * e + 1]);
+                l[e] = pack_bf16(x[2 * e] - bf16_lo(h), x[2 * e + 1] - bf16_hi(h));
+            }
+            w = make_uint4(l[0], l[1], l[2], l[3]);
+        }
+        *reinterpret_cast<uint4*>(dst + sw128_off(static_cast<uint32_t>(i), static_cast<uint32_t>(cc))) = w;
+    }
+}
+
 // One WY record into shared memory, on bar_f: T (bf16, into TB's place), P (into PB; the
 // summary has none: PBdst null) and the factors beta, sx, sq, sd (into sc.bet .. sc.sd,
 // contiguous).  One thread.
@@ -1372,6 +1397,7 @@ __global__ void __launch_bounds__(kCta, 4)
         __syncthreads();  // A and P complete; the K/Q tile (read by the finished G product) becomes T's space
         solve_unit_lower(M, Tf, Y, tid);
         t_to_bf16(Tf, TB, tid);
+        if (a.wy_tlo) t_lo_store(Tf, a.wy_tlo + item * static_cast<int64_t>(kWyTileBytes), tid);
         fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0) {

@@ -26,7 +26,9 @@
 //   dS^T     += a^T K + b^T Q   A = a^T, b^T (hi, lo)   B = K, Q (MN-major), a = -sx dY, b = sq dO
 // The K/Q and dO tiles and the records arrive by TMA (128-byte swizzle), prefetched one chunk
 // ahead (in reverse order); the state gradient is pre-multiplied by the decay of the chunk it is
-// about to enter, so the update product accumulates onto it.  Every wait is bounded.
+// about to enter, so the update product accumulates onto it.  For the full backward (gdn_bwd) the
+// pass also stores the gradient leaving every chunk (its bf16 hi + lo copy, the layout the chunk
+// pass reads) and the gradient entering each sequence is d_initial_state.  Every wait is bounded.
 #include <cuda_bf16.h>
 
 #include "../../include/liblinattn.h"
@@ -182,7 +184,7 @@ __global__ void __launch_bounds__(kGT, 1)
                     const uint32_t off = (kc >> 3) * 16384 + sw128_off(r, kc & 7);
                     store8_split(WB + off, SLO + off, &x[8 * hh]);
                 }
-                if (nch == 0 && r < a.V) {
+                if (nch == 0 && r < a.V && a.final_state) {
 #pragma unroll
                     for (int e = 0; e < 16; ++e) a.final_state[base + static_cast<int64_t>(16 * p + e) * a.V] = x[e];
                 }
@@ -229,6 +231,14 @@ __global__ void __launch_bounds__(kGT, 1)
                 fence_proxy_async_smem();
                 tc_fence_before();
                 if (__syncthreads_or(!ok)) { failed = true; break; }
+            }
+            if (tid == 0 && ok && a.ds_chunks) {
+                // the full backward's chunk pass reads the gradient leaving this chunk: its bf16
+                // hi + lo copy goes out by bulk copy before the dD^T tiles take its place
+                const int64_t item = (a.chunk_off[seq] + c) * HO + h;
+                bulk_store(a.ds_chunks + item * 65536, WB, 32768u);
+                bulk_store(a.ds_chunks + item * 65536 + 32768, SLO, 32768u);
+                bulk_commit_group();
             }
             if (tid == 0 && ok) {
                 tc_fence_after();
@@ -296,6 +306,10 @@ __global__ void __launch_bounds__(kGT, 1)
                     pend_mma = false;
                 }
                 ok = ok && okm;
+            }
+            if (a.ds_chunks) {
+                if (tid == 0) bulk_wait_read_all();
+                __syncthreads();
             }
             tc_fence_after();
             {
@@ -436,7 +450,7 @@ __global__ void __launch_bounds__(kGT, 1)
                         if (p >= KP) break;
                         float* x = &s64[16 * pp];
                         if (last) {
-                            if (r < a.V) {
+                            if (r < a.V && a.final_state) {
 #pragma unroll
                                 for (int e = 0; e < 16; ++e) a.final_state[obase + static_cast<int64_t>(16 * p + e) * a.V] = x[e];
                             }
@@ -474,6 +488,7 @@ __global__ void __launch_bounds__(kGT, 1)
             if (a.user_status) atomicCAS(a.user_status, LA_OK, LA_ERR_TIMEOUT);
         }
     }
+    if (tid == 0 && a.ds_chunks) bulk_wait_all();
     tc_fence_before();
     __syncthreads();
     if (tid < 32) tmem_dealloc(tmem, G_TMEM);

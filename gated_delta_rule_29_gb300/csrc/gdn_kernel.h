@@ -158,6 +158,11 @@ struct ChunkArgs {
     const int64_t* chunk_off;
     const int32_t* chunk_seq;
     uint8_t* wy;
+    // the state-gradient pass of gdn_bwd: the gradient of the state leaving every chunk, per
+    // (chunk, head) item, as the bf16 hi and lo parts of dS^T [2][128 rows][128 B] (64 KB), or null
+    uint8_t* ds_chunks;
+    // the WY pass for gdn_bwd also writes T's bf16 residual per item (8 KB, swizzled), or null
+    uint8_t* wy_tlo;
 };
 
 // One recurrence step per sequence against a state pool (gdn_decode).
@@ -213,6 +218,8 @@ struct BwdArgs {
     float* dkh;
     int32_t vec_out;                 // dq, dk rows 16-byte aligned: 16-byte stores
     int32_t vo_async;                // v, dO pairs 4-byte aligned: asynchronous 4-byte copies
+    int32_t out_tma;                 // dq, dk, dv rows 16-byte aligned with strides in 16-byte units:
+                                     // the tensor-core pass stores full chunks by TMA
     int32_t state_only;              // only the entering-state gradient (gdn_summary_bwd): no
                                      // checkpoints, v, dq, dk, dv, dg, dbeta
     // input transforms as in the forward; dg, dbeta then refer to the raw inputs
@@ -281,6 +288,9 @@ cudaError_t launch_gdp_expand(const GdpArgs& a, cudaStream_t s);
 cudaError_t launch_gdp_gather(const GdpArgs& a, cudaStream_t s);
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_bwd(const BwdArgs& a, cudaStream_t s);
+// After the chunk-parallel gradient pass: the sums over grouped value heads (dqh, dkh -> dq, dk)
+// and the gate-parameter sums (gpart, N x HV x pieces slots, added in slot order).
+cudaError_t launch_bwd_finish(const BwdArgs& a, cudaStream_t s);
 cudaError_t launch_prologue(const PrologueArgs& a, cudaStream_t s);
 // Composition of span summaries (gdn_compose_spans): out [R + 1, HO, K, V].
 struct ComposeArgs {
@@ -299,6 +309,13 @@ cudaError_t launch_compose(const ComposeArgs& a, cudaStream_t s);
 // span or null, a.final_state: the gradient entering it; domap: dO as [T][HV][V] bf16).
 cudaError_t launch_grad(const ChunkArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
                         const CUtensorMap& domap, const CUtensorMap& wymap, cudaStream_t s);
+// The chunk-parallel gradient pass of gdn_bwd (K = V = 128): per (chunk, head) item, from the
+// entering state (bw.ckpt, fp32 at the chunk cadence), the stored leaving-state gradient
+// (a.ds_chunks), the WY record and T's residual (a.wy_tlo), the gradients dq, dk (or the per-value-head dqh, dkh), dv,
+// dg, dbeta and the per-item gate-parameter sums (bw.gpart, slot head * bw.pieces + chunk).
+cudaError_t launch_dchunk(const ChunkArgs& a, const BwdArgs& bw, const CUtensorMap& qmap, const CUtensorMap& kmap,
+                          const CUtensorMap& domap, const CUtensorMap& wymap, const CUtensorMap& dkmap,
+                          const CUtensorMap& dqmap, const CUtensorMap& dvmap, cudaStream_t s);
 enum WyKind : int { kWyFwd = 0, kWySummary = 1, kWyGdp = 2 };
 cudaError_t launch_wy_kernel(const ChunkArgs& a, const CUtensorMap& qmap, const CUtensorMap& kmap,
                              const CUtensorMap& wymap, int kind, cudaStream_t s);

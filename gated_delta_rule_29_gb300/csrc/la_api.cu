@@ -580,6 +580,9 @@ int64_t max_segments(int64_t T, int32_t N, int64_t n) { return (T + n - 1) / n +
 
 struct BwdLayout {
     size_t pro, ck, o, ds, gh, gp, pro_n, pro_seg, cu_seg, s0_seg, total;
+    // the tensor-core path (K = V = 128) after the rest: the split layout's prologue area, chunk
+    // numbering and WY records, the gradient leaving every (chunk, head), per-item gate sums
+    size_t tc_split, tc_ds, tc_tlo, tc_gp, total_tc;
 };
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 BwdLayout bwd_layout(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, int32_t V, int mode, int64_t n = 0) {
@@ -610,8 +613,20 @@ BwdLayout bwd_layout(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, in
         off += up256(static_cast<size_t>(S) * HV * K * V * sizeof(float));
     }
     L.total = off;
+    const la::SplitLayout GL = la::split_layout(T, N, HV);
+    L.tc_split = off;
+    off += up256(GL.total);
+    L.tc_ds = off;
+    off += up256(static_cast<size_t>(GL.items) * 65536);
+    L.tc_tlo = off;
+    off += up256(static_cast<size_t>(GL.items) * la::kWyTileBytes);
+    L.tc_gp = off;
+    off += up256(2 * static_cast<size_t>(HV) * static_cast<size_t>(GL.chunks) * sizeof(float));
+    L.total_tc = off;
     return L;
 }
+// the full backward runs on the tensor cores for K = V = 128 (else the tile kernel)
+bool bwd_tc_shape(int32_t K, int32_t V) { return K == 128 && V == 128; }
 // gdn_summary_bwd: the prologue's area, then the carried state gradient of every (sequence, head).
 struct SumBwdLayout {
     size_t pro, ds, total;
@@ -635,11 +650,127 @@ size_t la_gdn_summary_bwd_workspace_bytes(int32_t N, int32_t HV, int32_t K, int3
 size_t la_gdn_bwd_workspace_bytes(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, int32_t V,
                                   int32_t checkpoints_given) {
     if (T < 0 || N < 0 || HK <= 0 || HV <= 0) return 0;
-    return bwd_layout(T, N, HK, HV, K, V, checkpoints_given != 0 ? kCkDirect : kCkNone).total;
+    const BwdLayout L = bwd_layout(T, N, HK, HV, K, V, checkpoints_given != 0 ? kCkDirect : kCkNone);
+    return bwd_tc_shape(K, V) ? L.total_tc : L.total;
 }
 
 size_t la_gdn_bwd_workspace_bytes_ckpt(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, int32_t V,
                                        int64_t checkpoint_every_n, int32_t checkpoint_bf16) {
+    if (T < 0 || N < 0 || HK <= 0 || HV <= 0 || checkpoint_every_n < 0 || checkpoint_every_n % la::kChunk != 0)
+        return 0;
+    const int mode = bwd_ckpt_mode(checkpoint_every_n > 0, checkpoint_every_n, checkpoint_bf16 != 0);
+    const BwdLayout L = bwd_layout(T, N, HK, HV, K, V, mode, checkpoint_every_n);
+    return bwd_tc_shape(K, V) ? L.total_tc : L.total;
+}
+
+}  // extern "C"
+
+namespace {
+// gdn_bwd on the tensor cores (K = V = 128), once the states entering every chunk are in
+// b.ckpt: the prologue (chunk numbering), the forward's WY pass over every (chunk, head), the
+// state-gradient pass (the gradient leaving every chunk into the workspace, d_initial_state),
+// the chunk-parallel gradient pass, then the grouped-head and gate-parameter sums.
+la_status bwd_tensor_path(const la_gdn_bwd_params* p, const BwdLayout& BL, uint8_t* wb, la::BwdArgs b,
+                          cudaStream_t s) {
+    la_status st;
+    const la::SplitLayout GL = la::split_layout(p->T, p->N, p->HV);
+    uint8_t* gw = wb + BL.tc_split;
+    const la::WorkspaceLayout PL = la::ws_layout(p->N);
+    PrologueArgs pa;
+    pa.cu = p->cu_seqlens;
+    pa.chunk_off = reinterpret_cast<int64_t*>(gw + GL.chunk_off);
+    pa.chunk_seq = reinterpret_cast<int32_t*>(gw + GL.chunk_seq);
+    pa.chunk_rows = 1;
+    pa.cu64 = p->cu_seqlens_bits == 64;
+    pa.T = p->T;
+    pa.N = p->N;
+    pa.ckpt_n = 0;
+    pa.hdr = reinterpret_cast<la::WsHeader*>(gw);
+    pa.order = reinterpret_cast<int32_t*>(gw + PL.order);
+    pa.ckpt_off = reinterpret_cast<int64_t*>(gw + PL.ckpt_off);
+    pa.keys = reinterpret_cast<uint64_t*>(gw + PL.keys);
+    pa.user_status = p->status;
+    if (la::launch_prologue(pa, s) != cudaSuccess) return LA_ERR_CUDA;
+
+    ChunkArgs ka;
+    std::memset(&ka, 0, sizeof(ka));
+    if ((st = set_transforms(ka, p->gate_mode, p->a_log, p->dt_bias, p->gate_lower_bound, p->beta_sigmoid,
+                             p->beta_bf16)) != LA_OK)
+        return st;
+    ka.g = p->g;
+    ka.g_st = p->g_stride_t;
+    ka.g_sh = p->g_stride_h;
+    ka.beta = p->beta;
+    ka.b_st = p->beta_stride_t;
+    ka.b_sh = p->beta_stride_h;
+    ka.cu = p->cu_seqlens;
+    ka.cu64 = p->cu_seqlens_bits == 64;
+    ka.T = p->T;
+    ka.N = p->N;
+    ka.HK = p->HK;
+    ka.HV = p->HV;
+    ka.K = p->K;
+    ka.V = p->V;
+    ka.group = p->HV / p->HK;
+    ka.scale = b.scale;
+    ka.l2norm = p->use_qk_l2norm != 0;
+    ka.s0 = p->d_final_state;
+    ka.final_state = p->d_initial_state;
+    ka.tiles_per_head = 1;
+    ka.num_units = static_cast<int64_t>(p->N) * p->HV;
+    ka.hdr = pa.hdr;
+    ka.order = pa.order;
+    ka.ckpt_off = pa.ckpt_off;
+    ka.chunk_off = pa.chunk_off;
+    ka.chunk_seq = pa.chunk_seq;
+    ka.wy = gw + GL.wy;
+    ka.ds_chunks = wb + BL.tc_ds;
+    ka.user_status = p->status;
+    ka.wait_budget_ns = kWaitBudgetNs;
+    ka.gdp_n = 1;
+    if (const uint64_t wb_ns = g_test_wait_budget_ns.load(std::memory_order_relaxed)) ka.wait_budget_ns = wb_ns;
+
+    CUtensorMap qm, km, dom, wm;
+    if ((st = make_map(&km, p->k, p->T, p->HK, p->K, p->k_stride_t, p->k_stride_h)) != LA_OK) return st;
+    if ((st = make_map(&qm, p->q, p->T, p->HK, p->K, p->q_stride_t, p->q_stride_h)) != LA_OK) return st;
+    if ((st = make_map(&dom, p->d_o, p->T, p->HV, p->V, p->d_o_stride_t, p->d_o_stride_h)) != LA_OK) return st;
+    if ((st = make_map(&wm, ka.wy, 136, GL.items, 64, 64, static_cast<int64_t>(la::kWyRecordBytes / 2))) != LA_OK)
+        return st;
+    // per-item gate-parameter sums: slot (head, chunk) over the chunk bound, unused slots zero
+    b.N = 1;
+    b.pieces = static_cast<int32_t>(GL.chunks);
+    if (b.gpart) {
+        b.gpart = reinterpret_cast<float*>(wb + BL.tc_gp);
+        if (cudaMemsetAsync(b.gpart, 0, 2 * static_cast<size_t>(p->HV) * GL.chunks * sizeof(float), s) != cudaSuccess)
+            return LA_ERR_CUDA;
+    }
+    ka.wy_tlo = wb + BL.tc_tlo;
+    // full chunks of dq, dk, dv leave by TMA when the output rows allow it
+    b.out_tma = b.vec_out && aligned(p->dv, 16) && p->dv_stride_t % 8 == 0 && (p->HV == 1 || p->dv_stride_h % 8 == 0);
+    CUtensorMap dkm, dqm, dvm;
+    std::memset(&dkm, 0, sizeof(dkm));
+    std::memset(&dqm, 0, sizeof(dqm));
+    std::memset(&dvm, 0, sizeof(dvm));
+    if (b.out_tma && (make_map(&dkm, p->dk, p->T, p->HK, p->K, p->dk_stride_t, p->dk_stride_h) != LA_OK ||
+                      make_map(&dqm, p->dq, p->T, p->HK, p->K, p->dq_stride_t, p->dq_stride_h) != LA_OK ||
+                      make_map(&dvm, p->dv, p->T, p->HV, p->V, p->dv_stride_t, p->dv_stride_h) != LA_OK))
+        b.out_tma = 0;  // (per-thread stores then)
+    ChunkArgs kw = ka;
+    kw.num_units = GL.items;  // the bound on (chunk, head) items
+    if (la::launch_wy_kernel(kw, qm, km, wm, la::kWyFwd, s) != cudaSuccess) return LA_ERR_CUDA;
+    if (la::launch_grad(ka, qm, km, dom, wm, s) != cudaSuccess) return LA_ERR_CUDA;
+    ChunkArgs kd = ka;
+    kd.items = GL.items;
+    if (la::launch_dchunk(kd, b, qm, km, dom, wm, dkm, dqm, dvm, s) != cudaSuccess) return LA_ERR_CUDA;
+    if (la::launch_bwd_finish(b, s) != cudaSuccess) return LA_ERR_CUDA;
+    return LA_OK;
+}
+}  // namespace
+
+extern "C" {
+
+size_t la_gdn_bwd_workspace_bytes_min(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, int32_t V,
+                                      int64_t checkpoint_every_n, int32_t checkpoint_bf16) {
     if (T < 0 || N < 0 || HK <= 0 || HV <= 0 || checkpoint_every_n < 0 || checkpoint_every_n % la::kChunk != 0)
         return 0;
     const int mode = bwd_ckpt_mode(checkpoint_every_n > 0, checkpoint_every_n, checkpoint_bf16 != 0);
@@ -679,11 +810,21 @@ la_status gdn_bwd(const la_gdn_bwd_params* p, void* stream) {
     const int mode = bwd_ckpt_mode(p->checkpoints != nullptr, p->checkpoint_every_n, ck_bf16);
     const int64_t ck_n = mode == kCkSegments ? p->checkpoint_every_n : la::kChunk;
     const BwdLayout BL = bwd_layout(p->T, p->N, p->HK, p->HV, p->K, p->V, mode, ck_n);
+    // the tensor-core path when the shapes, the d_o operand (TMA) and the workspace allow it
+    const la::SplitLayout GLb = la::split_layout(p->T, p->N, p->HV);
+    bool tc = g_test_fwd_passes.load(std::memory_order_relaxed) != 1 && p->T > 0 && bwd_tc_shape(p->K, p->V) &&
+              GLb.items < (int64_t(1) << 31) && aligned(p->d_o, 16) && p->d_o_stride_t % 8 == 0 &&
+              (p->HV == 1 || p->d_o_stride_h % 8 == 0);
     void* ws = p->workspace;
     if (ws) {
         if (p->workspace_bytes < BL.total || !aligned(ws, 256)) return LA_ERR_WORKSPACE;
-    } else if ((st = internal_workspace(BL.total, static_cast<cudaStream_t>(stream), &ws)) != LA_OK) {
-        return st;
+        tc = tc && p->workspace_bytes >= BL.total_tc;
+    } else {
+        if (tc && internal_workspace(BL.total_tc, static_cast<cudaStream_t>(stream), &ws) != LA_OK) {
+            tc = false;
+            ws = nullptr;
+        }
+        if (!ws && (st = internal_workspace(BL.total, static_cast<cudaStream_t>(stream), &ws)) != LA_OK) return st;
     }
     uint8_t* wb = static_cast<uint8_t*>(ws);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -815,10 +956,15 @@ la_status gdn_bwd(const la_gdn_bwd_params* p, void* stream) {
         b.d_a_log = p->d_a_log;
         b.d_dt_bias = p->d_dt_bias;
     }
+    tc = tc && aligned(ck, 16);  // the states arrive by bulk copy
     cudaEvent_t ev0 = t_timing_start, ev1 = t_timing_stop;
     t_timing_start = t_timing_stop = nullptr;
     if (ev0 && cudaEventRecord(ev0, s) != cudaSuccess) return LA_ERR_CUDA;
-    if (la::launch_bwd(b, s) != cudaSuccess) return LA_ERR_CUDA;
+    if (tc) {
+        if ((st = bwd_tensor_path(p, BL, wb, b, s)) != LA_OK) return st;
+    } else if (la::launch_bwd(b, s) != cudaSuccess) {
+        return LA_ERR_CUDA;
+    }
     if (ev1 && cudaEventRecord(ev1, s) != cudaSuccess) return LA_ERR_CUDA;
     return LA_OK;
 }

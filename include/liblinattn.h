@@ -416,7 +416,8 @@ typedef struct la_gdn_bwd_params {
     float* dg;        int64_t dg_stride_t, dg_stride_h;     /* [T, HO] fp32 */
     float* dbeta;     int64_t dbeta_stride_t, dbeta_stride_h; /* [T, HO] fp32 */
     float* d_initial_state;      /* [N, HO, K, V] fp32 or NULL */
-    void* workspace;             /* >= la_gdn_bwd_workspace_bytes(...), 256-byte aligned, or NULL */
+    void* workspace;             /* >= la_gdn_bwd_workspace_bytes_min(...), 256-byte aligned, or NULL
+                                    (then a per-device buffer, the tensor-core size when possible) */
     size_t workspace_bytes;
     int32_t* status;
     /* ---- optional input transforms, as in gdn_fwd (zero-initialised: none) ---- */
@@ -449,11 +450,22 @@ typedef struct la_gdn_bwd_params {
  *     (independent, so they run side by side) regenerates the states entering every chunk.
  *     From fp32 rows these are bitwise the states the full forward produced;
  *   - no rows: the library re-runs the forward with fp32 checkpoints every 64 tokens.
- * Each
- * (sequence, head) runs in a fixed order, so results do not depend on the batch around a
- * sequence.  When the (sequence, head) units outnumber the CTAs the GPU holds at once, the
- * call enqueues several launches that walk each unit in four chunk ranges, the state gradient
- * handed from range to range exactly (the same bits as one walk).  With gdn_fwd's input
+ * Two schedules, the same mathematics:
+ *   - tensor cores (K = V = 128, d_o 16-byte aligned with strides in 8-element units, fp32
+ *     states 16-byte aligned, and a workspace of la_gdn_bwd_workspace_bytes_ckpt): the
+ *     forward's WY pass over every (chunk, head), which also keeps T's bf16 residual; the
+ *     state-gradient pass (as gdn_summary_bwd's), which walks each (sequence, head) backwards
+ *     and stores the gradient leaving every chunk; then a chunk-parallel pass that forms every
+ *     (chunk, head)'s gradients from its entering state, that stored gradient and its WY
+ *     record with tcgen05 products (bf16 hi + lo splits where fp32 gradients depend on them).
+ *     Full chunks of dq, dk, dv leave by TMA when their rows are 16-byte aligned;
+ *   - otherwise (other head sizes, a workspace of at least la_gdn_bwd_workspace_bytes_min but
+ *     less than the above) the tile kernel: one CTA per (sequence, head) walks the chunks in
+ *     reverse with warp-level tensor-core MMAs, in four chunk ranges launched one after the
+ *     other when the units outnumber the CTAs the GPU holds at once (the state gradient handed
+ *     from range to range exactly, the same bits as one walk).
+ * Every (sequence, head) runs in a fixed order on either schedule, so results do not depend on
+ * the batch around a sequence.  With gdn_fwd's input
  * transforms (cudnn-frontend PR #616 fusions) dg and dbeta are the gradients of the raw inputs
  * (the gate input, the beta logits), and the softplus gate also gives d_a_log and d_dt_bias,
  * summed over the batch in a fixed order (deterministic).
@@ -461,14 +473,22 @@ typedef struct la_gdn_bwd_params {
 la_status gdn_bwd(const la_gdn_bwd_params* p, void* stream);
 
 /* Bytes of device workspace gdn_bwd needs (checkpoints_given = 0 when they are regenerated,
-   1 for fp32 rows every 64 tokens). */
+   1 for fp32 rows every 64 tokens), with room for the tensor-core schedule when K = V = 128. */
 size_t la_gdn_bwd_workspace_bytes(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, int32_t V,
                                   int32_t checkpoints_given);
 
 /* Bytes of device workspace gdn_bwd needs with given checkpoint rows every checkpoint_every_n
-   tokens (0: none given), fp32 or bf16 (checkpoint_bf16). */
+   tokens (0: none given), fp32 or bf16 (checkpoint_bf16): room for the tensor-core schedule
+   when K = V = 128 (the split layout's WY records, T's residual and the gradient leaving every
+   (chunk, head), about 90 KB per chunk and head more than the tile kernel needs). */
 size_t la_gdn_bwd_workspace_bytes_ckpt(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, int32_t V,
                                        int64_t checkpoint_every_n, int32_t checkpoint_bf16);
+
+/* The least workspace gdn_bwd accepts for the same call: the tile kernel's (a smaller one
+   gives LA_ERR_WORKSPACE; one between this and la_gdn_bwd_workspace_bytes_ckpt selects the
+   tile kernel).  0 for invalid arguments. */
+size_t la_gdn_bwd_workspace_bytes_min(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, int32_t V,
+                                      int64_t checkpoint_every_n, int32_t checkpoint_bf16);
 
 /* Parameters of gdn_summary_bwd.  Strides are in elements. */
 typedef struct la_gdn_summary_bwd_params {

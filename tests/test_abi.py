@@ -313,6 +313,21 @@ def test_bwd_workspace_bytes_by_checkpoint_kind():
     assert lib.la_gdn_bwd_workspace_bytes_ckpt(*args, 100, 0) == 0
 
 
+def test_bwd_workspace_min_is_the_tile_kernels():
+    """K = V = 128: the default size adds the tensor-core schedule's areas (the WY records, T's
+    residual and the gradient leaving every (chunk, head)) to the tile kernel's minimum; other
+    head sizes have the tile kernel only, so the two sizes agree."""
+    lib = B.load()
+    for ck in ((0, 0), (64, 0), (64, 1), (1024, 0)):
+        args = (65536, 8, 32, 32, 128, 128, *ck)
+        full, least = lib.la_gdn_bwd_workspace_bytes_ckpt(*args), lib.la_gdn_bwd_workspace_bytes_min(*args)
+        items = (65536 // 64 + 8) * 32
+        assert least > 0 and full - least >= items * (17408 + 8192 + 65536)
+        small = (65536, 8, 32, 32, 64, 64, *ck)
+        assert lib.la_gdn_bwd_workspace_bytes_ckpt(*small) == lib.la_gdn_bwd_workspace_bytes_min(*small) > 0
+    assert lib.la_gdn_bwd_workspace_bytes_min(65536, 8, 32, 32, 128, 128, 100, 0) == 0
+
+
 def _compose(**over):
     p = B.GdnComposeParams()
     p.R, p.HO, p.K, p.V = 3, 2, 128, 64

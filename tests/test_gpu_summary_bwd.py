@@ -98,17 +98,26 @@ def test_summary_bwd_without_l2norm():
 
 
 def test_summary_bwd_equals_backward_state_gradient_bitwise():
-    """The tile kernel's state-only mode is bitwise the entering-state gradient of the full
-    backward (same recursion, same kernel); the tensor-core pass agrees with both to fp32-level
-    tolerance."""
+    """Each path of gdn_summary_bwd is bitwise the entering-state gradient of the full backward
+    on the same path (the tile kernel's state-only mode and the tile backward; the state-gradient
+    pass, which the tensor-core backward runs too); the two paths agree to fp32-level tolerance."""
     w = W.draw("sbwd vs bwd", [130, 64, 257], 2, 2, 128, 128, seed=531, initial_state=True, slow_decay=True)
     do, dfin = cotangents(w, 532)
     d = dev()
+    lib = la.binding.load()
+
+    def full_bwd(passes):
+        assert lib.la_test_set_fwd_passes(passes) == 0
+        try:
+            return la.gdn_bwd(w.q.to(d), w.k.to(d), w.v.to(d), w.g.to(d), w.beta.to(d), w.cu_seqlens.to(d),
+                              do.to(d), initial_state=w.initial_state.to(d), d_final_state=dfin.to(d))[5]
+        finally:
+            assert lib.la_test_set_fwd_passes(0) == 0
+
     a = run(w, do, dfin, passes=1)
-    b = la.gdn_bwd(w.q.to(d), w.k.to(d), w.v.to(d), w.g.to(d), w.beta.to(d), w.cu_seqlens.to(d), do.to(d),
-                   initial_state=w.initial_state.to(d), d_final_state=dfin.to(d))[5]
-    assert torch.equal(a, b)
+    assert torch.equal(a, full_bwd(1))
     c = run(w, do, dfin)
+    assert torch.equal(c, full_bwd(0))
     e = rel(c.cpu().numpy(), a.cpu().numpy())
     print(f"[parity] summary_bwd tensor-core pass vs tile kernel: {e:.2e}")
     assert e <= F32_TOL
