@@ -41,6 +41,7 @@ namespace la {
 namespace {
 
 constexpr int kDT = 512;  // threads
+constexpr int kIo = 64;   // the thread that issues the copies (not in the gate-scan warps; thread 0 issues the products)
 constexpr float kLog2eD = 1.4426950408889634f;
 
 // Shared memory (byte offsets from the 1024-aligned base).  Phase by phase a region is reused
@@ -78,10 +79,10 @@ constexpr uint32_t T_DT = 192;   // D^T
 constexpr uint32_t T_ET = 256;   // (P^T dO)^T
 constexpr uint32_t T_DY = 320;   // dX^T
 constexpr uint32_t T_G = 384;    // G = [K; Q] [K; Q]^T (token rows)
-constexpr uint32_t T_DKQ = 0;    // [dk~ | dq~]^T (key rows), 128 columns
+constexpr uint32_t T_DKQ = 0;    // [dk~ ; dq~] (token rows: dk~ 0-63, dq~ 64-127), 128 columns
 constexpr uint32_t T_DAP = 128;  // [dX D^T ; dO D^T] (token rows)
 constexpr uint32_t T_DAP2 = 192; // dX_lo D_hi^T (rows 0-63)
-constexpr uint32_t T_ACC2 = 256; // (D dS'^T)^T (key rows)
+constexpr uint32_t T_ACC2 = 384; // D dS'^T (token rows 0-63; after G is read)
 constexpr uint32_t T_COLS = 512;
 
 struct __align__(16) DcScalars {
@@ -94,11 +95,11 @@ struct __align__(16) DcScalars {
     float psb[4][64], psg[4][64], pso[4][64], pw[4][64];  // per lane-quadrant sums over values
     float rowA[4][64], rowP[4][64], sbA[4][64];           // per column-group row sums
     float colA[2][64], colP[2][64];                       // per row-quadrant column sums
-    float dots[2][4][64];                                 // norm backward: k . dk~, q . dq~
+    float pdot[4][128];                                   // norm backward: partial k . dk~, q . dq~
     float db[64];
     float gp[4];
     float red[16];
-    uint64_t bar_in, bar_pre, bar_mma;
+    uint64_t bar_in, bar_pre, bar_mma, bar_mma2;
     uint32_t tmem_base;
     int32_t status0;
 };
@@ -232,6 +233,7 @@ __global__ void __launch_bounds__(kDT, 1)
         mbar_init(&sc.bar_in, 1);
         mbar_init(&sc.bar_pre, 1);
         mbar_init(&sc.bar_mma, 1);
+        mbar_init(&sc.bar_mma2, 1);
         fence_mbar_init();
     }
     tc_fence_before();
@@ -262,7 +264,7 @@ __global__ void __launch_bounds__(kDT, 1)
     const uint64_t d_ax_mn = sdesc_sw128(smem_u32(DSTLO + 16384), 16384, 1024);  // [dX hi ; dO (TLO)] MN-major
     const uint64_t d_axlo_mn = sdesc_sw128(smem_u32(DSTLO), 16384, 1024);        // [dX lo ; dX hi]
     const uint64_t d_w_mn = sdesc_sw128(smem_u32(TB), 16384, 1024);       // W = [-sx dX | sq dO]^T
-    const uint64_t d_af = sdesc_sw128(smem_u32(STLO), 16, 1024);          // A_full^T, K-major
+    const uint64_t d_af = sdesc_sw128(smem_u32(TB), 16, 1024);            // A_full (rows t_out), K-major
     const uint64_t budget = a.wait_budget_ns;
     // K and Q, dO, T hi (TMA), T lo, the factors (bulk); then S (fp32) and dS' (bulk)
     const uint32_t in_bytes = 2u * 16384u + 2u * 8192u + 2u * static_cast<uint32_t>(kWyTileBytes) +
@@ -270,8 +272,8 @@ __global__ void __launch_bounds__(kDT, 1)
     constexpr uint32_t kPreBytes = 2u * 65536u;
 
     const int64_t total_items = a.chunk_off[a.N] * HO;
-    uint32_t ph_in = 0, ph_pre = 0, ph_mma = 0;
-    bool pend_in = false, pend_pre = false, pend_mma = false, failed = false;
+    uint32_t ph_in = 0, ph_pre = 0, ph_mma = 0, ph_mma2 = 0;
+    bool pend_in = false, pend_pre = false, pend_mma = false, pend_mma2 = false, failed = false;
     bool prefetched = false;  // this item's S and dS' were requested during the previous item
     // S (fp32, into ST..STLO) and dS' (into DST..DSTLO) of an item, on bar_pre.  One thread.
     auto load_states = [&](int64_t it) {
@@ -290,16 +292,36 @@ __global__ void __launch_bounds__(kDT, 1)
         tc_fence_after();
     };
 
+    // an item's first token and length, and (threads 0-63) its token's gate after the transform;
+    // read one item ahead, so that these dependent global loads stay off the item's path
+    int64_t nt0 = 0;
+    int nn = 0;
+    float ngt = 0.f;
+    auto item_meta = [&](int64_t it) {
+        const int64_t chunk_ = it / HO;
+        const int h_ = static_cast<int>(it % HO);
+        const int seq_ = a.chunk_seq[chunk_];
+        const int64_t c_ = chunk_ - a.chunk_off[seq_];
+        const int64_t ts_ = cu_get(a.cu, a.cu64, seq_);
+        const int64_t L_ = cu_get(a.cu, a.cu64, seq_ + 1) - ts_;
+        nt0 = ts_ + c_ * kChunk;
+        nn = static_cast<int>(L_ - c_ * kChunk < kChunk ? L_ - c_ * kChunk : kChunk);
+        float gA_ = 0.f, gdt_ = 0.f;
+        if (a.gate_mode == LA_GATE_SOFTPLUS) {
+            gA_ = -expf(a.a_log[h_]);
+            gdt_ = a.dt_bias[h_];
+        }
+        ngt = (tid < 64 && tid < nn) ? gate_at(a, nt0 + tid, h_, gA_, gdt_) : 0.f;
+    };
+    if (static_cast<int64_t>(blockIdx.x) < total_items) item_meta(blockIdx.x);
+
     for (int64_t item = blockIdx.x; item < total_items; item += gridDim.x) {
         const int64_t chunk = item / HO;
         const int h = static_cast<int>(item % HO);
         const int hk = h / a.group;
-        const int seq = a.chunk_seq[chunk];
-        const int64_t c = chunk - a.chunk_off[seq];
-        const int64_t tok_s = cu_get(a.cu, a.cu64, seq);
-        const int64_t L = cu_get(a.cu, a.cu64, seq + 1) - tok_s;
-        const int64_t t0 = tok_s + c * kChunk;
-        const int n = static_cast<int>(L - c * kChunk < kChunk ? L - c * kChunk : kChunk);
+        const int64_t t0 = nt0;
+        const int n = nn;
+        const float gt_mine = ngt;
         float gAh = 0.f, gdt = 0.f;
         if (a.gate_mode == LA_GATE_SOFTPLUS) {
             gAh = -expf(a.a_log[h]);
@@ -307,7 +329,7 @@ __global__ void __launch_bounds__(kDT, 1)
         }
 
         // ---- P0: tiles, T, factors and dS' by TMA / bulk copy; S^T hi + lo from the fp32 state
-        if (tid == 0) {
+        if (tid == kIo) {
             if (!prefetched) load_states(item);
             bulk_wait_read_all();  // the previous item's output tiles have left their staging buffers
             mbar_arrive_expect_tx(&sc.bar_in, in_bytes);
@@ -334,7 +356,7 @@ __global__ void __launch_bounds__(kDT, 1)
         }
         if (tid < 64) {
             // gates: per-warp inclusive scans of g * log2(e) (rows past the end carry 0)
-            const float gt = tid < n ? gate_at(a, t0 + tid, h, gAh, gdt) : 0.f;
+            const float gt = gt_mine;
             float x = gt * kLog2eD;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -442,11 +464,15 @@ __global__ void __launch_bounds__(kDT, 1)
             tmem_ld16(trow + T_G + 16 * cg, gq);
             tmem_wait_ld();
             const float ci = a.scale * sc.rq[i], bi = sc.b[i];
-            float pv[16];
+            float pv[16], bj[16], rkj[16];
+            ld8(bj, &sc.b[16 * cg]);
+            ld8(bj + 8, &sc.b[16 * cg + 8]);
+            ld8(rkj, &sc.rk[16 * cg]);
+            ld8(rkj + 8, &sc.rk[16 * cg + 8]);
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
                 const int j = 16 * cg + e;
-                pv[e] = (i < n && j <= i) ? ci * sc.rk[j] * gq[e] * exp2f(bi - sc.b[j]) : 0.f;
+                pv[e] = (i < n && j <= i) ? ci * rkj[e] * gq[e] * exp2f(bi - bj[e]) : 0.f;
             }
 #pragma unroll
             for (int c2 = 0; c2 < 2; ++c2) {
@@ -605,16 +631,14 @@ __global__ void __launch_bounds__(kDT, 1)
             for (int kk = 0; kk < 8; ++kk) umma_bf16(tmem + T_DAP, d_ax_mn + moff(kk), d_dt_mn + dlo + moff(kk), imn, 1u);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) umma_bf16(tmem + T_DAP2, d_axlo_mn + moff(kk), d_dt_mn + moff(kk), imn, kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) umma_bf16(tmem + T_ACC2, d_ds_mn + moff(kk), d_dt_mn + moff(kk), imn, kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) umma_bf16(tmem + T_ACC2, d_ds_mn + moff(kk), d_dt_mn + dlo + moff(kk), imn, 1u);
+            umma_commit(&sc.bar_mma);  // dA / dP: the token-row phase starts while the rest runs
+            // [dk~ ; dq~] = W^T S^T: token rows (A = W, MN-major), key columns (B = S^T, MN-major)
             const uint32_t ikq = idesc_bf16_f32(128, 128, true, true);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) umma_bf16(tmem + T_DKQ, d_s_mn + moff(kk), d_w_mn + moff(kk), ikq, kk > 0);
-            umma_commit(&sc.bar_mma);
+            for (int kk = 0; kk < 8; ++kk) umma_bf16(tmem + T_DKQ, d_w_mn + moff(kk), d_s_mn + moff(kk), ikq, kk > 0);
+            umma_commit(&sc.bar_mma2);
         }
-        pend_mma = true;
+        pend_mma = pend_mma2 = true;
         wait_mma(ok);
 
         // ---- P5 (token rows): dA, dP with A, P recomputed from G; dbeta and db row / column
@@ -643,14 +667,16 @@ __global__ void __launch_bounds__(kDT, 1)
                 } else {
                     tmem_wait_ld();
                 }
-                float colv[8];
+                float colv[8], bj[8], rkj[8];
+                ld8(bj, &sc.b[j0]);
+                ld8(rkj, &sc.rk[j0]);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int j = j0 + e;
                     float mval = 0.f, cv = 0.f;
                     if (rowv && (isP ? j <= i : j < i)) {
-                        const float dec = exp2f(bi - sc.b[j]);
-                        const float gk = ri * sc.rk[j] * gg[e] * dec;  // normalised, decayed (k_i . k_j) or (q_i . k_j)
+                        const float dec = exp2f(bi - bj[e]);
+                        const float gk = ri * rkj[e] * gg[e] * dec;  // normalised, decayed (k_i . k_j) or (q_i . k_j)
                         if (isP) {
                             const float dP = dv8[e];
                             cv = dP * a.scale * gk;
@@ -676,6 +702,16 @@ __global__ void __launch_bounds__(kDT, 1)
                 sc.sbA[cg][i] = sbsum;
             }
         }
+        {
+            // dk~ += W^T S^T has read W, whose region A_full takes
+            const bool ok2 = wait_phase(&sc.bar_mma2, ph_mma2, budget);
+            if (ok2) {
+                ph_mma2 ^= 1u;
+                pend_mma2 = false;
+            }
+            ok = ok && ok2;
+            tc_fence_after();
+        }
         __syncthreads();
         {
             // A_full^T row r (K-major B of the product; region 0: key tokens j, region 1: query
@@ -688,16 +724,18 @@ __global__ void __launch_bounds__(kDT, 1)
             const float ri = top ? sc.rk[i] : sc.rq[i];
 #pragma unroll 1
             for (int c4 = 0; c4 < 4; ++c4) {
-                float v8[8];
+                float v8[8], cj[8];
+                const int jb = 32 * (cg & 1) + 8 * c4;
+                ld8(cj, (top && rg == 1) ? &sc.rq[jb] : &sc.rk[jb]);
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const int j = 32 * (cg & 1) + 8 * c4 + e;
+                    const int j = jb + e;
                     float v;
-                    if (top) v = rg == 0 ? ri * (Mf[i * kMS + j] + Mf[j * kMS + i]) * sc.rk[j] : ri * Hf[j * kMS + i] * sc.rq[j];
-                    else v = rg == 0 ? ri * Hf[i * kMS + j] * sc.rk[j] : 0.f;
+                    if (top) v = rg == 0 ? ri * (Mf[i * kMS + j] + Mf[j * kMS + i]) * cj[e] : ri * Hf[j * kMS + i] * cj[e];
+                    else v = rg == 0 ? ri * Hf[i * kMS + j] * cj[e] : 0.f;
                     v8[e] = v;
                 }
-                store8_split(STLO + rg * 16384 + sw128_off(r, 4 * (cg & 1) + c4), nullptr, v8);
+                store8_split(TB + rg * 16384 + sw128_off(r, 4 * (cg & 1) + c4), nullptr, v8);
             }
         }
         fence_proxy_async_smem();
@@ -705,9 +743,17 @@ __global__ void __launch_bounds__(kDT, 1)
         __syncthreads();
         if (tid == 0) {
             tc_fence_after();
-            const uint32_t iaf = idesc_bf16_f32(128, 128, true, false);
+            // acc2 = D dS'^T on the token rows (A = [D^T hi | next 16 KB]: rows 64-127 unused), D hi + lo
+            const uint32_t imn = idesc_bf16_f32(128, 128, true, true);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) umma_bf16(tmem + T_DKQ, d_kq_mn + moff(kk), d_af + koff128(kk), iaf, 1u);
+            for (int kk = 0; kk < 8; ++kk) umma_bf16(tmem + T_ACC2, d_dt_mn + moff(kk), d_ds_mn + moff(kk), imn, kk > 0);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                umma_bf16(tmem + T_ACC2, d_dt_mn + (16384 >> 4) + moff(kk), d_ds_mn + moff(kk), imn, 1u);
+            // [dk~ ; dq~] += A_full [K; Q]: A K-major (rows t_out), B = [K; Q] MN-major (key columns)
+            const uint32_t iaf = idesc_bf16_f32(128, 128, false, true);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) umma_bf16(tmem + T_DKQ, d_af + koff128(kk), d_kq_mn + moff(kk), iaf, 1u);
             umma_commit(&sc.bar_mma);
         }
         pend_mma = true;
@@ -795,72 +841,75 @@ __global__ void __launch_bounds__(kDT, 1)
             // the next item's S and dS' stream in while this one finishes: their regions are free
             const int64_t nx = item + static_cast<int64_t>(gridDim.x);
             prefetched = nx < total_items;
-            if (tid == 0 && prefetched) load_states(nx);
+            if (tid == kIo && prefetched) load_states(nx);
             pend_pre = prefetched;
+            if (prefetched) item_meta(nx);
         }
 
-        // ---- P6 (key rows): dk~ = [dk~]^T + sd (.) acc2, dq~; the L2-norm backward; dk, dq, dv out.
-        // This thread: key column r; cg 0, 1: dk tokens 32 cg ..; cg 2, 3: dq tokens 32 (cg - 2) ..
+        // ---- P6 (token rows): dk = dk~ - rk^2 (k . dk~) k, dq alike (thread: row r, 32 key columns
+        // 32 cg ..; rows 0-63 dk, 64-127 dq), dk~ adding sd (.) acc2; then dv = beta (.) dX
         const bool full = n == kChunk && bw.out_tma != 0;
         {
-            const int kq = cg >> 1, th = cg & 1;
-            const uint8_t* rows = KQ + kq * 8192;  // key rows, or query rows (64 rows on)
-            const float* rr = kq == 0 ? sc.rk : sc.rq;
-            const uint32_t xcol = T_DKQ + 32 * cg, ycol = T_ACC2 + 32 * th;
-            // dk~ (with sd (.) acc2) or dq~ of tokens 32 th + 8 g .., and the raw key / query column
-            auto cols8 = [&](int g, float (&x)[8], float (&kv)[8]) {
-                tmem_ld8(trow + xcol + 8 * g, x);
-                if (kq == 0) {
-                    float y[8], sdv[8];
-                    tmem_ld8(trow + ycol + 8 * g, y);
-                    ld8(sdv, &sc.sd[32 * th + 8 * g]);
-                    tmem_wait_ld();
+            const int i = r & 63;
+            const bool isq = r >= 64;
+            float x[32];
+            tmem_ld32(trow + T_DKQ + 32 * cg, x);
+            if (!isq) {
+                float y[32];
+                tmem_ld32(trow + T_ACC2 + 32 * cg, y);
+                tmem_wait_ld();
+                const float sdi = sc.sd[i];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) x[e] = fmaf(sdv[e], y[e], x[e]);
-                } else {
-                    tmem_wait_ld();
-                }
-#pragma unroll
-                for (int e = 0; e < 8; ++e) kv[e] = tile_col(rows, 16384, r, 32 * th + 8 * g + e);
-            };
-            if (a.l2norm) {
-#pragma unroll 1
-                for (int g = 0; g < 4; ++g) {
-                    float x[8], kv[8];
-                    cols8(g, x, kv);
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) x[e] *= kv[e];
-                    const float d = scatter_sum8(x, lane);
-                    if (lane < 8) sc.dots[kq][q4][32 * th + 8 * g + lane] = d;
-                }
+                for (int e = 0; e < 32; ++e) x[e] = fmaf(sdi, y[e], x[e]);
+            } else {
+                tmem_wait_ld();
             }
-            __syncthreads();
-            // full chunks of single-group heads: staged for a TMA store ([a / 64][64 rows][128 B]);
-            // otherwise per-thread stores (bf16, or fp32 per value head for grouped heads)
-            uint8_t* stg = (kq == 0 ? TB : TLO) + (r >> 6) * 8192 + (r & 7) * 2;
-            const uint32_t sck = static_cast<uint32_t>((r & 63) >> 3);
-            uint16_t* ob = (kq == 0 ? bw.dk + hk * bw.dk_sh : bw.dq + hk * bw.dq_sh) + r;
-            const int64_t ost = kq == 0 ? bw.dk_st : bw.dq_st;
-#pragma unroll 1
-            for (int g = 0; g < 4; ++g) {
-                float x[8], kv[8];
-                cols8(g, x, kv);
+            if (a.l2norm) {
+                // the raw row's columns (the K/Q tile: region cg / 2, row r, chunks 4 (cg % 2) ..)
+                float kv[32];
+                const uint8_t* row = KQ + (cg >> 1) * 16384;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int i = 32 * th + 8 * g + e;
-                    if (i >= n) continue;
-                    float out = x[e];
-                    if (a.l2norm) {
-                        const float dot = ((sc.dots[kq][0][i] + sc.dots[kq][1][i]) + sc.dots[kq][2][i]) + sc.dots[kq][3][i];
-                        out = fmaf(-rr[i] * rr[i] * dot, kv[e], x[e]);
-                    }
-                    if (a.group == 1) {
-                        if (full) *reinterpret_cast<uint16_t*>(stg + sw128_off(static_cast<uint32_t>(i), sck)) = f_to_bf16_bits(out);
-                        else ob[(t0 + i) * ost] = f_to_bf16_bits(out);
-                    } else {
-                        (kq == 0 ? bw.dkh : bw.dqh)[((t0 + i) * HO + h) * KD + r] = out;
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    const uint4 wv = *reinterpret_cast<const uint4*>(row + sw128_off(r, 4 * (cg & 1) + c4));
+                    const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        kv[8 * c4 + 2 * e] = bf16_lo(ww[e]);
+                        kv[8 * c4 + 2 * e + 1] = bf16_hi(ww[e]);
                     }
                 }
+                float pd = 0.f;
+#pragma unroll
+                for (int e = 0; e < 32; ++e) pd = fmaf(kv[e], x[e], pd);
+                sc.pdot[cg][r] = pd;
+                __syncthreads();
+                const float rv = isq ? sc.rq[i] : sc.rk[i];
+                const float cf = rv * rv * (((sc.pdot[0][r] + sc.pdot[1][r]) + sc.pdot[2][r]) + sc.pdot[3][r]);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) x[e] = fmaf(-cf, kv[e], x[e]);
+            }
+            if (a.group == 1) {
+                if (full) {
+                    // staged for the TMA store: [column region][64 rows][128 B], swizzled
+                    uint8_t* stg = (isq ? TLO : TB) + (cg >> 1) * 8192;
+#pragma unroll
+                    for (int c4 = 0; c4 < 4; ++c4) store8_split(stg + sw128_off(i, 4 * (cg & 1) + c4), nullptr, &x[8 * c4]);
+                } else if (i < n) {
+                    uint16_t* o = (isq ? bw.dq + (t0 + i) * bw.dq_st + hk * bw.dq_sh
+                                       : bw.dk + (t0 + i) * bw.dk_st + hk * bw.dk_sh) + 32 * cg;
+                    if (bw.vec_out) {
+#pragma unroll
+                        for (int c4 = 0; c4 < 4; ++c4) store8_split(reinterpret_cast<uint8_t*>(o + 8 * c4), nullptr, &x[8 * c4]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] = f_to_bf16_bits(x[e]);
+                    }
+                }
+            } else if (i < n) {
+                float* o = (isq ? bw.dqh : bw.dkh) + ((t0 + i) * HO + h) * KD + 32 * cg;
+#pragma unroll
+                for (int c4 = 0; c4 < 8; ++c4)
+                    *reinterpret_cast<float4*>(o + 4 * c4) = make_float4(x[4 * c4], x[4 * c4 + 1], x[4 * c4 + 2], x[4 * c4 + 3]);
             }
         }
         {
@@ -886,7 +935,7 @@ __global__ void __launch_bounds__(kDT, 1)
         if (full) {
             fence_proxy_async_smem();
             __syncthreads();
-            if (tid == 0) {
+            if (tid == kIo) {
 #pragma unroll
                 for (int rg = 0; rg < 2; ++rg) {
                     tma_store_3d(&dvmap, DO + rg * 8192, rg * 64, h, static_cast<int>(t0));
@@ -907,12 +956,13 @@ __global__ void __launch_bounds__(kDT, 1)
         if (pend_in) wait_phase(&sc.bar_in, ph_in, budget);
         if (pend_pre) wait_phase(&sc.bar_pre, ph_pre, budget);
         if (pend_mma) wait_phase(&sc.bar_mma, ph_mma, budget);
+        if (pend_mma2) wait_phase(&sc.bar_mma2, ph_mma2, budget);
         if (tid == 0) {
             atomicCAS(&a.hdr->status, LA_OK, LA_ERR_TIMEOUT);
             if (a.user_status) atomicCAS(a.user_status, LA_OK, LA_ERR_TIMEOUT);
         }
     }
-    if (tid == 0) bulk_wait_all();  // the last output tiles are out before the CTA ends
+    if (tid == kIo) bulk_wait_all();  // the last output tiles are out before the CTA ends
     tc_fence_before();
     __syncthreads();
     if (tid < 32) tmem_dealloc(tmem, T_COLS);
