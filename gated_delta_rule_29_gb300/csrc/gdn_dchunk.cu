@@ -42,6 +42,7 @@ namespace {
 
 constexpr int kDT = 512;  // threads
 constexpr int kIo = 64;   // the thread that issues the copies (not in the gate-scan warps; thread 0 issues the products)
+constexpr int kMmaLast = 96;  // the issuer of the last products (its warp has no token-row epilogue after them)
 constexpr float kLog2eD = 1.4426950408889634f;
 
 // Shared memory (byte offsets from the 1024-aligned base).  Phase by phase a region is reused
@@ -297,6 +298,7 @@ __global__ void __launch_bounds__(kDT, 1)
     int64_t nt0 = 0;
     int nn = 0;
     float ngt = 0.f;
+    uint16_t nv[16];  // V of value column r, tokens 16 cg .. (bf16 bits)
     auto item_meta = [&](int64_t it) {
         const int64_t chunk_ = it / HO;
         const int h_ = static_cast<int>(it % HO);
@@ -312,6 +314,12 @@ __global__ void __launch_bounds__(kDT, 1)
             gdt_ = a.dt_bias[h_];
         }
         ngt = (tid < 64 && tid < nn) ? gate_at(a, nt0 + tid, h_, gA_, gdt_) : 0.f;
+        const uint16_t* vp = bw.v + h_ * bw.v_sh + r;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const int i = 16 * cg + e;
+            nv[e] = i < nn ? vp[(nt0 + i) * bw.v_st] : uint16_t(0);
+        }
     };
     if (static_cast<int64_t>(blockIdx.x) < total_items) item_meta(blockIdx.x);
 
@@ -346,14 +354,10 @@ __global__ void __launch_bounds__(kDT, 1)
                       static_cast<uint32_t>(kWyFactorBytes), &sc.bar_in);
         }
         pend_in = pend_pre = true;
-        // V: this thread's value column r, tokens 16 cg .. (registers, for X and the dbeta sums)
-        const uint16_t* vp = bw.v + h * bw.v_sh + r;
+        // V: this thread's value column r, tokens 16 cg .. (read one item ahead; for X and the dbeta sums)
         float vv[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-            const int i = 16 * cg + e;
-            vv[e] = i < n ? bf16_bits_to_f(vp[(t0 + i) * bw.v_st]) : 0.f;
-        }
+        for (int e = 0; e < 16; ++e) vv[e] = bf16_bits_to_f(nv[e]);
         if (tid < 64) {
             // gates: per-warp inclusive scans of g * log2(e) (rows past the end carry 0)
             const float gt = gt_mine;
@@ -741,15 +745,13 @@ __global__ void __launch_bounds__(kDT, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
-        if (tid == 0) {
+        if (tid == kMmaLast) {
             tc_fence_after();
-            // acc2 = D dS'^T on the token rows (A = [D^T hi | next 16 KB]: rows 64-127 unused), D hi + lo
+            // acc2 = D dS'^T on the token rows (A = [D^T hi | D^T lo]: rows 64-127 unused; D hi only,
+            // this term reaching only dk)
             const uint32_t imn = idesc_bf16_f32(128, 128, true, true);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) umma_bf16(tmem + T_ACC2, d_dt_mn + moff(kk), d_ds_mn + moff(kk), imn, kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                umma_bf16(tmem + T_ACC2, d_dt_mn + (16384 >> 4) + moff(kk), d_ds_mn + moff(kk), imn, 1u);
             // [dk~ ; dq~] += A_full [K; Q]: A K-major (rows t_out), B = [K; Q] MN-major (key columns)
             const uint32_t iaf = idesc_bf16_f32(128, 128, false, true);
 #pragma unroll
