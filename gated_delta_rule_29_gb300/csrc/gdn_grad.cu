@@ -15,8 +15,9 @@
 // records of the forward's WY pass, so this pass only walks each (span, head) backwards over
 // its chunks with the state-dependent products.
 //
-// Mapping, mirrored from the forward's state pass: one persistent CTA of 128 threads per SM takes
-// (span, head) units longest first; thread r owns TMEM lane r = value column v.  dS^T (fp32,
+// Mapping, mirrored from the forward's state pass: one persistent CTA of 256 threads per SM takes
+// (span, head) units longest first; threads r and r + 128 own TMEM lane r = value column v and
+// split its columns (the chunk's tokens, or the key columns of dS^T) in halves.  dS^T (fp32,
 // lane v, column k) lives in TMEM for the whole span and is updated in place by the tensor core;
 // every product is a tcgen05.mma (kind::f16, bf16 operands split into hi + lo parts, fp32
 // accumulation, M = 128 value columns) in transposed form:
@@ -39,7 +40,7 @@
 namespace la {
 namespace {
 
-constexpr int kGT = 128;  // threads
+constexpr int kGT = 256;  // threads: two per TMEM lane, splitting the columns
 constexpr float kLog2eG = 1.4426950408889634f;
 
 // shared memory (byte offsets from the 1024-aligned base)
@@ -96,7 +97,8 @@ __global__ void __launch_bounds__(kGT, 1)
     uint8_t* TB = sm + G_TB;
     uint8_t* PB = sm + G_PB;
     const int tid = threadIdx.x;
-    const int r = tid;  // TMEM lane = value column
+    const int r = tid & 127;  // TMEM lane = value column
+    const int hf = tid >> 7;  // column half: tokens 32 hf .., key columns KD / 2 hf ..
     const int HO = a.HV;
 
     if (tid == 0) sc.status0 = *reinterpret_cast<volatile int32_t*>(&a.hdr->status);
@@ -118,6 +120,7 @@ __global__ void __launch_bounds__(kGT, 1)
     tc_fence_after();
     const uint32_t tmem = sc.tmem_base;
     const uint32_t trow = tmem + (static_cast<uint32_t>(r & ~31) << 16);
+    constexpr int KH = KP / 2;  // 16-column pieces of the state gradient per column half
     // operand descriptors (an operand at byte offset off from a buffer uses base + (off >> 4))
     const uint64_t d_kq = sdesc_sw128(smem_u32(KQ), 16, 1024);             // K rows, K-major
     const uint64_t d_k_mn = sdesc_sw128(smem_u32(KQ), 16384, 1024);        // K rows, MN-major
@@ -172,7 +175,7 @@ __global__ void __launch_bounds__(kGT, 1)
         {
             const int64_t base = unit_state * KD * a.V + r;
 #pragma unroll 1
-            for (int p = 0; p < KP; ++p) {
+            for (int p = hf * KH; p < (hf + 1) * KH; ++p) {
                 float x[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
@@ -284,7 +287,7 @@ __global__ void __launch_bounds__(kGT, 1)
                 const uint8_t* vcol = DO + (r >> 6) * 8192 + (r & 7) * 2;
                 const uint32_t vchunk = (r & 63) >> 3;
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
+                for (int cc = 4 * hf; cc < 4 * hf + 4; ++cc) {
                     float x[8], sqv[8];
                     ld8(sqv, &sc.sq[8 * cc]);
 #pragma unroll
@@ -313,19 +316,20 @@ __global__ void __launch_bounds__(kGT, 1)
             }
             tc_fence_after();
             {
-                float k64[64], p64[64];
+                float k32[32], p32[32];
 #pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    tmem_ld16(trow + G_R1 + 16 * p, *reinterpret_cast<float(*)[16]>(&k64[16 * p]));
-                    tmem_ld16(trow + G_R2 + 16 * p, *reinterpret_cast<float(*)[16]>(&p64[16 * p]));
+                for (int p = 0; p < 2; ++p) {
+                    tmem_ld16(trow + G_R1 + 32 * hf + 16 * p, *reinterpret_cast<float(*)[16]>(&k32[16 * p]));
+                    tmem_ld16(trow + G_R2 + 32 * hf + 16 * p, *reinterpret_cast<float(*)[16]>(&p32[16 * p]));
                 }
                 tmem_wait_ld();
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    const int cc = 4 * hf + c4;
                     float x[8], sdv[8];
                     ld8(sdv, &sc.sd[8 * cc]);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) x[e] = p64[8 * cc + e] + sdv[e] * k64[8 * cc + e];
+                    for (int e = 0; e < 8; ++e) x[e] = p32[8 * c4 + e] + sdv[e] * k32[8 * c4 + e];
                     store8_split(WB + sw128_off(r, cc), WB + 16384 + sw128_off(r, cc), x);
                 }
             }
@@ -372,16 +376,18 @@ __global__ void __launch_bounds__(kGT, 1)
 
             // ---- G4: a^T = -sx (.) dY^T -> WB (hi, lo), dD^T being consumed
             {
-                float d64[64];
+                float d32[32];
 #pragma unroll
-                for (int p = 0; p < 4; ++p) tmem_ld16(trow + G_R1 + 16 * p, *reinterpret_cast<float(*)[16]>(&d64[16 * p]));
+                for (int p = 0; p < 2; ++p)
+                    tmem_ld16(trow + G_R1 + 32 * hf + 16 * p, *reinterpret_cast<float(*)[16]>(&d32[16 * p]));
                 tmem_wait_ld();
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    const int cc = 4 * hf + c4;
                     float x[8], sxv[8];
                     ld8(sxv, &sc.sx[8 * cc]);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) x[e] = -sxv[e] * d64[8 * cc + e];
+                    for (int e = 0; e < 8; ++e) x[e] = -sxv[e] * d32[8 * c4 + e];
                     store8_split(WB + sw128_off(r, cc), WB + 16384 + sw128_off(r, cc), x);
                 }
             }
@@ -437,17 +443,17 @@ __global__ void __launch_bounds__(kGT, 1)
                 const float gnext = last ? 1.f : exp2f(sc.gsum[0] + sc.gsum[1]);
                 const int64_t obase = unit_state * KD * a.V + r;
 #pragma unroll 1
-                for (int p0 = 0; p0 < KP; p0 += 4) {
+                for (int p0 = hf * KH; p0 < (hf + 1) * KH; p0 += 4) {
                     float s64[64];
 #pragma unroll
                     for (int pp = 0; pp < 4; ++pp)
-                        if (p0 + pp < KP)
+                        if (p0 + pp < (hf + 1) * KH)
                             tmem_ld16(trow + G_DS + 16 * (p0 + pp), *reinterpret_cast<float(*)[16]>(&s64[16 * pp]));
                     tmem_wait_ld();
 #pragma unroll
                     for (int pp = 0; pp < 4; ++pp) {
                         const int p = p0 + pp;
-                        if (p >= KP) break;
+                        if (p >= (hf + 1) * KH) break;
                         float* x = &s64[16 * pp];
                         if (last) {
                             if (r < a.V && a.final_state) {
