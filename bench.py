@@ -595,8 +595,18 @@ def run_bwd_bench(args, world, rank, local):
     assert la.read_status(status) == 0
     flops = bwd_algorithmic_flops(w.lengths(), HV, K, V)
     _, bf16_peak, peak_src = load_peaks()
-    tf32_peak = bf16_peak * TF32_PER_BF16  # TFLOP/s: the products run on tf32 tensor-core MMAs
+    # the tensor-core schedule (the default) computes on bf16 hi + lo tcgen05 operands (its peak:
+    # the bf16 rate); the tile kernel (--fwd-passes fused) on split tf32 warp MMAs (the tf32 rate)
+    tile = args.fwd_passes == "fused"
+    tf32_peak = bf16_peak * TF32_PER_BF16
+    tc_peak = tf32_peak if tile else bf16_peak
     achieved = flops / (kern_ms * 1e-3) / 1e12
+    # launches per step: the prologue and the tile kernel's range launches (four ranges per unit
+    # in one-wave launches when the units outnumber the SMs), or the prologue, the WY pass, the
+    # state-gradient pass and the chunk-parallel pass
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    units = N * HV
+    launches = (1 + (-(-units * 4 // sms) if units > sms else 1)) if tile else 4
 
     # end to end: the step's inputs, cotangents and checkpoints copied from pinned host memory,
     # the gradients copied back, all inside the timed region
@@ -655,14 +665,18 @@ def run_bwd_bench(args, world, rank, local):
                            "; bwd without checkpoints (the forward re-runs)"), "global_batch": N * world, "seq_len": L,
                        "parallelism": "single GPU" if world == 1 else f"independent batches per GPU x{world}",
                        "l2": "inputs larger than L2 (1.6 GB of q/k/v + 2.1 GB of checkpoints per step); no flush"},
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": tf32_peak, "unit": "TFLOP/s",
-                         "frac": achieved / tf32_peak, "traffic": None,
-                         "peak_source": f"{peak_src} bf16 x {TF32_PER_BF16:.3f} (nominal dense tf32 / bf16); "
-                                        "each fp32 product is 2-3 tf32 MMAs (head and remainder splits)",
-                         "kernel": "gdn_bwd_kernel<128, 128>", "kernel_ms": kern_ms, "algorithmic_flops": flops},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": tc_peak, "unit": "TFLOP/s",
+                         "frac": achieved / tc_peak, "traffic": None,
+                         "peak_source": (f"{peak_src} bf16 x {TF32_PER_BF16:.3f} (nominal dense tf32 / bf16); "
+                                         "each fp32 product is 2-3 tf32 MMAs (head and remainder splits)" if tile else
+                                         f"{peak_src} bf16; fp32-level products are 2-3 bf16 tcgen05 MMAs (hi and lo "
+                                         "splits)"),
+                         "kernel": ("gdn_bwd_kernel<128, 128>" if tile else
+                                    "gdn_wy_kernel<128> + gdn_grad_kernel<128> + gdn_dchunk_kernel (timed together)"),
+                         "kernel_ms": kern_ms, "algorithmic_flops": flops},
             "cpu_baseline": cpu,
             "e2e": e2e,
-            "gpu_launches": args.steps * 2,
+            "gpu_launches": args.steps * launches,
             "clocks": clk.summary(),
         }
         print(json.dumps(line), flush=True)

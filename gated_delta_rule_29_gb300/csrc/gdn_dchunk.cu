@@ -49,9 +49,9 @@ constexpr float kLog2eD = 1.4426950408889634f;
 // once the products reading it have completed:
 //   KQ     [K; Q] tile [region 0..1 (key columns)][128 rows][128 B]             whole item
 //   ST     S^T hi [region 0..1 (key columns)][128 rows v][128 B]                 until dk~ += S W
-//   STLO   S^T lo -> X^T hi, lo -> D^T hi, lo -> A_full^T [2][128][128 B]
+//   STLO   S^T lo -> X^T hi, lo -> D^T hi, lo
 //   DST    dS'^T hi                                                              until acc2
-//   DSTLO  dS'^T lo -> dD^T hi, lo -> [dX lo | dX hi | (V region) dO^T] -> M, H fp32
+//   DSTLO  dS'^T lo -> dD^T hi, lo -> [dX lo | dX hi | (TLO) dO^T] -> [N ; Hs] bf16 and a zero tile
 //   TLO    T lo, P lo [64 rows][128 B] each -> dO^T (the MN-major A's upper half)
 //   TB, PB T hi, P hi [64 rows][128 B] -> W region 0
 //   DO     dO tile -> W region 1
@@ -70,7 +70,6 @@ constexpr uint32_t D_TB = 180224;
 constexpr uint32_t D_PB = 188416;
 constexpr uint32_t D_DO = 196608;
 constexpr uint32_t D_SC = 212992;
-constexpr int kMS = 65;  // row stride (floats) of the fp32 M and H staging
 
 // TMEM columns (fp32, 128 lanes): value-column accumulators first, then (their regions consumed)
 // the token- and key-column ones; G stays from the first phase to the dA / dP phase.
@@ -214,8 +213,7 @@ __global__ void __launch_bounds__(kDT, 1)
     uint8_t* TB = sm + D_TB;
     uint8_t* PB = sm + D_PB;
     uint8_t* DO = sm + D_DO;
-    float* Mf = reinterpret_cast<float*>(sm + D_DSTLO);
-    float* Hf = Mf + 64 * kMS;
+    uint8_t* NH = sm + D_DSTLO;  // [N ; Hs] bf16 [128 rows][128 B], then an 8 KB zero tile
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int q4 = (tid >> 5) & 3;  // TMEM lane quadrant of this warp
@@ -265,7 +263,9 @@ __global__ void __launch_bounds__(kDT, 1)
     const uint64_t d_ax_mn = sdesc_sw128(smem_u32(DSTLO + 16384), 16384, 1024);  // [dX hi ; dO (TLO)] MN-major
     const uint64_t d_axlo_mn = sdesc_sw128(smem_u32(DSTLO), 16384, 1024);        // [dX lo ; dX hi]
     const uint64_t d_w_mn = sdesc_sw128(smem_u32(TB), 16384, 1024);       // W = [-sx dX | sq dO]^T
-    const uint64_t d_af = sdesc_sw128(smem_u32(TB), 16, 1024);            // A_full (rows t_out), K-major
+    const uint64_t d_nh = sdesc_sw128(smem_u32(NH), 16, 1024);            // [N ; Hs], K-major (rows i)
+    const uint64_t d_nt_mn = sdesc_sw128(smem_u32(NH), 16384, 1024);      // [N^T ; 0]: N read MN-major
+    const uint64_t d_ht_mn = sdesc_sw128(smem_u32(NH + 8192), 8192, 1024);  // [Hs^T ; 0]
     const uint64_t budget = a.wait_budget_ns;
     // K and Q, dO, T hi (TMA), T lo, the factors (bulk); then S (fp32) and dS' (bulk)
     const uint32_t in_bytes = 2u * 16384u + 2u * 8192u + 2u * static_cast<uint32_t>(kWyTileBytes) +
@@ -646,7 +646,7 @@ __global__ void __launch_bounds__(kDT, 1)
         wait_mma(ok);
 
         // ---- P5 (token rows): dA, dP with A, P recomputed from G; dbeta and db row / column
-        // terms; M and H into shared memory, then A_full^T for dk~ / dq~ += [K; Q]^T A_full^T
+        // terms; N = diag(rk) M diag(rk) and Hs = diag(rq) H diag(rk) as bf16 tiles for the last products
         {
             const int i = r & 63;
             const bool isP = r >= 64;  // rows 64-127: dO D^T (else dX D^T)
@@ -654,7 +654,6 @@ __global__ void __launch_bounds__(kDT, 1)
             const float bi = sc.b[i];
             const float ri = isP ? sc.rq[i] : sc.rk[i];
             const float beti = sc.bet[i];
-            float* Mrow = (isP ? Hf : Mf) + i * kMS;
             float rowsum = 0.f, sbsum = 0.f;
 #pragma unroll 1
             for (int g = 0; g < 2; ++g) {
@@ -671,7 +670,7 @@ __global__ void __launch_bounds__(kDT, 1)
                 } else {
                     tmem_wait_ld();
                 }
-                float colv[8], bj[8], rkj[8];
+                float colv[8], bj[8], rkj[8], tv[8];
                 ld8(bj, &sc.b[j0]);
                 ld8(rkj, &sc.rk[j0]);
 #pragma unroll
@@ -694,8 +693,9 @@ __global__ void __launch_bounds__(kDT, 1)
                         rowsum += cv;
                     }
                     colv[e] = cv;
-                    Mrow[j] = mval;
+                    tv[e] = ri * mval * rkj[e];  // N_ij = rk_i M_ij rk_j, Hs_ij = rq_i H_ij rk_j
                 }
+                store8_split(NH + sw128_off(r, 2 * cg + g), nullptr, tv);
                 const float cs = scatter_sum8(colv, lane);
                 if (lane < 8) (isP ? sc.colP : sc.colA)[q4 & 1][j0 + lane] = cs;
             }
@@ -705,42 +705,17 @@ __global__ void __launch_bounds__(kDT, 1)
                 sc.rowA[cg][i] = rowsum;
                 sc.sbA[cg][i] = sbsum;
             }
+            // the zero tile the transposed reads of N and Hs take as their rows 64-127
+            *reinterpret_cast<uint4*>(NH + 16384 + 16 * tid) = make_uint4(0u, 0u, 0u, 0u);
         }
         {
-            // dk~ += W^T S^T has read W, whose region A_full takes
+            // dk~ += W^T S^T has completed (the last products accumulate onto it)
             const bool ok2 = wait_phase(&sc.bar_mma2, ph_mma2, budget);
             if (ok2) {
                 ph_mma2 ^= 1u;
                 pend_mma2 = false;
             }
             ok = ok && ok2;
-            tc_fence_after();
-        }
-        __syncthreads();
-        {
-            // A_full^T row r (K-major B of the product; region 0: key tokens j, region 1: query
-            // tokens j; this thread: region cg / 2, columns 32 (cg % 2) ..):
-            //   r = i < 64:  [rk_i (M_ij + M_ji) rk_j | rk_i H_ji rq_j]
-            //   r = 64 + i:  [rq_i H_ij rk_j | 0]
-            const int i = r & 63;
-            const bool top = r < 64;
-            const int rg = cg >> 1;
-            const float ri = top ? sc.rk[i] : sc.rq[i];
-#pragma unroll 1
-            for (int c4 = 0; c4 < 4; ++c4) {
-                float v8[8], cj[8];
-                const int jb = 32 * (cg & 1) + 8 * c4;
-                ld8(cj, (top && rg == 1) ? &sc.rq[jb] : &sc.rk[jb]);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int j = jb + e;
-                    float v;
-                    if (top) v = rg == 0 ? ri * (Mf[i * kMS + j] + Mf[j * kMS + i]) * cj[e] : ri * Hf[j * kMS + i] * cj[e];
-                    else v = rg == 0 ? ri * Hf[i * kMS + j] * cj[e] : 0.f;
-                    v8[e] = v;
-                }
-                store8_split(TB + rg * 16384 + sw128_off(r, 4 * (cg & 1) + c4), nullptr, v8);
-            }
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -752,10 +727,16 @@ __global__ void __launch_bounds__(kDT, 1)
             const uint32_t imn = idesc_bf16_f32(128, 128, true, true);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) umma_bf16(tmem + T_ACC2, d_dt_mn + moff(kk), d_ds_mn + moff(kk), imn, kk > 0);
-            // [dk~ ; dq~] += A_full [K; Q]: A K-major (rows t_out), B = [K; Q] MN-major (key columns)
-            const uint32_t iaf = idesc_bf16_f32(128, 128, false, true);
+            // [dk~ ; dq~] += [N ; Hs] K  +  [N^T ; 0] K  +  [Hs^T ; 0] Q: the symmetric scalings make
+            // the transposes plain MN-major reads of the same tiles (B: key or query rows, MN-major)
+            const uint32_t ikm = idesc_bf16_f32(128, 128, false, true);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk) umma_bf16(tmem + T_DKQ, d_af + koff128(kk), d_kq_mn + moff(kk), iaf, 1u);
+            for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem + T_DKQ, d_nh + koff64(kk), d_kq_mn + moff(kk), ikm, 1u);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) umma_bf16(tmem + T_DKQ, d_nt_mn + moff(kk), d_kq_mn + moff(kk), imn, 1u);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                umma_bf16(tmem + T_DKQ, d_ht_mn + moff(kk), d_kq_mn + (8192 >> 4) + moff(kk), imn, 1u);
             umma_commit(&sc.bar_mma);
         }
         pend_mma = true;
