@@ -875,8 +875,10 @@ la_status gdn_bwd(const la_gdn_bwd_params* p, void* stream) {
         if ((st = gdn_fwd(&f, stream)) != LA_OK) return st;
         ck = reinterpret_cast<const float*>(wb + BL.ck);
     } else if (mode == kCkDirect) {
-        // only the prologue: validation and the chunk-row offsets of the caller's checkpoints
-        if ((st = prologue(BL.pro, la::kChunk)) != LA_OK) return st;
+        // only the prologue: validation and the chunk-row offsets of the caller's checkpoints (the
+        // tensor-core schedule runs its own, which also numbers the chunks)
+        tc = tc && aligned(ck, 16);
+        if (!tc && (st = prologue(BL.pro, la::kChunk)) != LA_OK) return st;
     } else if (mode == kCkWiden) {
         // bf16 rows at the chunk cadence: widened to fp32
         if ((st = prologue(BL.pro, la::kChunk)) != LA_OK) return st;
