@@ -53,8 +53,15 @@
 
 namespace la {
 
-constexpr int kCta = 128;  // threads per CTA
+constexpr int kCta = 128;  // threads per CTA (the state passes: two per TMEM lane, below)
 constexpr int kSumPieces = 4;  // chunk ranges per summary unit when the units outnumber one wave
+
+// Threads of a chunk-kernel CTA: the state passes of the two-pass schedules (no solve, only the
+// chain's per-chunk phases) run two threads per TMEM lane, splitting each lane's columns (the
+// chunk's tokens, the state's key columns) in halves; the fused kernel one.
+__host__ __device__ constexpr int chunk_threads(int mode) {
+    return (mode == kModeFwdSplit || mode == kModeSummarySplit || mode == kModeGdpSplit) ? 2 * kCta : kCta;
+}
 
 // ------------------------------------------------------------------ shared memory map
 // Byte offsets from the 1024-aligned base, per mode:
@@ -505,7 +512,7 @@ __device__ __forceinline__ void load_wy(const ChunkArgs& a, const CUtensorMap& w
 }
 
 template <int KD, int MODE>
-__global__ void __launch_bounds__(kCta, 2)
+__global__ void __launch_bounds__(chunk_threads(MODE), 2)
     gdn_chunk_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
                      const __grid_constant__ CUtensorMap wymap, const ChunkArgs a) {
@@ -521,6 +528,7 @@ __global__ void __launch_bounds__(kCta, 2)
     // pass run two per SM; the fused summary, with its larger shared-memory footprint, one)
     constexpr bool kSleep = !kSum || kSplit;
     constexpr int KP = KD / 16;  // 16-column pieces of the state
+    constexpr int PPT = KP / (chunk_threads(MODE) / kCta);
     // GDP: the tokens whose last update row falls in a chunk of 64 update rows (at most QR of
     // them) have their queries in rows 0 .. QR-1 of the query half of the K/Q tile (the other
     // rows stay zero) and their outputs in columns 0 .. QR-1; when n does not divide 64 a chunk
@@ -542,7 +550,13 @@ __global__ void __launch_bounds__(kCta, 2)
     uint8_t* OST = sm + L.m;  // O staging for the bulk store, once the O product has read D^T
 
     const int tid = threadIdx.x;
-    const int r = tid;  // TMEM lane, value column, stacked token row
+    constexpr int NT = chunk_threads(MODE);
+    constexpr int NHALF = NT / kCta;         // threads per TMEM lane
+    const int r = tid & (kCta - 1);          // TMEM lane, value column, stacked token row
+    const int hf = tid / kCta;               // this thread's share of the lane's columns:
+    constexpr int TPT = kChunk / NHALF;      //   tokens tb .. tb + TPT - 1,
+    constexpr int CPT = 8 / NHALF;           //   8-token chunks cb .. cb + CPT - 1,
+    const int tb = hf * TPT, cb = hf * CPT;  //   and 16-column state pieces pb .. pb + PPT - 1
     const int HO = a.HV;
 
     // one read of the status word for the whole CTA (another CTA may set it meanwhile), and of
@@ -607,7 +621,7 @@ __global__ void __launch_bounds__(kCta, 2)
 
     if constexpr (kGdp) {
         // the query rows past a chunk's QR tokens are never written by the tile loads: zero them once
-        for (int e = tid; e < (KD / 64) * (64 - QR) * 8; e += kCta) {
+        for (int e = tid; e < (KD / 64) * (64 - QR) * 8; e += NT) {
             const int rg = e / ((64 - QR) * 8), rem = e % ((64 - QR) * 8);
             *reinterpret_cast<uint4*>(KQ + rg * RQ + 8192 + (QR + rem / 8) * 128 + (rem % 8) * 16) =
                 make_uint4(0u, 0u, 0u, 0u);
@@ -703,8 +717,9 @@ __global__ void __launch_bounds__(kCta, 2)
             const bool from_out = ranged && rng > 0;
             const bool ckpt0 = kFwd && a.ckpt && nchunks > 0 && r < a.V && !from_out;
             const int64_t cbase = ckpt0 ? ((a.ckpt_off[seq] * HO + h) * KD) * a.V + r : 0;
+            const int pb = hf * PPT;
 #pragma unroll 1
-            for (int p = 0; p < KP; ++p) {
+            for (int p = pb; p < pb + PPT; ++p) {
                 float x[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
@@ -876,7 +891,7 @@ __global__ void __launch_bounds__(kCta, 2)
 
             // ---- S4: X^T = beta V^T - sx (K S)^T (hi + lo); then T = (I + A)^{-1} in the V tile's space.
             // This thread's column of V (64 bf16, packed in pairs) is read while the K S product runs.
-            uint32_t vpk[32];
+            uint32_t vpk[TPT / 2];
             {
                 bool okv = true;
                 if (value_tile) {
@@ -890,9 +905,10 @@ __global__ void __launch_bounds__(kCta, 2)
                 const uint8_t* vcol = VT + (r >> 6) * 8192 + (r & 7) * 2;
                 const uint32_t vchunk = (r & 63) >> 3;
 #pragma unroll
-                for (int j2 = 0; j2 < 32; ++j2) {
-                    const uint32_t lo16 = has_v ? *reinterpret_cast<const uint16_t*>(vcol + sw128_off(2 * j2, vchunk)) : 0u;
-                    const uint32_t hi16 = has_v ? *reinterpret_cast<const uint16_t*>(vcol + sw128_off(2 * j2 + 1, vchunk)) : 0u;
+                for (int j2 = 0; j2 < TPT / 2; ++j2) {
+                    const uint32_t i0 = static_cast<uint32_t>(tb + 2 * j2);
+                    const uint32_t lo16 = has_v ? *reinterpret_cast<const uint16_t*>(vcol + sw128_off(i0, vchunk)) : 0u;
+                    const uint32_t hi16 = has_v ? *reinterpret_cast<const uint16_t*>(vcol + sw128_off(i0 + 1, vchunk)) : 0u;
                     vpk[j2] = lo16 | (hi16 << 16);
                 }
                 ok = ok && okv;
@@ -916,33 +932,30 @@ __global__ void __launch_bounds__(kCta, 2)
             tc_fence_after();
             {
                 const int v = r;
-                float k64[64];
+                float kx[TPT];
 #pragma unroll
-                for (int p = 0; p < 4; ++p) tmem_ld16(trow + COL_R1 + 16 * p, *reinterpret_cast<float(*)[16]>(&k64[16 * p]));
+                for (int p = 0; p < TPT / 16; ++p)
+                    tmem_ld16(trow + COL_R1 + tb + 16 * p, *reinterpret_cast<float(*)[16]>(&kx[16 * p]));
                 tmem_wait_ld();
 #pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    const float* ks = &k64[16 * p];
+                for (int c2 = 0; c2 < CPT; ++c2) {
+                    const int cc = cb + c2;
+                    float x[8], bt[8], sxv[8];
+                    ld8(bt, &sc.bet[8 * cc]);
+                    ld8(sxv, &sc.sx[8 * cc]);
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int cc = 2 * p + hh;
-                        float x[8], bt[8], sxv[8];
-                        ld8(bt, &sc.bet[8 * cc]);
-                        ld8(sxv, &sc.sx[8 * cc]);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const int j = 8 * cc + e;
-                            const float vv = __uint_as_float((j & 1) ? (vpk[j >> 1] & 0xFFFF0000u) : (vpk[j >> 1] << 16));
-                            x[e] = bt[e] * vv - sxv[e] * ks[8 * hh + e];
-                        }
-                        store8_split(WB + sw128_off(v, cc), WB + 16384 + sw128_off(v, cc), x);
+                    for (int e = 0; e < 8; ++e) {
+                        const int j = 8 * c2 + e;  // (relative to tb, which is even)
+                        const float vv = __uint_as_float((j & 1) ? (vpk[j >> 1] & 0xFFFF0000u) : (vpk[j >> 1] << 16));
+                        x[e] = bt[e] * vv - sxv[e] * kx[j];
                     }
+                    store8_split(WB + sw128_off(v, cc), WB + 16384 + sw128_off(v, cc), x);
                 }
             }
             if (kFwd) {
                 // (Q S)^T -> (scale rq gamma) (Q S)^T in place: column i is query row i
 #pragma unroll
-                for (int p = 0; p < 4; ++p) {
+                for (int p = tb / 16; p < tb / 16 + TPT / 16; ++p) {
                     float qs[16], f[16];
                     tmem_ld16(trow + COL_R2 + 16 * p, qs);
                     ld8(f, &sc.sq[16 * p]);
@@ -999,23 +1012,20 @@ __global__ void __launch_bounds__(kCta, 2)
             tc_fence_after();
             {
                 const int v = r;
-                float d64[64];
+                float dd[TPT];
 #pragma unroll
-                for (int p = 0; p < 4; ++p) tmem_ld16(trow + COL_R1 + 16 * p, *reinterpret_cast<float(*)[16]>(&d64[16 * p]));
+                for (int p = 0; p < TPT / 16; ++p)
+                    tmem_ld16(trow + COL_R1 + tb + 16 * p, *reinterpret_cast<float(*)[16]>(&dd[16 * p]));
                 tmem_wait_ld();
 #pragma unroll
-                for (int p = 0; p < 4; ++p) {
-                    float* dd = &d64[16 * p];
+                for (int c2 = 0; c2 < CPT; ++c2) {
+                    const int cc = cb + c2;
+                    float x[8], sdv[8];
+                    ld8(sdv, &sc.sd[8 * cc]);
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        const int cc = 2 * p + hh;
-                        float x[8], sdv[8];
-                        ld8(sdv, &sc.sd[8 * cc]);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) x[e] = sdv[e] * dd[8 * hh + e];
-                        if (kFwd) store8_split(DT + sw128_off(v, cc), nullptr, &dd[8 * hh]);
-                        store8_split(WB + sw128_off(v, cc), WB + 16384 + sw128_off(v, cc), x);
-                    }
+                    for (int e = 0; e < 8; ++e) x[e] = sdv[e] * dd[8 * c2 + e];
+                    if (kFwd) store8_split(DT + sw128_off(v, cc), nullptr, &dd[8 * c2]);
+                    store8_split(WB + sw128_off(v, cc), WB + 16384 + sw128_off(v, cc), x);
                 }
             }
             if (pend_st) {
@@ -1056,9 +1066,10 @@ __global__ void __launch_bounds__(kCta, 2)
                 }
                 ok = ok && oko;
                 tc_fence_after();
-                float o64[64];
+                float o64[TPT];
 #pragma unroll
-                for (int p = 0; p < 4; ++p) tmem_ld16(trow + COL_R2 + 16 * p, *reinterpret_cast<float(*)[16]>(&o64[16 * p]));
+                for (int p = 0; p < TPT / 16; ++p)
+                    tmem_ld16(trow + COL_R2 + tb + 16 * p, *reinterpret_cast<float(*)[16]>(&o64[16 * p]));
                 tmem_wait_ld();
                 if (o_tma_chunk) {
                     // a full chunk: O (bf16) into the free M buffer in the TMA box layout
@@ -1067,9 +1078,10 @@ __global__ void __launch_bounds__(kCta, 2)
                         uint8_t* col = OST + (r >> 6) * 8192 + (r & 7) * 2;
                         const uint32_t vchunk = (r & 63) >> 3;
 #pragma unroll
-                        for (int i = 0; i < 64; ++i)
-                            if (!kGdp || i < QR)  // (the bulk store needs 64 / n whole tokens: n divides 64)
-                                *reinterpret_cast<uint16_t*>(col + sw128_off(i, vchunk)) = f_to_bf16_bits(o64[i]);
+                        for (int i = 0; i < TPT; ++i)
+                            if (!kGdp || tb + i < QR)  // (the bulk store needs 64 / n whole tokens: n divides 64)
+                                *reinterpret_cast<uint16_t*>(col + sw128_off(static_cast<uint32_t>(tb + i), vchunk)) =
+                                    f_to_bf16_bits(o64[i]);
                     }
                     fence_proxy_async_smem();
                     __syncthreads();
@@ -1081,8 +1093,8 @@ __global__ void __launch_bounds__(kCta, 2)
                 } else if (r < a.V) {
                     uint16_t* op = a.o + tok0 * a.o_st + static_cast<int64_t>(h) * a.o_sh + r;
 #pragma unroll
-                    for (int i = 0; i < 64; ++i)
-                        if (i < nq) op[static_cast<int64_t>(i) * a.o_st] = f_to_bf16_bits(o64[i]);
+                    for (int i = 0; i < TPT; ++i)
+                        if (tb + i < nq) op[static_cast<int64_t>(tb + i) * a.o_st] = f_to_bf16_bits(o64[i]);
                 }
             }
             {
@@ -1125,18 +1137,19 @@ __global__ void __launch_bounds__(kCta, 2)
                 const int64_t cbase =
                     ckpt ? (((a.ckpt_off[seq] + static_cast<int64_t>(c + 1) * kChunk / a.ckpt_n) * HO + h) * KD) * a.V + r
                          : 0;
+                const int pb = hf * PPT;
 #pragma unroll 1
-                for (int p0 = 0; p0 < KP; p0 += 4) {
+                for (int p0 = pb; p0 < pb + PPT; p0 += 4) {
                     float s64[64];
 #pragma unroll
                     for (int pp = 0; pp < 4; ++pp)
-                        if (p0 + pp < KP)
+                        if (p0 + pp < pb + PPT)
                             tmem_ld16(trow + COL_S + 16 * (p0 + pp), *reinterpret_cast<float(*)[16]>(&s64[16 * pp]));
                     tmem_wait_ld();
 #pragma unroll
                     for (int pp = 0; pp < 4; ++pp) {
                         const int p = p0 + pp;
-                        if (p >= KP) break;
+                        if (p >= pb + PPT) break;
                         float* x = &s64[16 * pp];
 #pragma unroll
                         for (int hh = 0; hh < 2; ++hh) {
@@ -1435,9 +1448,9 @@ __global__ void __launch_bounds__(kCta, 4)
 // from the hardware limits (registers allocated per warp in units of 256, shared memory per SM
 // minus the per-block reserve), whichever is larger.  A CTA that cannot be resident yet simply
 // starts later and finds no work left, so overestimating costs nothing.
-static cudaError_t resident_per_sm(const void* fn, uint32_t smem, int cap, int device, int* out) {
+static cudaError_t resident_per_sm(const void* fn, uint32_t smem, int cap, int device, int* out, int threads = kCta) {
     int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kCta, smem);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem);
     if (e != cudaSuccess) return e;
     cudaFuncAttributes fa;
     int smem_sm = 0, reserve = 0, regs_sm = 0;
@@ -1445,7 +1458,7 @@ static cudaError_t resident_per_sm(const void* fn, uint32_t smem, int cap, int d
         cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device) == cudaSuccess &&
         cudaDeviceGetAttribute(&reserve, cudaDevAttrReservedSharedMemoryPerBlock, device) == cudaSuccess &&
         cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, device) == cudaSuccess) {
-        const int regs_cta = ((fa.numRegs * 32 + 255) / 256) * 256 * (kCta / 32);
+        const int regs_cta = ((fa.numRegs * 32 + 255) / 256) * 256 * (threads / 32);
         const int by_regs = regs_cta > 0 ? regs_sm / regs_cta : 1;
         const int by_smem = smem_sm / (static_cast<int>(smem) + reserve);
         const int hw = by_regs < by_smem ? by_regs : by_smem;
@@ -1489,7 +1502,7 @@ static cudaError_t launch_one(const ChunkArgs& a, const CUtensorMap& qm, const C
     e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
     int per_sm = 0, sms = 0;
-    e = resident_per_sm(reinterpret_cast<const void*>(fn), smem, 2, device, &per_sm);
+    e = resident_per_sm(reinterpret_cast<const void*>(fn), smem, 2, device, &per_sm, chunk_threads(MODE));
     if (e != cudaSuccess) return e;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
     if (e != cudaSuccess) return e;
@@ -1511,7 +1524,7 @@ static cudaError_t launch_one(const ChunkArgs& a, const CUtensorMap& qm, const C
         for (int64_t base = 0; base < items; base += slots) {
             b.item_base = base;
             b.items = items - base < slots ? items - base : slots;
-            fn<<<static_cast<int>(b.items), kCta, smem, s>>>(qm, km, vm, om, wm, b);
+            fn<<<static_cast<int>(b.items), chunk_threads(MODE), smem, s>>>(qm, km, vm, om, wm, b);
             e = cudaGetLastError();
             if (e != cudaSuccess) return e;
         }
@@ -1519,7 +1532,7 @@ static cudaError_t launch_one(const ChunkArgs& a, const CUtensorMap& qm, const C
     }
     const int grid = static_cast<int>(b.num_units < slots ? b.num_units : slots);
     if (grid <= 0) return cudaSuccess;
-    fn<<<grid, kCta, smem, s>>>(qm, km, vm, om, wm, b);
+    fn<<<grid, chunk_threads(MODE), smem, s>>>(qm, km, vm, om, wm, b);
     return cudaGetLastError();
 }
 
