@@ -41,6 +41,7 @@ namespace la {
 namespace {
 
 constexpr int kGT = 256;  // threads: two per TMEM lane, splitting the columns
+constexpr int kGradPieces = 4;  // chunk ranges per unit when the units outnumber the SMs
 constexpr float kLog2eG = 1.4426950408889634f;
 
 // shared memory (byte offsets from the 1024-aligned base)
@@ -65,9 +66,26 @@ struct __align__(16) GradScalars {
     float gsum[2];                          // per-warp sums of the next chunk's g * log2(e)
     uint64_t bar_kq, bar_do, bar_mma, bar_f;
     uint32_t tmem_base;
-    int32_t unit_lo, unit_hi, status0;
+    int32_t unit_lo, unit_hi, status0, flag_ok;
 };
 static_assert(sizeof(GradScalars) <= 2048, "gradient-pass scalar area");
+
+// Bounded wait until *f >= need (acquire, GPU scope); false after budget_ns.  One thread.
+__device__ __forceinline__ bool wait_flag(const int32_t* f, int32_t need, uint64_t budget_ns) {
+    uint64_t t0 = 0;
+    for (int it = 0;; ++it) {
+        int32_t v;
+        asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+        if (v >= need) return true;
+        if (it == 0) t0 = globaltimer_ns();
+        else if (globaltimer_ns() - t0 > budget_ns) return false;
+        __nanosleep(256);
+    }
+}
+__device__ __forceinline__ void set_flag(int32_t* f, int32_t v) {
+    __threadfence();
+    asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
 
 // One WY record's T, P and factors, on bar_f.  One thread.
 __device__ __forceinline__ void grad_load_record(const ChunkArgs& a, const CUtensorMap& wymap, int64_t chunk, int h,
@@ -134,6 +152,7 @@ __global__ void __launch_bounds__(kGT, 1)
     const uint32_t kq_bytes = KD * 256u;                                    // K and Q rows
     const uint32_t do_bytes = static_cast<uint32_t>(a.V) * 128u;
     const uint64_t budget = a.wait_budget_ns;
+    const int NP = a.pieces > 1 ? a.pieces : 1;  // chunk ranges per unit
     uint32_t ph_kq = 0, ph_do = 0, ph_mma = 0, ph_f = 0;
     bool pend_kq = false, pend_do = false, pend_mma = false, pend_f = false, failed = false;
 
@@ -144,31 +163,45 @@ __global__ void __launch_bounds__(kGT, 1)
             sc.unit_hi = static_cast<int32_t>(u >> 32);
         }
         __syncthreads();
-        const int64_t unit = (static_cast<int64_t>(sc.unit_hi) << 32) | static_cast<uint32_t>(sc.unit_lo);
+        const int64_t tk = (static_cast<int64_t>(sc.unit_hi) << 32) | static_cast<uint32_t>(sc.unit_lo);
         __syncthreads();  // every thread has read the ticket before thread 0 may take the next one
-        if (unit >= a.num_units) break;
+        // tickets run through the units' last ranges first, then the ranges before them: a
+        // range's successor has an earlier ticket, held by a CTA that is running or done
+        if (tk >= a.num_units * NP) break;
+        const int64_t unit = tk % a.num_units;
+        const int piece = NP - 1 - static_cast<int>(tk / a.num_units);
         const int seq = a.order[unit / HO];
         const int h = static_cast<int>(unit % HO);
         const int hk = h / a.group;
         const int64_t tok_s = cu_get(a.cu, a.cu64, seq);
         const int64_t L = cu_get(a.cu, a.cu64, seq + 1) - tok_s;
-        const int nch = static_cast<int>((L + kChunk - 1) / kChunk);
+        const int nch_all = static_cast<int>((L + kChunk - 1) / kChunk);
+        const int clo = static_cast<int>(static_cast<int64_t>(piece) * nch_all / NP);        // chunks clo ..
+        const int chi = static_cast<int>(static_cast<int64_t>(piece + 1) * nch_all / NP);    // .. chi - 1
+        const int nch = chi;  // (the walk starts at chunk chi - 1)
         const int64_t unit_state = static_cast<int64_t>(seq) * HO + h;
+        // where the range starts from (d_final_state, or its successor's output) and where it ends
+        const float* src = piece == NP - 1 ? static_cast<const float*>(a.s0) : a.grad_carry;
+        float* dst = piece == 0 ? a.final_state : a.grad_carry;
+        if (piece < NP - 1) {
+            if (tid == 0) sc.flag_ok = wait_flag(a.grad_flags + unit_state, NP - 1 - piece, budget) ? 1 : 0;
+            if (__syncthreads_or(tid == 0 && sc.flag_ok == 0)) { failed = true; break; }
+        }
         float gA = 0.f, gdt = 0.f;
         if (a.gate_mode == LA_GATE_SOFTPLUS && tid < 64) {
             gA = -expf(a.a_log[h]);
             gdt = a.dt_bias[h];
         }
-        // the total decay of the last chunk, the first one walked
+        // the total decay of the range's last chunk, the first one walked
         if (tid < 64) {
-            const int64_t t_last = tok_s + static_cast<int64_t>(nch > 0 ? nch - 1 : 0) * kChunk;
-            float x = (nch > 0 && t_last + tid < tok_s + L) ? gate_row<false>(a, t_last + tid, h, gA, gdt) * kLog2eG : 0.f;
+            const int64_t t_last = tok_s + static_cast<int64_t>(nch > clo ? nch - 1 : 0) * kChunk;
+            float x = (nch > clo && t_last + tid < tok_s + L) ? gate_row<false>(a, t_last + tid, h, gA, gdt) * kLog2eG : 0.f;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
             if ((tid & 31) == 0) sc.gsum[tid >> 5] = x;
         }
         __syncthreads();
-        const float gam0 = nch > 0 ? exp2f(sc.gsum[0] + sc.gsum[1]) : 1.f;
+        const float gam0 = nch > clo ? exp2f(sc.gsum[0] + sc.gsum[1]) : 1.f;
 
         // ---- the gradient leaving the span (d_final_state, or 0): bf16 hi + lo copy for (K dS), and
         // TMEM pre-multiplied by the last chunk's decay; an empty span passes it straight through
@@ -179,17 +212,16 @@ __global__ void __launch_bounds__(kGT, 1)
                 float x[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
-                    x[e] = (a.s0 && r < a.V) ? static_cast<const float*>(a.s0)[base + static_cast<int64_t>(16 * p + e) * a.V]
-                                             : 0.f;
+                    x[e] = (src && r < a.V) ? src[base + static_cast<int64_t>(16 * p + e) * a.V] : 0.f;
 #pragma unroll
                 for (int hh = 0; hh < 2; ++hh) {
                     const int kc = 2 * p + hh;
                     const uint32_t off = (kc >> 3) * 16384 + sw128_off(r, kc & 7);
                     store8_split(WB + off, SLO + off, &x[8 * hh]);
                 }
-                if (nch == 0 && r < a.V && a.final_state) {
+                if (nch == clo && r < a.V && dst) {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) a.final_state[base + static_cast<int64_t>(16 * p + e) * a.V] = x[e];
+                    for (int e = 0; e < 16; ++e) dst[base + static_cast<int64_t>(16 * p + e) * a.V] = x[e];
                 }
 #pragma unroll
                 for (int e = 0; e < 16; ++e) x[e] *= gam0;
@@ -197,7 +229,12 @@ __global__ void __launch_bounds__(kGT, 1)
             }
             tmem_wait_st();
         }
-        if (nch == 0) continue;
+        if (nch == clo) {
+            // an empty range passes the gradient straight through
+            __syncthreads();
+            if (tid == 0 && piece > 0) set_flag(a.grad_flags + unit_state, NP - piece);
+            continue;
+        }
 
         // ---- the last chunk's tiles and record
         {
@@ -216,8 +253,8 @@ __global__ void __launch_bounds__(kGT, 1)
             }
             pend_kq = pend_do = pend_f = true;
         }
-        for (int c = nch - 1; c >= 0; --c) {
-            const bool last = c == 0;  // the last chunk walked (the span's first)
+        for (int c = nch - 1; c >= clo; --c) {
+            const bool last = c == clo;  // the last chunk walked (the range's first)
             const int64_t t0 = tok_s + static_cast<int64_t>(c) * kChunk;
             // the gates of the chunk walked next (a full chunk: only the span's last can be short)
             float g_nx = 0.f;
@@ -456,9 +493,9 @@ __global__ void __launch_bounds__(kGT, 1)
                         if (p >= (hf + 1) * KH) break;
                         float* x = &s64[16 * pp];
                         if (last) {
-                            if (r < a.V && a.final_state) {
+                            if (r < a.V && dst) {
 #pragma unroll
-                                for (int e = 0; e < 16; ++e) a.final_state[obase + static_cast<int64_t>(16 * p + e) * a.V] = x[e];
+                                for (int e = 0; e < 16; ++e) dst[obase + static_cast<int64_t>(16 * p + e) * a.V] = x[e];
                             }
                         } else {
 #pragma unroll
@@ -480,6 +517,8 @@ __global__ void __launch_bounds__(kGT, 1)
             if (__syncthreads_or(!ok)) { failed = true; break; }
         }
         if (failed) break;
+        // the range's output (the gradient entering its first chunk) is written: its predecessor may start
+        if (tid == 0 && piece > 0) set_flag(a.grad_flags + unit_state, NP - piece);
     }
 
     if (failed) {
@@ -515,7 +554,28 @@ cudaError_t launch_grad(const ChunkArgs& a, const CUtensorMap& qm, const CUtenso
     // one CTA per SM (163 KB of shared memory), persistent over the units
     const int64_t grid = a.num_units < sms ? a.num_units : sms;
     if (grid <= 0) return cudaSuccess;
-    fn<<<static_cast<int>(grid), kGT, G_SMEM, s>>>(qm, km, dom, wm, a);
+    ChunkArgs b = a;
+    b.pieces = 1;
+    if (a.grad_carry && a.grad_flags && a.num_units > sms) {
+        // more units than SMs: four chunk ranges per unit over co-resident CTAs (a cooperative
+        // launch, which guarantees them), so that the last wave is not left half empty; not under
+        // stream capture (then one walk per unit, as below)
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        int coop = 0;
+        if (cudaStreamIsCapturing(s, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusNone &&
+            cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && coop) {
+            e = cudaMemsetAsync(a.grad_flags, 0, static_cast<size_t>(a.num_units) * sizeof(int32_t), s);
+            if (e != cudaSuccess) return e;
+            b.pieces = kGradPieces;
+            void* args[] = {const_cast<CUtensorMap*>(&qm), const_cast<CUtensorMap*>(&km), const_cast<CUtensorMap*>(&dom),
+                            const_cast<CUtensorMap*>(&wm), &b};
+            e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(fn), dim3(sms), dim3(kGT), args, G_SMEM, s);
+            if (e == cudaSuccess) return cudaSuccess;
+            (void)cudaGetLastError();  // (not launched: one walk per unit instead)
+            b.pieces = 1;
+        }
+    }
+    fn<<<static_cast<int>(grid), kGT, G_SMEM, s>>>(qm, km, dom, wm, b);
     return cudaGetLastError();
 }
 

@@ -163,6 +163,11 @@ struct ChunkArgs {
     uint8_t* ds_chunks;
     // the WY pass for gdn_bwd also writes T's bf16 residual per item (8 KB, swizzled), or null
     uint8_t* wy_tlo;
+    // the state-gradient pass of gdn_bwd when its units outnumber the SMs: each unit's chunks in
+    // `pieces` ranges taken in dependency order by co-resident CTAs, a range starting from the
+    // gradient its successor left here ([N * HO][K][V] fp32) once the unit's flag says so
+    float* grad_carry;
+    int32_t* grad_flags;             // [N * HO], zeroed by the launch
 };
 
 // One recurrence step per sequence against a state pool (gdn_decode).

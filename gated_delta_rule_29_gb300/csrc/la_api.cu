@@ -582,7 +582,7 @@ struct BwdLayout {
     size_t pro, ck, o, ds, gh, gp, pro_n, pro_seg, cu_seg, s0_seg, total;
     // the tensor-core path (K = V = 128) after the rest: the split layout's prologue area, chunk
     // numbering and WY records, the gradient leaving every (chunk, head), per-item gate sums
-    size_t tc_split, tc_ds, tc_tlo, tc_gp, total_tc;
+    size_t tc_split, tc_ds, tc_tlo, tc_gp, tc_carry, tc_flags, total_tc;
 };
 size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 BwdLayout bwd_layout(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, int32_t V, int mode, int64_t n = 0) {
@@ -622,6 +622,10 @@ BwdLayout bwd_layout(int64_t T, int32_t N, int32_t HK, int32_t HV, int32_t K, in
     off += up256(static_cast<size_t>(GL.items) * la::kWyTileBytes);
     L.tc_gp = off;
     off += up256(2 * static_cast<size_t>(HV) * static_cast<size_t>(GL.chunks) * sizeof(float));
+    L.tc_carry = off;  // the state-gradient pass's range hand-off and its flags
+    off += up256(static_cast<size_t>(N) * HV * K * V * sizeof(float));
+    L.tc_flags = off;
+    off += up256(static_cast<size_t>(N) * HV * sizeof(int32_t));
     L.total_tc = off;
     return L;
 }
@@ -725,6 +729,8 @@ la_status bwd_tensor_path(const la_gdn_bwd_params* p, const BwdLayout& BL, uint8
     ka.chunk_seq = pa.chunk_seq;
     ka.wy = gw + GL.wy;
     ka.ds_chunks = wb + BL.tc_ds;
+    ka.grad_carry = reinterpret_cast<float*>(wb + BL.tc_carry);
+    ka.grad_flags = reinterpret_cast<int32_t*>(wb + BL.tc_flags);
     ka.user_status = p->status;
     ka.wait_budget_ns = kWaitBudgetNs;
     ka.gdp_n = 1;

@@ -161,3 +161,35 @@ def test_bwd_tensor_small_workspace_takes_the_tile_kernel():
     tile = host(bwd(w, do, dfin, passes=1))
     for name, x, y in zip(NAMES, small, tile):
         assert np.array_equal(x, y), name
+
+
+def test_bwd_tensor_state_gradient_ranges_same_bits():
+    """More (sequence, head) units than SMs: the state-gradient pass walks every unit in four
+    chunk ranges over co-resident CTAs, each range starting from the exact fp32 gradient its
+    successor left; the gradient entering every sequence is bitwise the summary backward's (one
+    walk per unit), and the chunk pass's gradients match the oracle on sampled units."""
+    sms = torch.cuda.get_device_properties(dev()).multi_processor_count
+    n_seq = sms // 2 + 8
+    lengths = [200 + 7 * (i % 5) for i in range(n_seq)]
+    w = W.draw("bwd tc ranges", lengths, 1, 2, 128, 128, seed=681, initial_state=True, slow_decay=True)
+    assert w.N * w.HV > sms
+    do, dfin = cotangents(w, 682)
+    d = dev()
+    got = bwd(w, do, dfin)
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    ds = la.gdn_summary_bwd(w.q.to(d), w.k.to(d), w.g.to(d), w.beta.to(d), w.cu_seqlens.to(d), do.to(d),
+                            d_final_state=dfin.to(d), status=status)
+    assert la.read_status(status) == 0
+    assert torch.equal(got[5], ds)
+    # two sequences against the oracle (all of their heads)
+    cu = w.cu_seqlens.numpy().astype(np.int64)
+    for i in (0, n_seq - 1):
+        sl = slice(cu[i], cu[i + 1])
+        sub = W.Workload(name="one", cu_seqlens=torch.tensor([0, cu[i + 1] - cu[i]]), q=w.q[sl], k=w.k[sl],
+                         v=w.v[sl], g=w.g[sl].contiguous(), beta=w.beta[sl].contiguous(),
+                         initial_state=w.initial_state[i:i + 1])
+        ref = oracle.gdn_bwd(sub.q, sub.k, sub.v, sub.g, sub.beta, sub.cu_seqlens, do[sl],
+                             initial_state=sub.initial_state, d_final_state=dfin[i:i + 1])
+        part = [got[0][sl].float().cpu().numpy(), got[1][sl].float().cpu().numpy(), got[2][sl].float().cpu().numpy(),
+                got[3][sl].float().cpu().numpy(), got[4][sl].float().cpu().numpy(), got[5][i:i + 1].float().cpu().numpy()]
+        compare(sub, part, ref, label=f" tensor cores, ranged state gradient, sequence {i}")
