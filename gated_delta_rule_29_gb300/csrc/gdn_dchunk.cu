@@ -340,6 +340,8 @@ __global__ void __launch_bounds__(kDT, 1)
         if (tid == kIo) {
             if (!prefetched) load_states(item);
             bulk_wait_read_all();  // the previous item's output tiles have left their staging buffers
+        }
+        if (tid == kIo && !a.test_skip_tile_load) {  // (the failure-path test hook: no tile loads)
             mbar_arrive_expect_tx(&sc.bar_in, in_bytes);
 #pragma unroll
             for (int rg = 0; rg < 2; ++rg) {
@@ -353,7 +355,8 @@ __global__ void __launch_bounds__(kDT, 1)
             bulk_load(sc.bet, a.wy + item * static_cast<int64_t>(kWyRecordBytes) + 2 * kWyTileBytes,
                       static_cast<uint32_t>(kWyFactorBytes), &sc.bar_in);
         }
-        pend_in = pend_pre = true;
+        pend_in = !a.test_skip_tile_load;
+        pend_pre = true;
         // V: this thread's value column r, tokens 16 cg .. (read one item ahead; for X and the dbeta sums)
         float vv[16];
 #pragma unroll

@@ -767,6 +767,8 @@ la_status bwd_tensor_path(const la_gdn_bwd_params* p, const BwdLayout& BL, uint8
     if (la::launch_grad(ka, qm, km, dom, wm, s) != cudaSuccess) return LA_ERR_CUDA;
     ChunkArgs kd = ka;
     kd.items = GL.items;
+    // the failure-path test hook reaches the chunk pass only (its first tile wait runs out)
+    kd.test_skip_tile_load = g_test_skip_tile_load.load(std::memory_order_relaxed) != 0;
     if (la::launch_dchunk(kd, b, qm, km, dom, wm, dkm, dqm, dvm, s) != cudaSuccess) return LA_ERR_CUDA;
     if (la::launch_bwd_finish(b, s) != cudaSuccess) return LA_ERR_CUDA;
     return LA_OK;

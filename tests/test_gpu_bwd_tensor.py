@@ -193,3 +193,26 @@ def test_bwd_tensor_state_gradient_ranges_same_bits():
         part = [got[0][sl].float().cpu().numpy(), got[1][sl].float().cpu().numpy(), got[2][sl].float().cpu().numpy(),
                 got[3][sl].float().cpu().numpy(), got[4][sl].float().cpu().numpy(), got[5][i:i + 1].float().cpu().numpy()]
         compare(sub, part, ref, label=f" tensor cores, ranged state gradient, sequence {i}")
+
+
+def test_bwd_tensor_bounded_wait_timeout_reports_and_context_survives():
+    """The chunk-parallel pass's failure path, made on the host: the library's test hook stops its
+    tile loads, so every CTA's first tile wait runs out after a 20 ms budget; the call reports
+    LA_ERR_TIMEOUT and returns, and the next call on the same context matches the oracle."""
+    w = W.draw("bwd tc timeout", [130, 64], 1, 2, 128, 128, seed=691, initial_state=True, slow_decay=True)
+    do, dfin = cotangents(w, 692)
+    d = dev()
+    lib = la.binding.load()
+    status = torch.zeros(1, dtype=torch.int32, device=d)
+    assert lib.la_test_set_wait_hooks(1, 20000000) == 0
+    try:
+        la.gdn_bwd(w.q.to(d), w.k.to(d), w.v.to(d), w.g.to(d), w.beta.to(d), w.cu_seqlens.to(d), do.to(d),
+                   initial_state=w.initial_state.to(d), d_final_state=dfin.to(d), status=status)
+        assert la.read_status(status) == la.binding.LA_ERR_TIMEOUT
+    finally:
+        assert lib.la_test_set_wait_hooks(0, 0) == 0
+    torch.cuda.synchronize()
+    got = host(bwd(w, do, dfin))
+    ref = oracle.gdn_bwd(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, do, initial_state=w.initial_state,
+                         d_final_state=dfin)
+    compare(w, got, ref, label=" tensor cores, after a timed-out call")
