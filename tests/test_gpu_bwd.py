@@ -141,13 +141,14 @@ def test_bwd_sparse_fp32_checkpoints_regenerate_the_same_bits(n):
         assert np.array_equal(x, z), name
 
 
-@pytest.mark.parametrize("n", [64, 192])
-def test_bwd_bf16_checkpoints_against_oracle(n):
+@pytest.mark.parametrize("n,KV", [(64, 64), (192, 64), (64, 128), (192, 128)])
+def test_bwd_bf16_checkpoints_against_oracle(n, KV):
     """bf16 rows (the io dtype) at the chunk cadence are widened; at n = 192 the dense series is
     regenerated from them.  The states then carry bf16's 2^-9 relative rounding before the
     backward starts, so every gradient is held to the bf16 bound 1e-2 (as bf16 checkpoints are);
-    the oracle differentiates the exact recurrence."""
-    w = W.draw("bwd bf16 ckpt", [200, 64, 450, 77], 2, 2, 64, 64, seed=481, initial_state=True, slow_decay=True)
+    the oracle differentiates the exact recurrence.  K = V = 64: the tile kernel; 128: the
+    tensor-core schedule."""
+    w = W.draw("bwd bf16 ckpt", [200, 64, 450, 77], 2, 2, KV, KV, seed=481, initial_state=True, slow_decay=True)
     do, dfin = cotangents(w, 482)
     got = run_bwd(w, do, dfin, checkpoints=fwd_checkpoints(w, n, torch.bfloat16), checkpoint_every_n=n)
     ref = oracle.gdn_bwd(w.q, w.k, w.v, w.g, w.beta, w.cu_seqlens, do, initial_state=w.initial_state,
@@ -266,12 +267,14 @@ def test_bwd_bf16_start_state_regenerated_checkpoints():
     compare(w, got, ref, label=" bf16 start state")
 
 
-@pytest.mark.parametrize("save_checkpoints,n", [(True, 64), (True, 128), (False, 64)])
-def test_autograd_matches_oracle_gradients(save_checkpoints, n):
+@pytest.mark.parametrize("save_checkpoints,n,KV", [(True, 64, 64), (True, 128, 64), (False, 64, 64),
+                                                    (True, 64, 128), (False, 64, 128)])
+def test_autograd_matches_oracle_gradients(save_checkpoints, n, KV):
     """gdn_attention under torch.autograd: a scalar loss of o and the final state, backward through
     the library's kernels, gradients of every input against the oracle's reverse mode (the forward
-    keeping fp32 states every 64 or 128 tokens, or none)."""
-    w = W.draw("autograd", [70, 129, 1, 300], 2, 4, 64, 64, seed=491, initial_state=True, slow_decay=True)
+    keeping fp32 states every 64 or 128 tokens, or none; K = V = 128 takes the tensor-core
+    backward)."""
+    w = W.draw("autograd", [70, 129, 1, 300], 2, 4, KV, KV, seed=491, initial_state=True, slow_decay=True)
     d = dev()
     gen = torch.Generator().manual_seed(492)
     wo = torch.randn(w.T, w.HV, w.V, generator=gen).to(torch.bfloat16)
