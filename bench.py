@@ -385,7 +385,9 @@ def run_ours(args, world, rank, local):
                        "l2": f"inputs larger than L2 ({qkv_bytes / 1e9:.2f} GB of q/k/v per step); no flush"},
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak,
-                         "traffic": None if args.fwd_passes == "fused" else profiled_traffic(),
+                         # (the recorded traffic is the dense batch's: another length has none)
+                         "traffic": (None if args.fwd_passes == "fused" or args.seq_len != 8192
+                                     else profiled_traffic()),
                          "peak_source": peak_src,
                          "kernel": ("gdn_chunk_kernel<128, fwd> (fused)" if args.fwd_passes == "fused" else
                                     "gdn_wy_kernel<128> + gdn_chunk_kernel<128, state pass> (timed together)"),
