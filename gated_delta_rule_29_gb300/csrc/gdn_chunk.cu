@@ -686,6 +686,33 @@ __global__ void __launch_bounds__(chunk_threads(MODE), 2)
         }
         const int64_t fin_unit = a.state_idx ? s0_unit : unit_state;
 
+        // ---- first chunk's tiles (and record): issued before the start state is read, so that
+        // their latency overlaps that read
+        if (hi > lo) {
+            const int64_t tf = ts + tlo;
+            if (tid == 0 && !a.test_skip_tile_load) {
+                mbar_arrive_expect_tx(&sc.bar_kq, kq_bytes);
+#pragma unroll
+                for (int rg = 0; rg < KD / 64; ++rg) {
+                    tma_load_3d(KQ + rg * RQ, &kmap, &sc.bar_kq, rg * 64, hk, static_cast<int>(tf));
+                    if (kFwd)
+                        tma_load_3d(KQ + rg * RQ + 8192, &qmap, &sc.bar_kq, rg * 64, hk, static_cast<int>(tf / NH));
+                }
+            }
+            if (tid == 0) {
+                if (value_tile) {
+                    mbar_arrive_expect_tx(&sc.bar_v, v_bytes);
+                    for (int rg = 0; rg < a.V / 64; ++rg)
+                        tma_load_3d(VT + rg * 8192, &vmap, &sc.bar_v, rg * 64, h, static_cast<int>(tf));
+                }
+            }
+            pend_kq = !a.test_skip_tile_load;
+            pend_v = value_tile;
+            if (kSplit) {
+                if (tid == 0) load_wy(a, wymap, a.chunk_off[seq] + lo, h, M, PB, sc);
+                pend_f = true;
+            }
+        }
         // ---- chunk 0's gate total: the state kept in TMEM is pre-multiplied by the decay of the
         // chunk it is about to enter, so the state-update product can accumulate onto it
         float g_nx = 0.f, b_nx = 0.f;
@@ -776,32 +803,6 @@ __global__ void __launch_bounds__(chunk_threads(MODE), 2)
             tmem_wait_st();
         }
 
-        // ---- first chunk's tiles and per-token scalars
-        if (hi > lo) {
-            const int64_t tf = ts + tlo;
-            if (tid == 0 && !a.test_skip_tile_load) {
-                mbar_arrive_expect_tx(&sc.bar_kq, kq_bytes);
-#pragma unroll
-                for (int rg = 0; rg < KD / 64; ++rg) {
-                    tma_load_3d(KQ + rg * RQ, &kmap, &sc.bar_kq, rg * 64, hk, static_cast<int>(tf));
-                    if (kFwd)
-                        tma_load_3d(KQ + rg * RQ + 8192, &qmap, &sc.bar_kq, rg * 64, hk, static_cast<int>(tf / NH));
-                }
-            }
-            if (tid == 0) {
-                if (value_tile) {
-                    mbar_arrive_expect_tx(&sc.bar_v, v_bytes);
-                    for (int rg = 0; rg < a.V / 64; ++rg)
-                        tma_load_3d(VT + rg * 8192, &vmap, &sc.bar_v, rg * 64, h, static_cast<int>(tf));
-                }
-            }
-            pend_kq = !a.test_skip_tile_load;
-            pend_v = value_tile;
-            if (kSplit) {
-                if (tid == 0) load_wy(a, wymap, a.chunk_off[seq] + lo, h, M, PB, sc);
-                pend_f = true;
-            }
-        }
         for (int c = lo; c < hi; ++c) {
             const int64_t t0 = ts + static_cast<int64_t>(c) * kChunk;
             const int64_t left = L - static_cast<int64_t>(c) * kChunk;
