@@ -890,7 +890,15 @@ def run_table(args, world, rank, local):
     cores = os.cpu_count() or 1
     stream = torch.cuda.current_stream()
 
+    clock_log = []  # one clock record per timed configuration
+
     def timed(step):
+        with ClockSampler(local) as clk:
+            out = timed_inner(step)
+        clock_log.append(clk.summary())
+        return out
+
+    def timed_inner(step):
         for _ in range(args.warmup):
             step()
         torch.cuda.synchronize()
@@ -965,7 +973,7 @@ def run_table(args, world, rank, local):
                      "algorithmic_bytes": alg, "hbm_gbs": alg / (kern_ms * 1e-3) / 1e9,
                      "hbm_frac": alg / (kern_ms * 1e-3) / 1e9 / hbm_peak,
                      "tensor_tflops": flops / (kern_ms * 1e-3) / 1e12,
-                     "tensor_frac": flops / (kern_ms * 1e-3) / 1e12 / tc_peak,
+                     "tensor_frac": flops / (kern_ms * 1e-3) / 1e12 / tc_peak, "clocks": clock_log[-1],
                      "oracle": oracle_rates(w, spread(w, n1), spread(w, na))})
         del t, o, fin, ck
     w = W.config(5)
@@ -988,6 +996,7 @@ def run_table(args, world, rank, local):
                  "algorithmic_bytes": alg, "hbm_gbs": alg / (kern_ms * 1e-3) / 1e9,
                  "hbm_frac": alg / (kern_ms * 1e-3) / 1e9 / hbm_peak,
                  "tensor_tflops": flops / (kern_ms * 1e-3) / 1e12, "tensor_frac": flops / (kern_ms * 1e-3) / 1e12 / tc_peak,
+                 "clocks": clock_log[-1],
                  "oracle": oracle_rates(ws5, [(0, 0)], [(0, h) for h in range(min(HV, cores))], summary=True)})
     for r_ in rows:
         r_["peak_source"] = peak_src
