@@ -337,23 +337,29 @@ __global__ void __launch_bounds__(kDT, 1)
         }
 
         // ---- P0: tiles, T, factors and dS' by TMA / bulk copy; S^T hi + lo from the fp32 state
-        if (tid == kIo) {
-            if (!prefetched) load_states(item);
-            bulk_wait_read_all();  // the previous item's output tiles have left their staging buffers
-        }
+        // the K/Q tile and the factors first (their buffers are no output's staging), then, once the
+        // previous item's output tiles have left their staging buffers, dO, T and T's residual
         if (tid == kIo && !a.test_skip_tile_load) {  // (the failure-path test hook: no tile loads)
             mbar_arrive_expect_tx(&sc.bar_in, in_bytes);
 #pragma unroll
             for (int rg = 0; rg < 2; ++rg) {
                 tma_load_3d(KQ + rg * 16384, &kmap, &sc.bar_in, rg * 64, hk, static_cast<int>(t0));
                 tma_load_3d(KQ + rg * 16384 + 8192, &qmap, &sc.bar_in, rg * 64, hk, static_cast<int>(t0));
-                tma_load_3d(DO + rg * 8192, &domap, &sc.bar_in, rg * 64, h, static_cast<int>(t0));
             }
+            bulk_load(sc.bet, a.wy + item * static_cast<int64_t>(kWyRecordBytes) + 2 * kWyTileBytes,
+                      static_cast<uint32_t>(kWyFactorBytes), &sc.bar_in);
+        }
+        if (tid == kIo) {
+            if (!prefetched) load_states(item);
+            bulk_wait_read_all();  // the previous item's output tiles have left their staging buffers
+        }
+        if (tid == kIo && !a.test_skip_tile_load) {
+#pragma unroll
+            for (int rg = 0; rg < 2; ++rg)
+                tma_load_3d(DO + rg * 8192, &domap, &sc.bar_in, rg * 64, h, static_cast<int>(t0));
             tma_load_3d(TB, &wymap, &sc.bar_in, 0, static_cast<int>(item), 0);
             bulk_load(TLO, a.wy_tlo + item * static_cast<int64_t>(kWyTileBytes), static_cast<uint32_t>(kWyTileBytes),
                       &sc.bar_in);
-            bulk_load(sc.bet, a.wy + item * static_cast<int64_t>(kWyRecordBytes) + 2 * kWyTileBytes,
-                      static_cast<uint32_t>(kWyFactorBytes), &sc.bar_in);
         }
         pend_in = !a.test_skip_tile_load;
         pend_pre = true;
