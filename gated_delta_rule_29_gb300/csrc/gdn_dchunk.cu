@@ -48,7 +48,8 @@ constexpr float kLog2eD = 1.4426950408889634f;
 // Shared memory (byte offsets from the 1024-aligned base).  Phase by phase a region is reused
 // once the products reading it have completed:
 //   KQ     [K; Q] tile [region 0..1 (key columns)][128 rows][128 B]             whole item
-//   ST     S^T hi [region 0..1 (key columns)][128 rows v][128 B]                 until dk~ += S W
+//   ST     S^T hi [region 0..1 (key columns)][128 rows v][128 B]                 until dk~ += S W,
+//          then the first half of the next item's S (fp32)
 //   STLO   S^T lo -> X^T hi, lo -> D^T hi, lo
 //   DST    dS'^T hi                                                              until acc2
 //   DSTLO  dS'^T lo -> dD^T hi, lo -> [dX lo | dX hi | (TLO) dO^T] -> [N ; Hs] bf16 and a zero tile
@@ -100,6 +101,7 @@ struct __align__(16) DcScalars {
     float gp[4];
     float red[16];
     uint64_t bar_in, bar_pre, bar_mma, bar_mma2;
+    uint64_t bar_pre0;  // the first half of S's fp32 staging, requested early
     uint32_t tmem_base;
     int32_t status0;
 };
@@ -231,6 +233,7 @@ __global__ void __launch_bounds__(kDT, 1)
     if (tid == 0) {
         mbar_init(&sc.bar_in, 1);
         mbar_init(&sc.bar_pre, 1);
+        mbar_init(&sc.bar_pre0, 1);
         mbar_init(&sc.bar_mma, 1);
         mbar_init(&sc.bar_mma2, 1);
         fence_mbar_init();
@@ -273,14 +276,25 @@ __global__ void __launch_bounds__(kDT, 1)
     constexpr uint32_t kPreBytes = 2u * 65536u;
 
     const int64_t total_items = a.chunk_off[a.N] * HO;
-    uint32_t ph_in = 0, ph_pre = 0, ph_mma = 0, ph_mma2 = 0;
-    bool pend_in = false, pend_pre = false, pend_mma = false, pend_mma2 = false, failed = false;
+    uint32_t ph_in = 0, ph_pre = 0, ph_pre0 = 0, ph_mma = 0, ph_mma2 = 0;
+    bool pend_in = false, pend_pre = false, pend_pre0 = false, pend_mma = false, pend_mma2 = false, failed = false;
     bool prefetched = false;  // this item's S and dS' were requested during the previous item
-    // S (fp32, into ST..STLO) and dS' (into DST..DSTLO) of an item, on bar_pre.  One thread.
-    auto load_states = [&](int64_t it) {
-        mbar_arrive_expect_tx(&sc.bar_pre, kPreBytes);
-        bulk_load(ST, bw.ckpt + it * static_cast<int64_t>(KD * KD), 65536u, &sc.bar_pre);
+    // S (fp32, into ST..STLO) and dS' (into DST..DSTLO) of an item: S's first half (keys 0-63,
+    // into ST) on bar_pre0, the rest on bar_pre.  ST is free once dk~ += W^T S^T has completed, so
+    // the first half of the next item's S is requested then, the rest after the last products.
+    // One thread.
+    auto load_state_half = [&](int64_t it) {
+        mbar_arrive_expect_tx(&sc.bar_pre0, 32768u);
+        bulk_load(ST, bw.ckpt + it * static_cast<int64_t>(KD * KD), 32768u, &sc.bar_pre0);
+    };
+    auto load_states_rest = [&](int64_t it) {
+        mbar_arrive_expect_tx(&sc.bar_pre, kPreBytes - 32768u);
+        bulk_load(ST + 32768, bw.ckpt + it * static_cast<int64_t>(KD * KD) + KD * KD / 2, 32768u, &sc.bar_pre);
         bulk_load(DST, a.ds_chunks + it * 65536, 65536u, &sc.bar_pre);
+    };
+    auto load_states = [&](int64_t it) {
+        load_state_half(it);
+        load_states_rest(it);
     };
     // waits on the product barrier (every thread), folding the outcome into ok
     auto wait_mma = [&](bool& ok) {
@@ -363,6 +377,7 @@ __global__ void __launch_bounds__(kDT, 1)
         }
         pend_in = !a.test_skip_tile_load;
         pend_pre = true;
+        pend_pre0 = true;
         // V: this thread's value column r, tokens 16 cg .. (read one item ahead; for X and the dbeta sums)
         float vv[16];
 #pragma unroll
@@ -383,10 +398,18 @@ __global__ void __launch_bounds__(kDT, 1)
         float s32[32];
         const uint32_t sreg = static_cast<uint32_t>(cg >> 1) * 16384u;
         const uint32_t sch = static_cast<uint32_t>(cg & 1) * 4u;
-        bool ok = wait_phase(&sc.bar_pre, ph_pre, budget);
+        bool ok = wait_phase(&sc.bar_pre0, ph_pre0, budget);
         if (ok) {
-            ph_pre ^= 1u;
-            pend_pre = false;
+            ph_pre0 ^= 1u;
+            pend_pre0 = false;
+        }
+        {
+            const bool okp = wait_phase(&sc.bar_pre, ph_pre, budget);
+            if (okp) {
+                ph_pre ^= 1u;
+                pend_pre = false;
+            }
+            ok = ok && okp;
         }
         {
             const float* Sf = reinterpret_cast<const float*>(ST) + (32 * cg) * KD + r;  // S[a][v], fp32 staging
@@ -725,6 +748,12 @@ __global__ void __launch_bounds__(kDT, 1)
                 pend_mma2 = false;
             }
             ok = ok && ok2;
+            // ... so S^T hi is read for the last time: the next item's S starts streaming into it
+            const int64_t nx0 = item + static_cast<int64_t>(gridDim.x);
+            if (ok2 && nx0 < total_items) {
+                if (tid == kIo) load_state_half(nx0);
+                pend_pre0 = true;
+            }
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -833,7 +862,7 @@ __global__ void __launch_bounds__(kDT, 1)
             // the next item's S and dS' stream in while this one finishes: their regions are free
             const int64_t nx = item + static_cast<int64_t>(gridDim.x);
             prefetched = nx < total_items;
-            if (tid == kIo && prefetched) load_states(nx);
+            if (tid == kIo && prefetched) load_states_rest(nx);
             pend_pre = prefetched;
             if (prefetched) item_meta(nx);
         }
@@ -947,6 +976,7 @@ __global__ void __launch_bounds__(kDT, 1)
         // let in-flight copies and products finish (bounded) before TMEM and shared memory go away
         if (pend_in) wait_phase(&sc.bar_in, ph_in, budget);
         if (pend_pre) wait_phase(&sc.bar_pre, ph_pre, budget);
+        if (pend_pre0) wait_phase(&sc.bar_pre0, ph_pre0, budget);
         if (pend_mma) wait_phase(&sc.bar_mma, ph_mma, budget);
         if (pend_mma2) wait_phase(&sc.bar_mma2, ph_mma2, budget);
         if (tid == 0) {
