@@ -1,7 +1,7 @@
 """Benchmark: chunked GDN forward tokens/s and fraction of the GB300 roofline.
 
-Workload (one step = one gdn_fwd over the whole batch, prologue + fused chunk
-kernel): the dense batch of 8 sequences x 8192 tokens (T = 65536), 32 heads,
+Workload (one step = one gdn_fwd over the whole batch: the prologue, the WY pass and the
+state pass): the dense batch of 8 sequences x 8192 tokens (T = 65536), 32 heads,
 K = V = 128, bf16 q/k/v, fp32 g/beta, fp32 initial state, final state and fp32
 checkpoints every 1024 tokens, q/k L2-normalised in kernel.  Inputs are seeded
 synthetic tensors with the cuDNN page's distributions; q/k/v alone are 1.6 GB per
